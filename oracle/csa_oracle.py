@@ -1,0 +1,281 @@
+"""CPU oracle for the Compressed Sparse Attention (CSA) hot path.
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the CPU-baseline leg of
+the benchmark may import this module.  The CUDA library never calls it and shares no
+code with it: it is a plain, slow restatement of what each step computes, in float64
+numpy, stage by stage, so that it can be checked against the source pages by eye.
+
+Sources (cited by page title and section):
+  [V4]   "DeepSeek V4-Flash: The Cost of Deciding What to Read"
+         (thesoftwarefrontier.com): sections "The compressor has two streams and they
+         overlap", "The Lightning Indexer", "Attention sink, and heads that abstain",
+         "The sliding window is not an optimisation", "Key and value are the same vector".
+  [V41]  "DeepSeek-V4.1-Flash's KV-Cache Compression, Checked Down to the Byte"
+         (flozi-tech-stuff.pages.dev): section 3 "CSA2: three multiplicative
+         dimensions, three modes, one cadence" (Hierarchical Sparse Indexer, Cell 4);
+         section 5 "SWA Bounded Replay" (window bounds [max(s, i-W+1), i]).
+  [V41d] "deepseek-v4-1-flash" (shuhuayu.github.io): "CSA2: separate producing,
+         selecting, and reading" and "Hierarchical indexing bounds the deeper searches".
+
+Readings taken where the pages are open (each is a documented reading, not a fact of
+the pages):
+  * compressor intervals are half-open: entry i mixes stream a over tokens
+    [m*i, m*(i+1)) and stream b over [m*(i-1), m*i) (8 tokens at stride 4 for m = 4);
+  * entry 0 has no b-stream: those logits are absent from its softmax;
+  * the positional bias B^a, B^b is added to the gate logits before the softmax,
+    indexed by the token's position inside its block;
+  * the indexer score has no extra scale and w is not normalised;
+  * a query at t sees compressed entry s iff s < floor((t + 1) / m);
+  * the window is positions [max(0, t - W + 1), t] (t included) that the caller's
+    local rows hold; window rows and selected entries are not de-duplicated;
+  * top-k order is (score descending, index ascending) with -0 == +0; output indices
+    ascending, padded with -1 when fewer than k entries are visible;
+  * attention logits are softmax_scale * q . r with softmax_scale = 1/sqrt(d) by default.
+
+Parity status: every function here is pinned by tests (closed forms, hand-computed
+examples, brute force against library routines, invariants); see tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+# ----------------------------------------------------------------------------------
+# storage formats, from their public definitions
+# ----------------------------------------------------------------------------------
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 is the upper half of an IEEE binary32: widen by 16 zero bits."""
+    u32 = bits.astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round binary32 to bfloat16 bits, round-to-nearest, ties to even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    u = u + np.uint64(0x7FFF) + lsb
+    return ((u >> np.uint64(16)) & np.uint64(0xFFFF)).astype(np.uint16)
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """OCP 8-bit floating point, E4M3 (no infinities): bias 7, 3 mantissa bits.
+
+    exponent field 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; max 448.
+    """
+    c = codes.astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    mant = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, mant / 8.0 * 2.0 ** -6, (1.0 + mant / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & ((c & 7) == 7), np.nan, val)
+    return sign * val
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # codes 0x00..0x7E, ascending
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 code, ties to the even code, saturating to +-448 (finite inputs)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.searchsorted(_E4M3_POS, a, side="left")          # first value >= a
+    hi = np.minimum(hi, len(_E4M3_POS) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where((x < 0) & (code != 0), code | 0x80, code).astype(np.uint8)
+
+
+def quantize_rows_e4m3(x_f32: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """One fp32 scale per row: scale = amax/448 and codes = e4m3(x / scale), in binary32.
+
+    The scale and the division are taken in binary32 so that the code decision is made in
+    the same precision as a binary32 kernel would make it.
+    """
+    x = np.asarray(x_f32, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    y = (x / scale[..., None]).astype(np.float32)
+    return e4m3_encode(y), scale
+
+
+# ----------------------------------------------------------------------------------
+# a1: gated two-stream compressor  [V4] "The compressor has two streams and they overlap"
+# ----------------------------------------------------------------------------------
+
+
+def compress_entry(kv: np.ndarray, z: np.ndarray, bias: np.ndarray, m: int, i: int,
+                   tok0: int = 0, return_weights: bool = False):
+    """Compressed entry i.
+
+    kv, z: [n_tok, 2, dim] rows of tokens tok0 .. tok0 + n_tok - 1; [:, 0] is stream a
+    (C^a, Z^a), [:, 1] stream b.  bias: [2, m, dim] (B^a, B^b).
+    Stream a contributes tokens m*i .. m*i + m - 1, stream b tokens m*(i-1) .. m*i - 1;
+    the softmax runs over those 2m logits (m for entry 0) separately for every channel,
+    and the entry is the weighted sum of the matching C values.
+    """
+    logits: List[np.ndarray] = []
+    values: List[np.ndarray] = []
+    for j in range(m):                                   # stream a, current block
+        r = m * i + j - tok0
+        logits.append(z[r, 0].astype(np.float64) + bias[0, j])
+        values.append(kv[r, 0].astype(np.float64))
+    if i >= 1:
+        for j in range(m):                               # stream b, previous block
+            r = m * (i - 1) + j - tok0
+            if r < 0:
+                raise ValueError("stream rows for the previous block are missing")
+            logits.append(z[r, 1].astype(np.float64) + bias[1, j])
+            values.append(kv[r, 1].astype(np.float64))
+    lg = np.stack(logits)                                # [2m or m, dim]
+    lg = lg - lg.max(axis=0, keepdims=True)
+    wts = np.exp(lg)
+    wts = wts / wts.sum(axis=0, keepdims=True)
+    entry = (wts * np.stack(values)).sum(axis=0)
+    return (entry, wts) if return_weights else entry
+
+
+def compress_range(kv, z, bias, m: int, i_begin: int, i_end: int, tok0: int = 0) -> np.ndarray:
+    """Entries i_begin .. i_end - 1, stacked [i_end - i_begin, dim]."""
+    dim = kv.shape[-1]
+    out = np.empty((max(0, i_end - i_begin), dim), dtype=np.float64)
+    for n, i in enumerate(range(i_begin, i_end)):
+        out[n] = compress_entry(kv, z, bias, m, i, tok0)
+    return out
+
+
+# ----------------------------------------------------------------------------------
+# a2: lightning indexer  [V4] "The Lightning Indexer";  causality: "The sliding window is
+# not an optimisation" (entry i may be read from t only if m(i+1) - 1 <= t)
+# ----------------------------------------------------------------------------------
+
+
+def visible_entries(t: int, m: int) -> int:
+    """Number of compressed entries a query at position t may read: floor((t+1)/m)."""
+    return (t + 1) // m
+
+
+def indexer_scores(qI: np.ndarray, w: np.ndarray, kI: np.ndarray, nv: int) -> np.ndarray:
+    """I(t, s) = sum_h w[h] * ReLU(qI[h] . kI[s]) for s < nv, -inf for s >= nv.
+
+    qI: [HI, dI], w: [HI], kI: [E, dI] (already dequantised).  float64 result.
+    """
+    E = kI.shape[0]
+    out = np.full(E, -np.inf, dtype=np.float64)
+    if nv > 0:
+        dots = kI[:nv].astype(np.float64) @ qI.astype(np.float64).T      # [nv, HI]
+        out[:nv] = np.maximum(dots, 0.0) @ w.astype(np.float64)
+    return out
+
+
+def indexer_scores_subset(qI, w, kI, positions: np.ndarray) -> np.ndarray:
+    """Scores of the listed positions only (CSA2 Reindex rescoring of a candidate pool)."""
+    dots = kI[positions].astype(np.float64) @ qI.astype(np.float64).T
+    return np.maximum(dots, 0.0) @ w.astype(np.float64)
+
+
+# ----------------------------------------------------------------------------------
+# a3: top-k  [V4] "The Lightning Indexer" ("a cheap scoring pass picks the top 512")
+# ----------------------------------------------------------------------------------
+
+
+def topk(scores_f32: np.ndarray, nv: int, k: int) -> np.ndarray:
+    """The k best of scores[0:nv] under (score desc, index asc); ascending, -1 padded."""
+    vals = np.asarray(scores_f32[:nv], dtype=np.float64)
+    pos = np.arange(nv)
+    order = np.lexsort((pos, -vals))            # primary -score, secondary index
+    chosen = np.sort(order[:min(k, nv)])
+    out = np.full(k, -1, dtype=np.int64)
+    out[:chosen.size] = chosen
+    return out
+
+
+# ----------------------------------------------------------------------------------
+# a3': CSA2 hierarchical candidate pool  [V41] section 3, [V41d] "Hierarchical indexing"
+# ----------------------------------------------------------------------------------
+
+
+def hier_pool(scores_f32: np.ndarray, nv: int, block: int = 8, n_blocks: int = 2048) -> np.ndarray:
+    """Candidate positions: the n_blocks best `block`-position blocks by their max score.
+
+    Block j covers visible positions [block*j, min(block*(j+1), nv)); its score is the max
+    over them.  Blocks are ranked (max desc, block asc); the kept blocks expand to their
+    visible positions, returned ascending.
+    """
+    if nv <= 0:
+        return np.zeros(0, dtype=np.int64)
+    nb = -(-nv // block)
+    vals = np.asarray(scores_f32[:nv], dtype=np.float64)
+    bmax = np.array([vals[j * block:min((j + 1) * block, nv)].max() for j in range(nb)])
+    order = np.lexsort((np.arange(nb), -bmax))
+    kept = np.sort(order[:min(n_blocks, nb)])
+    pos = [p for j in kept for p in range(j * block, min((j + 1) * block, nv))]
+    return np.asarray(pos, dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------------
+# a4: sparse MQA attention with window and sink
+#     [V4] "Key and value are the same vector", "Attention sink, and heads that abstain",
+#     "The sliding window is not an optimisation"; window bounds as in [V41] section 5.
+# ----------------------------------------------------------------------------------
+
+
+def window_positions(t: int, W: int, local_base: int, n_local: int) -> List[int]:
+    """Positions max(0, t-W+1) .. t that the local rows [local_base, local_base+n_local) hold."""
+    lo = max(0, t - W + 1, local_base)
+    hi = min(t, local_base + n_local - 1)
+    return list(range(lo, hi + 1))
+
+
+def gather_rows(kv_comp: np.ndarray, idx: np.ndarray, kv_local: np.ndarray,
+                local_base: int, t: int, W: int) -> np.ndarray:
+    """The rows one query attends to: selected compressed entries, then window rows."""
+    sel = [kv_comp[i] for i in idx if i >= 0]
+    win = [kv_local[p - local_base] for p in window_positions(t, W, local_base, kv_local.shape[0])]
+    rows = sel + win
+    d = kv_comp.shape[-1]
+    return np.stack(rows).astype(np.float64) if rows else np.zeros((0, d))
+
+
+def sparse_attention(q: np.ndarray, rows: np.ndarray, sink: np.ndarray, scale: float):
+    """Per head h: o = sum_j e^{l_j} r_j / (sum_j e^{l_j} + e^{sink_h}), l_j = scale q_h . r_j.
+
+    Every row is both key and value.  Returns (out [H, d], lse [H]) where
+    lse = log(sum_j e^{l_j} + e^{sink_h}).
+    """
+    q = q.astype(np.float64)
+    sink = np.asarray(sink, dtype=np.float64)
+    logits = scale * (q @ rows.T) if rows.shape[0] else np.zeros((q.shape[0], 0))
+    mx = np.maximum(logits.max(axis=1) if rows.shape[0] else -np.inf, sink)
+    e = np.exp(logits - mx[:, None])
+    den = e.sum(axis=1) + np.exp(sink - mx)
+    out = (e @ rows) / den[:, None] if rows.shape[0] else np.zeros_like(q)
+    return out, mx + np.log(den)
+
+
+# ----------------------------------------------------------------------------------
+# compositions
+# ----------------------------------------------------------------------------------
+
+
+def decode_token(cfg, inp: Dict[str, np.ndarray], b: int, tq: int,
+                 kv_comp: np.ndarray, kI_deq: np.ndarray) -> Dict[str, np.ndarray]:
+    """Indexer -> top-k -> attention for one query (sequence b, query slot tq).
+
+    kv_comp [E, d] and kI_deq [E, dI] are sequence b's caches after compression.
+    `inp` holds float64 numpy views of the inputs of `synth.make_inputs`.
+    """
+    t = int(inp["q_pos"][b * cfg.T + tq])
+    nv = min(visible_entries(t, cfg.m), kv_comp.shape[0])
+    s64 = indexer_scores(inp["qI"][b, tq], inp["w"][b, tq], kI_deq, nv)
+    s32 = s64.astype(np.float32)
+    idx = topk(s32, nv, cfg.k)
+    rows = gather_rows(kv_comp, idx, inp["kv_local"][b], int(inp["local_base"][b]), t, cfg.W)
+    out, lse = sparse_attention(inp["q"][b, tq], rows, inp["sink"], cfg.softmax_scale)
+    return {"scores": s64, "scores_f32": s32, "idx": idx, "out": out, "lse": lse, "nv": nv}

@@ -1,0 +1,368 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test ties one oracle function to a hand-computed example, a closed form, a
+library routine on a special case, or an invariant stated by the CSA pages, chosen so
+that a dropped term, a swapped stream, a wrong index or a transposed operand fails.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import csa_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ------------------------------------------------------------------ formats
+
+def test_bf16_roundtrip_matches_torch():
+    x = rng.standard_normal(20000).astype(np.float32) * 10.0 ** rng.integers(-6, 6, 20000)
+    ours = O.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    back = O.bf16_bits_to_f64(ours)
+    assert np.array_equal(back, torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy())
+
+
+def test_e4m3_decode_spec_points():
+    # OCP FP8 E4M3: bias 7, max normal S.1111.110 = 448, min subnormal 2^-9, 0x7F NaN
+    assert O.e4m3_decode(np.array([0x7E], np.uint8))[0] == 448.0
+    assert O.e4m3_decode(np.array([0x01], np.uint8))[0] == 2.0 ** -9
+    assert O.e4m3_decode(np.array([0x08], np.uint8))[0] == 2.0 ** -6
+    assert O.e4m3_decode(np.array([0x38], np.uint8))[0] == 1.0
+    assert O.e4m3_decode(np.array([0xB8], np.uint8))[0] == -1.0
+    assert np.isnan(O.e4m3_decode(np.array([0x7F], np.uint8))[0])
+
+
+def test_e4m3_tables_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = O.e4m3_decode(codes)
+    fin = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), ~fin)
+    assert np.array_equal(ours[fin], ref[fin])
+    x = (rng.standard_normal(50000) * 60).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    enc = O.e4m3_encode(x)
+    ref_enc = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # -0 and +0 are the same value; compare decoded values
+    assert np.array_equal(O.e4m3_decode(enc), O.e4m3_decode(ref_enc))
+
+
+def test_quantize_rows_e4m3_roundtrip_bound():
+    x = rng.standard_normal((64, 128)).astype(np.float32)
+    codes, scale = O.quantize_rows_e4m3(x)
+    back = O.e4m3_decode(codes) * scale[:, None]
+    # relative error of a normal e4m3 value is at most 2^-4; subnormals: 2^-10 * scale
+    err = np.abs(back - x)
+    assert np.all(err <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * scale[:, None]) + 1e-12)
+    assert np.all(np.max(np.abs(back), axis=1) == pytest.approx(np.max(np.abs(x), axis=1), rel=1e-6))
+
+
+# ------------------------------------------------------------------ compressor
+
+def _load_compress_golden():
+    rows = {}
+    with open(os.path.join(GOLDEN, "compress_m4_two_entries.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(None, 1)
+            if key.startswith("expect"):
+                rows[key] = [Fraction(v) for v in rest.split()]
+            else:
+                rows[key] = np.array([[float(v) for v in g.split()] for g in rest.split("|")])
+    return rows
+
+
+def test_compress_hand_example():
+    g = _load_compress_golden()
+    n = g["Ca"].shape[0]
+    kv = np.stack([g["Ca"], g["Cb"]], axis=1)                   # [8, 2, 2]
+    z = np.log(np.stack([g["expZa"], g["expZb"]], axis=1))
+    bias = np.log(np.stack([g["expBa"], g["expBb"]], axis=0))   # [2, 4, 2]
+    e0 = O.compress_entry(kv, z, bias, 4, 0)
+    e1 = O.compress_entry(kv, z, bias, 4, 1)
+    assert n == 8
+    np.testing.assert_allclose(e0, [float(v) for v in g["expect_entry0"]], rtol=1e-13)
+    np.testing.assert_allclose(e1, [float(v) for v in g["expect_entry1"]], rtol=1e-13)
+
+
+def _rand_streams(n_tok, dim, m, scale=1.0):
+    kv = rng.standard_normal((n_tok, 2, dim))
+    z = rng.standard_normal((n_tok, 2, dim)) * scale
+    bias = rng.standard_normal((2, m, dim)) * 0.1
+    return kv, z, bias
+
+
+def test_compress_constant_gate_is_mean():
+    m, dim = 4, 5
+    kv, _, _ = _rand_streams(16, dim, m)
+    z = np.full((16, 2, dim), 0.7)
+    bias = np.zeros((2, m, dim))
+    e0 = O.compress_entry(kv, z, bias, m, 0)
+    np.testing.assert_allclose(e0, kv[0:4, 0].mean(axis=0), rtol=1e-12)
+    e2 = O.compress_entry(kv, z, bias, m, 2)
+    np.testing.assert_allclose(e2, (kv[8:12, 0].sum(0) + kv[4:8, 1].sum(0)) / 8, rtol=1e-12)
+
+
+def test_compress_dominant_logit_copies_token():
+    m, dim = 4, 3
+    kv, z, bias = _rand_streams(12, dim, m)
+    z[5, 1, :] = 800.0          # token 5 in stream b; it belongs to block 1 -> entry 2
+    e2 = O.compress_entry(kv, z, bias, m, 2)
+    np.testing.assert_allclose(e2, kv[5, 1], rtol=1e-12)
+    e1 = O.compress_entry(kv, z, bias, m, 1)
+    assert not np.allclose(e1, kv[5, 1])
+
+
+def test_compress_weights_positive_sum_to_one():
+    m, dim = 4, 7
+    kv, z, bias = _rand_streams(20, dim, m, scale=3.0)
+    for i in range(5):
+        _, w = O.compress_entry(kv, z, bias, m, i, return_weights=True)
+        assert w.shape[0] == (m if i == 0 else 2 * m)
+        assert np.all(w > 0)
+        np.testing.assert_allclose(w.sum(axis=0), 1.0, rtol=1e-13)
+
+
+def test_compress_each_token_in_two_entries_and_causal():
+    m, dim, n = 4, 3, 24
+    kv, z, bias = _rand_streams(n, dim, m)
+    base = O.compress_range(kv, z, bias, m, 0, n // m)
+    for t in range(n):
+        kv2 = kv.copy()
+        kv2[t, :, :] += 1.0
+        changed = np.where(np.any(O.compress_range(kv2, z, bias, m, 0, n // m) != base, axis=1))[0]
+        expect = [i for i in (t // m, t // m + 1) if i < n // m]
+        assert list(changed) == expect, (t, changed)
+        # causality: entry i uses no token >= m*(i+1)
+        assert all(t < m * (i + 1) for i in changed)
+    # every token t >= m (with a following block) appears in exactly two entries
+    for t in range(m, n - m):
+        assert len([i for i in (t // m, t // m + 1)]) == 2
+
+
+def test_compress_tok0_offset_equivalent():
+    m, dim = 4, 4
+    kv, z, bias = _rand_streams(32, dim, m)
+    full = O.compress_range(kv, z, bias, m, 3, 8)
+    part = O.compress_range(kv[8:], z[8:], bias, m, 3, 8, tok0=8)
+    np.testing.assert_array_equal(full, part)
+    with pytest.raises(ValueError):
+        O.compress_entry(kv[8:], z[8:], bias, m, 2, tok0=8)
+
+
+# ------------------------------------------------------------------ indexer
+
+def test_indexer_one_hot_closed_form():
+    # q_h = a_h e_{c_h}, k_s = e_{c}: score_s = sum_h w_h relu(a_h) [c_h == c_s]
+    HI, dI, E = 5, 6, 6
+    a = np.array([1.5, -2.0, 0.5, 3.0, -1.0])
+    ch = np.array([0, 0, 3, 5, 5])
+    qI = np.zeros((HI, dI))
+    qI[np.arange(HI), ch] = a
+    w = np.array([2.0, 7.0, -1.0, 0.25, 4.0])
+    kI = np.eye(dI)[:E]
+    s = O.indexer_scores(qI, w, kI, nv=E)
+    expect = np.zeros(E)
+    expect[0] = 2.0 * 1.5          # head 1 (a=-2) vetoed by ReLU
+    expect[3] = -1.0 * 0.5
+    expect[5] = 0.25 * 3.0          # head 4 (a=-1) vetoed
+    np.testing.assert_array_equal(s, expect)
+
+
+def test_indexer_single_head_is_matvec_and_causal_mask():
+    dI, E = 16, 40
+    q = np.abs(rng.standard_normal((1, dI)))
+    kI = np.abs(rng.standard_normal((E, dI)))       # all dots positive: ReLU inactive
+    s = O.indexer_scores(q, np.array([1.0]), kI, nv=25)
+    np.testing.assert_allclose(s[:25], np.dot(kI[:25], q[0]), rtol=1e-14)
+    assert np.all(np.isneginf(s[25:]))
+
+
+def test_indexer_relu_veto_and_w_linearity():
+    HI, dI, E = 4, 8, 30
+    qI = rng.standard_normal((HI, dI))
+    kI = rng.standard_normal((E, dI))
+    w = rng.standard_normal(HI)
+    s = O.indexer_scores(qI, w, kI, E)
+    np.testing.assert_allclose(O.indexer_scores(qI, 3.5 * w, kI, E), 3.5 * s, rtol=1e-13)
+    # a key anti-aligned with every head scores exactly 0
+    kneg = -np.abs(rng.standard_normal(dI))
+    qpos = np.abs(rng.standard_normal((HI, dI)))
+    s2 = O.indexer_scores(qpos, w, kneg[None, :], 1)
+    assert s2[0] == 0.0
+    # brute force over heads with explicit loops
+    brute = np.array([sum(w[h] * max(0.0, sum(qI[h, c] * kI[s_, c] for c in range(dI)))
+                          for h in range(HI)) for s_ in range(E)])
+    np.testing.assert_allclose(s, brute, rtol=1e-12, atol=1e-15)
+
+
+def test_indexer_fp8_scale_one_equals_exact_path():
+    HI, dI, E = 4, 16, 20
+    codes = rng.integers(0, 0x7E, (E, dI)).astype(np.uint8) | (rng.integers(0, 2, (E, dI)) * 0x80).astype(np.uint8)
+    kdeq = O.e4m3_decode(codes) * 1.0
+    qI = rng.standard_normal((HI, dI))
+    w = rng.standard_normal(HI)
+    s_fp8 = O.indexer_scores(qI, w, kdeq, E)
+    s_f64 = O.indexer_scores(qI, w, O.e4m3_decode(codes), E)
+    np.testing.assert_array_equal(s_fp8, s_f64)
+
+
+def test_indexer_mac_count_matches_pages():
+    vals = {}
+    with open(os.path.join(GOLDEN, "indexer_mac_counts.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = int(v)
+    from compressed_sparse_attention_csa_gb300.accounting import indexer_macs
+    assert indexer_macs(vals["heads"], vals["dim"], vals["positions_full"]) == vals["macs_full"]
+    assert indexer_macs(vals["heads"], vals["dim"], vals["pool_blocks"] * vals["pool_block"]) == vals["macs_pool"]
+
+
+# ------------------------------------------------------------------ top-k
+
+def test_topk_brute_force_sort():
+    for trial in range(50):
+        n = int(rng.integers(1, 300))
+        k = int(rng.integers(1, 80))
+        nv = int(rng.integers(0, n + 1))
+        s = rng.standard_normal(n).astype(np.float32)
+        s[rng.random(n) < 0.2] = 0.0
+        got = O.topk(s, nv, k)
+        # brute force: python sort of (score, index) pairs
+        pairs = sorted(((-float(s[i]), i) for i in range(nv)))
+        expect = sorted(i for _, i in pairs[:min(k, nv)])
+        assert list(got[:len(expect)]) == expect
+        assert np.all(got[len(expect):] == -1)
+        assert (got >= 0).sum() == min(k, nv)
+
+
+def test_topk_adversarial_ties():
+    k = 16
+    assert list(O.topk(np.zeros(100, np.float32), 100, k)) == list(range(k))
+    assert list(O.topk(np.full(100, 2.5, np.float32), 100, k)) == list(range(k))
+    mix = np.where(np.arange(100) % 2 == 0, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+    assert list(O.topk(mix, 100, k)) == list(range(k))        # -0 == +0
+    inc = np.arange(100, dtype=np.float32)
+    assert list(O.topk(inc, 100, k)) == list(range(100 - k, 100))
+    assert list(O.topk(inc, 5, k)) == list(range(5)) + [-1] * (k - 5)
+
+
+# ------------------------------------------------------------------ hierarchical pool
+
+def test_hier_pool_superset_of_topk_and_size():
+    for trial in range(20):
+        nv = int(rng.integers(1, 5000))
+        s = rng.standard_normal(nv + 37).astype(np.float32)
+        block, nblk, k = 8, int(rng.integers(1, 200)), int(rng.integers(1, 64))
+        k = min(k, nblk)   # a block holding a top-k position has max >= k-th score
+        pool = O.hier_pool(s, nv, block, nblk)
+        nb = -(-nv // block)
+        kept = min(nblk, nb)
+        # size: kept blocks x 8, minus the invisible tail of the last block if it is kept
+        last_kept = (nb - 1) in set(pool // block)
+        assert pool.size == kept * block - (nb * block - nv if last_kept else 0)
+        assert np.all(np.diff(pool) > 0) and pool.max() < nv
+        full = O.topk(s, nv, k)
+        sub_slots = O.topk(s[pool], pool.size, k)
+        sub = np.where(sub_slots >= 0, pool[np.maximum(sub_slots, 0)], -1)
+        assert np.array_equal(full, sub)
+
+
+def test_hier_pool_block_max_ranking():
+    s = np.zeros(64, np.float32)
+    s[13] = 5.0     # block 1
+    s[40] = 4.0     # block 5
+    s[63] = 3.0     # block 7
+    pool = O.hier_pool(s, 64, 8, 2)
+    assert list(pool) == list(range(8, 16)) + list(range(40, 48))
+    pool = O.hier_pool(s, 60, 8, 3)   # position 63 invisible; block 7 covers 56..59
+    assert list(pool) == list(range(0, 16)) + list(range(40, 48))
+
+
+# ------------------------------------------------------------------ attention
+
+def _sdpa_with_sink(q, rows, sink, scale):
+    """torch's scaled_dot_product_attention, sink as an extra key of value zero."""
+    H, d = q.shape
+    n = rows.shape[0]
+    K = torch.from_numpy(np.concatenate([rows, np.zeros((1, d))]))[None, None]
+    V = K.clone()
+    Q = torch.from_numpy(q)[None, :, None, :].transpose(0, 1)    # [H,1,1,d]
+    mask = torch.zeros(H, 1, 1, n + 1, dtype=torch.float64)
+    mask[:, 0, 0, n] = torch.from_numpy(np.asarray(sink, np.float64))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        Q, K.expand(H, 1, n + 1, d), V.expand(H, 1, n + 1, d), attn_mask=mask, scale=scale)
+    return out[:, 0, 0, :].numpy()
+
+
+def test_attention_matches_sdpa_with_sink_column():
+    H, d, n = 6, 16, 37
+    q = rng.standard_normal((H, d))
+    rows = rng.standard_normal((n, d))
+    sink = rng.standard_normal(H)
+    out, lse = O.sparse_attention(q, rows, sink, 1 / math.sqrt(d))
+    np.testing.assert_allclose(out, _sdpa_with_sink(q, rows, sink, 1 / math.sqrt(d)), rtol=1e-12, atol=1e-14)
+    lg = q @ rows.T / math.sqrt(d)
+    np.testing.assert_allclose(lse, np.log(np.exp(lg).sum(1) + np.exp(sink)), rtol=1e-13)
+
+
+def test_attention_sink_limits():
+    H, d, n = 4, 8, 20
+    q = rng.standard_normal((H, d))
+    rows = rng.standard_normal((n, d))
+    # sink -> -inf: plain softmax attention (SDPA without the extra column)
+    out, _ = O.sparse_attention(q, rows, np.full(H, -np.inf), 0.3)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, None, None, :], torch.from_numpy(rows)[None, None].expand(H, 1, n, d),
+        torch.from_numpy(rows)[None, None].expand(H, 1, n, d), scale=0.3)[:, 0, 0]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12)
+    # a large sink drives the output to 0 (the head abstains)
+    out, _ = O.sparse_attention(q, rows, np.full(H, 60.0), 0.3)
+    assert np.max(np.abs(out)) < 1e-20
+    # equal rows r: out = r * (1 - sink mass)
+    r = rng.standard_normal(d)
+    eq = np.tile(r, (n, 1))
+    sink = rng.standard_normal(H)
+    out, _ = O.sparse_attention(q, eq, sink, 0.3)
+    lg = 0.3 * q @ r
+    mass = np.exp(sink) / (n * np.exp(lg) + np.exp(sink))
+    np.testing.assert_allclose(out, (1 - mass)[:, None] * r[None, :], rtol=1e-12)
+
+
+def test_attention_dense_reduction():
+    # k = all entries, window empty: dense MQA attention over the compressed cache
+    H, d, E = 4, 8, 24
+    q = rng.standard_normal((H, d))
+    kv = rng.standard_normal((E, d))
+    idx = O.topk(rng.standard_normal(E).astype(np.float32), E, E)
+    rows = O.gather_rows(kv, idx, np.zeros((1, d)), local_base=10 ** 9, t=100, W=0)
+    np.testing.assert_array_equal(rows, kv)
+    sink = rng.standard_normal(H)
+    out, _ = O.sparse_attention(q, rows, sink, 0.25)
+    np.testing.assert_allclose(out, _sdpa_with_sink(q, kv, sink, 0.25), rtol=1e-12)
+
+
+def test_window_positions():
+    assert O.window_positions(t=10, W=4, local_base=0, n_local=100) == [7, 8, 9, 10]
+    assert O.window_positions(t=2, W=4, local_base=0, n_local=100) == [0, 1, 2]
+    assert O.window_positions(t=10, W=4, local_base=9, n_local=100) == [9, 10]     # replay start
+    assert O.window_positions(t=10, W=4, local_base=0, n_local=9) == [7, 8]
+    assert O.window_positions(t=10, W=0, local_base=0, n_local=100) == []
+
+
+def test_gather_rows_order_and_padding():
+    d = 3
+    kv = np.arange(30, dtype=np.float64).reshape(10, d)
+    loc = -np.arange(12, dtype=np.float64).reshape(4, d)
+    rows = O.gather_rows(kv, np.array([2, 7, -1, -1]), loc, local_base=20, t=22, W=2)
+    np.testing.assert_array_equal(rows, np.stack([kv[2], kv[7], loc[1], loc[2]]))
