@@ -1,0 +1,491 @@
+// C ABI of libcsa: argument validation, workspace planning, the device error word, TMA
+// descriptor encoding and the fused decode step.  Every entry point validates on the host,
+// then enqueues kernels on the caller's stream; nothing here allocates memory.
+#include <cmath>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+
+#include "csa_internal.h"
+
+namespace csa {
+
+// ------------------------------------------------------------------ device state
+static __device__ int g_err_word;  // first device-side error since the last read
+
+static constexpr int kMaxDevices = 64;
+
+static int* err_word_ptr() {
+  static int* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+static std::atomic<int64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 152;  // planning default when no device is visible (no launch happens then)
+  }
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace csa
+
+using namespace csa;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa_status check_cfg(const csa_config* c) {
+  if (!c) return CSA_ERR_NULL;
+  if (c->B < 1 || c->H < 1 || c->d < 1 || c->HI < 1 || c->m < 1 || c->k < 1 || c->k > 4096 || c->W < 0)
+    return CSA_ERR_SHAPE;
+  if (c->dI != 32 && c->dI != 64 && c->dI != 128) return CSA_ERR_SHAPE;
+  if (c->act != CSA_F32 && c->act != CSA_BF16) return CSA_ERR_DTYPE;
+  if (c->kidx != c->act && c->kidx != CSA_E4M3) return CSA_ERR_DTYPE;
+  if (!std::isfinite(c->softmax_scale)) return CSA_ERR_SHAPE;
+  return CSA_OK;
+}
+
+csa_status launch_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+bool attn_shape_ok(const csa_config* c) {
+  const bool tc = c->act == CSA_BF16 && c->H == 64 && c->d == 512 && c->k <= 2048;
+  const bool simt = c->d <= 128 && c->H <= 64;
+  return tc || simt;
+}
+
+size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
+  const int64_t B = c->B;
+  size_t bytes = align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
+  bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
+  bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
+  bytes += align_up(topk_workspace_bytes(B, E_cap, c->k, sms), 256);
+  bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms), 256);
+  return bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa_version(void) { return 100; }
+
+int64_t csa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_NULL: return "null pointer";
+    case CSA_ERR_SHAPE: return "invalid shape";
+    case CSA_ERR_DTYPE: return "unsupported dtype";
+    case CSA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case CSA_ERR_WORKSPACE: return "workspace too small";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+    case CSA_ERR_INDEX: return "selected index out of range";
+  }
+  return "unknown status";
+}
+
+csa_status csa_get_last_error(csa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return CSA_ERR_CUDA;
+  int* p = err_word_ptr();
+  if (!p) return CSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  return static_cast<csa_status>(v);
+}
+
+size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_t n_cols) {
+  if (check_cfg(cfg) != CSA_OK || rows < 0 || n_cols < 0) return static_cast<size_t>(-1);
+  const int sms = device_sm_count();
+  switch (op) {
+    case CSA_OP_COMPRESS:
+    case CSA_OP_INDEXER:
+      return 0;
+    case CSA_OP_TOPK:
+      if (n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
+      return topk_workspace_bytes(rows, n_cols, cfg->k, sms);
+    case CSA_OP_ATTN: {
+      if (n_cols < 1 || rows % n_cols) return static_cast<size_t>(-1);
+      return attn_workspace_bytes(static_cast<int>(rows / n_cols), static_cast<int>(n_cols), cfg->H, cfg->d,
+                                  cfg->k, cfg->W, cfg->act, sms);
+    }
+    case CSA_OP_DECODE:
+      if (rows != cfg->B || n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
+      return decode_ws(cfg, n_cols, sms);
+    case CSA_OP_POOL:
+      return static_cast<size_t>(-1);
+  }
+  return static_cast<size_t>(-1);
+}
+
+size_t csa_block_pool_workspace_size(int64_t rows, int64_t n_cols, int32_t block, int32_t n_blocks) {
+  if (rows < 0 || n_cols < 0 || block < 1 || n_blocks < 1 || n_blocks > 4096 || n_cols > (int64_t(1) << 24))
+    return static_cast<size_t>(-1);
+  return pool_workspace_bytes(rows, n_cols, block, n_blocks, device_sm_count());
+}
+
+csa_status csa_compress_kv(const csa_config* cfg, int32_t dim, const void* kv, const void* z, const float* bias,
+                           int64_t n_tok, int64_t tok0, int64_t ent_begin, int64_t ent_end, void* out,
+                           csa_dtype out_dtype, float* out_scale, int64_t E_cap, csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!kv || !z || !bias || !out) return CSA_ERR_NULL;
+  if (out_dtype == CSA_E4M3 && !out_scale) return CSA_ERR_NULL;
+  if (out_dtype != CSA_F32 && out_dtype != CSA_BF16 && out_dtype != CSA_E4M3) return CSA_ERR_DTYPE;
+  if (!aligned16(kv) || !aligned16(z) || !aligned16(bias) || !aligned16(out) || (out_scale && !aligned16(out_scale)))
+    return CSA_ERR_ALIGN;
+  if (dim < 1 || dim > 1024 || n_tok < 0 || ent_begin < 0 || ent_end < ent_begin || ent_end > E_cap)
+    return CSA_ERR_SHAPE;
+  const int64_t m = cfg->m;
+  if (ent_end > ent_begin) {
+    const int64_t need_lo = ent_begin > 0 ? m * (ent_begin - 1) : 0;
+    if (tok0 > need_lo || m * ent_end > tok0 + n_tok) return CSA_ERR_SHAPE;
+  }
+  CompressArgs a{};
+  a.kv = kv;
+  a.z = z;
+  a.bias = bias;
+  a.B = cfg->B;
+  a.dim = dim;
+  a.m = cfg->m;
+  a.act_bf16 = cfg->act == CSA_BF16;
+  a.n_tok = n_tok;
+  a.tok0 = tok0;
+  a.ent_begin = ent_begin;
+  a.n_ent = ent_end - ent_begin;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.out_scale = out_scale;
+  a.E_cap = E_cap;
+  a.err = err_word_ptr();
+  return launch_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float* w, int32_t T,
+                              const int64_t* q_pos, const void* kI, const float* kscale, int64_t E_cap,
+                              const int32_t* cand, int32_t n_cand, float* scores, int64_t ld_scores, void* ws,
+                              size_t ws_bytes, csa_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!qI || !w || !q_pos || !kI || !scores) return CSA_ERR_NULL;
+  if (cfg->kidx == CSA_E4M3 && !kscale) return CSA_ERR_NULL;
+  if (!aligned16(qI) || !aligned16(w) || !aligned16(q_pos) || !aligned16(kI) || !aligned16(scores) ||
+      (kscale && !aligned16(kscale)) || (cand && !aligned16(cand)))
+    return CSA_ERR_ALIGN;
+  const int64_t n_cols = cand ? n_cand : E_cap;
+  if (T < 0 || E_cap < 0 || (cand && n_cand < 0) || ld_scores < n_cols || cfg->HI > 128 ||
+      E_cap * cfg->B >= (int64_t(1) << 31))
+    return CSA_ERR_SHAPE;
+  IndexerArgs a{};
+  a.qI = qI;
+  a.w = w;
+  a.q_pos = q_pos;
+  a.kI = kI;
+  a.kscale = kscale;
+  a.cand = cand;
+  a.n_cand = n_cand;
+  a.scores = scores;
+  a.ld = ld_scores;
+  a.B = cfg->B;
+  a.T = T;
+  a.HI = cfg->HI;
+  a.dI = cfg->dI;
+  a.m = cfg->m;
+  a.E_cap = E_cap;
+  a.act = cfg->act;
+  a.kidx = cfg->kidx;
+  a.err = err_word_ptr();
+  a.num_sms = device_sm_count();
+  return launch_status(launch_indexer(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_topk(const csa_config* cfg, const float* scores, int64_t ld, int64_t rows, int64_t n_cols,
+                    const int32_t* n_valid, const int32_t* cand, int32_t* idx, void* ws, size_t ws_bytes,
+                    csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!scores || !idx) return CSA_ERR_NULL;
+  if (!aligned16(scores) || !aligned16(idx) || (n_valid && !aligned16(n_valid)) || (cand && !aligned16(cand)) ||
+      (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (rows < 0 || n_cols < 0 || ld < n_cols || n_cols > (int64_t(1) << 24) || rows > 65535) return CSA_ERR_SHAPE;
+  const int sms = device_sm_count();
+  const size_t need = topk_workspace_bytes(rows, n_cols, cfg->k, sms);
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  TopkArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.rows = rows;
+  a.n_cols = n_cols;
+  a.n_valid = n_valid;
+  a.cand = cand;
+  a.k = cfg->k;
+  a.idx = idx;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.err = err_word_ptr();
+  a.num_sms = sms;
+  return launch_status(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_block_pool(const csa_config* cfg, const float* scores, int64_t ld, int64_t rows, int64_t n_cols,
+                          const int32_t* n_valid, int32_t block, int32_t n_blocks, int32_t* pool,
+                          int32_t* pool_count, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!scores || !pool) return CSA_ERR_NULL;
+  if (!aligned16(scores) || !aligned16(pool) || (n_valid && !aligned16(n_valid)) ||
+      (pool_count && !aligned16(pool_count)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (rows < 0 || n_cols < 0 || ld < n_cols || block < 1 || n_blocks < 1 || n_blocks > 4096 ||
+      n_cols > (int64_t(1) << 24) || rows > 65535 || static_cast<int64_t>(block) * n_blocks > (int64_t(1) << 24))
+    return CSA_ERR_SHAPE;
+  const int sms = device_sm_count();
+  const size_t need = pool_workspace_bytes(rows, n_cols, block, n_blocks, sms);
+  if (!ws || ws_bytes < need) return CSA_ERR_WORKSPACE;
+  PoolArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.rows = rows;
+  a.n_cols = n_cols;
+  a.n_valid = n_valid;
+  a.block = block;
+  a.n_blocks = n_blocks;
+  a.pool = pool;
+  a.pool_count = pool_count;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.err = err_word_ptr();
+  a.num_sms = sms;
+  return launch_status(launch_block_pool(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_sparse_attn(const csa_config* cfg, const void* q, int32_t T, const void* kv_comp, int64_t E_cap,
+                           const int32_t* idx, const void* kv_local, int64_t L, const int64_t* local_base,
+                           const int64_t* q_pos, const float* sink, void* out, float* lse, void* ws,
+                           size_t ws_bytes, csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!q || !kv_comp || !idx || !kv_local || !local_base || !q_pos || !sink || !out) return CSA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv_comp) || !aligned16(idx) || !aligned16(kv_local) || !aligned16(local_base) ||
+      !aligned16(q_pos) || !aligned16(sink) || !aligned16(out) || (lse && !aligned16(lse)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (T < 0 || E_cap < 0 || L < 0 || !attn_shape_ok(cfg)) return CSA_ERR_SHAPE;
+  const int sms = device_sm_count();
+  const size_t need = attn_workspace_bytes(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms);
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  AttnArgs a{};
+  a.q = q;
+  a.kv_comp = kv_comp;
+  a.idx = idx;
+  a.kv_local = kv_local;
+  a.local_base = local_base;
+  a.q_pos = q_pos;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.B = cfg->B;
+  a.T = T;
+  a.H = cfg->H;
+  a.d = cfg->d;
+  a.k = cfg->k;
+  a.W = cfg->W;
+  a.E_cap = E_cap;
+  a.L = L;
+  a.softmax_scale = cfg->softmax_scale;
+  a.act = cfg->act;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.err = err_word_ptr();
+  a.num_sms = sms;
+  return launch_status(launch_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
+                           csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!d) return CSA_ERR_NULL;
+  if (!d->q_pos || !d->q || !d->qI || !d->w || !d->sink || !d->kv_comp || !d->kI || !d->kv_tail || !d->z_tail ||
+      !d->kvI_tail || !d->zI_tail || !d->bias || !d->biasI || !d->kv_local || !d->local_base || !d->out)
+    return CSA_ERR_NULL;
+  if (cfg->kidx == CSA_E4M3 && !d->kscale) return CSA_ERR_NULL;
+  const void* ptrs[] = {d->q_pos, d->q, d->qI, d->w, d->sink, d->kv_comp, d->kI, d->kv_tail, d->z_tail,
+                        d->kvI_tail, d->zI_tail, d->bias, d->biasI, d->kv_local, d->local_base, d->out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA_ERR_ALIGN;
+  if ((d->kscale && !aligned16(d->kscale)) || (d->lse && !aligned16(d->lse)) ||
+      (d->idx_out && !aligned16(d->idx_out)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (d->E_cap < 1 || d->E_cap > (int64_t(1) << 24) || d->L < 0 || !attn_shape_ok(cfg) || cfg->d > 1024 ||
+      cfg->HI > 128 || d->E_cap * cfg->B >= (int64_t(1) << 31))
+    return CSA_ERR_SHAPE;
+  const int sms = device_sm_count();
+  if (!ws || ws_bytes < decode_ws(cfg, d->E_cap, sms)) return CSA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* err = err_word_ptr();
+
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(cfg->B) * d->E_cap * 4, 256);
+  int32_t* nv = reinterpret_cast<int32_t*>(p);
+  p += align_up(static_cast<size_t>(cfg->B) * 4, 256);
+  int32_t* idx = reinterpret_cast<int32_t*>(p);
+  p += align_up(static_cast<size_t>(cfg->B) * cfg->k * 4, 256);
+  const size_t topk_ws = topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms);
+  void* ws_topk = p;
+  p += align_up(topk_ws, 256);
+  void* ws_attn = p;
+  if (d->idx_out) idx = d->idx_out;
+
+  // 1. compress the block the new token completes (main KV, then indexer keys)
+  CompressArgs c{};
+  c.B = cfg->B;
+  c.m = cfg->m;
+  c.act_bf16 = cfg->act == CSA_BF16;
+  c.q_pos = d->q_pos;
+  c.E_cap = d->E_cap;
+  c.err = err;
+  c.kv = d->kv_tail;
+  c.z = d->z_tail;
+  c.bias = d->bias;
+  c.dim = cfg->d;
+  c.out = d->kv_comp;
+  c.out_dtype = cfg->act;
+  cudaError_t e = launch_compress(c, s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  c.kv = d->kvI_tail;
+  c.z = d->zI_tail;
+  c.bias = d->biasI;
+  c.dim = cfg->dI;
+  c.out = d->kI;
+  c.out_dtype = cfg->kidx;
+  c.out_scale = d->kscale;
+  e = launch_compress(c, s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+
+  // 2. indexer over the visible entries
+  IndexerArgs ia{};
+  ia.qI = d->qI;
+  ia.w = d->w;
+  ia.q_pos = d->q_pos;
+  ia.kI = d->kI;
+  ia.kscale = d->kscale;
+  ia.scores = scores;
+  ia.ld = d->E_cap;
+  ia.B = cfg->B;
+  ia.T = 1;
+  ia.HI = cfg->HI;
+  ia.dI = cfg->dI;
+  ia.m = cfg->m;
+  ia.E_cap = d->E_cap;
+  ia.act = cfg->act;
+  ia.kidx = cfg->kidx;
+  ia.err = err;
+  ia.num_sms = sms;
+  ia.nv_out = nv;
+  e = launch_indexer(ia, s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+
+  // 3. top-k
+  TopkArgs ta{};
+  ta.scores = scores;
+  ta.ld = d->E_cap;
+  ta.rows = cfg->B;
+  ta.n_cols = d->E_cap;
+  ta.n_valid = nv;
+  ta.k = cfg->k;
+  ta.idx = idx;
+  ta.ws = ws_topk;
+  ta.ws_bytes = topk_ws;
+  ta.err = err;
+  ta.num_sms = sms;
+  e = launch_topk(ta, s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+
+  // 4. sparse attention over the selection plus the window, with the sink
+  AttnArgs aa{};
+  aa.q = d->q;
+  aa.kv_comp = d->kv_comp;
+  aa.idx = idx;
+  aa.kv_local = d->kv_local;
+  aa.local_base = d->local_base;
+  aa.q_pos = d->q_pos;
+  aa.sink = d->sink;
+  aa.out = d->out;
+  aa.lse = d->lse;
+  aa.B = cfg->B;
+  aa.T = 1;
+  aa.H = cfg->H;
+  aa.d = cfg->d;
+  aa.k = cfg->k;
+  aa.W = cfg->W;
+  aa.E_cap = d->E_cap;
+  aa.L = d->L;
+  aa.softmax_scale = cfg->softmax_scale;
+  aa.act = cfg->act;
+  aa.ws = ws_attn;
+  aa.err = err;
+  aa.num_sms = sms;
+  return launch_status(launch_attn(aa, s));
+}
+
+}  // extern "C"

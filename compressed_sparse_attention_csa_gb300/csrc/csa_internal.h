@@ -1,0 +1,115 @@
+// Internal launch interface between the C ABI (csa_api.cu) and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "csa.h"
+
+namespace csa {
+
+// ---- compression ------------------------------------------------------------------
+struct CompressArgs {
+  const void* kv;       // [B, n_tok, 2, dim]
+  const void* z;        // [B, n_tok, 2, dim]
+  const float* bias;    // [2, m, dim]
+  int B, dim, m;
+  bool act_bf16;        // input dtype
+  int64_t n_tok, tok0;  // uniform mode: stream row r holds token tok0 + r
+  int64_t ent_begin, n_ent;
+  const int64_t* q_pos; // decode mode (non-null): per sequence t = q_pos[b]; rows hold t-2m+1..t;
+                        // the entry (t+1)/m - 1 is produced only when (t+1) % m == 0
+  void* out;            // [B, E_cap, dim]
+  int out_dtype;        // CSA_F32 / CSA_BF16 / CSA_E4M3
+  float* out_scale;     // [B, E_cap] for e4m3
+  int64_t E_cap;
+  int* err;
+};
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
+
+// ---- indexer ----------------------------------------------------------------------
+struct IndexerArgs {
+  const void* qI;        // [B*T, HI, dI]
+  const float* w;        // [B*T, HI]
+  const int64_t* q_pos;  // [B*T]
+  const void* kI;        // [B, E_cap, dI]
+  const float* kscale;   // [B, E_cap] (e4m3)
+  const int32_t* cand;   // [B*T, n_cand] or null
+  int n_cand;
+  float* scores;         // [B*T, ld]
+  int64_t ld;
+  int B, T, HI, dI, m;
+  int64_t E_cap;
+  int act;               // CSA_F32 / CSA_BF16
+  int kidx;              // CSA_F32 / CSA_BF16 / CSA_E4M3
+  int* err;
+  int num_sms;
+  int32_t* nv_out;       // [B*T] visible-entry count per query row, or null
+};
+cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
+bool indexer_uses_tensor_cores(const IndexerArgs& a);
+
+// ---- top-k ------------------------------------------------------------------------
+struct TopkArgs {
+  const float* scores;   // [rows, ld]
+  int64_t ld, rows, n_cols;
+  const int32_t* n_valid;
+  const int32_t* cand;   // [rows, n_cols] or null
+  int k;
+  int32_t* idx;          // [rows, k]
+  void* ws;
+  size_t ws_bytes;
+  int* err;
+  int num_sms;
+};
+size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+
+struct PoolArgs {
+  const float* scores;
+  int64_t ld, rows, n_cols;
+  const int32_t* n_valid;
+  int block, n_blocks;
+  int32_t* pool;         // [rows, n_blocks*block]
+  int32_t* pool_count;   // [rows] or null
+  void* ws;
+  size_t ws_bytes;
+  int* err;
+  int num_sms;
+};
+size_t pool_workspace_bytes(int64_t rows, int64_t n_cols, int block, int n_blocks, int num_sms);
+cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s);
+
+// ---- attention --------------------------------------------------------------------
+struct AttnArgs {
+  const void* q;          // [B*T, H, d]
+  const void* kv_comp;    // [B, E_cap, d]
+  const int32_t* idx;     // [B*T, k]
+  const void* kv_local;   // [B, L, d]
+  const int64_t* local_base;
+  const int64_t* q_pos;
+  const float* sink;      // [H]
+  void* out;              // [B*T, H, d]
+  float* lse;             // [B*T, H] or null
+  int B, T, H, d, k, W;
+  int64_t E_cap, L;
+  float softmax_scale;
+  int act;
+  void* ws;
+  size_t ws_bytes;
+  int* err;
+  int num_sms;
+};
+size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+
+// ---- shared host utilities ---------------------------------------------------------
+int device_sm_count();
+void count_launches(int n);  // bookkeeping for csa_launch_count()
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace csa

@@ -1,0 +1,560 @@
+// Core sparse MQA attention over the selected compressed entries plus the sliding window,
+// with a per-head attention sink.
+//
+// "DeepSeek V4-Flash: The Cost of Deciding What to Read":
+//  * "Key and value are the same vector": one cached 512-dim row per entry serves as key and
+//    value for all 64 query heads (multi-query);
+//  * "Attention sink, and heads that abstain": exp(z'_h) joins the softmax denominator only;
+//  * "The sliding window is not an optimisation": the W most recent uncompressed rows are
+//    concatenated with the selected entries before the softmax.
+// Window rows are positions [max(0, t-W+1), t] that the caller's local rows hold.
+//
+// Tensor-core path (bf16, d = 512, H = 64).  The rows of one query are gathered 128 at a
+// time into shared memory (16-byte cp.async, 128B-swizzled).  The same tile is the A operand
+// of both products, K-major for S^T = R Q^T (M = 128 rows, N = 64 heads, K = 512) and
+// MN-major for O^T += R^T P^T (M = 128 dims per chunk, N = 64 heads, K = 128 rows), so each
+// TMEM lane of S^T is one row and each TMEM lane of O^T one output dim.  The softmax is
+// online across row blocks; the row max and row sum over the 128 lanes use a butterfly
+// that halves the live values at every step.  The running max is only moved when it grows
+// by more than 2^8 (rescaling O^T in TMEM then), which keeps every exponent bounded.
+// Decode splits the rows of one query over CTAs and merges the partial (m, l, O) in fixed
+// order with the sink; prefill runs one CTA per query.
+#include <algorithm>
+
+#include "csa_internal.h"
+#include "csa_ptx.cuh"
+
+namespace csa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ------------------------------------------------------------------ row list helpers
+struct RowList {
+  int n_sel, n_win;
+  int64_t p_lo;
+};
+
+// Compacts the valid entries of idx[0:k) into sel[] (kept order) with a block scan.
+template <int NT>
+__device__ int compact_idx(const int32_t* idx, int k, int64_t E_cap, int32_t* sel, uint32_t* tmp, int* err) {
+  const int per = (k + NT - 1) / NT;
+  const int lo = threadIdx.x * per, hi = min(k, lo + per);
+  uint32_t cnt = 0;
+  for (int j = lo; j < hi; ++j) {
+    const int32_t v = idx[j];
+    if (v >= 0 && v < E_cap) ++cnt;
+    else if (v >= E_cap) set_error(err, kErrIndex);
+  }
+  uint32_t total;
+  uint32_t off = block_exclusive_scan<NT>(cnt, tmp, &total);
+  for (int j = lo; j < hi; ++j) {
+    const int32_t v = idx[j];
+    if (v >= 0 && v < E_cap) sel[off++] = v;
+  }
+  __syncthreads();
+  return static_cast<int>(total);
+}
+
+__device__ __forceinline__ void window_of(int64_t t, int W, int64_t base, int64_t L, int64_t& p_lo, int& n_win) {
+  int64_t lo = t - W + 1;
+  lo = lo > 0 ? lo : 0;
+  lo = lo > base ? lo : base;
+  int64_t hi = t < base + L - 1 ? t : base + L - 1;
+  p_lo = lo;
+  n_win = hi >= lo ? static_cast<int>(hi - lo + 1) : 0;
+}
+
+// ------------------------------------------------------------------ CUDA-core path
+constexpr int kSimtThreads = 256;
+constexpr int kSimtTile = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(AttnArgs a) {
+  extern __shared__ float sm[];
+  const int H = a.H, d = a.d, k = a.k;
+  float* sq = sm;                           // [H][d]
+  float* so = sq + H * d;                   // [H][d]
+  float* srow = so + H * d;                 // [32][d+1]
+  float* sp = srow + kSimtTile * (d + 1);   // [H][32]
+  float* sm_run = sp + H * kSimtTile;       // [H]
+  float* sl_run = sm_run + H;
+  float* salpha = sl_run + H;
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(salpha + H);  // 32
+  int32_t* sel = reinterpret_cast<int32_t*>(tmp + 32);      // [k]
+
+  const int64_t r = blockIdx.x;
+  const int b = static_cast<int>(r / a.T);
+  const int tid = threadIdx.x;
+  const T* q = static_cast<const T*>(a.q) + r * H * d;
+  for (int i = tid; i < H * d; i += kSimtThreads) {
+    sq[i] = load_f<T>(q + i);
+    so[i] = 0.f;
+  }
+  for (int h = tid; h < H; h += kSimtThreads) {
+    sm_run[h] = -INFINITY;
+    sl_run[h] = 0.f;
+  }
+  const int n_sel = compact_idx<kSimtThreads>(a.idx + r * k, k, a.E_cap, sel, tmp, a.err);
+  const int64_t t = a.q_pos[r];
+  int64_t p_lo;
+  int n_win;
+  window_of(t, a.W, a.local_base[b], a.L, p_lo, n_win);
+  const int n_rows = n_sel + n_win;
+  const T* kvc = static_cast<const T*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * d;
+  const T* kvl = static_cast<const T*>(a.kv_local) + static_cast<int64_t>(b) * a.L * d;
+  const int64_t lbase = a.local_base[b];
+
+  for (int r0 = 0; r0 < n_rows; r0 += kSimtTile) {
+    const int nr = min(kSimtTile, n_rows - r0);
+    for (int i = tid; i < kSimtTile * d; i += kSimtThreads) {
+      const int j = i / d, c = i - j * d;
+      float v = 0.f;
+      if (j < nr) {
+        const int lp = r0 + j;
+        const T* src = lp < n_sel ? kvc + static_cast<int64_t>(sel[lp]) * d
+                                  : kvl + (p_lo + (lp - n_sel) - lbase) * d;
+        v = load_f<T>(src + c);
+      }
+      srow[j * (d + 1) + c] = v;
+    }
+    __syncthreads();
+    for (int i = tid; i < H * kSimtTile; i += kSimtThreads) {
+      const int h = i / kSimtTile, j = i - h * kSimtTile;
+      float dot = 0.f;
+      for (int c = 0; c < d; ++c) dot = fmaf(sq[h * d + c], srow[j * (d + 1) + c], dot);
+      sp[i] = j < nr ? dot * a.softmax_scale : -INFINITY;
+    }
+    __syncthreads();
+    for (int h = tid; h < H; h += kSimtThreads) {
+      float mx = -INFINITY;
+      for (int j = 0; j < nr; ++j) mx = fmaxf(mx, sp[h * kSimtTile + j]);
+      const float mold = sm_run[h];
+      const float mnew = fmaxf(mold, mx);
+      const float alpha = mold == -INFINITY ? 0.f : expf(mold - mnew);
+      float sum = 0.f;
+      for (int j = 0; j < kSimtTile; ++j) {
+        const float e = j < nr ? expf(sp[h * kSimtTile + j] - mnew) : 0.f;
+        sp[h * kSimtTile + j] = e;
+        sum += e;
+      }
+      sl_run[h] = sl_run[h] * alpha + sum;
+      sm_run[h] = mnew;
+      salpha[h] = alpha;
+    }
+    __syncthreads();
+    for (int i = tid; i < H * d; i += kSimtThreads) {
+      const int h = i / d, c = i - h * d;
+      float acc = so[i] * salpha[h];
+      for (int j = 0; j < nr; ++j) acc = fmaf(sp[h * kSimtTile + j], srow[j * (d + 1) + c], acc);
+      so[i] = acc;
+    }
+    __syncthreads();
+  }
+  T* out = static_cast<T*>(a.out) + r * H * d;
+  for (int i = tid; i < H * d; i += kSimtThreads) {
+    const int h = i / d;
+    const float mr = sm_run[h], sk = a.sink[h];
+    const float M = fmaxf(mr, sk);
+    const float f = mr == -INFINITY ? 0.f : expf(mr - M);
+    const float den = sl_run[h] * f + expf(sk - M);
+    store_f<T>(out + i, so[i] * f / den);
+  }
+  if (a.lse) {
+    for (int h = tid; h < H; h += kSimtThreads) {
+      const float mr = sm_run[h], sk = a.sink[h];
+      const float M = fmaxf(mr, sk);
+      const float f = mr == -INFINITY ? 0.f : expf(mr - M);
+      a.lse[r * H + h] = M + logf(sl_run[h] * f + expf(sk - M));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ tensor-core path
+constexpr int kTcThreads = 256;   // warps 0-3 softmax (S^T lanes), all 8 warps gather / O work
+constexpr int kRows = 128;        // rows per block (MMA M of S^T)
+constexpr int kD = 512;
+constexpr int kH = 64;
+constexpr uint32_t kQOff = 0;                       // 8 regions x (64 rows x 128 B)
+constexpr uint32_t kROff = kQOff + kH * kD * 2;     // 8 regions x (128 rows x 128 B)
+constexpr uint32_t kPOff = kROff + kRows * kD * 2;  // 128 rows x 128 B (MN-major P, N = heads)
+constexpr uint32_t kMiscOff = kPOff + kRows * kH * 2;
+constexpr int kMaxK = 2048;
+constexpr uint32_t kTmemCols = 512;                 // S^T: cols 0..63, O^T: cols 64..319
+
+struct TcAttnSplit {
+  int n_split;
+  int rows_per_split;
+  float* part_o;   // [B*T, n_split, H, d]
+  float* part_ml;  // [B*T, n_split, 2, H]
+};
+
+// Reduce 64 per-lane values over the 32 lanes of a warp; lane l ends with the results for
+// heads 2l and 2l+1 (halving exchange: 32+16+8+4+2 shuffles).
+template <bool MAX>
+__device__ __forceinline__ float2 warp_reduce64(float (&v)[64]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int half = 32 >> step;  // live values before this step: 2*half
+    const int bit = 16 >> step;
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float lo = v[i], hi = v[i + half];
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, bit);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return make_float2(v[0], v[1]);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + kQOff;
+  uint8_t* sR = smem + kROff;
+  uint8_t* sP = smem + kPOff;
+  float* s_mrun = reinterpret_cast<float*>(smem + kMiscOff);  // [64]
+  float* s_lrun = s_mrun + kH;
+  float* s_mu = s_lrun + kH;
+  float* s_alpha = s_mu + kH;
+  float* s_red = s_alpha + kH;                                 // [4][64]
+  float* s_f = s_red + 4 * kH;                                 // [64]
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(s_f + kH);       // [32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tmp + 32);      // bar_s, bar_o
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2);
+  int* s_flag = reinterpret_cast<int*>(sTmem + 1);
+  int32_t* sel = reinterpret_cast<int32_t*>(s_flag + 4);       // [k]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t r = blockIdx.y;
+  const int split = blockIdx.x;
+  const int b = static_cast<int>(r / a.T);
+  const float scale_log2 = a.softmax_scale * kLog2e;
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    s_flag[0] = 0;
+  }
+  if (warp == 4) {
+    tmem_alloc(sTmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid < kH) {
+    s_mrun[tid] = -INFINITY;
+    s_lrun[tid] = 0.f;
+  }
+  const int n_sel = compact_idx<kTcThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
+  const int64_t t = a.q_pos[r];
+  int64_t p_lo;
+  int n_win;
+  window_of(t, a.W, a.local_base[b], a.L, p_lo, n_win);
+  const int n_rows = n_sel + n_win;
+  const int row_lo = split * sp.rows_per_split;
+  const int row_hi = min(n_rows, row_lo + sp.rows_per_split);
+  const int nblk = row_hi > row_lo ? (row_hi - row_lo + kRows - 1) / kRows : 0;
+
+  const __nv_bfloat16* kvc = static_cast<const __nv_bfloat16*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kD;
+  const __nv_bfloat16* kvl = static_cast<const __nv_bfloat16*>(a.kv_local) + static_cast<int64_t>(b) * a.L * kD;
+  const int64_t lbase = a.local_base[b];
+
+  // Q: 64 rows x 64 chunks of 16 B
+  if (nblk > 0) {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + r * kH * kD;
+    for (int i = tid; i < kH * 64; i += kTcThreads) {
+      const int h = i >> 6, c = i & 63;
+      cp_async16(sQ + (c >> 3) * (kH * 128) + sw128(h, c & 7), q + h * kD + c * 8);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const uint32_t tS = tmem, tO = tmem + 64;
+  const uint32_t qbase = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int r0 = row_lo + blk * kRows;
+    const int nr = min(kRows, row_hi - r0);
+    // ---- gather 128 rows x 1 KiB
+    for (int i = tid; i < kRows * 64; i += kTcThreads) {
+      const int j = i >> 6, c = i & 63;
+      uint8_t* dst = sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7);
+      if (j < nr) {
+        const int lp = r0 + j;
+        const __nv_bfloat16* src = lp < n_sel ? kvc + static_cast<int64_t>(sel[lp]) * kD
+                                              : kvl + (p_lo + (lp - n_sel) - lbase) * kD;
+        cp_async16(dst, src + c * 8);
+      } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- S^T = R Q^T
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(kRows, kH, false, false);
+      const uint32_t rb = smem_u32(sR), qb = smem_u32(sQ);
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks) {
+        const uint32_t reg = ks >> 2, off = (ks & 3) * 32u;
+        mma_bf16(tS, smem_desc(rb + reg * (kRows * 128) + off, 16, 1024),
+                 smem_desc(qb + reg * (kH * 128) + off, 16, 1024), idesc, ks > 0);
+      }
+      mma_commit(&bars[0]);
+    }
+    float x[64];
+    if (warp < 4) {
+      mbar_wait(&bars[0], blk & 1, a.err, nullptr);
+      tc_fence_after();
+      float v0[32], v1[32];
+      tmem_ld32(tS + qbase, v0);
+      tmem_ld32(tS + qbase + 32, v1);
+      tmem_wait_ld(v0);
+      tmem_wait_ld(v1);
+      const bool valid = (warp * 32 + lane) < nr;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        x[h] = valid ? v0[h] * scale_log2 : -INFINITY;
+        x[h + 32] = valid ? v1[h] * scale_log2 : -INFINITY;
+      }
+      float red[64];
+#pragma unroll
+      for (int h = 0; h < 64; ++h) red[h] = x[h];
+      const float2 mm = warp_reduce64<true>(red);
+      s_red[warp * kH + 2 * lane] = mm.x;
+      s_red[warp * kH + 2 * lane + 1] = mm.y;
+    }
+    __syncthreads();
+    if (tid < kH) {
+      const float mb = fmaxf(fmaxf(s_red[tid], s_red[kH + tid]), fmaxf(s_red[2 * kH + tid], s_red[3 * kH + tid]));
+      const float mold = s_mrun[tid];
+      float mu = mold;
+      if (mold == -INFINITY || mb > mold + 8.f) mu = fmaxf(mold, mb);
+      const float alpha = (mu == mold) ? 1.f : exp2f(mold - mu);
+      s_mu[tid] = mu;
+      s_alpha[tid] = alpha;
+      s_mrun[tid] = mu;
+      if (alpha != 1.f && blk > 0) s_flag[0] = 1;
+    }
+    __syncthreads();
+    if (warp < 4) {
+      const int j = warp * 32 + lane;
+      float p[64];
+#pragma unroll
+      for (int h = 0; h < 64; ++h) {
+        const float mu = s_mu[h];
+        p[h] = (mu == -INFINITY) ? 0.f : exp2f(x[h] - mu);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 pk;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 two = __floats2bfloat162_rn(p[c * 8 + 2 * e], p[c * 8 + 2 * e + 1]);
+          w[e] = *reinterpret_cast<uint32_t*>(&two);
+        }
+        *reinterpret_cast<uint4*>(sP + sw128(j, c)) = pk;
+      }
+      const float2 ss = warp_reduce64<false>(p);
+      s_red[warp * kH + 2 * lane] = ss.x;
+      s_red[warp * kH + 2 * lane + 1] = ss.y;
+      tc_fence_before();
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (tid < kH)
+      s_lrun[tid] = s_lrun[tid] * s_alpha[tid] + (s_red[tid] + s_red[kH + tid]) + (s_red[2 * kH + tid] + s_red[3 * kH + tid]);
+    if (s_flag[0]) {
+      // O^T columns of heads whose reference max moved: scale by alpha
+      tc_fence_after();
+      const int c_lo = warp < 4 ? 0 : 2;
+      for (int cc = c_lo; cc < c_lo + 2; ++cc) {
+#pragma unroll
+        for (int hc = 0; hc < 64; hc += 32) {
+          float v[32];
+          const uint32_t ta = tO + qbase + cc * 64 + hc;
+          tmem_ld32(ta, v);
+          tmem_wait_ld(v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] *= s_alpha[hc + e];
+          tmem_st32(ta, v);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+    }
+    __syncthreads();
+    // ---- O^T += R^T P^T
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(kRows, kH, true, true);
+      const uint32_t rb = smem_u32(sR), pb = smem_u32(sP);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+        for (int ks = 0; ks < kRows / 16; ++ks) {
+          mma_bf16(tO + cc * 64, smem_desc(rb + (2 * cc) * (kRows * 128) + ks * 2048, kRows * 128, 1024),
+                   smem_desc(pb + ks * 2048, 8192, 1024), idesc, (blk > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(&bars[1]);
+    }
+    mbar_wait(&bars[1], blk & 1, a.err, nullptr);
+    tc_fence_after();
+    if (tid == 0) s_flag[0] = 0;
+  }
+
+  // ---- epilogue
+  const bool single = sp.n_split == 1;
+  if (tid < kH) {
+    const float mr = s_mrun[tid], lr = s_lrun[tid];
+    if (single) {
+      const float sk = a.sink[tid] * kLog2e;
+      const float M = fmaxf(mr, sk);
+      const float f = mr == -INFINITY ? 0.f : exp2f(mr - M);
+      const float den = lr * f + exp2f(sk - M);
+      s_f[tid] = f / den;
+      if (a.lse) a.lse[r * kH + tid] = (M + log2f(den)) * kLn2;
+    } else {
+      float* ml = sp.part_ml + (r * sp.n_split + split) * 2 * kH;
+      ml[tid] = mr;
+      ml[kH + tid] = lr;
+    }
+  }
+  __syncthreads();
+  if (nblk > 0) {
+    const int c_lo = warp < 4 ? 0 : 2;
+    for (int cc = c_lo; cc < c_lo + 2; ++cc) {
+      const int dd = cc * 128 + (warp & 3) * 32 + lane;
+#pragma unroll
+      for (int hc = 0; hc < 64; hc += 32) {
+        float v[32];
+        tmem_ld32(tO + qbase + cc * 64 + hc, v);
+        tmem_wait_ld(v);
+        if (single) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + r * kH * kD + dd;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[(hc + e) * kD] = __float2bfloat16_rn(v[e] * s_f[hc + e]);
+        } else {
+          float* o = sp.part_o + ((r * sp.n_split + split) * kH) * kD + dd;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[(hc + e) * kD] = v[e];
+        }
+      }
+    }
+  } else if (single) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + r * kH * kD;
+    for (int i = tid; i < kH * kD; i += kTcThreads) o[i] = __float2bfloat16_rn(0.f);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Fixed-order merge of the split partials with the sink.
+__global__ void __launch_bounds__(512) attn_merge_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  const int64_t r = blockIdx.x;
+  const int dd = threadIdx.x;  // 0..511
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + r * kH * kD;
+  const float* ml = sp.part_ml + r * sp.n_split * 2 * kH;
+  const float* po = sp.part_o + r * sp.n_split * kH * kD;
+  for (int h = 0; h < kH; ++h) {
+    const float sk = a.sink[h] * kLog2e;
+    float M = sk;
+    for (int s = 0; s < sp.n_split; ++s) M = fmaxf(M, ml[s * 2 * kH + h]);
+    float den = exp2f(sk - M), acc = 0.f;
+    for (int s = 0; s < sp.n_split; ++s) {
+      const float ms = ml[s * 2 * kH + h];
+      if (ms == -INFINITY) continue;
+      const float f = exp2f(ms - M);
+      den = fmaf(ml[s * 2 * kH + kH + h], f, den);
+      acc = fmaf(po[(static_cast<int64_t>(s) * kH + h) * kD + dd], f, acc);
+    }
+    out[h * kD + dd] = __float2bfloat16_rn(acc / den);
+    if (dd == 0 && a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+  }
+}
+
+bool attn_uses_tensor_cores(int act, int H, int d, int k) {
+  return act == CSA_BF16 && H == kH && d == kD && k <= kMaxK;
+}
+
+TcAttnSplit plan_split(int B, int T, int k, int W, int num_sms) {
+  TcAttnSplit s{};
+  const int64_t rows = static_cast<int64_t>(B) * T;
+  const int max_rows = k + W;
+  if (rows < num_sms && max_rows > kRows) {
+    s.rows_per_split = kRows;
+    s.n_split = (max_rows + kRows - 1) / kRows;
+  } else {
+    s.rows_per_split = max_rows;
+    s.n_split = 1;
+  }
+  return s;
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
+  if (!attn_uses_tensor_cores(act, H, d, k)) return 0;
+  const TcAttnSplit s = plan_split(B, T, k, W, num_sms);
+  if (s.n_split == 1) return 0;
+  const int64_t rows = static_cast<int64_t>(B) * T;
+  return align_up(static_cast<size_t>(rows * s.n_split * kH * kD) * 4, 256) +
+         align_up(static_cast<size_t>(rows * s.n_split * 2 * kH) * 4, 256);
+}
+
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.B) * a.T;
+  if (rows == 0) return cudaSuccess;
+  if (attn_uses_tensor_cores(a.act, a.H, a.d, a.k)) {
+    TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
+    if (sp.n_split > 1) {
+      uint8_t* ws = static_cast<uint8_t*>(a.ws);
+      sp.part_o = reinterpret_cast<float*>(ws);
+      sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));
+    }
+    const size_t smem = 1024 + kMiscOff + (kH * 7 + 32) * 4 + 64 + static_cast<size_t>(kMaxK) * 4;
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      attr = true;
+    }
+    dim3 grid(sp.n_split, static_cast<unsigned>(rows));
+    attn_tc_kernel<<<grid, kTcThreads, smem, s>>>(a, sp);
+    count_launches(1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || sp.n_split == 1) return e;
+    attn_merge_kernel<<<static_cast<unsigned>(rows), kD, 0, s>>>(a, sp);
+    count_launches(1);
+    return cudaGetLastError();
+  }
+  const size_t smem = (static_cast<size_t>(a.H) * a.d * 2 + kSimtTile * (a.d + 1) + a.H * kSimtTile + 3 * a.H + 32) * 4 +
+                      static_cast<size_t>(a.k) * 4;
+  if (a.act == CSA_F32) {
+    cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    attn_simt_kernel<float><<<static_cast<unsigned>(rows), kSimtThreads, smem, s>>>(a);
+  } else {
+    cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    attn_simt_kernel<__nv_bfloat16><<<static_cast<unsigned>(rows), kSimtThreads, smem, s>>>(a);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,422 @@
+// Lightning-indexer scores.
+//
+// "DeepSeek V4-Flash: The Cost of Deciding What to Read", section "The Lightning Indexer":
+//   I(t, s) = sum_h w^I(t, h) * ReLU(q^I(t, h) . K^IComp_s)
+// with 64 indexer heads of dimension 128 and one gate per head.  Causality ("The sliding
+// window is not an optimisation"): a query at t reads entry s only if m(s+1) - 1 <= t, i.e.
+// s < floor((t + 1) / m).  Every other column is -inf.
+//
+// Tensor-core path (bf16 or e4m3 keys, dI = 128): the contraction qI . kI is a dense GEMM
+// with the KEYS as the M dimension: D[s, (g, h)] = kI[s] . qI[g, h] for a 128-key tile and
+// the G*HI query-heads of a query group as N.  Each TMEM lane then holds one key's scores
+// for every head, so ReLU, the gate weights and the sum over heads are thread-local in the
+// epilogue.  Key tiles stream through a TMA ring (evict-first), the MMA is issued by one
+// thread into two TMEM accumulators so that the epilogue of tile i overlaps the MMA of
+// tile i+1.  E4M3 keys use kind::f8f6f4 with qI split into two E4M3 terms,
+// q/s ~= hi + lo/16 (s = per-head amax/448), which keeps the score error near bf16 level;
+// the per-key fp32 scale and the per-head s are positive and factor out of the ReLU.
+#include <algorithm>
+
+#include "csa_internal.h"
+#include "csa_ptx.cuh"
+
+namespace csa {
+namespace {
+
+// ------------------------------------------------------------------ CUDA-core path
+template <typename TQ, typename TK, int DI>
+__global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_t n_cols) {
+  extern __shared__ float sm[];
+  float* sq = sm;              // [HI][DI]
+  float* sw = sm + a.HI * DI;  // [HI]
+  const int64_t row = blockIdx.y;
+  const int b = static_cast<int>(row / a.T);
+  const TQ* q = static_cast<const TQ*>(a.qI) + row * a.HI * DI;
+  for (int i = threadIdx.x; i < a.HI * DI; i += blockDim.x) sq[i] = load_f<TQ>(q + i);
+  for (int i = threadIdx.x; i < a.HI; i += blockDim.x) sw[i] = a.w[row * a.HI + i];
+  __syncthreads();
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (col >= n_cols) return;
+  const int64_t t = a.q_pos[row];
+  int64_t nv = t < 0 ? 0 : (t + 1) / a.m;
+  nv = nv < a.E_cap ? nv : a.E_cap;
+  if (a.nv_out && col == 0) a.nv_out[row] = static_cast<int32_t>(nv);
+  const int64_t s = a.cand ? a.cand[row * a.n_cand + col] : col;
+  float score = -INFINITY;
+  if (s >= 0 && s < nv) {
+    float kv[DI];
+    const int64_t krow = static_cast<int64_t>(b) * a.E_cap + s;
+    if constexpr (sizeof(TK) == 1) {
+      const uint8_t* kp = static_cast<const uint8_t*>(a.kI) + krow * DI;
+#pragma unroll
+      for (int c = 0; c < DI; ++c) kv[c] = e4m3_to_f(kp[c]);
+    } else {
+      const TK* kp = static_cast<const TK*>(a.kI) + krow * DI;
+#pragma unroll
+      for (int c = 0; c < DI; ++c) kv[c] = load_f<TK>(kp + c);
+    }
+    float acc = 0.f;
+    for (int h = 0; h < a.HI; ++h) {
+      float dot = 0.f;
+#pragma unroll
+      for (int c = 0; c < DI; ++c) dot = fmaf(sq[h * DI + c], kv[c], dot);
+      acc = fmaf(sw[h], fmaxf(dot, 0.f), acc);
+    }
+    if constexpr (sizeof(TK) == 1) acc *= a.kscale[krow];
+    score = acc;
+  }
+  a.scores[row * a.ld + col] = score;
+}
+
+// ------------------------------------------------------------------ tensor-core path
+constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kTile = 128;       // keys per tile (MMA M)
+constexpr int kMaxG = 8;
+
+struct TcLayout {
+  int G;               // queries per CTA
+  int N;               // MMA N = G * HI (bf16) or G * 2 * HI (e4m3 hi/lo)
+  int stages;
+  uint32_t b_bytes;    // B operand (queries), 1024-aligned
+  uint32_t stage_bytes;
+  uint32_t smem_bytes;
+  uint32_t tmem_cols;
+  int n_splits;        // key-range splits per (sequence, query group)
+  int n_qgroups;
+};
+
+__device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitBudgetNs) return false;
+  return true;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                const IndexerArgs a, const TcLayout L,
+                                                                const int64_t n_cols) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int HI = a.HI, G = L.G, N = L.N, S = L.stages;
+  uint8_t* sB = smem;
+  uint8_t* sA = smem + L.b_bytes;
+  float* sW = reinterpret_cast<float*>(sA + static_cast<size_t>(S) * L.stage_bytes);
+  int* sNv = reinterpret_cast<int*>(sW + G * HI);
+  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sNv + kMaxG) + 7) & ~uintptr_t(7));
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + 2;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, g0 = blockIdx.y * G, split = blockIdx.x;
+  const int T = a.T;
+  const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
+
+  if (tid < kMaxG) {
+    int nv = 0;
+    if (tid < G && g0 + tid < T) {
+      const int64_t t = a.q_pos[qrow0 + tid];
+      int64_t v = t < 0 ? 0 : (t + 1) / a.m;
+      nv = static_cast<int>(v < a.E_cap ? v : a.E_cap);
+      if (a.nv_out && split == 0) a.nv_out[qrow0 + tid] = nv;
+    }
+    sNv[tid] = nv;
+  }
+  if (tid == 0) *sAbort = 0;
+
+  // ---- stage the B operand (the group's query heads) in the 128B-swizzled K-major layout
+  if constexpr (!FP8) {
+    const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
+    const int n_chunks = N * 16;  // 256 bytes per row = 16 chunks of 16 B
+    for (int i = tid; i < n_chunks; i += kTcThreads) {
+      const int n = i >> 4, c = i & 15;
+      const int g = n / HI, h = n - g * HI;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G && g0 + g < T) v = *reinterpret_cast<const uint4*>(qI + ((qrow0 + g) * HI + h) * 128 + c * 8);
+      *reinterpret_cast<uint4*>(sB + (c >> 3) * (N * 128) + sw128(n, c & 7)) = v;
+    }
+    for (int i = tid; i < G * HI; i += kTcThreads) {
+      const int g = i / HI;
+      sW[i] = (g0 + g < T) ? a.w[(qrow0 + g) * HI + (i - g * HI)] : 0.f;
+    }
+  } else {
+    const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
+    for (int gh = warp; gh < G * HI; gh += kTcThreads / 32) {
+      const int g = gh / HI, h = gh - g * HI;
+      const bool valid = g0 + g < T;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (valid) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(qI + ((qrow0 + g) * HI + h) * 128 + lane * 4);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        x[0] = __low2float(p0);
+        x[1] = __high2float(p0);
+        x[2] = __low2float(p1);
+        x[3] = __high2float(p1);
+      }
+      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float sc = am > 0.f ? am / 448.f : 1.f;
+      const float inv = 1.f / sc;
+      uint32_t hi4 = 0u, lo4 = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float y = x[j] * inv;
+        const uint8_t ch = f_to_e4m3(y);
+        const uint8_t cl = f_to_e4m3((y - e4m3_to_f(ch)) * 16.f);
+        hi4 |= static_cast<uint32_t>(ch) << (8 * j);
+        lo4 |= static_cast<uint32_t>(cl) << (8 * j);
+      }
+      const int n_hi = g * 2 * HI + h, n_lo = n_hi + HI;
+      *reinterpret_cast<uint32_t*>(sB + sw128(n_hi, lane >> 2) + (lane & 3) * 4) = hi4;
+      *reinterpret_cast<uint32_t*>(sB + sw128(n_lo, lane >> 2) + (lane & 3) * 4) = lo4;
+      if (lane == 0) sW[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
+    }
+  }
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sTmem, L.tmem_cols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+
+  int nv_max = 0;
+  for (int g = 0; g < G; ++g) nv_max = max(nv_max, sNv[g]);
+  const int tiles_needed = (nv_max + kTile - 1) / kTile;
+  const int tile_lo = static_cast<int>(static_cast<int64_t>(split) * tiles_needed / L.n_splits);
+  const int tile_hi = static_cast<int>(static_cast<int64_t>(split + 1) * tiles_needed / L.n_splits);
+  const int n_it = tile_hi - tile_lo;
+
+  // columns past the last visible tile: -inf (written by the last split of the group)
+  if (split == L.n_splits - 1) {
+    for (int g = 0; g < G; ++g) {
+      if (g0 + g >= T) break;
+      float* dst = a.scores + (qrow0 + g) * a.ld;
+      for (int64_t c = static_cast<int64_t>(tiles_needed) * kTile + tid; c < n_cols; c += kTcThreads)
+        dst[c] = -INFINITY;
+    }
+  }
+
+  if (warp == 0) {
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&kmap);
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % S;
+        if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) break;
+        mbar_arrive_expect_tx(&full[st], L.stage_bytes);
+        const int row = static_cast<int>(static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it) * kTile);
+        uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
+        tma_load_2d_hint(dst, &kmap, &full[st], 0, row, pol);
+        if constexpr (!FP8) tma_load_2d_hint(dst + 16384, &kmap, &full[st], 64, row, pol);
+        ++issued;
+      }
+      // every load issued must have landed before the CTA may exit
+      for (int it = max(0, issued - S); it < issued; ++it) wait_time_only(&full[it % S], (it / S) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_it > 0) {
+      const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
+      const uint32_t bBase = smem_u32(sB);
+      int committed = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % S, acc = it & 1;
+        if (!mbar_wait(&full[st], (it / S) & 1, a.err, sAbort)) break;
+        if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, a.err, sAbort)) break;
+        tc_fence_after();
+        const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
+        const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
+        if constexpr (FP8) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f8(d, smem_desc(aBase + ks * 32, 16, 1024), smem_desc(bBase + ks * 32, 16, 1024), idesc, ks > 0);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
+            const uint32_t boff = (ks >> 2) * static_cast<uint32_t>(N * 128) + (ks & 3) * 32u;
+            mma_bf16(d, smem_desc(aBase + off, 16, 1024), smem_desc(bBase + boff, 16, 1024), idesc, ks > 0);
+          }
+        }
+        mma_commit(&empty[st]);
+        mma_commit(&tfull[acc]);
+        ++committed;
+      }
+      if (committed > 0) wait_time_only(&tfull[(committed - 1) & 1], ((committed - 1) >> 1) & 1);
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int rin = q * 32 + lane;
+    const int hstride = FP8 ? 2 * HI : HI;
+    for (int it = 0; it < n_it; ++it) {
+      const int acc = it & 1;
+      if (!mbar_wait(&tfull[acc], (it >> 1) & 1, a.err, sAbort)) break;
+      tc_fence_after();
+      const int64_t s = static_cast<int64_t>(tile_lo + it) * kTile + rin;
+      float res[kMaxG];
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
+#pragma unroll
+      for (int g = 0; g < kMaxG; ++g) {
+        res[g] = 0.f;
+        if (g >= G) continue;
+        const float* wg = sW + g * HI;
+        float accum = 0.f;
+        for (int hc = 0; hc < HI; hc += 32) {
+          float v[32];
+          tmem_ld32(lane_base + g * hstride + hc, v);
+          if constexpr (FP8) {
+            float u[32];
+            tmem_ld32(lane_base + g * hstride + HI + hc, u);
+            tmem_wait_ld(v);
+            tmem_wait_ld(u);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) accum = fmaf(wg[hc + j], fmaxf(fmaf(u[j], 0.0625f, v[j]), 0.f), accum);
+          } else {
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) accum = fmaf(wg[hc + j], fmaxf(v[j], 0.f), accum);
+          }
+        }
+        res[g] = accum;
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      float ksc = 1.f;
+      if constexpr (FP8) {
+        if (s < a.E_cap) ksc = a.kscale[static_cast<int64_t>(b) * a.E_cap + s];
+      }
+      if (s < n_cols) {
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g) {
+          if (g >= G || g0 + g >= T) continue;
+          a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? res[g] * ksc : -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L.tmem_cols);
+  }
+}
+
+TcLayout plan_tc(const IndexerArgs& a) {
+  TcLayout L{};
+  const bool fp8 = a.kidx == CSA_E4M3;
+  const int per_q = a.HI * (fp8 ? 2 : 1);
+  L.G = std::max(1, std::min({256 / per_q, a.T, kMaxG}));
+  L.N = L.G * per_q;
+  L.b_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * (fp8 ? 128 : 256), 1024));
+  L.stage_bytes = fp8 ? 16384u : 32768u;
+  L.n_qgroups = (a.T + L.G - 1) / L.G;
+  const int tiles = static_cast<int>((a.E_cap + kTile - 1) / kTile);
+  const int64_t groups = static_cast<int64_t>(a.B) * L.n_qgroups;
+  // few long rows (decode): two CTAs per SM, key range split over them
+  const bool decode_like = groups < a.num_sms;
+  const size_t misc = 1024 + static_cast<size_t>(L.G) * a.HI * 4 + 64 + 16 * 16 + 64;
+  const size_t budget = decode_like ? (113 * 1024) : (227 * 1024);
+  int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
+  S = std::max(2, std::min(S, 8));
+  L.stages = S;
+  L.smem_bytes = static_cast<uint32_t>(misc + L.b_bytes + static_cast<size_t>(S) * L.stage_bytes);
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(2 * L.N)) cols <<= 1;
+  L.tmem_cols = cols;
+  if (decode_like) {
+    const int64_t target = 2 * static_cast<int64_t>(a.num_sms);
+    L.n_splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(target / groups, tiles)));
+  } else {
+    L.n_splits = 1;
+  }
+  return L;
+}
+
+}  // namespace
+
+bool indexer_uses_tensor_cores(const IndexerArgs& a) {
+  return a.cand == nullptr && a.act == CSA_BF16 && a.dI == 128 && a.HI % 16 == 0 && a.HI <= 128 &&
+         (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
+}
+
+cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.B) * a.T;
+  const int64_t n_cols = a.cand ? a.n_cand : a.E_cap;
+  if (rows == 0 || n_cols == 0) return cudaSuccess;
+  if (indexer_uses_tensor_cores(a)) {
+    const bool fp8 = a.kidx == CSA_E4M3;
+    const TcLayout L = plan_tc(a);
+    CUtensorMap map;
+    if (!encode_tmap_2d(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        const_cast<void*>(a.kI), 128, static_cast<uint64_t>(a.B) * a.E_cap, fp8 ? 128 : 256,
+                        fp8 ? 128 : 64, kTile))
+      return cudaErrorInvalidValue;
+    dim3 grid(L.n_splits, L.n_qgroups, a.B);
+    if (fp8) {
+      cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+      indexer_tc_kernel<true><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, n_cols);
+    } else {
+      cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
+      indexer_tc_kernel<false><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, n_cols);
+    }
+    count_launches(1);
+    return cudaGetLastError();
+  }
+  dim3 grid(static_cast<unsigned>((n_cols + 127) / 128), static_cast<unsigned>(rows));
+  const size_t smem = static_cast<size_t>(a.HI) * (a.dI + 1) * 4;
+#define CSA_SIMT(TQ, TK, DI)                                                                          \
+  do {                                                                                                \
+    cudaFuncSetAttribute(indexer_simt_kernel<TQ, TK, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                         static_cast<int>(smem));                                                     \
+    indexer_simt_kernel<TQ, TK, DI><<<grid, 128, smem, s>>>(a, n_cols);                              \
+  } while (0)
+#define CSA_SIMT_DI(TQ, TK)         \
+  do {                              \
+    if (a.dI == 32)                 \
+      CSA_SIMT(TQ, TK, 32);         \
+    else if (a.dI == 64)            \
+      CSA_SIMT(TQ, TK, 64);         \
+    else                            \
+      CSA_SIMT(TQ, TK, 128);        \
+  } while (0)
+  if (a.act == CSA_F32) {
+    if (a.kidx == CSA_E4M3)
+      CSA_SIMT_DI(float, uint8_t);
+    else
+      CSA_SIMT_DI(float, float);
+  } else {
+    if (a.kidx == CSA_E4M3)
+      CSA_SIMT_DI(__nv_bfloat16, uint8_t);
+    else
+      CSA_SIMT_DI(__nv_bfloat16, __nv_bfloat16);
+  }
+#undef CSA_SIMT_DI
+#undef CSA_SIMT
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

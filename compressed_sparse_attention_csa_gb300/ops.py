@@ -1,0 +1,188 @@
+"""Python binding of libcsa: the same calls as include/csa.h, taking torch tensors.
+
+Argument marshalling only: shapes and dtypes are checked, device pointers and the current
+CUDA stream are passed to the C ABI, and the scratch workspace the library asks for is
+allocated here (torch owns device memory; the library allocates nothing).  Every step of
+the computation runs in libcsa's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+
+class CsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {L.STATUS.get(status, status)}")
+        self.status = status
+
+
+@dataclass
+class Config:
+    B: int
+    H: int
+    d: int
+    HI: int
+    dI: int
+    m: int
+    k: int
+    W: int
+    act: torch.dtype = torch.bfloat16          # torch.float32 or torch.bfloat16
+    fp8_keys: bool = False                     # indexer keys stored as e4m3 + fp32 scale
+    softmax_scale: Optional[float] = None      # default 1/sqrt(d)
+
+    def c(self) -> L.csa_config:
+        act = L.CSA_F32 if self.act == torch.float32 else L.CSA_BF16
+        scale = self.softmax_scale if self.softmax_scale is not None else self.d ** -0.5
+        return L.csa_config(self.B, self.H, self.d, self.HI, self.dI, self.m, self.k, self.W, act,
+                            L.CSA_E4M3 if self.fp8_keys else act, scale)
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libcsa takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libcsa takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise CsaError(fn, st)
+
+
+_ws_cache = {}
+
+
+def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    if nbytes == ctypes.c_size_t(-1).value:
+        raise CsaError("csa_workspace_size", 2)
+    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _ws_args(buf):
+    return (None, 0) if buf is None else (ctypes.c_void_p(buf.data_ptr()), buf.numel())
+
+
+def version() -> int:
+    return L.load().csa_version()
+
+
+def launch_count() -> int:
+    """Kernels enqueued through libcsa by this process so far."""
+    return L.load().csa_launch_count()
+
+
+def get_last_error() -> int:
+    """Synchronise the current stream and return (and clear) the device error word."""
+    return L.load().csa_get_last_error(_stream())
+
+
+def workspace_size(op: int, cfg: Config, rows: int, n_cols: int) -> int:
+    c = cfg.c()
+    return L.load().csa_workspace_size(op, ctypes.byref(c), rows, n_cols)
+
+
+def compress_kv(cfg: Config, kv: torch.Tensor, z: torch.Tensor, bias: torch.Tensor, tok0: int, ent_begin: int,
+                ent_end: int, out: torch.Tensor, out_scale: Optional[torch.Tensor] = None) -> None:
+    """csa_compress_kv: kv, z [B, n_tok, 2, dim]; bias [2, m, dim] fp32; out [B, E_cap, dim]."""
+    lib = L.load()
+    c = cfg.c()
+    dim = kv.shape[-1]
+    if out.dtype == torch.float32:
+        od = L.CSA_F32
+    elif out.dtype == torch.bfloat16:
+        od = L.CSA_BF16
+    elif out.dtype == torch.uint8:
+        od = L.CSA_E4M3
+    else:
+        raise ValueError("out dtype")
+    _check("csa_compress_kv", lib.csa_compress_kv(ctypes.byref(c), dim, _p(kv), _p(z), _p(bias), kv.shape[1], tok0,
+                                                  ent_begin, ent_end, _p(out), od, _p(out_scale), out.shape[1],
+                                                  _stream()))
+
+
+def indexer_scores(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.Tensor, kI: torch.Tensor,
+                   scores: torch.Tensor, kscale: Optional[torch.Tensor] = None,
+                   cand: Optional[torch.Tensor] = None) -> None:
+    """csa_indexer_scores: qI [B, T, HI, dI], w [B, T, HI], kI [B, E_cap, dI] (+ kscale)."""
+    lib = L.load()
+    c = cfg.c()
+    T = qI.shape[1]
+    n_cand = cand.shape[-1] if cand is not None else 0
+    _check("csa_indexer_scores",
+           lib.csa_indexer_scores(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), kI.shape[1],
+                                  _p(cand), n_cand, _p(scores), scores.shape[-1], None, 0, _stream()))
+
+
+def topk(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional[torch.Tensor] = None,
+         cand: Optional[torch.Tensor] = None, n_cols: Optional[int] = None) -> None:
+    """csa_topk: scores [rows, ld] fp32 -> idx [rows, k] int32 (ascending, -1 padded)."""
+    lib = L.load()
+    c = cfg.c()
+    rows, ld = scores.shape
+    n_cols = ld if n_cols is None else n_cols
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_TOPK, ctypes.byref(c), rows, n_cols), scores.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_topk", lib.csa_topk(ctypes.byref(c), _p(scores), ld, rows, n_cols, _p(n_valid), _p(cand), _p(idx),
+                                    wp, wb, _stream()))
+
+
+def block_pool(cfg: Config, scores: torch.Tensor, pool: torch.Tensor, pool_count: Optional[torch.Tensor] = None,
+               n_valid: Optional[torch.Tensor] = None, block: int = 8, n_blocks: int = 2048,
+               n_cols: Optional[int] = None) -> None:
+    """csa_block_pool: scores [rows, ld] -> pool [rows, n_blocks*block] int32 positions."""
+    lib = L.load()
+    c = cfg.c()
+    rows, ld = scores.shape
+    n_cols = ld if n_cols is None else n_cols
+    ws = _workspace(lib.csa_block_pool_workspace_size(rows, n_cols, block, n_blocks), scores.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_block_pool", lib.csa_block_pool(ctypes.byref(c), _p(scores), ld, rows, n_cols, _p(n_valid), block,
+                                                n_blocks, _p(pool), _p(pool_count), wp, wb, _stream()))
+
+
+def sparse_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, idx: torch.Tensor, kv_local: torch.Tensor,
+                local_base: torch.Tensor, q_pos: torch.Tensor, sink: torch.Tensor, out: torch.Tensor,
+                lse: Optional[torch.Tensor] = None) -> None:
+    """csa_sparse_attn: q [B, T, H, d]; kv_comp [B, E_cap, d]; idx [B*T, k]; kv_local [B, L, d]."""
+    lib = L.load()
+    c = cfg.c()
+    B, T = q.shape[0], q.shape[1]
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_ATTN, ctypes.byref(c), B * T, T), q.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_sparse_attn",
+           lib.csa_sparse_attn(ctypes.byref(c), _p(q), T, _p(kv_comp), kv_comp.shape[1], _p(idx), _p(kv_local),
+                               kv_local.shape[1], _p(local_base), _p(q_pos), _p(sink), _p(out), _p(lse), wp, wb,
+                               _stream()))
+
+
+def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
+                biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None) -> None:
+    """csa_decode_step: one token per sequence (T = 1); caches are updated in place."""
+    lib = L.load()
+    c = cfg.c()
+    a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
+                          _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias), _p(biasI),
+                          _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse), _p(idx_out))
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1]), q.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_decode_step", lib.csa_decode_step(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))

@@ -1,0 +1,224 @@
+/*
+ * csa.h — C ABI of libcsa, the Compressed Sparse Attention (CSA) hot path on one GPU.
+ *
+ * The operations are those of the CSA layer described in "DeepSeek V4-Flash: The Cost of
+ * Deciding What to Read" (sections "The compressor has two streams and they overlap",
+ * "The Lightning Indexer", "Attention sink, and heads that abstain", "The sliding window
+ * is not an optimisation", "Key and value are the same vector") and of its CSA2 variant
+ * in "DeepSeek-V4.1-Flash's KV-Cache Compression, Checked Down to the Byte", section 3
+ * (Full / Reindex / Reuse modes, Hierarchical Sparse Indexer).
+ *
+ * Conventions (every call):
+ *  - All tensor arguments are DEVICE pointers to caller-owned memory, dense row-major in the
+ *    shapes given, 16-byte aligned.  The library allocates nothing; scratch comes from the
+ *    caller's workspace `ws` of at least csa_workspace_size(...) bytes (16-byte aligned).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and returns a csa_status.  Arguments are validated on the host before any launch; on a
+ *    validation error nothing is launched.  CSA_ERR_CUDA reports a failed launch.
+ *  - Errors the kernels detect on the device (a bounded wait that expired, an index out of
+ *    range) are recorded in a device error word; csa_get_last_error() synchronises the
+ *    stream, returns and clears it.
+ *  - No C++ exceptions cross this boundary; no torch types appear in it.
+ *  - Shapes use: B sequences, T query tokens per sequence, H query heads, d head dim,
+ *    HI indexer heads, dI indexer dim, m compression ratio, k top-k, W window,
+ *    E_cap rows allocated per sequence in the compressed caches.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *csa_stream_t; /* same object as cudaStream_t */
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_NULL = 1,        /* a required pointer is NULL                                   */
+  CSA_ERR_SHAPE = 2,       /* a size is out of range or inconsistent                       */
+  CSA_ERR_DTYPE = 3,       /* unsupported dtype combination                                */
+  CSA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned                             */
+  CSA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than csa_workspace_size()       */
+  CSA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed                         */
+  CSA_ERR_TIMEOUT = 7,     /* a device-side bounded wait expired (pipeline stalled)        */
+  CSA_ERR_INDEX = 8        /* a selected index was >= E_cap (the row was skipped)          */
+} csa_status;
+
+typedef enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2 } csa_dtype;
+
+typedef struct {
+  int32_t B, H, d;      /* sequences, query heads, head dim (= compressed entry dim)        */
+  int32_t HI, dI;       /* indexer heads, indexer dim                                       */
+  int32_t m;            /* compression ratio (1 = CSA2 one-to-one store)                    */
+  int32_t k;            /* entries kept by the top-k                                        */
+  int32_t W;            /* sliding-window length                                            */
+  csa_dtype act;        /* CSA_F32 or CSA_BF16: q, qI, KV streams, caches, window, output   */
+  csa_dtype kidx;       /* storage of indexer keys: == act, or CSA_E4M3 (+ fp32 row scale)  */
+  float softmax_scale;  /* attention logit scale, e.g. 1/sqrt(d)                            */
+} csa_config;
+
+/* Operation ids for csa_workspace_size. */
+typedef enum {
+  CSA_OP_COMPRESS = 0, CSA_OP_INDEXER = 1, CSA_OP_TOPK = 2, CSA_OP_ATTN = 3,
+  CSA_OP_DECODE = 4, CSA_OP_POOL = 5
+} csa_op;
+
+/*
+ * csa_workspace_size — bytes of scratch the operation needs.
+ *   rows   : query rows (B*T) of the call;
+ *   n_cols : the longest score row (E_cap, or n_cand) for TOPK / DECODE;
+ *            T (queries per sequence) for ATTN.  (POOL: see csa_block_pool_workspace_size.)
+ * Returns 0 for operations that need none, (size_t)-1 for an invalid configuration.
+ */
+size_t csa_workspace_size(csa_op op, const csa_config *cfg, int64_t rows, int64_t n_cols);
+
+/*
+ * csa_compress_kv — gated two-stream compression ("The compressor has two streams and
+ * they overlap"): entry i mixes stream a over tokens [m*i, m*(i+1)) and stream b over
+ * [m*(i-1), m*i) with a per-channel softmax of the 2m logits Z + B (m logits for entry 0,
+ * which has no previous block), then sums the matching C values with those weights.
+ *
+ *   dim        : channels (d for the main KV, dI for indexer keys)
+ *   kv, z      : [B, n_tok, 2, dim] (cfg->act) — C^a/C^b and Z^a/Z^b of tokens
+ *                tok0 .. tok0+n_tok-1; [..][0][..] is stream a, [..][1][..] stream b
+ *   bias       : [2, m, dim] fp32 — B^a, B^b by position inside the block
+ *   ent_begin, ent_end : entries to produce; needs tok0 <= m*max(ent_begin-1, 0) and
+ *                m*ent_end <= tok0 + n_tok (else CSA_ERR_SHAPE)
+ *   out        : [B, E_cap, dim] in out_dtype (CSA_F32, CSA_BF16 or CSA_E4M3); entry i is
+ *                written at row i, rows outside [ent_begin, ent_end) are untouched
+ *   out_scale  : [B, E_cap] fp32, required iff out_dtype == CSA_E4M3 (scale = amax/448,
+ *                code = e4m3_rn_satfinite(x / scale); an all-zero row gets scale 1)
+ */
+csa_status csa_compress_kv(const csa_config *cfg, int32_t dim, const void *kv, const void *z,
+                           const float *bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
+                           int64_t ent_end, void *out, csa_dtype out_dtype, float *out_scale,
+                           int64_t E_cap, csa_stream_t stream);
+
+/*
+ * csa_indexer_scores — lightning-indexer scores ("The Lightning Indexer"):
+ *   score[r, s] = sum_h w[r, h] * ReLU(qI[r, h, :] . kI[b, s, :])      (kI dequantised)
+ * for query row r = b*T + t at position q_pos[r], over entries s < nv = min(floor((q_pos+1)/m),
+ * E_cap) — the causal rule of "The sliding window is not an optimisation"; every other
+ * column of the row is set to -inf.
+ *
+ *   qI     : [B, T, HI, dI] (cfg->act);  w : [B, T, HI] fp32;  q_pos : [B*T] int64
+ *   kI     : [B, E_cap, dI] in cfg->kidx; kscale : [B, E_cap] fp32 iff kidx == CSA_E4M3
+ *   cand   : NULL — score every column s in [0, n_cols) with n_cols = E_cap;
+ *            else [B*T, n_cand] int32 positions (CSA2 Reindex: a candidate pool); column j
+ *            scores position cand[r, j]; cand < 0 or >= nv gives -inf.
+ *   scores : [B*T, ld_scores] fp32, ld_scores >= n_cols (E_cap or n_cand)
+ * bf16 keys with dI == 128 run on the tcgen05 tensor cores (fp32 accumulate); E4M3 keys run
+ * the FP8 tensor-core path with qI split into two E4M3 terms; otherwise a CUDA-core path.
+ */
+csa_status csa_indexer_scores(const csa_config *cfg, const void *qI, const float *w, int32_t T,
+                              const int64_t *q_pos, const void *kI, const float *kscale,
+                              int64_t E_cap, const int32_t *cand, int32_t n_cand, float *scores,
+                              int64_t ld_scores, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * csa_topk — per row, the cfg->k best of scores[r, 0:n_valid[r]] under the total order
+ * (score descending, position ascending; -0 == +0), written to idx[r, 0:k] in ascending
+ * position order, padded with -1 when fewer than k are valid.  Deterministic.
+ *
+ *   scores  : [rows, ld] fp32;  n_valid : [rows] int32 (NULL = n_cols for every row)
+ *   cand    : NULL, or [rows, ld_cand = n_cols] int32 ascending positions: idx holds cand[r, j]
+ *             instead of the column j (CSA2 Reindex over a pool)
+ *   idx     : [rows, k] int32
+ */
+csa_status csa_topk(const csa_config *cfg, const float *scores, int64_t ld, int64_t rows,
+                    int64_t n_cols, const int32_t *n_valid, const int32_t *cand, int32_t *idx,
+                    void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * csa_block_pool — CSA2 Hierarchical Sparse Indexer candidate pool (V4.1 page, section 3):
+ * block j covers positions [block*j, block*(j+1)) ∩ [0, n_valid[r]); its score is the max
+ * there; the n_blocks best blocks under (max desc, j asc) are kept and expanded to their
+ * visible positions.
+ *   pool       : [rows, n_blocks*block] int32, ascending, -1 padded
+ *   pool_count : [rows] int32 (number of valid positions), may be NULL
+ */
+/* Workspace bytes csa_block_pool needs for these sizes ((size_t)-1 if they are invalid). */
+size_t csa_block_pool_workspace_size(int64_t rows, int64_t n_cols, int32_t block, int32_t n_blocks);
+
+csa_status csa_block_pool(const csa_config *cfg, const float *scores, int64_t ld, int64_t rows,
+                          int64_t n_cols, const int32_t *n_valid, int32_t block, int32_t n_blocks,
+                          int32_t *pool, int32_t *pool_count, void *ws, size_t ws_bytes,
+                          csa_stream_t stream);
+
+/*
+ * csa_sparse_attn — core sparse MQA attention with window and sink ("Key and value are the
+ * same vector", "Attention sink, and heads that abstain", "The sliding window is not an
+ * optimisation").  For query row r = b*T + t at position p = q_pos[r], the rows are
+ *   kv_comp[b, idx[r, j]] for every idx[r, j] >= 0, then
+ *   kv_local[b, p' - local_base[b]] for p' in [max(0, p-W+1), p] ∩ [local_base, local_base+L)
+ * each used as both key and value; per head h with l_j = softmax_scale * q[r,h] . row_j:
+ *   out[r, h] = sum_j e^{l_j} row_j / (sum_j e^{l_j} + e^{sink[h]}),
+ *   lse[r, h] = log(sum_j e^{l_j} + e^{sink[h]}).
+ *
+ *   q : [B, T, H, d]; kv_comp : [B, E_cap, d]; idx : [B*T, k] int32 (-1 = empty slot;
+ *   >= E_cap is skipped and reported as CSA_ERR_INDEX); kv_local : [B, L, d];
+ *   local_base, q_pos : int64 [B] and [B*T]; sink : [H] fp32; out : [B, T, H, d] (cfg->act);
+ *   lse : [B, T, H] fp32 or NULL.
+ * bf16 with d == 512, H == 64 runs on the tcgen05 tensor cores; other shapes with d <= 128,
+ * H <= 64 run a CUDA-core path.
+ */
+csa_status csa_sparse_attn(const csa_config *cfg, const void *q, int32_t T, const void *kv_comp,
+                           int64_t E_cap, const int32_t *idx, const void *kv_local, int64_t L,
+                           const int64_t *local_base, const int64_t *q_pos, const float *sink,
+                           void *out, float *lse, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/* All inputs of one decode token per sequence (T = 1). */
+typedef struct {
+  int64_t E_cap;             /* rows of kv_comp / kI / kscale per sequence                    */
+  const int64_t *q_pos;      /* [B] position t of the new token                               */
+  const void *q;             /* [B, H, d]                                                     */
+  const void *qI;            /* [B, HI, dI]                                                   */
+  const float *w;            /* [B, HI]                                                       */
+  const float *sink;         /* [H]                                                           */
+  void *kv_comp;             /* [B, E_cap, d]    row (t+1)/m - 1 rewritten when (t+1) % m == 0 */
+  void *kI;                  /* [B, E_cap, dI]   (cfg->kidx), same row                         */
+  float *kscale;             /* [B, E_cap] iff kidx == CSA_E4M3                               */
+  const void *kv_tail;       /* [B, 2m, 2, d]  C^a/C^b of tokens t-2m+1 .. t                  */
+  const void *z_tail;        /* [B, 2m, 2, d]  Z^a/Z^b of the same tokens                     */
+  const void *kvI_tail;      /* [B, 2m, 2, dI] indexer-key streams of the same tokens          */
+  const void *zI_tail;       /* [B, 2m, 2, dI]                                                */
+  const float *bias;         /* [2, m, d]                                                     */
+  const float *biasI;        /* [2, m, dI]                                                    */
+  const void *kv_local;      /* [B, L, d] uncompressed window rows                            */
+  int64_t L;
+  const int64_t *local_base; /* [B] position of kv_local[b, 0]                                */
+  void *out;                 /* [B, H, d]                                                     */
+  float *lse;                /* [B, H] or NULL                                                */
+  int32_t *idx_out;          /* [B, k] or NULL: the entries the step selected                 */
+} csa_decode_args;
+
+/*
+ * csa_decode_step — one decode token per sequence: compress the block the token completes
+ * (only when (t+1) % m == 0), score the visible entries with the lightning indexer, keep the
+ * top-k, and attend over them plus the window with the sink.  Same semantics as calling
+ * csa_compress_kv (main KV and indexer keys), csa_indexer_scores, csa_topk and
+ * csa_sparse_attn in that order with T = 1.
+ */
+csa_status csa_decode_step(const csa_config *cfg, const csa_decode_args *args, void *ws,
+                           size_t ws_bytes, csa_stream_t stream);
+
+/* Synchronise `stream`, then return and clear the first device-side error recorded since the
+ * last call (CSA_OK if none; CSA_ERR_CUDA if the stream itself reports an error). */
+csa_status csa_get_last_error(csa_stream_t stream);
+
+/* Static description of a status code. */
+const char *csa_status_string(csa_status s);
+
+/* Number of kernels this process has enqueued through libcsa so far (all devices). */
+int64_t csa_launch_count(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t csa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H_ */

@@ -61,21 +61,30 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u >> np.uint64(16)) & np.uint64(0xFFFF)).astype(np.uint16)
 
 
-def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+def _e4m3_value(c: int) -> float:
     """OCP 8-bit floating point, E4M3 (no infinities): bias 7, 3 mantissa bits.
 
     exponent field 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; max 448.
     """
-    c = codes.astype(np.int64)
-    sign = np.where(c & 0x80, -1.0, 1.0)
+    sign = -1.0 if c & 0x80 else 1.0
     e = (c >> 3) & 0xF
-    mant = (c & 0x7).astype(np.float64)
-    val = np.where(e == 0, mant / 8.0 * 2.0 ** -6, (1.0 + mant / 8.0) * np.exp2(e - 7.0))
-    val = np.where((e == 15) & ((c & 7) == 7), np.nan, val)
-    return sign * val
+    mant = c & 0x7
+    if e == 15 and mant == 7:
+        return math.nan
+    if e == 0:
+        return sign * (mant / 8.0) * 2.0 ** -6
+    return sign * (1.0 + mant / 8.0) * 2.0 ** (e - 7)
 
 
-_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))  # codes 0x00..0x7E, ascending
+_E4M3_ALL = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Values of E4M3 codes (a lookup in the 256-entry table of _e4m3_value)."""
+    return _E4M3_ALL[np.asarray(codes, dtype=np.uint8)]
+
+
+_E4M3_POS = _E4M3_ALL[:0x7F]  # codes 0x00..0x7E, ascending
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
@@ -279,3 +288,30 @@ def decode_token(cfg, inp: Dict[str, np.ndarray], b: int, tq: int,
     rows = gather_rows(kv_comp, idx, inp["kv_local"][b], int(inp["local_base"][b]), t, cfg.W)
     out, lse = sparse_attention(inp["q"][b, tq], rows, inp["sink"], cfg.softmax_scale)
     return {"scores": s64, "scores_f32": s32, "idx": idx, "out": out, "lse": lse, "nv": nv}
+
+
+def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.ndarray,
+                         kI_deq: np.ndarray, fp8_keys: bool = False) -> Dict[str, np.ndarray]:
+    """One decode token of sequence b (T = 1).
+
+    When the token at t completes a block ((t + 1) % m == 0), entry (t + 1)/m - 1 is
+    compressed from the tail streams (rows = tokens t-2m+1 .. t) into the caches kv_comp
+    [E, d] and kI_deq [E, dI] (updated in place; FP8 keys are stored as e4m3 codes with one
+    fp32 scale and read back dequantised); then indexer -> top-k -> attention.
+    """
+    t = int(inp["q_pos"][b])
+    entry = None
+    if (t + 1) % cfg.m == 0:
+        e = (t + 1) // cfg.m - 1
+        tok0 = t - 2 * cfg.m + 1
+        kv_comp[e] = compress_entry(inp["kv_str"][b], inp["z_str"][b], inp["bias"], cfg.m, e, tok0)
+        ki = compress_entry(inp["kvI_str"][b], inp["zI_str"][b], inp["biasI"], cfg.m, e, tok0)
+        if fp8_keys:
+            codes, sc = quantize_rows_e4m3(ki.astype(np.float32)[None, :])
+            kI_deq[e] = e4m3_decode(codes[0]) * float(sc[0])
+        else:
+            kI_deq[e] = ki
+        entry = (e, kv_comp[e].copy(), ki)
+    r = decode_token(cfg, inp, b, 0, kv_comp, kI_deq)
+    r["entry"] = entry
+    return r

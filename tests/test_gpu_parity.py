@@ -1,0 +1,417 @@
+"""Parity of every CUDA stage with the CPU oracle on seeded inputs (GPU required).
+
+Sizes span several tiles with ragged tails; agreement per stage:
+  top-k / pool: bit-exact given the same fp32 scores;
+  indexer: |g - r| <= rtol * max(|r|, row rms), rtol 1e-2 (bf16), 5e-2 (FP8 keys), 1e-5 (fp32);
+  attention: |g - r| <= 2e-2 * max|r_row| for bf16 outputs, 1e-4 absolute for fp32;
+  compressor: bf16 rounding (2^-8 relative) or fp32 (1e-5 relative).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_csa_gb300 as csa
+from _helpers import (assert_rows_close, assert_scores_close, assert_selection_ok, keys_f64, lib_config, np64)
+from oracle import csa_oracle as O
+from synth import gen
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+def rnd(seed, shape, std=1.0, dtype=torch.float32):
+    n = int(np.prod(shape))
+    return gen.normal(seed, n, device=DEV, std=std).reshape(shape).to(dtype)
+
+
+def cfg_obj(**kw):
+    base = dict(B=2, H=64, d=512, HI=64, dI=128, m=4, k=512, W=128, act=BF16, fp8_keys=False, softmax_scale=None)
+    base.update(kw)
+    return csa.Config(**base)
+
+
+def check_dev_error():
+    assert csa.get_last_error() == 0
+
+
+# ------------------------------------------------------------------ compressor
+
+def test_compress_tiny_fp32_all_entries():
+    cfg = gen.CONFIGS[1]
+    inp = gen.make_inputs(cfg, DEV)
+    c = lib_config(cfg)
+    for kv, z, bias, dim in [(inp["kv_str"], inp["z_str"], inp["bias"], cfg.d),
+                             (inp["kvI_str"], inp["zI_str"], inp["biasI"], cfg.dI)]:
+        out = torch.zeros(cfg.B, cfg.E, dim, device=DEV)
+        csa.compress_kv(c, kv, z, bias, 0, 0, cfg.E, out)
+        check_dev_error()
+        ref = O.compress_range(np64(kv[0]), np64(z[0]), np64(bias), cfg.m, 0, cfg.E)
+        np.testing.assert_allclose(np64(out[0]), ref, rtol=1e-5, atol=1e-7)
+
+
+def test_compress_bf16_range_and_e4m3():
+    B, m, dim, n_tok, tok0 = 3, 4, 512, 160, 16
+    kv = rnd(11, (B, n_tok, 2, dim), dim ** -0.5, BF16)
+    z = rnd(12, (B, n_tok, 2, dim), 1.0, BF16)
+    bias = rnd(13, (2, m, dim), 0.1)
+    c = cfg_obj(B=B, m=m)
+    e0, e1, cap = 5, 44, 50
+    out = torch.full((B, cap, dim), 7.0, device=DEV, dtype=BF16)
+    csa.compress_kv(c, kv, z, bias, tok0, e0, e1, out)
+    codes = torch.zeros(B, cap, dim, device=DEV, dtype=torch.uint8)
+    scale = torch.zeros(B, cap, device=DEV)
+    csa.compress_kv(c, kv, z, bias, tok0, e0, e1, codes, out_scale=scale)
+    check_dev_error()
+    o = np64(out)
+    assert np.all(o[:, :e0] == 7.0) and np.all(o[:, e1:] == 7.0)
+    for b in range(B):
+        ref = O.compress_range(np64(kv[b]), np64(z[b]), np64(bias), m, e0, e1, tok0=tok0)
+        assert np.all(np.abs(o[b, e0:e1] - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-9)
+        ref32 = ref.astype(np.float32)
+        rc, rs = O.quantize_rows_e4m3(ref32)
+        gs = scale[b, e0:e1].cpu().numpy()
+        np.testing.assert_allclose(gs, rs, rtol=2e-6)
+        gc = codes[b, e0:e1].cpu().numpy()
+        deq = O.e4m3_decode(gc) * gs[:, None]
+        bound = 2.0 ** -4 * np.abs(ref) + 2.0 ** -9 * gs[:, None] + 1e-12
+        assert np.all(np.abs(deq - ref) <= bound)
+        assert (gc == rc).mean() > 0.999
+
+
+# ------------------------------------------------------------------ indexer
+
+def _indexer_ref(qI, w, q_pos, kdeq, m, T):
+    B = kdeq.shape[0]
+    E = kdeq.shape[1]
+    q = np64(qI)
+    ww = np64(w)
+    pos = q_pos.cpu().numpy()
+    out = np.empty((B * T, E))
+    for r in range(B * T):
+        b, t = divmod(r, T)
+        nv = min(O.visible_entries(int(pos[r]), m), E)
+        out[r] = O.indexer_scores(q[b, t], ww[b, t], kdeq[b], nv)
+    return out
+
+
+@pytest.mark.parametrize("HI,T,fp8", [(64, 1, False), (64, 37, False), (32, 21, False), (64, 1, True),
+                                      (64, 9, True)])
+def test_indexer_tensor_cores(HI, T, fp8):
+    B, dI, m, E = 3, 128, 4, 128 * 9 + 37
+    qI = rnd(21 + HI + T, (B, T, HI, dI), dI ** -0.5, BF16)
+    w = rnd(22 + T, (B, T, HI))
+    kf = rnd(23, (B, E, dI), dI ** -0.5)
+    if fp8:
+        kI, ks = gen.quantize_keys_e4m3(kf)
+    else:
+        kI, ks = kf.to(BF16), None
+    if T == 1:
+        q_pos = torch.tensor([m * E - 1, m * 700 + 2, m * 128 - 1], dtype=torch.int64, device=DEV)
+    else:
+        g = torch.Generator().manual_seed(T)
+        q_pos = torch.randint(0, m * E + 40, (B * T,), generator=g).to(torch.int64).to(DEV)
+    c = cfg_obj(B=B, HI=HI, dI=dI, m=m, fp8_keys=fp8)
+    scores = torch.full((B * T, E + 5), 3.0, device=DEV)
+    csa.indexer_scores(c, qI, w, q_pos, kI, scores, kscale=ks)
+    check_dev_error()
+    got = np64(scores)
+    assert np.all(got[:, E:] == 3.0)           # columns past E_cap untouched
+    ref = _indexer_ref(qI, w, q_pos, keys_f64(kI, ks), m, T)
+    worst = assert_scores_close(got[:, :E], ref, 5e-2 if fp8 else 1e-2)
+    print(f"indexer HI={HI} T={T} fp8={fp8}: worst/tol = {worst:.3f}")
+
+
+def test_indexer_cuda_core_fp32_and_candidates():
+    cfg = gen.CONFIGS[1].replace(mode="decode")
+    inp = gen.make_inputs(cfg, DEV)
+    c = lib_config(cfg)
+    rows = cfg.B * cfg.T
+    scores = torch.empty(rows, cfg.E, device=DEV)
+    csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], scores)
+    check_dev_error()
+    ref = _indexer_ref(inp["qI"], inp["w"], inp["q_pos"], np64(inp["kI"]), cfg.m, cfg.T)
+    assert_scores_close(np64(scores), ref, 1e-5)
+    # candidate mode: positions with -1 tail and some beyond the visible range
+    g = torch.Generator().manual_seed(5)
+    cand = torch.sort(torch.randperm(cfg.E, generator=g)[:100]).values.to(torch.int32)
+    cand = torch.cat([cand, torch.full((28,), -1, dtype=torch.int32)]).repeat(rows, 1).to(DEV).contiguous()
+    sc = torch.empty(rows, 128, device=DEV)
+    csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], sc, cand=cand)
+    check_dev_error()
+    cn = cand.cpu().numpy()
+    ref_c = np.where(cn >= 0, np.take_along_axis(ref, np.maximum(cn, 0), axis=1), -np.inf)
+    assert_scores_close(np64(sc), ref_c, 1e-5)
+
+
+# ------------------------------------------------------------------ top-k
+
+def _topk_check(scores, k, n_valid=None, cand=None):
+    rows, n = scores.shape
+    c = cfg_obj(k=k)
+    idx = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    nvt = None if n_valid is None else torch.tensor(n_valid, dtype=torch.int32, device=DEV)
+    csa.topk(c, scores, idx, n_valid=nvt, cand=cand)
+    check_dev_error()
+    s = scores.cpu().numpy()
+    got = idx.cpu().numpy()
+    for r in range(rows):
+        nv = n if n_valid is None else n_valid[r]
+        if cand is not None:
+            cn = cand[r].cpu().numpy()
+            nv = min(nv, int((cn >= 0).sum()))
+            slots = O.topk(s[r], nv, k)
+            ref = np.where(slots >= 0, cn[np.maximum(slots, 0)], -1)
+        else:
+            ref = O.topk(s[r], nv, k)
+        assert np.array_equal(got[r], ref), f"row {r}"
+
+
+def test_topk_long_rows_multilevel_with_ties():
+    n = 300007
+    s = rnd(31, (5, n))
+    s = torch.round(s * 64) / 64          # coarse grid: many exact ties
+    _topk_check(s.contiguous(), 512, n_valid=[n, 200000, 300, 511, 0])
+
+
+def test_topk_small_rows_and_adversarial():
+    s = rnd(32, (16, 512))
+    _topk_check(s, 64)
+    rows = torch.stack([torch.zeros(5000), torch.where(torch.arange(5000) % 2 == 0, 0.0, -0.0),
+                        torch.full((5000,), -math.inf), torch.arange(5000, dtype=torch.float32),
+                        -torch.arange(5000, dtype=torch.float32)]).to(DEV)
+    _topk_check(rows.contiguous(), 512)
+    _topk_check(rows.contiguous(), 4096)
+
+
+def test_topk_candidate_map():
+    rows, n = 4, 16384
+    s = rnd(33, (rows, n))
+    cand = torch.stack([torch.sort(torch.randperm(262144, generator=torch.Generator().manual_seed(r))[:n]).values
+                        for r in range(rows)]).to(torch.int32)
+    cand[1, 9000:] = -1
+    cand = cand.to(DEV).contiguous()
+    _topk_check(s, 512, cand=cand)
+
+
+def test_block_pool_matches_oracle():
+    rows, n = 3, 20005
+    s = rnd(34, (rows, n))
+    s = torch.round(s * 16) / 16
+    nv = [20005, 12345, 100]
+    c = cfg_obj()
+    for n_blocks in (256, 2048):
+        pool = torch.full((rows, n_blocks * 8), -7, dtype=torch.int32, device=DEV)
+        cnt = torch.zeros(rows, dtype=torch.int32, device=DEV)
+        csa.block_pool(c, s, pool, cnt, n_valid=torch.tensor(nv, dtype=torch.int32, device=DEV),
+                       n_blocks=n_blocks)
+        check_dev_error()
+        sn = s.cpu().numpy()
+        for r in range(rows):
+            ref = O.hier_pool(sn[r], nv[r], 8, n_blocks)
+            got = pool[r].cpu().numpy()
+            assert int(cnt[r]) == ref.size
+            assert np.array_equal(got[:ref.size], ref)
+            assert np.all(got[ref.size:] == -1)
+
+
+# ------------------------------------------------------------------ attention
+
+def _attn_inputs(seed, B, T, H, d, E, k, L, dtype, n_sel_rows=None):
+    q = rnd(seed, (B, T, H, d), d ** -0.5, dtype)
+    kv = rnd(seed + 1, (B, E, d), d ** -0.5, dtype)
+    kl = rnd(seed + 2, (B, L, d), d ** -0.5, dtype)
+    sink = rnd(seed + 3, (H,))
+    g = torch.Generator().manual_seed(seed)
+    idx = torch.full((B * T, k), -1, dtype=torch.int32)
+    for r in range(B * T):
+        nsel = k if n_sel_rows is None else n_sel_rows[r % len(n_sel_rows)]
+        idx[r, :nsel] = torch.sort(torch.randperm(E, generator=g)[:nsel]).values.to(torch.int32)
+    return q, kv, kl, sink, idx.to(DEV)
+
+
+def _attn_ref(q, kv, idx, kl, local_base, q_pos, sink, W, scale):
+    B, T = q.shape[:2]
+    qn, kvn, kln = np64(q), np64(kv), np64(kl)
+    idn, lb, qp, sk = idx.cpu().numpy(), local_base.cpu().numpy(), q_pos.cpu().numpy(), np64(sink)
+    outs, lses = [], []
+    for r in range(B * T):
+        b, t = divmod(r, T)
+        rows = O.gather_rows(kvn[b], idn[r], kln[b], int(lb[b]), int(qp[r]), W)
+        o, l = O.sparse_attention(qn[b, t], rows, sk, scale)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs).reshape(q.shape), np.stack(lses).reshape(B, T, -1)
+
+
+@pytest.mark.parametrize("B,T,nsel", [(3, 1, [512, 300, 512]), (1, 160, [512, 77]), (2, 2, [0, 512])])
+def test_attention_tensor_cores(B, T, nsel):
+    H, d, E, k, W, L = 64, 512, 1500, 512, 128, 200
+    q, kv, kl, sink, idx = _attn_inputs(40 + T, B, T, H, d, E, k, L, BF16, nsel)
+    local_base = torch.tensor([1000, 1040, 0][:B], dtype=torch.int64, device=DEV)
+    # windows: fully held, clipped by the local rows' start, and t < W - 1 (starts at 0)
+    base_t = [1000 + 150, 1040 + 60, 50]
+    q_pos = torch.tensor([base_t[b] + (t % 3) for b in range(B) for t in range(T)], dtype=torch.int64, device=DEV)
+    c = cfg_obj(B=B)
+    out = torch.empty(B, T, H, d, device=DEV, dtype=BF16)
+    lse = torch.empty(B, T, H, device=DEV)
+    csa.sparse_attn(c, q, kv, idx, kl, local_base, q_pos, sink, out, lse)
+    check_dev_error()
+    ro, rl = _attn_ref(q, kv, idx, kl, local_base, q_pos, sink, W, d ** -0.5)
+    w1 = assert_rows_close(np64(out), ro, 2e-2)
+    np.testing.assert_allclose(np64(lse), rl, atol=2e-3, rtol=0)
+    print(f"attention B={B} T={T}: worst/tol = {w1:.3f}")
+
+
+def test_attention_cuda_core_fp32():
+    cfg = gen.CONFIGS[1]
+    H, d, k, W = cfg.H, cfg.d, cfg.k, cfg.W
+    B, T, E, L = 2, 16, 512, 60
+    q, kv, kl, sink, idx = _attn_inputs(50, B, T, H, d, E, k, L, torch.float32, [64, 10, 0, 64])
+    local_base = torch.tensor([100, 0], dtype=torch.int64, device=DEV)
+    q_pos = torch.tensor([130 + t for t in range(T)] + [5 + t for t in range(T)], dtype=torch.int64, device=DEV)
+    c = lib_config(cfg, B=B)
+    out = torch.empty(B, T, H, d, device=DEV)
+    lse = torch.empty(B, T, H, device=DEV)
+    csa.sparse_attn(c, q, kv, idx, kl, local_base, q_pos, sink, out, lse)
+    check_dev_error()
+    ro, rl = _attn_ref(q, kv, idx, kl, local_base, q_pos, sink, W, cfg.softmax_scale)
+    np.testing.assert_allclose(np64(out), ro, atol=1e-5, rtol=1e-4)
+    np.testing.assert_allclose(np64(lse), rl, atol=1e-5, rtol=1e-5)
+
+
+# ------------------------------------------------------------------ compositions
+
+def _np_inputs(inp):
+    out = {}
+    for k_, v in inp.items():
+        if v.dtype in (torch.float32, torch.bfloat16):
+            out[k_] = np64(v)
+        else:
+            out[k_] = v.cpu().numpy()
+    return out
+
+
+def _oracle_decode(cfg, inp):
+    """The oracle's decode step for every sequence of the batch."""
+    nb = _np_inputs(inp)
+    fp8 = cfg.kidx == "fp8"
+    res = []
+    for b in range(cfg.B):
+        kdeq = keys_f64(inp["kI"][b], inp["kscale"][b] if fp8 else None)
+        res.append(O.decode_step_sequence(cfg, nb, b, nb["kv_comp"][b].copy(), kdeq, fp8_keys=fp8))
+    return res
+
+
+def _run_gpu_decode(cfg, inp):
+    c = lib_config(cfg)
+    out = torch.empty(cfg.B, cfg.H, cfg.d, device=DEV, dtype=cfg.torch_act)
+    lse = torch.empty(cfg.B, cfg.H, device=DEV)
+    idx = torch.empty(cfg.B, cfg.k, dtype=torch.int32, device=DEV)
+    csa.decode_step(c, q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"],
+                    kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
+                    z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
+                    biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse,
+                    idx_out=idx)
+    check_dev_error()
+    return out, lse, idx
+
+
+@pytest.mark.parametrize("cid,N", [(2, 4 * 1500), (4, 4 * 2500)])
+def test_decode_step_matches_oracle(cid, N):
+    cfg = gen.CONFIGS[cid].replace(B=3, N=N)
+    inp = gen.make_inputs(cfg, DEV)
+    inp["q_pos"][1] = N - 3          # this token completes no block: no compression
+    kv_before = inp["kv_comp"].clone()
+    ref = _oracle_decode(cfg, inp)   # oracle reads the inputs before the step mutates the caches
+    out, lse, idx = _run_gpu_decode(cfg, inp)
+    rtol_s = 5e-2 if cfg.kidx == "fp8" else 1e-2
+    for b in range(cfg.B):
+        r = ref[b]
+        fin = r["scores"][np.isfinite(r["scores"])]
+        tol = rtol_s * max(np.sqrt((fin ** 2).mean()), 1e-30)
+        swaps = assert_selection_ok(idx[b].cpu().numpy(), r["idx"], r["scores"], cfg.k, tol)
+        assert_rows_close(np64(out[b]), r["out"], 2e-2, what=f"out b={b} swaps={swaps}")
+        np.testing.assert_allclose(np64(lse[b]), r["lse"], atol=5e-3)
+        if r["entry"] is not None:
+            e, ent, _ = r["entry"]
+            assert np.all(np.abs(np64(inp["kv_comp"][b, e]) - ent) <= 2.0 ** -8 * np.abs(ent) + 1e-9)
+        else:
+            assert torch.equal(inp["kv_comp"][b], kv_before[b])
+
+
+def test_tiny_end_to_end_fp32():
+    """Preset 1: compress every entry from the streams, index, select, attend (16 queries)."""
+    cfg = gen.CONFIGS[1]
+    inp = gen.make_inputs(cfg, DEV)
+    c = lib_config(cfg)
+    kvc = torch.zeros(cfg.B, cfg.E, cfg.d, device=DEV)
+    kI = torch.zeros(cfg.B, cfg.E, cfg.dI, device=DEV)
+    csa.compress_kv(c, inp["kv_str"], inp["z_str"], inp["bias"], 0, 0, cfg.E, kvc)
+    csa.compress_kv(c, inp["kvI_str"], inp["zI_str"], inp["biasI"], 0, 0, cfg.E, kI)
+    rows = cfg.B * cfg.T
+    scores = torch.empty(rows, cfg.E, device=DEV)
+    csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], kI, scores)
+    idx = torch.empty(rows, cfg.k, dtype=torch.int32, device=DEV)
+    nv = ((inp["q_pos"] + 1) // cfg.m).clamp(max=cfg.E).to(torch.int32)
+    csa.topk(c, scores, idx, n_valid=nv)
+    out = torch.empty(cfg.B, cfg.T, cfg.H, cfg.d, device=DEV)
+    lse = torch.empty(cfg.B, cfg.T, cfg.H, device=DEV)
+    csa.sparse_attn(c, inp["q"], kvc, idx, inp["kv_local"], inp["local_base"], inp["q_pos"], inp["sink"], out, lse)
+    check_dev_error()
+    nb = _np_inputs(inp)
+    kv_ref = O.compress_range(nb["kv_str"][0], nb["z_str"][0], nb["bias"], cfg.m, 0, cfg.E)
+    ki_ref = O.compress_range(nb["kvI_str"][0], nb["zI_str"][0], nb["biasI"], cfg.m, 0, cfg.E)
+    for tq in range(cfg.T):
+        r = O.decode_token(cfg, nb, 0, tq, kv_ref, ki_ref)
+        fin = r["scores"][np.isfinite(r["scores"])]
+        tol = 1e-5 * np.sqrt((fin ** 2).mean())
+        swaps = assert_selection_ok(idx[tq].cpu().numpy(), r["idx"], r["scores"], cfg.k, tol)
+        assert swaps == 0
+        np.testing.assert_allclose(np64(out[0, tq]), r["out"], atol=1e-4, rtol=0)
+        np.testing.assert_allclose(np64(lse[0, tq]), r["lse"], atol=1e-4, rtol=0)
+
+
+def test_csa2_group_matches_oracle():
+    """CSA2 decoder group: Full-layer scan -> block pool -> Reindex rescoring -> top-k -> 4 attentions."""
+    base = gen.CONFIGS[5]
+    cfg = base.replace(B=2, N=6000)
+    n_blocks = 128
+    inp = gen.make_inputs(cfg, DEV)
+    c = lib_config(cfg)
+    B, E = cfg.B, cfg.E
+    s_full = torch.empty(B, E, device=DEV)
+    csa.indexer_scores(c, inp["qI_full"], inp["w_full"], inp["q_pos"], inp["kI"], s_full)
+    pool = torch.empty(B, n_blocks * 8, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(B, dtype=torch.int32, device=DEV)
+    csa.block_pool(c, s_full, pool, cnt, n_blocks=n_blocks)
+    s_pool = torch.empty(B, n_blocks * 8, device=DEV)
+    csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], s_pool, cand=pool)
+    idx = torch.empty(B, cfg.k, dtype=torch.int32, device=DEV)
+    csa.topk(c, s_pool, idx, n_valid=cnt, cand=pool)
+    outs = []
+    for layer in range(1 + cfg.n_reuse):
+        o = torch.empty(B, 1, cfg.H, cfg.d, device=DEV, dtype=BF16)
+        csa.sparse_attn(c, inp["q"][layer], inp["kv_comp"], idx, inp["kv_local"][layer], inp["local_base"],
+                        inp["q_pos"], inp["sink"][layer], o)
+        outs.append(o)
+    check_dev_error()
+    nb = _np_inputs(inp)
+    for b in range(B):
+        t = int(nb["q_pos"][b])
+        nv = min(t + 1, E)
+        sf = O.indexer_scores(nb["qI_full"][b, 0], nb["w_full"][b, 0], nb["kI"][b], nv).astype(np.float32)
+        rpool = O.hier_pool(sf, nv, 8, n_blocks)
+        srei = O.indexer_scores_subset(nb["qI"][b, 0], nb["w"][b, 0], nb["kI"][b], rpool)
+        slots = O.topk(srei.astype(np.float32), rpool.size, cfg.k)
+        ridx = np.where(slots >= 0, rpool[np.maximum(slots, 0)], -1)
+        all_rei = O.indexer_scores(nb["qI"][b, 0], nb["w"][b, 0], nb["kI"][b], nv)
+        tol = 1e-2 * np.sqrt((all_rei[:nv] ** 2).mean())
+        assert_selection_ok(idx[b].cpu().numpy(), ridx, all_rei, cfg.k, tol)
+        for layer in range(1 + cfg.n_reuse):
+            rows = O.gather_rows(nb["kv_comp"][b], ridx, nb["kv_local"][layer][b], int(nb["local_base"][b]), t,
+                                 cfg.W)
+            ro, _ = O.sparse_attention(nb["q"][layer][b, 0], rows, nb["sink"][layer], cfg.softmax_scale)
+            assert_rows_close(np64(outs[layer][b, 0]), ro, 2e-2, what=f"layer {layer} b={b}")
