@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--config", type=int, default=4, choices=[2, 4])
     ap.add_argument("--cpu-seqs", type=int, default=12, help="decode tokens in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["step", "indexer"], default=None,
+                    help="run only this stage on the workload (for profiler captures); prints its time")
     return ap.parse_args()
 
 
@@ -219,6 +221,26 @@ def main():
         csa.decode_step(c, **args_d)
 
     stream = torch.cuda.current_stream(dev)
+    if args.only:
+        scores_only = torch.empty(cfg.B, cfg.E, device=dev)
+
+        def only_fn():
+            if args.only == "step":
+                step()
+            else:
+                csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], scores_only,
+                                   kscale=inp.get("kscale"))
+        for _ in range(args.warmup):
+            only_fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            only_fn()
+        torch.cuda.synchronize(dev)
+        assert csa.get_last_error() == 0
+        print(json.dumps({"only": args.only, "config": args.config, "calls": args.steps,
+                          "ms_per_call_back_to_back": 1e3 * (time.perf_counter() - t0) / max(args.steps, 1)}))
+        return
     for _ in range(args.warmup):
         flush.zero_()
         step()

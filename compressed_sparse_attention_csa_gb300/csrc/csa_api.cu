@@ -3,6 +3,7 @@
 // then enqueues kernels on the caller's stream; nothing here allocates memory.
 #include <cmath>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -63,6 +64,22 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+bool encode_tmap_generic(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[5] = {0, 0, 0, 0, 0};
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  return fn(map, dtype, static_cast<cuuint32_t>(rank), base, d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -108,7 +125,8 @@ size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   size_t bytes = align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
   bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
-  bytes += align_up(topk_workspace_bytes(B, E_cap, c->k, sms), 256);
+  bytes += align_up(static_cast<size_t>(B) * (kTopkHistBins + 1) * 4, 256);  // histograms + counters
+  bytes += align_up(std::max(topk_workspace_bytes(B, E_cap, c->k, sms), topk_hist_workspace_bytes(B, c->k)), 256);
   bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms), 256);
   return bytes;
 }
@@ -190,7 +208,7 @@ csa_status csa_compress_kv(const csa_config* cfg, int32_t dim, const void* kv, c
   if (out_dtype != CSA_F32 && out_dtype != CSA_BF16 && out_dtype != CSA_E4M3) return CSA_ERR_DTYPE;
   if (!aligned16(kv) || !aligned16(z) || !aligned16(bias) || !aligned16(out) || (out_scale && !aligned16(out_scale)))
     return CSA_ERR_ALIGN;
-  if (dim < 1 || dim > 1024 || n_tok < 0 || ent_begin < 0 || ent_end < ent_begin || ent_end > E_cap)
+  if (dim < 1 || dim > 512 || cfg->m > 16 || n_tok < 0 || ent_begin < 0 || ent_end < ent_begin || ent_end > E_cap)
     return CSA_ERR_SHAPE;
   const int64_t m = cfg->m;
   if (ent_end > ent_begin) {
@@ -198,20 +216,15 @@ csa_status csa_compress_kv(const csa_config* cfg, int32_t dim, const void* kv, c
     if (tok0 > need_lo || m * ent_end > tok0 + n_tok) return CSA_ERR_SHAPE;
   }
   CompressArgs a{};
-  a.kv = kv;
-  a.z = z;
-  a.bias = bias;
+  a.job[0] = CompressJob{kv, z, bias, dim, out, out_dtype, out_scale};
+  a.n_jobs = 1;
   a.B = cfg->B;
-  a.dim = dim;
   a.m = cfg->m;
   a.act_bf16 = cfg->act == CSA_BF16;
   a.n_tok = n_tok;
   a.tok0 = tok0;
   a.ent_begin = ent_begin;
   a.n_ent = ent_end - ent_begin;
-  a.out = out;
-  a.out_dtype = out_dtype;
-  a.out_scale = out_scale;
   a.E_cap = E_cap;
   a.err = err_word_ptr();
   return launch_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -375,7 +388,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   if ((d->kscale && !aligned16(d->kscale)) || (d->lse && !aligned16(d->lse)) ||
       (d->idx_out && !aligned16(d->idx_out)) || (ws && !aligned16(ws)))
     return CSA_ERR_ALIGN;
-  if (d->E_cap < 1 || d->E_cap > (int64_t(1) << 24) || d->L < 0 || !attn_shape_ok(cfg) || cfg->d > 1024 ||
+  if (d->E_cap < 1 || d->E_cap > (int64_t(1) << 24) || d->L < 0 || !attn_shape_ok(cfg) || cfg->d > 512 || cfg->m > 16 ||
       cfg->HI > 128 || d->E_cap * cfg->B >= (int64_t(1) << 31))
     return CSA_ERR_SHAPE;
   const int sms = device_sm_count();
@@ -390,7 +403,10 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   p += align_up(static_cast<size_t>(cfg->B) * 4, 256);
   int32_t* idx = reinterpret_cast<int32_t*>(p);
   p += align_up(static_cast<size_t>(cfg->B) * cfg->k * 4, 256);
-  const size_t topk_ws = topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms);
+  uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(p);
+  p += align_up(static_cast<size_t>(cfg->B) * (kTopkHistBins + 1) * 4, 256);
+  const size_t topk_ws =
+      std::max(topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms), topk_hist_workspace_bytes(cfg->B, cfg->k));
   void* ws_topk = p;
   p += align_up(topk_ws, 256);
   void* ws_attn = p;
@@ -404,25 +420,14 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   c.q_pos = d->q_pos;
   c.E_cap = d->E_cap;
   c.err = err;
-  c.kv = d->kv_tail;
-  c.z = d->z_tail;
-  c.bias = d->bias;
-  c.dim = cfg->d;
-  c.out = d->kv_comp;
-  c.out_dtype = cfg->act;
+  c.job[0] = CompressJob{d->kv_tail, d->z_tail, d->bias, cfg->d, d->kv_comp, cfg->act, nullptr};
+  c.job[1] = CompressJob{d->kvI_tail, d->zI_tail, d->biasI, cfg->dI, d->kI, cfg->kidx, d->kscale};
+  c.n_jobs = 2;
+  c.zero_hist = hist_cnt;
   cudaError_t e = launch_compress(c, s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
-  c.kv = d->kvI_tail;
-  c.z = d->zI_tail;
-  c.bias = d->biasI;
-  c.dim = cfg->dI;
-  c.out = d->kI;
-  c.out_dtype = cfg->kidx;
-  c.out_scale = d->kscale;
-  e = launch_compress(c, s);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
 
-  // 2. indexer over the visible entries
+  // 2. indexer over the visible entries (the tensor-core path also histograms the scores)
   IndexerArgs ia{};
   ia.qI = d->qI;
   ia.w = d->w;
@@ -442,10 +447,16 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   ia.err = err;
   ia.num_sms = sms;
   ia.nv_out = nv;
+  const bool hist_topk = indexer_uses_tensor_cores(ia);
+  ia.hist_out = hist_topk ? hist_cnt : nullptr;
   e = launch_indexer(ia, s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
 
   // 3. top-k
+  if (hist_topk) {
+    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+  } else {
   TopkArgs ta{};
   ta.scores = scores;
   ta.ld = d->E_cap;
@@ -460,6 +471,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   ta.num_sms = sms;
   e = launch_topk(ta, s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
+  }
 
   // 4. sparse attention over the selection plus the window, with the sink
   AttnArgs aa{};

@@ -10,21 +10,28 @@
 namespace csa {
 
 // ---- compression ------------------------------------------------------------------
-struct CompressArgs {
+struct CompressJob {    // one cache produced by the compressor
   const void* kv;       // [B, n_tok, 2, dim]
   const void* z;        // [B, n_tok, 2, dim]
   const float* bias;    // [2, m, dim]
-  int B, dim, m;
+  int dim;              // <= 512
+  void* out;            // [B, E_cap, dim]
+  int out_dtype;        // CSA_F32 / CSA_BF16 / CSA_E4M3
+  float* out_scale;     // [B, E_cap] for e4m3
+};
+struct CompressArgs {
+  CompressJob job[2];
+  int n_jobs;
+  int B, m;             // m <= 16
   bool act_bf16;        // input dtype
   int64_t n_tok, tok0;  // uniform mode: stream row r holds token tok0 + r
   int64_t ent_begin, n_ent;
   const int64_t* q_pos; // decode mode (non-null): per sequence t = q_pos[b]; rows hold t-2m+1..t;
                         // the entry (t+1)/m - 1 is produced only when (t+1) % m == 0
-  void* out;            // [B, E_cap, dim]
-  int out_dtype;        // CSA_F32 / CSA_BF16 / CSA_E4M3
-  float* out_scale;     // [B, E_cap] for e4m3
   int64_t E_cap;
   int* err;
+  uint32_t* zero_hist;  // decode step: per-sequence top-k histogram rows [B, 4096] and the B
+                        // candidate counters after them, zeroed here before the indexer runs
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 
@@ -46,6 +53,8 @@ struct IndexerArgs {
   int* err;
   int num_sms;
   int32_t* nv_out;       // [B*T] visible-entry count per query row, or null
+  uint32_t* hist_out;    // [B*T, 4096] digit histogram of the visible scores (one query per CTA
+                         // only), accumulated with atomics; null = none
 };
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
 bool indexer_uses_tensor_cores(const IndexerArgs& a);
@@ -65,6 +74,17 @@ struct TopkArgs {
 };
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+
+// Histogram-guided top-k for a few long rows.  hist_cnt holds rows x 4096 digit counts
+// followed by rows candidate counters, all zero before the indexer fills the histogram.
+constexpr int kTopkHistBins = 4096;
+int topk_hist_cap(int k);
+size_t topk_hist_workspace_bytes(int64_t rows, int k);  // the candidate lists (ws_cand)
+bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);
+size_t topk_hist_standalone_bytes(int64_t rows, int k);
+cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
+cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s);
 
 struct PoolArgs {
   const float* scores;
@@ -107,6 +127,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 // ---- shared host utilities ---------------------------------------------------------
 int device_sm_count();
 void count_launches(int n);  // bookkeeping for csa_launch_count()
+bool encode_tmap_generic(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 

@@ -465,28 +465,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   }
 }
 
-// Fixed-order merge of the split partials with the sink.
-__global__ void __launch_bounds__(512) attn_merge_kernel(const AttnArgs a, const TcAttnSplit sp) {
+// Fixed-order merge of the split partials with the sink.  One CTA per (row, 4 heads); each
+// thread owns 4 consecutive dims of one head and issues all its partial loads at once.
+constexpr int kMergeHeads = 4;
+constexpr int kMaxSplit = 16;
+__global__ void __launch_bounds__(kMergeHeads * kD / 4) attn_merge_kernel(const AttnArgs a, const TcAttnSplit sp) {
   const int64_t r = blockIdx.x;
-  const int dd = threadIdx.x;  // 0..511
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + r * kH * kD;
-  const float* ml = sp.part_ml + r * sp.n_split * 2 * kH;
-  const float* po = sp.part_o + r * sp.n_split * kH * kD;
-  for (int h = 0; h < kH; ++h) {
-    const float sk = a.sink[h] * kLog2e;
-    float M = sk;
-    for (int s = 0; s < sp.n_split; ++s) M = fmaxf(M, ml[s * 2 * kH + h]);
-    float den = exp2f(sk - M), acc = 0.f;
-    for (int s = 0; s < sp.n_split; ++s) {
-      const float ms = ml[s * 2 * kH + h];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - M);
-      den = fmaf(ml[s * 2 * kH + kH + h], f, den);
-      acc = fmaf(po[(static_cast<int64_t>(s) * kH + h) * kD + dd], f, acc);
+  const int h = blockIdx.y * kMergeHeads + threadIdx.x / (kD / 4);
+  const int d4 = threadIdx.x % (kD / 4);
+  const int ns = sp.n_split;
+  const float* ml = sp.part_ml + r * ns * 2 * kH;
+  const float* po = sp.part_o + r * ns * kH * kD;
+  const float sk = a.sink[h] * kLog2e;
+  float ms[kMaxSplit], ls[kMaxSplit];
+  float4 o[kMaxSplit];
+  float M = sk;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < ns) {
+      ms[s] = ml[s * 2 * kH + h];
+      ls[s] = ml[s * 2 * kH + kH + h];
+      o[s] = *reinterpret_cast<const float4*>(po + (static_cast<int64_t>(s) * kH + h) * kD + 4 * d4);
+      M = fmaxf(M, ms[s]);
     }
-    out[h * kD + dd] = __float2bfloat16_rn(acc / den);
-    if (dd == 0 && a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
   }
+  float den = exp2f(sk - M);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < ns && ms[s] != -INFINITY) {
+      const float f = exp2f(ms[s] - M);
+      den = fmaf(ls[s], f, den);
+      acc.x = fmaf(o[s].x, f, acc.x);
+      acc.y = fmaf(o[s].y, f, acc.y);
+      acc.z = fmaf(o[s].z, f, acc.z);
+      acc.w = fmaf(o[s].w, f, acc.w);
+    }
+  }
+  const float inv = 1.f / den;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (r * kH + h) * kD + 4 * d4;
+  const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<const uint32_t*>(&p0);
+  pk.y = *reinterpret_cast<const uint32_t*>(&p1);
+  *reinterpret_cast<uint2*>(out) = pk;
+  if (d4 == 0 && a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
 }
 
 bool attn_uses_tensor_cores(int act, int H, int d, int k) {
@@ -500,6 +524,10 @@ TcAttnSplit plan_split(int B, int T, int k, int W, int num_sms) {
   if (rows < num_sms && max_rows > kRows) {
     s.rows_per_split = kRows;
     s.n_split = (max_rows + kRows - 1) / kRows;
+    if (s.n_split > kMaxSplit) {
+      s.rows_per_split = ((max_rows + kMaxSplit - 1) / kMaxSplit + kRows - 1) / kRows * kRows;
+      s.n_split = (max_rows + s.rows_per_split - 1) / s.rows_per_split;
+    }
   } else {
     s.rows_per_split = max_rows;
     s.n_split = 1;
@@ -539,7 +567,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || sp.n_split == 1) return e;
-    attn_merge_kernel<<<static_cast<unsigned>(rows), kD, 0, s>>>(a, sp);
+    attn_merge_kernel<<<dim3(static_cast<unsigned>(rows), kH / kMergeHeads), kMergeHeads * kD / 4, 0, s>>>(a, sp);
     count_launches(1);
     return cudaGetLastError();
   }

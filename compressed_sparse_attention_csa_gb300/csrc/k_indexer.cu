@@ -78,12 +78,15 @@ struct TcLayout {
   int N;               // MMA N = G * HI (bf16) or G * 2 * HI (e4m3 hi/lo)
   int stages;
   uint32_t b_bytes;    // B operand (queries), 1024-aligned
-  uint32_t stage_bytes;
+  uint32_t stage_bytes;  // stride between ring stages (1024-aligned)
+  uint32_t stage_tx;     // bytes the TMA delivers per stage (keys, + scales for e4m3)
   uint32_t smem_bytes;
   uint32_t tmem_cols;
   int n_splits;        // key-range splits per (sequence, query group)
   int n_qgroups;
 };
+
+constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
 
 __device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -92,6 +95,12 @@ __device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Warp 0: TMA producer (starts streaming key tiles at once).  Warps 1..5 stage the query
+// operand, then warp 1 issues the MMAs and warps 2..5 run the epilogue.
 template <bool FP8>
 __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const IndexerArgs a, const TcLayout L,
@@ -110,12 +119,16 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
   uint64_t* tempty = bars + 2 * S + 2;
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
+  uint32_t* sHist = reinterpret_cast<uint32_t*>(sTmem + 4);  // [4096] when a.hist_out (G == 1)
+  const bool hist = a.hist_out != nullptr && G == 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, g0 = blockIdx.y * G, split = blockIdx.x;
   const int T = a.T;
   const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
 
+  if (hist)
+    for (int i = tid; i < kTopkHistBins; i += kTcThreads) sHist[i] = 0u;
   if (tid < kMaxG) {
     int nv = 0;
     if (tid < G && g0 + tid < T) {
@@ -127,58 +140,6 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
     sNv[tid] = nv;
   }
   if (tid == 0) *sAbort = 0;
-
-  // ---- stage the B operand (the group's query heads) in the 128B-swizzled K-major layout
-  if constexpr (!FP8) {
-    const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-    const int n_chunks = N * 16;  // 256 bytes per row = 16 chunks of 16 B
-    for (int i = tid; i < n_chunks; i += kTcThreads) {
-      const int n = i >> 4, c = i & 15;
-      const int g = n / HI, h = n - g * HI;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (g < G && g0 + g < T) v = *reinterpret_cast<const uint4*>(qI + ((qrow0 + g) * HI + h) * 128 + c * 8);
-      *reinterpret_cast<uint4*>(sB + (c >> 3) * (N * 128) + sw128(n, c & 7)) = v;
-    }
-    for (int i = tid; i < G * HI; i += kTcThreads) {
-      const int g = i / HI;
-      sW[i] = (g0 + g < T) ? a.w[(qrow0 + g) * HI + (i - g * HI)] : 0.f;
-    }
-  } else {
-    const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-    for (int gh = warp; gh < G * HI; gh += kTcThreads / 32) {
-      const int g = gh / HI, h = gh - g * HI;
-      const bool valid = g0 + g < T;
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (valid) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(qI + ((qrow0 + g) * HI + h) * 128 + lane * 4);
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        x[0] = __low2float(p0);
-        x[1] = __high2float(p0);
-        x[2] = __low2float(p1);
-        x[3] = __high2float(p1);
-      }
-      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      const float sc = am > 0.f ? am / 448.f : 1.f;
-      const float inv = 1.f / sc;
-      uint32_t hi4 = 0u, lo4 = 0u;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float y = x[j] * inv;
-        const uint8_t ch = f_to_e4m3(y);
-        const uint8_t cl = f_to_e4m3((y - e4m3_to_f(ch)) * 16.f);
-        hi4 |= static_cast<uint32_t>(ch) << (8 * j);
-        lo4 |= static_cast<uint32_t>(cl) << (8 * j);
-      }
-      const int n_hi = g * 2 * HI + h, n_lo = n_hi + HI;
-      *reinterpret_cast<uint32_t*>(sB + sw128(n_hi, lane >> 2) + (lane & 3) * 4) = hi4;
-      *reinterpret_cast<uint32_t*>(sB + sw128(n_lo, lane >> 2) + (lane & 3) * 4) = lo4;
-      if (lane == 0) sW[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
-    }
-  }
-
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -194,7 +155,6 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
     tmem_alloc(sTmem, L.tmem_cols);
     tmem_relinquish();
   }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -207,16 +167,6 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
   const int tile_hi = static_cast<int>(static_cast<int64_t>(split + 1) * tiles_needed / L.n_splits);
   const int n_it = tile_hi - tile_lo;
 
-  // columns past the last visible tile: -inf (written by the last split of the group)
-  if (split == L.n_splits - 1) {
-    for (int g = 0; g < G; ++g) {
-      if (g0 + g >= T) break;
-      float* dst = a.scores + (qrow0 + g) * a.ld;
-      for (int64_t c = static_cast<int64_t>(tiles_needed) * kTile + tid; c < n_cols; c += kTcThreads)
-        dst[c] = -INFINITY;
-    }
-  }
-
   if (warp == 0) {
     if (lane == 0 && n_it > 0) {
       tma_prefetch_desc(&kmap);
@@ -225,8 +175,9 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
       for (int it = 0; it < n_it; ++it) {
         const int st = it % S;
         if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) break;
-        mbar_arrive_expect_tx(&full[st], L.stage_bytes);
-        const int row = static_cast<int>(static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it) * kTile);
+        mbar_arrive_expect_tx(&full[st], L.stage_tx);
+        const int64_t row64 = static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it) * kTile;
+        const int row = static_cast<int>(row64);
         uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
         tma_load_2d_hint(dst, &kmap, &full[st], 0, row, pol);
         if constexpr (!FP8) tma_load_2d_hint(dst + 16384, &kmap, &full[st], 64, row, pol);
@@ -235,82 +186,181 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
       // every load issued must have landed before the CTA may exit
       for (int it = max(0, issued - S); it < issued; ++it) wait_time_only(&full[it % S], (it / S) & 1);
     }
-  } else if (warp == 1) {
-    if (lane == 0 && n_it > 0) {
-      const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
-      const uint32_t bBase = smem_u32(sB);
-      int committed = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % S, acc = it & 1;
-        if (!mbar_wait(&full[st], (it / S) & 1, a.err, sAbort)) break;
-        if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, a.err, sAbort)) break;
-        tc_fence_after();
-        const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
-        const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
-        if constexpr (FP8) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f8(d, smem_desc(aBase + ks * 32, 16, 1024), smem_desc(bBase + ks * 32, 16, 1024), idesc, ks > 0);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
-            const uint32_t boff = (ks >> 2) * static_cast<uint32_t>(N * 128) + (ks & 3) * 32u;
-            mma_bf16(d, smem_desc(aBase + off, 16, 1024), smem_desc(bBase + boff, 16, 1024), idesc, ks > 0);
-          }
-        }
-        mma_commit(&empty[st]);
-        mma_commit(&tfull[acc]);
-        ++committed;
+    // columns past the last visible tile: -inf (written by the last split of the group)
+    if (split == L.n_splits - 1) {
+      for (int g = 0; g < G; ++g) {
+        if (g0 + g >= T) break;
+        float* dst = a.scores + (qrow0 + g) * a.ld;
+        for (int64_t c = static_cast<int64_t>(tiles_needed) * kTile + lane; c < n_cols; c += 32) dst[c] = -INFINITY;
       }
-      if (committed > 0) wait_time_only(&tfull[(committed - 1) & 1], ((committed - 1) >> 1) & 1);
     }
   } else {
-    const int q = warp & 3;  // TMEM lane quadrant of this warp
-    const int rin = q * 32 + lane;
-    const int hstride = FP8 ? 2 * HI : HI;
-    for (int it = 0; it < n_it; ++it) {
-      const int acc = it & 1;
-      if (!mbar_wait(&tfull[acc], (it >> 1) & 1, a.err, sAbort)) break;
-      tc_fence_after();
-      const int64_t s = static_cast<int64_t>(tile_lo + it) * kTile + rin;
-      float res[kMaxG];
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
+    // ---- stage the B operand (the group's query heads), 128B-swizzled K-major
+    const int t2 = tid - 32, nthr = kTcThreads - 32;
+    if constexpr (!FP8) {
+      const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
+      const int n_chunks = N * 16;  // 256 bytes per row = 16 chunks of 16 B
+      for (int i = t2; i < n_chunks; i += nthr) {
+        const int n = i >> 4, c = i & 15;
+        const int g = n / HI, h = n - g * HI;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (g < G && g0 + g < T) v = *reinterpret_cast<const uint4*>(qI + ((qrow0 + g) * HI + h) * 128 + c * 8);
+        *reinterpret_cast<uint4*>(sB + (c >> 3) * (N * 128) + sw128(n, c & 7)) = v;
+      }
+      for (int i = t2; i < G * HI; i += nthr) {
+        const int g = i / HI;
+        sW[i] = (g0 + g < T) ? a.w[(qrow0 + g) * HI + (i - g * HI)] : 0.f;
+      }
+    } else {
+      const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
+      // all of this warp's query rows are loaded first (one round trip), then quantised
+      constexpr int kMaxRowsPerWarp = (256 / 2 + 4) / 5;  // G*HI <= 128 rows over 5 warps
+      uint2 raw[kMaxRowsPerWarp];
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
-        res[g] = 0.f;
-        if (g >= G) continue;
-        const float* wg = sW + g * HI;
-        float accum = 0.f;
-        for (int hc = 0; hc < HI; hc += 32) {
-          float v[32];
-          tmem_ld32(lane_base + g * hstride + hc, v);
-          if constexpr (FP8) {
-            float u[32];
-            tmem_ld32(lane_base + g * hstride + HI + hc, u);
-            tmem_wait_ld(v);
-            tmem_wait_ld(u);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) accum = fmaf(wg[hc + j], fmaxf(fmaf(u[j], 0.0625f, v[j]), 0.f), accum);
-          } else {
-            tmem_wait_ld(v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) accum = fmaf(wg[hc + j], fmaxf(v[j], 0.f), accum);
-          }
+      for (int i = 0; i < kMaxRowsPerWarp; ++i) {
+        const int gh = warp - 1 + 5 * i;
+        raw[i] = make_uint2(0u, 0u);
+        if (gh < G * HI) {
+          const int g = gh / HI, h = gh - g * HI;
+          if (g0 + g < T) raw[i] = *reinterpret_cast<const uint2*>(qI + ((qrow0 + g) * HI + h) * 128 + lane * 4);
         }
-        res[g] = accum;
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      float ksc = 1.f;
-      if constexpr (FP8) {
-        if (s < a.E_cap) ksc = a.kscale[static_cast<int64_t>(b) * a.E_cap + s];
+#pragma unroll
+      for (int i = 0; i < kMaxRowsPerWarp; ++i) {
+        const int gh = warp - 1 + 5 * i;
+        if (gh >= G * HI) break;
+        const int g = gh / HI, h = gh - g * HI;
+        const bool valid = g0 + g < T;
+        float x[4];
+        {
+          const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].x);
+          const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].y);
+          x[0] = __low2float(p0);
+          x[1] = __high2float(p0);
+          x[2] = __low2float(p1);
+          x[3] = __high2float(p1);
+        }
+        float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const float sc = am > 0.f ? am / 448.f : 1.f;
+        const float inv = 1.f / sc;
+        uint32_t hi4 = 0u, lo4 = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float y = x[j] * inv;
+          const uint8_t ch = f_to_e4m3(y);
+          const uint8_t cl = f_to_e4m3((y - e4m3_to_f(ch)) * 16.f);
+          hi4 |= static_cast<uint32_t>(ch) << (8 * j);
+          lo4 |= static_cast<uint32_t>(cl) << (8 * j);
+        }
+        const int n_hi = g * 2 * HI + h, n_lo = n_hi + HI;
+        *reinterpret_cast<uint32_t*>(sB + sw128(n_hi, lane >> 2) + (lane & 3) * 4) = hi4;
+        *reinterpret_cast<uint32_t*>(sB + sw128(n_lo, lane >> 2) + (lane & 3) * 4) = lo4;
+        if (lane == 0) sW[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
       }
-      if (s < n_cols) {
+    }
+    fence_proxy_async_smem();
+    named_sync(1, nthr);
+
+    if (warp == 1) {
+      if (lane == 0 && n_it > 0) {
+        const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
+        const uint32_t bBase = smem_u32(sB);
+        int committed = 0;
+        for (int it = 0; it < n_it; ++it) {
+          const int st = it % S, acc = it & 1;
+          if (!mbar_wait(&full[st], (it / S) & 1, a.err, sAbort)) break;
+          if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, a.err, sAbort)) break;
+          tc_fence_after();
+          const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
+          const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
+          if constexpr (FP8) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_f8(d, smem_desc(aBase + ks * 32, 16, 1024), smem_desc(bBase + ks * 32, 16, 1024), idesc, ks > 0);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
+              const uint32_t boff = (ks >> 2) * static_cast<uint32_t>(N * 128) + (ks & 3) * 32u;
+              mma_bf16(d, smem_desc(aBase + off, 16, 1024), smem_desc(bBase + boff, 16, 1024), idesc, ks > 0);
+            }
+          }
+          mma_commit(&empty[st]);
+          mma_commit(&tfull[acc]);
+          ++committed;
+        }
+        if (committed > 0) wait_time_only(&tfull[(committed - 1) & 1], ((committed - 1) >> 1) & 1);
+      }
+    } else {
+      const int q = warp & 3;  // TMEM lane quadrant of this warp
+      const int rin = q * 32 + lane;
+      const int hstride = FP8 ? 2 * HI : HI;
+      // per-key fp32 scales (e4m3 keys), prefetched two tiles ahead with coalesced loads
+      const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
+      auto scale_of = [&](int itx) -> float {
+        const int64_t sx = static_cast<int64_t>(tile_lo + itx) * kTile + rin;
+        return (FP8 && itx < n_it && sx < a.E_cap) ? kscale_b[sx] : 1.f;
+      };
+      float ks0 = scale_of(0), ks1 = scale_of(1);
+      for (int it = 0; it < n_it; ++it) {
+        const int acc = it & 1;
+        const float ksc = ks0;
+        ks0 = ks1;
+        ks1 = scale_of(it + 2);
+        if (!mbar_wait(&tfull[acc], (it >> 1) & 1, a.err, sAbort)) break;
+        tc_fence_after();
+        const int64_t s = static_cast<int64_t>(tile_lo + it) * kTile + rin;
+        float res[kMaxG];
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
 #pragma unroll
         for (int g = 0; g < kMaxG; ++g) {
-          if (g >= G || g0 + g >= T) continue;
-          a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? res[g] * ksc : -INFINITY;
+          res[g] = 0.f;
+          if (g >= G) continue;
+          const float* wg = sW + g * HI;
+          float acc0 = 0.f, acc1 = 0.f;
+          for (int hc = 0; hc < HI; hc += 32) {
+            float v[32];
+            tmem_ld32(lane_base + g * hstride + hc, v);
+            if constexpr (FP8) {
+              float u[32];
+              tmem_ld32(lane_base + g * hstride + HI + hc, u);
+              tmem_wait_ld(v);
+              tmem_wait_ld(u);
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                acc0 = fmaf(wg[hc + j], fmaxf(fmaf(u[j], 0.0625f, v[j]), 0.f), acc0);
+                acc1 = fmaf(wg[hc + j + 1], fmaxf(fmaf(u[j + 1], 0.0625f, v[j + 1]), 0.f), acc1);
+              }
+            } else {
+              tmem_wait_ld(v);
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                acc0 = fmaf(wg[hc + j], fmaxf(v[j], 0.f), acc0);
+                acc1 = fmaf(wg[hc + j + 1], fmaxf(v[j + 1], 0.f), acc1);
+              }
+            }
+          }
+          res[g] = acc0 + acc1;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        if (s < n_cols) {
+#pragma unroll
+          for (int g = 0; g < kMaxG; ++g) {
+            if (g >= G || g0 + g >= T) continue;
+            const float sc = res[g] * ksc;
+            a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
+            if (hist && s < sNv[0]) atomicAdd(&sHist[f2key(sc) >> 20], 1u);
+          }
+        }
+      }
+      if (hist) {
+        named_sync(2, 128);
+        for (int i = tid - 64; i < kTopkHistBins; i += 128) {
+          const uint32_t c = sHist[i];
+          if (c) atomicAdd(&a.hist_out[qrow0 * kTopkHistBins + i], c);
         }
       }
     }
@@ -331,13 +381,15 @@ TcLayout plan_tc(const IndexerArgs& a) {
   L.G = std::max(1, std::min({256 / per_q, a.T, kMaxG}));
   L.N = L.G * per_q;
   L.b_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * (fp8 ? 128 : 256), 1024));
-  L.stage_bytes = fp8 ? 16384u : 32768u;
+  L.stage_bytes = fp8 ? kKeyTileBytesF8 : 32768u;
+  L.stage_tx = L.stage_bytes;
   L.n_qgroups = (a.T + L.G - 1) / L.G;
   const int tiles = static_cast<int>((a.E_cap + kTile - 1) / kTile);
   const int64_t groups = static_cast<int64_t>(a.B) * L.n_qgroups;
   // few long rows (decode): two CTAs per SM, key range split over them
   const bool decode_like = groups < a.num_sms;
-  const size_t misc = 1024 + static_cast<size_t>(L.G) * a.HI * 4 + 64 + 16 * 16 + 64;
+  const size_t misc = 1024 + static_cast<size_t>(L.G) * a.HI * 4 + 64 + 16 * 16 + 64 +
+                      (a.hist_out && L.G == 1 ? kTopkHistBins * 4 : 0);
   const size_t budget = decode_like ? (113 * 1024) : (227 * 1024);
   int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
   S = std::max(2, std::min(S, 8));
@@ -370,6 +422,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
     const bool fp8 = a.kidx == CSA_E4M3;
     const TcLayout L = plan_tc(a);
     CUtensorMap map;
+    // rows of 128 keys; the innermost coordinate of every load is 0 or 64 (16-byte aligned)
     if (!encode_tmap_2d(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         const_cast<void*>(a.kI), 128, static_cast<uint64_t>(a.B) * a.E_cap, fp8 ? 128 : 256,
                         fp8 ? 128 : 64, kTile))

@@ -55,6 +55,28 @@ def assert_rows_close(got: np.ndarray, ref: np.ndarray, rtol: float, atol: float
     return worst
 
 
+def swap_bound(q, lse, scale, rows_in, rows_out):
+    """First-order change of the attention output when rows_out leave the selection and rows_in
+    join it: sum over those rows of weight_h(row) * |row|, with weight_h = exp(scale q_h.r - lse_h)."""
+    q = np.asarray(q, np.float64)
+    bound = np.zeros_like(q)
+    for r in list(rows_in) + list(rows_out):
+        r = np.asarray(r, np.float64)
+        w = np.exp(scale * (q @ r) - lse)            # [H]
+        bound += w[:, None] * np.abs(r)[None, :]
+    return bound
+
+
+def assert_out_close_with_swaps(got, ref, rtol, bound, what="out"):
+    """|g - r| <= rtol * max|r_row| + 1.5 * (swap bound); the bound is 0 without swaps."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    tol = rtol * np.abs(ref).max(axis=-1, keepdims=True) + 1.5 * bound
+    worst = float((np.abs(got - ref) / np.maximum(tol, 1e-300)).max())
+    assert worst <= 1.0, f"{what}: worst error is {worst:.3f} x tolerance"
+    return worst
+
+
 def assert_selection_ok(got_idx, ref_idx, ref_scores: np.ndarray, k: int, score_tol: float):
     """The selections agree except for swaps at near-ties: every entry only one side kept has an
     oracle score within score_tol of the oracle's k-th score."""
