@@ -125,7 +125,7 @@ size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   size_t bytes = align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
   bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
-  bytes += align_up(static_cast<size_t>(B) * (kTopkHistBins + 1) * 4, 256);  // histograms + counters
+  bytes += align_up(static_cast<size_t>(B) * (kTopkHistRowWords + 1) * 4, 256);  // histograms + counters
   bytes += align_up(std::max(topk_workspace_bytes(B, E_cap, c->k, sms), topk_hist_workspace_bytes(B, c->k)), 256);
   bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms), 256);
   return bytes;
@@ -404,7 +404,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   int32_t* idx = reinterpret_cast<int32_t*>(p);
   p += align_up(static_cast<size_t>(cfg->B) * cfg->k * 4, 256);
   uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(p);
-  p += align_up(static_cast<size_t>(cfg->B) * (kTopkHistBins + 1) * 4, 256);
+  p += align_up(static_cast<size_t>(cfg->B) * (kTopkHistRowWords + 1) * 4, 256);
   const size_t topk_ws =
       std::max(topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms), topk_hist_workspace_bytes(cfg->B, cfg->k));
   void* ws_topk = p;

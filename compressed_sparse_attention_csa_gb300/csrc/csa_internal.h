@@ -75,9 +75,12 @@ struct TopkArgs {
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 
-// Histogram-guided top-k for a few long rows.  hist_cnt holds rows x 4096 digit counts
-// followed by rows candidate counters, all zero before the indexer fills the histogram.
+// Histogram-guided top-k for a few long rows.  hist_cnt holds, per row, 4096 fine digit
+// counts (key >> 20) and 64 coarse counts (key >> 26), then one candidate counter per row;
+// all zero before the histogram is filled.
 constexpr int kTopkHistBins = 4096;
+constexpr int kTopkHistCoarse = 64;
+constexpr int kTopkHistRowWords = kTopkHistBins + kTopkHistCoarse;
 int topk_hist_cap(int k);
 size_t topk_hist_workspace_bytes(int64_t rows, int k);  // the candidate lists (ws_cand)
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);

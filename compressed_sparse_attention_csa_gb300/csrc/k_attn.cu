@@ -447,9 +447,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[(hc + e) * kD] = __float2bfloat16_rn(v[e] * s_f[hc + e]);
         } else {
-          float* o = sp.part_o + ((r * sp.n_split + split) * kH) * kD + dd;
+          // partials are stored [dim][head]: this thread's 32 heads are contiguous
+          float4* o = reinterpret_cast<float4*>(sp.part_o + ((r * sp.n_split + split) * kD + dd) * kH + hc);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[(hc + e) * kD] = v[e];
+          for (int e = 0; e < 32; e += 4) o[e / 4] = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
       }
     }
@@ -465,52 +466,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
   }
 }
 
-// Fixed-order merge of the split partials with the sink.  One CTA per (row, 4 heads); each
-// thread owns 4 consecutive dims of one head and issues all its partial loads at once.
+// Fixed-order merge of the split partials with the sink.  One CTA per (row, 4 heads), one
+// thread per output dim; partials are [split][dim][head], so each thread reads one float4
+// (its 4 heads) per split.
 constexpr int kMergeHeads = 4;
 constexpr int kMaxSplit = 16;
-__global__ void __launch_bounds__(kMergeHeads * kD / 4) attn_merge_kernel(const AttnArgs a, const TcAttnSplit sp) {
+__global__ void __launch_bounds__(kD) attn_merge_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  __shared__ float s_f[kMaxSplit][kMergeHeads];  // per split, per head: 2^(m_s - M) / den
+  __shared__ float s_inv[kMergeHeads];
   const int64_t r = blockIdx.x;
-  const int h = blockIdx.y * kMergeHeads + threadIdx.x / (kD / 4);
-  const int d4 = threadIdx.x % (kD / 4);
+  const int h0 = blockIdx.y * kMergeHeads;
+  const int dd = threadIdx.x;
   const int ns = sp.n_split;
   const float* ml = sp.part_ml + r * ns * 2 * kH;
-  const float* po = sp.part_o + r * ns * kH * kD;
-  const float sk = a.sink[h] * kLog2e;
-  float ms[kMaxSplit], ls[kMaxSplit];
+  const float* po = sp.part_o + r * ns * kD * kH;
+  if (threadIdx.x < kMergeHeads) {
+    const int h = h0 + threadIdx.x;
+    const float sk = a.sink[h] * kLog2e;
+    float M = sk;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * 2 * kH + h]);
+    float den = exp2f(sk - M);
+    for (int s = 0; s < ns; ++s) {
+      const float ms = ml[s * 2 * kH + h];
+      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      den = fmaf(ml[s * 2 * kH + kH + h], f, den);
+      s_f[s][threadIdx.x] = f;
+    }
+    s_inv[threadIdx.x] = 1.f / den;
+    if (a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+  }
+  __syncthreads();
   float4 o[kMaxSplit];
-  float M = sk;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s)
+    if (s < ns) o[s] = *reinterpret_cast<const float4*>(po + (static_cast<int64_t>(s) * kD + dd) * kH + h0);
+  float acc[kMergeHeads] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < ns) {
-      ms[s] = ml[s * 2 * kH + h];
-      ls[s] = ml[s * 2 * kH + kH + h];
-      o[s] = *reinterpret_cast<const float4*>(po + (static_cast<int64_t>(s) * kH + h) * kD + 4 * d4);
-      M = fmaxf(M, ms[s]);
+    if (s < ns && s_f[s][0] + s_f[s][1] + s_f[s][2] + s_f[s][3] > 0.f) {
+      acc[0] = fmaf(o[s].x, s_f[s][0], acc[0]);
+      acc[1] = fmaf(o[s].y, s_f[s][1], acc[1]);
+      acc[2] = fmaf(o[s].z, s_f[s][2], acc[2]);
+      acc[3] = fmaf(o[s].w, s_f[s][3], acc[3]);
     }
   }
-  float den = exp2f(sk - M);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (r * kH + h0) * kD + dd;
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < ns && ms[s] != -INFINITY) {
-      const float f = exp2f(ms[s] - M);
-      den = fmaf(ls[s], f, den);
-      acc.x = fmaf(o[s].x, f, acc.x);
-      acc.y = fmaf(o[s].y, f, acc.y);
-      acc.z = fmaf(o[s].z, f, acc.z);
-      acc.w = fmaf(o[s].w, f, acc.w);
-    }
-  }
-  const float inv = 1.f / den;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (r * kH + h) * kD + 4 * d4;
-  const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 pk;
-  pk.x = *reinterpret_cast<const uint32_t*>(&p0);
-  pk.y = *reinterpret_cast<const uint32_t*>(&p1);
-  *reinterpret_cast<uint2*>(out) = pk;
-  if (d4 == 0 && a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+  for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j] * s_inv[j]);
 }
 
 bool attn_uses_tensor_cores(int act, int H, int d, int k) {
@@ -567,7 +569,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || sp.n_split == 1) return e;
-    attn_merge_kernel<<<dim3(static_cast<unsigned>(rows), kH / kMergeHeads), kMergeHeads * kD / 4, 0, s>>>(a, sp);
+    attn_merge_kernel<<<dim3(static_cast<unsigned>(rows), kH / kMergeHeads), kD, 0, s>>>(a, sp);
     count_launches(1);
     return cudaGetLastError();
   }

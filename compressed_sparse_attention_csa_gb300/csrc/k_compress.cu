@@ -25,8 +25,9 @@ __global__ void __launch_bounds__(512) compress_kernel(CompressArgs a) {
   const int b = blockIdx.y;
   const int m = a.m;
   if (a.zero_hist && blockIdx.x == 0 && blockIdx.z == 0) {
-    for (int i = threadIdx.x; i < kTopkHistBins; i += blockDim.x) a.zero_hist[b * kTopkHistBins + i] = 0u;
-    if (threadIdx.x == 0) a.zero_hist[static_cast<int64_t>(a.B) * kTopkHistBins + b] = 0u;
+    for (int i = threadIdx.x; i < kTopkHistRowWords; i += blockDim.x)
+      a.zero_hist[static_cast<int64_t>(b) * kTopkHistRowWords + i] = 0u;
+    if (threadIdx.x == 0) a.zero_hist[static_cast<int64_t>(a.B) * kTopkHistRowWords + b] = 0u;
   }
   int64_t entry, tok0, n_tok;
   if (a.q_pos) {

@@ -10,11 +10,14 @@
 // with the KEYS as the M dimension: D[s, (g, h)] = kI[s] . qI[g, h] for a 128-key tile and
 // the G*HI query-heads of a query group as N.  Each TMEM lane then holds one key's scores
 // for every head, so ReLU, the gate weights and the sum over heads are thread-local in the
-// epilogue.  Key tiles stream through a TMA ring (evict-first), the MMA is issued by one
-// thread into two TMEM accumulators so that the epilogue of tile i overlaps the MMA of
-// tile i+1.  E4M3 keys use kind::f8f6f4 with qI split into two E4M3 terms,
-// q/s ~= hi + lo/16 (s = per-head amax/448), which keeps the score error near bf16 level;
-// the per-key fp32 scale and the per-head s are positive and factor out of the ReLU.
+// epilogue.  Key tiles stream through a TMA ring (evict-first); one thread issues the MMAs
+// into two TMEM accumulators so that the epilogue of tile i overlaps the MMA of tile i+1.
+// Eight epilogue warps, two per TMEM lane quadrant, each reduce half of the heads.
+//
+// E4M3 keys use kind::f8f6f4.  The query is split into two E4M3 terms, q/s = hi + lo with
+// s = per-head amax/448, and both terms run through the same accumulator (the K loop is
+// issued twice, with the same key tile), so D = k . (hi + lo) to about bf16 accuracy.  The
+// per-key fp32 scale and the per-head s are positive and factor out of the ReLU.
 #include <algorithm>
 
 #include "csa_internal.h"
@@ -69,24 +72,23 @@ __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_
 }
 
 // ------------------------------------------------------------------ tensor-core path
-constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
-constexpr int kTile = 128;       // keys per tile (MMA M)
+constexpr int kEpiWarps = 8;
+constexpr int kTcThreads = 64 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
+constexpr int kTile = 128;                       // keys per tile (MMA M)
 constexpr int kMaxG = 8;
+constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
 
 struct TcLayout {
   int G;               // queries per CTA
-  int N;               // MMA N = G * HI (bf16) or G * 2 * HI (e4m3 hi/lo)
+  int N;               // MMA N = G * HI
   int stages;
-  uint32_t b_bytes;    // B operand (queries), 1024-aligned
-  uint32_t stage_bytes;  // stride between ring stages (1024-aligned)
-  uint32_t stage_tx;     // bytes the TMA delivers per stage (keys, + scales for e4m3)
+  uint32_t b_bytes;    // B operand (queries; hi and lo regions for e4m3), 1024-aligned
+  uint32_t stage_bytes;
   uint32_t smem_bytes;
   uint32_t tmem_cols;
   int n_splits;        // key-range splits per (sequence, query group)
   int n_qgroups;
 };
-
-constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
 
 __device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -99,10 +101,23 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Warp 0: TMA producer (starts streaming key tiles at once).  Warps 1..5 stage the query
-// operand, then warp 1 issues the MMAs and warps 2..5 run the epilogue.
+// sum_j w[j] * relu(v[j]) over 32 values, four independent chains
+__device__ __forceinline__ float relu_dot32(const float (&v)[32], const float* w) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    a0 = fmaf(w[j], fmaxf(v[j], 0.f), a0);
+    a1 = fmaf(w[j + 1], fmaxf(v[j + 1], 0.f), a1);
+    a2 = fmaf(w[j + 2], fmaxf(v[j + 2], 0.f), a2);
+    a3 = fmaf(w[j + 3], fmaxf(v[j + 3], 0.f), a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+// Warp 0: TMA producer (starts streaming key tiles at once).  Warps 1..9 stage the query
+// operand; then warp 1 issues the MMAs and warps 2..9 run the epilogue.
 template <bool FP8>
-__global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const IndexerArgs a, const TcLayout L,
                                                                 const int64_t n_cols) {
   extern __shared__ uint8_t smem_raw[];
@@ -110,14 +125,17 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
   const int HI = a.HI, G = L.G, N = L.N, S = L.stages;
   uint8_t* sB = smem;
   uint8_t* sA = smem + L.b_bytes;
-  float* sW = reinterpret_cast<float*>(sA + static_cast<size_t>(S) * L.stage_bytes);
-  int* sNv = reinterpret_cast<int*>(sW + G * HI);
+  float* sW = reinterpret_cast<float*>(sA + static_cast<size_t>(S) * L.stage_bytes);  // [G][HI]
+  float* sPart = sW + G * HI;                                                           // [2][G][128]
+  int* sNv = reinterpret_cast<int*>(sPart + 2 * G * kTile);
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sNv + kMaxG) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = bars + 2 * S + 2;
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  uint64_t* pfull = bars + 2 * S + 4;   // [4 quadrants][2 slots]: second half's partials ready
+  uint64_t* pempty = bars + 2 * S + 12; // [4][2]: first half has read the slot
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 20);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(sTmem + 4);  // [4096] when a.hist_out (G == 1)
   const bool hist = a.hist_out != nullptr && G == 1;
@@ -147,7 +165,11 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], 32 * kEpiWarps);
+    }
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(&pfull[i], 32);
+      mbar_init(&pempty[i], 32);
     }
     fence_mbar_init();
   }
@@ -175,10 +197,11 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
       for (int it = 0; it < n_it; ++it) {
         const int st = it % S;
         if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) break;
-        mbar_arrive_expect_tx(&full[st], L.stage_tx);
+        mbar_arrive_expect_tx(&full[st], L.stage_bytes);
         const int64_t row64 = static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it) * kTile;
         const int row = static_cast<int>(row64);
         uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
+        // innermost coordinate 0 or 64 elements: always 16-byte aligned
         tma_load_2d_hint(dst, &kmap, &full[st], 0, row, pol);
         if constexpr (!FP8) tma_load_2d_hint(dst + 16384, &kmap, &full[st], 64, row, pol);
         ++issued;
@@ -196,7 +219,7 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
     }
   } else {
     // ---- stage the B operand (the group's query heads), 128B-swizzled K-major
-    const int t2 = tid - 32, nthr = kTcThreads - 32;
+    const int t2 = tid - 32, nthr = kTcThreads - 32, nwarps = nthr / 32;
     if constexpr (!FP8) {
       const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
       const int n_chunks = N * 16;  // 256 bytes per row = 16 chunks of 16 B
@@ -212,13 +235,16 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
         sW[i] = (g0 + g < T) ? a.w[(qrow0 + g) * HI + (i - g * HI)] : 0.f;
       }
     } else {
+      // one warp per query row: amax, scale s, hi = e4m3(q/s), lo = e4m3(q/s - hi); all of a
+      // warp's rows are loaded first (one round trip), then quantised
       const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-      // all of this warp's query rows are loaded first (one round trip), then quantised
-      constexpr int kMaxRowsPerWarp = (256 / 2 + 4) / 5;  // G*HI <= 128 rows over 5 warps
-      uint2 raw[kMaxRowsPerWarp];
+      constexpr int kBatch = 8;  // rows loaded per round trip
+      const int wq = warp - 1;
+      for (int i0 = 0; wq + nwarps * i0 < G * HI; i0 += kBatch) {
+      uint2 raw[kBatch];
 #pragma unroll
-      for (int i = 0; i < kMaxRowsPerWarp; ++i) {
-        const int gh = warp - 1 + 5 * i;
+      for (int i = 0; i < kBatch; ++i) {
+        const int gh = wq + nwarps * (i0 + i);
         raw[i] = make_uint2(0u, 0u);
         if (gh < G * HI) {
           const int g = gh / HI, h = gh - g * HI;
@@ -226,8 +252,8 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
         }
       }
 #pragma unroll
-      for (int i = 0; i < kMaxRowsPerWarp; ++i) {
-        const int gh = warp - 1 + 5 * i;
+      for (int i = 0; i < kBatch; ++i) {
+        const int gh = wq + nwarps * (i0 + i);
         if (gh >= G * HI) break;
         const int g = gh / HI, h = gh - g * HI;
         const bool valid = g0 + g < T;
@@ -250,14 +276,15 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
         for (int j = 0; j < 4; ++j) {
           const float y = x[j] * inv;
           const uint8_t ch = f_to_e4m3(y);
-          const uint8_t cl = f_to_e4m3((y - e4m3_to_f(ch)) * 16.f);
+          const uint8_t cl = f_to_e4m3(y - e4m3_to_f(ch));
           hi4 |= static_cast<uint32_t>(ch) << (8 * j);
           lo4 |= static_cast<uint32_t>(cl) << (8 * j);
         }
-        const int n_hi = g * 2 * HI + h, n_lo = n_hi + HI;
-        *reinterpret_cast<uint32_t*>(sB + sw128(n_hi, lane >> 2) + (lane & 3) * 4) = hi4;
-        *reinterpret_cast<uint32_t*>(sB + sw128(n_lo, lane >> 2) + (lane & 3) * 4) = lo4;
+        const uint32_t off = sw128(gh, lane >> 2) + (lane & 3) * 4;
+        *reinterpret_cast<uint32_t*>(sB + off) = hi4;
+        *reinterpret_cast<uint32_t*>(sB + N * 128 + off) = lo4;
         if (lane == 0) sW[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
+      }
       }
     }
     fence_proxy_async_smem();
@@ -276,9 +303,13 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
           const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
           const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
           if constexpr (FP8) {
+            // D = k . hi (+)= k . lo: the same key descriptors against both query terms
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_f8(d, smem_desc(aBase + ks * 32, 16, 1024), smem_desc(bBase + ks * 32, 16, 1024), idesc, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t koff = (ks & 3) * 32u;
+              const uint32_t boff = (ks >> 2) * static_cast<uint32_t>(N * 128) + koff;
+              mma_f8(d, smem_desc(aBase + koff, 16, 1024), smem_desc(bBase + boff, 16, 1024), idesc, ks > 0);
+            }
           } else {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -294,16 +325,26 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
         if (committed > 0) wait_time_only(&tfull[(committed - 1) & 1], ((committed - 1) >> 1) & 1);
       }
     } else {
-      const int q = warp & 3;  // TMEM lane quadrant of this warp
+      // ---- epilogue: warp pair (e, e+4) shares TMEM lane quadrant q; `half` picks the heads
+      const int e = warp - 2;
+      const int q = warp & 3;
+      const int half = e >> 2;
+      const int hh = HI / 2;        // heads per warp (HI = 32, 64 or 128: 16, 32, 64)
+      const int h0 = half * hh;
       const int rin = q * 32 + lane;
-      const int hstride = FP8 ? 2 * HI : HI;
-      // per-key fp32 scales (e4m3 keys), prefetched two tiles ahead with coalesced loads
+      const int hb = hh == 16 ? 0 : h0;  // first head of the 32 columns this warp loads
+      // gates of those 32 heads for the single-query layout stay in registers
+      float wreg[32];
+      if (G == 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) wreg[j] = sW[hb + j];
+      }
       const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
       auto scale_of = [&](int itx) -> float {
         const int64_t sx = static_cast<int64_t>(tile_lo + itx) * kTile + rin;
         return (FP8 && itx < n_it && sx < a.E_cap) ? kscale_b[sx] : 1.f;
       };
-      float ks0 = scale_of(0), ks1 = scale_of(1);
+      float ks0 = scale_of(0), ks1 = scale_of(1);  // e4m3 key scales, prefetched two tiles ahead
       for (int it = 0; it < n_it; ++it) {
         const int acc = it & 1;
         const float ksc = ks0;
@@ -312,55 +353,73 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
         if (!mbar_wait(&tfull[acc], (it >> 1) & 1, a.err, sAbort)) break;
         tc_fence_after();
         const int64_t s = static_cast<int64_t>(tile_lo + it) * kTile + rin;
-        float res[kMaxG];
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
+        float part[kMaxG];
 #pragma unroll
         for (int g = 0; g < kMaxG; ++g) {
-          res[g] = 0.f;
+          part[g] = 0.f;
           if (g >= G) continue;
-          const float* wg = sW + g * HI;
-          float acc0 = 0.f, acc1 = 0.f;
-          for (int hc = 0; hc < HI; hc += 32) {
-            float v[32];
-            tmem_ld32(lane_base + g * hstride + hc, v);
-            if constexpr (FP8) {
-              float u[32];
-              tmem_ld32(lane_base + g * hstride + HI + hc, u);
-              tmem_wait_ld(v);
-              tmem_wait_ld(u);
+          float v[32];
+          // first 32 columns of this warp's heads; with 16 heads per warp (HI = 32) both
+          // warps of the pair load heads 0..31 and each zeroes the other warp's 16
+          tmem_ld32(lane_base + g * HI + hb, v);
+          tmem_wait_ld(v);
+          if (hh == 16) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                acc0 = fmaf(wg[hc + j], fmaxf(fmaf(u[j], 0.0625f, v[j]), 0.f), acc0);
-                acc1 = fmaf(wg[hc + j + 1], fmaxf(fmaf(u[j + 1], 0.0625f, v[j + 1]), 0.f), acc1);
-              }
-            } else {
-              tmem_wait_ld(v);
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                acc0 = fmaf(wg[hc + j], fmaxf(v[j], 0.f), acc0);
-                acc1 = fmaf(wg[hc + j + 1], fmaxf(v[j + 1], 0.f), acc1);
-              }
+            for (int j = 0; j < 16; ++j) {
+              v[j] = half ? 0.f : v[j];
+              v[j + 16] = half ? v[j + 16] : 0.f;
             }
           }
-          res[g] = acc0 + acc1;
+          // gates: registers for one query, shared memory otherwise
+          part[g] = (G == 1) ? relu_dot32(v, wreg) : relu_dot32(v, sW + g * HI + hb);
+          if (hh == 64) {  // 128 indexer heads: a second group of 32 columns
+            tmem_ld32(lane_base + g * HI + h0 + 32, v);
+            tmem_wait_ld(v);
+            part[g] += relu_dot32(v, sW + g * HI + h0 + 32);
+          }
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
-        if (s < n_cols) {
+        // combine the two halves of every key through a double-buffered smem slot
+        const int slot_i = it & 1;
+        const uint32_t pph = (it >> 1) & 1;
+        float* slot = sPart + slot_i * G * kTile;
+        bool ok = true;
+        if (half) {
+          ok = mbar_wait(&pempty[q * 2 + slot_i], pph ^ 1, a.err, sAbort);
+#pragma unroll
+          for (int g = 0; g < kMaxG; ++g)
+            if (g < G) slot[g * kTile + rin] = part[g];
+          mbar_arrive(&pfull[q * 2 + slot_i]);
+          if (!ok) break;
+          continue;
+        }
+        ok = mbar_wait(&pfull[q * 2 + slot_i], pph, a.err, sAbort);
+        if (ok && s < n_cols) {
 #pragma unroll
           for (int g = 0; g < kMaxG; ++g) {
             if (g >= G || g0 + g >= T) continue;
-            const float sc = res[g] * ksc;
+            const float sc = (part[g] + slot[g * kTile + rin]) * ksc;
             a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
             if (hist && s < sNv[0]) atomicAdd(&sHist[f2key(sc) >> 20], 1u);
           }
         }
+        mbar_arrive(&pempty[q * 2 + slot_i]);
+        if (!ok) break;
       }
       if (hist) {
-        named_sync(2, 128);
-        for (int i = tid - 64; i < kTopkHistBins; i += 128) {
+        named_sync(6, 32 * kEpiWarps);
+        uint32_t* rh = a.hist_out + qrow0 * kTopkHistRowWords;
+        for (int i = tid - 64; i < kTopkHistBins; i += 32 * kEpiWarps) {
           const uint32_t c = sHist[i];
-          if (c) atomicAdd(&a.hist_out[qrow0 * kTopkHistBins + i], c);
+          if (c) atomicAdd(&rh[i], c);
+        }
+        if (tid - 64 < kTopkHistCoarse) {
+          const int cb = tid - 64;
+          uint32_t c = 0;
+          for (int j = 0; j < kTopkHistBins / kTopkHistCoarse; ++j) c += sHist[cb * (kTopkHistBins / kTopkHistCoarse) + j];
+          if (c) atomicAdd(&rh[kTopkHistBins + cb], c);
         }
       }
     }
@@ -377,18 +436,16 @@ __global__ void __launch_bounds__(kTcThreads) indexer_tc_kernel(const __grid_con
 TcLayout plan_tc(const IndexerArgs& a) {
   TcLayout L{};
   const bool fp8 = a.kidx == CSA_E4M3;
-  const int per_q = a.HI * (fp8 ? 2 : 1);
-  L.G = std::max(1, std::min({256 / per_q, a.T, kMaxG}));
-  L.N = L.G * per_q;
-  L.b_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * (fp8 ? 128 : 256), 1024));
+  L.G = std::max(1, std::min({256 / a.HI, a.T, kMaxG}));
+  L.N = L.G * a.HI;
+  L.b_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * 256, 1024));  // bf16 rows or hi+lo
   L.stage_bytes = fp8 ? kKeyTileBytesF8 : 32768u;
-  L.stage_tx = L.stage_bytes;
   L.n_qgroups = (a.T + L.G - 1) / L.G;
   const int tiles = static_cast<int>((a.E_cap + kTile - 1) / kTile);
   const int64_t groups = static_cast<int64_t>(a.B) * L.n_qgroups;
   // few long rows (decode): two CTAs per SM, key range split over them
   const bool decode_like = groups < a.num_sms;
-  const size_t misc = 1024 + static_cast<size_t>(L.G) * a.HI * 4 + 64 + 16 * 16 + 64 +
+  const size_t misc = 1024 + static_cast<size_t>(L.G) * a.HI * 4 + 2 * L.G * kTile * 4 + 64 + 40 * 8 + 64 +
                       (a.hist_out && L.G == 1 ? kTopkHistBins * 4 : 0);
   const size_t budget = decode_like ? (113 * 1024) : (227 * 1024);
   int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
@@ -410,7 +467,7 @@ TcLayout plan_tc(const IndexerArgs& a) {
 }  // namespace
 
 bool indexer_uses_tensor_cores(const IndexerArgs& a) {
-  return a.cand == nullptr && a.act == CSA_BF16 && a.dI == 128 && a.HI % 16 == 0 && a.HI <= 128 &&
+  return a.cand == nullptr && a.act == CSA_BF16 && a.dI == 128 && (a.HI == 32 || a.HI == 64 || a.HI == 128) &&
          (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
 }
 
@@ -422,7 +479,6 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
     const bool fp8 = a.kidx == CSA_E4M3;
     const TcLayout L = plan_tc(a);
     CUtensorMap map;
-    // rows of 128 keys; the innermost coordinate of every load is 0 or 64 (16-byte aligned)
     if (!encode_tmap_2d(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         const_cast<void*>(a.kI), 128, static_cast<uint64_t>(a.B) * a.E_cap, fp8 ? 128 : 256,
                         fp8 ? 128 : 64, kTile))

@@ -421,305 +421,3 @@ cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s) {
 
 }  // namespace csa
 
-// ====================================================================================
-// Histogram-guided top-k for a few long rows (the decode step).
-//
-// The indexer epilogue adds every visible score of row r to hist[r][key >> 20] (12-bit
-// digit of the order-preserving key).  From that histogram the threshold digit b1 is the
-// largest digit whose suffix count reaches k, so the k best scores all have digit >= b1.
-// topk_filter_kernel (wide grid) appends every score with digit >= b1 to a per-row
-// candidate list (typically ~k plus one histogram bin); topk_final_kernel (one CTA per row)
-// selects exactly among the candidates under (score desc, position asc) and writes the
-// chosen positions in ascending order.  If the candidate list overflows its capacity (a
-// row full of ties) the final kernel selects over the whole row in global memory instead.
-// ====================================================================================
-namespace csa {
-namespace {
-
-constexpr int kHist12 = 4096;
-
-__device__ __forceinline__ uint32_t row_threshold_digit(const uint32_t* hist, int k, uint32_t* tmp, uint32_t* s_res) {
-  // largest digit b with sum_{b' >= b} hist[b'] >= k; 0 when the row holds fewer than k scores
-  const int tid = threadIdx.x;
-  constexpr int bpt = kHist12 / NT;  // 8
-  uint32_t local = 0;
-  for (int q = 0; q < bpt; ++q) local += hist[tid * bpt + q];
-  uint32_t tot;
-  const uint32_t excl = block_exclusive_scan<NT>(local, tmp, &tot);
-  if (tid == 0) s_res[0] = 0u;
-  __syncthreads();
-  uint32_t run = tot - excl - local;
-  for (int q = bpt - 1; q >= 0; --q) {
-    const uint32_t h = hist[tid * bpt + q];
-    if (run < static_cast<uint32_t>(k) && run + h >= static_cast<uint32_t>(k)) s_res[0] = tid * bpt + q;
-    run += h;
-  }
-  __syncthreads();
-  return s_res[0];
-}
-
-__device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int64_t row, int64_t n_cols) {
-  if (!n_valid) return n_cols;
-  const int64_t v = n_valid[row];
-  return v < 0 ? 0 : (v < n_cols ? v : n_cols);
-}
-
-// Digit histogram of each row's valid scores (standalone csa_topk; the decode step gets it
-// from the indexer epilogue instead).
-__global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                             int64_t n_cols, uint32_t* hist, int chunk) {
-  __shared__ uint32_t h[kHist12];
-  for (int i = threadIdx.x; i < kHist12; i += NT) h[i] = 0u;
-  __syncthreads();
-  const int64_t row = blockIdx.y;
-  const int64_t nv = row_valid(n_valid, row, n_cols);
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
-  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
-  for (int64_t s = c0 + threadIdx.x; s < c1; s += NT) atomicAdd(&h[f2key(scores[row * ld + s]) >> 20], 1u);
-  __syncthreads();
-  for (int i = threadIdx.x; i < kHist12; i += NT)
-    if (h[i]) atomicAdd(&hist[row * kHist12 + i], h[i]);
-}
-
-__global__ void __launch_bounds__(NT) topk_filter_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                         int64_t n_cols, const uint32_t* hist, int k, uint32_t* cnt,
-                                                         uint32_t* ckey, int32_t* cpos, int cap, int chunk) {
-  __shared__ uint32_t tmp[32];
-  __shared__ uint32_t s_res[4];
-  const int64_t row = blockIdx.y;
-  const uint32_t b1 = row_threshold_digit(hist + row * kHist12, k, tmp, s_res);
-  const int64_t nv = row_valid(n_valid, row, n_cols);
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
-  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
-  const int lane = threadIdx.x & 31;
-  for (int64_t base = c0; base < c1; base += NT) {
-    const int64_t s = base + threadIdx.x;
-    uint32_t key = 0u;
-    if (s < c1) {
-      key = f2key(scores[row * ld + s]);
-      if (key == 0u) key = 1u;
-    }
-    const bool take = s < c1 && (key >> 20) >= b1;
-    const uint32_t m = __ballot_sync(0xffffffffu, take);
-    if (m == 0u) continue;
-    uint32_t slot0 = 0;
-    if (lane == __ffs(m) - 1) slot0 = atomicAdd(&cnt[row], static_cast<uint32_t>(__popc(m)));
-    slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(m) - 1);
-    if (take) {
-      const uint32_t slot = slot0 + __popc(m & lanemask_lt());
-      if (slot < static_cast<uint32_t>(cap)) {
-        ckey[row * cap + slot] = key;
-        cpos[row * cap + slot] = static_cast<int32_t>(s);
-      }
-    }
-  }
-}
-
-// Items are (key, position) pairs, read from the candidate list in shared memory, or, on
-// overflow, straight from the score row.
-struct FinalItems {
-  const uint32_t* key;  // shared
-  const int32_t* pos;   // shared
-  const float* row;     // global fallback
-  int n;
-  bool from_row;
-  __device__ __forceinline__ uint32_t k_at(int e) const {
-    if (!from_row) return key[e];
-    uint32_t x = f2key(row[e]);
-    return x == 0u ? 1u : x;
-  }
-  __device__ __forceinline__ int32_t p_at(int e) const { return from_row ? e : pos[e]; }
-};
-
-__global__ void __launch_bounds__(NT) topk_final_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                        int64_t n_cols, const uint32_t* cnt, const uint32_t* ckey,
-                                                        const int32_t* cpos, int cap, int k, int32_t* idx) {
-  extern __shared__ uint32_t sm[];
-  uint32_t* skey = sm;                                        // [cap]
-  int32_t* spos = reinterpret_cast<int32_t*>(sm + cap);       // [cap]
-  uint32_t* hist = sm + 2 * cap;                              // [2048]
-  uint32_t* tmp = hist + kHistBins;                           // [32]
-  uint32_t* s_res = tmp + 32;                                 // [8]
-  int32_t* sel = reinterpret_cast<int32_t*>(s_res + 8);       // [k]
-  int32_t* eqp = sel + k;                                     // [cap] positions of keys equal to T
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int64_t row = blockIdx.x;
-  const uint32_t n_cand = cnt[row];
-  FinalItems it;
-  it.from_row = n_cand > static_cast<uint32_t>(cap);
-  it.n = it.from_row ? static_cast<int>(row_valid(n_valid, row, n_cols)) : static_cast<int>(n_cand);
-  it.row = scores + row * ld;
-  it.key = skey;
-  it.pos = spos;
-  if (!it.from_row) {
-    for (int e = tid; e < it.n; e += NT) {
-      skey[e] = ckey[row * cap + e];
-      spos[e] = cpos[row * cap + e];
-    }
-  }
-  __syncthreads();
-  // radix select over the item keys (as block_select, with the key read through `it`)
-  uint32_t T = 1u;
-  int quota = 0x7fffffff;
-  if (it.n > k) {
-    uint32_t prefix = 0u, mask = 0u;
-    int kk = k;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = shifts[pass], nb = 1 << widths[pass];
-      for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-      __syncthreads();
-      for (int base = 0; base < it.n; base += NT) {
-        const int e = base + tid;
-        const uint32_t key = e < it.n ? it.k_at(e) : 0u;
-        const bool part = key != 0u && (key & mask) == prefix;
-        const uint32_t digit = part ? ((key >> shift) & static_cast<uint32_t>(nb - 1)) : 0xffffffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (part && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
-      }
-      __syncthreads();
-      const int bpt = nb / NT;
-      const int b0 = tid * bpt;
-      uint32_t local = 0;
-      for (int q = 0; q < bpt; ++q) local += hist[b0 + q];
-      uint32_t tot;
-      const uint32_t excl = block_exclusive_scan<NT>(local, tmp, &tot);
-      uint32_t run = tot - excl - local;
-      for (int q = bpt - 1; q >= 0; --q) {
-        const uint32_t h = hist[b0 + q];
-        if (run < static_cast<uint32_t>(kk) && run + h >= static_cast<uint32_t>(kk)) {
-          s_res[0] = static_cast<uint32_t>(b0 + q);
-          s_res[1] = run;
-        }
-        run += h;
-      }
-      __syncthreads();
-      kk -= static_cast<int>(s_res[1]);
-      prefix |= s_res[0] << shift;
-      mask |= static_cast<uint32_t>(nb - 1) << shift;
-      __syncthreads();
-    }
-    T = prefix;
-    quota = kk;
-  }
-  // gather keys > T, and the positions of keys == T
-  if (tid == 0) {
-    s_res[2] = 0u;
-    s_res[3] = 0u;
-  }
-  __syncthreads();
-  for (int e = tid; e < it.n; e += NT) {
-    const uint32_t key = it.k_at(e);
-    if (key == 0u) continue;
-    if (key > T) {
-      sel[atomicAdd(&s_res[2], 1u)] = it.p_at(e);
-    } else if (key == T && !it.from_row) {
-      eqp[atomicAdd(&s_res[3], 1u)] = it.p_at(e);
-    }
-  }
-  __syncthreads();
-  const int n_gt = static_cast<int>(s_res[2]);
-  int take_eq;
-  if (!it.from_row) {
-    // among equal keys the lowest positions win: rank each by counting smaller positions
-    const int n_eq = static_cast<int>(s_res[3]);
-    take_eq = min(n_eq, max(0, min(quota, k - n_gt)));
-    for (int j = tid; j < n_eq; j += NT) {
-      const int32_t p = eqp[j];
-      int rank = 0;
-      for (int i = 0; i < n_eq; ++i) rank += eqp[i] < p;
-      if (rank < take_eq) sel[n_gt + rank] = p;
-    }
-  } else {
-    // the row is in position order: the first equal keys of the row win
-    const int seg = (it.n + NT - 1) / NT;
-    const int lo = tid * seg, hi = min(it.n, lo + seg);
-    uint32_t c = 0;
-    for (int e = lo; e < hi; ++e) c += it.k_at(e) == T;
-    uint32_t n_eq;
-    uint32_t r = block_exclusive_scan<NT>(c, tmp, &n_eq);
-    take_eq = min(static_cast<int>(n_eq), max(0, min(quota, k - n_gt)));
-    for (int e = lo; e < hi; ++e)
-      if (it.k_at(e) == T) {
-        if (r < static_cast<uint32_t>(take_eq)) sel[n_gt + r] = e;
-        ++r;
-      }
-  }
-  __syncthreads();
-  const int n_sel = n_gt + take_eq;
-  // ascending output: the rank of each chosen position among the chosen ones
-  for (int j = tid; j < n_sel; j += NT) {
-    const int32_t p = sel[j];
-    int rank = 0;
-    for (int i = 0; i < n_sel; ++i) rank += sel[i] < p;
-    idx[row * k + rank] = p;
-  }
-  for (int j = n_sel + tid; j < k; j += NT) idx[row * k + j] = -1;
-}
-
-}  // namespace
-
-size_t topk_hist_workspace_bytes(int64_t rows, int k) {
-  const int cap = topk_hist_cap(k);
-  return 2 * align_up(static_cast<size_t>(rows) * cap * 4, 256);
-}
-
-int topk_hist_cap(int k) { return std::max(8192, 4 * k); }
-
-cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s) {
-  const int cap = topk_hist_cap(k);
-  uint32_t* cnt = hist_cnt + rows * kHist12;
-  uint8_t* w = static_cast<uint8_t*>(ws_cand);
-  uint32_t* ckey = reinterpret_cast<uint32_t*>(w);
-  int32_t* cpos = reinterpret_cast<int32_t*>(w + align_up(static_cast<size_t>(rows) * cap * 4, 256));
-  int chunk = 4096;
-  while (chunk > 1024 && rows * ((n_cols + chunk - 1) / chunk) < 2 * num_sms) chunk /= 2;
-  dim3 g1(static_cast<unsigned>(std::max<int64_t>(1, (n_cols + chunk - 1) / chunk)), static_cast<unsigned>(rows));
-  topk_filter_kernel<<<g1, NT, 0, s>>>(scores, ld, n_valid, n_cols, hist_cnt, k, cnt, ckey, cpos, cap, chunk);
-  count_launches(1);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t smem = (static_cast<size_t>(cap) * 3 + kHistBins + 40 + k) * 4;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>((static_cast<size_t>(topk_hist_cap(4096)) * 3 + kHistBins + 40 + 4096) * 4));
-    attr = true;
-  }
-  topk_final_kernel<<<static_cast<unsigned>(rows), NT, smem, s>>>(scores, ld, n_valid, n_cols, cnt, ckey, cpos, cap, k,
-                                                                  idx);
-  count_launches(1);
-  return cudaGetLastError();
-}
-
-}  // namespace csa
-
-namespace csa {
-
-bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand) {
-  return !has_cand && rows <= 64 && n_cols >= 16384;
-}
-
-size_t topk_hist_standalone_bytes(int64_t rows, int k) {
-  return align_up(static_cast<size_t>(rows) * (kTopkHistBins + 1) * 4, 256) + topk_hist_workspace_bytes(rows, k);
-}
-
-cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s) {
-  uint8_t* w = static_cast<uint8_t*>(a.ws);
-  uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(w);
-  const size_t hbytes = static_cast<size_t>(a.rows) * (kTopkHistBins + 1) * 4;
-  cudaError_t e = cudaMemsetAsync(hist_cnt, 0, hbytes, s);
-  if (e != cudaSuccess) return e;
-  const int chunk = 8192;
-  dim3 g(static_cast<unsigned>((a.n_cols + chunk - 1) / chunk), static_cast<unsigned>(a.rows));
-  topk_hist_build_kernel<<<g, NT, 0, s>>>(a.scores, a.ld, a.n_valid, a.n_cols, hist_cnt, chunk);
-  count_launches(1);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_topk_hist(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, hist_cnt, a.k, a.idx,
-                          w + align_up(hbytes, 256), a.num_sms, s);
-}
-
-}  // namespace csa
