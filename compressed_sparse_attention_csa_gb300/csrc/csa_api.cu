@@ -120,9 +120,24 @@ bool attn_shape_ok(const csa_config* c) {
   return tc || simt;
 }
 
+IndexerArgs indexer_shape(const csa_config* c, int T, int64_t E_cap, int sms) {
+  IndexerArgs a{};
+  a.B = c->B;
+  a.T = T;
+  a.HI = c->HI;
+  a.dI = c->dI;
+  a.m = c->m;
+  a.E_cap = E_cap;
+  a.act = c->act;
+  a.kidx = c->kidx;
+  a.num_sms = sms;
+  return a;
+}
+
 size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   const int64_t B = c->B;
-  size_t bytes = align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
+  size_t bytes = align_up(indexer_workspace_bytes(indexer_shape(c, 1, E_cap, sms)), 256);  // query images
+  bytes += align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
   bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
   bytes += align_up(static_cast<size_t>(B) * (kTopkHistRowWords + 1) * 4, 256);  // histograms + counters
@@ -173,8 +188,11 @@ size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_
   const int sms = device_sm_count();
   switch (op) {
     case CSA_OP_COMPRESS:
-    case CSA_OP_INDEXER:
       return 0;
+    case CSA_OP_INDEXER: {  // rows = B*T, n_cols = T
+      if (n_cols < 1 || rows % n_cols || rows / n_cols != cfg->B) return static_cast<size_t>(-1);
+      return indexer_workspace_bytes(indexer_shape(cfg, static_cast<int>(n_cols), 1, sms));
+    }
     case CSA_OP_TOPK:
       if (n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
       return topk_workspace_bytes(rows, n_cols, cfg->k, sms);
@@ -234,20 +252,19 @@ csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float
                               const int64_t* q_pos, const void* kI, const float* kscale, int64_t E_cap,
                               const int32_t* cand, int32_t n_cand, float* scores, int64_t ld_scores, void* ws,
                               size_t ws_bytes, csa_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!qI || !w || !q_pos || !kI || !scores) return CSA_ERR_NULL;
   if (cfg->kidx == CSA_E4M3 && !kscale) return CSA_ERR_NULL;
   if (!aligned16(qI) || !aligned16(w) || !aligned16(q_pos) || !aligned16(kI) || !aligned16(scores) ||
-      (kscale && !aligned16(kscale)) || (cand && !aligned16(cand)))
+      (kscale && !aligned16(kscale)) || (cand && !aligned16(cand)) || (ws && !aligned16(ws)))
     return CSA_ERR_ALIGN;
   const int64_t n_cols = cand ? n_cand : E_cap;
   if (T < 0 || E_cap < 0 || (cand && n_cand < 0) || ld_scores < n_cols || cfg->HI > 128 ||
       E_cap * cfg->B >= (int64_t(1) << 31))
     return CSA_ERR_SHAPE;
   IndexerArgs a{};
+  a.ws = ws;
   a.qI = qI;
   a.w = w;
   a.q_pos = q_pos;
@@ -265,8 +282,10 @@ csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float
   a.E_cap = E_cap;
   a.act = cfg->act;
   a.kidx = cfg->kidx;
-  a.err = err_word_ptr();
   a.num_sms = device_sm_count();
+  const size_t need = indexer_workspace_bytes(a);
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  a.err = err_word_ptr();
   return launch_status(launch_indexer(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -397,6 +416,8 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   int* err = err_word_ptr();
 
   uint8_t* p = static_cast<uint8_t*>(ws);
+  void* q_images = p;
+  p += align_up(indexer_workspace_bytes(indexer_shape(cfg, 1, d->E_cap, sms)), 256);
   float* scores = reinterpret_cast<float*>(p);
   p += align_up(static_cast<size_t>(cfg->B) * d->E_cap * 4, 256);
   int32_t* nv = reinterpret_cast<int32_t*>(p);
@@ -447,6 +468,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   ia.err = err;
   ia.num_sms = sms;
   ia.nv_out = nv;
+  ia.ws = q_images;
   const bool hist_topk = indexer_uses_tensor_cores(ia);
   ia.hist_out = hist_topk ? hist_cnt : nullptr;
   e = launch_indexer(ia, s);

@@ -53,11 +53,13 @@ struct IndexerArgs {
   int* err;
   int num_sms;
   int32_t* nv_out;       // [B*T] visible-entry count per query row, or null
-  uint32_t* hist_out;    // [B*T, 4096] digit histogram of the visible scores (one query per CTA
+  uint32_t* hist_out;    // [B*T, 4160] digit histogram of the visible scores (one query per CTA
                          // only), accumulated with atomics; null = none
+  void* ws;              // tensor-core path: query images (indexer_workspace_bytes)
 };
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
 bool indexer_uses_tensor_cores(const IndexerArgs& a);
+size_t indexer_workspace_bytes(const IndexerArgs& a);
 
 // ---- top-k ------------------------------------------------------------------------
 struct TopkArgs {

@@ -25,6 +25,8 @@ __device__ __forceinline__ uint64_t global_ns() {
 // A wait that gives up after this many nanoseconds sets kErrTimeout.
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 
+__host__ __device__ constexpr uint32_t align_up_dev(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -11,8 +11,9 @@
 // the G*HI query-heads of a query group as N.  Each TMEM lane then holds one key's scores
 // for every head, so ReLU, the gate weights and the sum over heads are thread-local in the
 // epilogue.  Key tiles stream through a TMA ring (evict-first); one thread issues the MMAs
-// into two TMEM accumulators so that the epilogue of tile i overlaps the MMA of tile i+1.
-// Eight epilogue warps, two per TMEM lane quadrant, each reduce half of the heads.
+// into a ring of TMEM accumulators; two groups of four epilogue warps take alternate tiles.
+// The query operand of each query group is prepared once (indexer_qprep_kernel) as the
+// exact shared-memory image, and every CTA of the group pulls it with one bulk copy.
 //
 // E4M3 keys use kind::f8f6f4.  The query is split into two E4M3 terms, q/s = hi + lo with
 // s = per-head amax/448, and both terms run through the same accumulator (the K loop is
@@ -82,10 +83,12 @@ struct TcLayout {
   int G;               // queries per CTA
   int N;               // MMA N = G * HI
   int stages;
-  uint32_t b_bytes;    // B operand (queries; hi and lo regions for e4m3), 1024-aligned
+  uint32_t b_bytes;    // B operand image (bf16 rows, or e4m3 hi + lo regions), 1024-aligned
+  uint32_t w_bytes;    // gate vector image (G*HI fp32), 16-aligned
   uint32_t stage_bytes;
   uint32_t smem_bytes;
   uint32_t tmem_cols;
+  int n_acc;           // TMEM accumulators in the MMA -> epilogue ring (2..4)
   int n_splits;        // key-range splits per (sequence, query group)
   int n_qgroups;
 };
@@ -101,47 +104,113 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// sum_j w[j] * relu(v[j]) over 32 values, four independent chains
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// sum_j w[j] * relu(v[j]) over 32 values (w in shared memory, read as float4), four chains
 __device__ __forceinline__ float relu_dot32(const float (&v)[32], const float* w) {
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
-    a0 = fmaf(w[j], fmaxf(v[j], 0.f), a0);
-    a1 = fmaf(w[j + 1], fmaxf(v[j + 1], 0.f), a1);
-    a2 = fmaf(w[j + 2], fmaxf(v[j + 2], 0.f), a2);
-    a3 = fmaf(w[j + 3], fmaxf(v[j + 3], 0.f), a3);
+    const float4 w4 = *reinterpret_cast<const float4*>(w + j);
+    a0 = fmaf(w4.x, fmaxf(v[j], 0.f), a0);
+    a1 = fmaf(w4.y, fmaxf(v[j + 1], 0.f), a1);
+    a2 = fmaf(w4.z, fmaxf(v[j + 2], 0.f), a2);
+    a3 = fmaf(w4.w, fmaxf(v[j + 3], 0.f), a3);
   }
   return (a0 + a1) + (a2 + a3);
 }
 
-// Warp 0: TMA producer (starts streaming key tiles at once).  Warps 1..9 stage the query
-// operand; then warp 1 issues the MMAs and warps 2..9 run the epilogue.
+// Query operand of every query group, written once as the CTA's shared-memory image:
+// [b_bytes: B operand, 128B-swizzled K-major][w_bytes: gates (x per-head scale for e4m3)].
+// One CTA per (query group, sequence); one warp per query row.
+template <bool FP8>
+__global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a, const TcLayout L,
+                                                            uint8_t* images) {
+  const int HI = a.HI, G = L.G, N = L.N, T = a.T;
+  const int qg = blockIdx.x, b = blockIdx.y;
+  const int g0 = qg * G;
+  const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
+  uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
+  float* wimg = reinterpret_cast<float*>(img + L.b_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
+  for (int gh = warp; gh < N; gh += 8) {
+    const int g = gh / HI, h = gh - g * HI;
+    const bool valid = g0 + g < T;
+    if constexpr (!FP8) {
+      // 256-byte bf16 row: lane l copies 16-byte chunk l/2 ... as two regions of 64 elements
+      const int c = lane >> 1;  // 0..15
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (valid && (lane & 1) == 0)
+        v = *reinterpret_cast<const uint4*>(qI + ((qrow0 + g) * HI + h) * 128 + c * 8);
+      if ((lane & 1) == 0) *reinterpret_cast<uint4*>(img + (c >> 3) * (N * 128) + sw128(gh, c & 7)) = v;
+      if (lane == 0) wimg[gh] = valid ? a.w[(qrow0 + g) * HI + h] : 0.f;
+    } else {
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (valid) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(qI + ((qrow0 + g) * HI + h) * 128 + lane * 4);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        x[0] = __low2float(p0);
+        x[1] = __high2float(p0);
+        x[2] = __low2float(p1);
+        x[3] = __high2float(p1);
+      }
+      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float sc = am > 0.f ? am / 448.f : 1.f;
+      const float inv = 1.f / sc;
+      uint32_t hi4 = 0u, lo4 = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float y = x[j] * inv;
+        const uint8_t ch = f_to_e4m3(y);
+        const uint8_t cl = f_to_e4m3(y - e4m3_to_f(ch));
+        hi4 |= static_cast<uint32_t>(ch) << (8 * j);
+        lo4 |= static_cast<uint32_t>(cl) << (8 * j);
+      }
+      const uint32_t off = sw128(gh, lane >> 2) + (lane & 3) * 4;
+      *reinterpret_cast<uint32_t*>(img + off) = hi4;
+      *reinterpret_cast<uint32_t*>(img + N * 128 + off) = lo4;
+      if (lane == 0) wimg[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
+    }
+  }
+}
+
+// Warp 0: TMA producer.  Warp 1: TMEM owner and MMA issuer (it also pulls the query image).
+// Warps 2..9: epilogue, as two groups of four (one warp per TMEM lane quadrant) that take
+// alternate tiles.
 template <bool FP8>
 __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                const IndexerArgs a, const TcLayout L,
-                                                                const int64_t n_cols) {
+                                                                   const IndexerArgs a, const TcLayout L,
+                                                                   const uint8_t* images, const int64_t n_cols) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int HI = a.HI, G = L.G, N = L.N, S = L.stages;
   uint8_t* sB = smem;
-  uint8_t* sA = smem + L.b_bytes;
-  float* sW = reinterpret_cast<float*>(sA + static_cast<size_t>(S) * L.stage_bytes);  // [G][HI]
-  float* sPart = sW + G * HI;                                                           // [2][G][128]
-  int* sNv = reinterpret_cast<int*>(sPart + 2 * G * kTile);
+  float* sW = reinterpret_cast<float*>(smem + L.b_bytes);  // [G][HI], right after the B image
+  uint8_t* sA = smem + L.b_bytes + align_up_dev(L.w_bytes, 1024);
+  int* sNv = reinterpret_cast<int*>(sA + static_cast<size_t>(S) * L.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sNv + kMaxG) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
-  uint64_t* tfull = bars + 2 * S;
-  uint64_t* tempty = bars + 2 * S + 2;
-  uint64_t* pfull = bars + 2 * S + 4;   // [4 quadrants][2 slots]: second half's partials ready
-  uint64_t* pempty = bars + 2 * S + 12; // [4][2]: first half has read the slot
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 20);
+  uint64_t* tfull = bars + 2 * S;       // [4] accumulator ready for the epilogue
+  uint64_t* tempty = bars + 2 * S + 4;  // [4] accumulator drained
+  uint64_t* qbar = bars + 2 * S + 8;    // query image landed
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 9);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(sTmem + 4);  // [4096] when a.hist_out (G == 1)
   const bool hist = a.hist_out != nullptr && G == 1;
+  const int NA = L.n_acc;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z, g0 = blockIdx.y * G, split = blockIdx.x;
+  const int b = blockIdx.z, qg = blockIdx.y, g0 = qg * G, split = blockIdx.x;
   const int T = a.T;
   const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
 
@@ -163,14 +232,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 32 * kEpiWarps);
+      mbar_init(&tempty[i], 32 * (kEpiWarps / 2));
     }
-    for (int i = 0; i < 8; ++i) {
-      mbar_init(&pfull[i], 32);
-      mbar_init(&pempty[i], 32);
-    }
+    mbar_init(qbar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -185,9 +251,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   int nv_max = 0;
   for (int g = 0; g < G; ++g) nv_max = max(nv_max, sNv[g]);
   const int tiles_needed = (nv_max + kTile - 1) / kTile;
-  const int tile_lo = static_cast<int>(static_cast<int64_t>(split) * tiles_needed / L.n_splits);
-  const int tile_hi = static_cast<int>(static_cast<int64_t>(split + 1) * tiles_needed / L.n_splits);
-  const int n_it = tile_hi - tile_lo;
+  // the splits of a row interleave tile by tile (split, split + n_splits, ...)
+  const int tile_lo = split, tile_step = L.n_splits;
+  const int n_it = tiles_needed > tile_lo ? (tiles_needed - tile_lo + tile_step - 1) / tile_step : 0;
 
   if (warp == 0) {
     if (lane == 0 && n_it > 0) {
@@ -198,7 +264,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         const int st = it % S;
         if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) break;
         mbar_arrive_expect_tx(&full[st], L.stage_bytes);
-        const int64_t row64 = static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it) * kTile;
+        const int64_t row64 =
+            static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it * tile_step) * kTile;
         const int row = static_cast<int>(row64);
         uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
         // innermost coordinate 0 or 64 elements: always 16-byte aligned
@@ -217,88 +284,22 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         for (int64_t c = static_cast<int64_t>(tiles_needed) * kTile + lane; c < n_cols; c += 32) dst[c] = -INFINITY;
       }
     }
-  } else {
-    // ---- stage the B operand (the group's query heads), 128B-swizzled K-major
-    const int t2 = tid - 32, nthr = kTcThreads - 32, nwarps = nthr / 32;
-    if constexpr (!FP8) {
-      const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-      const int n_chunks = N * 16;  // 256 bytes per row = 16 chunks of 16 B
-      for (int i = t2; i < n_chunks; i += nthr) {
-        const int n = i >> 4, c = i & 15;
-        const int g = n / HI, h = n - g * HI;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (g < G && g0 + g < T) v = *reinterpret_cast<const uint4*>(qI + ((qrow0 + g) * HI + h) * 128 + c * 8);
-        *reinterpret_cast<uint4*>(sB + (c >> 3) * (N * 128) + sw128(n, c & 7)) = v;
-      }
-      for (int i = t2; i < G * HI; i += nthr) {
-        const int g = i / HI;
-        sW[i] = (g0 + g < T) ? a.w[(qrow0 + g) * HI + (i - g * HI)] : 0.f;
-      }
-    } else {
-      // one warp per query row: amax, scale s, hi = e4m3(q/s), lo = e4m3(q/s - hi); all of a
-      // warp's rows are loaded first (one round trip), then quantised
-      const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-      constexpr int kBatch = 8;  // rows loaded per round trip
-      const int wq = warp - 1;
-      for (int i0 = 0; wq + nwarps * i0 < G * HI; i0 += kBatch) {
-      uint2 raw[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int gh = wq + nwarps * (i0 + i);
-        raw[i] = make_uint2(0u, 0u);
-        if (gh < G * HI) {
-          const int g = gh / HI, h = gh - g * HI;
-          if (g0 + g < T) raw[i] = *reinterpret_cast<const uint2*>(qI + ((qrow0 + g) * HI + h) * 128 + lane * 4);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int gh = wq + nwarps * (i0 + i);
-        if (gh >= G * HI) break;
-        const int g = gh / HI, h = gh - g * HI;
-        const bool valid = g0 + g < T;
-        float x[4];
-        {
-          const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].x);
-          const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].y);
-          x[0] = __low2float(p0);
-          x[1] = __high2float(p0);
-          x[2] = __low2float(p1);
-          x[3] = __high2float(p1);
-        }
-        float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        const float sc = am > 0.f ? am / 448.f : 1.f;
-        const float inv = 1.f / sc;
-        uint32_t hi4 = 0u, lo4 = 0u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float y = x[j] * inv;
-          const uint8_t ch = f_to_e4m3(y);
-          const uint8_t cl = f_to_e4m3(y - e4m3_to_f(ch));
-          hi4 |= static_cast<uint32_t>(ch) << (8 * j);
-          lo4 |= static_cast<uint32_t>(cl) << (8 * j);
-        }
-        const uint32_t off = sw128(gh, lane >> 2) + (lane & 3) * 4;
-        *reinterpret_cast<uint32_t*>(sB + off) = hi4;
-        *reinterpret_cast<uint32_t*>(sB + N * 128 + off) = lo4;
-        if (lane == 0) sW[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
-      }
-      }
-    }
-    fence_proxy_async_smem();
-    named_sync(1, nthr);
-
-    if (warp == 1) {
-      if (lane == 0 && n_it > 0) {
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // the group's query image (B operand + gates) in one bulk copy
+      const uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
+      mbar_arrive_expect_tx(qbar, L.b_bytes + L.w_bytes);
+      bulk_g2s(sB, img, L.b_bytes, qbar);
+      bulk_g2s(sW, img + L.b_bytes, L.w_bytes, qbar);
+      const bool q_ok = mbar_wait(qbar, 0, a.err, sAbort);
+      if (q_ok && n_it > 0) {
         const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
         const uint32_t bBase = smem_u32(sB);
         int committed = 0;
         for (int it = 0; it < n_it; ++it) {
-          const int st = it % S, acc = it & 1;
+          const int st = it % S, acc = it % NA;
           if (!mbar_wait(&full[st], (it / S) & 1, a.err, sAbort)) break;
-          if (!mbar_wait(&tempty[acc], ((it >> 1) & 1) ^ 1, a.err, sAbort)) break;
+          if (!mbar_wait(&tempty[acc], ((it / NA) & 1) ^ 1, a.err, sAbort)) break;
           tc_fence_after();
           const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
           const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
@@ -322,105 +323,70 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
           mma_commit(&tfull[acc]);
           ++committed;
         }
-        if (committed > 0) wait_time_only(&tfull[(committed - 1) & 1], ((committed - 1) >> 1) & 1);
+        if (committed > 0) wait_time_only(&tfull[(committed - 1) % NA], ((committed - 1) / NA) & 1);
       }
-    } else {
-      // ---- epilogue: warp pair (e, e+4) shares TMEM lane quadrant q; `half` picks the heads
-      const int e = warp - 2;
-      const int q = warp & 3;
-      const int half = e >> 2;
-      const int hh = HI / 2;        // heads per warp (HI = 32, 64 or 128: 16, 32, 64)
-      const int h0 = half * hh;
-      const int rin = q * 32 + lane;
-      const int hb = hh == 16 ? 0 : h0;  // first head of the 32 columns this warp loads
-      // gates of those 32 heads for the single-query layout stay in registers
-      float wreg[32];
-      if (G == 1) {
+      if (!q_ok) wait_time_only(qbar, 0);  // the image copy must land before the CTA exits
+    }
+  } else {
+    // ---- epilogue: group gp (0/1) takes tiles gp, gp + 2, ...; warp (warp & 3) owns TMEM
+    //      lanes 32q..32q+31, i.e. 32 keys of the tile, and reduces every head of them
+    const int q = warp & 3;
+    const int gp = (warp - 2) >> 2;
+    const int rin = q * 32 + lane;
+    const bool w_ok = mbar_wait(qbar, 0, a.err, sAbort);  // gates landed with the query image
+    const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
+    auto scale_of = [&](int itx) -> float {
+      const int64_t sx = static_cast<int64_t>(tile_lo + itx * tile_step) * kTile + rin;
+      return (FP8 && itx < n_it && sx < a.E_cap) ? kscale_b[sx] : 1.f;
+    };
+    float ks_next = scale_of(gp);  // e4m3 key scales, prefetched one tile of this group ahead
+    for (int it = gp; w_ok && it < n_it; it += 2) {
+      const int acc = it % NA;
+      const float ksc = ks_next;
+      ks_next = scale_of(it + 2);
+      if (!mbar_wait(&tfull[acc], (it / NA) & 1, a.err, sAbort)) break;
+      tc_fence_after();
+      const int64_t s = static_cast<int64_t>(tile_lo + it * tile_step) * kTile + rin;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
+      float res[kMaxG];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) wreg[j] = sW[hb + j];
+      for (int g = 0; g < kMaxG; ++g) {
+        res[g] = 0.f;
+        if (g >= G) continue;
+        float sum = 0.f;
+        for (int hc = 0; hc < HI; hc += 32) {
+          float v[32];
+          tmem_ld32(lane_base + g * HI + hc, v);
+          tmem_wait_ld(v);
+          sum += relu_dot32(v, sW + g * HI + hc);
+        }
+        res[g] = sum;
       }
-      const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
-      auto scale_of = [&](int itx) -> float {
-        const int64_t sx = static_cast<int64_t>(tile_lo + itx) * kTile + rin;
-        return (FP8 && itx < n_it && sx < a.E_cap) ? kscale_b[sx] : 1.f;
-      };
-      float ks0 = scale_of(0), ks1 = scale_of(1);  // e4m3 key scales, prefetched two tiles ahead
-      for (int it = 0; it < n_it; ++it) {
-        const int acc = it & 1;
-        const float ksc = ks0;
-        ks0 = ks1;
-        ks1 = scale_of(it + 2);
-        if (!mbar_wait(&tfull[acc], (it >> 1) & 1, a.err, sAbort)) break;
-        tc_fence_after();
-        const int64_t s = static_cast<int64_t>(tile_lo + it) * kTile + rin;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
-        float part[kMaxG];
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (s < n_cols) {
 #pragma unroll
         for (int g = 0; g < kMaxG; ++g) {
-          part[g] = 0.f;
-          if (g >= G) continue;
-          float v[32];
-          // first 32 columns of this warp's heads; with 16 heads per warp (HI = 32) both
-          // warps of the pair load heads 0..31 and each zeroes the other warp's 16
-          tmem_ld32(lane_base + g * HI + hb, v);
-          tmem_wait_ld(v);
-          if (hh == 16) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              v[j] = half ? 0.f : v[j];
-              v[j + 16] = half ? v[j + 16] : 0.f;
-            }
-          }
-          // gates: registers for one query, shared memory otherwise
-          part[g] = (G == 1) ? relu_dot32(v, wreg) : relu_dot32(v, sW + g * HI + hb);
-          if (hh == 64) {  // 128 indexer heads: a second group of 32 columns
-            tmem_ld32(lane_base + g * HI + h0 + 32, v);
-            tmem_wait_ld(v);
-            part[g] += relu_dot32(v, sW + g * HI + h0 + 32);
-          }
+          if (g >= G || g0 + g >= T) continue;
+          const float sc = res[g] * ksc;
+          a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
+          if (hist && s < sNv[0]) atomicAdd(&sHist[f2key(sc) >> 20], 1u);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
-        // combine the two halves of every key through a double-buffered smem slot
-        const int slot_i = it & 1;
-        const uint32_t pph = (it >> 1) & 1;
-        float* slot = sPart + slot_i * G * kTile;
-        bool ok = true;
-        if (half) {
-          ok = mbar_wait(&pempty[q * 2 + slot_i], pph ^ 1, a.err, sAbort);
-#pragma unroll
-          for (int g = 0; g < kMaxG; ++g)
-            if (g < G) slot[g * kTile + rin] = part[g];
-          mbar_arrive(&pfull[q * 2 + slot_i]);
-          if (!ok) break;
-          continue;
-        }
-        ok = mbar_wait(&pfull[q * 2 + slot_i], pph, a.err, sAbort);
-        if (ok && s < n_cols) {
-#pragma unroll
-          for (int g = 0; g < kMaxG; ++g) {
-            if (g >= G || g0 + g >= T) continue;
-            const float sc = (part[g] + slot[g * kTile + rin]) * ksc;
-            a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
-            if (hist && s < sNv[0]) atomicAdd(&sHist[f2key(sc) >> 20], 1u);
-          }
-        }
-        mbar_arrive(&pempty[q * 2 + slot_i]);
-        if (!ok) break;
       }
-      if (hist) {
-        named_sync(6, 32 * kEpiWarps);
-        uint32_t* rh = a.hist_out + qrow0 * kTopkHistRowWords;
-        for (int i = tid - 64; i < kTopkHistBins; i += 32 * kEpiWarps) {
-          const uint32_t c = sHist[i];
-          if (c) atomicAdd(&rh[i], c);
-        }
-        if (tid - 64 < kTopkHistCoarse) {
-          const int cb = tid - 64;
-          uint32_t c = 0;
-          for (int j = 0; j < kTopkHistBins / kTopkHistCoarse; ++j) c += sHist[cb * (kTopkHistBins / kTopkHistCoarse) + j];
-          if (c) atomicAdd(&rh[kTopkHistBins + cb], c);
-        }
+    }
+    if (hist) {
+      named_sync(6, 32 * kEpiWarps);
+      uint32_t* rh = a.hist_out + qrow0 * kTopkHistRowWords;
+      for (int i = tid - 64; i < kTopkHistBins; i += 32 * kEpiWarps) {
+        const uint32_t c = sHist[i];
+        if (c) atomicAdd(&rh[i], c);
+      }
+      if (tid - 64 < kTopkHistCoarse) {
+        const int cb = tid - 64;
+        constexpr int per = kTopkHistBins / kTopkHistCoarse;
+        uint32_t c = 0;
+        for (int j = 0; j < per; ++j) c += sHist[cb * per + j];
+        if (c) atomicAdd(&rh[kTopkHistBins + cb], c);
       }
     }
   }
@@ -439,21 +405,25 @@ TcLayout plan_tc(const IndexerArgs& a) {
   L.G = std::max(1, std::min({256 / a.HI, a.T, kMaxG}));
   L.N = L.G * a.HI;
   L.b_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * 256, 1024));  // bf16 rows or hi+lo
+  L.w_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * 4, 16));
   L.stage_bytes = fp8 ? kKeyTileBytesF8 : 32768u;
   L.n_qgroups = (a.T + L.G - 1) / L.G;
   const int tiles = static_cast<int>((a.E_cap + kTile - 1) / kTile);
   const int64_t groups = static_cast<int64_t>(a.B) * L.n_qgroups;
   // few long rows (decode): two CTAs per SM, key range split over them
   const bool decode_like = groups < a.num_sms;
-  const size_t misc = 1024 + static_cast<size_t>(L.G) * a.HI * 4 + 2 * L.G * kTile * 4 + 64 + 40 * 8 + 64 +
+  const size_t misc = 1024 + align_up(L.w_bytes, 1024) + 64 + 32 * 8 + 64 +
                       (a.hist_out && L.G == 1 ? kTopkHistBins * 4 : 0);
   const size_t budget = decode_like ? (113 * 1024) : (227 * 1024);
   int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
   S = std::max(2, std::min(S, 8));
   L.stages = S;
   L.smem_bytes = static_cast<uint32_t>(misc + L.b_bytes + static_cast<size_t>(S) * L.stage_bytes);
+  // as many accumulators (2..4) as the TMEM share of this CTA (512 columns per SM) holds
+  const int share = decode_like ? 256 : 512;
+  L.n_acc = std::max(2, std::min(4, share / L.N));
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(2 * L.N)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(L.n_acc * L.N)) cols <<= 1;
   L.tmem_cols = cols;
   if (decode_like) {
     const int64_t target = 2 * static_cast<int64_t>(a.num_sms);
@@ -471,6 +441,12 @@ bool indexer_uses_tensor_cores(const IndexerArgs& a) {
          (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
 }
 
+size_t indexer_workspace_bytes(const IndexerArgs& a) {
+  if (!indexer_uses_tensor_cores(a) || a.B * a.T == 0) return 0;
+  const TcLayout L = plan_tc(a);
+  return static_cast<size_t>(a.B) * L.n_qgroups * (L.b_bytes + L.w_bytes);
+}
+
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T;
   const int64_t n_cols = a.cand ? a.n_cand : a.E_cap;
@@ -483,14 +459,24 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
                         const_cast<void*>(a.kI), 128, static_cast<uint64_t>(a.B) * a.E_cap, fp8 ? 128 : 256,
                         fp8 ? 128 : 64, kTile))
       return cudaErrorInvalidValue;
+    uint8_t* images = static_cast<uint8_t*>(a.ws);
+    dim3 gq(L.n_qgroups, a.B);
+    if (fp8)
+      indexer_qprep_kernel<true><<<gq, 256, 0, s>>>(a, L, images);
+    else
+      indexer_qprep_kernel<false><<<gq, 256, 0, s>>>(a, L, images);
+    count_launches(1);
     dim3 grid(L.n_splits, L.n_qgroups, a.B);
-    if (fp8) {
-      cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
-      indexer_tc_kernel<true><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, n_cols);
-    } else {
-      cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem_bytes);
-      indexer_tc_kernel<false><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, n_cols);
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      attr = true;
     }
+    if (fp8)
+      indexer_tc_kernel<true><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, images, n_cols);
+    else
+      indexer_tc_kernel<false><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, images, n_cols);
     count_launches(1);
     return cudaGetLastError();
   }

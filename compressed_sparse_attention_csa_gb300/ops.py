@@ -128,9 +128,11 @@ def indexer_scores(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.
     c = cfg.c()
     T = qI.shape[1]
     n_cand = cand.shape[-1] if cand is not None else 0
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_INDEXER, ctypes.byref(c), cfg.B * T, T), qI.device)
+    wp, wb = _ws_args(ws)
     _check("csa_indexer_scores",
            lib.csa_indexer_scores(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), kI.shape[1],
-                                  _p(cand), n_cand, _p(scores), scores.shape[-1], None, 0, _stream()))
+                                  _p(cand), n_cand, _p(scores), scores.shape[-1], wp, wb, _stream()))
 
 
 def topk(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional[torch.Tensor] = None,
