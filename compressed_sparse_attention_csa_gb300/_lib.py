@@ -44,6 +44,8 @@ SIGNATURES = {
                                           c_vp, c_i32, c_vp, c_i64, c_vp, c_sz, c_vp]),
     "csa_topk": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp,
                                 c_sz, c_vp]),
+    "csa_topk_noalloc": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp,
+                                        c_vp]),
     "csa_block_pool": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_i32,
                                       c_vp, c_vp, c_vp, c_sz, c_vp]),
     "csa_sparse_attn": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i32, c_vp, c_i64, c_vp, c_vp, c_i64,

@@ -148,6 +148,17 @@ def topk(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional
                                     wp, wb, _stream()))
 
 
+def topk_noalloc(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional[torch.Tensor] = None,
+                 cand: Optional[torch.Tensor] = None, n_cols: Optional[int] = None) -> None:
+    """csa_topk_noalloc: csa_topk using the library's fixed device scratch (no workspace)."""
+    lib = L.load()
+    c = cfg.c()
+    rows, ld = scores.shape
+    n_cols = ld if n_cols is None else n_cols
+    _check("csa_topk_noalloc", lib.csa_topk_noalloc(ctypes.byref(c), _p(scores), ld, rows, n_cols, _p(n_valid),
+                                                    _p(cand), _p(idx), _stream()))
+
+
 def block_pool(cfg: Config, scores: torch.Tensor, pool: torch.Tensor, pool_count: Optional[torch.Tensor] = None,
                n_valid: Optional[torch.Tensor] = None, block: int = 8, n_blocks: int = 2048,
                n_cols: Optional[int] = None) -> None:

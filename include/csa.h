@@ -133,6 +133,29 @@ csa_status csa_topk(const csa_config *cfg, const float *scores, int64_t ld, int6
                     void *ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
+ * csa_topk_noalloc — csa_topk for callers that cannot allocate device memory.  There is no
+ * counterpart in the source pages; it exists for callers that are only ever given input and
+ * output buffers (for example a plugin inside another runtime that owns all device memory,
+ * or a latency-critical path where an allocation could block or fail), so they cannot pass
+ * csa_topk a workspace.
+ *
+ * Same arguments and results as csa_topk, without ws/ws_bytes.  The scratch is a fixed array
+ * of CSA_NOALLOC_SCRATCH_BYTES inside the library (a __device__ object that every GPU which
+ * loads the library holds until the process exits); this call allocates nothing.  Sizes whose
+ * scratch need (csa_workspace_size(CSA_OP_TOPK, ...)) exceeds that limit are rejected with
+ * CSA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device (with that device current) looks up the array's device address
+ *    with cudaGetSymbolAddress; make that first call before any stream capture.
+ *  - All calls share the one array and find it as the previous call left it; what must start
+ *    at zero is cleared on the stream.  Calls whose work overlaps on the GPU (different streams,
+ *    or different host threads without ordering) race on it: order them on one stream.
+ */
+#define CSA_NOALLOC_SCRATCH_BYTES (4u << 20)
+csa_status csa_topk_noalloc(const csa_config *cfg, const float *scores, int64_t ld, int64_t rows,
+                            int64_t n_cols, const int32_t *n_valid, const int32_t *cand, int32_t *idx,
+                            csa_stream_t stream);
+
+/*
  * csa_block_pool — CSA2 Hierarchical Sparse Indexer candidate pool (V4.1 page, section 3):
  * block j covers positions [block*j, block*(j+1)) ∩ [0, n_valid[r]); its score is the max
  * there; the n_blocks best blocks under (max desc, j asc) are kept and expanded to their
