@@ -31,6 +31,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Kernels of a dependent chain are launched with programmatic stream serialization: a kernel
+// may start while its predecessor drains, runs only its independent prologue, and waits here
+// before it touches anything the predecessor writes (the wait returns once the predecessor
+// grid has completed and its memory is visible).  Every kernel of the chain waits, so the
+// ordering stays transitive.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

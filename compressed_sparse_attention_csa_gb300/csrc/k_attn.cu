@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(AttnArgs a) {
   uint32_t* tmp = reinterpret_cast<uint32_t*>(salpha + H);  // 32
   int32_t* sel = reinterpret_cast<int32_t*>(tmp + 32);      // [k]
 
+  pdl_wait();
+  pdl_trigger();
   const int64_t r = blockIdx.x;
   const int b = static_cast<int>(r / a.T);
   const int tid = threadIdx.x;
@@ -250,6 +252,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     s_mrun[tid] = -INFINITY;
     s_lrun[tid] = 0.f;
   }
+  pdl_wait();  // the selection and the caches come from the kernels before this one
+  pdl_trigger();
   const int n_sel = compact_idx<kTcThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
   const int64_t t = a.q_pos[r];
   int64_t p_lo;
@@ -474,6 +478,8 @@ constexpr int kMaxSplit = 16;
 __global__ void __launch_bounds__(kD) attn_merge_kernel(const AttnArgs a, const TcAttnSplit sp) {
   __shared__ float s_f[kMaxSplit][kMergeHeads];  // per split, per head: 2^(m_s - M) / den
   __shared__ float s_inv[kMergeHeads];
+  pdl_wait();
+  pdl_trigger();
   const int64_t r = blockIdx.x;
   const int h0 = blockIdx.y * kMergeHeads;
   const int dd = threadIdx.x;
@@ -565,26 +571,26 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       attr = true;
     }
     dim3 grid(sp.n_split, static_cast<unsigned>(rows));
-    attn_tc_kernel<<<grid, kTcThreads, smem, s>>>(a, sp);
+    cudaError_t e = launch_pdl(attn_tc_kernel, grid, dim3(kTcThreads), smem, s, a, sp);
     count_launches(1);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || sp.n_split == 1) return e;
-    attn_merge_kernel<<<dim3(static_cast<unsigned>(rows), kH / kMergeHeads), kD, 0, s>>>(a, sp);
+    e = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads), dim3(kD), 0, s, a, sp);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
   }
   const size_t smem = (static_cast<size_t>(a.H) * a.d * 2 + kSimtTile * (a.d + 1) + a.H * kSimtTile + 3 * a.H + 32) * 4 +
                       static_cast<size_t>(a.k) * 4;
+  cudaError_t e;
   if (a.act == CSA_F32) {
     cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    attn_simt_kernel<float><<<static_cast<unsigned>(rows), kSimtThreads, smem, s>>>(a);
+    e = launch_pdl(attn_simt_kernel<float>, dim3(static_cast<unsigned>(rows)), dim3(kSimtThreads), smem, s, a);
   } else {
     cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
-    attn_simt_kernel<__nv_bfloat16><<<static_cast<unsigned>(rows), kSimtThreads, smem, s>>>(a);
+    e = launch_pdl(attn_simt_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(rows)), dim3(kSimtThreads), smem, s, a);
   }
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa

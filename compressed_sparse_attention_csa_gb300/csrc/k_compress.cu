@@ -21,6 +21,8 @@ constexpr int kMaxTok = 32;  // 2m <= 32
 
 template <typename T>
 __global__ void __launch_bounds__(512) compress_kernel(CompressArgs a) {
+  pdl_wait();  // the caches and histograms may still be read by the previous step
+  pdl_trigger();
   const CompressJob& job = a.job[blockIdx.z];
   const int b = blockIdx.y;
   const int m = a.m;
@@ -107,12 +109,10 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   int dmax = a.job[0].dim;
   if (a.n_jobs > 1 && a.job[1].dim > dmax) dmax = a.job[1].dim;
   const int threads = (dmax + 31) / 32 * 32;
-  if (a.act_bf16)
-    compress_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
-  else
-    compress_kernel<float><<<grid, threads, 0, s>>>(a);
+  const cudaError_t e = a.act_bf16 ? launch_pdl(compress_kernel<__nv_bfloat16>, grid, dim3(threads), 0, s, a)
+                                   : launch_pdl(compress_kernel<float>, grid, dim3(threads), 0, s, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa

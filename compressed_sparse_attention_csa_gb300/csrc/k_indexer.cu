@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_
   extern __shared__ float sm[];
   float* sq = sm;              // [HI][DI]
   float* sw = sm + a.HI * DI;  // [HI]
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.y;
   const int b = static_cast<int>(row / a.T);
   const TQ* q = static_cast<const TQ*>(a.qI) + row * a.HI * DI;
@@ -131,6 +133,8 @@ __device__ __forceinline__ float relu_dot32(const float (&v)[32], const float* w
 template <bool FP8>
 __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a, const TcLayout L,
                                                             uint8_t* images) {
+  pdl_wait();  // the images may still be read by the previous indexer launch
+  pdl_trigger();
   const int HI = a.HI, G = L.G, N = L.N, T = a.T;
   const int qg = blockIdx.x, b = blockIdx.y;
   const int g0 = qg * G;
@@ -247,6 +251,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sTmem;
+  // the keys, scales, query images and histograms are written by the kernels before this one
+  pdl_wait();
 
   int nv_max = 0;
   for (int g = 0; g < G; ++g) nv_max = max(nv_max, sNv[g]);
@@ -391,6 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     }
   }
 
+  pdl_trigger();  // the next kernel may start launching while this CTA tears down
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -461,11 +468,10 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
       return cudaErrorInvalidValue;
     uint8_t* images = static_cast<uint8_t*>(a.ws);
     dim3 gq(L.n_qgroups, a.B);
-    if (fp8)
-      indexer_qprep_kernel<true><<<gq, 256, 0, s>>>(a, L, images);
-    else
-      indexer_qprep_kernel<false><<<gq, 256, 0, s>>>(a, L, images);
+    cudaError_t e = fp8 ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
+                        : launch_pdl(indexer_qprep_kernel<false>, gq, dim3(256), 0, s, a, L, images);
     count_launches(1);
+    if (e != cudaSuccess) return e;
     dim3 grid(L.n_splits, L.n_qgroups, a.B);
     static bool attr = false;
     if (!attr) {
@@ -473,12 +479,11 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
       cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       attr = true;
     }
-    if (fp8)
-      indexer_tc_kernel<true><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, images, n_cols);
-    else
-      indexer_tc_kernel<false><<<grid, kTcThreads, L.smem_bytes, s>>>(map, a, L, images, n_cols);
+    const uint8_t* cimages = images;
+    e = fp8 ? launch_pdl(indexer_tc_kernel<true>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L, cimages, n_cols)
+            : launch_pdl(indexer_tc_kernel<false>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L, cimages, n_cols);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
   }
   dim3 grid(static_cast<unsigned>((n_cols + 127) / 128), static_cast<unsigned>(rows));
   const size_t smem = static_cast<size_t>(a.HI) * (a.dI + 1) * 4;

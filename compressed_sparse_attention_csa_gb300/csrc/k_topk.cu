@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(NT) topk_level_kernel(LevelParams p) {
   uint32_t* wtot = tmp + 32;  // [3][NW]
   uint32_t* s_res = wtot + 3 * NW;
 
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.y;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
@@ -270,6 +272,8 @@ size_t level_smem(int chunk, bool raw) {
 
 __global__ void blockmax_kernel(const float* scores, int64_t ld, int64_t n_cols, const int32_t* n_valid,
                                 int block, float* bmax, int64_t ld_b, int32_t* nb_out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.y;
   int64_t nv = n_valid ? n_valid[row] : n_cols;
   nv = nv < n_cols ? nv : n_cols;
@@ -288,6 +292,8 @@ __global__ void blockmax_kernel(const float* scores, int64_t ld, int64_t n_cols,
 __global__ void pool_expand_kernel(const int32_t* sel, int n_blocks, int block, const int32_t* n_valid,
                                    int64_t n_cols, int32_t* pool, int32_t* pool_count) {
   __shared__ uint32_t tmp[32];
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.x;
   int64_t nv = n_valid ? n_valid[row] : n_cols;
   nv = nv < n_cols ? nv : n_cols;
@@ -356,12 +362,9 @@ cudaError_t run_levels(const Plan& pl, const float* scores, int64_t ld, int64_t 
                            static_cast<int>(level_smem(kCandChunk, false)));
       attr_set = true;
     }
-    if (l == 0)
-      topk_level_kernel<true><<<grid, NT, smem, s>>>(p);
-    else
-      topk_level_kernel<false><<<grid, NT, smem, s>>>(p);
+    cudaError_t e = (l == 0) ? launch_pdl(topk_level_kernel<true>, grid, dim3(NT), smem, s, p)
+                             : launch_pdl(topk_level_kernel<false>, grid, dim3(NT), smem, s, p);
     count_launches(1);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -406,17 +409,18 @@ cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s) {
   int32_t* sel = reinterpret_cast<int32_t*>(ws);
   ws += align_up(static_cast<size_t>(a.rows) * a.n_blocks * 4, 256);
   dim3 g1(static_cast<unsigned>((nbmax + 255) / 256), static_cast<unsigned>(a.rows));
-  blockmax_kernel<<<g1, 256, 0, s>>>(a.scores, a.ld, a.n_cols, a.n_valid, a.block, bmax, nbmax, nb);
+  cudaError_t e = launch_pdl(blockmax_kernel, g1, dim3(256), 0, s, a.scores, a.ld, a.n_cols, a.n_valid, a.block,
+                             bmax, static_cast<int64_t>(nbmax), nb);
   count_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const Plan pl = make_plan(a.rows, nbmax, a.n_blocks, a.num_sms);
   e = run_levels(pl, bmax, nbmax, a.rows, nb, nullptr, a.n_blocks, sel, ws, s);
   if (e != cudaSuccess) return e;
-  pool_expand_kernel<<<static_cast<unsigned>(a.rows), 256, 0, s>>>(sel, a.n_blocks, a.block, a.n_valid, a.n_cols,
-                                                                    a.pool, a.pool_count);
+  const int32_t* csel = sel;
+  e = launch_pdl(pool_expand_kernel, dim3(static_cast<unsigned>(a.rows)), dim3(256), 0, s, csel, a.n_blocks, a.block,
+                 a.n_valid, a.n_cols, a.pool, a.pool_count);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa

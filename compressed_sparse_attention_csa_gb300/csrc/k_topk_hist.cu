@@ -85,6 +85,8 @@ __device__ uint32_t threshold_digit(const uint32_t* row_hist, int k) {
 __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
                                                              int64_t n_cols, uint32_t* hist, int chunk) {
   __shared__ uint32_t h[kFine];
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < kFine; i += NT) h[i] = 0u;
   __syncthreads();
   const int64_t row = blockIdx.y;
@@ -107,6 +109,8 @@ __global__ void __launch_bounds__(NT) topk_filter_kernel(const float* scores, in
                                                          int64_t n_cols, const uint32_t* hist, int k, uint32_t* cnt,
                                                          uint32_t* ckey, int32_t* cpos, int cap, int chunk) {
   __shared__ uint32_t s_b1;
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.y;
   if (threadIdx.x < 32) {
     const uint32_t b1 = threshold_digit(hist + row * kRowWords, k);
@@ -170,6 +174,8 @@ __global__ void __launch_bounds__(NT) topk_final_kernel(const float* scores, int
   int32_t* srt = sel + k;                                // [k]  winners grouped by bucket
   int32_t* eqp = srt + k;                                // [cap] positions of keys equal to T
   const int tid = threadIdx.x, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.x;
   const int64_t nvr = row_valid(n_valid, row, n_cols);
   const uint32_t n_cand = cnt[row];
@@ -348,9 +354,10 @@ cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int6
   int32_t* cpos = reinterpret_cast<int32_t*>(w + align_up(static_cast<size_t>(rows) * cap * 4, 256));
   const HistPlan pl = plan_hist(rows, n_cols, num_sms);
   dim3 g1(static_cast<unsigned>(std::max<int64_t>(1, (n_cols + pl.chunk - 1) / pl.chunk)), static_cast<unsigned>(rows));
-  topk_filter_kernel<<<g1, NT, 0, s>>>(scores, ld, n_valid, n_cols, hist_cnt, k, cnt, ckey, cpos, cap, pl.chunk);
+  const uint32_t* chist = hist_cnt;
+  cudaError_t e = launch_pdl(topk_filter_kernel, g1, dim3(NT), 0, s, scores, ld, n_valid, n_cols, chist, k, cnt, ckey,
+                             cpos, cap, pl.chunk);
   count_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   static bool attr = false;
   if (!attr) {
@@ -358,10 +365,13 @@ cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int6
                          static_cast<int>(topk_hist_final_smem(4096)));
     attr = true;
   }
-  topk_final_kernel<<<static_cast<unsigned>(rows), NT, topk_hist_final_smem(k), s>>>(scores, ld, n_valid, n_cols, cnt,
-                                                                                     ckey, cpos, cap, k, idx);
+  const uint32_t* ccnt = cnt;
+  const uint32_t* cckey = ckey;
+  const int32_t* ccpos = cpos;
+  e = launch_pdl(topk_final_kernel, dim3(static_cast<unsigned>(rows)), dim3(NT), topk_hist_final_smem(k), s, scores, ld,
+                 n_valid, n_cols, ccnt, cckey, ccpos, cap, k, idx);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand) {
@@ -380,9 +390,8 @@ cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int chunk = 8192;
   dim3 g(static_cast<unsigned>((a.n_cols + chunk - 1) / chunk), static_cast<unsigned>(a.rows));
-  topk_hist_build_kernel<<<g, NT, 0, s>>>(a.scores, a.ld, a.n_valid, a.n_cols, hist_cnt, chunk);
+  e = launch_pdl(topk_hist_build_kernel, g, dim3(NT), 0, s, a.scores, a.ld, a.n_valid, a.n_cols, hist_cnt, chunk);
   count_launches(1);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_topk_hist(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, hist_cnt, a.k, a.idx,
                           w + align_up(hbytes, 256), a.num_sms, s);
