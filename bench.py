@@ -56,6 +56,39 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+STAGE_PROFILES = {4: "indexer_tc_e4m3_1M_decode.md", 2: "indexer_tc_bf16_64K_decode.md"}
+STAGE_KERNELS = ("indexer_qprep_kernel", "indexer_tc_kernel")
+STAGE_SOURCES = ("k_indexer.cu", "csa_ptx.cuh", "csa_internal.h")
+
+
+def stage_traffic(config):
+    """DRAM bytes per indexer-stage launch from the committed ncu summary, or None.
+
+    The summary carries `traffic-bytes-per-launch <kernel> <bytes>` lines and the sha256 of
+    the kernel sources it was taken with; the figure is used only while every stage kernel
+    has a line and the sources are unchanged."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", STAGE_PROFILES.get(config, ""))
+    if not os.path.isfile(path):
+        return None
+    per, sha = {}, None
+    with open(path) as f:
+        for line in f:
+            w = line.split()
+            if len(w) == 3 and w[0] == "traffic-bytes-per-launch":
+                per[w[1]] = int(w[2])
+            elif len(w) == 2 and w[0] == "sources-sha256":
+                sha = w[1]
+    src = os.path.join(ROOT, "compressed_sparse_attention_csa_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in STAGE_SOURCES:
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    if sha != h.hexdigest() or any(k not in per for k in STAGE_KERNELS):
+        return None
+    return sum(per[k] for k in STAGE_KERNELS)
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while the timed loop runs."""
     FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
@@ -326,16 +359,7 @@ def main():
     idx_bytes = work["indexer_bytes"] + cfg.B * cfg.E * 4        # + the fp32 scores the kernel writes
     hbm, bf16, peak_kind = peaks()
     achieved = idx_bytes / (idx_ms / 1e3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "indexer_traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                pj = json.load(f)
-            if pj.get("config") == args.config:
-                traffic = pj.get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = stage_traffic(args.config)
     roofline = {"bound": "hbm",
                 "kernel": "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<%s>" % (
                     "e4m3" if cfg.kidx == "fp8" else "bf16"),
