@@ -238,7 +238,11 @@ def main():
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
 
-    inp = gen.make_inputs(cfg, dev)
+    # weak scaling: every rank decodes its own cfg.B sequences of a batch of cfg.B * world
+    from compressed_sparse_attention_csa_gb300.shard import max_over_ranks, shard_rows
+    row0, n_rows = shard_rows(cfg.B * world, world, rank)
+    assert n_rows == cfg.B
+    inp = gen.make_inputs(cfg, dev, row0=row0)
     c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                    act=torch.bfloat16, fp8_keys=cfg.kidx == "fp8", softmax_scale=cfg.softmax_scale)
     out = torch.empty(cfg.B, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
@@ -325,10 +329,7 @@ def main():
     launches = launches_per_step * K
     total_ms = sum(a.elapsed_time(b) for a, b in ev)
     assert csa.get_last_error() == 0
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms)
     clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
 
     tokens = cfg.B * K * world
@@ -355,7 +356,7 @@ def main():
         g_idx.replay()
         evi[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    idx_ms = sum(a.elapsed_time(b) for a, b in evi) / Ki
+    idx_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evi) / Ki)
     idx_bytes = work["indexer_bytes"] + cfg.B * cfg.E * 4        # + the fp32 scores the kernel writes
     hbm, bf16, peak_kind = peaks()
     achieved = idx_bytes / (idx_ms / 1e3) / 1e9
@@ -385,7 +386,7 @@ def main():
         host_out.copy_(out, non_blocking=True)
         eve[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eve) / Ke)
     e2e_val = cfg.B * world / (e2e_ms / 1e3)
 
     cpu = None

@@ -163,12 +163,14 @@ _IDS = {
 }
 
 
-def _gen(cfg: CsaConfig, name: str, shape, std, dtype, device, layer: int = 0):
+def _gen(cfg: CsaConfig, name: str, shape, std, dtype, device, layer: int = 0, row0: int = 0):
+    """Draws of one tensor; with row0 > 0 the leading axis holds rows row0.. of a larger batch."""
     seed = _tensor_seed(cfg.seed, _IDS[name] + 64 * layer)
     n = 1
     for s in shape:
         n *= s
-    return normal(seed, n, device=device, std=std, dtype=dtype).reshape(shape)
+    per_row = n // shape[0] if shape[0] else 0
+    return normal(seed, n, device=device, std=std, dtype=dtype, offset=row0 * per_row).reshape(shape)
 
 
 def quantize_keys_e4m3(x: torch.Tensor):
@@ -181,8 +183,12 @@ def quantize_keys_e4m3(x: torch.Tensor):
     return codes, scale
 
 
-def make_inputs(cfg: CsaConfig, device="cpu", *, skip=()) -> Dict[str, torch.Tensor]:
+def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict[str, torch.Tensor]:
     """All input tensors of one preset, generated on `device`.
+
+    With row0 > 0 the cfg.B sequences are sequences row0 .. row0+B-1 of a larger batch: every
+    per-sequence tensor holds exactly the values the larger batch has in those rows, so a
+    batch can be split across processes that each generate only their own rows.
 
     Keys (shapes use B, T, H, d, HI, dI, E = N // m, L = window rows held):
       q [B,T,H,d], qI [B,T,HI,dI], w [B,T,HI] f32, sink [H] f32, q_pos [B*T] i64,
@@ -205,31 +211,31 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=()) -> Dict[str, torch.Ten
 
     if cfg.mode == "csa2":
         nl = 1 + cfg.n_reuse
-        out["q"] = torch.stack([_gen(cfg, "q", (B, T, H, d), 1 / math.sqrt(d), act, device, l)
+        out["q"] = torch.stack([_gen(cfg, "q", (B, T, H, d), 1 / math.sqrt(d), act, device, l, row0=row0)
                                 for l in range(nl)])
-        out["kv_local"] = torch.stack([_gen(cfg, "kv_local", (B, L, d), 1 / math.sqrt(d), act, device, l)
+        out["kv_local"] = torch.stack([_gen(cfg, "kv_local", (B, L, d), 1 / math.sqrt(d), act, device, l, row0=row0)
                                        for l in range(nl)])
         out["sink"] = torch.stack([_gen(cfg, "sink", (H,), 1.0, f32, device, l) for l in range(nl)])
-        out["qI_full"] = _gen(cfg, "qI_full", (B, T, HI, dI), 1 / math.sqrt(dI), act, device)
-        out["w_full"] = _gen(cfg, "w_full", (B, T, HI), 1.0, f32, device)
+        out["qI_full"] = _gen(cfg, "qI_full", (B, T, HI, dI), 1 / math.sqrt(dI), act, device, row0=row0)
+        out["w_full"] = _gen(cfg, "w_full", (B, T, HI), 1.0, f32, device, row0=row0)
     else:
-        out["q"] = _gen(cfg, "q", (B, T, H, d), 1 / math.sqrt(d), act, device)
-        out["kv_local"] = _gen(cfg, "kv_local", (B, L, d), 1 / math.sqrt(d), act, device)
+        out["q"] = _gen(cfg, "q", (B, T, H, d), 1 / math.sqrt(d), act, device, row0=row0)
+        out["kv_local"] = _gen(cfg, "kv_local", (B, L, d), 1 / math.sqrt(d), act, device, row0=row0)
         out["sink"] = _gen(cfg, "sink", (H,), 1.0, f32, device)
-    out["qI"] = _gen(cfg, "qI", (B, T, HI, dI), 1 / math.sqrt(dI), act, device)
-    out["w"] = _gen(cfg, "w", (B, T, HI), 1.0, f32, device)
+    out["qI"] = _gen(cfg, "qI", (B, T, HI, dI), 1 / math.sqrt(dI), act, device, row0=row0)
+    out["w"] = _gen(cfg, "w", (B, T, HI), 1.0, f32, device, row0=row0)
 
     # compressed caches: entries not produced by compression in this workload are drawn
     if "kv_comp" not in skip:
         if cfg.mode == "full":
             out["kv_comp"] = torch.zeros((B, E, d), dtype=act, device=device)
         else:
-            out["kv_comp"] = _gen(cfg, "kv_comp", (B, E, d), 1 / math.sqrt(d), act, device)
+            out["kv_comp"] = _gen(cfg, "kv_comp", (B, E, d), 1 / math.sqrt(d), act, device, row0=row0)
     if "kI" not in skip:
         if cfg.mode == "full":
             kI = torch.zeros((B, E, dI), dtype=f32, device=device)
         else:
-            kI = _gen(cfg, "kI", (B, E, dI), 1 / math.sqrt(dI), f32, device)
+            kI = _gen(cfg, "kI", (B, E, dI), 1 / math.sqrt(dI), f32, device, row0=row0)
         if cfg.kidx == "fp8":
             out["kI"], out["kscale"] = quantize_keys_e4m3(kI)
         else:
@@ -244,10 +250,10 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=()) -> Dict[str, torch.Ten
         else:
             base, n_str = t0 - m, T + m
         out["str_base"] = torch.full((B,), base, dtype=torch.int64, device=device)
-        out["kv_str"] = _gen(cfg, "kv_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device)
-        out["z_str"] = _gen(cfg, "z_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device)
-        out["kvI_str"] = _gen(cfg, "kvI_str", (B, n_str, 2, dI), 1 / math.sqrt(dI), act, device)
-        out["zI_str"] = _gen(cfg, "zI_str", (B, n_str, 2, dI), 1 / math.sqrt(dI), act, device)
+        out["kv_str"] = _gen(cfg, "kv_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device, row0=row0)
+        out["z_str"] = _gen(cfg, "z_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device, row0=row0)
+        out["kvI_str"] = _gen(cfg, "kvI_str", (B, n_str, 2, dI), 1 / math.sqrt(dI), act, device, row0=row0)
+        out["zI_str"] = _gen(cfg, "zI_str", (B, n_str, 2, dI), 1 / math.sqrt(dI), act, device, row0=row0)
         out["bias"] = _gen(cfg, "bias", (2, m, d), 0.1, f32, device)
         out["biasI"] = _gen(cfg, "biasI", (2, m, dI), 0.1, f32, device)
     return out
