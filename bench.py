@@ -1,24 +1,32 @@
 #!/usr/bin/env python
-"""CSA hot-path benchmark: decode tokens/s of the fused decode step at 1M-token context.
+"""CSA hot-path benchmark.
 
-Workload (default): V4-Flash CSA decode at 1,048,576 tokens of context, batch 4, m = 4
-(262,144 compressed entries per sequence), FP8 e4m3 indexer keys with one fp32 scale per
-entry, bf16 KV, 64 query heads x 512, indexer 64 heads x 128, top-k 512, window 128.
-One step = one decode token for each of the 4 sequences through csa_decode_step: compress
-the completed block, score every visible entry, top-512, sparse attention with sink.
+Default workload: the fused decode step at 1M-token context: V4-Flash CSA, batch 4,
+1,048,576 tokens of context, m = 4 (262,144 compressed entries per sequence), FP8 e4m3
+indexer keys with one fp32 scale per entry, bf16 KV, 64 query heads x 512, indexer 64 heads
+x 128, top-k 512, window 128.  One step = one decode token for each sequence through
+csa_decode_step: compress the completed block, score every visible entry, top-512, sparse
+attention with sink.
 
-Timing: W warm-up steps, then K timed steps; L2 is flushed (512 MiB written) before every
-step, outside the timed events; each step is bracketed by CUDA events on the launching
-stream.  `value` uses inputs resident in HBM; `e2e` adds, every step, the pinned-host ->
-device copy of the step's inputs and the device -> host copy of its output.  The dominant
-kernel (the indexer) is timed the same way on its own for the roofline entry.
+Other workloads (`--config`): 2 = decode at 64K context (batch 16, bf16 keys); 3 = prefill
+chunk (4,096 new queries after 131,072 tokens: compression of the chunk, indexer, top-k and
+attention for every query); 5 = CSA2 decoder group at 262,144 tokens (Full-layer indexer
+scan, block pool, Reindex rescoring, top-k, four attentions), also timed without the scan.
+
+Timing: W warm-up steps, then K timed steps, each a CUDA-graph replay of the step's library
+calls bracketed by CUDA events on the launching stream; L2 is flushed (512 MiB written)
+before every step, outside the events.  `value` uses inputs resident in HBM; `e2e` calls
+the public API eagerly and adds, every step, the pinned-host -> device copy of the step's
+inputs and the device -> host copy of its output.  The dominant kernel stage is timed the
+same way on its own for the roofline entry.
 
 `--impl reference` times the CPU oracle (oracle/csa_oracle.py, float64 numpy) on a bounded
 sample of the same workload on the host cores.  Multi-GPU (torchrun): every rank runs its
-own batch (sequences are independent; no collective on the data path), `value` is the sum
-over ranks, time is the max over ranks.
+own slice of a batch of B x world sequences (sequences are independent; no collective on the
+data path), `value` is the units of all ranks over the slowest rank's time.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -31,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20
+REFERENCE_BUDGET_S = 120.0
 
 
 def parse_args():
@@ -39,24 +48,28 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 4])
-    ap.add_argument("--cpu-seqs", type=int, default=12, help="decode tokens in the oracle sample")
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5])
+    ap.add_argument("--cpu-sample", type=int, default=None,
+                    help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["step", "indexer"], default=None,
-                    help="run only this stage on the workload (for profiler captures); prints its time")
+                    help="run only this stage on the workload, eagerly (for profiler captures)")
     return ap.parse_args()
 
 
 def peaks():
+    """(HBM GB/s, bf16 TF/s burst, bf16 TF/s sustained, kind) from the measured peaks file."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-STAGE_PROFILES = {4: "indexer_tc_e4m3_1M_decode.md", 2: "indexer_tc_bf16_64K_decode.md"}
+STAGE_PROFILES = {4: "indexer_tc_e4m3_1M_decode.md", 2: "indexer_tc_bf16_64K_decode.md",
+                  3: "indexer_tc_bf16_prefill_4K.md", 5: "indexer_tc_bf16_csa2_scan_256K.md"}
 STAGE_KERNELS = ("indexer_qprep_kernel", "indexer_tc_kernel")
 STAGE_SOURCES = ("k_indexer.cu", "csa_ptx.cuh", "csa_internal.h")
 
@@ -67,7 +80,6 @@ def stage_traffic(config):
     The summary carries `traffic-bytes-per-launch <kernel> <bytes>` lines and the sha256 of
     the kernel sources it was taken with; the figure is used only while every stage kernel
     has a line and the sources are unchanged."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", STAGE_PROFILES.get(config, ""))
     if not os.path.isfile(path):
         return None
@@ -138,38 +150,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ CPU oracle sample
-
-def oracle_sample(cfg, inp, n_seqs):
-    """Time the oracle on n_seqs sequences of the workload (float64 numpy on the host cores)."""
-    import numpy as np
-    import torch
-    from oracle import csa_oracle as O
-
-    n_seqs = max(1, n_seqs)
-    elapsed = 0.0
-    cache = {}
-    sub = cfg.replace(B=1)
-    for i in range(n_seqs):
-        b = (i * cfg.B) // n_seqs
-        if b not in cache:
-            # host copies of sequence b's inputs (not timed: the oracle reads host arrays)
-            host = {}
-            for k, v in inp.items():
-                x = v if k in ("bias", "biasI", "sink") else v[b:b + 1]
-                host[k] = x.cpu().to(torch.float64).numpy() if x.is_floating_point() else x.cpu().numpy()
-            cache = {b: host}
-        host = dict(cache[b])
-        codes = host.pop("kI")
-        kscale = host.pop("kscale", None)
-        kv_comp = host["kv_comp"][0].copy()
-        t0 = time.perf_counter()
-        kdeq = O.e4m3_decode(codes[0]) * kscale[0][:, None] if kscale is not None else codes[0].astype(np.float64)
-        O.decode_step_sequence(sub, host, 0, kv_comp, kdeq, fp8_keys=kscale is not None)
-        elapsed += time.perf_counter() - t0
-    return n_seqs, elapsed
-
-
 def cpu_threads():
     try:
         import numpy as np  # noqa: F401
@@ -180,6 +160,284 @@ def cpu_threads():
     except Exception:
         pass
     return os.cpu_count() or 1
+
+
+def _host64(x):
+    import torch
+    return x.cpu().to(torch.float64).numpy() if x.is_floating_point() else x.cpu().numpy()
+
+
+# ------------------------------------------------------------------ workloads
+#
+# A workload builds its inputs and buffers and exposes:
+#   step()             one pass of the whole hot path over the batch (inputs resident)
+#   units              tokens per step (the metric's unit)
+#   stage_fn()         the dominant kernel stage alone, with stage_bound / stage_amount
+#   e2e_in / e2e_out   the per-step inputs a user copies in and the output read back
+#   oracle(n)          (units, seconds, description) of the CPU oracle on a bounded sample
+
+
+class Decode:
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        self.units = cfg.B
+        self.metric = "CSA decode tok/s @1M ctx" if cfg.cid == 4 else "CSA decode tok/s @64K ctx"
+        self.workload = (f"V4-Flash CSA decode step, batch {cfg.B} @ {cfg.N:,}-token context "
+                         f"({cfg.E:,} entries/seq), " +
+                         ("FP8 e4m3 indexer keys + fp32 scale" if cfg.kidx == "fp8" else "bf16 indexer keys") +
+                         f", bf16 KV, {cfg.H}x{cfg.d} heads, indexer {cfg.HI}x{cfg.dI}, k {cfg.k}, W {cfg.W}")
+        self.config_extra = {"batch": cfg.B, "context": cfg.N, "m": cfg.m, "entries_per_seq": cfg.E,
+                             "heads": cfg.H, "head_dim": cfg.d, "indexer": f"{cfg.HI}x{cfg.dI}", "top_k": cfg.k,
+                             "window": cfg.W,
+                             "indexer_keys": "e4m3+fp32 scale" if cfg.kidx == "fp8" else "bf16"}
+        if host_only:
+            return
+        self.csa = csa
+        inp = gen.make_inputs(cfg, dev, row0=row0)
+        self.inp = inp
+        self.c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, fp8_keys=cfg.kidx == "fp8", softmax_scale=cfg.softmax_scale)
+        self.out = torch.empty(cfg.B, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
+        self.lse = torch.empty(cfg.B, cfg.H, device=dev)
+        self.idx = torch.empty(cfg.B, cfg.k, device=dev, dtype=torch.int32)
+        self.scores = torch.empty(cfg.B, cfg.E, device=dev)
+        self.args = dict(q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"],
+                         kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
+                         z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
+                         biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"],
+                         out=self.out, lse=self.lse, idx_out=self.idx)
+        from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
+        work = decode_step_work(cfg)
+        self.stage_label = "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<%s>" % (
+            "e4m3" if cfg.kidx == "fp8" else "bf16")
+        self.stage_bound = "hbm"
+        self.stage_amount = work["indexer_bytes"] + cfg.B * cfg.E * 4   # + the fp32 scores written
+        self.step_bytes = work["bytes"]
+        self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str",
+                                            "kv_local"]}
+        self.e2e_out = self.out
+
+    def step(self):
+        self.csa.decode_step(self.c, **self.args)
+
+    def stage_fn(self):
+        inp = self.inp
+        self.csa.indexer_scores(self.c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], self.scores,
+                                kscale=inp.get("kscale"))
+
+    def oracle(self, n, inp_cpu=None):
+        """n sequences of the workload, one decode token each."""
+        import numpy as np
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        nb = src["q_pos"].shape[0]
+        elapsed = 0.0
+        sub = cfg.replace(B=1)
+        cache = {}
+        for i in range(n):
+            b = (i * nb) // n
+            if b not in cache:
+                # host copies of sequence b's inputs (not timed: the oracle reads host arrays)
+                cache = {b: {k: _host64(v if k in ("bias", "biasI", "sink") else v[b:b + 1])
+                             for k, v in src.items()}}
+            host = dict(cache[b])
+            codes = host.pop("kI")
+            kscale = host.pop("kscale", None)
+            kv_comp = host["kv_comp"][0].copy()
+            t0 = time.perf_counter()
+            kdeq = (O.e4m3_decode(codes[0]) * kscale[0][:, None] if kscale is not None
+                    else codes[0].astype(np.float64))
+            O.decode_step_sequence(sub, host, 0, kv_comp, kdeq, fp8_keys=kscale is not None)
+            elapsed += time.perf_counter() - t0
+        desc = (f"{n} sequence(s) of this workload, one decode token each (compress, {cfg.E:,}-key indexer, "
+                f"top-{cfg.k}, attention over {cfg.k}+{cfg.W} rows), float64 numpy, {elapsed:.1f} s")
+        return n, elapsed, desc
+
+
+class Prefill:
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        B, T, E = cfg.B, cfg.T, cfg.E
+        self.units = B * T
+        self.metric = "CSA prefill tok/s (4,096-token chunk @128K ctx)"
+        self.workload = (f"V4-Flash CSA prefill chunk: {T:,} new tokens after {cfg.N - T:,} (entries "
+                         f"{(cfg.N - T) // cfg.m:,} -> {E:,}), batch {B}, bf16, {cfg.H}x{cfg.d} heads, indexer "
+                         f"{cfg.HI}x{cfg.dI}, k {cfg.k}, W {cfg.W}; compression of the chunk, indexer, top-k, "
+                         f"attention")
+        self.config_extra = {"batch": B, "chunk": T, "context_before": cfg.N - T, "m": cfg.m,
+                             "entries_after": E, "heads": cfg.H, "head_dim": cfg.d,
+                             "indexer": f"{cfg.HI}x{cfg.dI}", "top_k": cfg.k, "window": cfg.W}
+        self.tok0 = cfg.N - T - cfg.m
+        self.e0, self.e1 = (cfg.N - T) // cfg.m, cfg.N // cfg.m
+        if host_only:
+            return
+        self.csa = csa
+        inp = gen.make_inputs(cfg, dev, row0=row0)
+        self.inp = inp
+        self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, fp8_keys=False, softmax_scale=cfg.softmax_scale)
+        self.scores = torch.empty(B * T, E, device=dev)
+        self.idx = torch.empty(B * T, cfg.k, device=dev, dtype=torch.int32)
+        self.out = torch.empty(B, T, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
+        self.lse = torch.empty(B, T, cfg.H, device=dev)
+        from compressed_sparse_attention_csa_gb300.accounting import prefill_work
+        work = prefill_work(cfg)
+        self.stage_label = "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<bf16>"
+        self.stage_bound = "tensor"
+        self.stage_amount = work["indexer_flops"]
+        self.step_flops = work["flops"]
+        self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str",
+                                            "kv_local"]}
+        self.e2e_out = self.out
+
+    def step(self):
+        csa, c, inp = self.csa, self.c, self.inp
+        csa.compress_kv(c, inp["kv_str"], inp["z_str"], inp["bias"], self.tok0, self.e0, self.e1, inp["kv_comp"])
+        csa.compress_kv(c, inp["kvI_str"], inp["zI_str"], inp["biasI"], self.tok0, self.e0, self.e1, inp["kI"])
+        self.stage_fn()
+        csa.topk(c, self.scores, self.idx)
+        csa.sparse_attn(c, inp["q"], inp["kv_comp"], self.idx, inp["kv_local"], inp["local_base"], inp["q_pos"],
+                        inp["sink"], self.out, self.lse)
+
+    def stage_fn(self):
+        inp = self.inp
+        self.csa.indexer_scores(self.c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"],
+                                self.scores.view(self.cfg.B, self.cfg.T, self.cfg.E))
+
+    def oracle(self, n, inp_cpu=None):
+        """The chunk's compression (charged pro rata) plus n query rows spread over the chunk."""
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        h = {k: _host64(v if k in ("bias", "biasI", "sink", "q_pos") else v[0:1]) for k, v in src.items()}
+        kv_comp, kI = h["kv_comp"][0].copy(), h["kI"][0].copy()
+        t0 = time.perf_counter()
+        kv_comp[self.e0:self.e1] = O.compress_range(h["kv_str"][0], h["z_str"][0], h["bias"], cfg.m, self.e0,
+                                                    self.e1, tok0=self.tok0)
+        kI[self.e0:self.e1] = O.compress_range(h["kvI_str"][0], h["zI_str"][0], h["biasI"], cfg.m, self.e0,
+                                               self.e1, tok0=self.tok0)
+        t_comp = time.perf_counter() - t0
+        sub = cfg.replace(B=1)
+        t_rows = 0.0
+        for i in range(n):
+            tq = (i * (cfg.T - 1)) // max(n - 1, 1)
+            t0 = time.perf_counter()
+            O.decode_token(sub, h, 0, tq, kv_comp, kI)
+            t_rows += time.perf_counter() - t0
+        elapsed = t_rows + t_comp * n / cfg.T
+        desc = (f"{n} query row(s) of the chunk (indexer over ~{cfg.E:,} entries, top-{cfg.k}, attention) plus "
+                f"{n}/{cfg.T} of the chunk's compression ({t_comp:.1f} s whole), float64 numpy, "
+                f"{t_rows:.1f} s of rows")
+        return n, elapsed, desc
+
+
+class Csa2Group:
+    N_BLOCKS = 2048
+
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        B, E = cfg.B, cfg.E
+        self.units = B
+        self.layers = 1 + cfg.n_reuse
+        self.metric = "CSA2 decoder-group tok/s @256K ctx"
+        self.workload = (f"V4.1-Flash CSA2 decoder group, batch {B} @ {cfg.N:,} tokens at 1:1 (indexer "
+                         f"{cfg.HI}x{cfg.dI} bf16), Full-layer scan -> {self.N_BLOCKS} blocks of 8 -> Reindex "
+                         f"rescoring -> top-{cfg.k} -> {self.layers} attentions ({cfg.H}x{cfg.d}, W {cfg.W})")
+        self.config_extra = {"batch": B, "context": cfg.N, "m": cfg.m, "indexer": f"{cfg.HI}x{cfg.dI}",
+                             "pool_blocks": self.N_BLOCKS, "block": 8, "top_k": cfg.k, "window": cfg.W,
+                             "layers": self.layers}
+        if host_only:
+            return
+        self.csa = csa
+        inp = gen.make_inputs(cfg, dev, row0=row0)
+        self.inp = inp
+        self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, fp8_keys=False, softmax_scale=cfg.softmax_scale)
+        P = self.N_BLOCKS * 8
+        self.s_full = torch.empty(B, E, device=dev)
+        self.pool = torch.empty(B, P, dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(B, dtype=torch.int32, device=dev)
+        self.s_pool = torch.empty(B, P, device=dev)
+        self.idx = torch.empty(B, cfg.k, dtype=torch.int32, device=dev)
+        self.outs = torch.empty(self.layers, B, 1, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
+        from compressed_sparse_attention_csa_gb300.accounting import csa2_group_work
+        work = csa2_group_work(cfg, self.N_BLOCKS, 8, self.layers)
+        self.work = work
+        self.stage_label = "Full-layer scan, indexer stage: indexer_qprep_kernel + indexer_tc_kernel<bf16>"
+        self.stage_bound = "hbm"
+        self.stage_amount = work["scan_bytes"] + B * E * 4
+        self.step_bytes = work["bytes"]
+        self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "qI_full", "w_full", "q_pos", "kv_local"]}
+        self.e2e_out = self.outs
+
+    def stage_fn(self):
+        inp = self.inp
+        self.csa.indexer_scores(self.c, inp["qI_full"], inp["w_full"], inp["q_pos"], inp["kI"], self.s_full)
+
+    def step_without_scan(self):
+        csa, c, inp = self.csa, self.c, self.inp
+        csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], self.s_pool, cand=self.pool)
+        csa.topk(c, self.s_pool, self.idx, n_valid=self.cnt, cand=self.pool)
+        for layer in range(self.layers):
+            csa.sparse_attn(c, inp["q"][layer], inp["kv_comp"], self.idx, inp["kv_local"][layer],
+                            inp["local_base"], inp["q_pos"], inp["sink"][layer], self.outs[layer])
+
+    def step(self):
+        self.stage_fn()
+        self.csa.block_pool(self.c, self.s_full, self.pool, self.cnt, n_blocks=self.N_BLOCKS)
+        self.step_without_scan()
+
+    def oracle(self, n, inp_cpu=None):
+        """n sequences of the group, one token each, all four layers."""
+        import numpy as np
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        nb = src["q_pos"].shape[0]
+        elapsed = 0.0
+        for i in range(n):
+            b = (i * nb) // n
+            h = {}
+            for k, v in src.items():
+                if k in ("q", "kv_local"):
+                    h[k] = _host64(v[:, b])
+                elif k == "sink":
+                    h[k] = _host64(v)
+                else:
+                    h[k] = _host64(v[b])
+            t = int(h["q_pos"])
+            t0 = time.perf_counter()
+            nv = min(t + 1, cfg.E)
+            sf = O.indexer_scores(h["qI_full"][0], h["w_full"][0], h["kI"], nv).astype(np.float32)
+            pool = O.hier_pool(sf, nv, 8, self.N_BLOCKS)
+            sr = O.indexer_scores_subset(h["qI"][0], h["w"][0], h["kI"], pool)
+            slots = O.topk(sr.astype(np.float32), pool.size, cfg.k)
+            sel = np.where(slots >= 0, pool[np.maximum(slots, 0)], -1)
+            for layer in range(self.layers):
+                rows = O.gather_rows(h["kv_comp"], sel, h["kv_local"][layer], int(h["local_base"]), t, cfg.W)
+                O.sparse_attention(h["q"][layer][0], rows, h["sink"][layer], cfg.softmax_scale)
+            elapsed += time.perf_counter() - t0
+        desc = (f"{n} sequence(s) of the group, one token each (Full scan over {cfg.E:,} positions, block pool, "
+                f"Reindex rescoring, top-{cfg.k}, {self.layers} attentions), float64 numpy, {elapsed:.1f} s")
+        return n, elapsed, desc
+
+
+WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group}
+
+
+def config_of(wl):
+    """The JSON line's `config` (identical for both arms)."""
+    return dict(workload=wl.workload, **wl.config_extra,
+                l2="flushed (512 MiB write) before every timed step",
+                timing="device time per step: CUDA events around a CUDA-graph replay")
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6}
 
 
 # ------------------------------------------------------------------ main
@@ -195,99 +453,76 @@ def main():
 
     from synth import gen
     cfg = gen.CONFIGS[args.config]
-    workload = ("V4-Flash CSA decode step, batch 4 @ 1,048,576-token context (262,144 entries/seq), "
-                "FP8 e4m3 indexer keys + fp32 scale, bf16 KV, 64x512 heads, indexer 64x128, k 512, W 128"
-                if args.config == 4 else
-                "V4-Flash CSA decode step, batch 16 @ 65,536-token context (16,384 entries/seq), bf16, "
-                "64x512 heads, indexer 64x128, k 512, W 128")
-    metric = "CSA decode tok/s @1M ctx" if args.config == 4 else "CSA decode tok/s @64K ctx"
-    config_obj = {"workload": workload, "batch": cfg.B, "context": cfg.N, "m": cfg.m, "entries_per_seq": cfg.E,
-                  "heads": cfg.H, "head_dim": cfg.d, "indexer": f"{cfg.HI}x{cfg.dI}", "top_k": cfg.k,
-                  "window": cfg.W, "indexer_keys": "e4m3+fp32 scale" if cfg.kidx == "fp8" else "bf16",
-                  "l2": "flushed (512 MiB write) before every timed step",
-                  "timing": "device time per step: CUDA events around a CUDA-graph replay of csa_decode_step"}
+    Wl = WORKLOADS[args.config]
+    sample_n = args.cpu_sample if args.cpu_sample is not None else DEFAULT_SAMPLE[args.config]
 
     if args.impl == "reference":
+        # The CPU oracle on the host cores, on this workload's config and metric.
         if rank != 0:
             return
-        torch.manual_seed(0)
+        # One step = the oracle on one sequence (decode, CSA2) or on 4 query rows (prefill).  A
+        # float64 numpy step takes seconds, so the run stops after REFERENCE_BUDGET_S of oracle
+        # time even if fewer than --steps steps ran; `steps` reports the steps actually timed.
+        wl = Wl(cfg, None, torch, "cpu", 0, host_only=True)
+        n1 = 4 if args.config == 3 else 1
         inp = gen.make_inputs(cfg.replace(B=1), "cpu")
-        for _ in range(max(0, args.warmup and 1)):
-            pass
-        n_total, t_total = 0, 0.0
-        for _ in range(args.steps):
-            n, t = oracle_sample(cfg.replace(B=1), inp, 1)
+        n_total, t_total, desc, done = 0, 0.0, "", 0
+        while done < max(args.steps, 1) and (done == 0 or t_total < REFERENCE_BUDGET_S):
+            n, t, desc = wl.oracle(n1, inp_cpu=inp)
             n_total += n
             t_total += t
+            done += 1
         v = n_total / t_total
-        line = {"impl": "reference", "metric": metric, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+        line = {"impl": "reference", "metric": wl.metric, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
+                "steps": done, "steps_requested": args.steps, "warmup": 0,
+                "ms_per_step": 1e3 * t_total / done,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config_obj,
+                "data": "synthetic", "config": config_of(wl),
                 "cpu_baseline": {"value": v, "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle",
-                                 "sample": "each step: one sequence of the workload (compress, 262,144-key indexer, "
-                                           "top-512, attention) in float64 numpy"},
+                                 "sample": f"{done} step(s) of {REFERENCE_BUDGET_S:.0f} s oracle budget; "
+                                           f"last step: " + desc},
                 "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
     import compressed_sparse_attention_csa_gb300 as csa
+    from compressed_sparse_attention_csa_gb300.shard import max_over_ranks, shard_rows
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
 
-    # weak scaling: every rank decodes its own cfg.B sequences of a batch of cfg.B * world
-    from compressed_sparse_attention_csa_gb300.shard import max_over_ranks, shard_rows
+    # weak scaling: every rank runs its own cfg.B sequences of a batch of cfg.B * world
     row0, n_rows = shard_rows(cfg.B * world, world, rank)
     assert n_rows == cfg.B
-    inp = gen.make_inputs(cfg, dev, row0=row0)
-    c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
-                   act=torch.bfloat16, fp8_keys=cfg.kidx == "fp8", softmax_scale=cfg.softmax_scale)
-    out = torch.empty(cfg.B, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
-    lse = torch.empty(cfg.B, cfg.H, device=dev)
-    idx = torch.empty(cfg.B, cfg.k, device=dev, dtype=torch.int32)
+    wl = Wl(cfg, csa, torch, dev, row0)
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
-    args_d = dict(q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"],
-                  kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
-                  z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
-                  biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse,
-                  idx_out=idx)
-
-    def step():
-        csa.decode_step(c, **args_d)
-
     stream = torch.cuda.current_stream(dev)
-    if args.only:
-        scores_only = torch.empty(cfg.B, cfg.E, device=dev)
 
-        def only_fn():
-            if args.only == "step":
-                step()
-            else:
-                csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], scores_only,
-                                   kscale=inp.get("kscale"))
+    if args.only:
+        fn = wl.step if args.only == "step" else wl.stage_fn
         for _ in range(args.warmup):
-            only_fn()
+            fn()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            only_fn()
+            fn()
         torch.cuda.synchronize(dev)
         assert csa.get_last_error() == 0
         print(json.dumps({"only": args.only, "config": args.config, "calls": args.steps,
                           "ms_per_call_back_to_back": 1e3 * (time.perf_counter() - t0) / max(args.steps, 1)}))
         return
+
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        wl.step()
     torch.cuda.synchronize(dev)
     assert csa.get_last_error() == 0
 
-    # The decode step is captured once into a CUDA graph (the library's launches are
-    # stream-ordered and allocate nothing) and replayed: the device time of a step then does
-    # not depend on how fast the host enqueues it.
+    # Each timed function is captured once into a CUDA graph (the library's launches are
+    # stream-ordered and allocate nothing once the workspace exists) and replayed: the device
+    # time then does not depend on how fast the host enqueues the launches.
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -295,8 +530,18 @@ def main():
         torch.cuda.synchronize(dev)
         return g
 
+    def time_graph(g, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in ev)
+
     n_cap = csa.launch_count()
-    g_step = capture(step)
+    g_step = capture(wl.step)
     launches_per_step = csa.launch_count() - n_cap
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -312,67 +557,56 @@ def main():
     sampler = ClockSampler(gpu_id) if rank == 0 else None
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    for i in range(K):
-        flush.zero_()
-        ev[i][0].record(stream)
-        g_step.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    total_ms = time_graph(g_step, K)
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
     launches = launches_per_step * K
-    total_ms = sum(a.elapsed_time(b) for a, b in ev)
     assert csa.get_last_error() == 0
     total_ms = max_over_ranks(total_ms)
     clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
 
-    tokens = cfg.B * K * world
-    value = tokens / (total_ms / 1e3)
+    value = wl.units * K * world / (total_ms / 1e3)
     ms_per_step = total_ms / K
 
-    # ---- dominant kernel alone: the indexer over the same inputs (same launch configuration)
-    from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
-    work = decode_step_work(cfg)
-    scores = torch.empty(cfg.B, cfg.E, device=dev)
-    Ki = max(3, min(K, 200))
-    evi = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ki)]
-
-    def indexer_call():
-        csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"], scores, kscale=inp.get("kscale"))
-
-    indexer_call()
-    g_idx = capture(indexer_call)  # the query-operand prep kernel plus the indexer kernel
+    # ---- dominant kernel stage alone, same inputs and launch configuration
+    wl.stage_fn()
+    g_stage = capture(wl.stage_fn)
     for _ in range(3):
-        g_idx.replay()
-    for i in range(Ki):
-        flush.zero_()
-        evi[i][0].record(stream)
-        g_idx.replay()
-        evi[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    idx_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evi) / Ki)
-    idx_bytes = work["indexer_bytes"] + cfg.B * cfg.E * 4        # + the fp32 scores the kernel writes
-    hbm, bf16, peak_kind = peaks()
-    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
-    traffic = stage_traffic(args.config)
-    roofline = {"bound": "hbm",
-                "kernel": "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<%s>" % (
-                    "e4m3" if cfg.kidx == "fp8" else "bf16"),
-                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "traffic": traffic, "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
-                "bytes_per_launch": idx_bytes, "launch_us": round(idx_ms * 1e3, 2),
-                "step_frac_of_hbm": round(work["bytes"] / (ms_per_step / 1e3) / 1e9 / hbm, 4)}
+        g_stage.replay()
+    Ki = max(3, min(K, 200))
+    stage_ms = max_over_ranks(time_graph(g_stage, Ki) / Ki)
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    if wl.stage_bound == "hbm":
+        achieved = wl.stage_amount / (stage_ms / 1e3) / 1e9
+        peak, unit, pk = hbm, "GB/s", f"{peak_kind} HBM copy bandwidth (burst)"
+        step_frac = {"step_frac_of_hbm": round(wl.step_bytes / (ms_per_step / 1e3) / 1e9 / hbm, 4)}
+    else:
+        achieved = wl.stage_amount / (stage_ms / 1e3) / 1e12
+        peak, unit, pk = bf16, "TFLOP/s", f"{peak_kind} dense bf16 GEMM throughput (burst)"
+        step_frac = {"step_tflops": round(wl.step_flops / (ms_per_step / 1e3) / 1e12, 1),
+                     "stage_frac_of_sustained": round(achieved / bf16_sus, 4)}
+    roofline = {"bound": wl.stage_bound, "kernel": wl.stage_label, "achieved": round(achieved, 1), "peak": peak,
+                "unit": unit, "frac": round(achieved / peak, 4), "traffic": stage_traffic(args.config),
+                "peak_kind": pk, "amount_per_launch": wl.stage_amount, "launch_us": round(stage_ms * 1e3, 2)}
+    roofline.update(step_frac)
 
-    # ---- end to end: host buffers, copies inside the timed region
-    per_step_in = ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str", "kv_local"]
-    host_in = {k: inp[k].cpu().pin_memory() for k in per_step_in}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    extra = {}
+    if isinstance(wl, Csa2Group):
+        g_ns = capture(wl.step_without_scan)
+        for _ in range(3):
+            g_ns.replay()
+        ns_ms = max_over_ranks(time_graph(g_ns, K) / K)
+        extra["without_scan"] = {"value": round(wl.units * world / (ns_ms / 1e3), 1), "ms_per_step": round(ns_ms, 5),
+                                 "frac_of_hbm": round(wl.work["bytes_without_scan"] / (ns_ms / 1e3) / 1e9 / hbm, 4)}
+
+    # ---- end to end: the public API with host buffers, copies inside the timed region
+    host_in = {k: v.cpu().pin_memory() for k, v in wl.e2e_in.items()}
+    host_out = torch.empty(wl.e2e_out.shape, dtype=wl.e2e_out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
     Ke = max(3, min(K, 500))
@@ -381,30 +615,30 @@ def main():
         flush.zero_()
         eve[i][0].record(stream)
         for k, v in host_in.items():
-            inp[k].copy_(v, non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
+            wl.e2e_in[k].copy_(v, non_blocking=True)
+        wl.step()
+        host_out.copy_(wl.e2e_out, non_blocking=True)
         eve[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    assert csa.get_last_error() == 0
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eve) / Ke)
-    e2e_val = cfg.B * world / (e2e_ms / 1e3)
+    e2e_val = wl.units * world / (e2e_ms / 1e3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n, t = oracle_sample(cfg, inp, args.cpu_seqs)
-        cpu = {"value": n / t, "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": f"{n} sequence(s) of this workload, one decode token each (compress, "
-                         f"{cfg.E:,}-key indexer, top-{cfg.k}, attention over {cfg.k}+{cfg.W} rows), "
-                         f"float64 numpy, {t:.1f} s"}
+        n, t, desc = wl.oracle(sample_n)
+        cpu = {"value": n / t, "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        line = {"metric": metric, "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": K,
+        line = {"metric": wl.metric, "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": config_obj, "roofline": roofline, "cpu_baseline": cpu,
+                "config": config_of(wl),
+                "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e_val, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "clocks": clocks}
+        line.update(extra)
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

@@ -56,3 +56,54 @@ def decode_step_work(cfg) -> Dict[str, float]:
         "attention_flops": attn_flops,
         "flops": idx_flops + attn_flops,
     }
+
+
+def prefill_work(cfg) -> Dict[str, float]:
+    """Algorithmic work of one prefill chunk: T new queries at t = N-T .. N-1 per sequence.
+
+    indexer: one multiply-add per (head, dim, visible key) for each query (causal pairs only);
+    attention: QK^T and PV over the k selected entries plus min(W, t+1) window rows per query;
+    compression: the T/m new entries of both caches from T+m stream tokens.
+    """
+    ab = _act_bytes(cfg.act)
+    B, T, m = cfg.B, cfg.T, cfg.m
+    t0 = cfg.N - T
+    pairs = 0
+    rows = 0
+    for t in range(t0, cfg.N):
+        nv = min((t + 1) // m, cfg.E)
+        pairs += nv
+        rows += min(cfg.k, nv) + min(cfg.W, t + 1)
+    pairs *= B
+    rows *= B
+    idx_flops = 2 * indexer_macs(cfg.HI, cfg.dI, pairs)
+    attn_flops = 4 * cfg.H * cfg.d * rows
+    n_new = T // m
+    comp_bytes = B * ((T + m) * 2 * 2 * (cfg.d + cfg.dI) * ab + n_new * (cfg.d + cfg.dI) * ab)
+    idx_bytes = B * cfg.E * indexer_key_bytes(cfg) + B * T * cfg.HI * (cfg.dI * ab + 4)
+    attn_bytes = B * (cfg.E * cfg.d * ab + T * 2 * cfg.H * cfg.d * ab)   # every entry once, q/out once
+    return {"pairs": pairs, "attention_rows": rows, "indexer_flops": idx_flops, "attention_flops": attn_flops,
+            "flops": idx_flops + attn_flops, "indexer_bytes": idx_bytes, "attention_bytes": attn_bytes,
+            "compress_bytes": comp_bytes, "bytes": idx_bytes + attn_bytes + comp_bytes}
+
+
+def csa2_group_work(cfg, pool_blocks: int = 2048, block: int = 8, layers: int = 4) -> Dict[str, float]:
+    """Algorithmic bytes of one CSA2 decoder-group token per sequence (m = 1).
+
+    scan: the Full layer reads every visible indexer key once; rescoring: the Reindex layer
+    reads the pooled keys once; each of the `layers` attentions gathers k + W rows and reads
+    q / writes out once.
+    """
+    ab = _act_bytes(cfg.act)
+    B = cfg.B
+    nv = min(cfg.N, cfg.E)
+    pool = min(pool_blocks * block, nv)
+    key_b = indexer_key_bytes(cfg)
+    q_b = cfg.HI * (cfg.dI * ab + 4)
+    scan = B * (nv * key_b + q_b)
+    rescore = B * (pool * key_b + q_b)
+    rows = min(cfg.k, pool) + cfg.W
+    attn = layers * B * (rows * cfg.d * ab + 2 * cfg.H * cfg.d * ab)
+    return {"scan_bytes": scan, "rescore_bytes": rescore, "attention_bytes": attn,
+            "bytes": scan + rescore + attn, "bytes_without_scan": rescore + attn,
+            "scan_flops": 2 * indexer_macs(cfg.HI, cfg.dI, nv) * B}

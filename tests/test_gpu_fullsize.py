@@ -1,0 +1,125 @@
+"""Parity at the benchmark's full sizes, through the benchmark's own step functions.
+
+The workloads are built by bench.py's workload classes and run as a CUDA-graph replay of
+their step, exactly as the benchmark times them, then checked against the oracle:
+  decode @64K (batch 16, bf16 keys) and @1M (batch 4, FP8 keys): every sequence;
+  prefill chunk (4,096 queries after 131,072 tokens): all 1,024 new entries of both caches,
+  and indexer scores / top-k / attention on sampled query rows (first and last included);
+  CSA2 decoder group at 262,144 tokens (batch 8): every sequence through all four layers.
+Agreement criteria are those of the small-size parity tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_csa_gb300 as csa
+from _helpers import (assert_decode_matches, assert_entries_close, assert_out_close_with_swaps, assert_pool_valid,
+                      assert_scores_close, assert_selection_ok, np64, oracle_decode, swap_bound)
+from bench import Csa2Group, Decode, Prefill
+from oracle import csa_oracle as O
+from synth import gen
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = torch.device("cuda", 0)
+
+
+def replay_once(fn):
+    fn()                       # first call allocates the workspace outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    assert csa.get_last_error() == 0
+
+
+def host(x):
+    return np64(x) if x.is_floating_point() else x.cpu().numpy()
+
+
+@pytest.mark.parametrize("cid", [2, 4])
+def test_decode_full_size(cid):
+    cfg = gen.CONFIGS[cid]
+    wl = Decode(cfg, csa, torch, DEV, 0)
+    ref = oracle_decode(cfg, wl.inp)          # reads the caches before the step writes entry E-1
+    replay_once(wl.step)
+    assert_decode_matches(cfg, wl.inp, ref, wl.out, wl.lse, wl.idx)
+
+
+def test_prefill_full_size_sampled_rows():
+    cfg = gen.CONFIGS[3]
+    wl = Prefill(cfg, csa, torch, DEV, 0)
+    inp = wl.inp
+    h = {k: host(v if k in ("bias", "biasI", "sink", "q_pos") else v[0:1]) for k, v in inp.items()}
+    kv_o, kI_o = h["kv_comp"][0].copy(), h["kI"][0].copy()
+    replay_once(wl.step)
+
+    # the chunk's compression: every new entry of both caches
+    new_kv = O.compress_range(h["kv_str"][0], h["z_str"][0], h["bias"], cfg.m, wl.e0, wl.e1, tok0=wl.tok0)
+    new_kI = O.compress_range(h["kvI_str"][0], h["zI_str"][0], h["biasI"], cfg.m, wl.e0, wl.e1, tok0=wl.tok0)
+    assert_entries_close(np64(inp["kv_comp"][0, wl.e0:wl.e1]), new_kv, h["kv_str"])
+    assert_entries_close(np64(inp["kI"][0, wl.e0:wl.e1]), new_kI, h["kvI_str"])
+    kv_o[wl.e0:wl.e1] = new_kv
+    kI_o[wl.e0:wl.e1] = new_kI
+
+    rng = np.random.default_rng(3)
+    rows = sorted(set([0, 1, 2, 3, 4, 1023, 2048, 3071, 4092, 4093, 4094, 4095] +
+                      rng.integers(0, cfg.T, 12).tolist()))
+    sub = cfg.replace(B=1)
+    scores = wl.scores
+    for tq in rows:
+        r = O.decode_token(sub, h, 0, tq, kv_o, kI_o)
+        nv = r["nv"]
+        got_s = np64(scores[tq])
+        assert_scores_close(got_s[:nv], r["scores"][:nv], 1e-2, what=f"scores row {tq}")
+        assert np.all(np.isneginf(got_s[nv:])), f"row {tq}: invisible entries must be -inf"
+        fin = r["scores"][:nv]
+        tol = 1e-2 * np.sqrt((fin ** 2).mean())
+        gi = wl.idx[tq].cpu().numpy()
+        swaps = assert_selection_ok(gi, r["idx"], r["scores"], cfg.k, tol)
+        g_set, r_set = set(gi[gi >= 0].tolist()), set(r["idx"][r["idx"] >= 0].tolist())
+        bound = swap_bound(h["q"][0, tq], r["lse"], cfg.softmax_scale, [kv_o[x] for x in g_set - r_set],
+                           [kv_o[y] for y in r_set - g_set])
+        assert_out_close_with_swaps(np64(wl.out[0, tq]), r["out"], 2e-2, bound, what=f"out row {tq} swaps={swaps}")
+        np.testing.assert_allclose(np64(wl.lse[0, tq]), r["lse"], atol=5e-3)
+
+
+def test_csa2_group_full_size():
+    cfg = gen.CONFIGS[5]
+    wl = Csa2Group(cfg, csa, torch, DEV, 0)
+    inp = wl.inp
+    replay_once(wl.step)
+    for b in range(cfg.B):
+        h = {}
+        for k, v in inp.items():
+            if k in ("q", "kv_local"):
+                h[k] = host(v[:, b])
+            elif k == "sink":
+                h[k] = host(v)
+            else:
+                h[k] = host(v[b])
+        t = int(h["q_pos"])
+        nv = min(t + 1, cfg.E)
+        sf64 = O.indexer_scores(h["qI_full"][0], h["w_full"][0], h["kI"], nv)
+        assert_scores_close(np64(wl.s_full[b])[:nv], sf64[:nv], 1e-2, what=f"full scan b={b}")
+        # The GPU pool comes from the GPU's scan scores: it must be one of the pools that
+        # scores within tolerance of the oracle's give (membership differs only at near-tied
+        # block maxima).  The Reindex step is then checked on that validated pool.
+        gpool = wl.pool[b, :int(wl.cnt[b])].cpu().numpy().astype(np.int64)
+        tol_scan = 1e-2 * np.sqrt((sf64[:nv] ** 2).mean())
+        assert_pool_valid(gpool, sf64.astype(np.float32), nv, 8, wl.N_BLOCKS, tol_scan)
+        all_rei = O.indexer_scores(h["qI"][0], h["w"][0], h["kI"], nv)
+        slots = O.topk(all_rei[gpool].astype(np.float32), gpool.size, cfg.k)
+        ridx = np.where(slots >= 0, gpool[np.maximum(slots, 0)], -1)
+        tol = 1e-2 * np.sqrt((all_rei[:nv] ** 2).mean())
+        gi = wl.idx[b].cpu().numpy()
+        assert_selection_ok(gi, ridx, all_rei, cfg.k, tol)
+        assert np.all(np.isin(gi[gi >= 0], gpool))
+        g_set, r_set = set(gi[gi >= 0].tolist()), set(ridx[ridx >= 0].tolist())
+        for layer in range(wl.layers):
+            rows = O.gather_rows(h["kv_comp"], ridx, h["kv_local"][layer], int(h["local_base"]), t, cfg.W)
+            ro, rl = O.sparse_attention(h["q"][layer][0], rows, h["sink"][layer], cfg.softmax_scale)
+            bound = swap_bound(h["q"][layer][0], rl, cfg.softmax_scale, [h["kv_comp"][x] for x in g_set - r_set],
+                               [h["kv_comp"][y] for y in r_set - g_set])
+            assert_out_close_with_swaps(np64(wl.outs[layer, b, 0]), ro, 2e-2, bound, what=f"layer {layer} b={b}")

@@ -14,7 +14,8 @@ import torch
 
 import compressed_sparse_attention_csa_gb300 as csa
 from _helpers import (assert_out_close_with_swaps, assert_rows_close, assert_scores_close, assert_selection_ok,
-                      keys_f64, lib_config, np64, swap_bound)
+                      keys_f64, lib_config, np64, np_inputs, oracle_decode, run_gpu_decode, swap_bound,
+                      assert_decode_matches, assert_entries_close, assert_pool_valid)
 from oracle import csa_oracle as O
 from synth import gen
 
@@ -70,7 +71,7 @@ def test_compress_bf16_range_and_e4m3():
     assert np.all(o[:, :e0] == 7.0) and np.all(o[:, e1:] == 7.0)
     for b in range(B):
         ref = O.compress_range(np64(kv[b]), np64(z[b]), np64(bias), m, e0, e1, tok0=tok0)
-        assert np.all(np.abs(o[b, e0:e1] - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-9)
+        assert_entries_close(o[b, e0:e1], ref, np64(kv[b]))
         ref32 = ref.astype(np.float32)
         rc, rs = O.quantize_rows_e4m3(ref32)
         gs = scale[b, e0:e1].cpu().numpy()
@@ -298,69 +299,17 @@ def test_attention_cuda_core_fp32():
 
 # ------------------------------------------------------------------ compositions
 
-def _np_inputs(inp):
-    out = {}
-    for k_, v in inp.items():
-        if v.dtype in (torch.float32, torch.bfloat16):
-            out[k_] = np64(v)
-        else:
-            out[k_] = v.cpu().numpy()
-    return out
-
-
-def _oracle_decode(cfg, inp):
-    """The oracle's decode step for every sequence of the batch."""
-    nb = _np_inputs(inp)
-    fp8 = cfg.kidx == "fp8"
-    res = []
-    for b in range(cfg.B):
-        kdeq = keys_f64(inp["kI"][b], inp["kscale"][b] if fp8 else None)
-        kvc = nb["kv_comp"][b].copy()
-        r = O.decode_step_sequence(cfg, nb, b, kvc, kdeq, fp8_keys=fp8)
-        r["kv_comp"] = kvc
-        r["q"] = nb["q"][b, 0]
-        res.append(r)
-    return res
-
-
-def _run_gpu_decode(cfg, inp):
-    c = lib_config(cfg)
-    out = torch.empty(cfg.B, cfg.H, cfg.d, device=DEV, dtype=cfg.torch_act)
-    lse = torch.empty(cfg.B, cfg.H, device=DEV)
-    idx = torch.empty(cfg.B, cfg.k, dtype=torch.int32, device=DEV)
-    csa.decode_step(c, q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"],
-                    kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
-                    z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
-                    biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse,
-                    idx_out=idx)
-    check_dev_error()
-    return out, lse, idx
-
-
 @pytest.mark.parametrize("cid,N", [(2, 4 * 1500), (4, 4 * 2500)])
 def test_decode_step_matches_oracle(cid, N):
     cfg = gen.CONFIGS[cid].replace(B=3, N=N)
     inp = gen.make_inputs(cfg, DEV)
     inp["q_pos"][1] = N - 3          # this token completes no block: no compression
     kv_before = inp["kv_comp"].clone()
-    ref = _oracle_decode(cfg, inp)   # oracle reads the inputs before the step mutates the caches
-    out, lse, idx = _run_gpu_decode(cfg, inp)
-    rtol_s = 5e-2 if cfg.kidx == "fp8" else 1e-2
+    ref = oracle_decode(cfg, inp)   # oracle reads the inputs before the step mutates the caches
+    out, lse, idx = run_gpu_decode(cfg, inp)
+    assert_decode_matches(cfg, inp, ref, out, lse, idx)
     for b in range(cfg.B):
-        r = ref[b]
-        fin = r["scores"][np.isfinite(r["scores"])]
-        tol = rtol_s * max(np.sqrt((fin ** 2).mean()), 1e-30)
-        gi = idx[b].cpu().numpy()
-        swaps = assert_selection_ok(gi, r["idx"], r["scores"], cfg.k, tol)
-        g_set, r_set = set(gi[gi >= 0].tolist()), set(r["idx"][r["idx"] >= 0].tolist())
-        bound = swap_bound(r["q"], r["lse"], cfg.softmax_scale, [r["kv_comp"][x] for x in g_set - r_set],
-                           [r["kv_comp"][y] for y in r_set - g_set])
-        assert_out_close_with_swaps(np64(out[b]), r["out"], 2e-2, bound, what=f"out b={b} swaps={swaps}")
-        np.testing.assert_allclose(np64(lse[b]), r["lse"], atol=5e-3)
-        if r["entry"] is not None:
-            e, ent, _ = r["entry"]
-            assert np.all(np.abs(np64(inp["kv_comp"][b, e]) - ent) <= 2.0 ** -8 * np.abs(ent) + 1e-9)
-        else:
+        if ref[b]["entry"] is None:
             assert torch.equal(inp["kv_comp"][b], kv_before[b])
 
 
@@ -383,7 +332,7 @@ def test_tiny_end_to_end_fp32():
     lse = torch.empty(cfg.B, cfg.T, cfg.H, device=DEV)
     csa.sparse_attn(c, inp["q"], kvc, idx, inp["kv_local"], inp["local_base"], inp["q_pos"], inp["sink"], out, lse)
     check_dev_error()
-    nb = _np_inputs(inp)
+    nb = np_inputs(inp)
     kv_ref = O.compress_range(nb["kv_str"][0], nb["z_str"][0], nb["bias"], cfg.m, 0, cfg.E)
     ki_ref = O.compress_range(nb["kvI_str"][0], nb["zI_str"][0], nb["biasI"], cfg.m, 0, cfg.E)
     for tq in range(cfg.T):
@@ -420,15 +369,17 @@ def test_csa2_group_matches_oracle():
                         inp["q_pos"], inp["sink"][layer], o)
         outs.append(o)
     check_dev_error()
-    nb = _np_inputs(inp)
+    nb = np_inputs(inp)
     for b in range(B):
         t = int(nb["q_pos"][b])
         nv = min(t + 1, E)
-        sf = O.indexer_scores(nb["qI_full"][b, 0], nb["w_full"][b, 0], nb["kI"][b], nv).astype(np.float32)
-        rpool = O.hier_pool(sf, nv, 8, n_blocks)
-        srei = O.indexer_scores_subset(nb["qI"][b, 0], nb["w"][b, 0], nb["kI"][b], rpool)
-        slots = O.topk(srei.astype(np.float32), rpool.size, cfg.k)
-        ridx = np.where(slots >= 0, rpool[np.maximum(slots, 0)], -1)
+        sf64 = O.indexer_scores(nb["qI_full"][b, 0], nb["w_full"][b, 0], nb["kI"][b], nv)
+        gpool = pool[b, :int(cnt[b])].cpu().numpy().astype(np.int64)
+        tol_scan = 1e-2 * np.sqrt((sf64[:nv] ** 2).mean())
+        assert_pool_valid(gpool, sf64.astype(np.float32), nv, 8, n_blocks, tol_scan)
+        srei = O.indexer_scores_subset(nb["qI"][b, 0], nb["w"][b, 0], nb["kI"][b], gpool)
+        slots = O.topk(srei.astype(np.float32), gpool.size, cfg.k)
+        ridx = np.where(slots >= 0, gpool[np.maximum(slots, 0)], -1)
         all_rei = O.indexer_scores(nb["qI"][b, 0], nb["w"][b, 0], nb["kI"][b], nv)
         tol = 1e-2 * np.sqrt((all_rei[:nv] ** 2).mean())
         gi = idx[b].cpu().numpy()
