@@ -13,12 +13,14 @@ chunk (4,096 new queries after 131,072 tokens: compression of the chunk, indexer
 attention for every query); 5 = CSA2 decoder group at 262,144 tokens (Full-layer indexer
 scan, block pool, Reindex rescoring, top-k, four attentions), also timed without the scan.
 
-Timing: W warm-up steps, then K timed steps, each a CUDA-graph replay of the step's library
-calls bracketed by CUDA events on the launching stream; L2 is flushed (512 MiB written)
-before every step, outside the events.  `value` uses inputs resident in HBM; `e2e` calls
-the public API eagerly and adds, every step, the pinned-host -> device copy of the step's
-inputs and the device -> host copy of its output.  The dominant kernel stage is timed the
-same way on its own for the roofline entry.
+Timing: the workload is built R times (independent copies, like the caches of R layers) so
+that stepping the copies in rotation keeps every step's inputs out of L2.  W warm-up steps,
+then K timed steps: CUDA-graph replays of the step's library calls, back to back between one
+pair of CUDA events on the launching stream.  `value` uses inputs resident in HBM;
+`flushed_step` times one copy's step alone after a 512 MiB L2 flush, one event pair per step;
+`e2e` calls the public API eagerly and adds, every step, the pinned-host -> device copy of
+the step's inputs and the device -> host copy of its output.  The dominant kernel stage is
+timed in the same rotation on its own for the roofline entry.
 
 `--impl reference` times the CPU oracle (oracle/csa_oracle.py, float64 numpy) on a bounded
 sample of the same workload on the host cores.  Multi-GPU (torchrun): every rank runs its
@@ -39,6 +41,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20
+
+
+def copies_for(touched_bytes):
+    """Copies to rotate so that more than twice the L2 of other data passes between two
+    steps on the same copy."""
+    import math
+    return max(2, math.ceil(2 * L2_BYTES / max(touched_bytes, 1)) + 1)
 REFERENCE_BUDGET_S = 120.0
 
 
@@ -214,6 +224,7 @@ class Decode:
         self.stage_bound = "hbm"
         self.stage_amount = work["indexer_bytes"] + cfg.B * cfg.E * 4   # + the fp32 scores written
         self.step_bytes = work["bytes"]
+        self.touched_bytes = work["bytes"] + cfg.B * cfg.E * 4
         self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str",
                                             "kv_local"]}
         self.e2e_out = self.out
@@ -290,6 +301,7 @@ class Prefill:
         self.stage_bound = "tensor"
         self.stage_amount = work["indexer_flops"]
         self.step_flops = work["flops"]
+        self.touched_bytes = work["bytes"] + B * T * E * 4
         self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str",
                                             "kv_local"]}
         self.e2e_out = self.out
@@ -373,6 +385,7 @@ class Csa2Group:
         self.stage_bound = "hbm"
         self.stage_amount = work["scan_bytes"] + B * E * 4
         self.step_bytes = work["bytes"]
+        self.touched_bytes = work["bytes"] + B * E * 4
         self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "qI_full", "w_full", "q_pos", "kv_local"]}
         self.e2e_out = self.outs
 
@@ -435,8 +448,8 @@ WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group}
 def config_of(wl):
     """The JSON line's `config` (identical for both arms)."""
     return dict(workload=wl.workload, **wl.config_extra,
-                l2="flushed (512 MiB write) before every timed step",
-                timing="device time per step: CUDA events around a CUDA-graph replay")
+                l2="inputs larger than L2: independent copies of the workload stepped in rotation",
+                timing="K steps replayed back to back as CUDA graphs between one pair of CUDA events")
 DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6}
 
 
@@ -497,7 +510,6 @@ def main():
     row0, n_rows = shard_rows(cfg.B * world, world, rank)
     assert n_rows == cfg.B
     wl = Wl(cfg, csa, torch, dev, row0)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream(dev)
 
     if args.only:
@@ -514,15 +526,21 @@ def main():
                           "ms_per_call_back_to_back": 1e3 * (time.perf_counter() - t0) / max(args.steps, 1)}))
         return
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        wl.step()
+    # Inputs larger than L2: R independent copies of the workload (like the caches of R
+    # layers) are stepped in rotation, so the data a step reads was last touched R - 1 steps
+    # earlier, with more than twice the L2 of other traffic in between.
+    R = copies_for(wl.touched_bytes)
+    wls = [wl] + [Wl(cfg, csa, torch, dev, row0) for _ in range(R - 1)]
+    for w in wls:
+        for _ in range(max(1, args.warmup // R)):
+            w.step()
     torch.cuda.synchronize(dev)
     assert csa.get_last_error() == 0
 
-    # Each timed function is captured once into a CUDA graph (the library's launches are
-    # stream-ordered and allocate nothing once the workspace exists) and replayed: the device
-    # time then does not depend on how fast the host enqueues the launches.
+    # Each timed function is captured once per copy into a CUDA graph (the library's launches
+    # are stream-ordered and allocate nothing once the workspace exists); the graphs are
+    # replayed back to back between one pair of CUDA events, so the host stays ahead of the
+    # device and the time is the device's.
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -530,23 +548,19 @@ def main():
         torch.cuda.synchronize(dev)
         return g
 
-    def time_graph(g, n):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    def time_rotation(gs, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
         for i in range(n):
-            flush.zero_()
-            ev[i][0].record(stream)
-            g.replay()
-            ev[i][1].record(stream)
+            gs[i % len(gs)].replay()
+        e1.record(stream)
         torch.cuda.synchronize(dev)
-        return sum(a.elapsed_time(b) for a, b in ev)
+        return e0.elapsed_time(e1)
 
     n_cap = csa.launch_count()
-    g_step = capture(wl.step)
-    launches_per_step = csa.launch_count() - n_cap
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        g_step.replay()
-    torch.cuda.synchronize(dev)
+    g_steps = [capture(w.step) for w in wls]
+    launches_per_step = (csa.launch_count() - n_cap) // R
+    time_rotation(g_steps, max(3, args.warmup))
     assert csa.get_last_error() == 0
 
     gpu_id = "0"
@@ -561,7 +575,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    total_ms = time_graph(g_step, K)
+    total_ms = time_rotation(g_steps, K)
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
@@ -573,13 +587,25 @@ def main():
     value = wl.units * K * world / (total_ms / 1e3)
     ms_per_step = total_ms / K
 
-    # ---- dominant kernel stage alone, same inputs and launch configuration
-    wl.stage_fn()
-    g_stage = capture(wl.stage_fn)
-    for _ in range(3):
-        g_stage.replay()
-    Ki = max(3, min(K, 200))
-    stage_ms = max_over_ranks(time_graph(g_stage, Ki) / Ki)
+    # ---- the same step timed alone: L2 flushed (512 MiB written) before each step, one event
+    #      pair per step (includes the device-side cost of starting a graph from idle)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    Kf = max(3, min(K, 500))
+    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kf)]
+    for i in range(Kf):
+        flush.zero_()
+        evf[i][0].record(stream)
+        g_steps[0].replay()
+        evf[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    flushed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evf) / Kf)
+    del flush
+
+    # ---- dominant kernel stage alone, same inputs and launch configuration, same rotation
+    g_stages = [capture(w.stage_fn) for w in wls]
+    time_rotation(g_stages, 3 * R)
+    Ki = max(3, min(K, 500))
+    stage_ms = max_over_ranks(time_rotation(g_stages, Ki) / Ki)
     hbm, bf16, bf16_sus, peak_kind = peaks()
     if wl.stage_bound == "hbm":
         achieved = wl.stage_amount / (stage_ms / 1e3) / 1e9
@@ -595,16 +621,17 @@ def main():
                 "peak_kind": pk, "amount_per_launch": wl.stage_amount, "launch_us": round(stage_ms * 1e3, 2)}
     roofline.update(step_frac)
 
-    extra = {}
+    extra = {"flushed_step": {"ms_per_step": round(flushed_ms, 5),
+                              "value": round(wl.units * world / (flushed_ms / 1e3), 1)}}
     if isinstance(wl, Csa2Group):
-        g_ns = capture(wl.step_without_scan)
-        for _ in range(3):
-            g_ns.replay()
-        ns_ms = max_over_ranks(time_graph(g_ns, K) / K)
+        g_ns = [capture(w.step_without_scan) for w in wls]
+        time_rotation(g_ns, 3 * R)
+        ns_ms = max_over_ranks(time_rotation(g_ns, K) / K)
         extra["without_scan"] = {"value": round(wl.units * world / (ns_ms / 1e3), 1), "ms_per_step": round(ns_ms, 5),
                                  "frac_of_hbm": round(wl.work["bytes_without_scan"] / (ns_ms / 1e3) / 1e9 / hbm, 4)}
 
-    # ---- end to end: the public API with host buffers, copies inside the timed region
+    # ---- end to end: the public API called eagerly with host buffers; every step copies its
+    #      inputs in from pinned host memory and its output back, inside its own event pair
     host_in = {k: v.cpu().pin_memory() for k, v in wl.e2e_in.items()}
     host_out = torch.empty(wl.e2e_out.shape, dtype=wl.e2e_out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
@@ -612,12 +639,12 @@ def main():
     Ke = max(3, min(K, 500))
     eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     for i in range(Ke):
-        flush.zero_()
+        w = wls[i % R]
         eve[i][0].record(stream)
         for k, v in host_in.items():
-            wl.e2e_in[k].copy_(v, non_blocking=True)
-        wl.step()
-        host_out.copy_(wl.e2e_out, non_blocking=True)
+            w.e2e_in[k].copy_(v, non_blocking=True)
+        w.step()
+        host_out.copy_(w.e2e_out, non_blocking=True)
         eve[i][1].record(stream)
     torch.cuda.synchronize(dev)
     assert csa.get_last_error() == 0

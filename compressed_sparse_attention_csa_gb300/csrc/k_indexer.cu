@@ -129,7 +129,8 @@ __device__ __forceinline__ float relu_dot32(const float (&v)[32], const float* w
 
 // Query operand of every query group, written once as the CTA's shared-memory image:
 // [b_bytes: B operand, 128B-swizzled K-major][w_bytes: gates (x per-head scale for e4m3)].
-// One CTA per (query group, sequence); one warp per query row.
+// Grid (query group, sequence, row block of 8): one warp per (query, head) row, so every
+// row's load is issued at once instead of one after another.
 template <bool FP8>
 __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a, const TcLayout L,
                                                             uint8_t* images) {
@@ -143,7 +144,9 @@ __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a,
   float* wimg = reinterpret_cast<float*>(img + L.b_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-  for (int gh = warp; gh < N; gh += 8) {
+  {
+    const int gh = blockIdx.z * 8 + warp;
+    if (gh >= N) return;
     const int g = gh / HI, h = gh - g * HI;
     const bool valid = g0 + g < T;
     if constexpr (!FP8) {
@@ -467,7 +470,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
                         fp8 ? 128 : 64, kTile))
       return cudaErrorInvalidValue;
     uint8_t* images = static_cast<uint8_t*>(a.ws);
-    dim3 gq(L.n_qgroups, a.B);
+    dim3 gq(L.n_qgroups, a.B, (L.N + 7) / 8);
     cudaError_t e = fp8 ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
                         : launch_pdl(indexer_qprep_kernel<false>, gq, dim3(256), 0, s, a, L, images);
     count_launches(1);
