@@ -141,7 +141,7 @@ size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
   bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
   bytes += align_up(static_cast<size_t>(B) * (kTopkHistRowWords + 1) * 4, 256);  // histograms + counters
-  bytes += align_up(std::max(topk_workspace_bytes(B, E_cap, c->k, sms), topk_hist_workspace_bytes(B, c->k)), 256);
+  bytes += align_up(std::max(topk_workspace_bytes(B, E_cap, c->k, sms), topk_hist_workspace_bytes(B, E_cap)), 256);
   bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms), 256);
   return bytes;
 }
@@ -427,28 +427,13 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(p);
   p += align_up(static_cast<size_t>(cfg->B) * (kTopkHistRowWords + 1) * 4, 256);
   const size_t topk_ws =
-      std::max(topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms), topk_hist_workspace_bytes(cfg->B, cfg->k));
+      std::max(topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms), topk_hist_workspace_bytes(cfg->B, d->E_cap));
   void* ws_topk = p;
   p += align_up(topk_ws, 256);
   void* ws_attn = p;
   if (d->idx_out) idx = d->idx_out;
 
-  // 1. compress the block the new token completes (main KV, then indexer keys)
-  CompressArgs c{};
-  c.B = cfg->B;
-  c.m = cfg->m;
-  c.act_bf16 = cfg->act == CSA_BF16;
-  c.q_pos = d->q_pos;
-  c.E_cap = d->E_cap;
-  c.err = err;
-  c.job[0] = CompressJob{d->kv_tail, d->z_tail, d->bias, cfg->d, d->kv_comp, cfg->act, nullptr};
-  c.job[1] = CompressJob{d->kvI_tail, d->zI_tail, d->biasI, cfg->dI, d->kI, cfg->kidx, d->kscale};
-  c.n_jobs = 2;
-  c.zero_hist = hist_cnt;
-  cudaError_t e = launch_compress(c, s);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-
-  // 2. indexer over the visible entries (the tensor-core path also histograms the scores)
+  // indexer over the visible entries (the tensor-core path also histograms the scores)
   IndexerArgs ia{};
   ia.qI = d->qI;
   ia.w = d->w;
@@ -471,6 +456,35 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   ia.ws = q_images;
   const bool hist_topk = indexer_uses_tensor_cores(ia);
   ia.hist_out = hist_topk ? hist_cnt : nullptr;
+
+  // 1. compress the block the new token completes (main KV, then indexer keys); on the
+  //    tensor-core path the same launch writes the indexer's query images
+  CompressArgs c{};
+  c.B = cfg->B;
+  c.m = cfg->m;
+  c.act_bf16 = cfg->act == CSA_BF16;
+  c.q_pos = d->q_pos;
+  c.E_cap = d->E_cap;
+  c.err = err;
+  c.job[0] = CompressJob{d->kv_tail, d->z_tail, d->bias, cfg->d, d->kv_comp, cfg->act, nullptr};
+  c.job[1] = CompressJob{d->kvI_tail, d->zI_tail, d->biasI, cfg->dI, d->kI, cfg->kidx, d->kscale};
+  c.n_jobs = 2;
+  c.zero_hist = hist_cnt;
+  cudaError_t e;
+  if (hist_topk) {
+    QprepPart qp{};
+    qp.ia = ia;
+    qp.L = indexer_layout(ia);
+    qp.images = static_cast<uint8_t*>(q_images);
+    qp.fp8 = cfg->kidx == CSA_E4M3;
+    e = launch_compress_with_qprep(c, qp, s);
+    ia.images_ready = true;
+  } else {
+    e = launch_compress(c, s);
+  }
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+
+  // 2. indexer
   e = launch_indexer(ia, s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
 

@@ -32,6 +32,9 @@ struct CompressArgs {
   int* err;
   uint32_t* zero_hist;  // decode step: per-sequence top-k histogram rows [B, 4096] and the B
                         // candidate counters after them, zeroed here before the indexer runs
+  // decode step: the indexer's query images are prepared in the same launch (extra CTAs
+  // along z after the compression jobs); qp_ctas = 0 disables it
+  int qp_ctas;
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 
@@ -56,10 +59,37 @@ struct IndexerArgs {
   uint32_t* hist_out;    // [B*T, 4160] digit histogram of the visible scores (one query per CTA
                          // only), accumulated with atomics; null = none
   void* ws;              // tensor-core path: query images (indexer_workspace_bytes)
+  bool images_ready;     // the query images in ws were already written (fused decode prep)
 };
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
 bool indexer_uses_tensor_cores(const IndexerArgs& a);
 size_t indexer_workspace_bytes(const IndexerArgs& a);
+
+// Tensor-core indexer plan (see k_indexer.cu).
+struct IndexerLayout {
+  int G;               // queries per CTA
+  int N;               // MMA N = G * HI
+  int stages;
+  uint32_t b_bytes;    // B operand image (bf16 rows, or e4m3 hi + lo regions), 1024-aligned
+  uint32_t w_bytes;    // gate vector image (G*HI fp32), 16-aligned
+  uint32_t stage_bytes;
+  uint32_t smem_bytes;
+  uint32_t tmem_cols;
+  int n_acc;           // TMEM accumulators in the MMA -> epilogue ring (2..4)
+  int n_splits;        // key-range splits per (sequence, query group)
+  int n_qgroups;
+};
+IndexerLayout indexer_layout(const IndexerArgs& a);
+
+// The compressor launch of the decode step also writes the indexer's query images: the
+// arguments of that part (set by the caller with qp_ctas > 0 in CompressArgs).
+struct QprepPart {
+  IndexerArgs ia;
+  IndexerLayout L;
+  uint8_t* images;
+  bool fp8;
+};
+cudaError_t launch_compress_with_qprep(const CompressArgs& a, const QprepPart& q, cudaStream_t s);
 
 // ---- top-k ------------------------------------------------------------------------
 struct TopkArgs {
@@ -78,15 +108,15 @@ size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 
 // Histogram-guided top-k for a few long rows.  hist_cnt holds, per row, 4096 fine digit
-// counts (key >> 20) and 64 coarse counts (key >> 26), then one candidate counter per row;
-// all zero before the histogram is filled.
+// counts (key >> 20) and 64 coarse counts (key >> 26), then one ticket word per row; all
+// zero before the histogram is filled.
 constexpr int kTopkHistBins = 4096;
 constexpr int kTopkHistCoarse = 64;
 constexpr int kTopkHistRowWords = kTopkHistBins + kTopkHistCoarse;
 int topk_hist_cap(int k);
-size_t topk_hist_workspace_bytes(int64_t rows, int k);  // the candidate lists (ws_cand)
+size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols);  // the candidate slots (ws_cand)
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);
-size_t topk_hist_standalone_bytes(int64_t rows, int k);
+size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols);
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s);

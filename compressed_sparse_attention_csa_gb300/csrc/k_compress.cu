@@ -10,9 +10,11 @@
 // Bandwidth/latency-bound: one CTA per (entry, sequence, job) where a job is one cache (main
 // KV or indexer keys, both in one launch); one thread per channel; the 2m gate and value
 // loads of a channel are issued before any arithmetic.  fp32 math; an E4M3 output gets one
-// fp32 scale per entry (amax/448, codes rounded to nearest, saturating).
+// fp32 scale per entry (amax/448, codes rounded to nearest, saturating).  In the decode step
+// the same launch carries extra CTAs that write the indexer's query images (qprep_dev.cuh).
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
+#include "qprep_dev.cuh"
 
 namespace csa {
 namespace {
@@ -20,50 +22,74 @@ namespace {
 constexpr int kMaxTok = 32;  // 2m <= 32
 
 template <typename T>
-__global__ void __launch_bounds__(512) compress_kernel(CompressArgs a) {
-  pdl_wait();  // the caches and histograms may still be read by the previous step
+__global__ void __launch_bounds__(512) compress_kernel(CompressArgs a, QprepPart qp) {
+  pdl_wait();  // the caches, images and histograms may still be read by the previous step
   pdl_trigger();
-  const CompressJob& job = a.job[blockIdx.z];
   const int b = blockIdx.y;
+  if (static_cast<int>(blockIdx.z) >= a.n_jobs) {
+    // decode step: the indexer's query images, one (query, head) row per warp
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    const int gh = (static_cast<int>(blockIdx.z) - a.n_jobs) * nw + static_cast<int>(threadIdx.x >> 5);
+    if (gh < qp.L.N) {
+      if (qp.fp8)
+        qprep_row<true>(qp.ia, qp.L, qp.images, 0, b, gh, threadIdx.x & 31);
+      else
+        qprep_row<false>(qp.ia, qp.L, qp.images, 0, b, gh, threadIdx.x & 31);
+    }
+    return;
+  }
+  const CompressJob& job = a.job[blockIdx.z];
   const int m = a.m;
   if (a.zero_hist && blockIdx.x == 0 && blockIdx.z == 0) {
     for (int i = threadIdx.x; i < kTopkHistRowWords; i += blockDim.x)
       a.zero_hist[static_cast<int64_t>(b) * kTopkHistRowWords + i] = 0u;
     if (threadIdx.x == 0) a.zero_hist[static_cast<int64_t>(a.B) * kTopkHistRowWords + b] = 0u;
   }
-  int64_t entry, tok0, n_tok;
+  // Stream rows of the two token blocks: stream a (current block) starts at row ra0, stream b
+  // (previous block) at row rb0.  Decode mode: the buffer holds tokens t-2m+1..t, so the rows
+  // are fixed (b: 0..m-1, a: m..2m-1) and every load is issued before q_pos is known.
+  int64_t entry = 0, ra0, rb0, n_tok;
+  bool b_ok;
   if (a.q_pos) {
-    const int64_t t = a.q_pos[b];
-    if ((t + 1) % m != 0) return;
-    entry = (t + 1) / m - 1;
-    tok0 = t - 2 * m + 1;
+    ra0 = m;
+    rb0 = 0;
     n_tok = 2 * m;
+    b_ok = true;
   } else {
     entry = a.ent_begin + blockIdx.x;
-    tok0 = a.tok0;
+    ra0 = m * entry - a.tok0;
+    rb0 = m * (entry - 1) - a.tok0;
     n_tok = a.n_tok;
+    b_ok = entry > 0;
   }
-  if (entry < 0 || entry >= a.E_cap) return;
   const int dim = job.dim;
   const int c = threadIdx.x;
   const T* kv = static_cast<const T*>(job.kv) + static_cast<int64_t>(b) * n_tok * 2 * dim;
   const T* z = static_cast<const T*>(job.z) + static_cast<int64_t>(b) * n_tok * 2 * dim;
-  const int nt = entry == 0 ? m : 2 * m;  // stream-a tokens first, then stream-b tokens
 
-  float v = 0.f;
+  float lg[kMaxTok], val[kMaxTok];
   if (c < dim) {
-    float lg[kMaxTok], val[kMaxTok];
 #pragma unroll
     for (int j = 0; j < kMaxTok; ++j) {
-      if (j < nt) {
+      if (j < 2 * m && (j < m || b_ok)) {
         const int st = j < m ? 0 : 1;
         const int jj = j < m ? j : j - m;
-        const int64_t tok = (st == 0 ? m * entry : m * (entry - 1)) + jj;
-        const int64_t off = ((tok - tok0) * 2 + st) * dim + c;
+        const int64_t off = (((st == 0 ? ra0 : rb0) + jj) * 2 + st) * dim + c;
         lg[j] = load_f<T>(z + off) + job.bias[(st * m + jj) * dim + c];
         val[j] = load_f<T>(kv + off);
       }
     }
+  }
+  if (a.q_pos) {
+    const int64_t t = a.q_pos[b];
+    if ((t + 1) % m != 0) return;
+    entry = (t + 1) / m - 1;
+  }
+  if (entry < 0 || entry >= a.E_cap) return;
+  const int nt = entry == 0 ? m : 2 * m;  // stream-a tokens first, then stream-b tokens
+
+  float v = 0.f;
+  if (c < dim) {
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kMaxTok; ++j)
@@ -101,18 +127,34 @@ __global__ void __launch_bounds__(512) compress_kernel(CompressArgs a) {
   }
 }
 
-}  // namespace
-
-cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
-  dim3 grid(a.q_pos ? 1 : static_cast<unsigned>(a.n_ent), a.B, a.n_jobs);
+cudaError_t launch_impl(const CompressArgs& a, const QprepPart& qp, int qp_ctas, cudaStream_t s) {
+  dim3 grid(a.q_pos ? 1 : static_cast<unsigned>(a.n_ent), a.B, a.n_jobs + qp_ctas);
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   int dmax = a.job[0].dim;
   if (a.n_jobs > 1 && a.job[1].dim > dmax) dmax = a.job[1].dim;
-  const int threads = (dmax + 31) / 32 * 32;
-  const cudaError_t e = a.act_bf16 ? launch_pdl(compress_kernel<__nv_bfloat16>, grid, dim3(threads), 0, s, a)
-                                   : launch_pdl(compress_kernel<float>, grid, dim3(threads), 0, s, a);
+  int threads = (dmax + 31) / 32 * 32;
+  if (qp_ctas > 0 && threads < 256) threads = 256;
+  const cudaError_t e = a.act_bf16 ? launch_pdl(compress_kernel<__nv_bfloat16>, grid, dim3(threads), 0, s, a, qp)
+                                   : launch_pdl(compress_kernel<float>, grid, dim3(threads), 0, s, a, qp);
   count_launches(1);
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
+  QprepPart none{};
+  return launch_impl(a, none, 0, s);
+}
+
+cudaError_t launch_compress_with_qprep(const CompressArgs& a, const QprepPart& q, cudaStream_t s) {
+  if (!a.q_pos || q.L.n_qgroups != 1) return cudaErrorInvalidValue;  // decode step only (T = 1)
+  int dmax = a.job[0].dim;
+  if (a.n_jobs > 1 && a.job[1].dim > dmax) dmax = a.job[1].dim;
+  int threads = (dmax + 31) / 32 * 32;
+  if (threads < 256) threads = 256;
+  const int nw = threads / 32;
+  return launch_impl(a, q, (q.L.N + nw - 1) / nw, s);
 }
 
 }  // namespace csa

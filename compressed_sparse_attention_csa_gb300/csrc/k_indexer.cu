@@ -23,6 +23,7 @@
 
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
+#include "qprep_dev.cuh"
 
 namespace csa {
 namespace {
@@ -81,19 +82,7 @@ constexpr int kTile = 128;                       // keys per tile (MMA M)
 constexpr int kMaxG = 8;
 constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
 
-struct TcLayout {
-  int G;               // queries per CTA
-  int N;               // MMA N = G * HI
-  int stages;
-  uint32_t b_bytes;    // B operand image (bf16 rows, or e4m3 hi + lo regions), 1024-aligned
-  uint32_t w_bytes;    // gate vector image (G*HI fp32), 16-aligned
-  uint32_t stage_bytes;
-  uint32_t smem_bytes;
-  uint32_t tmem_cols;
-  int n_acc;           // TMEM accumulators in the MMA -> epilogue ring (2..4)
-  int n_splits;        // key-range splits per (sequence, query group)
-  int n_qgroups;
-};
+using TcLayout = IndexerLayout;
 
 __device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -127,67 +116,16 @@ __device__ __forceinline__ float relu_dot32(const float (&v)[32], const float* w
   return (a0 + a1) + (a2 + a3);
 }
 
-// Query operand of every query group, written once as the CTA's shared-memory image:
-// [b_bytes: B operand, 128B-swizzled K-major][w_bytes: gates (x per-head scale for e4m3)].
-// Grid (query group, sequence, row block of 8): one warp per (query, head) row, so every
-// row's load is issued at once instead of one after another.
+// Query operand of every query group, written once as the CTA's shared-memory image
+// (qprep_row in qprep_dev.cuh).  Grid (query group, sequence, row block of 8): one warp per
+// (query, head) row, so every row's load is in flight at once.
 template <bool FP8>
 __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a, const TcLayout L,
                                                             uint8_t* images) {
   pdl_wait();  // the images may still be read by the previous indexer launch
   pdl_trigger();
-  const int HI = a.HI, G = L.G, N = L.N, T = a.T;
-  const int qg = blockIdx.x, b = blockIdx.y;
-  const int g0 = qg * G;
-  const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
-  uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
-  float* wimg = reinterpret_cast<float*>(img + L.b_bytes);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
-  {
-    const int gh = blockIdx.z * 8 + warp;
-    if (gh >= N) return;
-    const int g = gh / HI, h = gh - g * HI;
-    const bool valid = g0 + g < T;
-    if constexpr (!FP8) {
-      // 256-byte bf16 row: lane l copies 16-byte chunk l/2 ... as two regions of 64 elements
-      const int c = lane >> 1;  // 0..15
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (valid && (lane & 1) == 0)
-        v = *reinterpret_cast<const uint4*>(qI + ((qrow0 + g) * HI + h) * 128 + c * 8);
-      if ((lane & 1) == 0) *reinterpret_cast<uint4*>(img + (c >> 3) * (N * 128) + sw128(gh, c & 7)) = v;
-      if (lane == 0) wimg[gh] = valid ? a.w[(qrow0 + g) * HI + h] : 0.f;
-    } else {
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (valid) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(qI + ((qrow0 + g) * HI + h) * 128 + lane * 4);
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        x[0] = __low2float(p0);
-        x[1] = __high2float(p0);
-        x[2] = __low2float(p1);
-        x[3] = __high2float(p1);
-      }
-      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      const float sc = am > 0.f ? am / 448.f : 1.f;
-      const float inv = 1.f / sc;
-      uint32_t hi4 = 0u, lo4 = 0u;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float y = x[j] * inv;
-        const uint8_t ch = f_to_e4m3(y);
-        const uint8_t cl = f_to_e4m3(y - e4m3_to_f(ch));
-        hi4 |= static_cast<uint32_t>(ch) << (8 * j);
-        lo4 |= static_cast<uint32_t>(cl) << (8 * j);
-      }
-      const uint32_t off = sw128(gh, lane >> 2) + (lane & 3) * 4;
-      *reinterpret_cast<uint32_t*>(img + off) = hi4;
-      *reinterpret_cast<uint32_t*>(img + N * 128 + off) = lo4;
-      if (lane == 0) wimg[gh] = valid ? a.w[(qrow0 + g) * HI + h] * sc : 0.f;
-    }
-  }
+  const int gh = blockIdx.z * 8 + (threadIdx.x >> 5);
+  if (gh < L.N) qprep_row<FP8>(a, L, images, blockIdx.x, blockIdx.y, gh, threadIdx.x & 31);
 }
 
 // Warp 0: TMA producer.  Warp 1: TMEM owner and MMA issuer (it also pulls the query image).
@@ -446,6 +384,8 @@ TcLayout plan_tc(const IndexerArgs& a) {
 
 }  // namespace
 
+IndexerLayout indexer_layout(const IndexerArgs& a) { return plan_tc(a); }
+
 bool indexer_uses_tensor_cores(const IndexerArgs& a) {
   return a.cand == nullptr && a.act == CSA_BF16 && a.dI == 128 && (a.HI == 32 || a.HI == 64 || a.HI == 128) &&
          (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
@@ -470,11 +410,14 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
                         fp8 ? 128 : 64, kTile))
       return cudaErrorInvalidValue;
     uint8_t* images = static_cast<uint8_t*>(a.ws);
-    dim3 gq(L.n_qgroups, a.B, (L.N + 7) / 8);
-    cudaError_t e = fp8 ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
-                        : launch_pdl(indexer_qprep_kernel<false>, gq, dim3(256), 0, s, a, L, images);
-    count_launches(1);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!a.images_ready) {
+      dim3 gq(L.n_qgroups, a.B, (L.N + 7) / 8);
+      e = fp8 ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
+              : launch_pdl(indexer_qprep_kernel<false>, gq, dim3(256), 0, s, a, L, images);
+      count_launches(1);
+      if (e != cudaSuccess) return e;
+    }
     dim3 grid(L.n_splits, L.n_qgroups, a.B);
     static bool attr = false;
     if (!attr) {

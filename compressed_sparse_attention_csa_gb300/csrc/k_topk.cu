@@ -380,7 +380,7 @@ size_t levels_ws(const Plan& pl, int64_t rows, int k) {
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms) {
   const size_t lv = levels_ws(make_plan(rows, n_cols, k, num_sms), rows, k);
-  return topk_uses_hist(rows, n_cols, false) ? std::max(lv, topk_hist_standalone_bytes(rows, k)) : lv;
+  return topk_uses_hist(rows, n_cols, false) ? std::max(lv, topk_hist_standalone_bytes(rows, n_cols)) : lv;
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {

@@ -17,11 +17,15 @@
 //     (a bin full of ties) it selects over the whole row instead, in position order.
 #include <algorithm>
 
+#include <cooperative_groups.h>
+
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
 
 namespace csa {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int NT = 512;
 constexpr int kFine = kTopkHistBins;     // 4096
@@ -105,190 +109,60 @@ __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores
   }
 }
 
-__global__ void __launch_bounds__(NT) topk_filter_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                         int64_t n_cols, const uint32_t* hist, int k, uint32_t* cnt,
-                                                         uint32_t* ckey, int32_t* cpos, int cap, int chunk) {
-  __shared__ uint32_t s_b1;
-  pdl_wait();
-  pdl_trigger();
-  const int64_t row = blockIdx.y;
-  if (threadIdx.x < 32) {
-    const uint32_t b1 = threshold_digit(hist + row * kRowWords, k);
-    if (threadIdx.x == 0) s_b1 = b1;
-  }
-  __syncthreads();
-  const uint32_t b1 = s_b1;
-  const int64_t nv = row_valid(n_valid, row, n_cols);
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
-  const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
-  const int lane = threadIdx.x & 31;
-  for (int64_t base = c0; base < c1; base += NT) {
-    const int64_t s = base + threadIdx.x;
-    uint32_t key = 0u;
-    if (s < c1) {
-      key = f2key(scores[row * ld + s]);
-      if (key == 0u) key = 1u;
+// Largest-`want` selection among candidate values (block-wide, radix passes of up to 10
+// bits over the low `lo_bits` bits; the bits above are fixed to `prefix` under `mask`): on
+// return the `want` largest are every value > *T plus *quota values equal to *T.  The caller
+// guarantees at least `want` values match the fixed bits.
+template <typename F>
+__device__ void block_select_largest(F val, int n, int want, int lo_bits, uint32_t prefix, uint32_t mask,
+                                     uint32_t* hist, uint32_t* tmp, uint32_t* res, uint32_t* T, int* quota) {
+  int kk = want;
+  int shift = lo_bits;
+  while (shift > 0) {
+    const int wbits = shift < 10 ? shift : 10;
+    shift -= wbits;
+    const int nb = 1 << wbits;
+    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0u;
+    __syncthreads();
+    for (int e = threadIdx.x; e < n; e += NT) {
+      const uint32_t v = val(e);
+      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
     }
-    const bool take = s < c1 && (key >> 20) >= b1;
-    const uint32_t m = __ballot_sync(0xffffffffu, take);
-    if (m == 0u) continue;
-    uint32_t slot0 = 0;
-    if (lane == __ffs(m) - 1) slot0 = atomicAdd(&cnt[row], static_cast<uint32_t>(__popc(m)));
-    slot0 = __shfl_sync(0xffffffffu, slot0, __ffs(m) - 1);
-    if (take) {
-      const uint32_t slot = slot0 + __popc(m & lanemask_lt());
-      if (slot < static_cast<uint32_t>(cap)) {
-        ckey[row * cap + slot] = key;
-        cpos[row * cap + slot] = static_cast<int32_t>(s);
+    __syncthreads();
+    // thread t owns bins nb-1-2t and nb-2-2t (descending), so the exclusive scan counts from the top
+    uint32_t local = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int bin = nb - 1 - (2 * static_cast<int>(threadIdx.x) + q);
+      if (bin >= 0) local += hist[bin];
+    }
+    uint32_t run = block_exclusive_scan<NT>(local, tmp, nullptr);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int bin = nb - 1 - (2 * static_cast<int>(threadIdx.x) + q);
+      if (bin < 0) break;
+      const uint32_t h = hist[bin];
+      if (run < static_cast<uint32_t>(kk) && run + h >= static_cast<uint32_t>(kk)) {
+        res[0] = static_cast<uint32_t>(bin);
+        res[1] = run;
       }
+      run += h;
     }
+    __syncthreads();
+    kk -= static_cast<int>(res[1]);
+    prefix |= res[0] << shift;
+    mask |= static_cast<uint32_t>(nb - 1) << shift;
+    __syncthreads();
   }
+  *T = prefix;
+  *quota = kk;
 }
 
-// Items are (key, position) pairs: the candidate list in shared memory, or, on overflow, the
-// score row itself in position order.
-struct FinalItems {
-  const uint32_t* key;
-  const int32_t* pos;
-  const float* row;
-  int n;
-  bool from_row;
-  __device__ __forceinline__ uint32_t k_at(int e) const {
-    if (!from_row) return key[e];
-    const uint32_t x = f2key(row[e]);
-    return x == 0u ? 1u : x;
-  }
-  __device__ __forceinline__ int32_t p_at(int e) const { return from_row ? e : pos[e]; }
-};
-
-__global__ void __launch_bounds__(NT) topk_final_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                        int64_t n_cols, const uint32_t* cnt, const uint32_t* ckey,
-                                                        const int32_t* cpos, int cap, int k, int32_t* idx) {
-  extern __shared__ uint32_t sm[];
-  uint32_t* skey = sm;                                   // [cap]
-  int32_t* spos = reinterpret_cast<int32_t*>(sm + cap);  // [cap]
-  uint32_t* hist = sm + 2 * cap;                         // [2048] radix / [1024] sort buckets
-  uint32_t* tmp = hist + kRadixBins;                     // [32]
-  uint32_t* s_res = tmp + 32;                            // [8]
-  int32_t* sel = reinterpret_cast<int32_t*>(s_res + 8);  // [k]  winners (unordered)
-  int32_t* srt = sel + k;                                // [k]  winners grouped by bucket
-  int32_t* eqp = srt + k;                                // [cap] positions of keys equal to T
-  const int tid = threadIdx.x, lane = tid & 31;
-  pdl_wait();
-  pdl_trigger();
-  const int64_t row = blockIdx.x;
-  const int64_t nvr = row_valid(n_valid, row, n_cols);
-  const uint32_t n_cand = cnt[row];
-  FinalItems it;
-  it.from_row = n_cand > static_cast<uint32_t>(cap);
-  it.n = it.from_row ? static_cast<int>(nvr) : static_cast<int>(n_cand);
-  it.row = scores + row * ld;
-  it.key = skey;
-  it.pos = spos;
-  if (!it.from_row) {
-    for (int e = tid; e < it.n; e += NT) {
-      skey[e] = ckey[row * cap + e];
-      spos[e] = cpos[row * cap + e];
-    }
-  }
-  __syncthreads();
-
-  // ---- exact k-th key: three radix passes (11/11/10 bits)
-  uint32_t T = 1u;
-  int quota = 0x7fffffff;
-  if (it.n > k) {
-    uint32_t prefix = 0u, mask = 0u;
-    int kk = k;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = shifts[pass], nb = 1 << widths[pass];
-      for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-      __syncthreads();
-      for (int base = 0; base < it.n; base += NT) {
-        const int e = base + tid;
-        const uint32_t key = e < it.n ? it.k_at(e) : 0u;
-        const bool part = key != 0u && (key & mask) == prefix;
-        const uint32_t digit = part ? ((key >> shift) & static_cast<uint32_t>(nb - 1)) : 0xffffffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (part && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
-      }
-      __syncthreads();
-      const int bpt = nb / NT;
-      const int b0 = tid * bpt;
-      uint32_t local = 0;
-      for (int q = 0; q < bpt; ++q) local += hist[b0 + q];
-      uint32_t tot;
-      const uint32_t excl = block_exclusive_scan<NT>(local, tmp, &tot);
-      uint32_t run = tot - excl - local;
-      for (int q = bpt - 1; q >= 0; --q) {
-        const uint32_t h = hist[b0 + q];
-        if (run < static_cast<uint32_t>(kk) && run + h >= static_cast<uint32_t>(kk)) {
-          s_res[0] = static_cast<uint32_t>(b0 + q);
-          s_res[1] = run;
-        }
-        run += h;
-      }
-      __syncthreads();
-      kk -= static_cast<int>(s_res[1]);
-      prefix |= s_res[0] << shift;
-      mask |= static_cast<uint32_t>(nb - 1) << shift;
-      __syncthreads();
-    }
-    T = prefix;
-    quota = kk;
-  }
-
-  // ---- winners: every key > T, then the lowest positions among keys == T
-  if (tid == 0) {
-    s_res[2] = 0u;
-    s_res[3] = 0u;
-  }
-  __syncthreads();
-  for (int e = tid; e < it.n; e += NT) {
-    const uint32_t key = it.k_at(e);
-    if (key == 0u) continue;
-    if (key > T) {
-      sel[atomicAdd(&s_res[2], 1u)] = it.p_at(e);
-    } else if (key == T && !it.from_row) {
-      eqp[atomicAdd(&s_res[3], 1u)] = it.p_at(e);
-    }
-  }
-  __syncthreads();
-  const int n_gt = static_cast<int>(s_res[2]);
-  int take_eq;
-  if (!it.from_row) {
-    const int n_eq = static_cast<int>(s_res[3]);
-    take_eq = min(n_eq, max(0, min(quota, k - n_gt)));
-    if (take_eq == n_eq) {
-      for (int j = tid; j < n_eq; j += NT) sel[n_gt + j] = eqp[j];
-    } else {  // rank the tied positions by counting (ties at the threshold are few)
-      for (int j = tid; j < n_eq; j += NT) {
-        const int32_t p = eqp[j];
-        int rank = 0;
-        for (int i = 0; i < n_eq; ++i) rank += eqp[i] < p;
-        if (rank < take_eq) sel[n_gt + rank] = p;
-      }
-    }
-  } else {
-    // the row is in position order: the first equal keys win
-    const int seg = (it.n + NT - 1) / NT;
-    const int lo = tid * seg, hi = min(it.n, lo + seg);
-    uint32_t c = 0;
-    for (int e = lo; e < hi; ++e) c += it.k_at(e) == T;
-    uint32_t n_eq;
-    uint32_t r = block_exclusive_scan<NT>(c, tmp, &n_eq);
-    take_eq = min(static_cast<int>(n_eq), max(0, min(quota, k - n_gt)));
-    for (int e = lo; e < hi; ++e)
-      if (it.k_at(e) == T) {
-        if (r < static_cast<uint32_t>(take_eq)) sel[n_gt + r] = e;
-        ++r;
-      }
-  }
-  __syncthreads();
-  const int n_sel = n_gt + take_eq;
-
-  // ---- ascending output: counting sort by position bucket, then rank inside the bucket
+// Winners in ascending position: counting sort by position bucket, then rank inside the
+// bucket (positions are distinct); -1 after the n_sel winners.
+__device__ void write_sorted(const int32_t* sel, int n_sel, int k, int64_t nvr, uint32_t* hist, uint32_t* tmp,
+                             int32_t* srt, int32_t* out) {
+  const int tid = threadIdx.x;
   int shift = 0;
   while ((nvr >> shift) >= kSortBuckets) ++shift;
   for (int i = tid; i < kSortBuckets; i += NT) hist[i] = 0u;
@@ -297,12 +171,10 @@ __global__ void __launch_bounds__(NT) topk_final_kernel(const float* scores, int
   __syncthreads();
   constexpr int bpt = kSortBuckets / NT;  // 2
   const uint32_t c0 = hist[tid * bpt], c1 = hist[tid * bpt + 1];
-  uint32_t tot;
-  const uint32_t start = block_exclusive_scan<NT>(c0 + c1, tmp, &tot);
+  const uint32_t start = block_exclusive_scan<NT>(c0 + c1, tmp, nullptr);
   hist[tid * bpt] = start;  // bucket starts (exclusive prefix)
   hist[tid * bpt + 1] = start + c0;
-  __syncthreads();
-  uint32_t* fill = hist + kSortBuckets;  // [1024] fill counters (hist has 2048 words)
+  uint32_t* fill = hist + kSortBuckets;
   for (int i = tid; i < kSortBuckets; i += NT) fill[i] = 0u;
   __syncthreads();
   for (int j = tid; j < n_sel; j += NT) {
@@ -317,59 +189,284 @@ __global__ void __launch_bounds__(NT) topk_final_kernel(const float* scores, int
     const int b0 = static_cast<int>(hist[bkt]), n_b = static_cast<int>(fill[bkt]);
     int rank = 0;
     for (int i = 0; i < n_b; ++i) rank += srt[b0 + i] < p;
-    idx[row * k + b0 + rank] = p;
+    out[b0 + rank] = p;
   }
-  for (int j = n_sel + tid; j < k; j += NT) idx[row * k + j] = -1;
+  for (int j = n_sel + tid; j < k; j += NT) out[j] = -1;
 }
 
-struct HistPlan {
-  int chunk;
+// One CTA per (row, chunk of kSelChunk positions).  Every CTA finds the threshold digit b1
+// of its row from the fine histogram (one read of the 4096 bins; every one of the k best
+// scores has digit >= b1), keeps the (key, position) of every score of its chunk with digit
+// >= b1, compacted in position order, in its own slot of the workspace, and takes a ticket.
+// The CTA that takes a row's last ticket reads the slots back in chunk order (so the row's
+// candidates are in position order), finds the exact k-th key among the b1 bin by radix
+// passes on its low 20 bits, and writes the winners (every key above it, then the lowest
+// positions among keys equal to it) with one stable compaction: the output is already
+// ascending.  If the candidates exceed kAllCap (a bin full of ties) it selects over the whole
+// row instead.  The tickets (one word per row after the histograms) start at zero.
+constexpr int kSelChunk = 4096;           // positions per CTA (8 per thread)
+constexpr int kSelPer = kSelChunk / NT;
+constexpr int kAllCap = 8192;
+constexpr int kSlotCap = 1024;         // candidates one chunk may keep (more: whole-row path)
+constexpr int kSlotWords = 4 + 2 * kSlotCap;
+
+constexpr int kMaxChunks = 4096;        // n_cols <= 2^24
+constexpr int kMaxChunkPer = kMaxChunks / NT;
+
+struct SelSmem {
+  uint32_t cpre[kMaxChunks];  // last CTA: first candidate index of every chunk
+  uint32_t ak[kAllCap];      // last CTA: the row's candidates in position order
+  int32_t ap[kAllCap];
+  uint32_t hist[2 * kSortBuckets];
+  uint32_t tmp[32];
+  uint32_t res[8];
+  uint32_t b1, last, n_gt;
 };
 
-HistPlan plan_hist(int64_t rows, int64_t n_cols, int num_sms) {
-  HistPlan p{4096};
-  while (p.chunk > 1024 && rows * ((n_cols + p.chunk - 1) / p.chunk) < 2 * num_sms) p.chunk /= 2;
-  return p;
+size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
+
+// Largest fine digit whose suffix count reaches k (0 when the row has fewer than k scores),
+// from one coalesced read of the row's 4096 fine bins.
+__device__ uint32_t block_threshold_digit(const uint32_t* fine, int k, uint32_t* tmp, uint32_t* res) {
+  const int tid = threadIdx.x;
+  constexpr int per = kFine / NT;  // 8
+  uint32_t c[per];
+  uint32_t mine = 0;
+#pragma unroll
+  for (int q = 0; q < per; ++q) {  // thread t owns bins 4095-8t .. 4088-8t (descending)
+    c[q] = __ldcg(fine + kFine - 1 - (tid * per + q));
+    mine += c[q];
+  }
+  if (tid == 0) res[4] = 0u;
+  uint32_t run = block_exclusive_scan<NT>(mine, tmp, nullptr);
+#pragma unroll
+  for (int q = 0; q < per; ++q) {
+    if (run < static_cast<uint32_t>(k) && run + c[q] >= static_cast<uint32_t>(k))
+      res[4] = static_cast<uint32_t>(kFine - 1 - (tid * per + q));
+    run += c[q];
+  }
+  __syncthreads();
+  const uint32_t b1 = res[4];
+  __syncthreads();
+  return b1;
+}
+
+__global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
+                                                         int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
+                                                         uint32_t* cand, int n_chunks) {
+  extern __shared__ __align__(16) uint8_t sel_raw[];
+  SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
+  int32_t* sel = reinterpret_cast<int32_t*>(sel_raw + sizeof(SelSmem));  // [k] (whole-row path)
+  int32_t* srt = sel + k;                                                // [k] (whole-row path)
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.y;
+  const int chunk_id = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nvr = row_valid(n_valid, row, n_cols);
+  const float* srow = scores + row * ld;
+  // this CTA's positions: thread t holds c0 + t*kSelPer .. +kSelPer-1 (contiguous, so the
+  // compaction below keeps position order); loads in flight while the threshold is read
+  const int64_t c0 = static_cast<int64_t>(chunk_id) * kSelChunk;
+  float v[kSelPer];
+  const int64_t t0 = c0 + tid * kSelPer;
+  if (t0 + kSelPer <= nvr && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+#pragma unroll
+    for (int u = 0; u < kSelPer; u += 4) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + t0 + u));
+      v[u] = x.x;
+      v[u + 1] = x.y;
+      v[u + 2] = x.z;
+      v[u + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < nvr ? __ldcg(srow + t0 + u) : 0.f;
+  }
+  uint32_t* rh = hist + row * kRowWords;
+  const uint32_t b1 = block_threshold_digit(rh, k, S.tmp, S.res);
+  uint32_t key[kSelPer];
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kSelPer; ++u) {
+    const int64_t s = c0 + tid * kSelPer + u;
+    uint32_t x = f2key(v[u]);
+    if (x == 0u) x = 1u;
+    key[u] = (s < nvr && (x >> 20) >= b1) ? x : 0u;
+    cnt += key[u] != 0u;
+  }
+  uint32_t n_mine;
+  uint32_t off = block_exclusive_scan<NT>(cnt, S.tmp, &n_mine);
+  // slot of this chunk: [count, 3 pad][keys x kSlotCap][positions x kSlotCap]
+  uint32_t* slot = cand + (static_cast<size_t>(row) * n_chunks + chunk_id) * kSlotWords;
+  uint32_t* skey = slot + 4;
+  uint32_t* spos = skey + kSlotCap;
+#pragma unroll
+  for (int u = 0; u < kSelPer; ++u) {
+    if (key[u] != 0u) {
+      if (off < static_cast<uint32_t>(kSlotCap)) {
+        skey[off] = key[u];
+        spos[off] = static_cast<uint32_t>(c0 + tid * kSelPer + u);
+      }
+      ++off;
+    }
+  }
+  if (tid == 0) slot[0] = n_mine;
+  // the last CTA of the row to finish selects
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t* ticket = hist + static_cast<size_t>(gridDim.y) * kRowWords + row;
+    S.last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(n_chunks - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!S.last) return;
+  __threadfence();
+
+  // ---- the row's last CTA: gather the candidates in chunk (= position) order
+  const uint32_t* base = cand + static_cast<size_t>(row) * n_chunks * kSlotWords;
+  uint32_t my_n = 0, my_over = 0;
+  const int cpt = (n_chunks + NT - 1) / NT;  // chunks per thread (contiguous)
+  uint32_t cc[kMaxChunkPer];
+#pragma unroll
+  for (int q = 0; q < kMaxChunkPer; ++q) {
+    const int ch = tid * cpt + q;
+    cc[q] = (q < cpt && ch < n_chunks) ? __ldcg(base + static_cast<size_t>(ch) * kSlotWords) : 0u;
+    my_n += cc[q];
+    my_over += cc[q] > static_cast<uint32_t>(kSlotCap);
+  }
+  uint32_t n_all_u, n_over;
+  uint32_t run = block_exclusive_scan<NT>(my_n, S.tmp, &n_all_u);
+  block_exclusive_scan<NT>(my_over, S.tmp, &n_over);
+#pragma unroll
+  for (int q = 0; q < kMaxChunkPer; ++q) {
+    const int ch = tid * cpt + q;
+    if (q < cpt && ch < n_chunks) S.cpre[ch] = run;
+    run += cc[q];
+  }
+  __syncthreads();
+  const int n_all = static_cast<int>(n_all_u);
+  int32_t* orow = idx + row * k;
+  if (n_all <= kAllCap && n_over == 0) {
+    uint32_t gt = 0;
+    for (int e = tid; e < n_all; e += NT) {
+      // the chunk holding candidate e: the last chunk whose prefix is <= e
+      int lo = 0, hi = n_chunks - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S.cpre[mid] <= static_cast<uint32_t>(e)) lo = mid; else hi = mid - 1;
+      }
+      const uint32_t* sl = base + static_cast<size_t>(lo) * kSlotWords;
+      const uint32_t j = static_cast<uint32_t>(e) - S.cpre[lo];
+      const uint32_t key = __ldcg(sl + 4 + j);
+      S.ak[e] = key;
+      S.ap[e] = static_cast<int32_t>(__ldcg(sl + 4 + kSlotCap + j));
+      gt += (key >> 20) > b1 ? 1u : 0u;
+    }
+    uint32_t n_gt;
+    block_exclusive_scan<NT>(gt, S.tmp, &n_gt);  // (its barriers also publish ak / ap)
+    const int need = k - static_cast<int>(n_gt);
+    uint32_t T = 1u;
+    int quota = 0x7fffffff;
+    if (n_all - static_cast<int>(n_gt) > need) {
+      const uint32_t* ak = S.ak;
+      block_select_largest([ak](int x) { return ak[x]; }, n_all, need, 20, b1 << 20, 0xFFF00000u, S.hist, S.tmp,
+                           S.res, &T, &quota);
+    }
+    // stable compaction over contiguous segments: keys above T, then the first quota keys
+    // equal to T in position order
+    const int seg = (n_all + NT - 1) / NT;
+    const int lo = tid * seg, hi = min(n_all, lo + seg);
+    uint32_t c_tie = 0;
+    for (int e = lo; e < hi; ++e) c_tie += S.ak[e] == T;
+    uint32_t tie_r = block_exclusive_scan<NT>(c_tie, S.tmp, nullptr);
+    uint32_t c_win = 0;
+    {
+      uint32_t tr = tie_r;
+      for (int e = lo; e < hi; ++e) {
+        const uint32_t key = S.ak[e];
+        if (key > T) {
+          ++c_win;
+        } else if (key == T) {
+          if (tr < static_cast<uint32_t>(quota)) ++c_win;
+          ++tr;
+        }
+      }
+    }
+    uint32_t n_win;
+    uint32_t out = block_exclusive_scan<NT>(c_win, S.tmp, &n_win);
+    for (int e = lo; e < hi; ++e) {
+      const uint32_t key = S.ak[e];
+      bool w = key > T;
+      if (key == T) {
+        w = tie_r < static_cast<uint32_t>(quota);
+        ++tie_r;
+      }
+      if (w && out < static_cast<uint32_t>(k)) orow[out++] = S.ap[e];
+    }
+    for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
+  } else {
+    // too many candidates (a bin full of ties, or crowded into one chunk): select over the whole
+    // row in position order
+    const float* rowp = srow;
+    auto key_at = [rowp](int x) {
+      const uint32_t y = f2key(__ldcg(rowp + x));
+      return y == 0u ? 1u : y;
+    };
+    const int n = static_cast<int>(nvr);
+    uint32_t T = 1u;
+    int quota = 0x7fffffff;
+    if (n > k) block_select_largest(key_at, n, k, 32, 0u, 0u, S.hist, S.tmp, S.res, &T, &quota);
+    if (tid == 0) S.n_gt = 0u;
+    __syncthreads();
+    for (int x = tid; x < n; x += NT)
+      if (key_at(x) > T) {
+        const uint32_t w = atomicAdd(&S.n_gt, 1u);
+        if (w < static_cast<uint32_t>(k)) sel[w] = x;
+      }
+    __syncthreads();
+    const int n_above = min(static_cast<int>(S.n_gt), k);
+    const int seg = (n + NT - 1) / NT;
+    const int lo = tid * seg, hi = min(n, lo + seg);
+    uint32_t c = 0;
+    for (int x = lo; x < hi; ++x) c += key_at(x) == T;
+    uint32_t n_eqT;
+    uint32_t r = block_exclusive_scan<NT>(c, S.tmp, &n_eqT);
+    const int take = min(static_cast<int>(n_eqT), max(0, min(quota, k - n_above)));
+    for (int x = lo; x < hi; ++x)
+      if (key_at(x) == T) {
+        if (r < static_cast<uint32_t>(take)) sel[n_above + r] = x;
+        ++r;
+      }
+    __syncthreads();
+    write_sorted(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow);
+  }
 }
 
 }  // namespace
 
-int topk_hist_cap(int k) { return std::max(8192, 2 * k); }
+int topk_hist_cap(int k) { return std::max(kAllCap, k); }
 
-size_t topk_hist_workspace_bytes(int64_t rows, int k) {
-  const int cap = topk_hist_cap(k);
-  return 2 * align_up(static_cast<size_t>(rows) * cap * 4, 256);
-}
+static int sel_chunks(int64_t n_cols) { return static_cast<int>((n_cols + kSelChunk - 1) / kSelChunk); }
 
-size_t topk_hist_final_smem(int k) {
-  return (static_cast<size_t>(topk_hist_cap(k)) * 3 + kRadixBins + 40 + 2 * static_cast<size_t>(k)) * 4;
+// Per-chunk candidate slots ([count, keys, positions] per chunk of every row).
+size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
+  return align_up(static_cast<size_t>(rows) * sel_chunks(n_cols) * kSlotWords * 4, 256);
 }
 
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s) {
-  const int cap = topk_hist_cap(k);
-  uint32_t* cnt = hist_cnt + rows * kRowWords;
-  uint8_t* w = static_cast<uint8_t*>(ws_cand);
-  uint32_t* ckey = reinterpret_cast<uint32_t*>(w);
-  int32_t* cpos = reinterpret_cast<int32_t*>(w + align_up(static_cast<size_t>(rows) * cap * 4, 256));
-  const HistPlan pl = plan_hist(rows, n_cols, num_sms);
-  dim3 g1(static_cast<unsigned>(std::max<int64_t>(1, (n_cols + pl.chunk - 1) / pl.chunk)), static_cast<unsigned>(rows));
-  const uint32_t* chist = hist_cnt;
-  cudaError_t e = launch_pdl(topk_filter_kernel, g1, dim3(NT), 0, s, scores, ld, n_valid, n_cols, chist, k, cnt, ckey,
-                             cpos, cap, pl.chunk);
-  count_launches(1);
-  if (e != cudaSuccess) return e;
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(topk_hist_final_smem(4096)));
+    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(sel_smem_bytes(4096)));
     attr = true;
   }
-  const uint32_t* ccnt = cnt;
-  const uint32_t* cckey = ckey;
-  const int32_t* ccpos = cpos;
-  e = launch_pdl(topk_final_kernel, dim3(static_cast<unsigned>(rows)), dim3(NT), topk_hist_final_smem(k), s, scores, ld,
-                 n_valid, n_cols, ccnt, cckey, ccpos, cap, k, idx);
+  const int n_chunks = std::max(1, sel_chunks(n_cols));
+  const cudaError_t e =
+      launch_pdl(topk_select_kernel, dim3(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows)), dim3(NT),
+                 sel_smem_bytes(k), s, scores, ld, n_valid, n_cols, hist_cnt, k, idx,
+                 static_cast<uint32_t*>(ws_cand), n_chunks);
   count_launches(1);
   return e;
 }
@@ -378,8 +475,8 @@ bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand) {
   return !has_cand && rows <= 64 && n_cols >= 16384;
 }
 
-size_t topk_hist_standalone_bytes(int64_t rows, int k) {
-  return align_up(static_cast<size_t>(rows) * (kRowWords + 1) * 4, 256) + topk_hist_workspace_bytes(rows, k);
+size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols) {
+  return align_up(static_cast<size_t>(rows) * (kRowWords + 1) * 4, 256) + topk_hist_workspace_bytes(rows, n_cols);
 }
 
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s) {
