@@ -521,6 +521,282 @@ __global__ void __launch_bounds__(kD) attn_merge_kernel(const AttnArgs a, const 
   for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j] * s_inv[j]);
 }
 
+// ------------------------------------------------------------------ decode path
+// One query row per sequence, its k + W rows split over CTAs: grid (row split, head group,
+// query).  A CTA takes 128 rows of the query's row list and NH of the 64 heads (S^T = R Q^T
+// with N = NH; O^T += R^T P^T with the P tile zero beyond NH heads).  The list puts the
+// window first: the window rows, like the query, are inputs that no earlier kernel of the
+// step writes, so they are gathered before the wait on the top-k; the selected rows follow.
+// Partials are stored [query][split][head][dim] (each warp store is 128 contiguous bytes)
+// and merged, with the sink, by attn_merge_dec_kernel.
+template <int NH>
+struct DecLayout {
+  static constexpr uint32_t kQ = 0;                          // 8 regions x (NH rows x 128 B)
+  static constexpr uint32_t kR = kQ + NH * kD * 2;           // 8 regions x (128 rows x 128 B)
+  static constexpr uint32_t kP = kR + kRows * kD * 2;        // 128 rows x 128 B (64 head columns)
+  static constexpr uint32_t kMisc = kP + kRows * 128;
+  static constexpr uint32_t kMiscBytes = (NH * 8 + 32) * 4 + 64;  // m, l, f, red[4], tmp; bars; tmem
+  static constexpr size_t kSmem = 1024 + kMisc + kMiscBytes + kMaxK * 4;
+};
+
+template <int NH>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  using LY = DecLayout<NH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + LY::kQ;
+  uint8_t* sR = smem + LY::kR;
+  uint8_t* sP = smem + LY::kP;
+  float* s_m = reinterpret_cast<float*>(smem + LY::kMisc);  // [NH] block max (log2 units)
+  float* s_l = s_m + NH;                                     // [NH] block sum
+  float* s_f = s_l + NH;                                     // [NH] output factor
+  float* s_red = s_f + NH;                                   // [4][NH]
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(s_red + 4 * NH);  // [32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tmp + 32 + ((NH * 7) & 1));  // 8-byte aligned
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2);
+  int32_t* sel = reinterpret_cast<int32_t*>(smem + LY::kMisc + LY::kMiscBytes);  // [k]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t r = blockIdx.z;
+  const int h0 = blockIdx.y * NH;
+  const int split = blockIdx.x;
+  const int b = static_cast<int>(r / a.T);
+  const float scale_log2 = a.softmax_scale * kLog2e;
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(sTmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if constexpr (NH < kH) {  // head columns of P beyond this CTA's heads stay zero
+    for (int i = tid; i < kRows * 8; i += kTcThreads) {
+      const int j = i >> 3, c = i & 7;
+      if (c >= NH / 8) *reinterpret_cast<uint4*>(sP + sw128(j, c)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // the query and the window rows: inputs, loaded before the wait
+  const int64_t t = a.q_pos[r];
+  const int64_t lbase = a.local_base[b];
+  int64_t p_lo;
+  int n_win;
+  window_of(t, a.W, lbase, a.L, p_lo, n_win);
+  const int row_lo = split * sp.rows_per_split;
+  const int row_cap = row_lo + kRows;
+  const __nv_bfloat16* kvc = static_cast<const __nv_bfloat16*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kD;
+  const __nv_bfloat16* kvl = static_cast<const __nv_bfloat16*>(a.kv_local) + static_cast<int64_t>(b) * a.L * kD;
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (r * kH + h0) * kD;
+    for (int i = tid; i < NH * 64; i += kTcThreads) {
+      const int h = i >> 6, c = i & 63;
+      cp_async16(sQ + (c >> 3) * (NH * 128) + sw128(h, c & 7), q + h * kD + c * 8);
+    }
+    const int w_hi = min(n_win, row_cap);
+    for (int i = tid; i < kRows * 64; i += kTcThreads) {
+      const int j = i >> 6, c = i & 63;
+      const int lp = row_lo + j;
+      if (lp < w_hi) cp_async16(sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7), kvl + (p_lo + lp - lbase) * kD + c * 8);
+    }
+  }
+  pdl_wait();  // the selection (and the entry compressed this step) come from earlier kernels
+  pdl_trigger();
+  const int n_sel = compact_idx<kTcThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
+  const int n_rows = n_win + n_sel;
+  const int row_hi = min(n_rows, row_cap);
+  const int nr = row_hi - row_lo;  // rows of this split (<= 0: none)
+  for (int i = tid; i < kRows * 64; i += kTcThreads) {
+    const int j = i >> 6, c = i & 63;
+    const int lp = row_lo + j;
+    uint8_t* dst = sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7);
+    if (lp >= row_hi) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    } else if (lp >= n_win) {
+      cp_async16(dst, kvc + static_cast<int64_t>(sel[lp - n_win]) * kD + c * 8);
+    }
+  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const uint32_t tS = tmem, tO = tmem + 64;
+  const uint32_t qbase = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+
+  if (nr > 0) {
+    // ---- S^T = R Q^T  (M = 128 rows, N = NH heads, K = 512)
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(kRows, NH, false, false);
+      const uint32_t rb = smem_u32(sR), qb = smem_u32(sQ);
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks) {
+        const uint32_t reg = ks >> 2, off = (ks & 3) * 32u;
+        mma_bf16(tS, smem_desc(rb + reg * (kRows * 128) + off, 16, 1024),
+                 smem_desc(qb + reg * (NH * 128) + off, 16, 1024), idesc, ks > 0);
+      }
+      mma_commit(&bars[0]);
+    }
+    float x[NH];
+    if (warp < 4) {
+      mbar_wait(&bars[0], 0, a.err, nullptr);
+      tc_fence_after();
+      const bool valid = (warp * 32 + lane) < nr;
+#pragma unroll
+      for (int hc = 0; hc < NH; hc += 32) {
+        float v[32];
+        tmem_ld32(tS + qbase + hc, v);
+        tmem_wait_ld(v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (hc + e < NH) x[hc + e] = valid ? v[e] * scale_log2 : -INFINITY;
+      }
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float mx = x[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_red[warp * NH + h] = mx;
+      }
+    }
+    __syncthreads();
+    if (tid < NH)
+      s_m[tid] = fmaxf(fmaxf(s_red[tid], s_red[NH + tid]), fmaxf(s_red[2 * NH + tid], s_red[3 * NH + tid]));
+    __syncthreads();
+    if (warp < 4) {
+      const int j = warp * 32 + lane;
+      float p[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float mu = s_m[h];
+        p[h] = (mu == -INFINITY) ? 0.f : exp2f(x[h] - mu);
+      }
+#pragma unroll
+      for (int c = 0; c < NH / 8; ++c) {
+        uint4 pk;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat162 two = __floats2bfloat162_rn(p[c * 8 + 2 * e], p[c * 8 + 2 * e + 1]);
+          w[e] = *reinterpret_cast<uint32_t*>(&two);
+        }
+        *reinterpret_cast<uint4*>(sP + sw128(j, c)) = pk;
+      }
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float sm = p[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+        if (lane == 0) s_red[warp * NH + h] = sm;
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (tid < NH) s_l[tid] = (s_red[tid] + s_red[NH + tid]) + (s_red[2 * NH + tid] + s_red[3 * NH + tid]);
+    // ---- O^T = R^T P^T  (M = 128 dims per chunk, N = 64 head columns, K = 128 rows)
+    if (warp == 4 && lane == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(kRows, kH, true, true);
+      const uint32_t rb = smem_u32(sR), pb = smem_u32(sP);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+        for (int ks = 0; ks < kRows / 16; ++ks) {
+          mma_bf16(tO + cc * 64, smem_desc(rb + (2 * cc) * (kRows * 128) + ks * 2048, kRows * 128, 1024),
+                   smem_desc(pb + ks * 2048, 8192, 1024), idesc, ks > 0 ? 1u : 0u);
+        }
+      }
+      mma_commit(&bars[1]);
+    }
+    mbar_wait(&bars[1], 0, a.err, nullptr);
+    tc_fence_after();
+  } else if (tid < NH) {
+    s_m[tid] = -INFINITY;
+    s_l[tid] = 0.f;
+  }
+  __syncthreads();
+
+  // ---- epilogue: (m, l) and the unnormalised O of this split's heads
+  if (tid < NH) {
+    float* ml = sp.part_ml + (r * sp.n_split + split) * 2 * kH;
+    ml[h0 + tid] = s_m[tid];
+    ml[kH + h0 + tid] = s_l[tid];
+  }
+  const int c_lo = warp < 4 ? 0 : 2;
+  for (int cc = c_lo; cc < c_lo + 2; ++cc) {
+    const int dd = cc * 128 + (warp & 3) * 32 + lane;
+    float* o = sp.part_o + ((r * sp.n_split + split) * kH + h0) * kD + dd;
+#pragma unroll
+    for (int hc = 0; hc < NH; hc += 32) {
+      float v[32];
+      if (nr > 0) {
+        tmem_ld32(tO + qbase + cc * 64 + hc, v);
+        tmem_wait_ld(v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (hc + e < NH) o[(hc + e) * kD] = v[e];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Fixed-order merge of the decode partials ([query][split][head][dim]) with the sink: one
+// CTA per (query, 4 heads), one thread per output dim.
+__global__ void __launch_bounds__(kD) attn_merge_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  __shared__ float s_f[kMaxSplit][kMergeHeads];  // per split, per head: 2^(m_s - M) / den
+  pdl_wait();
+  pdl_trigger();
+  const int64_t r = blockIdx.x;
+  const int h0 = blockIdx.y * kMergeHeads;
+  const int dd = threadIdx.x;
+  const int ns = sp.n_split;
+  const float* ml = sp.part_ml + r * ns * 2 * kH;
+  if (threadIdx.x < kMergeHeads) {
+    const int h = h0 + threadIdx.x;
+    const float sk = a.sink[h] * kLog2e;
+    float M = sk;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * 2 * kH + h]);
+    float den = exp2f(sk - M);
+    float f[kMaxSplit];
+    for (int s = 0; s < ns; ++s) {
+      const float ms = ml[s * 2 * kH + h];
+      f[s] = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      den = fmaf(ml[s * 2 * kH + kH + h], f[s], den);
+    }
+    const float inv = 1.f / den;
+    for (int s = 0; s < ns; ++s) s_f[s][threadIdx.x] = f[s] * inv;
+    if (a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+  }
+  __syncthreads();
+  const float* po = sp.part_o + (r * ns * kH + h0) * kD + dd;
+  float acc[kMergeHeads] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s >= ns) break;
+#pragma unroll
+    for (int j = 0; j < kMergeHeads; ++j) {
+      const float f = s_f[s][j];
+      if (f != 0.f) acc[j] = fmaf(po[(static_cast<int64_t>(s) * kH + j) * kD], f, acc[j]);
+    }
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (r * kH + h0) * kD + dd;
+#pragma unroll
+  for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j]);
+}
+
 bool attn_uses_tensor_cores(int act, int H, int d, int k) {
   return act == CSA_BF16 && H == kH && d == kD && k <= kMaxK;
 }
@@ -570,11 +846,36 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       attr = true;
     }
-    dim3 grid(sp.n_split, static_cast<unsigned>(rows));
-    cudaError_t e = launch_pdl(attn_tc_kernel, grid, dim3(kTcThreads), smem, s, a, sp);
+    if (sp.n_split == 1 || sp.rows_per_split != kRows) {
+      const cudaError_t e = launch_pdl(attn_tc_kernel, dim3(sp.n_split, static_cast<unsigned>(rows)),
+                                       dim3(kTcThreads), smem, s, a, sp);
+      count_launches(1);
+      if (e != cudaSuccess || sp.n_split == 1) return e;
+      const cudaError_t e2 = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads),
+                                        dim3(kD), 0, s, a, sp);
+      count_launches(1);
+      return e2;
+    }
+    // decode: head groups so that split x group x query fills the SMs once
+    const int64_t per = static_cast<int64_t>(sp.n_split) * rows;
+    const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
+    static bool dattr = false;
+    if (!dattr) {
+      cudaFuncSetAttribute(attn_dec_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(DecLayout<16>::kSmem));
+      cudaFuncSetAttribute(attn_dec_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(DecLayout<32>::kSmem));
+      cudaFuncSetAttribute(attn_dec_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(DecLayout<64>::kSmem));
+      dattr = true;
+    }
+    dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
+    cudaError_t e = hg == 4 ? launch_pdl(attn_dec_kernel<16>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
+                  : hg == 2 ? launch_pdl(attn_dec_kernel<32>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
+                            : launch_pdl(attn_dec_kernel<64>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
     count_launches(1);
-    if (e != cudaSuccess || sp.n_split == 1) return e;
-    e = launch_pdl(attn_merge_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads), dim3(kD), 0, s, a, sp);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(attn_merge_dec_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads), dim3(kD), 0, s, a, sp);
     count_launches(1);
     return e;
   }

@@ -261,14 +261,16 @@ def _attn_ref(q, kv, idx, kl, local_base, q_pos, sink, W, scale):
     return np.stack(outs).reshape(q.shape), np.stack(lses).reshape(B, T, -1)
 
 
-@pytest.mark.parametrize("B,T,nsel", [(3, 1, [512, 300, 512]), (1, 160, [512, 77]), (2, 2, [0, 512])])
+# B = 3, 2: four head groups per decode CTA; B = 10: two; B = 16: one (64 heads)
+@pytest.mark.parametrize("B,T,nsel", [(3, 1, [512, 300, 512]), (1, 160, [512, 77]), (2, 2, [0, 512]),
+                                      (10, 1, [512, 300, 17, 0, 512]), (16, 1, [512, 1, 400])])
 def test_attention_tensor_cores(B, T, nsel):
     H, d, E, k, W, L = 64, 512, 1500, 512, 128, 200
-    q, kv, kl, sink, idx = _attn_inputs(40 + T, B, T, H, d, E, k, L, BF16, nsel)
-    local_base = torch.tensor([1000, 1040, 0][:B], dtype=torch.int64, device=DEV)
+    q, kv, kl, sink, idx = _attn_inputs(40 + T + B, B, T, H, d, E, k, L, BF16, nsel)
+    local_base = torch.tensor([[1000, 1040, 0][b % 3] for b in range(B)], dtype=torch.int64, device=DEV)
     # windows: fully held, clipped by the local rows' start, and t < W - 1 (starts at 0)
     base_t = [1000 + 150, 1040 + 60, 50]
-    q_pos = torch.tensor([base_t[b] + (t % 3) for b in range(B) for t in range(T)], dtype=torch.int64, device=DEV)
+    q_pos = torch.tensor([base_t[b % 3] + (t % 3) for b in range(B) for t in range(T)], dtype=torch.int64, device=DEV)
     c = cfg_obj(B=B)
     out = torch.empty(B, T, H, d, device=DEV, dtype=BF16)
     lse = torch.empty(B, T, H, device=DEV)
