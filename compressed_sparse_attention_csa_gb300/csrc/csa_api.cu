@@ -136,11 +136,12 @@ IndexerArgs indexer_shape(const csa_config* c, int T, int64_t E_cap, int sms) {
 
 size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   const int64_t B = c->B;
-  size_t bytes = align_up(indexer_workspace_bytes(indexer_shape(c, 1, E_cap, sms)), 256);  // query images
+  // first, at a fixed offset: the top-k histograms, tickets and epochs kept across steps
+  size_t bytes = align_up(decode_hist_words(static_cast<int>(B)) * 4, 256);
+  bytes += align_up(indexer_workspace_bytes(indexer_shape(c, 1, E_cap, sms)), 256);  // query images
   bytes += align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
   bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
-  bytes += align_up(static_cast<size_t>(B) * (kTopkHistRowWords + 1) * 4, 256);  // histograms + counters
   bytes += align_up(std::max(topk_workspace_bytes(B, E_cap, c->k, sms), topk_hist_workspace_bytes(B, E_cap)), 256);
   bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms), 256);
   return bytes;
@@ -416,6 +417,8 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   int* err = err_word_ptr();
 
   uint8_t* p = static_cast<uint8_t*>(ws);
+  uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(p);  // kept across steps (zero before the first)
+  p += align_up(decode_hist_words(cfg->B) * 4, 256);
   void* q_images = p;
   p += align_up(indexer_workspace_bytes(indexer_shape(cfg, 1, d->E_cap, sms)), 256);
   float* scores = reinterpret_cast<float*>(p);
@@ -424,8 +427,6 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   p += align_up(static_cast<size_t>(cfg->B) * 4, 256);
   int32_t* idx = reinterpret_cast<int32_t*>(p);
   p += align_up(static_cast<size_t>(cfg->B) * cfg->k * 4, 256);
-  uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(p);
-  p += align_up(static_cast<size_t>(cfg->B) * (kTopkHistRowWords + 1) * 4, 256);
   const size_t topk_ws =
       std::max(topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms), topk_hist_workspace_bytes(cfg->B, d->E_cap));
   void* ws_topk = p;
@@ -454,59 +455,58 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   ia.num_sms = sms;
   ia.nv_out = nv;
   ia.ws = q_images;
-  const bool hist_topk = indexer_uses_tensor_cores(ia);
-  ia.hist_out = hist_topk ? hist_cnt : nullptr;
-
-  // 1. compress the block the new token completes (main KV, then indexer keys); on the
-  //    tensor-core path the same launch writes the indexer's query images
-  CompressArgs c{};
-  c.B = cfg->B;
-  c.m = cfg->m;
-  c.act_bf16 = cfg->act == CSA_BF16;
-  c.q_pos = d->q_pos;
-  c.E_cap = d->E_cap;
-  c.err = err;
-  c.job[0] = CompressJob{d->kv_tail, d->z_tail, d->bias, cfg->d, d->kv_comp, cfg->act, nullptr};
-  c.job[1] = CompressJob{d->kvI_tail, d->zI_tail, d->biasI, cfg->dI, d->kI, cfg->kidx, d->kscale};
-  c.n_jobs = 2;
-  c.zero_hist = hist_cnt;
   cudaError_t e;
-  if (hist_topk) {
-    QprepPart qp{};
-    qp.ia = ia;
-    qp.L = indexer_layout(ia);
-    qp.images = static_cast<uint8_t*>(q_images);
-    qp.fp8 = cfg->kidx == CSA_E4M3;
-    e = launch_compress_with_qprep(c, qp, s);
+  if (indexer_uses_tensor_cores(ia) && cfg->m <= 8) {
+    // 1-2. one launch: compression of the completed block (both caches), the query images,
+    //      the scores and their histogram; 3. the top-k from that histogram
+    DecodeFuse& f = ia.fuse;
+    f.on = true;
+    f.kv_tail = d->kv_tail;
+    f.z_tail = d->z_tail;
+    f.bias = d->bias;
+    f.kv_comp = d->kv_comp;
+    f.d = cfg->d;
+    f.kvI_tail = d->kvI_tail;
+    f.zI_tail = d->zI_tail;
+    f.biasI = d->biasI;
+    f.act_bf16 = cfg->act == CSA_BF16;
+    f.hist2 = hist_cnt;
     ia.images_ready = true;
-  } else {
-    e = launch_compress(c, s);
-  }
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-
-  // 2. indexer
-  e = launch_indexer(ia, s);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-
-  // 3. top-k
-  if (hist_topk) {
-    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s);
+    e = launch_indexer(ia, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s, true);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   } else {
-  TopkArgs ta{};
-  ta.scores = scores;
-  ta.ld = d->E_cap;
-  ta.rows = cfg->B;
-  ta.n_cols = d->E_cap;
-  ta.n_valid = nv;
-  ta.k = cfg->k;
-  ta.idx = idx;
-  ta.ws = ws_topk;
-  ta.ws_bytes = topk_ws;
-  ta.err = err;
-  ta.num_sms = sms;
-  e = launch_topk(ta, s);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
+    // 1. compress the block the new token completes (main KV, then indexer keys)
+    CompressArgs c{};
+    c.B = cfg->B;
+    c.m = cfg->m;
+    c.act_bf16 = cfg->act == CSA_BF16;
+    c.q_pos = d->q_pos;
+    c.E_cap = d->E_cap;
+    c.err = err;
+    c.job[0] = CompressJob{d->kv_tail, d->z_tail, d->bias, cfg->d, d->kv_comp, cfg->act, nullptr};
+    c.job[1] = CompressJob{d->kvI_tail, d->zI_tail, d->biasI, cfg->dI, d->kI, cfg->kidx, d->kscale};
+    c.n_jobs = 2;
+    e = launch_compress(c, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    // 2. indexer; 3. top-k
+    e = launch_indexer(ia, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    TopkArgs ta{};
+    ta.scores = scores;
+    ta.ld = d->E_cap;
+    ta.rows = cfg->B;
+    ta.n_cols = d->E_cap;
+    ta.n_valid = nv;
+    ta.k = cfg->k;
+    ta.idx = idx;
+    ta.ws = ws_topk;
+    ta.ws_bytes = topk_ws;
+    ta.err = err;
+    ta.num_sms = sms;
+    e = launch_topk(ta, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
   }
 
   // 4. sparse attention over the selection plus the window, with the sink

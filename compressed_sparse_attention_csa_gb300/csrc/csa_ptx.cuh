@@ -85,6 +85,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// generic-proxy global writes of this thread before later async-proxy (TMA) reads
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ------------------------------------------------------------------ TMA (tiled, 2D)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

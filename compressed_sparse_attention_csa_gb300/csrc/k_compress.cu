@@ -32,9 +32,9 @@ __global__ void __launch_bounds__(512) compress_kernel(CompressArgs a, QprepPart
     const int gh = (static_cast<int>(blockIdx.z) - a.n_jobs) * nw + static_cast<int>(threadIdx.x >> 5);
     if (gh < qp.L.N) {
       if (qp.fp8)
-        qprep_row<true>(qp.ia, qp.L, qp.images, 0, b, gh, threadIdx.x & 31);
+        qprep_row<true>(qp.ia, qp.L, qprep_image(qp.L, qp.images, 0, b), 0, b, gh, threadIdx.x & 31);
       else
-        qprep_row<false>(qp.ia, qp.L, qp.images, 0, b, gh, threadIdx.x & 31);
+        qprep_row<false>(qp.ia, qp.L, qprep_image(qp.L, qp.images, 0, b), 0, b, gh, threadIdx.x & 31);
     }
     return;
   }

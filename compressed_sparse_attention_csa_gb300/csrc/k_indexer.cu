@@ -125,13 +125,14 @@ __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a,
   pdl_wait();  // the images may still be read by the previous indexer launch
   pdl_trigger();
   const int gh = blockIdx.z * 8 + (threadIdx.x >> 5);
-  if (gh < L.N) qprep_row<FP8>(a, L, images, blockIdx.x, blockIdx.y, gh, threadIdx.x & 31);
+  if (gh < L.N)
+    qprep_row<FP8>(a, L, qprep_image(L, images, blockIdx.x, blockIdx.y), blockIdx.x, blockIdx.y, gh, threadIdx.x & 31);
 }
 
 // Warp 0: TMA producer.  Warp 1: TMEM owner and MMA issuer (it also pulls the query image).
 // Warps 2..9: epilogue, as two groups of four (one warp per TMEM lane quadrant) that take
 // alternate tiles.
-template <bool FP8>
+template <bool FP8, bool FUSE>
 __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const IndexerArgs a, const TcLayout L,
                                                                    const uint8_t* images, const int64_t n_cols) {
@@ -148,10 +149,16 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   uint64_t* tfull = bars + 2 * S;       // [4] accumulator ready for the epilogue
   uint64_t* tempty = bars + 2 * S + 4;  // [4] accumulator drained
   uint64_t* qbar = bars + 2 * S + 8;    // query image landed
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 9);
+  uint64_t* kbar = bars + 2 * S + 9;    // decode step: the new key entry is written
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 10);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
-  uint32_t* sHist = reinterpret_cast<uint32_t*>(sTmem + 4);  // [4096] when a.hist_out (G == 1)
-  const bool hist = a.hist_out != nullptr && G == 1;
+  int64_t* sNew = reinterpret_cast<int64_t*>(sTmem + 2);     // decode step: new entry (-1: none)
+  uint32_t* sEpoch = sTmem + 4;                               // decode step: histogram epoch
+  float* sNewScale = reinterpret_cast<float*>(sTmem + 5);
+  float* sRed4 = reinterpret_cast<float*>(sTmem + 8);        // [4] decode step: key amax
+  uint32_t* sHist = sTmem + 12;                               // [4096] when a histogram is kept (G == 1)
+  constexpr bool fuse = FUSE;  // decode step: see DecodeFuse
+  const bool hist = (a.hist_out != nullptr || fuse) && G == 1;
   const int NA = L.n_acc;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -168,6 +175,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       int64_t v = t < 0 ? 0 : (t + 1) / a.m;
       nv = static_cast<int>(v < a.E_cap ? v : a.E_cap);
       if (a.nv_out && split == 0) a.nv_out[qrow0 + tid] = nv;
+      if (fuse && tid == 0) {
+        // the entry the token completes (compressed in this launch), if it fits the cache
+        const int64_t e = t >= 0 && (t + 1) % a.m == 0 ? (t + 1) / a.m - 1 : -1;
+        *sNew = e < a.E_cap ? e : -1;
+        *sEpoch = __ldcg(a.fuse.hist2 + 2 * static_cast<size_t>(a.B) * kTopkHistRowWords + a.B + b);
+      }
     }
     sNv[tid] = nv;
   }
@@ -181,7 +194,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 32 * (kEpiWarps / 2));
     }
-    mbar_init(qbar, 1);
+    mbar_init(qbar, fuse ? 32 * kEpiWarps : 1);
+    mbar_init(kbar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -193,7 +207,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *sTmem;
   // the keys, scales, query images and histograms are written by the kernels before this one
-  pdl_wait();
+  // (decode step: nothing this launch reads is written by earlier kernels of the step)
+  if (!fuse) pdl_wait();
+  const int64_t e_new = fuse ? *sNew : -1;
 
   int nv_max = 0;
   for (int g = 0; g < G; ++g) nv_max = max(nv_max, sNv[g]);
@@ -203,13 +219,22 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   const int n_it = tiles_needed > tile_lo ? (tiles_needed - tile_lo + tile_step - 1) / tile_step : 0;
 
   if (warp == 0) {
-    if (lane == 0 && n_it > 0) {
-      tma_prefetch_desc(&kmap);
-      const uint64_t pol = policy_evict_first();
+    // decode step: this CTA scores the tile of the new entry (its last tile), whose key the
+    // epilogue warps compress first: that tile is loaded once the key is written
+    const bool own_new =
+        e_new >= 0 && n_it > 0 && static_cast<int64_t>(tile_lo + (n_it - 1) * tile_step) == e_new / kTile;
+    const int key_it = own_new ? n_it - 1 : n_it;
+    if (n_it > 0) {
+      uint64_t pol = 0;
+      bool ok = true;
       int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
+      if (lane == 0) {
+        tma_prefetch_desc(&kmap);
+        pol = policy_evict_first();
+      }
+      auto issue = [&](int it) {
         const int st = it % S;
-        if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) break;
+        if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) return false;
         mbar_arrive_expect_tx(&full[st], L.stage_bytes);
         const int64_t row64 =
             static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it * tile_step) * kTile;
@@ -218,10 +243,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         // innermost coordinate 0 or 64 elements: always 16-byte aligned
         tma_load_2d_hint(dst, &kmap, &full[st], 0, row, pol);
         if constexpr (!FP8) tma_load_2d_hint(dst + 16384, &kmap, &full[st], 64, row, pol);
-        ++issued;
+        return true;
+      };
+      if (lane == 0) {
+        for (int it = 0; ok && it < key_it; ++it) ok = issue(it), issued += ok;
+        if (FUSE && own_new && ok) ok = mbar_wait(kbar, 0, a.err, sAbort);
+        for (int it = key_it; ok && it < n_it; ++it) ok = issue(it), issued += ok;
+        // every load issued must have landed before the CTA may exit
+        for (int it = max(0, issued - S); it < issued; ++it) wait_time_only(&full[it % S], (it / S) & 1);
       }
-      // every load issued must have landed before the CTA may exit
-      for (int it = max(0, issued - S); it < issued; ++it) wait_time_only(&full[it % S], (it / S) & 1);
     }
     // columns past the last visible tile: -inf (written by the last split of the group)
     if (split == L.n_splits - 1) {
@@ -233,11 +263,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // the group's query image (B operand + gates) in one bulk copy
-      const uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
-      mbar_arrive_expect_tx(qbar, L.b_bytes + L.w_bytes);
-      bulk_g2s(sB, img, L.b_bytes, qbar);
-      bulk_g2s(sW, img + L.b_bytes, L.w_bytes, qbar);
+      // the group's query image (B operand + gates): one bulk copy, or (decode step) written
+      // by the epilogue warps
+      if (!fuse) {
+        const uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
+        mbar_arrive_expect_tx(qbar, L.b_bytes + L.w_bytes);
+        bulk_g2s(sB, img, L.b_bytes, qbar);
+        bulk_g2s(sW, img + L.b_bytes, L.w_bytes, qbar);
+      }
       const bool q_ok = mbar_wait(qbar, 0, a.err, sAbort);
       if (q_ok && n_it > 0) {
         const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
@@ -272,7 +305,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         }
         if (committed > 0) wait_time_only(&tfull[(committed - 1) % NA], ((committed - 1) / NA) & 1);
       }
-      if (!q_ok) wait_time_only(qbar, 0);  // the image copy must land before the CTA exits
+      if (!q_ok && !fuse) wait_time_only(qbar, 0);  // the image copy must land before the CTA exits
     }
   } else {
     // ---- epilogue: group gp (0/1) takes tiles gp, gp + 2, ...; warp (warp & 3) owns TMEM
@@ -280,6 +313,30 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     const int q = warp & 3;
     const int gp = (warp - 2) >> 2;
     const int rin = q * 32 + lane;
+    uint32_t* hist_row = hist ? a.hist_out + qrow0 * kTopkHistRowWords : nullptr;
+    if constexpr (FUSE) {
+      build_image_cta<FP8>(a, L, sB, b, tid - 64);
+      fence_proxy_async_smem();
+      mbar_arrive(qbar);
+      const size_t row_words = kTopkHistRowWords, bw = static_cast<size_t>(a.B) * row_words;
+      hist_row = a.fuse.hist2 + (*sEpoch & 1u) * bw + b * row_words;
+      // the new key entry, if this CTA scores it (first epilogue group, one channel a thread)
+      const bool own_new =
+          e_new >= 0 && n_it > 0 && static_cast<int64_t>(tile_lo + (n_it - 1) * tile_step) == e_new / kTile;
+      if (own_new && gp == 0) {
+        const float sc = decode_new_key<FP8>(a, b, e_new, tid - 64, sRed4, 7);
+        if (tid == 64) {
+          *sNewScale = sc;
+          mbar_arrive(kbar);
+        }
+      }
+      if (split == 0) {
+        // the sequence's new main-KV entry, and the other histogram buffer zeroed for the next step
+        if (e_new >= 0) decode_new_kv(a, b, e_new, tid - 64);
+        uint32_t* other = a.fuse.hist2 + ((*sEpoch + 1u) & 1u) * bw + b * row_words;
+        for (int i = tid - 64; i < kTopkHistRowWords; i += 32 * kEpiWarps) other[i] = 0u;
+      }
+    }
     const bool w_ok = mbar_wait(qbar, 0, a.err, sAbort);  // gates landed with the query image
     const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
     auto scale_of = [&](int itx) -> float {
@@ -294,6 +351,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       if (!mbar_wait(&tfull[acc], (it / NA) & 1, a.err, sAbort)) break;
       tc_fence_after();
       const int64_t s = static_cast<int64_t>(tile_lo + it * tile_step) * kTile + rin;
+      float ksc_use = ksc;
+      if (FUSE && FP8 && s == e_new) {  // the key compressed in this launch: its scale
+        if (!mbar_wait(kbar, 0, a.err, sAbort)) break;
+        ksc_use = *sNewScale;
+      }
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
       float res[kMaxG];
 #pragma unroll
@@ -315,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
 #pragma unroll
         for (int g = 0; g < kMaxG; ++g) {
           if (g >= G || g0 + g >= T) continue;
-          const float sc = res[g] * ksc;
+          const float sc = res[g] * ksc_use;
           a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
           if (hist && s < sNv[0]) atomicAdd(&sHist[f2key(sc) >> 20], 1u);
         }
@@ -323,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     }
     if (hist) {
       named_sync(6, 32 * kEpiWarps);
-      uint32_t* rh = a.hist_out + qrow0 * kTopkHistRowWords;
+      uint32_t* rh = hist_row;
       for (int i = tid - 64; i < kTopkHistBins; i += 32 * kEpiWarps) {
         const uint32_t c = sHist[i];
         if (c) atomicAdd(&rh[i], c);
@@ -339,6 +401,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   }
 
   pdl_trigger();  // the next kernel may start launching while this CTA tears down
+  // decode step: completing only after the previous kernel keeps the stream order transitive
+  if (fuse) pdl_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -361,7 +425,7 @@ TcLayout plan_tc(const IndexerArgs& a) {
   // few long rows (decode): two CTAs per SM, key range split over them
   const bool decode_like = groups < a.num_sms;
   const size_t misc = 1024 + align_up(L.w_bytes, 1024) + 64 + 32 * 8 + 64 +
-                      (a.hist_out && L.G == 1 ? kTopkHistBins * 4 : 0);
+                      ((a.hist_out || a.fuse.on) && L.G == 1 ? kTopkHistBins * 4 : 0);
   const size_t budget = decode_like ? (113 * 1024) : (227 * 1024);
   int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
   S = std::max(2, std::min(S, 8));
@@ -421,13 +485,22 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
     dim3 grid(L.n_splits, L.n_qgroups, a.B);
     static bool attr = false;
     if (!attr) {
-      cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(indexer_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(indexer_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(indexer_tc_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(indexer_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       attr = true;
     }
     const uint8_t* cimages = images;
-    e = fp8 ? launch_pdl(indexer_tc_kernel<true>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L, cimages, n_cols)
-            : launch_pdl(indexer_tc_kernel<false>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L, cimages, n_cols);
+    const bool fu = a.fuse.on;
+    e = fp8 ? (fu ? launch_pdl(indexer_tc_kernel<true, true>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L, cimages,
+                               n_cols)
+                  : launch_pdl(indexer_tc_kernel<true, false>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L,
+                               cimages, n_cols))
+            : (fu ? launch_pdl(indexer_tc_kernel<false, true>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L,
+                               cimages, n_cols)
+                  : launch_pdl(indexer_tc_kernel<false, false>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L,
+                               cimages, n_cols));
     count_launches(1);
     return e;
   }

@@ -253,7 +253,7 @@ __device__ uint32_t block_threshold_digit(const uint32_t* fine, int k, uint32_t*
 
 __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
                                                          int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
-                                                         uint32_t* cand, int n_chunks) {
+                                                         uint32_t* cand, int n_chunks, bool two_buffers) {
   extern __shared__ __align__(16) uint8_t sel_raw[];
   SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
   int32_t* sel = reinterpret_cast<int32_t*>(sel_raw + sizeof(SelSmem));  // [k] (whole-row path)
@@ -283,7 +283,12 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
 #pragma unroll
     for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < nvr ? __ldcg(srow + t0 + u) : 0.f;
   }
-  uint32_t* rh = hist + row * kRowWords;
+  // histogram rows, then the tickets (and with two buffers: [2][rows] rows, tickets, epochs)
+  const int64_t rows = gridDim.y;
+  uint32_t* ticket = hist + (two_buffers ? 2 : 1) * rows * kRowWords + row;
+  uint32_t* epoch = two_buffers ? hist + 2 * rows * kRowWords + rows + row : nullptr;
+  const uint32_t buf = two_buffers ? (__ldcg(epoch) & 1u) : 0u;
+  uint32_t* rh = hist + (buf * rows + row) * kRowWords;
   const uint32_t b1 = block_threshold_digit(rh, k, S.tmp, S.res);
   uint32_t key[kSelPer];
   uint32_t cnt = 0;
@@ -315,13 +320,15 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   // the last CTA of the row to finish selects
   __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    uint32_t* ticket = hist + static_cast<size_t>(gridDim.y) * kRowWords + row;
-    S.last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(n_chunks - 1) ? 1u : 0u;
-  }
+  if (tid == 0) S.last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(n_chunks - 1) ? 1u : 0u;
   __syncthreads();
   if (!S.last) return;
   __threadfence();
+  // every CTA of the row has read the histogram: reset the ticket, advance the epoch
+  if (tid == 0) {
+    *ticket = 0u;
+    if (epoch) *epoch = buf + 1u + (__ldcg(epoch) & ~1u);
+  }
 
   // ---- the row's last CTA: gather the candidates in chunk (= position) order
   const uint32_t* base = cand + static_cast<size_t>(row) * n_chunks * kSlotWords;
@@ -455,7 +462,8 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
 }
 
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s) {
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s,
+                             bool two_buffers) {
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -466,7 +474,7 @@ cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int6
   const cudaError_t e =
       launch_pdl(topk_select_kernel, dim3(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows)), dim3(NT),
                  sel_smem_bytes(k), s, scores, ld, n_valid, n_cols, hist_cnt, k, idx,
-                 static_cast<uint32_t*>(ws_cand), n_chunks);
+                 static_cast<uint32_t*>(ws_cand), n_chunks, two_buffers);
   count_launches(1);
   return e;
 }

@@ -6,20 +6,21 @@
 // split into two E4M3 terms hi + lo (hi = e4m3(q/s), lo = e4m3(q/s - hi)), and the gate stored
 // as w * s, since s > 0 factors out of the ReLU.
 //
-// Used by the standalone query-prep kernel and by the decode step's compressor launch.
+// Used by the standalone query-prep kernel, the compressor launch, and the decode-step
+// indexer (which writes the image straight into its shared memory).
 #pragma once
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
 
 namespace csa {
 
+// img: this query group's image (global workspace, or the indexer CTA's shared memory).
 template <bool FP8>
-__device__ __forceinline__ void qprep_row(const IndexerArgs& a, const IndexerLayout& L, uint8_t* images, int qg,
+__device__ __forceinline__ void qprep_row(const IndexerArgs& a, const IndexerLayout& L, uint8_t* img, int qg,
                                           int b, int gh, int lane) {
   const int HI = a.HI, G = L.G, N = L.N, T = a.T;
   const int g0 = qg * G;
   const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
-  uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
   float* wimg = reinterpret_cast<float*>(img + L.b_bytes);
   const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI);
   const int g = gh / HI, h = gh - g * HI;
@@ -62,6 +63,209 @@ __device__ __forceinline__ void qprep_row(const IndexerArgs& a, const IndexerLay
     *reinterpret_cast<uint32_t*>(img + off) = hi4;
     *reinterpret_cast<uint32_t*>(img + N * 128 + off) = lo4;
     if (lane == 0) wimg[gh] = wv * sc;
+  }
+}
+
+__device__ __forceinline__ uint8_t* qprep_image(const IndexerLayout& L, uint8_t* images, int qg, int b) {
+  return images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
+}
+
+// ---- decode step, inside the indexer launch -----------------------------------------
+
+// NC channels of the compressed entry the token t completes ("DeepSeek V4-Flash: The Cost of
+// Deciding What to Read", section "The compressor has two streams and they overlap"): the
+// tail holds tokens t-2m+1..t, so stream a (current block) is rows m..2m-1 and stream b
+// (previous block) rows 0..m-1; a softmax over the 2m gate logits plus the positional bias,
+// then the weighted sum of the values.  has_b = false (entry 0) keeps stream a only.  MT
+// bounds 2m at compile time so every load of every channel is in flight at once.
+template <typename T, int MT, int NC>
+__device__ __forceinline__ void compress_tail(const T* kv, const T* z, const float* bias, int m, int dim,
+                                              const int (&c)[NC], bool has_b, float (&out)[NC]) {
+  float lg[NC][MT], val[NC][MT];
+#pragma unroll
+  for (int j = 0; j < MT; ++j) {
+    if (j < 2 * m && (j < m || has_b)) {
+      const int st = j < m ? 0 : 1;
+      const int jj = j < m ? j : j - m;
+      const int64_t row = static_cast<int64_t>((st == 0 ? m : 0) + jj) * 2 + st;
+#pragma unroll
+      for (int n = 0; n < NC; ++n) {
+        lg[n][j] = load_f<T>(z + row * dim + c[n]) + bias[(st * m + jj) * dim + c[n]];
+        val[n][j] = load_f<T>(kv + row * dim + c[n]);
+      }
+    }
+  }
+  const int nt = has_b ? 2 * m : m;
+#pragma unroll
+  for (int n = 0; n < NC; ++n) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < MT; ++j)
+      if (j < nt) mx = fmaxf(mx, lg[n][j]);
+    float sum = 0.f, acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+      if (j < nt) {
+        const float e = expf(lg[n][j] - mx);
+        sum += e;
+        acc = fmaf(e, val[n][j], acc);
+      }
+    }
+    out[n] = acc / sum;
+  }
+}
+
+// m <= 8 (the fused decode path's limit): 2m <= 16 tokens.
+template <int NC>
+__device__ __forceinline__ void compress_tail_any(const void* kv, const void* z, const float* bias, bool bf16, int m,
+                                                  int dim, const int (&c)[NC], bool has_b, float (&out)[NC]) {
+#define CSA_TAIL(T, MT) \
+  compress_tail<T, MT, NC>(static_cast<const T*>(kv), static_cast<const T*>(z), bias, m, dim, c, has_b, out)
+  if (bf16) {
+    if (m <= 4) CSA_TAIL(__nv_bfloat16, 8); else CSA_TAIL(__nv_bfloat16, 16);
+  } else {
+    if (m <= 4) CSA_TAIL(float, 8); else CSA_TAIL(float, 16);
+  }
+#undef CSA_TAIL
+}
+
+// The new indexer-key entry e of sequence b (dI = 128), by 128 threads (one channel each,
+// t128 = 0..127, named barrier `bar`): stored as e4m3 codes with one fp32 scale (amax/448,
+// as the compressor does) or as bf16.  Returns the scale (1 for bf16 keys).  Every thread
+// fences its global writes for the TMA load of the same row that follows in this CTA.
+template <bool FP8>
+__device__ __forceinline__ float decode_new_key(const IndexerArgs& a, int b, int64_t e, int t128, float* red4,
+                                                int bar) {
+  const DecodeFuse& f = a.fuse;
+  const int dI = a.dI, m = a.m;
+  const size_t elem = f.act_bf16 ? 2 : 4;
+  const size_t tail = static_cast<size_t>(b) * 2 * m * 2 * dI * elem;
+  const int c[1] = {t128};
+  float v[1];
+  compress_tail_any<1>(static_cast<const uint8_t*>(f.kvI_tail) + tail, static_cast<const uint8_t*>(f.zI_tail) + tail,
+                       f.biasI, f.act_bf16, m, dI, c, e > 0, v);
+  const int64_t row = static_cast<int64_t>(b) * a.E_cap + e;
+  float scale = 1.f;
+  if constexpr (FP8) {
+    float am = fabsf(v[0]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if ((t128 & 31) == 0) red4[t128 >> 5] = am;
+    asm volatile("bar.sync %0, 128;" ::"r"(bar) : "memory");
+    am = fmaxf(fmaxf(red4[0], red4[1]), fmaxf(red4[2], red4[3]));
+    scale = am > 0.f ? __fdiv_rn(am, 448.f) : 1.f;
+    static_cast<uint8_t*>(const_cast<void*>(a.kI))[row * dI + t128] = f_to_e4m3(__fdiv_rn(v[0], scale));
+    if (t128 == 0) const_cast<float*>(a.kscale)[row] = scale;
+  } else {
+    static_cast<__nv_bfloat16*>(const_cast<void*>(a.kI))[row * dI + t128] = __float2bfloat16_rn(v[0]);
+  }
+  fence_proxy_async_global();
+  asm volatile("bar.sync %0, 128;" ::"r"(bar) : "memory");
+  return scale;
+}
+
+// The new main-KV entry e of sequence b by 256 threads (t256 = 0..255), two channels each
+// (d <= 512).
+__device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64_t e, int t256) {
+  const DecodeFuse& f = a.fuse;
+  const int d = f.d, m = a.m;
+  const size_t elem = f.act_bf16 ? 2 : 4;
+  const size_t tail = static_cast<size_t>(b) * 2 * m * 2 * d * elem;
+  float v[2];
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    const int c[1] = {t256 + 256 * n < d ? t256 + 256 * n : 0};
+    float o[1];
+    compress_tail_any<1>(static_cast<const uint8_t*>(f.kv_tail) + tail, static_cast<const uint8_t*>(f.z_tail) + tail,
+                         f.bias, f.act_bf16, m, d, c, e > 0, o);
+    v[n] = o[0];
+  }
+  const int64_t row = (static_cast<int64_t>(b) * a.E_cap + e) * d;
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    const int ch = t256 + 256 * n;
+    if (ch >= d) continue;
+    if (f.act_bf16)
+      static_cast<__nv_bfloat16*>(f.kv_comp)[row + ch] = __float2bfloat16_rn(v[n]);
+    else
+      static_cast<float*>(f.kv_comp)[row + ch] = v[n];
+  }
+}
+
+// The query image of sequence b (one query, N = HI <= 128 rows) written by 256 threads
+// straight into shared memory: 4 threads per head row, 32 dims each; the same arithmetic
+// as qprep_row.  img = B operand, followed by the gates.
+template <bool FP8>
+__device__ __forceinline__ void build_image_cta(const IndexerArgs& a, const IndexerLayout& L, uint8_t* img, int b,
+                                                int t256) {
+  const int N = L.N;
+  const __nv_bfloat16* qI = static_cast<const __nv_bfloat16*>(a.qI) + static_cast<int64_t>(b) * a.HI * 128;
+  const float* w = a.w + static_cast<int64_t>(b) * a.HI;
+  float* wimg = reinterpret_cast<float*>(img + L.b_bytes);
+  constexpr int kRowsPer = 2;  // N <= 128 = 2 x 64
+  uint4 raw[kRowsPer][4];
+  float wv[kRowsPer];
+  const int part = t256 & 3;  // dims 32*part .. 32*part + 31
+#pragma unroll
+  for (int rr = 0; rr < kRowsPer; ++rr) {
+    const int gh = (t256 >> 2) + 64 * rr;
+    if (gh < N) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) raw[rr][q] = *reinterpret_cast<const uint4*>(qI + gh * 128 + part * 32 + q * 8);
+      wv[rr] = w[gh];
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < kRowsPer; ++rr) {
+    const int gh = (t256 >> 2) + 64 * rr;
+    if (gh >= N) continue;  // uniform across the 4 threads of a row
+    if constexpr (!FP8) {
+      // dims 32*part.. = region (part >> 1), 16-byte chunks 4*(part & 1) .. +3
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(img + (part >> 1) * (N * 128) + sw128(gh, 4 * (part & 1) + q)) = raw[rr][q];
+      if (part == 0) wimg[gh] = wv[rr];
+    } else {
+      float x[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[rr][q]);
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          x[q * 8 + 2 * e2] = __low2float(p2[e2]);
+          x[q * 8 + 2 * e2 + 1] = __high2float(p2[e2]);
+        }
+      }
+      float am = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) am = fmaxf(am, fabsf(x[j]));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      const float sc = am > 0.f ? am / 448.f : 1.f;
+      const float inv = 1.f / sc;
+      // 32 codes = two 16-byte chunks (2*part, 2*part + 1) of the 128-byte row, hi then lo
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t hi4[4], lo4[4];
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          hi4[wd] = 0u;
+          lo4[wd] = 0u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float y = x[ch * 16 + wd * 4 + j] * inv;
+            const uint8_t chh = f_to_e4m3(y);
+            const uint8_t cl = f_to_e4m3(y - e4m3_to_f(chh));
+            hi4[wd] |= static_cast<uint32_t>(chh) << (8 * j);
+            lo4[wd] |= static_cast<uint32_t>(cl) << (8 * j);
+          }
+        }
+        const uint32_t off = sw128(gh, 2 * part + ch);
+        *reinterpret_cast<uint4*>(img + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
+        *reinterpret_cast<uint4*>(img + N * 128 + off) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+      }
+      if (part == 0) wimg[gh] = wv[rr] * sc;
+    }
   }
 }
 

@@ -78,6 +78,21 @@ def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
     return buf
 
 
+_decode_ws = {}
+
+
+def _decode_workspace(nbytes: int, device, batch: int) -> torch.Tensor:
+    """The decode step's own workspace, zero-filled when allocated: its first bytes carry the
+    top-k histograms from step to step, laid out by the batch size (one per device and batch
+    size; steps on it must be stream-ordered)."""
+    key = (str(device), batch)
+    buf = _decode_ws.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        _decode_ws[key] = buf
+    return buf
+
+
 def _ws_args(buf):
     return (None, 0) if buf is None else (ctypes.c_void_p(buf.data_ptr()), buf.numel())
 
@@ -196,6 +211,8 @@ def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_t
     a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                           _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias), _p(biasI),
                           _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse), _p(idx_out))
-    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1]), q.device)
-    wp, wb = _ws_args(ws)
+    nbytes = lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1])
+    if nbytes == ctypes.c_size_t(-1).value:
+        raise CsaError("csa_workspace_size", 2)
+    wp, wb = _ws_args(_decode_workspace(nbytes, q.device, cfg.B))
     _check("csa_decode_step", lib.csa_decode_step(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))

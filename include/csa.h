@@ -224,6 +224,11 @@ typedef struct {
  * top-k, and attend over them plus the window with the sink.  Same semantics as calling
  * csa_compress_kv (main KV and indexer keys), csa_indexer_scores, csa_topk and
  * csa_sparse_attn in that order with T = 1.
+ *
+ * Workspace state: the first bytes of ws (a fixed size that depends on cfg->B only) carry
+ * the top-k histograms from one step to the next.  ws must be zero-filled before the first
+ * call (one cudaMemsetAsync), every call leaves that region ready for the next, and it must
+ * not be handed to other calls in between.  Steps on one ws must run in stream order.
  */
 csa_status csa_decode_step(const csa_config *cfg, const csa_decode_args *args, void *ws,
                            size_t ws_bytes, csa_stream_t stream);
