@@ -136,8 +136,8 @@ IndexerArgs indexer_shape(const csa_config* c, int T, int64_t E_cap, int sms) {
 
 size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   const int64_t B = c->B;
-  // first, at a fixed offset: the top-k histograms, tickets and epochs kept across steps
-  size_t bytes = align_up(decode_hist_words(static_cast<int>(B)) * 4, 256);
+  // first, at a fixed offset: the top-k histograms and tickets kept across steps
+  size_t bytes = align_up(decode_state_words(static_cast<int>(B)) * 4, 256);
   bytes += align_up(indexer_workspace_bytes(indexer_shape(c, 1, E_cap, sms)), 256);  // query images
   bytes += align_up(static_cast<size_t>(B * E_cap) * 4, 256);  // scores
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
@@ -418,7 +418,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
 
   uint8_t* p = static_cast<uint8_t*>(ws);
   uint32_t* hist_cnt = reinterpret_cast<uint32_t*>(p);  // kept across steps (zero before the first)
-  p += align_up(decode_hist_words(cfg->B) * 4, 256);
+  p += align_up(decode_state_words(cfg->B) * 4, 256);
   void* q_images = p;
   p += align_up(indexer_workspace_bytes(indexer_shape(cfg, 1, d->E_cap, sms)), 256);
   float* scores = reinterpret_cast<float*>(p);
@@ -470,11 +470,11 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
     f.zI_tail = d->zI_tail;
     f.biasI = d->biasI;
     f.act_bf16 = cfg->act == CSA_BF16;
-    f.hist2 = hist_cnt;
+    f.hist = hist_cnt;
     ia.images_ready = true;
     e = launch_indexer(ia, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
-    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s, true);
+    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   } else {
     // 1. compress the block the new token completes (main KV, then indexer keys)

@@ -42,10 +42,8 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 // Decode step (T = 1, tensor-core path): the indexer launch also compresses the entry the
 // new token completes (main KV by the first CTA of each sequence, indexer key by the CTA
 // that scores it, before that tile is loaded), builds its query image in shared memory, and
-// accumulates the top-k histogram into one of two buffers picked by a per-sequence epoch:
-// the top-k advances the epoch after reading the histogram, and the first CTA of each
-// sequence zeroes the other buffer for the next step.  Layout of `hist2`: [2][B][4160]
-// words, then B top-k tickets, then B epochs; all zero before the first step.
+// histograms its scores into `hist` ([B][4160] rows then B top-k tickets), which the top-k
+// kernel reads and leaves zero again: zero before the first step.
 struct DecodeFuse {
   bool on;
   const void* kv_tail;   // [B, 2m, 2, d] tokens t-2m+1..t (stream a, stream b)
@@ -57,8 +55,9 @@ struct DecodeFuse {
   const void* zI_tail;
   const float* biasI;    // [2, m, dI]
   bool act_bf16;         // stream and kv_comp dtype
-  uint32_t* hist2;
+  uint32_t* hist;        // histograms + tickets
 };
+inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + B; }
 struct IndexerArgs {
   const void* qI;        // [B*T, HI, dI]
   const float* w;        // [B*T, HI]
@@ -82,7 +81,6 @@ struct IndexerArgs {
   bool images_ready;     // the query images in ws were already written (fused decode prep)
   DecodeFuse fuse;       // decode step only
 };
-inline size_t decode_hist_words(int B) { return (2 * static_cast<size_t>(B) * 4160) + 2 * static_cast<size_t>(B); }
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
 bool indexer_uses_tensor_cores(const IndexerArgs& a);
 size_t indexer_workspace_bytes(const IndexerArgs& a);
@@ -140,11 +138,9 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols);  // the candidat
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);
 size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols);
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
-// hist_cnt: [rows][4160] then rows tickets; or, with two_buffers (the decode step), the
-// DecodeFuse layout, whose epochs pick the buffer and are advanced here.
+// hist_cnt: [rows][4160] then rows tickets; left zero for the next use.
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s,
-                             bool two_buffers = false);
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s);
 
 struct PoolArgs {
   const float* scores;

@@ -153,7 +153,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 10);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   int64_t* sNew = reinterpret_cast<int64_t*>(sTmem + 2);     // decode step: new entry (-1: none)
-  uint32_t* sEpoch = sTmem + 4;                               // decode step: histogram epoch
   float* sNewScale = reinterpret_cast<float*>(sTmem + 5);
   float* sRed4 = reinterpret_cast<float*>(sTmem + 8);        // [4] decode step: key amax
   uint32_t* sHist = sTmem + 12;                               // [4096] when a histogram is kept (G == 1)
@@ -179,7 +178,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         // the entry the token completes (compressed in this launch), if it fits the cache
         const int64_t e = t >= 0 && (t + 1) % a.m == 0 ? (t + 1) / a.m - 1 : -1;
         *sNew = e < a.E_cap ? e : -1;
-        *sEpoch = __ldcg(a.fuse.hist2 + 2 * static_cast<size_t>(a.B) * kTopkHistRowWords + a.B + b);
       }
     }
     sNv[tid] = nv;
@@ -318,8 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       build_image_cta<FP8>(a, L, sB, b, tid - 64);
       fence_proxy_async_smem();
       mbar_arrive(qbar);
-      const size_t row_words = kTopkHistRowWords, bw = static_cast<size_t>(a.B) * row_words;
-      hist_row = a.fuse.hist2 + (*sEpoch & 1u) * bw + b * row_words;
+      hist_row = a.fuse.hist + static_cast<size_t>(b) * kTopkHistRowWords;
       // the new key entry, if this CTA scores it (first epilogue group, one channel a thread)
       const bool own_new =
           e_new >= 0 && n_it > 0 && static_cast<int64_t>(tile_lo + (n_it - 1) * tile_step) == e_new / kTile;
@@ -330,12 +327,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
           mbar_arrive(kbar);
         }
       }
-      if (split == 0) {
-        // the sequence's new main-KV entry, and the other histogram buffer zeroed for the next step
-        if (e_new >= 0) decode_new_kv(a, b, e_new, tid - 64);
-        uint32_t* other = a.fuse.hist2 + ((*sEpoch + 1u) & 1u) * bw + b * row_words;
-        for (int i = tid - 64; i < kTopkHistRowWords; i += 32 * kEpiWarps) other[i] = 0u;
-      }
+      // the sequence's new main-KV entry
+      if (split == 0 && e_new >= 0) decode_new_kv(a, b, e_new, tid - 64);
     }
     const bool w_ok = mbar_wait(qbar, 0, a.err, sAbort);  // gates landed with the query image
     const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
@@ -390,7 +383,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         const uint32_t c = sHist[i];
         if (c) atomicAdd(&rh[i], c);
       }
-      if (tid - 64 < kTopkHistCoarse) {
+      if (!fuse && tid - 64 < kTopkHistCoarse) {
         const int cb = tid - 64;
         constexpr int per = kTopkHistBins / kTopkHistCoarse;
         uint32_t c = 0;
@@ -449,6 +442,7 @@ TcLayout plan_tc(const IndexerArgs& a) {
 }  // namespace
 
 IndexerLayout indexer_layout(const IndexerArgs& a) { return plan_tc(a); }
+
 
 bool indexer_uses_tensor_cores(const IndexerArgs& a) {
   return a.cand == nullptr && a.act == CSA_BF16 && a.dI == 128 && (a.HI == 32 || a.HI == 64 || a.HI == 128) &&

@@ -21,6 +21,7 @@
 
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
+#include "select_dev.cuh"
 
 namespace csa {
 namespace {
@@ -46,46 +47,6 @@ __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int64_t row
   return v < 0 ? 0 : (v < n_cols ? v : n_cols);
 }
 
-// One warp: the largest index b of 64 bins (values cnt(b)) whose suffix count reaches `need`;
-// returns -1 when the 64 bins hold fewer than `need`, else b and (via *above) the count of
-// the bins above b.
-__device__ __forceinline__ int warp_suffix_find64(const uint32_t* bins, uint32_t need, uint32_t* above) {
-  const int lane = threadIdx.x & 31;
-  // lane l owns bins 63-2l and 62-2l (descending), so a prefix scan runs from the top
-  const uint32_t c_hi = __ldcg(bins + 63 - 2 * lane);
-  const uint32_t c_lo = __ldcg(bins + 62 - 2 * lane);
-  const uint32_t mine = c_hi + c_lo;
-  uint32_t incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const uint32_t excl = incl - mine;  // count of the bins above this lane's pair
-  const uint32_t hit = __ballot_sync(0xffffffffu, incl >= need);
-  if (hit == 0u) return -1;
-  const int l = __ffs(hit) - 1;  // first lane (from the top) whose inclusive count reaches need
-  const uint32_t ex = __shfl_sync(0xffffffffu, excl, l);
-  const uint32_t ch = __shfl_sync(0xffffffffu, c_hi, l);
-  if (ex + ch >= need) {
-    *above = ex;
-    return 63 - 2 * l;
-  }
-  *above = ex + ch;
-  return 62 - 2 * l;
-}
-
-// Threshold fine digit of a row (warp 0 of the block calls it); 0 when fewer than k scores.
-__device__ uint32_t threshold_digit(const uint32_t* row_hist, int k) {
-  const uint32_t* fine = row_hist;
-  const uint32_t* coarse = row_hist + kFine;
-  uint32_t above_c = 0, above_f = 0;
-  const int c = warp_suffix_find64(coarse, static_cast<uint32_t>(k), &above_c);
-  if (c < 0) return 0u;
-  const int f = warp_suffix_find64(fine + c * 64, static_cast<uint32_t>(k) - above_c, &above_f);
-  return static_cast<uint32_t>(c * 64 + (f < 0 ? 0 : f));
-}
-
 __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
                                                              int64_t n_cols, uint32_t* hist, int chunk) {
   __shared__ uint32_t h[kFine];
@@ -107,91 +68,6 @@ __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores
     for (int j = 0; j < 64; ++j) s += h[threadIdx.x * 64 + j];
     if (s) atomicAdd(&rh[kFine + threadIdx.x], s);
   }
-}
-
-// Largest-`want` selection among candidate values (block-wide, radix passes of up to 10
-// bits over the low `lo_bits` bits; the bits above are fixed to `prefix` under `mask`): on
-// return the `want` largest are every value > *T plus *quota values equal to *T.  The caller
-// guarantees at least `want` values match the fixed bits.
-template <typename F>
-__device__ void block_select_largest(F val, int n, int want, int lo_bits, uint32_t prefix, uint32_t mask,
-                                     uint32_t* hist, uint32_t* tmp, uint32_t* res, uint32_t* T, int* quota) {
-  int kk = want;
-  int shift = lo_bits;
-  while (shift > 0) {
-    const int wbits = shift < 10 ? shift : 10;
-    shift -= wbits;
-    const int nb = 1 << wbits;
-    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0u;
-    __syncthreads();
-    for (int e = threadIdx.x; e < n; e += NT) {
-      const uint32_t v = val(e);
-      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
-    }
-    __syncthreads();
-    // thread t owns bins nb-1-2t and nb-2-2t (descending), so the exclusive scan counts from the top
-    uint32_t local = 0;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int bin = nb - 1 - (2 * static_cast<int>(threadIdx.x) + q);
-      if (bin >= 0) local += hist[bin];
-    }
-    uint32_t run = block_exclusive_scan<NT>(local, tmp, nullptr);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int bin = nb - 1 - (2 * static_cast<int>(threadIdx.x) + q);
-      if (bin < 0) break;
-      const uint32_t h = hist[bin];
-      if (run < static_cast<uint32_t>(kk) && run + h >= static_cast<uint32_t>(kk)) {
-        res[0] = static_cast<uint32_t>(bin);
-        res[1] = run;
-      }
-      run += h;
-    }
-    __syncthreads();
-    kk -= static_cast<int>(res[1]);
-    prefix |= res[0] << shift;
-    mask |= static_cast<uint32_t>(nb - 1) << shift;
-    __syncthreads();
-  }
-  *T = prefix;
-  *quota = kk;
-}
-
-// Winners in ascending position: counting sort by position bucket, then rank inside the
-// bucket (positions are distinct); -1 after the n_sel winners.
-__device__ void write_sorted(const int32_t* sel, int n_sel, int k, int64_t nvr, uint32_t* hist, uint32_t* tmp,
-                             int32_t* srt, int32_t* out) {
-  const int tid = threadIdx.x;
-  int shift = 0;
-  while ((nvr >> shift) >= kSortBuckets) ++shift;
-  for (int i = tid; i < kSortBuckets; i += NT) hist[i] = 0u;
-  __syncthreads();
-  for (int j = tid; j < n_sel; j += NT) atomicAdd(&hist[sel[j] >> shift], 1u);
-  __syncthreads();
-  constexpr int bpt = kSortBuckets / NT;  // 2
-  const uint32_t c0 = hist[tid * bpt], c1 = hist[tid * bpt + 1];
-  const uint32_t start = block_exclusive_scan<NT>(c0 + c1, tmp, nullptr);
-  hist[tid * bpt] = start;  // bucket starts (exclusive prefix)
-  hist[tid * bpt + 1] = start + c0;
-  uint32_t* fill = hist + kSortBuckets;
-  for (int i = tid; i < kSortBuckets; i += NT) fill[i] = 0u;
-  __syncthreads();
-  for (int j = tid; j < n_sel; j += NT) {
-    const int32_t p = sel[j];
-    const int bkt = p >> shift;
-    srt[hist[bkt] + atomicAdd(&fill[bkt], 1u)] = p;
-  }
-  __syncthreads();
-  for (int j = tid; j < n_sel; j += NT) {
-    const int32_t p = sel[j];
-    const int bkt = p >> shift;
-    const int b0 = static_cast<int>(hist[bkt]), n_b = static_cast<int>(fill[bkt]);
-    int rank = 0;
-    for (int i = 0; i < n_b; ++i) rank += srt[b0 + i] < p;
-    out[b0 + rank] = p;
-  }
-  for (int j = n_sel + tid; j < k; j += NT) out[j] = -1;
 }
 
 // One CTA per (row, chunk of kSelChunk positions).  Every CTA finds the threshold digit b1
@@ -225,35 +101,9 @@ struct SelSmem {
 
 size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
 
-// Largest fine digit whose suffix count reaches k (0 when the row has fewer than k scores),
-// from one coalesced read of the row's 4096 fine bins.
-__device__ uint32_t block_threshold_digit(const uint32_t* fine, int k, uint32_t* tmp, uint32_t* res) {
-  const int tid = threadIdx.x;
-  constexpr int per = kFine / NT;  // 8
-  uint32_t c[per];
-  uint32_t mine = 0;
-#pragma unroll
-  for (int q = 0; q < per; ++q) {  // thread t owns bins 4095-8t .. 4088-8t (descending)
-    c[q] = __ldcg(fine + kFine - 1 - (tid * per + q));
-    mine += c[q];
-  }
-  if (tid == 0) res[4] = 0u;
-  uint32_t run = block_exclusive_scan<NT>(mine, tmp, nullptr);
-#pragma unroll
-  for (int q = 0; q < per; ++q) {
-    if (run < static_cast<uint32_t>(k) && run + c[q] >= static_cast<uint32_t>(k))
-      res[4] = static_cast<uint32_t>(kFine - 1 - (tid * per + q));
-    run += c[q];
-  }
-  __syncthreads();
-  const uint32_t b1 = res[4];
-  __syncthreads();
-  return b1;
-}
-
 __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
                                                          int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
-                                                         uint32_t* cand, int n_chunks, bool two_buffers) {
+                                                         uint32_t* cand, int n_chunks) {
   extern __shared__ __align__(16) uint8_t sel_raw[];
   SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
   int32_t* sel = reinterpret_cast<int32_t*>(sel_raw + sizeof(SelSmem));  // [k] (whole-row path)
@@ -283,13 +133,11 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
 #pragma unroll
     for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < nvr ? __ldcg(srow + t0 + u) : 0.f;
   }
-  // histogram rows, then the tickets (and with two buffers: [2][rows] rows, tickets, epochs)
+  // histogram rows, then the tickets
   const int64_t rows = gridDim.y;
-  uint32_t* ticket = hist + (two_buffers ? 2 : 1) * rows * kRowWords + row;
-  uint32_t* epoch = two_buffers ? hist + 2 * rows * kRowWords + rows + row : nullptr;
-  const uint32_t buf = two_buffers ? (__ldcg(epoch) & 1u) : 0u;
-  uint32_t* rh = hist + (buf * rows + row) * kRowWords;
-  const uint32_t b1 = block_threshold_digit(rh, k, S.tmp, S.res);
+  uint32_t* ticket = hist + rows * kRowWords + row;
+  uint32_t* rh = hist + row * kRowWords;
+  const uint32_t b1 = team_threshold_digit<NT>(rh, k, S.tmp, S.res, tid, 0);
   uint32_t key[kSelPer];
   uint32_t cnt = 0;
 #pragma unroll
@@ -324,11 +172,9 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   __syncthreads();
   if (!S.last) return;
   __threadfence();
-  // every CTA of the row has read the histogram: reset the ticket, advance the epoch
-  if (tid == 0) {
-    *ticket = 0u;
-    if (epoch) *epoch = buf + 1u + (__ldcg(epoch) & ~1u);
-  }
+  // every CTA of the row has read the histogram: clear it and the ticket for the next use
+  for (int i = tid; i < kRowWords; i += NT) rh[i] = 0u;
+  if (tid == 0) *ticket = 0u;
 
   // ---- the row's last CTA: gather the candidates in chunk (= position) order
   const uint32_t* base = cand + static_cast<size_t>(row) * n_chunks * kSlotWords;
@@ -377,8 +223,8 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
     int quota = 0x7fffffff;
     if (n_all - static_cast<int>(n_gt) > need) {
       const uint32_t* ak = S.ak;
-      block_select_largest([ak](int x) { return ak[x]; }, n_all, need, 20, b1 << 20, 0xFFF00000u, S.hist, S.tmp,
-                           S.res, &T, &quota);
+      team_select_largest<NT>([ak](int x) { return ak[x]; }, n_all, need, 20, b1 << 20, 0xFFF00000u, S.hist, S.tmp,
+                           S.res, &T, &quota, tid, 0);
     }
     // stable compaction over contiguous segments: keys above T, then the first quota keys
     // equal to T in position order
@@ -423,7 +269,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
     const int n = static_cast<int>(nvr);
     uint32_t T = 1u;
     int quota = 0x7fffffff;
-    if (n > k) block_select_largest(key_at, n, k, 32, 0u, 0u, S.hist, S.tmp, S.res, &T, &quota);
+    if (n > k) team_select_largest<NT>(key_at, n, k, 32, 0u, 0u, S.hist, S.tmp, S.res, &T, &quota, tid, 0);
     if (tid == 0) S.n_gt = 0u;
     __syncthreads();
     for (int x = tid; x < n; x += NT)
@@ -446,7 +292,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
         ++r;
       }
     __syncthreads();
-    write_sorted(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow);
+    team_write_sorted<NT>(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow, tid, 0);
   }
 }
 
@@ -462,8 +308,7 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
 }
 
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s,
-                             bool two_buffers) {
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -474,7 +319,7 @@ cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int6
   const cudaError_t e =
       launch_pdl(topk_select_kernel, dim3(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows)), dim3(NT),
                  sel_smem_bytes(k), s, scores, ld, n_valid, n_cols, hist_cnt, k, idx,
-                 static_cast<uint32_t*>(ws_cand), n_chunks, two_buffers);
+                 static_cast<uint32_t*>(ws_cand), n_chunks);
   count_launches(1);
   return e;
 }
