@@ -113,14 +113,14 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   const int chunk_id = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  const int64_t nvr = row_valid(n_valid, row, n_cols);
   const float* srow = scores + row * ld;
   // this CTA's positions: thread t holds c0 + t*kSelPer .. +kSelPer-1 (contiguous, so the
-  // compaction below keeps position order); loads in flight while the threshold is read
+  // compaction below keeps position order); the loads (bounded by the row length, the
+  // visible count is applied after) are in flight with those of n_valid and the histogram
   const int64_t c0 = static_cast<int64_t>(chunk_id) * kSelChunk;
   float v[kSelPer];
   const int64_t t0 = c0 + tid * kSelPer;
-  if (t0 + kSelPer <= nvr && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+  if (t0 + kSelPer <= n_cols && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
 #pragma unroll
     for (int u = 0; u < kSelPer; u += 4) {
       const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + t0 + u));
@@ -131,8 +131,9 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
     }
   } else {
 #pragma unroll
-    for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < nvr ? __ldcg(srow + t0 + u) : 0.f;
+    for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < n_cols ? __ldcg(srow + t0 + u) : 0.f;
   }
+  const int64_t nvr = row_valid(n_valid, row, n_cols);
   // histogram rows, then the tickets
   const int64_t rows = gridDim.y;
   uint32_t* ticket = hist + rows * kRowWords + row;
@@ -165,10 +166,13 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
     }
   }
   if (tid == 0) slot[0] = n_mine;
-  // the last CTA of the row to finish selects
-  __threadfence();
+  // the last CTA of the row to finish selects (the barrier orders the CTA's slot writes
+  // before the fence of the thread that takes the ticket)
   __syncthreads();
-  if (tid == 0) S.last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(n_chunks - 1) ? 1u : 0u;
+  if (tid == 0) {
+    __threadfence();
+    S.last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(n_chunks - 1) ? 1u : 0u;
+  }
   __syncthreads();
   if (!S.last) return;
   __threadfence();

@@ -107,13 +107,22 @@ __device__ void team_select_largest(F val, int n, int want, int lo_bits, uint32_
 template <int NT>
 __device__ uint32_t team_threshold_digit(const uint32_t* fine, int k, uint32_t* tmp, uint32_t* res, int t, int bar) {
   constexpr int per = kTopkHistBins / NT;
+  static_assert(per % 4 == 0, "16-byte loads");
   uint32_t c[per];
   uint32_t mine = 0;
+  // thread t owns bins 4095 - per*t - q (descending), loaded as per/4 16-byte vectors
+  // (fine must be 16-byte aligned)
+  const uint4* src = reinterpret_cast<const uint4*>(fine + kTopkHistBins - per * (t + 1));
 #pragma unroll
-  for (int q = 0; q < per; ++q) {  // thread t owns bins 4095 - per*t - q (descending)
-    c[q] = __ldcg(fine + kTopkHistBins - 1 - (t * per + q));
-    mine += c[q];
+  for (int w = 0; w < per / 4; ++w) {
+    const uint4 x = __ldcg(src + w);
+    c[per - 1 - 4 * w] = x.x;
+    c[per - 2 - 4 * w] = x.y;
+    c[per - 3 - 4 * w] = x.z;
+    c[per - 4 - 4 * w] = x.w;
   }
+#pragma unroll
+  for (int q = 0; q < per; ++q) mine += c[q];
   if (t == 0) res[4] = 0u;
   uint32_t run = team_scan<NT>(mine, t, tmp, nullptr, bar);
 #pragma unroll
