@@ -136,6 +136,10 @@ constexpr int kTopkHistRowWords = kTopkHistBins + kTopkHistCoarse;
 int topk_hist_cap(int k);
 size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols);  // the candidate slots (ws_cand)
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);
+// Many long rows: one CTA per row with a shared-memory histogram (no workspace).
+bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k);
+cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+                             int k, int32_t* idx, cudaStream_t s);
 size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols);
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
 // hist_cnt: [rows][4160] then rows tickets; left zero for the next use.

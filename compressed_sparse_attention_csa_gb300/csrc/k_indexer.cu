@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       // the sequence's new main-KV entry
       if (split == 0 && e_new >= 0) decode_new_kv(a, b, e_new, tid - 64);
     }
-    const bool w_ok = mbar_wait(qbar, 0, a.err, sAbort);  // gates landed with the query image
+    const bool w_ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, a.err, sAbort));  // gates landed with the image
     const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
     auto scale_of = [&](int itx) -> float {
       const int64_t sx = static_cast<int64_t>(tile_lo + itx * tile_step) * kTile + rin;
@@ -341,13 +341,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       const int acc = it % NA;
       const float ksc = ks_next;
       ks_next = scale_of(it + 2);
-      if (!mbar_wait(&tfull[acc], (it / NA) & 1, a.err, sAbort)) break;
+      // (waits are made warp-uniform: the TMEM loads and the histogram below are warp-wide)
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (it / NA) & 1, a.err, sAbort))) break;
       tc_fence_after();
       const int64_t s = static_cast<int64_t>(tile_lo + it * tile_step) * kTile + rin;
       float ksc_use = ksc;
-      if (FUSE && FP8 && s == e_new) {  // the key compressed in this launch: its scale
-        if (!mbar_wait(kbar, 0, a.err, sAbort)) break;
-        ksc_use = *sNewScale;
+      if (FUSE && FP8 && __any_sync(0xffffffffu, s == e_new)) {  // the key compressed in this launch
+        if (!__all_sync(0xffffffffu, mbar_wait(kbar, 0, a.err, sAbort))) break;
+        if (s == e_new) ksc_use = *sNewScale;
       }
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
       float res[kMaxG];
@@ -372,9 +373,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
           if (g >= G || g0 + g >= T) continue;
           const float sc = res[g] * ksc_use;
           a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
-          if (hist && s < sNv[0]) atomicAdd(&sHist[f2key(sc) >> 20], 1u);
         }
       }
+      if (hist && s < n_cols && s < sNv[0]) atomicAdd(&sHist[f2key(res[0] * ksc_use) >> 20], 1u);
     }
     if (hist) {
       named_sync(6, 32 * kEpiWarps);

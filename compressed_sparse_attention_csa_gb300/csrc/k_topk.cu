@@ -386,6 +386,8 @@ size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms) {
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
   if (topk_uses_hist(a.rows, a.n_cols, a.cand != nullptr)) return launch_topk_hist_standalone(a, s);
+  if (topk_uses_rows(a.rows, a.n_cols, a.cand != nullptr, a.k))
+    return launch_topk_rows(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, a.k, a.idx, s);
   const Plan pl = make_plan(a.rows, std::max<int64_t>(a.n_cols, 1), a.k, a.num_sms);
   return run_levels(pl, a.scores, a.ld, a.rows, a.n_valid, a.cand, a.k, a.idx, static_cast<uint8_t*>(a.ws), s);
 }
@@ -413,8 +415,12 @@ cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s) {
                              bmax, static_cast<int64_t>(nbmax), nb);
   count_launches(1);
   if (e != cudaSuccess) return e;
-  const Plan pl = make_plan(a.rows, nbmax, a.n_blocks, a.num_sms);
-  e = run_levels(pl, bmax, nbmax, a.rows, nb, nullptr, a.n_blocks, sel, ws, s);
+  if (topk_uses_rows(a.rows, nbmax, false, a.n_blocks) || topk_uses_hist(a.rows, nbmax, false)) {
+    e = launch_topk_rows(bmax, nbmax, a.rows, nbmax, nb, a.n_blocks, sel, s);
+  } else {
+    const Plan pl = make_plan(a.rows, nbmax, a.n_blocks, a.num_sms);
+    e = run_levels(pl, bmax, nbmax, a.rows, nb, nullptr, a.n_blocks, sel, ws, s);
+  }
   if (e != cudaSuccess) return e;
   const int32_t* csel = sel;
   e = launch_pdl(pool_expand_kernel, dim3(static_cast<unsigned>(a.rows)), dim3(256), 0, s, csel, a.n_blocks, a.block,

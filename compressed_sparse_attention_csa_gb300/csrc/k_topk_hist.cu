@@ -300,6 +300,177 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   }
 }
 
+// ---- one CTA per row (many long rows: the prefill chunk, the block pool)
+// The row is histogrammed in shared memory (4096 fine bins of the order-preserving key), the
+// threshold bin b1 found, and the row read again (now from L2) keeping the (key, position) of
+// every score with digit >= b1 in position order (per-thread contiguous slices, one block
+// scan per batch); the exact selection then runs as in topk_select_kernel.
+constexpr int kRowAllCap = 8192;
+constexpr int kRowPer = 8;                 // scores per thread per batch
+constexpr int kRowBatch = kRowPer * NT;    // 4096
+
+struct RowSmem {
+  uint32_t hist[kFine];
+  uint32_t ak[kRowAllCap];
+  int32_t ap[kRowAllCap];
+  uint32_t sort[2 * kSortBuckets];
+  uint32_t tmp[32];
+  uint32_t res[8];
+  uint32_t n_gt;
+};
+
+size_t row_smem_bytes(int k) { return sizeof(RowSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
+
+__device__ __forceinline__ void load_row8(const float* srow, int64_t t0, int64_t n, float (&v)[kRowPer]) {
+  if (t0 + kRowPer <= n && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + t0));
+    const float4 y = __ldcg(reinterpret_cast<const float4*>(srow + t0 + 4));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+  } else {
+#pragma unroll
+    for (int u = 0; u < kRowPer; ++u) v[u] = t0 + u < n ? __ldcg(srow + t0 + u) : 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
+                                                      int64_t n_cols, int k, int32_t* idx) {
+  extern __shared__ __align__(16) uint8_t row_raw[];
+  RowSmem& S = *reinterpret_cast<RowSmem*>(row_raw);
+  int32_t* sel = reinterpret_cast<int32_t*>(row_raw + sizeof(RowSmem));  // [k] (whole-row path)
+  int32_t* srt = sel + k;
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  for (int i = tid; i < kFine; i += NT) S.hist[i] = 0u;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nvr = row_valid(n_valid, row, n_cols);
+  const float* srow = scores + row * ld;
+  auto key_of = [](float x) {
+    const uint32_t y = f2key(x);
+    return y == 0u ? 1u : y;
+  };
+  __syncthreads();
+  // pass 1: the histogram of the visible scores
+  for (int64_t base = 0; base < nvr; base += kRowBatch) {
+    float v[kRowPer];
+    const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
+    load_row8(srow, t0, nvr, v);
+#pragma unroll
+    for (int u = 0; u < kRowPer; ++u)
+      if (t0 + u < nvr) atomicAdd(&S.hist[key_of(v[u]) >> 20], 1u);
+  }
+  __syncthreads();
+  const uint32_t b1 = team_threshold_digit_smem<NT>(S.hist, k, S.tmp, S.res, tid, 0);
+  // pass 2: the candidates (digit >= b1) in position order
+  uint32_t n_all = 0, n_gt = 0;
+  for (int64_t base = 0; base < nvr; base += kRowBatch) {
+    float v[kRowPer];
+    const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
+    load_row8(srow, t0, nvr, v);
+    uint32_t key[kRowPer];
+    uint32_t c = 0, g = 0;
+#pragma unroll
+    for (int u = 0; u < kRowPer; ++u) {
+      const uint32_t x = key_of(v[u]);
+      key[u] = (t0 + u < nvr && (x >> 20) >= b1) ? x : 0u;
+      c += key[u] != 0u;
+      g += key[u] != 0u && (x >> 20) > b1;
+    }
+    uint32_t tot, gtot;
+    uint32_t off = n_all + block_exclusive_scan<NT>(c, S.tmp, &tot);
+    block_exclusive_scan<NT>(g, S.tmp, &gtot);
+#pragma unroll
+    for (int u = 0; u < kRowPer; ++u) {
+      if (key[u] != 0u) {
+        if (off < static_cast<uint32_t>(kRowAllCap)) {
+          S.ak[off] = key[u];
+          S.ap[off] = static_cast<int32_t>(t0 + u);
+        }
+        ++off;
+      }
+    }
+    n_all += tot;
+    n_gt += gtot;
+  }
+  __syncthreads();
+  int32_t* orow = idx + row * k;
+  if (n_all <= static_cast<uint32_t>(kRowAllCap)) {
+    const int na = static_cast<int>(n_all);
+    const int need = k - static_cast<int>(n_gt);
+    uint32_t T = 1u;
+    int quota = 0x7fffffff;
+    if (na - static_cast<int>(n_gt) > need) {
+      const uint32_t* ak = S.ak;
+      team_select_largest<NT>([ak](int x) { return ak[x]; }, na, need, 20, b1 << 20, 0xFFF00000u, S.sort, S.tmp,
+                              S.res, &T, &quota, tid, 0);
+    }
+    // stable compaction over contiguous segments: keys above T, then the first quota keys
+    // equal to T in position order
+    const int seg = (na + NT - 1) / NT;
+    const int lo = tid * seg, hi = min(na, lo + seg);
+    uint32_t c_tie = 0;
+    for (int e = lo; e < hi; ++e) c_tie += S.ak[e] == T;
+    uint32_t tie_r = block_exclusive_scan<NT>(c_tie, S.tmp, nullptr);
+    uint32_t c_win = 0;
+    {
+      uint32_t tr = tie_r;
+      for (int e = lo; e < hi; ++e) {
+        const uint32_t key = S.ak[e];
+        if (key > T) {
+          ++c_win;
+        } else if (key == T) {
+          if (tr < static_cast<uint32_t>(quota)) ++c_win;
+          ++tr;
+        }
+      }
+    }
+    uint32_t n_win;
+    uint32_t out = block_exclusive_scan<NT>(c_win, S.tmp, &n_win);
+    for (int e = lo; e < hi; ++e) {
+      const uint32_t key = S.ak[e];
+      bool w = key > T;
+      if (key == T) {
+        w = tie_r < static_cast<uint32_t>(quota);
+        ++tie_r;
+      }
+      if (w && out < static_cast<uint32_t>(k)) orow[out++] = S.ap[e];
+    }
+    for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
+  } else {
+    // too many candidates (a bin full of ties): select over the whole row in position order
+    const float* rowp = srow;
+    auto key_at = [rowp, key_of](int x) { return key_of(__ldcg(rowp + x)); };
+    const int n = static_cast<int>(nvr);
+    uint32_t T = 1u;
+    int quota = 0x7fffffff;
+    if (n > k) team_select_largest<NT>(key_at, n, k, 32, 0u, 0u, S.sort, S.tmp, S.res, &T, &quota, tid, 0);
+    if (tid == 0) S.n_gt = 0u;
+    __syncthreads();
+    for (int x = tid; x < n; x += NT)
+      if (key_at(x) > T) {
+        const uint32_t w = atomicAdd(&S.n_gt, 1u);
+        if (w < static_cast<uint32_t>(k)) sel[w] = x;
+      }
+    __syncthreads();
+    const int n_above = min(static_cast<int>(S.n_gt), k);
+    const int seg = (n + NT - 1) / NT;
+    const int lo = tid * seg, hi = min(n, lo + seg);
+    uint32_t c = 0;
+    for (int x = lo; x < hi; ++x) c += key_at(x) == T;
+    uint32_t n_eqT;
+    uint32_t r = block_exclusive_scan<NT>(c, S.tmp, &n_eqT);
+    const int take = min(static_cast<int>(n_eqT), max(0, min(quota, k - n_above)));
+    for (int x = lo; x < hi; ++x)
+      if (key_at(x) == T) {
+        if (r < static_cast<uint32_t>(take)) sel[n_above + r] = x;
+        ++r;
+      }
+    __syncthreads();
+    team_write_sorted<NT>(sel, n_above + take, k, nvr, S.sort, S.tmp, srt, orow, tid, 0);
+  }
+}
+
 }  // namespace
 
 int topk_hist_cap(int k) { return std::max(kAllCap, k); }
@@ -330,6 +501,24 @@ cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int6
 
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand) {
   return !has_cand && rows <= 64 && n_cols >= 16384;
+}
+
+bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k) {
+  return !has_cand && n_cols >= 2048 && k <= 4096 && !topk_uses_hist(rows, n_cols, has_cand);
+}
+
+cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+                             int k, int32_t* idx, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(row_smem_bytes(4096)));
+    attr = true;
+  }
+  const cudaError_t e = launch_pdl(topk_row_kernel, dim3(static_cast<unsigned>(rows)), dim3(NT), row_smem_bytes(k), s,
+                                   scores, ld, n_valid, n_cols, k, idx);
+  count_launches(1);
+  return e;
 }
 
 size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols) {

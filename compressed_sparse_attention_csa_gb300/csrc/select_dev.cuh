@@ -137,6 +137,32 @@ __device__ uint32_t team_threshold_digit(const uint32_t* fine, int k, uint32_t* 
   return b1;
 }
 
+// The same threshold digit from a histogram in shared memory.
+template <int NT>
+__device__ uint32_t team_threshold_digit_smem(const uint32_t* fine, int k, uint32_t* tmp, uint32_t* res, int t,
+                                              int bar) {
+  constexpr int per = kTopkHistBins / NT;
+  uint32_t c[per];
+  uint32_t mine = 0;
+#pragma unroll
+  for (int q = 0; q < per; ++q) {
+    c[q] = fine[kTopkHistBins - 1 - (t * per + q)];
+    mine += c[q];
+  }
+  if (t == 0) res[4] = 0u;
+  uint32_t run = team_scan<NT>(mine, t, tmp, nullptr, bar);
+#pragma unroll
+  for (int q = 0; q < per; ++q) {
+    if (run < static_cast<uint32_t>(k) && run + c[q] >= static_cast<uint32_t>(k))
+      res[4] = static_cast<uint32_t>(kTopkHistBins - 1 - (t * per + q));
+    run += c[q];
+  }
+  team_sync<NT>(bar);
+  const uint32_t b1 = res[4];
+  team_sync<NT>(bar);
+  return b1;
+}
+
 // Winners (distinct positions < nvr) written in ascending position: counting sort by
 // position bucket, then rank inside the bucket; -1 after the n_sel winners.
 // hist: >= 2048 words; srt: >= n_sel words.
