@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   if (tid == 0) *sAbort = 0;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], !FUSE && a.cand ? 32 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
 
   int nv_max = 0;
   for (int g = 0; g < G; ++g) nv_max = max(nv_max, sNv[g]);
+  if (!FUSE && a.cand) nv_max = a.n_cand;  // candidate slots, each checked against the visible count
   const int tiles_needed = (nv_max + kTile - 1) / kTile;
   // the splits of a row interleave tile by tile (split, split + n_splits, ...)
   const int tile_lo = split, tile_step = L.n_splits;
@@ -226,7 +227,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       uint64_t pol = 0;
       bool ok = true;
       int issued = 0;
-      if (lane == 0) {
+      const bool gather = !FUSE && a.cand != nullptr;  // the decode step has no candidate lists
+      if (lane == 0 && !gather) {
         tma_prefetch_desc(&kmap);
         pol = policy_evict_first();
       }
@@ -243,7 +245,56 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         if constexpr (!FP8) tma_load_2d_hint(dst + 16384, &kmap, &full[st], 64, row, pol);
         return true;
       };
-      if (lane == 0) {
+      if (gather) {
+        // candidate mode: the warp gathers each tile's rows with 16-byte cp.async into the
+        // swizzled stage; once a stage's copies have landed it is fenced for the tensor core
+        // and its full barrier arrived on (up to S - 1 later stages stay in flight)
+        const int row_bytes = FP8 ? 128 : 256;
+        const uint8_t* kbase = static_cast<const uint8_t*>(a.kI) + static_cast<size_t>(b) * a.E_cap * row_bytes;
+        const int32_t* cb = a.cand + static_cast<int64_t>(qrow0) * a.n_cand;
+        // each lane's copies of tile j are complete: it fences them for the tensor core and
+        // arrives (the full barriers count 32 arrivals in this mode)
+        auto land = [&](int j) {
+          fence_proxy_async_smem();
+          mbar_arrive(&full[j % S]);
+        };
+        const int lag = min(S - 1, 3);  // tiles left in flight behind the newest
+        auto wait_lag = [&]() {
+          if (lag >= 3)
+            asm volatile("cp.async.wait_group 3;" ::: "memory");
+          else if (lag == 2)
+            asm volatile("cp.async.wait_group 2;" ::: "memory");
+          else
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        };
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int st = it % S;
+          if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
+          const int slot0 = (tile_lo + it * tile_step) * kTile;
+#pragma unroll
+          for (int rr = 0; rr < kTile / 32; ++rr) {
+            const int r = rr * 32 + lane;
+            const int slot = slot0 + r;
+            int64_t p = slot < a.n_cand ? cb[slot] : 0;
+            p = (p >= 0 && p < a.E_cap) ? p : 0;  // invisible or padded slots read row 0 (masked later)
+            const uint8_t* src = kbase + p * row_bytes;
+#pragma unroll
+            for (int c = 0; c < row_bytes / 16; ++c)
+              cp_async16(dst + (c >> 3) * 16384 + sw128(r, c & 7), src + c * 16);
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+          ++issued;
+          if (issued > lag) {
+            wait_lag();
+            land(it - lag);
+          }
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        for (int j = max(0, issued - lag); j < issued; ++j) land(j);
+      } else if (lane == 0) {
         for (int it = 0; ok && it < key_it; ++it) ok = issue(it), issued += ok;
         if (FUSE && own_new && ok) ok = mbar_wait(kbar, 0, a.err, sAbort);
         for (int it = key_it; ok && it < n_it; ++it) ok = issue(it), issued += ok;
@@ -332,9 +383,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     }
     const bool w_ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, a.err, sAbort));  // gates landed with the image
     const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
+    const int32_t* cand_b = !FUSE && a.cand ? a.cand + static_cast<int64_t>(qrow0) * a.n_cand : nullptr;
+    // the key row of slot sx: the slot itself, or (candidate mode) its position (-1: none)
+    auto pos_of = [&](int64_t sx) -> int64_t {
+      if (FUSE || !cand_b) return sx;
+      return sx < a.n_cand ? static_cast<int64_t>(cand_b[sx]) : -1;
+    };
     auto scale_of = [&](int itx) -> float {
-      const int64_t sx = static_cast<int64_t>(tile_lo + itx * tile_step) * kTile + rin;
-      return (FP8 && itx < n_it && sx < a.E_cap) ? kscale_b[sx] : 1.f;
+      const int64_t px = pos_of(static_cast<int64_t>(tile_lo + itx * tile_step) * kTile + rin);
+      return (FP8 && itx < n_it && (FUSE || px >= 0) && px < a.E_cap) ? kscale_b[px] : 1.f;
     };
     float ks_next = scale_of(gp);  // e4m3 key scales, prefetched one tile of this group ahead
     for (int it = gp; w_ok && it < n_it; it += 2) {
@@ -368,11 +425,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (s < n_cols) {
+        const int64_t ps = pos_of(s);  // the key's position (= s without candidates)
 #pragma unroll
         for (int g = 0; g < kMaxG; ++g) {
           if (g >= G || g0 + g >= T) continue;
           const float sc = res[g] * ksc_use;
-          a.scores[(qrow0 + g) * a.ld + s] = s < sNv[g] ? sc : -INFINITY;
+          a.scores[(qrow0 + g) * a.ld + s] = (FUSE || ps >= 0) && ps < sNv[g] ? sc : -INFINITY;
         }
       }
       if (hist && s < n_cols && s < sNv[0]) atomicAdd(&sHist[f2key(res[0] * ksc_use) >> 20], 1u);
@@ -414,7 +472,8 @@ TcLayout plan_tc(const IndexerArgs& a) {
   L.w_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * 4, 16));
   L.stage_bytes = fp8 ? kKeyTileBytesF8 : 32768u;
   L.n_qgroups = (a.T + L.G - 1) / L.G;
-  const int tiles = static_cast<int>((a.E_cap + kTile - 1) / kTile);
+  const int64_t n_cols = a.cand ? a.n_cand : a.E_cap;  // candidate slots or cache positions
+  const int tiles = static_cast<int>((n_cols + kTile - 1) / kTile);
   const int64_t groups = static_cast<int64_t>(a.B) * L.n_qgroups;
   // few long rows (decode): two CTAs per SM, key range split over them
   const bool decode_like = groups < a.num_sms;
@@ -446,8 +505,9 @@ IndexerLayout indexer_layout(const IndexerArgs& a) { return plan_tc(a); }
 
 
 bool indexer_uses_tensor_cores(const IndexerArgs& a) {
-  return a.cand == nullptr && a.act == CSA_BF16 && a.dI == 128 && (a.HI == 32 || a.HI == 64 || a.HI == 128) &&
-         (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
+  // candidate lists on the tensor cores for one query per sequence (the CSA2 Reindex step)
+  return (a.cand == nullptr || (a.T == 1 && !a.fuse.on && a.hist_out == nullptr)) && a.act == CSA_BF16 &&
+         a.dI == 128 && (a.HI == 32 || a.HI == 64 || a.HI == 128) && (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
 }
 
 size_t indexer_workspace_bytes(const IndexerArgs& a) {

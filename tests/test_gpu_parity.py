@@ -126,6 +126,35 @@ def test_indexer_tensor_cores(HI, T, fp8):
     print(f"indexer HI={HI} T={T} fp8={fp8}: worst/tol = {worst:.3f}")
 
 
+@pytest.mark.parametrize("HI,fp8,B,n_cand", [(64, False, 3, 128 * 5 + 19), (64, True, 3, 128 * 5 + 19),
+                                             (32, False, 2, 40), (64, True, 160, 300)])
+def test_indexer_tensor_cores_candidates(HI, fp8, B, n_cand):
+    """Candidate lists (one query per sequence) scored on the tensor cores: each slot holds the
+    score of its position, -inf for -1 and for positions not yet visible; duplicates allowed."""
+    dI, m, E = 128, 4, 128 * 7 + 45
+    qI = rnd(31 + HI, (B, 1, HI, dI), dI ** -0.5, BF16)
+    w = rnd(32, (B, 1, HI))
+    kf = rnd(33, (B, E, dI), dI ** -0.5)
+    kI, ks = gen.quantize_keys_e4m3(kf) if fp8 else (kf.to(BF16), None)
+    g = torch.Generator().manual_seed(n_cand + B)
+    q_pos = torch.randint(m * 300, m * E + 40, (B,), generator=g).to(torch.int64)
+    q_pos[0] = m * E - 1
+    cand = torch.randint(0, E, (B, n_cand), generator=g).to(torch.int32)
+    cand[:, n_cand - 7:] = -1                    # padded tail
+    cand[:, 3] = -1                              # a hole
+    cand[:, 5] = cand[:, 4]                      # a duplicate
+    c = cfg_obj(B=B, HI=HI, dI=dI, m=m, fp8_keys=fp8)
+    scores = torch.full((B, n_cand + 3), 3.0, device=DEV)
+    csa.indexer_scores(c, qI, w, q_pos.to(DEV), kI, scores, kscale=ks, cand=cand.to(DEV).contiguous())
+    check_dev_error()
+    got = np64(scores)
+    assert np.all(got[:, n_cand:] == 3.0)
+    ref = _indexer_ref(qI, w, q_pos, keys_f64(kI, ks), m, 1)
+    cn = cand.numpy()
+    ref_c = np.where(cn >= 0, np.take_along_axis(ref, np.maximum(cn, 0), axis=1), -np.inf)
+    assert_scores_close(got[:, :n_cand], ref_c, 5e-2 if fp8 else 1e-2)
+
+
 def test_indexer_cuda_core_fp32_and_candidates():
     cfg = gen.CONFIGS[1].replace(mode="decode")
     inp = gen.make_inputs(cfg, DEV)
