@@ -139,12 +139,13 @@ bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);
 // Many long rows: one CTA per row with a shared-memory histogram (no workspace).
 bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k);
 cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             int k, int32_t* idx, cudaStream_t s);
+                             int k, int32_t* idx, cudaStream_t s, const int32_t* cmap = nullptr);
 size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols);
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
 // hist_cnt: [rows][4160] then rows tickets; left zero for the next use.
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s);
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s,
+                             const int32_t* cmap = nullptr);
 
 struct PoolArgs {
   const float* scores;

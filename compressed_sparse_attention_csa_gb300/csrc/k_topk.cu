@@ -270,8 +270,16 @@ size_t level_smem(int chunk, bool raw) {
   return (static_cast<size_t>(chunk) * (raw ? 1 : 2) + kHistBins + 32 + 3 * NW + 4) * 4;
 }
 
-__global__ void blockmax_kernel(const float* scores, int64_t ld, int64_t n_cols, const int32_t* n_valid,
-                                int block, float* bmax, int64_t ld_b, int32_t* nb_out) {
+// Block maxima of a row (4 consecutive blocks per thread); with `hist`, also the row's
+// histogram of their order-preserving keys (4096 bins of key >> 20, added to a zeroed row of
+// kTopkHistRowWords words) for the histogram-guided top-k.
+constexpr int kBmaxPer = 4;
+constexpr int kBmaxThreads = 256;
+
+__global__ void __launch_bounds__(kBmaxThreads) blockmax_kernel(const float* scores, int64_t ld, int64_t n_cols,
+                                                                const int32_t* n_valid, int block, float* bmax,
+                                                                int64_t ld_b, int32_t* nb_out, uint32_t* hist) {
+  __shared__ uint32_t h[kTopkHistBins];
   pdl_wait();
   pdl_trigger();
   const int64_t row = blockIdx.y;
@@ -279,47 +287,92 @@ __global__ void blockmax_kernel(const float* scores, int64_t ld, int64_t n_cols,
   nv = nv < n_cols ? nv : n_cols;
   nv = nv < 0 ? 0 : nv;
   const int64_t nb = (nv + block - 1) / block;
-  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (blockIdx.x == 0 && threadIdx.x == 0) nb_out[row] = static_cast<int32_t>(nb);
-  if (j >= nb) return;
-  const float* s = scores + row * ld;
-  const int64_t hi = std::min<int64_t>((j + 1) * block, nv);
-  float m = -INFINITY;
-  for (int64_t p = j * block; p < hi; ++p) m = fmaxf(m, s[p]);
-  bmax[row * ld_b + j] = m;
+  if (hist) {
+    for (int i = threadIdx.x; i < kTopkHistBins; i += kBmaxThreads) h[i] = 0u;
+    __syncthreads();
+  }
+  const float* srow = scores + row * ld;
+  const int64_t j0 = (static_cast<int64_t>(blockIdx.x) * kBmaxThreads + threadIdx.x) * kBmaxPer;
+  float m[kBmaxPer];
+  const bool vec = block == 8 && j0 + kBmaxPer <= nb && (j0 + kBmaxPer) * 8 <= nv &&
+                   (reinterpret_cast<uintptr_t>(srow + j0 * 8) & 15) == 0;
+  if (vec) {
+    float4 x[2 * kBmaxPer];
+#pragma unroll
+    for (int u = 0; u < 2 * kBmaxPer; ++u) x[u] = __ldcg(reinterpret_cast<const float4*>(srow + j0 * 8) + u);
+#pragma unroll
+    for (int u = 0; u < kBmaxPer; ++u) {
+      const float4 a = x[2 * u], b = x[2 * u + 1];
+      m[u] = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kBmaxPer; ++u) {
+      const int64_t j = j0 + u;
+      m[u] = -INFINITY;
+      if (j < nb) {
+        const int64_t hi = std::min<int64_t>((j + 1) * block, nv);
+        for (int64_t p = j * block; p < hi; ++p) m[u] = fmaxf(m[u], srow[p]);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kBmaxPer; ++u) {
+    const int64_t j = j0 + u;
+    if (j < nb) {
+      bmax[row * ld_b + j] = m[u];
+      if (hist) atomicAdd(&h[f2key(m[u]) >> 20], 1u);
+    }
+  }
+  if (hist) {
+    __syncthreads();
+    uint32_t* rh = hist + row * kTopkHistRowWords;
+    for (int i = threadIdx.x; i < kTopkHistBins; i += kBmaxThreads)
+      if (h[i]) atomicAdd(&rh[i], h[i]);
+  }
 }
 
+// Expands the kept blocks (ascending, -1 padded) to their visible positions: thread t of the
+// row's grid writes slots 4t..4t+3.  The top-k keeps exactly min(n_blocks, nb) blocks, and only
+// the row's last block (index nb - 1, then last in ascending order) can be partial, so the
+// pool's size follows without a reduction.
 __global__ void pool_expand_kernel(const int32_t* sel, int n_blocks, int block, const int32_t* n_valid,
                                    int64_t n_cols, int32_t* pool, int32_t* pool_count) {
-  __shared__ uint32_t tmp[32];
   pdl_wait();
   pdl_trigger();
-  const int64_t row = blockIdx.x;
+  const int64_t row = blockIdx.y;
   int64_t nv = n_valid ? n_valid[row] : n_cols;
   nv = nv < n_cols ? nv : n_cols;
+  nv = nv < 0 ? 0 : nv;
   const int64_t width = static_cast<int64_t>(n_blocks) * block;
-  uint32_t cnt = 0;
-  for (int64_t i = threadIdx.x; i < width; i += blockDim.x) {
-    const int slot = static_cast<int>(i / block), o = static_cast<int>(i % block);
-    const int32_t j = sel[row * n_blocks + slot];
-    const int64_t ppos = static_cast<int64_t>(j) * block + o;
-    const bool ok = j >= 0 && ppos < nv;
-    pool[row * width + i] = ok ? static_cast<int32_t>(ppos) : -1;
-    cnt += ok;
-  }
-  if (pool_count) {
-    uint32_t total;
-    // blockDim.x == 256 for this kernel
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t* srow = sel + row * n_blocks;
+  const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i0 < width) {
+    int32_t o[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0) tmp[warp] = cnt;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      total = 0;
-      for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) total += tmp[w];
-      pool_count[row] = static_cast<int32_t>(total);
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u;
+      o[u] = -1;
+      if (i < width) {
+        const int32_t j = __ldg(srow + i / block);
+        const int64_t ppos = static_cast<int64_t>(j) * block + i % block;
+        if (j >= 0 && ppos < nv) o[u] = static_cast<int32_t>(ppos);
+      }
     }
+    int32_t* dst = pool + row * width + i0;
+    if ((width & 3) == 0) {
+      *reinterpret_cast<int4*>(dst) = make_int4(o[0], o[1], o[2], o[3]);
+    } else {
+      for (int u = 0; u < 4 && i0 + u < width; ++u) dst[u] = o[u];
+    }
+  }
+  if (pool_count && blockIdx.x == 0 && threadIdx.x == 0) {
+    const int64_t nb = (nv + block - 1) / block;
+    const int64_t n_sel = nb < n_blocks ? nb : n_blocks;
+    int64_t cnt = n_sel * block;
+    if (n_sel > 0 && srow[n_sel - 1] == nb - 1) cnt -= nb * block - nv;
+    pool_count[row] = static_cast<int32_t>(cnt);
   }
 }
 
@@ -387,7 +440,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
   if (topk_uses_hist(a.rows, a.n_cols, a.cand != nullptr)) return launch_topk_hist_standalone(a, s);
   if (topk_uses_rows(a.rows, a.n_cols, a.cand != nullptr, a.k))
-    return launch_topk_rows(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, a.k, a.idx, s);
+    return launch_topk_rows(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, a.k, a.idx, s, a.cand);
   const Plan pl = make_plan(a.rows, std::max<int64_t>(a.n_cols, 1), a.k, a.num_sms);
   return run_levels(pl, a.scores, a.ld, a.rows, a.n_valid, a.cand, a.k, a.idx, static_cast<uint8_t*>(a.ws), s);
 }
@@ -397,7 +450,10 @@ size_t pool_workspace_bytes(int64_t rows, int64_t n_cols, int block, int n_block
   const size_t bm = align_up(static_cast<size_t>(rows * std::max<int64_t>(nbmax, 1)) * 4, 256);
   const size_t nb = align_up(static_cast<size_t>(rows) * 4, 256);
   const size_t sel = align_up(static_cast<size_t>(rows) * n_blocks * 4, 256);
-  return bm + nb + sel + levels_ws(make_plan(rows, std::max<int64_t>(nbmax, 1), n_blocks, num_sms), rows, n_blocks);
+  const size_t rest = topk_uses_hist(rows, std::max<int64_t>(nbmax, 1), false)
+                          ? topk_hist_standalone_bytes(rows, std::max<int64_t>(nbmax, 1))
+                          : levels_ws(make_plan(rows, std::max<int64_t>(nbmax, 1), n_blocks, num_sms), rows, n_blocks);
+  return bm + nb + sel + rest;
 }
 
 cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s) {
@@ -410,12 +466,26 @@ cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s) {
   ws += align_up(static_cast<size_t>(a.rows) * 4, 256);
   int32_t* sel = reinterpret_cast<int32_t*>(ws);
   ws += align_up(static_cast<size_t>(a.rows) * a.n_blocks * 4, 256);
-  dim3 g1(static_cast<unsigned>((nbmax + 255) / 256), static_cast<unsigned>(a.rows));
-  cudaError_t e = launch_pdl(blockmax_kernel, g1, dim3(256), 0, s, a.scores, a.ld, a.n_cols, a.n_valid, a.block,
-                             bmax, static_cast<int64_t>(nbmax), nb);
+  // few rows of many blocks: the block maxima are histogrammed as they are made, and the
+  // histogram-guided top-k (several CTAs per row) selects the blocks
+  const bool by_hist = topk_uses_hist(a.rows, nbmax, false);
+  uint32_t* hist = nullptr;
+  cudaError_t e = cudaSuccess;
+  if (by_hist) {
+    hist = reinterpret_cast<uint32_t*>(ws);
+    e = cudaMemsetAsync(hist, 0, static_cast<size_t>(a.rows) * (kTopkHistRowWords + 1) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t per_cta = static_cast<int64_t>(kBmaxThreads) * kBmaxPer;
+  dim3 g1(static_cast<unsigned>((nbmax + per_cta - 1) / per_cta), static_cast<unsigned>(a.rows));
+  e = launch_pdl(blockmax_kernel, g1, dim3(kBmaxThreads), 0, s, a.scores, a.ld, a.n_cols, a.n_valid, a.block, bmax,
+                 static_cast<int64_t>(nbmax), nb, hist);
   count_launches(1);
   if (e != cudaSuccess) return e;
-  if (topk_uses_rows(a.rows, nbmax, false, a.n_blocks) || topk_uses_hist(a.rows, nbmax, false)) {
+  if (by_hist) {
+    const size_t hbytes = align_up(static_cast<size_t>(a.rows) * (kTopkHistRowWords + 1) * 4, 256);
+    e = launch_topk_hist(bmax, nbmax, a.rows, nbmax, nb, hist, a.n_blocks, sel, ws + hbytes, a.num_sms, s);
+  } else if (topk_uses_rows(a.rows, nbmax, false, a.n_blocks)) {
     e = launch_topk_rows(bmax, nbmax, a.rows, nbmax, nb, a.n_blocks, sel, s);
   } else {
     const Plan pl = make_plan(a.rows, nbmax, a.n_blocks, a.num_sms);
@@ -423,8 +493,10 @@ cudaError_t launch_block_pool(const PoolArgs& a, cudaStream_t s) {
   }
   if (e != cudaSuccess) return e;
   const int32_t* csel = sel;
-  e = launch_pdl(pool_expand_kernel, dim3(static_cast<unsigned>(a.rows)), dim3(256), 0, s, csel, a.n_blocks, a.block,
-                 a.n_valid, a.n_cols, a.pool, a.pool_count);
+  const int64_t width = static_cast<int64_t>(a.n_blocks) * a.block;
+  const dim3 ge(static_cast<unsigned>((width + 1023) / 1024), static_cast<unsigned>(a.rows));
+  e = launch_pdl(pool_expand_kernel, ge, dim3(256), 0, s, csel, a.n_blocks, a.block, a.n_valid, a.n_cols, a.pool,
+                 a.pool_count);
   count_launches(1);
   return e;
 }

@@ -47,15 +47,43 @@ __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int64_t row
   return v < 0 ? 0 : (v < n_cols ? v : n_cols);
 }
 
+// Slots of a candidate row before its first -1 (the map is ascending positions, then -1
+// padding), among the first nv: a 32-way search by the whole warp, identical in every lane.
+__device__ int64_t warp_cand_prefix(const int32_t* cm, int64_t nv) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = 0, hi = nv;  // the first -1 slot (or nv) lies in [lo, hi]
+  while (hi > lo) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t p = lo + lane * step;
+    const bool neg = p < hi ? __ldg(cm + p) < 0 : true;
+    const uint32_t m = __ballot_sync(0xffffffffu, neg);
+    if (m == 0u) {
+      lo += 31 * step + 1;
+    } else {
+      const int f = __ffs(m) - 1;
+      if (f == 0) {
+        hi = lo;
+      } else {
+        const int64_t pf = lo + f * step;
+        lo += (f - 1) * step + 1;
+        hi = pf < hi ? pf : hi;
+      }
+    }
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                             int64_t n_cols, uint32_t* hist, int chunk) {
+                                                             int64_t n_cols, uint32_t* hist, int chunk,
+                                                             const int32_t* cmap) {
   __shared__ uint32_t h[kFine];
   pdl_wait();
   pdl_trigger();
   for (int i = threadIdx.x; i < kFine; i += NT) h[i] = 0u;
   __syncthreads();
   const int64_t row = blockIdx.y;
-  const int64_t nv = row_valid(n_valid, row, n_cols);
+  int64_t nv = row_valid(n_valid, row, n_cols);
+  if (cmap) nv = warp_cand_prefix(cmap + row * n_cols, nv);
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
   for (int64_t s = c0 + threadIdx.x; s < c1; s += NT) atomicAdd(&h[f2key(scores[row * ld + s]) >> 20], 1u);
@@ -103,7 +131,7 @@ size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(
 
 __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
                                                          int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
-                                                         uint32_t* cand, int n_chunks) {
+                                                         uint32_t* cand, int n_chunks, const int32_t* cmap) {
   extern __shared__ __align__(16) uint8_t sel_raw[];
   SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
   int32_t* sel = reinterpret_cast<int32_t*>(sel_raw + sizeof(SelSmem));  // [k] (whole-row path)
@@ -133,7 +161,8 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
 #pragma unroll
     for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < n_cols ? __ldcg(srow + t0 + u) : 0.f;
   }
-  const int64_t nvr = row_valid(n_valid, row, n_cols);
+  int64_t nvr = row_valid(n_valid, row, n_cols);
+  if (cmap) nvr = warp_cand_prefix(cmap + row * n_cols, nvr);
   // histogram rows, then the tickets
   const int64_t rows = gridDim.y;
   uint32_t* ticket = hist + rows * kRowWords + row;
@@ -204,6 +233,8 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   __syncthreads();
   const int n_all = static_cast<int>(n_all_u);
   int32_t* orow = idx + row * k;
+  // with a candidate map (ascending positions) the winners' slots are written as positions
+  const int32_t* cm = cmap ? cmap + row * n_cols : nullptr;
   if (n_all <= kAllCap && n_over == 0) {
     uint32_t gt = 0;
     for (int e = tid; e < n_all; e += NT) {
@@ -259,7 +290,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
         w = tie_r < static_cast<uint32_t>(quota);
         ++tie_r;
       }
-      if (w && out < static_cast<uint32_t>(k)) orow[out++] = S.ap[e];
+      if (w && out < static_cast<uint32_t>(k)) orow[out++] = cm ? cm[S.ap[e]] : S.ap[e];
     }
     for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
   } else {
@@ -296,7 +327,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
         ++r;
       }
     __syncthreads();
-    team_write_sorted<NT>(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow, tid, 0);
+    team_write_sorted<NT>(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow, cm, tid, 0);
   }
 }
 
@@ -334,7 +365,7 @@ __device__ __forceinline__ void load_row8(const float* srow, int64_t t0, int64_t
 }
 
 __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
-                                                      int64_t n_cols, int k, int32_t* idx) {
+                                                      int64_t n_cols, int k, int32_t* idx, const int32_t* cmap) {
   extern __shared__ __align__(16) uint8_t row_raw[];
   RowSmem& S = *reinterpret_cast<RowSmem*>(row_raw);
   int32_t* sel = reinterpret_cast<int32_t*>(row_raw + sizeof(RowSmem));  // [k] (whole-row path)
@@ -344,7 +375,8 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
   for (int i = tid; i < kFine; i += NT) S.hist[i] = 0u;
   pdl_wait();
   pdl_trigger();
-  const int64_t nvr = row_valid(n_valid, row, n_cols);
+  int64_t nvr = row_valid(n_valid, row, n_cols);
+  if (cmap) nvr = warp_cand_prefix(cmap + row * n_cols, nvr);
   const float* srow = scores + row * ld;
   auto key_of = [](float x) {
     const uint32_t y = f2key(x);
@@ -395,6 +427,8 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
   }
   __syncthreads();
   int32_t* orow = idx + row * k;
+  // with a candidate map (ascending positions) the winners' slots are written as positions
+  const int32_t* cm = cmap ? cmap + row * n_cols : nullptr;
   if (n_all <= static_cast<uint32_t>(kRowAllCap)) {
     const int na = static_cast<int>(n_all);
     const int need = k - static_cast<int>(n_gt);
@@ -434,7 +468,7 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
         w = tie_r < static_cast<uint32_t>(quota);
         ++tie_r;
       }
-      if (w && out < static_cast<uint32_t>(k)) orow[out++] = S.ap[e];
+      if (w && out < static_cast<uint32_t>(k)) orow[out++] = cm ? cm[S.ap[e]] : S.ap[e];
     }
     for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
   } else {
@@ -467,7 +501,7 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
         ++r;
       }
     __syncthreads();
-    team_write_sorted<NT>(sel, n_above + take, k, nvr, S.sort, S.tmp, srt, orow, tid, 0);
+    team_write_sorted<NT>(sel, n_above + take, k, nvr, S.sort, S.tmp, srt, orow, cm, tid, 0);
   }
 }
 
@@ -483,7 +517,8 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
 }
 
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s) {
+                             uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s,
+                             const int32_t* cmap) {
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -494,21 +529,20 @@ cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int6
   const cudaError_t e =
       launch_pdl(topk_select_kernel, dim3(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows)), dim3(NT),
                  sel_smem_bytes(k), s, scores, ld, n_valid, n_cols, hist_cnt, k, idx,
-                 static_cast<uint32_t*>(ws_cand), n_chunks);
+                 static_cast<uint32_t*>(ws_cand), n_chunks, cmap);
   count_launches(1);
   return e;
 }
 
-bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand) {
-  return !has_cand && rows <= 64 && n_cols >= 16384;
-}
+// (candidate maps are ascending, so slot order is position order on both paths)
+bool topk_uses_hist(int64_t rows, int64_t n_cols, bool) { return rows <= 64 && n_cols >= 16384; }
 
 bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k) {
-  return !has_cand && n_cols >= 2048 && k <= 4096 && !topk_uses_hist(rows, n_cols, has_cand);
+  return n_cols >= 2048 && k <= 4096 && !topk_uses_hist(rows, n_cols, has_cand);
 }
 
 cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             int k, int32_t* idx, cudaStream_t s) {
+                             int k, int32_t* idx, cudaStream_t s, const int32_t* cmap) {
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -516,7 +550,7 @@ cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int6
     attr = true;
   }
   const cudaError_t e = launch_pdl(topk_row_kernel, dim3(static_cast<unsigned>(rows)), dim3(NT), row_smem_bytes(k), s,
-                                   scores, ld, n_valid, n_cols, k, idx);
+                                   scores, ld, n_valid, n_cols, k, idx, cmap);
   count_launches(1);
   return e;
 }
@@ -533,11 +567,12 @@ cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int chunk = 8192;
   dim3 g(static_cast<unsigned>((a.n_cols + chunk - 1) / chunk), static_cast<unsigned>(a.rows));
-  e = launch_pdl(topk_hist_build_kernel, g, dim3(NT), 0, s, a.scores, a.ld, a.n_valid, a.n_cols, hist_cnt, chunk);
+  e = launch_pdl(topk_hist_build_kernel, g, dim3(NT), 0, s, a.scores, a.ld, a.n_valid, a.n_cols, hist_cnt, chunk,
+                 a.cand);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return launch_topk_hist(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, hist_cnt, a.k, a.idx,
-                          w + align_up(hbytes, 256), a.num_sms, s);
+                          w + align_up(hbytes, 256), a.num_sms, s, a.cand);
 }
 
 }  // namespace csa

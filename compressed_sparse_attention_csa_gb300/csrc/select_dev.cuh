@@ -164,11 +164,12 @@ __device__ uint32_t team_threshold_digit_smem(const uint32_t* fine, int k, uint3
 }
 
 // Winners (distinct positions < nvr) written in ascending position: counting sort by
-// position bucket, then rank inside the bucket; -1 after the n_sel winners.
+// position bucket, then rank inside the bucket; -1 after the n_sel winners.  With `map`
+// (ascending), winner p is written as map[p].
 // hist: >= 2048 words; srt: >= n_sel words.
 template <int NT>
 __device__ void team_write_sorted(const int32_t* sel, int n_sel, int k, int64_t nvr, uint32_t* hist, uint32_t* tmp,
-                                  int32_t* srt, int32_t* out, int t, int bar) {
+                                  int32_t* srt, int32_t* out, const int32_t* map, int t, int bar) {
   constexpr int kBuckets = 1024;
   constexpr int per = kBuckets / NT;
   int shift = 0;
@@ -205,7 +206,7 @@ __device__ void team_write_sorted(const int32_t* sel, int n_sel, int k, int64_t 
     const int b0 = static_cast<int>(hist[bkt]), n_b = static_cast<int>(fill[bkt]);
     int rank = 0;
     for (int i = 0; i < n_b; ++i) rank += srt[b0 + i] < p;
-    out[b0 + rank] = p;
+    out[b0 + rank] = map ? map[p] : p;
   }
   for (int j = n_sel + t; j < k; j += NT) out[j] = -1;
 }

@@ -124,7 +124,8 @@ csa_status csa_indexer_scores(const csa_config *cfg, const void *qI, const float
  * position order, padded with -1 when fewer than k are valid.  Deterministic.
  *
  *   scores  : [rows, ld] fp32;  n_valid : [rows] int32 (NULL = n_cols for every row)
- *   cand    : NULL, or [rows, ld_cand = n_cols] int32 ascending positions: idx holds cand[r, j]
+ *   cand    : NULL, or [rows, ld_cand = n_cols] int32 ascending positions, optionally followed by
+ *             -1 padding (slots from the first -1 on are not candidates): idx holds cand[r, j]
  *             instead of the column j (CSA2 Reindex over a pool)
  *   idx     : [rows, k] int32
  */

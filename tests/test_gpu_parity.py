@@ -240,11 +240,16 @@ def test_topk_candidate_map():
     _topk_check(s, 512, cand=cand)
 
 
-def test_block_pool_matches_oracle():
-    rows, n = 3, 20005
+@pytest.mark.parametrize("n,nv,ties", [(20005, [20005, 12345, 100], True),
+                                        (131072 + 37, [131072 + 37, 100003, 5000, 1], False),
+                                        (131072 + 37, [131072 + 37, 70001], True)])
+def test_block_pool_matches_oracle(n, nv, ties):
+    """Sizes on both sides of the histogram-guided selection (>= 16,384 blocks a row), rows with
+    fewer blocks than kept, and tied block maxima (the whole-row fallback)."""
+    rows = len(nv)
     s = rnd(34, (rows, n))
-    s = torch.round(s * 16) / 16
-    nv = [20005, 12345, 100]
+    if ties:
+        s = torch.round(s * 16) / 16
     c = cfg_obj()
     for n_blocks in (256, 2048):
         pool = torch.full((rows, n_blocks * 8), -7, dtype=torch.int32, device=DEV)
