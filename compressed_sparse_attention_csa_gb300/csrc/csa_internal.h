@@ -98,6 +98,7 @@ struct IndexerLayout {
   int n_acc;           // TMEM accumulators in the MMA -> epilogue ring (2..4)
   int n_splits;        // key-range splits per (sequence, query group)
   int n_qgroups;
+  bool wide;           // one CTA per SM (many query groups); else two, with the key range split
 };
 IndexerLayout indexer_layout(const IndexerArgs& a);
 

@@ -76,8 +76,10 @@ __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_
 }
 
 // ------------------------------------------------------------------ tensor-core path
-constexpr int kEpiWarps = 8;
-constexpr int kTcThreads = 64 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
+// Warp 0 TMA, warp 1 MMA + TMEM, then the epilogue warps: 8 with two CTAs per SM, 16 with one.
+constexpr int epi_warps(int minb) { return minb == 1 ? 16 : 8; }
+constexpr int tc_threads(int minb) { return 64 + 32 * epi_warps(minb); }
+constexpr int kTcThreads = tc_threads(2);
 constexpr int kTile = 128;                       // keys per tile (MMA M)
 constexpr int kMaxG = 8;
 constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
@@ -130,10 +132,12 @@ __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a,
 }
 
 // Warp 0: TMA producer.  Warp 1: TMEM owner and MMA issuer (it also pulls the query image).
-// Warps 2..9: epilogue, as two groups of four (one warp per TMEM lane quadrant) that take
-// alternate tiles.
-template <bool FP8, bool FUSE>
-__global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+// Warps 2..: epilogue, in groups of four (one warp per TMEM lane quadrant).  Groups take
+// alternate tiles; with 16 epilogue warps (one CTA per SM) the two groups of a tile parity
+// split its queries between them, which doubles the warps that hide the TMEM and shared
+// memory latencies of the reduction.
+template <bool FP8, bool FUSE, int MINB>
+__global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const IndexerArgs a, const TcLayout L,
                                                                    const uint8_t* images, const int64_t n_cols) {
   extern __shared__ uint8_t smem_raw[];
@@ -165,8 +169,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
   const int T = a.T;
   const int64_t qrow0 = static_cast<int64_t>(b) * T + g0;
 
+  constexpr int EPI = epi_warps(MINB);
+  // epilogue groups per tile (two split the queries when there are 16 warps and >= 2 queries)
+  const int gpt = (EPI == 16 && G >= 2) ? 2 : 1;
   if (hist)
-    for (int i = tid; i < kTopkHistBins; i += kTcThreads) sHist[i] = 0u;
+    for (int i = tid; i < kTopkHistBins; i += tc_threads(MINB)) sHist[i] = 0u;
   if (tid < kMaxG) {
     int nv = 0;
     if (tid < G && g0 + tid < T) {
@@ -190,9 +197,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 32 * (kEpiWarps / 2));
+      mbar_init(&tempty[i], 32 * 4 * gpt);
     }
-    mbar_init(qbar, fuse ? 32 * kEpiWarps : 1);
+    mbar_init(qbar, fuse ? 32 * EPI : 1);
     mbar_init(kbar, 1);
     fence_mbar_init();
   }
@@ -360,7 +367,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
     // ---- epilogue: group gp (0/1) takes tiles gp, gp + 2, ...; warp (warp & 3) owns TMEM
     //      lanes 32q..32q+31, i.e. 32 keys of the tile, and reduces every head of them
     const int q = warp & 3;
-    const int gp = (warp - 2) >> 2;
+    const int gq = (warp - 2) >> 2;
+    const int gp = gq & 1, ch = gq >> 1;  // tile parity, query half
+    const int gh = (G + 1) / 2;
+    const int g_lo = gpt == 2 ? ch * gh : 0, g_hi = gpt == 2 ? min(G, g_lo + gh) : G;
     const int rin = q * 32 + lane;
     uint32_t* hist_row = hist ? a.hist_out + qrow0 * kTopkHistRowWords : nullptr;
     if constexpr (FUSE) {
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       return (FP8 && itx < n_it && (FUSE || px >= 0) && px < a.E_cap) ? kscale_b[px] : 1.f;
     };
     float ks_next = scale_of(gp);  // e4m3 key scales, prefetched one tile of this group ahead
-    for (int it = gp; w_ok && it < n_it; it += 2) {
+    for (int it = gp; w_ok && ch < gpt && it < n_it; it += 2) {
       const int acc = it % NA;
       const float ksc = ks_next;
       ks_next = scale_of(it + 2);
@@ -412,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
 #pragma unroll
       for (int g = 0; g < kMaxG; ++g) {
         res[g] = 0.f;
-        if (g >= G) continue;
+        if (g < g_lo || g >= g_hi) continue;
         float sum = 0.f;
         for (int hc = 0; hc < HI; hc += 32) {
           float v[32];
@@ -428,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
         const int64_t ps = pos_of(s);  // the key's position (= s without candidates)
 #pragma unroll
         for (int g = 0; g < kMaxG; ++g) {
-          if (g >= G || g0 + g >= T) continue;
+          if (g < g_lo || g >= g_hi || g0 + g >= T) continue;
           const float sc = res[g] * ksc_use;
           a.scores[(qrow0 + g) * a.ld + s] = (FUSE || ps >= 0) && ps < sNv[g] ? sc : -INFINITY;
         }
@@ -436,9 +446,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) indexer_tc_kernel(const __grid_
       if (hist && s < n_cols && s < sNv[0]) atomicAdd(&sHist[f2key(res[0] * ksc_use) >> 20], 1u);
     }
     if (hist) {
-      named_sync(6, 32 * kEpiWarps);
+      named_sync(6, 32 * EPI);
       uint32_t* rh = hist_row;
-      for (int i = tid - 64; i < kTopkHistBins; i += 32 * kEpiWarps) {
+      for (int i = tid - 64; i < kTopkHistBins; i += 32 * EPI) {
         const uint32_t c = sHist[i];
         if (c) atomicAdd(&rh[i], c);
       }
@@ -483,6 +493,7 @@ TcLayout plan_tc(const IndexerArgs& a) {
   int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
   S = std::max(2, std::min(S, 8));
   L.stages = S;
+  L.wide = !decode_like;  // one CTA per SM
   L.smem_bytes = static_cast<uint32_t>(misc + L.b_bytes + static_cast<size_t>(S) * L.stage_bytes);
   // as many accumulators (2..4) as the TMEM share of this CTA (512 columns per SM) holds
   const int share = decode_like ? 256 : 512;
@@ -540,22 +551,28 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
     dim3 grid(L.n_splits, L.n_qgroups, a.B);
     static bool attr = false;
     if (!attr) {
-      cudaFuncSetAttribute(indexer_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(indexer_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(indexer_tc_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(indexer_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      const int mx = 227 * 1024;
+      cudaFuncSetAttribute(indexer_tc_kernel<true, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(indexer_tc_kernel<false, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(indexer_tc_kernel<true, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(indexer_tc_kernel<false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(indexer_tc_kernel<true, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaFuncSetAttribute(indexer_tc_kernel<false, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
       attr = true;
     }
     const uint8_t* cimages = images;
-    const bool fu = a.fuse.on;
-    e = fp8 ? (fu ? launch_pdl(indexer_tc_kernel<true, true>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L, cimages,
-                               n_cols)
-                  : launch_pdl(indexer_tc_kernel<true, false>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L,
-                               cimages, n_cols))
-            : (fu ? launch_pdl(indexer_tc_kernel<false, true>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L,
-                               cimages, n_cols)
-                  : launch_pdl(indexer_tc_kernel<false, false>, grid, dim3(kTcThreads), L.smem_bytes, s, map, a, L,
-                               cimages, n_cols));
+    const dim3 blk(L.wide && !a.fuse.on ? tc_threads(1) : tc_threads(2));
+    const size_t sm = L.smem_bytes;
+    if (a.fuse.on) {
+      e = fp8 ? launch_pdl(indexer_tc_kernel<true, true, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols)
+              : launch_pdl(indexer_tc_kernel<false, true, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols);
+    } else if (L.wide) {
+      e = fp8 ? launch_pdl(indexer_tc_kernel<true, false, 1>, grid, blk, sm, s, map, a, L, cimages, n_cols)
+              : launch_pdl(indexer_tc_kernel<false, false, 1>, grid, blk, sm, s, map, a, L, cimages, n_cols);
+    } else {
+      e = fp8 ? launch_pdl(indexer_tc_kernel<true, false, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols)
+              : launch_pdl(indexer_tc_kernel<false, false, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols);
+    }
     count_launches(1);
     return e;
   }

@@ -100,7 +100,9 @@ def _indexer_ref(qI, w, q_pos, kdeq, m, T):
 
 
 @pytest.mark.parametrize("HI,T,fp8", [(64, 1, False), (64, 37, False), (32, 21, False), (64, 1, True),
-                                      (64, 9, True)])
+                                      (64, 9, True),
+                                      # enough query groups for one CTA per SM over the whole key range
+                                      (64, 700, False), (32, 700, False), (64, 700, True)])
 def test_indexer_tensor_cores(HI, T, fp8):
     B, dI, m, E = 3, 128, 4, 128 * 9 + 37
     qI = rnd(21 + HI + T, (B, T, HI, dI), dI ** -0.5, BF16)
