@@ -521,6 +521,343 @@ __global__ void __launch_bounds__(kD) attn_merge_kernel(const AttnArgs a, const 
   for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j] * s_inv[j]);
 }
 
+// ------------------------------------------------------------------ pipelined path (many queries)
+// One CTA per query over its whole row list, in tiles of 64 rows that 11 gather warps stage
+// (16-byte cp.async, many requests in flight per SM) into two shared-memory buffers while the
+// tensor cores and the softmax warps work on the other.
+//  * S = Q R^T at M = 64 (heads in TMEM lanes 0-15 of each warp quadrant, the tile's rows in
+//    64 columns), into two alternating accumulators, so that S of the next tile overlaps the
+//    softmax of this one.  Softmax warp w owns the heads of quadrant w & 3 and rows
+//    32 (w >> 2) .. +31 of the tile; the two warps of a quadrant combine their row maxima and
+//    sums through shared memory and keep identical running statistics in registers.
+//  * O^T += R^T P^T (M = 128 dims a chunk, N = 64 heads, K = 64 rows), P^T K-major: each head
+//    thread writes its 32 rows (64 bytes) of the head's 128-byte row.
+// Warps 0-7: softmax and output epilogue; warp 8: TMEM owner and MMA issuer; warps 9-19:
+// gathers (and the query).
+constexpr int kPR = 64;
+constexpr int kPfGatherWarps = 11;
+constexpr int kPfThreads = 32 * (9 + kPfGatherWarps);
+constexpr int kPfMaxK = 2048;
+struct PfLayout {
+  static constexpr uint32_t kQ = 0;                       // 8 regions x (64 heads x 128 B)
+  static constexpr uint32_t kRBytes = kPR * kD * 2;       // one row tile: 8 regions x (64 rows x 128 B)
+  static constexpr uint32_t kR = kQ + kH * kD * 2;        // [2] row tiles
+  static constexpr uint32_t kPBytes = kH * kPR * 2;       // one P^T tile: 64 heads x 128 B (rows)
+  static constexpr uint32_t kP = kR + 2 * kRBytes;        // [2] P^T tiles
+  static constexpr uint32_t kMisc = kP + 2 * kPBytes;
+  // alpha, f [64] + row-half maxima, sums [2][64] + tmp [32] + flags [4] + barriers [16] + tmem
+  static constexpr uint32_t kMiscBytes = (2 * kH + 4 * kH + 32 + 4) * 4 + 16 * 8 + 16;
+  static constexpr size_t kSmem = 1024 + kMisc + kMiscBytes + kPfMaxK * 4;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "l"(pol)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a) {
+  using LY = PfLayout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + LY::kQ;
+  uint8_t* sR = smem + LY::kR;
+  uint8_t* sP = smem + LY::kP;
+  float* s_alpha = reinterpret_cast<float*>(smem + LY::kMisc);  // [64] rescale of the earlier tiles
+  float* s_f = s_alpha + kH;                                     // [64] output factor
+  float* s_mx = s_f + kH;                                        // [2][64] row-half maxima
+  float* s_sm = s_mx + 2 * kH;                                   // [2][64] row-half sums
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(s_sm + 2 * kH);    // [32]
+  volatile int* s_flag = reinterpret_cast<volatile int*>(tmp + 32);  // [0] rescale, [1] abort
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tmp + 32 + 4);    // 8-byte aligned
+  uint64_t* full = bars;         // [2] row tile landed (gather threads)
+  uint64_t* empty = bars + 2;    // [2] row tile consumed (O^T product committed)
+  uint64_t* sfull = bars + 4;    // [2] S accumulator ready
+  uint64_t* sempty = bars + 6;   // [2] S accumulator read (softmax threads)
+  uint64_t* pfull = bars + 8;    // [2] P^T tile written (softmax threads)
+  uint64_t* pempty = bars + 10;  // [2] P^T tile consumed (O^T product committed)
+  uint64_t* qfull = bars + 12;   // Q landed (gather threads)
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 16);
+  int32_t* sel = reinterpret_cast<int32_t*>(smem + LY::kMisc + LY::kMiscBytes);  // [k]
+  volatile int* sAbort = s_flag + 1;
+  constexpr int kSoft = 256, kGath = 32 * kPfGatherWarps;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t r = blockIdx.x;
+  const int b = static_cast<int>(r / a.T);
+  const float scale_log2 = a.softmax_scale * kLog2e;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], kGath);
+      mbar_init(&empty[i], 1);
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], kSoft);
+      mbar_init(&pfull[i], kSoft);
+      mbar_init(&pempty[i], 1);
+    }
+    mbar_init(qfull, kGath);
+    fence_mbar_init();
+    s_flag[0] = 0;
+    s_flag[1] = 0;
+  }
+  if (warp == 8) {
+    tmem_alloc(sTmem, 512);
+    tmem_relinquish();
+  }
+  pdl_wait();  // the selection and the caches come from the kernels before this one
+  pdl_trigger();
+  const int n_sel = compact_idx<kPfThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
+  const int64_t t = a.q_pos[r];
+  int64_t p_lo;
+  int n_win;
+  window_of(t, a.W, a.local_base[b], a.L, p_lo, n_win);
+  const int n_rows = n_sel + n_win;
+  const int nt = (n_rows + kPR - 1) / kPR;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const uint32_t tO = tmem + 128;  // O^T: 4 chunks x 64 heads; S buffers at columns 0 and 64
+
+  if (warp > 8) {
+    // ---- gather warps: thread g copies chunks g, g + 352, ... of the tile (chunk i: row
+    //      i / 64, 16-byte piece i % 64); the query likewise
+    const int g = tid - 32 * 9;
+    const __nv_bfloat16* kvc = static_cast<const __nv_bfloat16*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kD;
+    const __nv_bfloat16* kvl = static_cast<const __nv_bfloat16*>(a.kv_local) + static_cast<int64_t>(b) * a.L * kD;
+    const int64_t lbase = a.local_base[b];
+    const uint64_t pol = policy_evict_last();  // the caches are re-read by the other queries
+    if (nt > 0) {
+      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + r * kH * kD;
+      for (int i = g; i < kH * 64; i += kGath) {
+        const int h = i >> 6, c = i & 63;
+        cp_async16(sQ + (c >> 3) * (kH * 128) + sw128(h, c & 7), q + h * kD + c * 8);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    bool ok = true;
+    for (int it = 0; ok && it < nt; ++it) {
+      const int buf = it & 1;
+      if (it >= 2) {
+        if (lane == 0) ok = mbar_wait(&empty[buf], ((it >> 1) & 1) ^ 1, a.err, sAbort);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      uint8_t* dst = sR + buf * LY::kRBytes;
+#pragma unroll 4
+      for (int i = g; i < kPR * 64; i += kGath) {
+        const int j = i >> 6, c = i & 63;
+        uint8_t* d = dst + (c >> 3) * (kPR * 128) + sw128(j, c & 7);
+        const int lp = it * kPR + j;
+        if (lp < n_rows) {
+          const __nv_bfloat16* src = lp < n_sel ? kvc + static_cast<int64_t>(sel[lp]) * kD
+                                                : kvl + (p_lo + (lp - n_sel) - lbase) * kD;
+          cp_async16_hint(d, src + c * 8, pol);
+        } else {
+          *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      fence_proxy_async_smem();
+      if (it == 0) mbar_arrive(qfull);
+      mbar_arrive(&full[buf]);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  } else if (warp == 8) {
+    // ---- MMA issuer: each product as soon as its inputs are ready (polled without
+    //      suspending), O^T += R^T P^T first since it frees a row tile for the gathers.
+    //      Descriptors are formed once; every MMA adds a constant to the start-address field
+    //      (an issue costs about 50 cycles, so the loops carry no descriptor arithmetic).
+    if (lane == 0 && nt > 0) {
+      const uint32_t idesc_s = idesc_bf16(kH, kPR, false, false);
+      const uint32_t idesc_o = idesc_bf16(128, kH, true, false);
+      const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024);
+      const uint64_t dr0 = smem_desc(smem_u32(sR), 16, 1024);                 // R as S's B operand
+      const uint64_t dv0 = smem_desc(smem_u32(sR), kPR * 128, 1024);          // R^T as O^T's A operand
+      const uint64_t dp0 = smem_desc(smem_u32(sP), 16, 1024);                 // P^T as O^T's B operand
+      constexpr uint64_t kRStep = LY::kRBytes >> 4, kPStep = LY::kPBytes >> 4;
+      bool ok = mbar_wait(qfull, 0, a.err, sAbort);
+      int ns = 0, np = 0;  // next S tile, next O^T product
+      uint64_t t_last = global_ns();
+      while (ok && np < nt) {
+        if (np < ns && mbar_test_wait(&pfull[np & 1], (np >> 1) & 1)) {
+          const int ub = np & 1;
+          tc_fence_after();
+          const uint64_t dv = dv0 + ub * kRStep, dp = dp0 + ub * kPStep;
+          const uint32_t acc0 = np > 0 ? 1u : 0u;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+            for (int ks = 0; ks < kPR / 16; ++ks)
+              mma_bf16(tO + cc * 64, dv + (((2 * cc) * (kPR * 128) + ks * 2048) >> 4), dp + ((ks * 32) >> 4), idesc_o,
+                       ks > 0 ? 1u : acc0);
+          }
+          mma_commit(&empty[ub]);
+          mma_commit(&pempty[ub]);
+          ++np;
+          t_last = global_ns();
+        } else if (ns < nt && mbar_test_wait(&full[ns & 1], (ns >> 1) & 1) &&
+                   (ns < 2 || mbar_test_wait(&sempty[ns & 1], ((ns >> 1) & 1) ^ 1))) {
+          const int buf = ns & 1;
+          tc_fence_after();
+          const uint64_t dr = dr0 + buf * kRStep;
+          const uint32_t ts = tmem + buf * 64;
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * (kPR * 128) + (ks & 3) * 32;  // kH == kPR: same for Q
+            mma_bf16(ts, dq + (off >> 4), dr + (off >> 4), idesc_s, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&sfull[buf]);
+          ++ns;
+          t_last = global_ns();
+        } else if (*sAbort) {
+          ok = false;
+        } else if (global_ns() - t_last > kWaitBudgetNs) {
+          set_error(a.err, kErrTimeout);
+          *sAbort = 1;
+          ok = false;
+        }
+      }
+    }
+  } else {
+    // ---- softmax warps 0-7: thread (warp w, lane l < 16) has head h = 16 (w & 3) + l (TMEM
+    //      lane 32 (w & 3) + l) and rows 32 (w >> 2) .. +31; lanes 16-31 only take part in
+    //      the barriers
+    const int qd = warp & 3, ch = warp >> 2;
+    const int h = qd * 16 + lane;
+    const bool own = lane < 16;
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int it = 0; ok && it < nt; ++it) {
+      const int buf = it & 1;
+      // (wait outcomes are made uniform over the softmax warps: they share named barriers)
+      ok = named_and(1, kSoft, mbar_wait(&sfull[buf], (it >> 1) & 1, a.err, sAbort));
+      if (!ok) break;
+      tc_fence_after();
+      float x[32];
+      tmem_ld32(tmem + lane_off + buf * 64 + ch * 32, x);
+      tmem_wait_ld(x);
+      tc_fence_before();
+      mbar_arrive(&sempty[buf]);  // S is in registers: the accumulator may take tile it + 2
+      float mh = -INFINITY;
+      const int r0 = it * kPR + ch * 32;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = (r0 + j < n_rows) ? x[j] * scale_log2 : -INFINITY;
+        mh = fmaxf(mh, x[j]);
+      }
+      if (own) s_mx[ch * kH + h] = mh;
+      named_sync(1, kSoft);
+      const float mb = own ? fmaxf(s_mx[h], s_mx[kH + h]) : -INFINITY;
+      // reference max: moved only when the tile's max exceeds it by more than 2^8
+      float mu = m_run;
+      if (m_run == -INFINITY || mb > m_run + 8.f) mu = fmaxf(m_run, mb);
+      const float alpha = (mu == m_run) ? 1.f : ex2_approx(m_run - mu);
+      m_run = mu;
+      if (own && ch == 0) {
+        s_alpha[h] = alpha;
+        if (it > 0 && alpha != 1.f) s_flag[0] = 1;
+      }
+      // the P^T tile of this buffer was last read by the product of tile it - 2
+      ok = named_and(1, kSoft, it < 2 || mbar_wait(&pempty[buf], ((it >> 1) & 1) ^ 1, a.err, sAbort));
+      if (!ok) break;
+      float ps = 0.f;
+      {
+        uint8_t* prow = sP + buf * LY::kPBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 pk;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = (mu == -INFINITY) ? 0.f : ex2_approx(x[c * 8 + 2 * e] - mu);
+            const float p1 = (mu == -INFINITY) ? 0.f : ex2_approx(x[c * 8 + 2 * e + 1] - mu);
+            ps += p0 + p1;
+            __nv_bfloat162 two = __floats2bfloat162_rn(p0, p1);
+            w[e] = *reinterpret_cast<uint32_t*>(&two);
+          }
+          if (own) *reinterpret_cast<uint4*>(prow + sw128(h, ch * 4 + c)) = pk;
+        }
+      }
+      if (own) s_sm[ch * kH + h] = ps;
+      // earlier tiles' O^T columns of heads whose reference max moved: after the product of
+      // tile it - 1, scale by alpha (warp w: dims 32 (w & 3) .. of chunks 2 (w >> 2), +1)
+      if (s_flag[0] != 0) {
+        ok = named_and(1, kSoft, mbar_wait(&pempty[(it - 1) & 1], ((it - 1) >> 1) & 1, a.err, sAbort));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 2 * ch; cc < 2 * ch + 2; ++cc) {
+#pragma unroll 1
+          for (int hc = 0; hc < 64; hc += 32) {
+            float v[32];
+            const uint32_t ta = tO + lane_off + cc * 64 + hc;
+            tmem_ld32(ta, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] *= s_alpha[hc + e];
+            tmem_st32(ta, v);
+          }
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(&pfull[buf]);
+      named_sync(1, kSoft);  // sums written; every thread has read the flag and s_alpha
+      if (own) l_run = l_run * alpha + (s_sm[h] + s_sm[kH + h]);
+      if (tid == 0) s_flag[0] = 0;
+    }
+    // ---- epilogue: the last product into O^T, then O / (l + sink) per head
+    if (ok && nt > 0)
+      ok = named_and(1, kSoft, mbar_wait(&pempty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, a.err, sAbort));
+    tc_fence_after();
+    if (own && ch == 0) {
+      const float sk = a.sink[h] * kLog2e;
+      const float M = fmaxf(m_run, sk);
+      const float f = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
+      const float den = l_run * f + exp2f(sk - M);
+      s_f[h] = f / den;
+      if (a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+    }
+    named_sync(1, kSoft);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + r * kH * kD;
+    if (ok && nt > 0) {
+      for (int cc = 2 * ch; cc < 2 * ch + 2; ++cc) {
+        const int dd = cc * 128 + qd * 32 + lane;
+#pragma unroll
+        for (int hc = 0; hc < 64; hc += 32) {
+          float v[32];
+          tmem_ld32(tO + lane_off + cc * 64 + hc, v);
+          tmem_wait_ld(v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[(hc + e) * kD + dd] = __float2bfloat16_rn(v[e] * s_f[hc + e]);
+        }
+      }
+    } else {
+      for (int i = tid; i < kH * kD; i += kSoft) o[i] = __float2bfloat16_rn(0.f);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ------------------------------------------------------------------ decode path
 // One query row per sequence, its k + W rows split over CTAs: grid (row split, head group,
 // query).  A CTA takes 128 rows of the query's row list and NH of the 64 heads (S^T = R Q^T
@@ -845,6 +1182,18 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     if (!attr) {
       cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       attr = true;
+    }
+    if (sp.n_split == 1 && a.k <= kPfMaxK) {
+      static bool pattr = false;
+      if (!pattr) {
+        cudaFuncSetAttribute(attn_pf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PfLayout::kSmem));
+        pattr = true;
+      }
+      const cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows)), dim3(kPfThreads),
+                                       PfLayout::kSmem, s, a);
+      count_launches(1);
+      return e;
     }
     if (sp.n_split == 1 || sp.rows_per_split != kRows) {
       const cudaError_t e = launch_pdl(attn_tc_kernel, dim3(sp.n_split, static_cast<unsigned>(rows)),

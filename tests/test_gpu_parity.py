@@ -297,9 +297,12 @@ def _attn_ref(q, kv, idx, kl, local_base, q_pos, sink, W, scale):
     return np.stack(outs).reshape(q.shape), np.stack(lses).reshape(B, T, -1)
 
 
-# B = 3, 2: four head groups per decode CTA; B = 10: two; B = 16: one (64 heads)
+# B = 3, 2: four head groups per decode CTA; B = 10: two; B = 16: one (64 heads).
+# >= 152 query rows take the one-CTA-per-query pipelined kernel (64-row tiles): ragged tiles,
+# empty selections and clipped windows
 @pytest.mark.parametrize("B,T,nsel", [(3, 1, [512, 300, 512]), (1, 160, [512, 77]), (2, 2, [0, 512]),
-                                      (10, 1, [512, 300, 17, 0, 512]), (16, 1, [512, 1, 400])])
+                                      (10, 1, [512, 300, 17, 0, 512]), (16, 1, [512, 1, 400]),
+                                      (3, 60, [0, 512, 1, 63, 64, 65, 300])])
 def test_attention_tensor_cores(B, T, nsel):
     H, d, E, k, W, L = 64, 512, 1500, 512, 128, 200
     q, kv, kl, sink, idx = _attn_inputs(40 + T + B, B, T, H, d, E, k, L, BF16, nsel)
