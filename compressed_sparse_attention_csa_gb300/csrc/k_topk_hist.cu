@@ -336,21 +336,23 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
 // threshold bin b1 found, and the row read again (now from L2) keeping the (key, position) of
 // every score with digit >= b1 in position order (per-thread contiguous slices, one block
 // scan per batch); the exact selection then runs as in topk_select_kernel.
-constexpr int kRowAllCap = 8192;
+// The candidate list holds CAP entries: 2048 for k <= 512 (four CTAs fit on an SM), else 8192.
 constexpr int kRowPer = 8;                 // scores per thread per batch
 constexpr int kRowBatch = kRowPer * NT;    // 4096
 
+template <int CAP>
 struct RowSmem {
   uint32_t hist[kFine];
-  uint32_t ak[kRowAllCap];
-  int32_t ap[kRowAllCap];
+  uint32_t ak[CAP];
+  int32_t ap[CAP];
   uint32_t sort[2 * kSortBuckets];
   uint32_t tmp[32];
   uint32_t res[8];
   uint32_t n_gt;
 };
 
-size_t row_smem_bytes(int k) { return sizeof(RowSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
+template <int CAP>
+size_t row_smem_bytes(int k) { return sizeof(RowSmem<CAP>) + 2 * static_cast<size_t>(k) * 4 + 16; }
 
 __device__ __forceinline__ void load_row8(const float* srow, int64_t t0, int64_t n, float (&v)[kRowPer]) {
   if (t0 + kRowPer <= n && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
@@ -364,11 +366,12 @@ __device__ __forceinline__ void load_row8(const float* srow, int64_t t0, int64_t
   }
 }
 
+template <int CAP>
 __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
                                                       int64_t n_cols, int k, int32_t* idx, const int32_t* cmap) {
   extern __shared__ __align__(16) uint8_t row_raw[];
-  RowSmem& S = *reinterpret_cast<RowSmem*>(row_raw);
-  int32_t* sel = reinterpret_cast<int32_t*>(row_raw + sizeof(RowSmem));  // [k] (whole-row path)
+  RowSmem<CAP>& S = *reinterpret_cast<RowSmem<CAP>*>(row_raw);
+  int32_t* sel = reinterpret_cast<int32_t*>(row_raw + sizeof(RowSmem<CAP>));  // [k] (whole-row path)
   int32_t* srt = sel + k;
   const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
@@ -383,14 +386,17 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
     return y == 0u ? 1u : y;
   };
   __syncthreads();
-  // pass 1: the histogram of the visible scores
-  for (int64_t base = 0; base < nvr; base += kRowBatch) {
-    float v[kRowPer];
-    const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
+  // pass 1: the histogram of the visible scores (two batches of loads in flight)
+  for (int64_t base = 0; base < nvr; base += 2 * kRowBatch) {
+    float v[kRowPer], w[kRowPer];
+    const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer, t1 = t0 + kRowBatch;
     load_row8(srow, t0, nvr, v);
+    load_row8(srow, t1, nvr, w);
 #pragma unroll
-    for (int u = 0; u < kRowPer; ++u)
+    for (int u = 0; u < kRowPer; ++u) {
       if (t0 + u < nvr) atomicAdd(&S.hist[key_of(v[u]) >> 20], 1u);
+      if (t1 + u < nvr) atomicAdd(&S.hist[key_of(w[u]) >> 20], 1u);
+    }
   }
   __syncthreads();
   const uint32_t b1 = team_threshold_digit_smem<NT>(S.hist, k, S.tmp, S.res, tid, 0);
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
 #pragma unroll
     for (int u = 0; u < kRowPer; ++u) {
       if (key[u] != 0u) {
-        if (off < static_cast<uint32_t>(kRowAllCap)) {
+        if (off < static_cast<uint32_t>(CAP)) {
           S.ak[off] = key[u];
           S.ap[off] = static_cast<int32_t>(t0 + u);
         }
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
   int32_t* orow = idx + row * k;
   // with a candidate map (ascending positions) the winners' slots are written as positions
   const int32_t* cm = cmap ? cmap + row * n_cols : nullptr;
-  if (n_all <= static_cast<uint32_t>(kRowAllCap)) {
+  if (n_all <= static_cast<uint32_t>(CAP)) {
     const int na = static_cast<int>(n_all);
     const int need = k - static_cast<int>(n_gt);
     uint32_t T = 1u;
@@ -545,12 +551,18 @@ cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int6
                              int k, int32_t* idx, cudaStream_t s, const int32_t* cmap) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(row_smem_bytes(4096)));
+    cudaFuncSetAttribute(topk_row_kernel<2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(row_smem_bytes<2048>(512)));
+    cudaFuncSetAttribute(topk_row_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(row_smem_bytes<8192>(4096)));
     attr = true;
   }
-  const cudaError_t e = launch_pdl(topk_row_kernel, dim3(static_cast<unsigned>(rows)), dim3(NT), row_smem_bytes(k), s,
-                                   scores, ld, n_valid, n_cols, k, idx, cmap);
+  const dim3 grid(static_cast<unsigned>(rows));
+  const cudaError_t e =
+      k <= 512 ? launch_pdl(topk_row_kernel<2048>, grid, dim3(NT), row_smem_bytes<2048>(k), s, scores, ld, n_valid,
+                            n_cols, k, idx, cmap)
+               : launch_pdl(topk_row_kernel<8192>, grid, dim3(NT), row_smem_bytes<8192>(k), s, scores, ld, n_valid,
+                            n_cols, k, idx, cmap);
   count_launches(1);
   return e;
 }

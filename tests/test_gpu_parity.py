@@ -232,6 +232,23 @@ def test_topk_long_rows_histogram_path_adversarial():
     _topk_check(rows, 2048, n_valid=[n, 5000, 0, 39999, 2048])
 
 
+def test_topk_many_prefill_rows():
+    """More than 64 rows of prefill length take the one-CTA-per-row kernel (2,048 candidate
+    slots for k <= 512): ragged and tiny valid counts, ties that overflow the candidate list,
+    a candidate map, and a longer row."""
+    n = 33792 + 5
+    s = rnd(36, (80, n))
+    s[40:] = torch.round(s[40:] * 8) / 8          # coarse values: many exact ties
+    nv = [n, n - 3, 0, 1, 511, 512, 513, 20000, 36, 37]
+    _topk_check(s.contiguous(), 512, n_valid=nv * 8)
+    cand = torch.sort(torch.randperm(262144, generator=torch.Generator().manual_seed(9))[:n]).values.to(torch.int32)
+    cand = cand.repeat(80, 1)
+    cand[3, 30000:] = -1
+    _topk_check(s.contiguous(), 512, cand=cand.to(DEV).contiguous())
+    s2 = rnd(37, (70, 50000))
+    _topk_check(s2.contiguous(), 512, n_valid=[50000, 40000, 7, 600, 36865] * 14)
+
+
 def test_topk_candidate_map():
     rows, n = 4, 16384
     s = rnd(33, (rows, n))
