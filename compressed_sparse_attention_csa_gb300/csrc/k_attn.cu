@@ -1093,40 +1093,62 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
 // Fixed-order merge of the decode partials ([query][split][head][dim]) with the sink: one
 // CTA per (query, 4 heads), one thread per output dim.
 __global__ void __launch_bounds__(kD) attn_merge_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
-  __shared__ float s_f[kMaxSplit][kMergeHeads];  // per split, per head: 2^(m_s - M) / den
+  __shared__ float s_ml[kMaxSplit][2][kMergeHeads];  // (m, l) of every split
+  __shared__ float s_f[kMaxSplit][kMergeHeads];      // per split, per head: 2^(m_s - M) / den
   pdl_wait();
   pdl_trigger();
   const int64_t r = blockIdx.x;
   const int h0 = blockIdx.y * kMergeHeads;
   const int dd = threadIdx.x;
   const int ns = sp.n_split;
-  const float* ml = sp.part_ml + r * ns * 2 * kH;
+  // every load of the CTA is issued before the first use: the partials of this thread's dim
+  // (all splits, 4 heads) and, by the first 2 * 4 * ns threads, one (m, l) value each
+  // (splits past the first kPre are loaded after the factors; the decode plans use 5)
+  constexpr int kPre = 8;
+  const float* po = sp.part_o + (r * ns * kH + h0) * kD + dd;
+  float v[kPre][kMergeHeads];
+#pragma unroll
+  for (int x = 0; x < kPre; ++x)
+#pragma unroll
+    for (int j = 0; j < kMergeHeads; ++j)
+      v[x][j] = x < ns ? __ldcg(po + (static_cast<int64_t>(x) * kH + j) * kD) : 0.f;
+  if (threadIdx.x < 2 * kMergeHeads * ns) {
+    const int x = threadIdx.x / (2 * kMergeHeads), w = (threadIdx.x / kMergeHeads) & 1, j = threadIdx.x % kMergeHeads;
+    s_ml[x][w][j] = __ldcg(sp.part_ml + (r * ns + x) * 2 * kH + w * kH + h0 + j);
+  }
+  __syncthreads();
   if (threadIdx.x < kMergeHeads) {
-    const int h = h0 + threadIdx.x;
+    const int j = threadIdx.x, h = h0 + j;
     const float sk = a.sink[h] * kLog2e;
     float M = sk;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * 2 * kH + h]);
+    for (int x = 0; x < ns; ++x) M = fmaxf(M, s_ml[x][0][j]);
     float den = exp2f(sk - M);
-    float f[kMaxSplit];
-    for (int s = 0; s < ns; ++s) {
-      const float ms = ml[s * 2 * kH + h];
-      f[s] = ms == -INFINITY ? 0.f : exp2f(ms - M);
-      den = fmaf(ml[s * 2 * kH + kH + h], f[s], den);
+    for (int x = 0; x < ns; ++x) {
+      const float ms = s_ml[x][0][j];
+      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      s_f[x][j] = f;
+      den = fmaf(s_ml[x][1][j], f, den);
     }
     const float inv = 1.f / den;
-    for (int s = 0; s < ns; ++s) s_f[s][threadIdx.x] = f[s] * inv;
+    for (int x = 0; x < ns; ++x) s_f[x][j] *= inv;
     if (a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
   }
   __syncthreads();
-  const float* po = sp.part_o + (r * ns * kH + h0) * kD + dd;
   float acc[kMergeHeads] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s >= ns) break;
+  for (int x = 0; x < kPre; ++x) {
+    if (x >= ns) break;
 #pragma unroll
     for (int j = 0; j < kMergeHeads; ++j) {
-      const float f = s_f[s][j];
-      if (f != 0.f) acc[j] = fmaf(po[(static_cast<int64_t>(s) * kH + j) * kD], f, acc[j]);
+      const float f = s_f[x][j];
+      if (f != 0.f) acc[j] = fmaf(v[x][j], f, acc[j]);
+    }
+  }
+  for (int x = kPre; x < ns; ++x) {
+#pragma unroll
+    for (int j = 0; j < kMergeHeads; ++j) {
+      const float f = s_f[x][j];
+      if (f != 0.f) acc[j] = fmaf(__ldcg(po + (static_cast<int64_t>(x) * kH + j) * kD), f, acc[j]);
     }
   }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (r * kH + h0) * kD + dd;
