@@ -357,9 +357,12 @@ def test_attention_cuda_core_fp32():
 
 # ------------------------------------------------------------------ compositions
 
-@pytest.mark.parametrize("cid,N", [(2, 4 * 1500), (4, 4 * 2500)])
-def test_decode_step_matches_oracle(cid, N):
-    cfg = gen.CONFIGS[cid].replace(B=3, N=N)
+@pytest.mark.parametrize("cid,N,HI", [(2, 4 * 1500, 64), (4, 4 * 2500, 64),
+                                      # fewer visible entries than k (padded selection), windows
+                                      # reaching back to position 0, and the 32-head indexer
+                                      (2, 4 * 30, 64), (4, 4 * 130, 64), (2, 4 * 700, 32)])
+def test_decode_step_matches_oracle(cid, N, HI):
+    cfg = gen.CONFIGS[cid].replace(B=3, N=N, HI=HI)
     inp = gen.make_inputs(cfg, DEV)
     inp["q_pos"][1] = N - 3          # this token completes no block: no compression
     kv_before = inp["kv_comp"].clone()
