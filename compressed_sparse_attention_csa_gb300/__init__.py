@@ -4,4 +4,4 @@ The computation lives in libcsa (hand-written CUDA, C ABI in include/csa.h); thi
 its thin Python binding.  See :mod:`compressed_sparse_attention_csa_gb300.ops`.
 """
 from .ops import (Config, CsaError, block_pool, compress_kv, decode_step, get_last_error,  # noqa: F401
-                  indexer_scores, launch_count, sparse_attn, topk, version, workspace_size)
+                  indexer_scores, indexer_topk, launch_count, sparse_attn, topk, version, workspace_size)

@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(HERE, "libcsa.so")
 c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
 CSA_F32, CSA_BF16, CSA_E4M3 = 0, 1, 2
-CSA_OP_COMPRESS, CSA_OP_INDEXER, CSA_OP_TOPK, CSA_OP_ATTN, CSA_OP_DECODE, CSA_OP_POOL = range(6)
+CSA_OP_COMPRESS, CSA_OP_INDEXER, CSA_OP_TOPK, CSA_OP_ATTN, CSA_OP_DECODE, CSA_OP_POOL, CSA_OP_INDEXER_TOPK = range(7)
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_DTYPE", 4: "CSA_ERR_ALIGN",
           5: "CSA_ERR_WORKSPACE", 6: "CSA_ERR_CUDA", 7: "CSA_ERR_TIMEOUT", 8: "CSA_ERR_INDEX"}
 
@@ -42,6 +42,8 @@ SIGNATURES = {
                                        c_i64, c_vp, ctypes.c_int, c_vp, c_i64, c_vp]),
     "csa_indexer_scores": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64,
                                           c_vp, c_i32, c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "csa_indexer_topk": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64,
+                                        c_vp, c_vp, c_sz, c_vp]),
     "csa_topk": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp,
                                 c_sz, c_vp]),
     "csa_topk_noalloc": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp,

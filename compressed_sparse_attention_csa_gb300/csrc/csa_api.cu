@@ -134,6 +134,14 @@ IndexerArgs indexer_shape(const csa_config* c, int T, int64_t E_cap, int sms) {
   return a;
 }
 
+// csa_indexer_topk: [query images][scores rows*E_cap*4][visible counts][top-k workspace].
+size_t indexer_topk_ws(const csa_config* c, int T, int64_t E_cap, int sms) {
+  const int64_t rows = static_cast<int64_t>(c->B) * T;
+  return align_up(indexer_workspace_bytes(indexer_shape(c, T, E_cap, sms)), 256) +
+         align_up(static_cast<size_t>(rows * E_cap) * 4, 256) + align_up(static_cast<size_t>(rows) * 4, 256) +
+         align_up(topk_workspace_bytes(rows, E_cap, c->k, sms), 256);
+}
+
 size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   const int64_t B = c->B;
   // first, at a fixed offset: the top-k histograms and tickets kept across steps
@@ -207,6 +215,9 @@ size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_
       return decode_ws(cfg, n_cols, sms);
     case CSA_OP_POOL:
       return static_cast<size_t>(-1);
+    case CSA_OP_INDEXER_TOPK:  // rows = B*T, n_cols = E_cap
+      if (rows % cfg->B || n_cols < 1 || n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
+      return indexer_topk_ws(cfg, static_cast<int>(rows / cfg->B), n_cols, sms);
   }
   return static_cast<size_t>(-1);
 }
@@ -288,6 +299,61 @@ csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float
   if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
   a.err = err_word_ptr();
   return launch_status(launch_indexer(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* w, int32_t T, const int64_t* q_pos,
+                            const void* kI, const float* kscale, int64_t E_cap, int32_t* idx, void* ws,
+                            size_t ws_bytes, csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!qI || !w || !q_pos || !kI || !idx) return CSA_ERR_NULL;
+  if (cfg->kidx == CSA_E4M3 && !kscale) return CSA_ERR_NULL;
+  if (!aligned16(qI) || !aligned16(w) || !aligned16(q_pos) || !aligned16(kI) || !aligned16(idx) ||
+      (kscale && !aligned16(kscale)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (T < 0 || E_cap < 1 || E_cap > (int64_t(1) << 24) || cfg->HI > 128 || E_cap * cfg->B >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(cfg->B) * T * E_cap >= (int64_t(1) << 40))
+    return CSA_ERR_SHAPE;
+  const int64_t rows = static_cast<int64_t>(cfg->B) * T;
+  if (rows == 0) return CSA_OK;
+  const int sms = device_sm_count();
+  const size_t need = indexer_topk_ws(cfg, T, E_cap, sms);
+  if (!ws || ws_bytes < need) return CSA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  IndexerArgs a = indexer_shape(cfg, T, E_cap, sms);
+  a.qI = qI;
+  a.w = w;
+  a.q_pos = q_pos;
+  a.kI = kI;
+  a.kscale = kscale;
+  a.err = err_word_ptr();
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  a.ws = p;
+  p += align_up(indexer_workspace_bytes(a), 256);
+  const size_t per_row = align_up(static_cast<size_t>(rows) * 4, 256);
+  float* scores = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(rows * E_cap) * 4, 256);
+  int32_t* nv = reinterpret_cast<int32_t*>(p);
+  p += per_row;
+  a.scores = scores;
+  a.ld = E_cap;
+  a.nv_out = nv;
+  cudaError_t e = launch_indexer(a, s);
+  if (e != cudaSuccess) return launch_status(e);
+  TopkArgs t{};
+  t.scores = scores;
+  t.ld = E_cap;
+  t.rows = rows;
+  t.n_cols = E_cap;
+  t.n_valid = nv;
+  t.cand = nullptr;
+  t.k = cfg->k;
+  t.idx = idx;
+  t.ws = p;
+  t.ws_bytes = ws_bytes - static_cast<size_t>(p - static_cast<uint8_t*>(ws));
+  t.err = a.err;
+  t.num_sms = sms;
+  return launch_status(launch_topk(t, s));
 }
 
 csa_status csa_topk(const csa_config* cfg, const float* scores, int64_t ld, int64_t rows, int64_t n_cols,

@@ -150,6 +150,21 @@ def indexer_scores(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.
                                   _p(cand), n_cand, _p(scores), scores.shape[-1], wp, wb, _stream()))
 
 
+def indexer_topk(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.Tensor, kI: torch.Tensor,
+                 idx: torch.Tensor, kscale: Optional[torch.Tensor] = None) -> None:
+    """csa_indexer_topk: the k best visible entries of every query row (ascending, -1 padded),
+    the scores kept in the call's workspace.  qI [B, T, HI, dI], w [B, T, HI], kI [B, E_cap, dI]."""
+    lib = L.load()
+    c = cfg.c()
+    T = qI.shape[1]
+    E_cap = kI.shape[1]
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_INDEXER_TOPK, ctypes.byref(c), cfg.B * T, E_cap), qI.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_indexer_topk",
+           lib.csa_indexer_topk(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), E_cap, _p(idx),
+                                wp, wb, _stream()))
+
+
 def topk(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional[torch.Tensor] = None,
          cand: Optional[torch.Tensor] = None, n_cols: Optional[int] = None) -> None:
     """csa_topk: scores [rows, ld] fp32 -> idx [rows, k] int32 (ascending, -1 padded)."""

@@ -63,14 +63,15 @@ typedef struct {
 /* Operation ids for csa_workspace_size. */
 typedef enum {
   CSA_OP_COMPRESS = 0, CSA_OP_INDEXER = 1, CSA_OP_TOPK = 2, CSA_OP_ATTN = 3,
-  CSA_OP_DECODE = 4, CSA_OP_POOL = 5
+  CSA_OP_DECODE = 4, CSA_OP_POOL = 5, CSA_OP_INDEXER_TOPK = 6
 } csa_op;
 
 /*
  * csa_workspace_size — bytes of scratch the operation needs.
  *   rows   : query rows (B*T) of the call;
- *   n_cols : the longest score row (E_cap, or n_cand) for TOPK / DECODE;
- *            T (queries per sequence) for ATTN.  (POOL: see csa_block_pool_workspace_size.)
+ *   n_cols : the longest score row (E_cap, or n_cand) for TOPK / DECODE / INDEXER_TOPK;
+ *            T (queries per sequence) for ATTN and INDEXER.  (POOL: see
+ *            csa_block_pool_workspace_size.)
  * Returns 0 for operations that need none, (size_t)-1 for an invalid configuration.
  */
 size_t csa_workspace_size(csa_op op, const csa_config *cfg, int64_t rows, int64_t n_cols);
@@ -117,6 +118,22 @@ csa_status csa_indexer_scores(const csa_config *cfg, const void *qI, const float
                               const int64_t *q_pos, const void *kI, const float *kscale,
                               int64_t E_cap, const int32_t *cand, int32_t n_cand, float *scores,
                               int64_t ld_scores, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * csa_indexer_topk — csa_indexer_scores followed by csa_topk over each row's visible entries
+ * ("The Lightning Indexer": keep the k best; ties to the lowest position) in one call:
+ * idx[r, 0:k] holds the k best visible positions of query row r in ascending order, -1
+ * padded, exactly as csa_topk returns them from the scores csa_indexer_scores writes.
+ *
+ *   qI, w, T, q_pos, kI, kscale, E_cap : as in csa_indexer_scores (all entries, no candidates)
+ *   idx : [B*T, cfg->k] int32
+ *   ws  : csa_workspace_size(CSA_OP_INDEXER_TOPK, cfg, B*T, E_cap) bytes
+ * The scores live in ws (the caller holds no score matrix) and the same kernels as the two
+ * separate calls run on them.
+ */
+csa_status csa_indexer_topk(const csa_config *cfg, const void *qI, const float *w, int32_t T,
+                            const int64_t *q_pos, const void *kI, const float *kscale, int64_t E_cap,
+                            int32_t *idx, void *ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
  * csa_topk — per row, the cfg->k best of scores[r, 0:n_valid[r]] under the total order

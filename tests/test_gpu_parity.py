@@ -157,6 +157,48 @@ def test_indexer_tensor_cores_candidates(HI, fp8, B, n_cand):
     assert_scores_close(got[:, :n_cand], ref_c, 5e-2 if fp8 else 1e-2)
 
 
+@pytest.mark.parametrize("HI,T,fp8,mode", [(64, 700, False, "random"), (64, 700, True, "random"),
+                                           (64, 640, False, "rising"), (64, 640, False, "ties"),
+                                           (32, 300, False, "random"), (64, 5, False, "random")])
+def test_indexer_topk_matches_scores_then_topk(HI, T, fp8, mode):
+    """csa_indexer_topk returns exactly what csa_topk returns on the scores csa_indexer_scores
+    writes, and agrees with the oracle up to score-tolerance swaps; rising scores and long runs
+    of tied scores are the selection's hard cases."""
+    B, dI, m, E, k = 2, 128, 4, 128 * 60 + 37, 512
+    qI = rnd(41 + HI, (B, T, HI, dI), dI ** -0.5, BF16)
+    w = rnd(42, (B, T, HI))
+    kf = rnd(43, (B, E, dI), dI ** -0.5)
+    if mode == "rising":        # every query scores a key higher than all keys before it
+        qI = qI.abs()
+        w = w.abs()
+        kf = kf.abs() * 0.05 + (torch.arange(E, device=DEV, dtype=torch.float32) / E)[None, :, None]
+    elif mode == "ties":        # 37 distinct keys: long runs of equal scores
+        kf = kf[:, torch.arange(E, device=DEV) % 37]
+    kI, ks = gen.quantize_keys_e4m3(kf) if fp8 else (kf.to(BF16), None)
+    g = torch.Generator().manual_seed(T + HI)
+    q_pos = torch.randint(0, m * E + 40, (B * T,), generator=g).to(torch.int64)
+    q_pos[:3] = torch.tensor([3, m * 100, m * E - 1])   # no entries, fewer than k, every entry
+    q_pos = q_pos.to(DEV)
+    c = cfg_obj(B=B, HI=HI, dI=dI, m=m, k=k, fp8_keys=fp8)
+    idx = torch.full((B * T, k), -7, dtype=torch.int32, device=DEV)
+    csa.indexer_topk(c, qI, w, q_pos, kI, idx, kscale=ks)
+    scores = torch.empty(B * T, E, device=DEV)
+    csa.indexer_scores(c, qI, w, q_pos, kI, scores, kscale=ks)
+    nv = ((q_pos + 1) // m).clamp(max=E).to(torch.int32)
+    ref_idx = torch.empty(B * T, k, dtype=torch.int32, device=DEV)
+    csa.topk(c, scores, ref_idx, n_valid=nv)
+    check_dev_error()
+    assert torch.equal(idx, ref_idx)
+    # and against the oracle on a few rows (score tolerance for swaps at near-ties)
+    kdeq, qn, wn, nvn = keys_f64(kI, ks), np64(qI), np64(w), nv.cpu().numpy()
+    for r in [0, 1, 2, 3, B * T // 2, B * T - 1]:
+        b, t = divmod(r, T)
+        ref = O.indexer_scores(qn[b, t], wn[b, t], kdeq[b], int(nvn[r]))
+        fin = ref[np.isfinite(ref)]
+        tol = (5e-2 if fp8 else 1e-2) * max(np.sqrt((fin ** 2).mean()) if fin.size else 0.0, 1e-30)
+        assert_selection_ok(idx[r].cpu().numpy(), O.topk(ref.astype(np.float32), int(nvn[r]), k), ref, k, tol)
+
+
 def test_indexer_cuda_core_fp32_and_candidates():
     cfg = gen.CONFIGS[1].replace(mode="decode")
     inp = gen.make_inputs(cfg, DEV)
