@@ -30,7 +30,12 @@ the pages):
     local rows hold; window rows and selected entries are not de-duplicated;
   * top-k order is (score descending, index ascending) with -0 == +0; output indices
     ascending, padded with -1 when fewer than k entries are visible;
-  * attention logits are softmax_scale * q . r with softmax_scale = 1/sqrt(d) by default.
+  * attention logits are softmax_scale * q . r with softmax_scale = 1/sqrt(d) by default;
+  * the one-stream compressor (HCA at m' = 128, the CSA2 encoder at m = 2) mixes the m
+    tokens of its own block only; HCA's positional bias is added to the gate logits by
+    position inside the block, and the CSA2 compressor has none;
+  * an HCA query at t attends to every entry s < floor((t + 1) / m') plus the same window
+    and sink as the CSA core attention.
 
 Parity status: every function here is pinned by tests (closed forms, hand-computed
 examples, brute force against library routines, invariants); see tests/test_oracle_pins.py.
@@ -160,6 +165,46 @@ def compress_range(kv, z, bias, m: int, i_begin: int, i_end: int, tok0: int = 0)
 
 
 # ----------------------------------------------------------------------------------
+# one-stream compressor without overlap
+#   [V4] "Heavily Compressed Attention": the same compressor at m' = 128 with a single KV
+#   stream, so no overlap between blocks; its positional bias runs over the m' positions of
+#   a block.  [V41d] "Encoder groups compress pairs": ratio 2, a learned channel-wise softmax
+#   pools each pair and the groups do not overlap; [V41d] also notes that the CSA2
+#   compressor drops the learned absolute position embedding (bias=None).
+# ----------------------------------------------------------------------------------
+
+
+def compress_single_entry(kv: np.ndarray, z: np.ndarray, bias: Optional[np.ndarray], m: int, i: int,
+                          tok0: int = 0, return_weights: bool = False):
+    """Entry i of the one-stream compressor.
+
+    kv, z: [n_tok, dim] rows (C and Z) of tokens tok0 .. tok0 + n_tok - 1; bias: [m, dim]
+    positional bias by position inside the block, or None.  For every channel the softmax
+    runs over the m logits Z[m*i + j] (+ bias[j]), j = 0 .. m-1, and the entry is the
+    weighted sum of C over the same m tokens.
+    """
+    r0 = m * i - tok0
+    if r0 < 0 or r0 + m > kv.shape[0]:
+        raise ValueError("stream rows of the block are missing")
+    lg = z[r0:r0 + m].astype(np.float64)
+    if bias is not None:
+        lg = lg + np.asarray(bias, np.float64)
+    lg = lg - lg.max(axis=0, keepdims=True)
+    wts = np.exp(lg)
+    wts = wts / wts.sum(axis=0, keepdims=True)
+    entry = (wts * kv[r0:r0 + m].astype(np.float64)).sum(axis=0)
+    return (entry, wts) if return_weights else entry
+
+
+def compress_single_range(kv, z, bias, m: int, i_begin: int, i_end: int, tok0: int = 0) -> np.ndarray:
+    """One-stream entries i_begin .. i_end - 1, stacked [i_end - i_begin, dim]."""
+    out = np.empty((max(0, i_end - i_begin), kv.shape[-1]), dtype=np.float64)
+    for n, i in enumerate(range(i_begin, i_end)):
+        out[n] = compress_single_entry(kv, z, bias, m, i, tok0)
+    return out
+
+
+# ----------------------------------------------------------------------------------
 # a2: lightning indexer  [V4] "The Lightning Indexer";  causality: "The sliding window is
 # not an optimisation" (entry i may be read from t only if m(i+1) - 1 <= t)
 # ----------------------------------------------------------------------------------
@@ -269,6 +314,19 @@ def sparse_attention(q: np.ndarray, rows: np.ndarray, sink: np.ndarray, scale: f
 
 
 # ----------------------------------------------------------------------------------
+# HCA core attention  [V4] "Heavily Compressed Attention": no indexer and no top-k; the
+# layer attends densely over every entry it holds, with the window and per-head sink of
+# the CSA core attention ("Attention sink, and heads that abstain": both CSA and HCA carry
+# one sink logit per head).
+# ----------------------------------------------------------------------------------
+
+
+def dense_rows(kv_comp: np.ndarray, nv: int, kv_local: np.ndarray, local_base: int, t: int, W: int) -> np.ndarray:
+    """HCA's rows for a query at t: compressed entries 0 .. nv-1, then the window rows."""
+    return gather_rows(kv_comp, np.arange(nv), kv_local, local_base, t, W)
+
+
+# ----------------------------------------------------------------------------------
 # compositions
 # ----------------------------------------------------------------------------------
 
@@ -313,5 +371,35 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
             kI_deq[e] = ki
         entry = (e, kv_comp[e].copy(), ki)
     r = decode_token(cfg, inp, b, 0, kv_comp, kI_deq)
+    r["entry"] = entry
+    return r
+
+
+def hca_token(cfg, inp: Dict[str, np.ndarray], b: int, tq: int, kv_comp: np.ndarray) -> Dict[str, np.ndarray]:
+    """HCA attention for one query (sequence b, query slot tq) over sequence b's cache
+    kv_comp [E, d] (entries 0 .. nv-1 with nv = min(floor((t+1)/m), E)) plus the window."""
+    t = int(inp["q_pos"][b * cfg.T + tq])
+    nv = min(visible_entries(t, cfg.m), kv_comp.shape[0])
+    rows = dense_rows(kv_comp, nv, inp["kv_local"][b], int(inp["local_base"][b]), t, cfg.W)
+    out, lse = sparse_attention(inp["q"][b, tq], rows, inp["sink"], cfg.softmax_scale)
+    return {"out": out, "lse": lse, "nv": nv}
+
+
+def hca_decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.ndarray) -> Dict[str, np.ndarray]:
+    """One HCA decode token of sequence b (T = 1).
+
+    When the token at t completes a block ((t + 1) % m == 0), entry (t + 1)/m - 1 is
+    compressed from the one-stream tail (rows = tokens t-m+1 .. t of kv_str / z_str, bias
+    [m, d] or None) into kv_comp [E, d] (updated in place); then dense attention.
+    """
+    t = int(inp["q_pos"][b])
+    entry = None
+    if (t + 1) % cfg.m == 0:
+        e = (t + 1) // cfg.m - 1
+        if e < kv_comp.shape[0]:
+            kv_comp[e] = compress_single_entry(inp["kv_str"][b], inp["z_str"][b], inp.get("bias"), cfg.m, e,
+                                               tok0=t - cfg.m + 1)
+            entry = (e, kv_comp[e].copy())
+    r = hca_token(cfg, inp, b, 0, kv_comp)
     r["entry"] = entry
     return r

@@ -1,4 +1,4 @@
-"""Counter-based seeded generator and the five workload presets.
+"""Counter-based seeded generator and the workload presets.
 
 Every element of every tensor is a pure function of (seed, tensor id, flat element
 index), so any slice of a tensor can be regenerated on its own, on the CPU or on a
@@ -112,7 +112,7 @@ class CsaConfig:
     T: int            # query tokens per sequence, at t = N-T .. N-1
     act: str          # "f32" | "bf16": dtype of q, qI, KV streams, caches, window rows
     kidx: str         # "act" | "fp8": storage of the indexer keys
-    mode: str         # "full" | "decode" | "prefill" | "csa2"
+    mode: str         # "full" | "decode" | "prefill" | "csa2" | "hca_full" | "hca_decode" | "hca_prefill"
     pool_block: int = 8
     pool_blocks: int = 2048
     n_reuse: int = 3
@@ -153,6 +153,17 @@ CONFIGS: Dict[int, CsaConfig] = {
     5: CsaConfig(5, "V4.1-Flash CSA2 decoder group bf16 (B 8 @ 262,144, 1 Reindex + 3 Reuse)",
                  B=8, N=262144, m=1, d=512, H=64, HI=32, dI=128, k=512, W=128, T=1,
                  act="bf16", kidx="act", mode="csa2"),
+    # Heavily Compressed Attention: one-stream compression at m' = 128, dense attention over
+    # every visible entry plus the window (the indexer fields are not used)
+    6: CsaConfig(6, "V4-Flash HCA decode @1M ctx (B 4, m' 128: 8,192 entries, dense attention)",
+                 B=4, N=1 << 20, m=128, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
+                 act="bf16", kidx="act", mode="hca_decode"),
+    7: CsaConfig(7, "V4-Flash HCA prefill bf16 (4,096 tokens after 131,072; m' 128)",
+                 B=1, N=131072 + 4096, m=128, d=512, H=64, HI=64, dI=128, k=512, W=128, T=4096,
+                 act="bf16", kidx="act", mode="hca_prefill"),
+    8: CsaConfig(8, "tiny HCA layer fp32 (N 4096, m' 128, 8x64 heads, W 128, 16 queries)",
+                 B=1, N=4096, m=128, d=64, H=8, HI=4, dI=32, k=64, W=128, T=16,
+                 act="f32", kidx="act", mode="hca_full"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)
@@ -197,6 +208,8 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
       compression streams kv_str/z_str [B,n_str,2,d], kvI_str/zI_str [B,n_str,2,dI],
       bias [2,m,d] f32, biasI [2,m,dI] f32, str_base [B] i64 (token of stream row 0).
     CSA2 presets add per-layer q/kv_local/sink stacks and the Full-layer indexer query.
+    HCA presets (mode hca_*) have no indexer tensors and one compression stream:
+      kv_str/z_str [B,n_str,d], bias [m,d] f32, str_base [B] i64.
     """
     act = cfg.torch_act
     B, T, H, d, HI, dI, m, E, W = cfg.B, cfg.T, cfg.H, cfg.d, cfg.HI, cfg.dI, cfg.m, cfg.E, cfg.W
@@ -222,6 +235,8 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
         out["q"] = _gen(cfg, "q", (B, T, H, d), 1 / math.sqrt(d), act, device, row0=row0)
         out["kv_local"] = _gen(cfg, "kv_local", (B, L, d), 1 / math.sqrt(d), act, device, row0=row0)
         out["sink"] = _gen(cfg, "sink", (H,), 1.0, f32, device)
+    if cfg.mode.startswith("hca"):
+        return _hca_inputs(cfg, out, device, row0, skip)
     out["qI"] = _gen(cfg, "qI", (B, T, HI, dI), 1 / math.sqrt(dI), act, device, row0=row0)
     out["w"] = _gen(cfg, "w", (B, T, HI), 1.0, f32, device, row0=row0)
 
@@ -256,6 +271,31 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
         out["zI_str"] = _gen(cfg, "zI_str", (B, n_str, 2, dI), 1 / math.sqrt(dI), act, device, row0=row0)
         out["bias"] = _gen(cfg, "bias", (2, m, d), 0.1, f32, device)
         out["biasI"] = _gen(cfg, "biasI", (2, m, dI), 0.1, f32, device)
+    return out
+
+
+def _hca_inputs(cfg: CsaConfig, out: Dict[str, torch.Tensor], device, row0: int, skip) -> Dict[str, torch.Tensor]:
+    """The compressed cache and the one-stream compression inputs of an HCA preset."""
+    act = cfg.torch_act
+    B, T, d, m, E = cfg.B, cfg.T, cfg.d, cfg.m, cfg.E
+    t0 = cfg.N - T
+    if "kv_comp" not in skip:
+        if cfg.mode == "hca_full":
+            out["kv_comp"] = torch.zeros((B, E, d), dtype=act, device=device)
+        else:
+            out["kv_comp"] = _gen(cfg, "kv_comp", (B, E, d), 1 / math.sqrt(d), act, device, row0=row0)
+    if cfg.mode == "hca_full":
+        base, n_str = 0, cfg.N
+    elif cfg.mode == "hca_decode":
+        base, n_str = cfg.N - m, m
+    else:
+        if t0 % m:
+            raise ValueError("an HCA prefill chunk starts on a block boundary")
+        base, n_str = t0, T
+    out["str_base"] = torch.full((B,), base, dtype=torch.int64, device=device)
+    out["kv_str"] = _gen(cfg, "kv_str", (B, n_str, d), 1 / math.sqrt(d), act, device, row0=row0)
+    out["z_str"] = _gen(cfg, "z_str", (B, n_str, d), 1 / math.sqrt(d), act, device, row0=row0)
+    out["bias"] = _gen(cfg, "bias", (m, d), 0.1, torch.float32, device)
     return out
 
 

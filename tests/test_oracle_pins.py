@@ -366,3 +366,132 @@ def test_gather_rows_order_and_padding():
     loc = -np.arange(12, dtype=np.float64).reshape(4, d)
     rows = O.gather_rows(kv, np.array([2, 7, -1, -1]), loc, local_base=20, t=22, W=2)
     np.testing.assert_array_equal(rows, np.stack([kv[2], kv[7], loc[1], loc[2]]))
+
+
+# ------------------------------------------------------------------ one-stream compressor (HCA, CSA2 encoder)
+
+def test_compress_single_hand_example():
+    # m = 2, two channels.  Channel 0: logits 0 and ln 3 give weights 1/4, 3/4 -> 1 + 6 = 7;
+    # channel 1: equal logits -> the mean 2.  With bias (ln 3, 0) / (0, ln 2): channel 0
+    # logits ln 3, ln 3 -> mean 6; channel 1 logits 0, ln 2 -> 1/3 * 1 + 2/3 * 3 = 7/3.
+    kv = np.array([[4.0, 1.0], [8.0, 3.0]])
+    z = np.array([[0.0, 0.0], [math.log(3.0), 0.0]])
+    np.testing.assert_allclose(O.compress_single_entry(kv, z, None, 2, 0), [7.0, 2.0], rtol=1e-15)
+    bias = np.array([[math.log(3.0), 0.0], [0.0, math.log(2.0)]])
+    np.testing.assert_allclose(O.compress_single_entry(kv, z, bias, 2, 0), [6.0, 7.0 / 3.0], rtol=1e-15)
+    # entry 1 reads tokens 2, 3 only (no overlap with entry 0)
+    kv2 = np.concatenate([kv, [[10.0, -2.0], [20.0, 4.0]]])
+    z2 = np.concatenate([z, [[0.0, math.log(3.0)], [0.0, 0.0]]])
+    np.testing.assert_allclose(O.compress_single_entry(kv2, z2, None, 2, 1), [15.0, 0.75 * -2.0 + 0.25 * 4.0],
+                               rtol=1e-15)
+
+
+def test_compress_single_closed_forms():
+    m, dim = 128, 7
+    kv = rng.standard_normal((3 * m, dim))
+    # constant gate, no bias: the arithmetic mean of the block's m tokens
+    z = np.full((3 * m, dim), 0.37)
+    for i in range(3):
+        np.testing.assert_allclose(O.compress_single_entry(kv, z, None, m, i), kv[m * i:m * (i + 1)].mean(0),
+                                   rtol=1e-12, atol=1e-15)
+    # a bias that cancels the gate's variation also gives the mean
+    z = rng.standard_normal((m, dim))
+    np.testing.assert_allclose(O.compress_single_entry(kv[:m], z, -z, m, 0), kv[:m].mean(0), rtol=1e-12, atol=1e-15)
+    # one dominant logit per channel copies that token's value
+    z = rng.standard_normal((m, dim))
+    pick = rng.integers(0, m, dim)
+    z[pick, np.arange(dim)] += 1e4
+    np.testing.assert_allclose(O.compress_single_entry(kv[:m], z, None, m, 0), kv[pick, np.arange(dim)], rtol=1e-12)
+    # m = 1: the softmax over one logit is 1, the entry is the token
+    z = rng.standard_normal((5, dim))
+    np.testing.assert_allclose(O.compress_single_range(kv[:5], z, None, 1, 0, 5), kv[:5], rtol=0, atol=0)
+    # weights are positive and sum to 1 per channel
+    _, w = O.compress_single_entry(kv, rng.standard_normal((3 * m, dim)) * 4, rng.standard_normal((m, dim)), m, 2,
+                                   return_weights=True)
+    assert w.shape == (m, dim) and np.all(w > 0)
+    np.testing.assert_allclose(w.sum(0), 1.0, rtol=1e-14)
+
+
+def test_compress_single_each_token_in_one_entry_and_causal():
+    m, dim, n_ent = 4, 3, 6
+    kv = rng.standard_normal((m * n_ent, dim))
+    z = rng.standard_normal((m * n_ent, dim))
+    bias = rng.standard_normal((m, dim)) * 0.1
+    base = O.compress_single_range(kv, z, bias, m, 0, n_ent)
+    for p in range(m * n_ent):
+        kv2 = kv.copy()
+        kv2[p] += 1.0
+        changed = np.any(O.compress_single_range(kv2, z, bias, m, 0, n_ent) != base, axis=1)
+        assert changed.tolist() == [i == p // m for i in range(n_ent)], p
+    # the bias is indexed by the position inside the block, not by the token
+    b2 = bias.copy()
+    b2[1] += 0.5
+    moved = np.any(O.compress_single_range(kv, z, b2, m, 0, n_ent) != base, axis=1)
+    assert moved.all()
+    # tok0 offset: the same entries from a buffer that starts at token m*2
+    np.testing.assert_array_equal(O.compress_single_range(kv[2 * m:], z[2 * m:], bias, m, 2, n_ent, tok0=2 * m),
+                                  base[2:])
+
+
+def test_compress_single_is_two_stream_entry_zero():
+    # the two-stream compressor's entry 0 has no stream b: it is the one-stream entry of
+    # stream a with bias B^a
+    m, dim = 4, 5
+    kv = rng.standard_normal((m, 2, dim))
+    z = rng.standard_normal((m, 2, dim))
+    bias = rng.standard_normal((2, m, dim))
+    np.testing.assert_allclose(O.compress_single_entry(kv[:, 0], z[:, 0], bias[0], m, 0),
+                               O.compress_entry(kv, z, bias, m, 0), rtol=1e-15)
+
+
+# ------------------------------------------------------------------ HCA attention
+
+def test_hca_dense_rows_and_sdpa_reduction():
+    H, d, E, W = 4, 16, 40, 6
+    q = rng.standard_normal((H, d))
+    kv = rng.standard_normal((E, d))
+    loc = rng.standard_normal((W + 3, d))
+    m, t, base = 128, 128 * 23 + 5, 128 * 23 + 5 - W - 2
+    nv = O.visible_entries(t, m)
+    assert nv == 23
+    rows = O.dense_rows(kv, nv, loc, base, t, W)
+    np.testing.assert_array_equal(rows, np.concatenate([kv[:nv], loc[t - W + 1 - base:t + 1 - base]]))
+    # no window, sink -> -inf: dense MQA attention over the visible entries (torch SDPA)
+    rows0 = O.dense_rows(kv, nv, loc, base, t, 0)
+    out, _ = O.sparse_attention(q, rows0, np.full(H, -np.inf), 1 / math.sqrt(d))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, None, None, :], torch.from_numpy(kv[:nv])[None, None].expand(H, 1, nv, d),
+        torch.from_numpy(kv[:nv])[None, None].expand(H, 1, nv, d), scale=1 / math.sqrt(d))[:, 0, 0]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12)
+    # with window and sink: SDPA over the same rows with the sink as a zero-value column
+    sink = rng.standard_normal(H)
+    out, _ = O.sparse_attention(q, rows, sink, 1 / math.sqrt(d))
+    np.testing.assert_allclose(out, _sdpa_with_sink(q, rows, sink, 1 / math.sqrt(d)), rtol=1e-12, atol=1e-14)
+
+
+def test_hca_decode_step_writes_the_block_entry_first():
+    class C:
+        m, W, T, softmax_scale = 8, 4, 1, 0.25
+    H, d, E = 2, 6, 10
+    t = 8 * 7 - 1                                   # completes block 6
+    inp = {"q_pos": np.array([t]), "q": rng.standard_normal((1, 1, H, d)), "sink": rng.standard_normal(H),
+           "kv_local": rng.standard_normal((1, 8, d)), "local_base": np.array([t - 7]),
+           "kv_str": rng.standard_normal((1, 8, d)), "z_str": rng.standard_normal((1, 8, d)),
+           "bias": rng.standard_normal((8, d))}
+    kv = rng.standard_normal((E, d))
+    kv_before = kv.copy()
+    r = O.hca_decode_step_sequence(C, inp, 0, kv)
+    assert r["nv"] == 7 and r["entry"][0] == 6
+    ent = O.compress_single_entry(inp["kv_str"][0], inp["z_str"][0], inp["bias"], 8, 6, tok0=t - 7)
+    np.testing.assert_array_equal(kv[6], ent)
+    np.testing.assert_array_equal(np.delete(kv, 6, 0), np.delete(kv_before, 6, 0))
+    rows = np.concatenate([kv[:7], inp["kv_local"][0][4:8]])
+    out, lse = O.sparse_attention(inp["q"][0, 0], rows, inp["sink"], 0.25)
+    np.testing.assert_allclose(r["out"], out, rtol=1e-15)
+    # a token inside a block writes nothing and sees only the completed entries
+    inp["q_pos"] = np.array([t + 3])
+    inp["local_base"] = np.array([t - 4])
+    kv2 = kv.copy()
+    r2 = O.hca_decode_step_sequence(C, inp, 0, kv2)
+    assert r2["entry"] is None and r2["nv"] == 7
+    np.testing.assert_array_equal(kv2, kv)
