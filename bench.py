@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -78,10 +78,15 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-STAGE_PROFILES = {4: "indexer_tc_e4m3_1M_decode.md", 2: "indexer_tc_bf16_64K_decode.md",
-                  3: "indexer_tc_bf16_prefill_4K.md", 5: "indexer_tc_bf16_csa2_scan_256K.md"}
-STAGE_KERNELS = ("indexer_qprep_kernel", "indexer_tc_kernel")
-STAGE_SOURCES = ("k_indexer.cu", "csa_ptx.cuh", "csa_internal.h")
+_INDEXER_STAGE = (("indexer_qprep_kernel", "indexer_tc_kernel"), ("k_indexer.cu", "csa_ptx.cuh", "csa_internal.h"))
+_DENSE_STAGE = (("attn_pf_kernel", "attn_merge_dec_kernel"), ("k_attn.cu", "csa_ptx.cuh", "csa_internal.h"))
+# config -> (summary file, kernels of the stage, sources the summary's counters were taken with)
+STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
+                  2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE,
+                  3: ("indexer_tc_bf16_prefill_4K.md",) + _INDEXER_STAGE,
+                  5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE,
+                  6: ("hca_dense_attn_1M_decode.md",) + _DENSE_STAGE,
+                  7: ("hca_dense_attn_prefill_4K.md", ("attn_pf_kernel",), _DENSE_STAGE[1])}
 
 
 def stage_traffic(config):
@@ -90,7 +95,10 @@ def stage_traffic(config):
     The summary carries `traffic-bytes-per-launch <kernel> <bytes>` lines and the sha256 of
     the kernel sources it was taken with; the figure is used only while every stage kernel
     has a line and the sources are unchanged."""
-    path = os.path.join(ROOT, "profiles", STAGE_PROFILES.get(config, ""))
+    if config not in STAGE_PROFILES:
+        return None
+    fname, kernels, sources = STAGE_PROFILES[config]
+    path = os.path.join(ROOT, "profiles", fname)
     if not os.path.isfile(path):
         return None
     per, sha = {}, None
@@ -103,12 +111,12 @@ def stage_traffic(config):
                 sha = w[1]
     src = os.path.join(ROOT, "compressed_sparse_attention_csa_gb300", "csrc")
     h = hashlib.sha256()
-    for name in STAGE_SOURCES:
+    for name in sources:
         with open(os.path.join(src, name), "rb") as f:
             h.update(f.read())
-    if sha != h.hexdigest() or any(k not in per for k in STAGE_KERNELS):
+    if sha != h.hexdigest() or any(k not in per for k in kernels):
         return None
-    return sum(per[k] for k in STAGE_KERNELS)
+    return sum(per[k] for k in kernels)
 
 
 class ClockSampler:
@@ -442,7 +450,146 @@ class Csa2Group:
         return n, elapsed, desc
 
 
-WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group}
+class HcaDecode:
+    """HCA ("Heavily Compressed Attention") decode: one-stream compression of the block the
+    token completes, then dense attention over every visible entry plus the window."""
+
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        self.units = cfg.B
+        self.metric = "HCA decode tok/s @1M ctx"
+        self.workload = (f"V4-Flash HCA decode step, batch {cfg.B} @ {cfg.N:,}-token context (m' {cfg.m}: "
+                         f"{cfg.E:,} entries/seq, dense attention), bf16 KV, {cfg.H}x{cfg.d} heads, W {cfg.W}; "
+                         f"one-stream compression of the completed block")
+        self.config_extra = {"batch": cfg.B, "context": cfg.N, "m": cfg.m, "entries_per_seq": cfg.E,
+                             "heads": cfg.H, "head_dim": cfg.d, "window": cfg.W}
+        if host_only:
+            return
+        self.csa = csa
+        inp = gen.make_inputs(cfg, dev, row0=row0)
+        self.inp = inp
+        self.c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
+        self.out = torch.empty(cfg.B, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
+        self.lse = torch.empty(cfg.B, cfg.H, device=dev)
+        self.args = dict(q_pos=inp["q_pos"], q=inp["q"], sink=inp["sink"], kv_comp=inp["kv_comp"],
+                         kv_tail=inp["kv_str"], z_tail=inp["z_str"], bias=inp["bias"], kv_local=inp["kv_local"],
+                         local_base=inp["local_base"], out=self.out, lse=self.lse)
+        from compressed_sparse_attention_csa_gb300.accounting import hca_decode_work
+        work = hca_decode_work(cfg)
+        self.stage_label = "dense attention: attn_pf_kernel (rows split over CTAs) + attn_merge_dec_kernel"
+        self.stage_bound = "hbm"
+        self.stage_amount = work["attention_bytes"]
+        self.step_bytes = work["bytes"]
+        self.touched_bytes = work["bytes"]
+        self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_str", "z_str", "kv_local"]}
+        self.e2e_out = self.out
+
+    def step(self):
+        self.csa.hca_decode_step(self.c, **self.args)
+
+    def stage_fn(self):
+        inp = self.inp
+        self.csa.dense_attn(self.c, inp["q"], inp["kv_comp"], inp["kv_local"], inp["local_base"], inp["q_pos"],
+                            inp["sink"], self.out, self.lse)
+
+    def oracle(self, n, inp_cpu=None):
+        """n sequences of the workload, one decode token each."""
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        nb = src["q_pos"].shape[0]
+        sub = cfg.replace(B=1)
+        elapsed, cache = 0.0, {}
+        for i in range(n):
+            b = (i * nb) // n
+            if b not in cache:
+                cache = {b: {k: _host64(v if k in ("bias", "sink") else v[b:b + 1]) for k, v in src.items()}}
+            host = cache[b]
+            kv_comp = host["kv_comp"][0].copy()
+            t0 = time.perf_counter()
+            O.hca_decode_step_sequence(sub, host, 0, kv_comp)
+            elapsed += time.perf_counter() - t0
+        desc = (f"{n} sequence(s) of this workload, one decode token each (one-stream compression, dense "
+                f"attention over {cfg.E:,}+{cfg.W} rows), float64 numpy, {elapsed:.1f} s")
+        return n, elapsed, desc
+
+
+class HcaPrefill:
+    """HCA prefill chunk: one-stream compression of the chunk's new entries, then dense
+    attention for every query of the chunk."""
+
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        B, T, E = cfg.B, cfg.T, cfg.E
+        self.units = B * T
+        self.metric = "HCA prefill tok/s (4,096-token chunk @128K ctx)"
+        self.workload = (f"V4-Flash HCA prefill chunk: {T:,} new tokens after {cfg.N - T:,} (m' {cfg.m}: entries "
+                         f"{(cfg.N - T) // cfg.m:,} -> {E:,}), batch {B}, bf16, {cfg.H}x{cfg.d} heads, W {cfg.W}; "
+                         f"one-stream compression of the chunk, dense attention")
+        self.config_extra = {"batch": B, "chunk": T, "context_before": cfg.N - T, "m": cfg.m,
+                             "entries_after": E, "heads": cfg.H, "head_dim": cfg.d, "window": cfg.W}
+        self.tok0 = cfg.N - T
+        self.e0, self.e1 = (cfg.N - T) // cfg.m, cfg.N // cfg.m
+        if host_only:
+            return
+        self.csa = csa
+        inp = gen.make_inputs(cfg, dev, row0=row0)
+        self.inp = inp
+        self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
+        self.out = torch.empty(B, T, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
+        self.lse = torch.empty(B, T, cfg.H, device=dev)
+        from compressed_sparse_attention_csa_gb300.accounting import hca_prefill_work
+        work = hca_prefill_work(cfg)
+        self.stage_label = "dense attention: attn_pf_kernel (one CTA per query)"
+        self.stage_bound = "tensor"
+        self.stage_amount = work["attention_flops"]
+        self.step_flops = work["flops"]
+        self.touched_bytes = work["bytes"]
+        self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_str", "z_str", "kv_local"]}
+        self.e2e_out = self.out
+
+    def step(self):
+        csa, c, inp = self.csa, self.c, self.inp
+        csa.compress_kv_single(c, inp["kv_str"], inp["z_str"], inp["bias"], self.tok0, self.e0, self.e1,
+                               inp["kv_comp"])
+        self.stage_fn()
+
+    def stage_fn(self):
+        inp = self.inp
+        self.csa.dense_attn(self.c, inp["q"], inp["kv_comp"], inp["kv_local"], inp["local_base"], inp["q_pos"],
+                            inp["sink"], self.out, self.lse)
+
+    def oracle(self, n, inp_cpu=None):
+        """The chunk's compression (charged pro rata) plus n query rows spread over the chunk."""
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        h = {k: _host64(v if k in ("bias", "sink", "q_pos") else v[0:1]) for k, v in src.items()}
+        kv_comp = h["kv_comp"][0].copy()
+        t0 = time.perf_counter()
+        kv_comp[self.e0:self.e1] = O.compress_single_range(h["kv_str"][0], h["z_str"][0], h["bias"], cfg.m,
+                                                           self.e0, self.e1, tok0=self.tok0)
+        t_comp = time.perf_counter() - t0
+        sub = cfg.replace(B=1)
+        t_rows = 0.0
+        for i in range(n):
+            tq = (i * (cfg.T - 1)) // max(n - 1, 1)
+            t0 = time.perf_counter()
+            O.hca_token(sub, h, 0, tq, kv_comp)
+            t_rows += time.perf_counter() - t0
+        elapsed = t_rows + t_comp * n / cfg.T
+        desc = (f"{n} query row(s) of the chunk (dense attention over ~{cfg.E:,}+{cfg.W} rows) plus {n}/{cfg.T} "
+                f"of the chunk's compression ({t_comp:.1f} s whole), float64 numpy, {t_rows:.1f} s of rows")
+        return n, elapsed, desc
+
+
+WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill}
 
 
 def config_of(wl):
@@ -450,7 +597,7 @@ def config_of(wl):
     return dict(workload=wl.workload, **wl.config_extra,
                 l2="inputs larger than L2: independent copies of the workload stepped in rotation",
                 timing="K steps replayed back to back as CUDA graphs between one pair of CUDA events")
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6}
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048}
 
 
 # ------------------------------------------------------------------ main
@@ -477,7 +624,7 @@ def main():
         # float64 numpy step takes seconds, so the run stops after REFERENCE_BUDGET_S of oracle
         # time even if fewer than --steps steps ran; `steps` reports the steps actually timed.
         wl = Wl(cfg, None, torch, "cpu", 0, host_only=True)
-        n1 = 4 if args.config == 3 else 1
+        n1 = 4 if args.config in (3, 7) else 1
         inp = gen.make_inputs(cfg.replace(B=1), "cpu")
         n_total, t_total, desc, done = 0, 0.0, "", 0
         while done < max(args.steps, 1) and (done == 0 or t_total < REFERENCE_BUDGET_S):

@@ -12,7 +12,8 @@ LIB_PATH = os.path.join(HERE, "libcsa.so")
 c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
 CSA_F32, CSA_BF16, CSA_E4M3 = 0, 1, 2
-CSA_OP_COMPRESS, CSA_OP_INDEXER, CSA_OP_TOPK, CSA_OP_ATTN, CSA_OP_DECODE, CSA_OP_POOL, CSA_OP_INDEXER_TOPK = range(7)
+(CSA_OP_COMPRESS, CSA_OP_INDEXER, CSA_OP_TOPK, CSA_OP_ATTN, CSA_OP_DECODE, CSA_OP_POOL, CSA_OP_INDEXER_TOPK,
+ CSA_OP_DENSE_ATTN, CSA_OP_HCA_DECODE) = range(9)
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_DTYPE", 4: "CSA_ERR_ALIGN",
           5: "CSA_ERR_WORKSPACE", 6: "CSA_ERR_CUDA", 7: "CSA_ERR_TIMEOUT", 8: "CSA_ERR_INDEX"}
 
@@ -30,6 +31,12 @@ class csa_decode_args(ctypes.Structure):
                 ("L", c_i64), ("local_base", c_vp), ("out", c_vp), ("lse", c_vp), ("idx_out", c_vp)]
 
 
+class csa_hca_decode_args(ctypes.Structure):
+    _fields_ = [("E_cap", c_i64), ("q_pos", c_vp), ("q", c_vp), ("sink", c_vp), ("kv_comp", c_vp),
+                ("kv_tail", c_vp), ("z_tail", c_vp), ("bias", c_vp), ("kv_local", c_vp), ("L", c_i64),
+                ("local_base", c_vp), ("out", c_vp), ("lse", c_vp)]
+
+
 # name -> (restype, argtypes); the exported symbols of include/csa.h
 SIGNATURES = {
     "csa_version": (c_i32, []),
@@ -40,6 +47,8 @@ SIGNATURES = {
     "csa_block_pool_workspace_size": (c_sz, [c_i64, c_i64, c_i32, c_i32]),
     "csa_compress_kv": (ctypes.c_int, [ctypes.POINTER(csa_config), c_i32, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64,
                                        c_i64, c_vp, ctypes.c_int, c_vp, c_i64, c_vp]),
+    "csa_compress_kv_single": (ctypes.c_int, [ctypes.POINTER(csa_config), c_i32, c_vp, c_vp, c_vp, c_i64, c_i64,
+                                              c_i64, c_i64, c_vp, c_i64, c_vp]),
     "csa_indexer_scores": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64,
                                           c_vp, c_i32, c_vp, c_i64, c_vp, c_sz, c_vp]),
     "csa_indexer_topk": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64,
@@ -52,6 +61,10 @@ SIGNATURES = {
                                       c_vp, c_vp, c_vp, c_sz, c_vp]),
     "csa_sparse_attn": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i32, c_vp, c_i64, c_vp, c_vp, c_i64,
                                        c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "csa_dense_attn": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp, c_vp,
+                                      c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "csa_hca_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_hca_decode_args), c_vp,
+                                           c_sz, c_vp]),
     "csa_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
                                        c_vp]),
 }

@@ -107,3 +107,38 @@ def csa2_group_work(cfg, pool_blocks: int = 2048, block: int = 8, layers: int = 
     return {"scan_bytes": scan, "rescore_bytes": rescore, "attention_bytes": attn,
             "bytes": scan + rescore + attn, "bytes_without_scan": rescore + attn,
             "scan_flops": 2 * indexer_macs(cfg.HI, cfg.dI, nv) * B}
+
+
+def hca_decode_work(cfg) -> Dict[str, float]:
+    """Algorithmic bytes of one HCA decode token per sequence ("Heavily Compressed Attention":
+    no indexer; dense over every entry).
+
+    attention: each visible entry and window row once, q read and out written once;
+    compression (the token completes a block): the m stream tokens (C and Z), the positional
+    bias and the entry written.
+    """
+    ab = _act_bytes(cfg.act)
+    B = cfg.B
+    nv = cfg.N // cfg.m
+    rows = nv + cfg.W
+    attn = B * (rows * cfg.d * ab + 2 * cfg.H * cfg.d * ab)
+    comp = B * (2 * cfg.m * cfg.d * ab + cfg.d * ab) + cfg.m * cfg.d * 4
+    return {"attention_bytes": attn, "compress_bytes": comp, "bytes": attn + comp,
+            "attention_flops": 4 * cfg.H * cfg.d * rows * B}
+
+
+def hca_prefill_work(cfg) -> Dict[str, float]:
+    """Algorithmic work of one HCA prefill chunk: T new queries at t = N-T .. N-1 per sequence,
+    each attending to its floor((t+1)/m) visible entries plus min(W, t+1) window rows;
+    compression of the chunk's T/m new entries from its T stream tokens."""
+    ab = _act_bytes(cfg.act)
+    B, T, m = cfg.B, cfg.T, cfg.m
+    rows = 0
+    for t in range(cfg.N - T, cfg.N):
+        rows += min((t + 1) // m, cfg.E) + min(cfg.W, t + 1)
+    rows *= B
+    flops = 4 * cfg.H * cfg.d * rows
+    comp = B * (2 * T * cfg.d * ab + (T // m) * cfg.d * ab) + m * cfg.d * 4
+    attn = B * (cfg.E * cfg.d * ab + T * 2 * cfg.H * cfg.d * ab)     # every entry once, q/out once
+    return {"attention_rows": rows, "attention_flops": flops, "flops": flops, "attention_bytes": attn,
+            "compress_bytes": comp, "bytes": attn + comp}

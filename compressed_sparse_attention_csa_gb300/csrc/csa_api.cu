@@ -114,6 +114,21 @@ csa_status check_cfg(const csa_config* c) {
 
 csa_status launch_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
+// The calls of the HCA path read B, H, d, m, W, act and softmax_scale only.
+csa_status check_cfg_hca(const csa_config* c) {
+  if (!c) return CSA_ERR_NULL;
+  if (c->B < 1 || c->H < 1 || c->d < 1 || c->m < 1 || c->m > 4096 || c->W < 0) return CSA_ERR_SHAPE;
+  if (c->act != CSA_F32 && c->act != CSA_BF16) return CSA_ERR_DTYPE;
+  if (!std::isfinite(c->softmax_scale)) return CSA_ERR_SHAPE;
+  return CSA_OK;
+}
+
+bool dense_shape_ok(const csa_config* c) {
+  const bool tc = c->act == CSA_BF16 && c->H == 64 && c->d == 512;
+  const bool simt = c->d <= 128 && c->H <= 64;
+  return tc || simt;
+}
+
 bool attn_shape_ok(const csa_config* c) {
   const bool tc = c->act == CSA_BF16 && c->H == 64 && c->d == 512 && c->k <= 2048;
   const bool simt = c->d <= 128 && c->H <= 64;
@@ -193,8 +208,15 @@ csa_status csa_get_last_error(csa_stream_t stream) {
 }
 
 size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_t n_cols) {
-  if (check_cfg(cfg) != CSA_OK || rows < 0 || n_cols < 0) return static_cast<size_t>(-1);
   const int sms = device_sm_count();
+  if (op == CSA_OP_DENSE_ATTN || op == CSA_OP_HCA_DECODE) {  // rows = B*T (B for the step), n_cols = E_cap
+    if (check_cfg_hca(cfg) != CSA_OK || rows < 0 || n_cols < 0 || rows % cfg->B || n_cols > (int64_t(1) << 24) ||
+        (op == CSA_OP_HCA_DECODE && rows != cfg->B))
+      return static_cast<size_t>(-1);
+    return attn_dense_workspace_bytes(cfg->B, static_cast<int>(rows / cfg->B), cfg->H, cfg->d, n_cols, cfg->W,
+                                      cfg->act, sms);
+  }
+  if (check_cfg(cfg) != CSA_OK || rows < 0 || n_cols < 0) return static_cast<size_t>(-1);
   switch (op) {
     case CSA_OP_COMPRESS:
       return 0;
@@ -218,6 +240,8 @@ size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_
     case CSA_OP_INDEXER_TOPK:  // rows = B*T, n_cols = E_cap
       if (rows % cfg->B || n_cols < 1 || n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
       return indexer_topk_ws(cfg, static_cast<int>(rows / cfg->B), n_cols, sms);
+    default:
+      break;
   }
   return static_cast<size_t>(-1);
 }
@@ -258,6 +282,35 @@ csa_status csa_compress_kv(const csa_config* cfg, int32_t dim, const void* kv, c
   a.E_cap = E_cap;
   a.err = err_word_ptr();
   return launch_status(launch_compress(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_compress_kv_single(const csa_config* cfg, int32_t dim, const void* kv, const void* z,
+                                  const float* bias, int64_t n_tok, int64_t tok0, int64_t ent_begin, int64_t ent_end,
+                                  void* out, int64_t E_cap, csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!kv || !z || !out) return CSA_ERR_NULL;
+  if (!aligned16(kv) || !aligned16(z) || !aligned16(out) || (bias && !aligned16(bias))) return CSA_ERR_ALIGN;
+  const int64_t m = cfg->m;
+  if (dim < 2 || dim > 4096 || (dim & 1) || n_tok < 0 || ent_begin < 0 || ent_end < ent_begin || ent_end > E_cap ||
+      E_cap * cfg->B >= (int64_t(1) << 31))
+    return CSA_ERR_SHAPE;
+  if (ent_end > ent_begin && (tok0 > m * ent_begin || m * ent_end > tok0 + n_tok)) return CSA_ERR_SHAPE;
+  Compress1Args a{};
+  a.kv = kv;
+  a.z = z;
+  a.bias = bias;
+  a.out = out;
+  a.B = cfg->B;
+  a.m = cfg->m;
+  a.dim = dim;
+  a.act_bf16 = cfg->act == CSA_BF16;
+  a.n_tok = n_tok;
+  a.tok0 = tok0;
+  a.ent_begin = ent_begin;
+  a.n_ent = ent_end - ent_begin;
+  a.E_cap = E_cap;
+  return launch_status(launch_compress1(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float* w, int32_t T,
@@ -456,6 +509,97 @@ csa_status csa_sparse_attn(const csa_config* cfg, const void* q, int32_t T, cons
   a.err = err_word_ptr();
   a.num_sms = sms;
   return launch_status(launch_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+AttnArgs dense_args(const csa_config* cfg, const void* q, int32_t T, const void* kv_comp, int64_t E_cap,
+                    const void* kv_local, int64_t L, const int64_t* local_base, const int64_t* q_pos,
+                    const float* sink, void* out, float* lse, void* ws, size_t ws_bytes) {
+  AttnArgs a{};
+  a.q = q;
+  a.kv_comp = kv_comp;
+  a.idx = nullptr;
+  a.kv_local = kv_local;
+  a.local_base = local_base;
+  a.q_pos = q_pos;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.B = cfg->B;
+  a.T = T;
+  a.H = cfg->H;
+  a.d = cfg->d;
+  a.k = 1;
+  a.W = cfg->W;
+  a.E_cap = E_cap;
+  a.L = L;
+  a.softmax_scale = cfg->softmax_scale;
+  a.act = cfg->act;
+  a.dense_m = cfg->m;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.err = err_word_ptr();
+  a.num_sms = device_sm_count();
+  return a;
+}
+}  // namespace
+
+csa_status csa_dense_attn(const csa_config* cfg, const void* q, int32_t T, const void* kv_comp, int64_t E_cap,
+                          const void* kv_local, int64_t L, const int64_t* local_base, const int64_t* q_pos,
+                          const float* sink, void* out, float* lse, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!q || !kv_comp || !kv_local || !local_base || !q_pos || !sink || !out) return CSA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv_comp) || !aligned16(kv_local) || !aligned16(local_base) || !aligned16(q_pos) ||
+      !aligned16(sink) || !aligned16(out) || (lse && !aligned16(lse)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (T < 0 || E_cap < 0 || E_cap > (int64_t(1) << 24) || L < 0 || !dense_shape_ok(cfg) ||
+      E_cap * cfg->B >= (int64_t(1) << 31))
+    return CSA_ERR_SHAPE;
+  const size_t need = attn_dense_workspace_bytes(cfg->B, T, cfg->H, cfg->d, E_cap, cfg->W, cfg->act,
+                                                 device_sm_count());
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  const AttnArgs a = dense_args(cfg, q, T, kv_comp, E_cap, kv_local, L, local_base, q_pos, sink, out, lse, ws,
+                                ws_bytes);
+  return launch_status(launch_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_hca_decode_step(const csa_config* cfg, const csa_hca_decode_args* d, void* ws, size_t ws_bytes,
+                               csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!d) return CSA_ERR_NULL;
+  if (!d->q_pos || !d->q || !d->sink || !d->kv_comp || !d->kv_tail || !d->z_tail || !d->kv_local ||
+      !d->local_base || !d->out)
+    return CSA_ERR_NULL;
+  const void* ptrs[] = {d->q_pos, d->q, d->sink, d->kv_comp, d->kv_tail, d->z_tail, d->kv_local, d->local_base, d->out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA_ERR_ALIGN;
+  if ((d->bias && !aligned16(d->bias)) || (d->lse && !aligned16(d->lse)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  if (d->E_cap < 1 || d->E_cap > (int64_t(1) << 24) || d->L < 0 || !dense_shape_ok(cfg) || (cfg->d & 1) ||
+      d->E_cap * cfg->B >= (int64_t(1) << 31))
+    return CSA_ERR_SHAPE;
+  const size_t need = attn_dense_workspace_bytes(cfg->B, 1, cfg->H, cfg->d, d->E_cap, cfg->W, cfg->act,
+                                                 device_sm_count());
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Compress1Args c{};
+  c.kv = d->kv_tail;
+  c.z = d->z_tail;
+  c.bias = d->bias;
+  c.out = d->kv_comp;
+  c.B = cfg->B;
+  c.m = cfg->m;
+  c.dim = cfg->d;
+  c.act_bf16 = cfg->act == CSA_BF16;
+  c.q_pos = d->q_pos;
+  c.E_cap = d->E_cap;
+  cudaError_t e = launch_compress1(c, s);
+  if (e != cudaSuccess) return launch_status(e);
+  const AttnArgs a = dense_args(cfg, d->q, 1, d->kv_comp, d->E_cap, d->kv_local, d->L, d->local_base, d->q_pos,
+                                d->sink, d->out, d->lse, ws, ws_bytes);
+  return launch_status(launch_attn(a, s));
 }
 
 csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,

@@ -38,6 +38,23 @@ struct CompressArgs {
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 
+// One-stream compression without overlap (HCA at m' = 128, the CSA2 encoder at m = 2):
+// entry i = per-channel softmax over the m logits Z[m i + j] (+ bias[j]) of its own block,
+// weighted sum of C over the same tokens.
+struct Compress1Args {
+  const void* kv;         // [B, n_tok, dim]: C of tokens tok0 .. (decode: [B, m, dim], t-m+1 .. t)
+  const void* z;          // same layout: gate logits Z
+  const float* bias;      // [m, dim] or null (no positional bias)
+  void* out;              // [B, E_cap, dim] (act dtype)
+  int B, m, dim;          // dim even
+  bool act_bf16;          // stream and output dtype: bf16 (else fp32)
+  int64_t n_tok, tok0;    // uniform mode: stream row r holds token tok0 + r
+  int64_t ent_begin, n_ent;
+  const int64_t* q_pos;   // decode mode (non-null): entry (t+1)/m - 1 when (t+1) % m == 0
+  int64_t E_cap;
+};
+cudaError_t launch_compress1(const Compress1Args& a, cudaStream_t s);
+
 // ---- indexer ----------------------------------------------------------------------
 // Decode step (T = 1, tensor-core path): the indexer launch also compresses the entry the
 // new token completes (main KV by the first CTA of each sequence, indexer key by the CTA
@@ -178,12 +195,15 @@ struct AttnArgs {
   int64_t E_cap, L;
   float softmax_scale;
   int act;
+  int dense_m;            // > 0: no idx; the entries are every s < min(floor((t+1)/dense_m), E_cap)
   void* ws;
   size_t ws_bytes;
   int* err;
   int num_sms;
 };
 size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms);
+// Dense (HCA) attention: workspace for the split plan over at most E_cap + W rows a query.
+size_t attn_dense_workspace_bytes(int B, int T, int H, int d, int64_t E_cap, int W, int act, int num_sms);
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 
 // ---- shared host utilities ---------------------------------------------------------

@@ -57,6 +57,21 @@ __device__ int compact_idx(const int32_t* idx, int k, int64_t E_cap, int32_t* se
   return static_cast<int>(total);
 }
 
+// The entry part of a query's row list.  Sparse (CSA): the valid idx entries, compacted into
+// sel.  Dense (HCA, "Heavily Compressed Attention": no indexer, every entry it holds): the
+// entries s < min(floor((t+1)/m), E_cap), row j being entry j, with no list.
+template <int NT>
+__device__ int entry_rows(const AttnArgs& a, int64_t r, int64_t t, int32_t* sel, uint32_t* tmp) {
+  if (a.dense_m > 0) {
+    const int64_t nv = t >= 0 ? (t + 1) / a.dense_m : 0;
+    return static_cast<int>(nv < a.E_cap ? nv : a.E_cap);
+  }
+  return compact_idx<NT>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
+}
+__device__ __forceinline__ int64_t entry_at(const AttnArgs& a, const int32_t* sel, int j) {
+  return a.dense_m > 0 ? j : sel[j];
+}
+
 __device__ __forceinline__ void window_of(int64_t t, int W, int64_t base, int64_t L, int64_t& p_lo, int& n_win) {
   int64_t lo = t - W + 1;
   lo = lo > 0 ? lo : 0;
@@ -98,8 +113,8 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(AttnArgs a) {
     sm_run[h] = -INFINITY;
     sl_run[h] = 0.f;
   }
-  const int n_sel = compact_idx<kSimtThreads>(a.idx + r * k, k, a.E_cap, sel, tmp, a.err);
   const int64_t t = a.q_pos[r];
+  const int n_sel = entry_rows<kSimtThreads>(a, r, t, sel, tmp);
   int64_t p_lo;
   int n_win;
   window_of(t, a.W, a.local_base[b], a.L, p_lo, n_win);
@@ -115,7 +130,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(AttnArgs a) {
       float v = 0.f;
       if (j < nr) {
         const int lp = r0 + j;
-        const T* src = lp < n_sel ? kvc + static_cast<int64_t>(sel[lp]) * d
+        const T* src = lp < n_sel ? kvc + entry_at(a, sel, lp) * d
                                   : kvl + (p_lo + (lp - n_sel) - lbase) * d;
         v = load_f<T>(src + c);
       }
@@ -565,7 +580,13 @@ __device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint
                : "memory");
 }
 
-__global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a) {
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a, const TcAttnSplit sp) {
   using LY = PfLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -616,13 +637,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
   }
   pdl_wait();  // the selection and the caches come from the kernels before this one
   pdl_trigger();
-  const int n_sel = compact_idx<kPfThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
   const int64_t t = a.q_pos[r];
+  const int n_sel = entry_rows<kPfThreads>(a, r, t, sel, tmp);
   int64_t p_lo;
   int n_win;
   window_of(t, a.W, a.local_base[b], a.L, p_lo, n_win);
   const int n_rows = n_sel + n_win;
-  const int nt = (n_rows + kPR - 1) / kPR;
+  // this CTA's part of the row list (all of it unless the rows are split over CTAs)
+  const int split = blockIdx.y;
+  const int row_lo = sp.n_split > 1 ? split * sp.rows_per_split : 0;
+  const int row_hi = sp.n_split > 1 ? min(n_rows, row_lo + sp.rows_per_split) : n_rows;
+  const int nt = row_hi > row_lo ? (row_hi - row_lo + kPR - 1) / kPR : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -636,7 +661,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
     const __nv_bfloat16* kvc = static_cast<const __nv_bfloat16*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kD;
     const __nv_bfloat16* kvl = static_cast<const __nv_bfloat16*>(a.kv_local) + static_cast<int64_t>(b) * a.L * kD;
     const int64_t lbase = a.local_base[b];
-    const uint64_t pol = policy_evict_last();  // the caches are re-read by the other queries
+    // many queries re-read the caches (keep them in L2); a split query reads its rows once
+    const uint64_t pol = sp.n_split > 1 ? policy_evict_first() : policy_evict_last();
     if (nt > 0) {
       const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + r * kH * kD;
       for (int i = g; i < kH * 64; i += kGath) {
@@ -658,9 +684,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
       for (int i = g; i < kPR * 64; i += kGath) {
         const int j = i >> 6, c = i & 63;
         uint8_t* d = dst + (c >> 3) * (kPR * 128) + sw128(j, c & 7);
-        const int lp = it * kPR + j;
-        if (lp < n_rows) {
-          const __nv_bfloat16* src = lp < n_sel ? kvc + static_cast<int64_t>(sel[lp]) * kD
+        const int lp = row_lo + it * kPR + j;
+        if (lp < row_hi) {
+          const __nv_bfloat16* src = lp < n_sel ? kvc + entry_at(a, sel, lp) * kD
                                                 : kvl + (p_lo + (lp - n_sel) - lbase) * kD;
           cp_async16_hint(d, src + c * 8, pol);
         } else {
@@ -752,10 +778,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
       tc_fence_before();
       mbar_arrive(&sempty[buf]);  // S is in registers: the accumulator may take tile it + 2
       float mh = -INFINITY;
-      const int r0 = it * kPR + ch * 32;
+      const int r0 = row_lo + it * kPR + ch * 32;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        x[j] = (r0 + j < n_rows) ? x[j] * scale_log2 : -INFINITY;
+        x[j] = (r0 + j < row_hi) ? x[j] * scale_log2 : -INFINITY;
         mh = fmaxf(mh, x[j]);
       }
       if (own) s_mx[ch * kH + h] = mh;
@@ -824,6 +850,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
     if (ok && nt > 0)
       ok = named_and(1, kSoft, mbar_wait(&pempty[(nt - 1) & 1], ((nt - 1) >> 1) & 1, a.err, sAbort));
     tc_fence_after();
+    if (sp.n_split > 1) {
+      // split partial: running (max, sum) per head and the unnormalised O (fp32,
+      // [query][split][head][dim]); attn_merge_dec_kernel adds the sink and normalises
+      const int64_t ps = r * sp.n_split + split;
+      if (own && ch == 0) {
+        const bool any = ok && nt > 0;
+        sp.part_ml[ps * 2 * kH + h] = any ? m_run : -INFINITY;
+        sp.part_ml[ps * 2 * kH + kH + h] = any ? l_run : 0.f;
+      }
+      if (ok && nt > 0) {
+        float* po = sp.part_o + ps * kH * kD;
+        for (int cc = 2 * ch; cc < 2 * ch + 2; ++cc) {
+          const int dd = cc * 128 + qd * 32 + lane;
+#pragma unroll
+          for (int hc = 0; hc < 64; hc += 32) {
+            float v[32];
+            tmem_ld32(tO + lane_off + cc * 64 + hc, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) po[(hc + e) * kD + dd] = v[e];
+          }
+        }
+      }
+    } else {
     if (own && ch == 0) {
       const float sk = a.sink[h] * kLog2e;
       const float M = fmaxf(m_run, sk);
@@ -848,6 +898,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
       }
     } else {
       for (int i = tid; i < kH * kD; i += kSoft) o[i] = __float2bfloat16_rn(0.f);
+    }
     }
   }
   tc_fence_before();
@@ -1092,9 +1143,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
 
 // Fixed-order merge of the decode partials ([query][split][head][dim]) with the sink: one
 // CTA per (query, 4 heads), one thread per output dim.
+constexpr int kMaxSplitDec = 64;  // 2 * kMergeHeads * kMaxSplitDec <= kD threads load (m, l)
 __global__ void __launch_bounds__(kD) attn_merge_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
-  __shared__ float s_ml[kMaxSplit][2][kMergeHeads];  // (m, l) of every split
-  __shared__ float s_f[kMaxSplit][kMergeHeads];      // per split, per head: 2^(m_s - M) / den
+  __shared__ float s_ml[kMaxSplitDec][2][kMergeHeads];  // (m, l) of every split
+  __shared__ float s_f[kMaxSplitDec][kMergeHeads];      // per split, per head: 2^(m_s - M) / den
   pdl_wait();
   pdl_trigger();
   const int64_t r = blockIdx.x;
@@ -1178,7 +1230,40 @@ TcAttnSplit plan_split(int B, int T, int k, int W, int num_sms) {
   return s;
 }
 
+// Dense rows (HCA): few queries split their rows over CTAs of attn_pf_kernel so that the
+// grid fills the SMs once (rows_per_split a multiple of the 64-row tile, at most
+// kMaxSplitDec splits); many queries take one CTA each.
+TcAttnSplit plan_dense(int64_t rows, int64_t max_rows, int num_sms) {
+  TcAttnSplit s{};
+  s.n_split = 1;
+  s.rows_per_split = 0;
+  if (rows >= num_sms || max_rows <= 2 * kPR) return s;
+  const int64_t want = num_sms / rows;  // >= 1
+  int64_t rps = (max_rows + want - 1) / want;
+  const int64_t lo = (max_rows + kMaxSplitDec - 1) / kMaxSplitDec;
+  if (rps < lo) rps = lo;
+  if (rps < 2 * kPR) rps = 2 * kPR;
+  rps = (rps + kPR - 1) / kPR * kPR;
+  const int64_t ns = (max_rows + rps - 1) / rps;
+  if (ns > 1) {
+    s.n_split = static_cast<int>(ns);
+    s.rows_per_split = static_cast<int>(rps);
+  }
+  return s;
+}
+
+bool dense_uses_tensor_cores(int act, int H, int d) { return act == CSA_BF16 && H == kH && d == kD; }
+
 }  // namespace
+
+size_t attn_dense_workspace_bytes(int B, int T, int H, int d, int64_t E_cap, int W, int act, int num_sms) {
+  if (!dense_uses_tensor_cores(act, H, d)) return 0;
+  const int64_t rows = static_cast<int64_t>(B) * T;
+  const TcAttnSplit s = plan_dense(rows, E_cap + W, num_sms);
+  if (s.n_split == 1) return 0;
+  return align_up(static_cast<size_t>(rows * s.n_split * kH * kD) * 4, 256) +
+         align_up(static_cast<size_t>(rows * s.n_split * 2 * kH) * 4, 256);
+}
 
 size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
   if (!attn_uses_tensor_cores(act, H, d, k)) return 0;
@@ -1192,6 +1277,27 @@ size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, i
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T;
   if (rows == 0) return cudaSuccess;
+  if (a.dense_m > 0 && dense_uses_tensor_cores(a.act, a.H, a.d)) {
+    TcAttnSplit sp = plan_dense(rows, a.E_cap + a.W, a.num_sms);
+    if (sp.n_split > 1) {
+      uint8_t* ws = static_cast<uint8_t*>(a.ws);
+      sp.part_o = reinterpret_cast<float*>(ws);
+      sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));
+    }
+    static bool dattr = false;
+    if (!dattr) {
+      cudaFuncSetAttribute(attn_pf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(PfLayout::kSmem));
+      dattr = true;
+    }
+    cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows), sp.n_split), dim3(kPfThreads),
+                               PfLayout::kSmem, s, a, sp);
+    count_launches(1);
+    if (e != cudaSuccess || sp.n_split == 1) return e;
+    e = launch_pdl(attn_merge_dec_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads), dim3(kD), 0, s, a, sp);
+    count_launches(1);
+    return e;
+  }
   if (attn_uses_tensor_cores(a.act, a.H, a.d, a.k)) {
     TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
     if (sp.n_split > 1) {
@@ -1213,7 +1319,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
         pattr = true;
       }
       const cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows)), dim3(kPfThreads),
-                                       PfLayout::kSmem, s, a);
+                                       PfLayout::kSmem, s, a, sp);
       count_launches(1);
       return e;
     }

@@ -140,7 +140,137 @@ cudaError_t launch_impl(const CompressArgs& a, const QprepPart& qp, int qp_ctas,
   return e;
 }
 
+// ------------------------------------------------------------------ one stream, no overlap
+// "DeepSeek V4-Flash: The Cost of Deciding What to Read", section "Heavily Compressed
+// Attention" (the same compressor at m' = 128 with one KV stream, so no overlap), and the
+// V4.1 diagram's "Encoder groups compress pairs" (ratio 2, channel-wise softmax per pair,
+// no positional embedding).  CTA = (entry, sequence, 64 channels); thread (slice s, lane l)
+// takes channels 2l, 2l+1 of the chunk over the tokens j = s, s+8, ... of the block with a
+// running max / sum / weighted sum, four tokens' loads in flight at a time; the eight slices
+// are combined through shared memory.
+constexpr int kC1Slices = 8, kC1Chan = 64;
+
+template <typename T>
+__device__ __forceinline__ float2 load_f2(const T* p);
+template <>
+__device__ __forceinline__ float2 load_f2<float>(const float* p) { return *reinterpret_cast<const float2*>(p); }
+template <>
+__device__ __forceinline__ float2 load_f2<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compress1Args a) {
+  __shared__ float s_red[kC1Slices][3][kC1Chan];
+  pdl_wait();  // the cache row may still be read by the previous step
+  pdl_trigger();
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int c = blockIdx.z * kC1Chan + 2 * lane;
+  const bool live = c < a.dim;
+  const int m = a.m;
+  int64_t entry, r0, n_tok;
+  if (a.q_pos) {
+    const int64_t t = a.q_pos[b];
+    if ((t + 1) % m != 0) return;
+    entry = (t + 1) / m - 1;
+    r0 = 0;
+    n_tok = m;
+  } else {
+    entry = a.ent_begin + blockIdx.x;
+    r0 = static_cast<int64_t>(m) * entry - a.tok0;
+    n_tok = a.n_tok;
+  }
+  if (entry < 0 || entry >= a.E_cap) return;
+  const T* kv = static_cast<const T*>(a.kv) + (static_cast<int64_t>(b) * n_tok + r0) * a.dim + c;
+  const T* z = static_cast<const T*>(a.z) + (static_cast<int64_t>(b) * n_tok + r0) * a.dim + c;
+  float mx0 = -INFINITY, mx1 = -INFINITY, sm0 = 0.f, sm1 = 0.f, ac0 = 0.f, ac1 = 0.f;
+  if (live) {
+    for (int j0 = sl; j0 < m; j0 += 4 * kC1Slices) {
+      float2 lg[4], v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kC1Slices;
+        if (j < m) {
+          lg[u] = load_f2<T>(z + static_cast<int64_t>(j) * a.dim);
+          v[u] = load_f2<T>(kv + static_cast<int64_t>(j) * a.dim);
+          if (a.bias) {
+            const float2 bb = *reinterpret_cast<const float2*>(a.bias + static_cast<int64_t>(j) * a.dim + c);
+            lg[u].x += bb.x;
+            lg[u].y += bb.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u * kC1Slices < m) {
+          if (lg[u].x > mx0) {
+            const float f = expf(mx0 - lg[u].x);
+            sm0 *= f;
+            ac0 *= f;
+            mx0 = lg[u].x;
+          }
+          if (lg[u].y > mx1) {
+            const float f = expf(mx1 - lg[u].y);
+            sm1 *= f;
+            ac1 *= f;
+            mx1 = lg[u].y;
+          }
+          const float e0 = expf(lg[u].x - mx0), e1 = expf(lg[u].y - mx1);
+          sm0 += e0;
+          sm1 += e1;
+          ac0 = fmaf(e0, v[u].x, ac0);
+          ac1 = fmaf(e1, v[u].y, ac1);
+        }
+      }
+    }
+  }
+  s_red[sl][0][2 * lane] = mx0;
+  s_red[sl][0][2 * lane + 1] = mx1;
+  s_red[sl][1][2 * lane] = sm0;
+  s_red[sl][1][2 * lane + 1] = sm1;
+  s_red[sl][2][2 * lane] = ac0;
+  s_red[sl][2][2 * lane + 1] = ac1;
+  __syncthreads();
+  if (sl != 0 || !live) return;
+  float res[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int cc = 2 * lane + q;
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kC1Slices; ++s) M = fmaxf(M, s_red[s][0][cc]);
+    float sum = 0.f, acc = 0.f;
+#pragma unroll
+    for (int s = 0; s < kC1Slices; ++s) {
+      const float ms = s_red[s][0][cc];
+      if (ms != -INFINITY) {  // slices with no token of this block hold nothing
+        const float f = expf(ms - M);
+        sum = fmaf(s_red[s][1][cc], f, sum);
+        acc = fmaf(s_red[s][2][cc], f, acc);
+      }
+    }
+    res[q] = acc / sum;
+  }
+  const int64_t row = static_cast<int64_t>(b) * a.E_cap + entry;
+  if (a.act_bf16)
+    *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.out) + row * a.dim + c) =
+        __floats2bfloat162_rn(res[0], res[1]);
+  else
+    *reinterpret_cast<float2*>(static_cast<float*>(a.out) + row * a.dim + c) = make_float2(res[0], res[1]);
+}
+
 }  // namespace
+
+cudaError_t launch_compress1(const Compress1Args& a, cudaStream_t s) {
+  dim3 grid(a.q_pos ? 1u : static_cast<unsigned>(a.n_ent), static_cast<unsigned>(a.B),
+            static_cast<unsigned>((a.dim + kC1Chan - 1) / kC1Chan));
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+  const cudaError_t e = a.act_bf16 ? launch_pdl(compress1_kernel<__nv_bfloat16>, grid, dim3(32 * kC1Slices), 0, s, a)
+                                   : launch_pdl(compress1_kernel<float>, grid, dim3(32 * kC1Slices), 0, s, a);
+  count_launches(1);
+  return e;
+}
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   QprepPart none{};

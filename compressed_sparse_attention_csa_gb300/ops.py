@@ -135,6 +135,17 @@ def compress_kv(cfg: Config, kv: torch.Tensor, z: torch.Tensor, bias: torch.Tens
                                                   _stream()))
 
 
+def compress_kv_single(cfg: Config, kv: torch.Tensor, z: torch.Tensor, bias: Optional[torch.Tensor], tok0: int,
+                       ent_begin: int, ent_end: int, out: torch.Tensor) -> None:
+    """csa_compress_kv_single (one stream, no overlap; ratio cfg.m): kv, z [B, n_tok, dim];
+    bias [m, dim] fp32 or None; out [B, E_cap, dim] in cfg.act."""
+    lib = L.load()
+    c = cfg.c()
+    _check("csa_compress_kv_single",
+           lib.csa_compress_kv_single(ctypes.byref(c), kv.shape[-1], _p(kv), _p(z), _p(bias), kv.shape[1], tok0,
+                                      ent_begin, ent_end, _p(out), out.shape[1], _stream()))
+
+
 def indexer_scores(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.Tensor, kI: torch.Tensor,
                    scores: torch.Tensor, kscale: Optional[torch.Tensor] = None,
                    cand: Optional[torch.Tensor] = None) -> None:
@@ -231,3 +242,31 @@ def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_t
         raise CsaError("csa_workspace_size", 2)
     wp, wb = _ws_args(_decode_workspace(nbytes, q.device, cfg.B))
     _check("csa_decode_step", lib.csa_decode_step(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))
+
+
+def dense_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, kv_local: torch.Tensor, local_base: torch.Tensor,
+               q_pos: torch.Tensor, sink: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None) -> None:
+    """csa_dense_attn (HCA): every entry s < floor((q_pos+1)/cfg.m) of kv_comp [B, E_cap, d] plus
+    the window rows of kv_local [B, L, d]; q [B, T, H, d]."""
+    lib = L.load()
+    c = cfg.c()
+    B, T = q.shape[0], q.shape[1]
+    E_cap = kv_comp.shape[1]
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_DENSE_ATTN, ctypes.byref(c), B * T, E_cap), q.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_dense_attn",
+           lib.csa_dense_attn(ctypes.byref(c), _p(q), T, _p(kv_comp), E_cap, _p(kv_local), kv_local.shape[1],
+                              _p(local_base), _p(q_pos), _p(sink), _p(out), _p(lse), wp, wb, _stream()))
+
+
+def hca_decode_step(cfg: Config, *, q_pos, q, sink, kv_comp, kv_tail, z_tail, bias, kv_local, local_base, out,
+                    lse=None) -> None:
+    """csa_hca_decode_step: one token per sequence (T = 1); kv_tail / z_tail [B, m, d] hold
+    tokens t-m+1 .. t; kv_comp is updated in place when the token completes a block."""
+    lib = L.load()
+    c = cfg.c()
+    a = L.csa_hca_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(sink), _p(kv_comp), _p(kv_tail), _p(z_tail),
+                              _p(bias), _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse))
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_HCA_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1]), q.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_hca_decode_step", lib.csa_hca_decode_step(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))

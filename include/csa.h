@@ -63,14 +63,16 @@ typedef struct {
 /* Operation ids for csa_workspace_size. */
 typedef enum {
   CSA_OP_COMPRESS = 0, CSA_OP_INDEXER = 1, CSA_OP_TOPK = 2, CSA_OP_ATTN = 3,
-  CSA_OP_DECODE = 4, CSA_OP_POOL = 5, CSA_OP_INDEXER_TOPK = 6
+  CSA_OP_DECODE = 4, CSA_OP_POOL = 5, CSA_OP_INDEXER_TOPK = 6, CSA_OP_DENSE_ATTN = 7,
+  CSA_OP_HCA_DECODE = 8
 } csa_op;
 
 /*
  * csa_workspace_size — bytes of scratch the operation needs.
  *   rows   : query rows (B*T) of the call;
  *   n_cols : the longest score row (E_cap, or n_cand) for TOPK / DECODE / INDEXER_TOPK;
- *            T (queries per sequence) for ATTN and INDEXER.  (POOL: see
+ *            T (queries per sequence) for ATTN and INDEXER; E_cap for DENSE_ATTN and
+ *            HCA_DECODE (rows = B*T, and B for HCA_DECODE).  (POOL: see
  *            csa_block_pool_workspace_size.)
  * Returns 0 for operations that need none, (size_t)-1 for an invalid configuration.
  */
@@ -97,6 +99,25 @@ csa_status csa_compress_kv(const csa_config *cfg, int32_t dim, const void *kv, c
                            const float *bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
                            int64_t ent_end, void *out, csa_dtype out_dtype, float *out_scale,
                            int64_t E_cap, csa_stream_t stream);
+
+/*
+ * csa_compress_kv_single — one-stream compression without overlap: HCA ("Heavily
+ * Compressed Attention": the compressor at m' = 128 with a single KV stream) and the CSA2
+ * encoder (V4.1 diagram, "Encoder groups compress pairs": m = 2, channel-wise softmax per
+ * pair, no positional embedding).  With m = cfg->m, entry i of every channel c is
+ *   sum_j softmax_j(Z[m*i + j, c] + bias[j, c]) * C[m*i + j, c],   j = 0 .. m-1
+ * (bias NULL: no positional term).  Only cfg->B, cfg->m and cfg->act are read.
+ *
+ *   dim        : channels, even, 2 .. 4096
+ *   kv, z      : [B, n_tok, dim] (cfg->act) — C and Z of tokens tok0 .. tok0+n_tok-1
+ *   bias       : [m, dim] fp32 or NULL
+ *   ent_begin, ent_end : entries to produce; needs tok0 <= m*ent_begin and
+ *                m*ent_end <= tok0 + n_tok (else CSA_ERR_SHAPE)
+ *   out        : [B, E_cap, dim] (cfg->act); rows outside [ent_begin, ent_end) untouched
+ */
+csa_status csa_compress_kv_single(const csa_config *cfg, int32_t dim, const void *kv, const void *z,
+                                  const float *bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
+                                  int64_t ent_end, void *out, int64_t E_cap, csa_stream_t stream);
 
 /*
  * csa_indexer_scores — lightning-indexer scores ("The Lightning Indexer"):
@@ -210,6 +231,50 @@ csa_status csa_sparse_attn(const csa_config *cfg, const void *q, int32_t T, cons
                            int64_t E_cap, const int32_t *idx, const void *kv_local, int64_t L,
                            const int64_t *local_base, const int64_t *q_pos, const float *sink,
                            void *out, float *lse, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * csa_dense_attn — HCA core attention ("Heavily Compressed Attention": no indexer and no
+ * top-k, the layer attends to every entry it holds; window and per-head sink as in
+ * csa_sparse_attn).  For query row r = b*T + t at position p = q_pos[r] the rows are
+ *   kv_comp[b, s] for s < min(floor((p+1)/cfg->m), E_cap), then the window rows of
+ *   csa_sparse_attn; out and lse as there.
+ * Only cfg->B, H, d, m, W, act and softmax_scale are read.
+ *   ws : csa_workspace_size(CSA_OP_DENSE_ATTN, cfg, B*T, E_cap) bytes (0 when many queries
+ *        share the launch; few queries split their rows over CTAs and merge partials in ws)
+ * bf16 with d == 512, H == 64 runs on the tcgen05 tensor cores; other shapes with d <= 128,
+ * H <= 64 run a CUDA-core path.
+ */
+csa_status csa_dense_attn(const csa_config *cfg, const void *q, int32_t T, const void *kv_comp,
+                          int64_t E_cap, const void *kv_local, int64_t L, const int64_t *local_base,
+                          const int64_t *q_pos, const float *sink, void *out, float *lse, void *ws,
+                          size_t ws_bytes, csa_stream_t stream);
+
+/* All inputs of one HCA decode token per sequence (T = 1). */
+typedef struct {
+  int64_t E_cap;             /* rows of kv_comp per sequence                                   */
+  const int64_t *q_pos;      /* [B] position t of the new token                                */
+  const void *q;             /* [B, H, d]                                                      */
+  const float *sink;         /* [H]                                                            */
+  void *kv_comp;             /* [B, E_cap, d]  row (t+1)/m - 1 written when (t+1) % m == 0     */
+  const void *kv_tail;       /* [B, m, d]  C of tokens t-m+1 .. t                              */
+  const void *z_tail;        /* [B, m, d]  Z of the same tokens                                */
+  const float *bias;         /* [m, d] fp32 or NULL                                            */
+  const void *kv_local;      /* [B, L, d] uncompressed window rows                             */
+  int64_t L;
+  const int64_t *local_base; /* [B] position of kv_local[b, 0]                                 */
+  void *out;                 /* [B, H, d]                                                      */
+  float *lse;                /* [B, H] or NULL                                                 */
+} csa_hca_decode_args;
+
+/*
+ * csa_hca_decode_step — one HCA decode token per sequence: compress the block the token
+ * completes (only when (t+1) % m == 0; m = cfg->m, e.g. 128) with the one-stream compressor,
+ * then attend densely over every visible entry plus the window, with the sink.  Same
+ * semantics as csa_compress_kv_single followed by csa_dense_attn with T = 1.
+ *   ws : csa_workspace_size(CSA_OP_HCA_DECODE, cfg, B, E_cap) bytes
+ */
+csa_status csa_hca_decode_step(const csa_config *cfg, const csa_hca_decode_args *args, void *ws,
+                               size_t ws_bytes, csa_stream_t stream);
 
 /* All inputs of one decode token per sequence (T = 1). */
 typedef struct {
