@@ -62,8 +62,9 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["step", "indexer"], default=None,
-                    help="run only this stage on the workload, eagerly (for profiler captures)")
+    ap.add_argument("--only", choices=["step", "stage", "indexer"], default=None,
+                    help="run only the step or the workload's dominant stage (\"indexer\": the stage of the CSA "
+                         "workloads), eagerly (for profiler captures)")
     return ap.parse_args()
 
 
@@ -79,7 +80,7 @@ def peaks():
 
 
 _INDEXER_STAGE = (("indexer_qprep_kernel", "indexer_tc_kernel"), ("k_indexer.cu", "csa_ptx.cuh", "csa_internal.h"))
-_DENSE_STAGE = (("attn_pf_kernel", "attn_merge_dec_kernel"), ("k_attn.cu", "csa_ptx.cuh", "csa_internal.h"))
+_DENSE_STAGE = (("attn_hca_dec_kernel", "attn_merge_wide_kernel"), ("k_attn.cu", "csa_ptx.cuh", "csa_internal.h"))
 # config -> (summary file, kernels of the stage, sources the summary's counters were taken with)
 STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
                   2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE,
@@ -478,7 +479,8 @@ class HcaDecode:
                          local_base=inp["local_base"], out=self.out, lse=self.lse)
         from compressed_sparse_attention_csa_gb300.accounting import hca_decode_work
         work = hca_decode_work(cfg)
-        self.stage_label = "dense attention: attn_pf_kernel (rows split over CTAs) + attn_merge_dec_kernel"
+        self.stage_label = ("dense attention: attn_hca_dec_kernel (rows split over CTAs, two TMA passes) + "
+                            "attn_merge_wide_kernel")
         self.stage_bound = "hbm"
         self.stage_amount = work["attention_bytes"]
         self.step_bytes = work["bytes"]

@@ -228,6 +228,25 @@ __device__ __forceinline__ float2 warp_reduce64(float (&v)[64]) {
   }
   return make_float2(v[0], v[1]);
 }
+// The same over 32 values; lane l ends with the result for value l.
+template <bool MAX>
+__device__ __forceinline__ float warp_reduce32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int half = 16 >> step;
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float lo = v[i], hi = v[i + half];
+      const float send = upper ? lo : hi;
+      const float keep = upper ? hi : lo;
+      const float got = __shfl_xor_sync(0xffffffffu, send, half);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a, const TcAttnSplit sp) {
   extern __shared__ uint8_t smem_raw[];
@@ -578,12 +597,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 __device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t pol) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "l"(pol)
                : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a, const TcAttnSplit sp) {
@@ -1141,6 +1154,287 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
   }
 }
 
+// ------------------------------------------------------------------ dense rows, few queries
+// HCA decode ("Heavily Compressed Attention": every entry the layer holds, plus the window,
+// with the sink).  Grid (split, query): a query's entries are cut into splits of up to
+// kHdTiles x 128 rows and its window rows form one more split.  The rows of a split are
+// contiguous, so a CTA streams them with TMA: a 128-row tile is 8 regions (64 dims x 128
+// rows, 128B-swizzled), region c always lands in slot c of an 8-slot ring, and a slot is
+// refilled as soon as the MMAs reading it complete.  Two passes over the tiles:
+//  pass 1: S^T = R Q^T per tile (M = 128 rows, N = 64 heads) into TMEM, 64 columns a tile;
+//  softmax: the exact per-head maximum over the split, then P^T = 2^(S - max) in bf16, one
+//          128-row tile at a time in two buffers, and the per-head sums;
+//  pass 2: the same tiles again (L2-resident by then): O^T += R^T P^T (M = 128 dims a chunk,
+//          N = 64 heads, K = 128 rows); rows past the split's end are zeroed in the slot first
+//          (they may hold anything, and 0 x NaN is NaN).
+// Warps 0-7: softmax and epilogue (warp w: TMEM lanes 32 (w & 3) .. +31, heads 32 (w >> 2) ..
+// +31; a lane is a row, then a dim); warp 8: TMA producer and TMEM owner; warp 9: MMA issuer.
+// The partials (max, sum, unnormalised O) are merged with the sink by attn_merge_wide_kernel.
+constexpr int kHdTiles = 4;
+constexpr int kHdThreads = 320;
+struct HdLayout {
+  static constexpr uint32_t kQ = 0;                        // 8 regions x (64 heads x 128 B)
+  static constexpr uint32_t kSlot = kRows * 128;           // one region of a tile: 16 KB
+  static constexpr uint32_t kRing = kQ + kH * kD * 2;      // 8 slots
+  static constexpr uint32_t kP = kRing + 8 * kSlot;        // [2] P^T tiles: 128 rows x 128 B
+  static constexpr uint32_t kMisc = kP + 2 * kRows * 128;
+  // s_red [4][64], s_max [64], s_sum [64]; 24 barriers; TMEM slot and abort flag
+  static constexpr uint32_t kMiscBytes = 6 * kH * 4 + 24 * 8 + 16;
+  static constexpr size_t kSmem = 1024 + kMisc + kMiscBytes;
+};
+static_assert(HdLayout::kSmem <= 232448, "shared memory of one CTA");
+
+struct HdPlan {
+  int n_es;      // entry splits of a query (the window split, if any, comes after them)
+  int rps;       // entry rows a split: a multiple of 128, at most kHdTiles * 128
+  int n_split;   // n_es + (W > 0)
+  float* part_o;
+  float* part_ml;
+};
+
+__global__ void __launch_bounds__(kHdThreads, 1)
+    attn_hca_dec_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap lmap,
+                        const __grid_constant__ CUtensorMap qmap, const AttnArgs a, const HdPlan hp) {
+  using LY = HdLayout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + LY::kQ;
+  uint8_t* sRing = smem + LY::kRing;
+  uint8_t* sP = smem + LY::kP;
+  float* s_red = reinterpret_cast<float*>(smem + LY::kMisc);  // [4][64]
+  float* s_max = s_red + 4 * kH;                               // [64]
+  float* s_sum = s_max + kH;                                   // [64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_sum + kH);
+  uint64_t* full = bars;          // [8] slot landed (producer, tx bytes)
+  uint64_t* empty = bars + 8;     // [8] slot read by its MMAs (commit)
+  uint64_t* qfull = bars + 16;    // Q landed
+  uint64_t* sdone = bars + 17;    // every S^T tile of the split committed
+  uint64_t* pfull = bars + 18;    // [2] P^T tile written (256 softmax threads)
+  uint64_t* pempty = bars + 20;   // [2] P^T tile read (commit)
+  uint64_t* odone = bars + 22;    // every O^T product committed
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 24);
+  volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x;
+  const int64_t r = blockIdx.y;
+  const int b = static_cast<int>(r / a.T);
+  const float scale_log2 = a.softmax_scale * kLog2e;
+
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(qfull, 1);
+    mbar_init(sdone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], 256);
+      mbar_init(&pempty[i], 1);
+    }
+    mbar_init(odone, 1);
+    fence_mbar_init();
+    *sAbort = 0;
+  }
+  if (warp == 8) {
+    tmem_alloc(sTmem, 512);
+    tmem_relinquish();
+  }
+  pdl_wait();  // the entry the step compresses comes from the kernel before this one
+  pdl_trigger();
+  const int64_t t = a.q_pos[r];
+  int n;          // rows of this split
+  int64_t row0;   // their first row in the tensor map
+  const CUtensorMap* map;
+  if (split < hp.n_es) {
+    int64_t nv = t >= 0 ? (t + 1) / a.dense_m : 0;
+    nv = nv < a.E_cap ? nv : a.E_cap;
+    const int64_t lo = static_cast<int64_t>(split) * hp.rps;
+    const int64_t cnt = nv - lo;
+    n = cnt <= 0 ? 0 : (cnt < hp.rps ? static_cast<int>(cnt) : hp.rps);
+    row0 = static_cast<int64_t>(b) * a.E_cap + lo;
+    map = &kvmap;
+  } else {
+    const int64_t lbase = a.local_base[b];
+    int64_t p_lo;
+    window_of(t, a.W, lbase, a.L, p_lo, n);
+    row0 = static_cast<int64_t>(b) * a.L + (p_lo - lbase);
+    map = &lmap;
+  }
+  const int nt = (n + kRows - 1) / kRows;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sTmem;
+  const uint32_t tS = tmem, tO = tmem + 256;  // S^T of tile i at columns 64 i; O^T chunk cc at 256 + 64 cc
+
+  if (warp == 8) {
+    // ---- producer: Q, then the regions of pass 1 and pass 2 in the order the MMAs read them
+    if (lane == 0 && nt > 0) {
+      mbar_arrive_expect_tx(qfull, kH * kD * 2);
+      for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * (kH * 128), &qmap, qfull, 64 * c, static_cast<int>(r * kH));
+      const uint64_t pol = policy_evict_first();
+      bool ok = true;
+      // use u of a slot: pass-1 tile u (u < nt), then pass-2 tile 2 nt - 2 - u (the last
+      // tile stays in the ring from pass 1 and is read first in pass 2)
+      for (int j = 0; ok && j < 8 * (2 * nt - 1); ++j) {
+        const int slot = j & 7, use = j >> 3, tile = use < nt ? use : 2 * nt - 2 - use;
+        if (use > 0) ok = mbar_wait(&empty[slot], (use - 1) & 1, a.err, sAbort);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&full[slot], LY::kSlot);
+        const int y = static_cast<int>(row0 + static_cast<int64_t>(tile) * kRows);
+        if (use < nt)
+          tma_load_2d(sRing + slot * LY::kSlot, map, &full[slot], 64 * slot, y);
+        else
+          tma_load_2d_hint(sRing + slot * LY::kSlot, map, &full[slot], 64 * slot, y, pol);
+      }
+    }
+  } else if (warp == 9) {
+    // ---- MMA issuer (lane 0 issues; the whole warp zeroes the tail rows of pass 2)
+    if (nt > 0) {
+      bool ok = __all_sync(0xffffffffu, mbar_wait(qfull, 0, a.err, sAbort));
+      const uint32_t ring = smem_u32(sRing), qb = smem_u32(sQ), pb = smem_u32(sP);
+      const uint32_t idesc_s = idesc_bf16(kRows, kH, false, false);
+      const uint32_t idesc_o = idesc_bf16(kRows, kH, true, true);
+      for (int i = 0; ok && i < nt; ++i) {
+        for (int c = 0; c < 8; ++c) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&full[c], i & 1, a.err, sAbort));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16(tS + 64 * i, smem_desc(ring + c * LY::kSlot + ks * 32, 16, 1024),
+                       smem_desc(qb + c * (kH * 128) + ks * 32, 16, 1024), idesc_s, (c | ks) > 0 ? 1u : 0u);
+            if (i + 1 < nt) mma_commit(&empty[c]);  // the last tile is read again by pass 2
+          }
+          __syncwarp();
+        }
+      }
+      if (ok && lane == 0) mma_commit(sdone);
+      // pass 2, tiles nt-1 .. 0: the k-th is in P^T buffer k & 1 and (k > 0) in use nt-1+k
+      for (int k = 0; ok && k < nt; ++k) {
+        const int i = nt - 1 - k, use = nt - 1 + k;
+        ok = __all_sync(0xffffffffu, mbar_wait(&pfull[k & 1], (k >> 1) & 1, a.err, sAbort));
+        const int vr = n - i * kRows;  // valid rows of this tile (> 0)
+        for (int cc = 0; ok && cc < 4; ++cc) {
+          if (k > 0)
+            ok = __all_sync(0xffffffffu, mbar_wait(&full[2 * cc], use & 1, a.err, sAbort) &&
+                                             mbar_wait(&full[2 * cc + 1], use & 1, a.err, sAbort));
+          if (!ok) break;
+          if (vr < kRows) {  // zero rows vr..127 of both regions (whole 128-byte rows); the S
+                             // products that read them completed before the softmax began
+            for (int q = lane; q < 2 * (kRows - vr) * 8; q += 32) {
+              const int reg = q / ((kRows - vr) * 8), rem = q % ((kRows - vr) * 8);
+              *reinterpret_cast<uint4*>(sRing + (2 * cc + reg) * LY::kSlot + (vr + rem / 8) * 128 + (rem % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int ks = 0; ks < kRows / 16; ++ks)
+              mma_bf16(tO + 64 * cc, smem_desc(ring + (2 * cc) * LY::kSlot + ks * 2048, LY::kSlot, 1024),
+                       smem_desc(pb + (k & 1) * (kRows * 128) + ks * 2048, 8192, 1024), idesc_o,
+                       (k > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&empty[2 * cc]);
+            mma_commit(&empty[2 * cc + 1]);
+          }
+          __syncwarp();
+        }
+        if (ok && lane == 0) mma_commit(&pempty[k & 1]);
+        __syncwarp();
+      }
+      if (ok && lane == 0) mma_commit(odone);
+    }
+  } else {
+    // ---- softmax and epilogue: warps 0-7, thread = TMEM lane 32 (w & 3) + l, heads hb .. hb+31
+    const int qd = warp & 3, hb = 32 * (warp >> 2);
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const int row = qd * 32 + lane;
+    float* ml = hp.part_ml + (r * hp.n_split + split) * 2 * kH;
+    if (nt > 0) {
+      bool ok = named_and(1, 256, mbar_wait(sdone, 0, a.err, sAbort));
+      tc_fence_after();
+      float mx = -INFINITY;  // of head hb + lane, over the rows this warp's lanes hold
+      for (int i = 0; ok && i < nt; ++i) {
+        float x[32];
+        tmem_ld32(tS + lane_off + 64 * i + hb, x);
+        tmem_wait_ld(x);
+        const bool valid = i * kRows + row < n;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = valid ? x[e] * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, warp_reduce32<true>(x));
+      }
+      s_red[qd * kH + hb + lane] = mx;
+      named_sync(1, 256);
+      if (tid < kH)
+        s_max[tid] = fmaxf(fmaxf(s_red[tid], s_red[kH + tid]), fmaxf(s_red[2 * kH + tid], s_red[3 * kH + tid]));
+      named_sync(1, 256);
+      float mh[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) mh[e] = s_max[hb + e];
+      float lsum = 0.f;  // of head hb + lane
+      for (int k = 0; ok && k < nt; ++k) {  // tiles in the order pass 2 reads them
+        const int i = nt - 1 - k, buf = k & 1;
+        if (k >= 2) ok = named_and(1, 256, mbar_wait(&pempty[buf], ((k >> 1) - 1) & 1, a.err, sAbort));
+        if (!ok) break;
+        float x[32];
+        tmem_ld32(tS + lane_off + 64 * i + hb, x);
+        tmem_wait_ld(x);
+        const bool valid = i * kRows + row < n;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = valid ? ex2_approx(fmaf(x[e], scale_log2, -mh[e])) : 0.f;
+        uint8_t* prow = sP + buf * (kRows * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 pk;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 two = __floats2bfloat162_rn(x[c * 8 + 2 * e], x[c * 8 + 2 * e + 1]);
+            w[e] = *reinterpret_cast<uint32_t*>(&two);
+          }
+          *reinterpret_cast<uint4*>(prow + sw128(row, (hb >> 3) + c)) = pk;
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(&pfull[buf]);
+        lsum += warp_reduce32<false>(x);
+      }
+      s_red[qd * kH + hb + lane] = lsum;
+      named_sync(1, 256);
+      if (tid < kH) {
+        ml[tid] = ok ? s_max[tid] : -INFINITY;
+        ml[kH + tid] = ok ? (s_red[tid] + s_red[kH + tid]) + (s_red[2 * kH + tid] + s_red[3 * kH + tid]) : 0.f;
+      }
+      ok = named_and(1, 256, ok && mbar_wait(odone, 0, a.err, sAbort));
+      tc_fence_after();
+      if (ok) {
+        float* po = hp.part_o + (r * hp.n_split + split) * kH * kD;
+        for (int cc = 0; cc < 4; ++cc) {
+          float v[32];
+          tmem_ld32(tO + lane_off + 64 * cc + hb, v);
+          tmem_wait_ld(v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) po[(hb + e) * kD + cc * 128 + row] = v[e];
+        }
+      }
+    } else if (tid < kH) {
+      ml[tid] = -INFINITY;
+      ml[kH + tid] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // Fixed-order merge of the decode partials ([query][split][head][dim]) with the sink: one
 // CTA per (query, 4 heads), one thread per output dim.
 constexpr int kMaxSplitDec = 64;  // 2 * kMergeHeads * kMaxSplitDec <= kD threads load (m, l)
@@ -1208,6 +1502,79 @@ __global__ void __launch_bounds__(kD) attn_merge_dec_kernel(const AttnArgs a, co
   for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j]);
 }
 
+// Merge of many split partials ([query][split][head][dim]) with the sink: one CTA per
+// (query, head), thread t owns dims 4t .. 4t+3.  Thread x < n_split reads split x's (m, l);
+// block reductions give M = max(m_x, sink) and den = sum_x l_x 2^(m_x - M) + 2^(sink - M);
+// the partials are then read 8 splits at a time (one float4 each, every load of a batch
+// issued before the first use) and summed in split order.
+constexpr int kMwThreads = 128;
+__global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  __shared__ float s_f[kMaxSplitDec];
+  __shared__ float s_red[kMwThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t r = blockIdx.x;
+  const int h = blockIdx.y;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int ns = sp.n_split;
+  const float* po = sp.part_o + (r * ns * kH + h) * kD + 4 * t;
+  float4 v[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (u < ns) v[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(u) * kH * kD));
+  float m = -INFINITY, l = 0.f;
+  if (t < ns) {
+    m = __ldcg(sp.part_ml + (r * ns + t) * 2 * kH + h);
+    l = __ldcg(sp.part_ml + (r * ns + t) * 2 * kH + kH + h);
+  }
+  const float sk = a.sink[h] * kLog2e;
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = sk;
+#pragma unroll
+  for (int w = 0; w < kMwThreads / 32; ++w) M = fmaxf(M, s_red[w]);
+  const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+  float part = l * f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  __syncthreads();  // every thread has read s_red
+  if (lane == 0) s_red[warp] = part;
+  if (t < ns) s_f[t] = f;
+  __syncthreads();
+  float den = exp2f(sk - M);
+#pragma unroll
+  for (int w = 0; w < kMwThreads / 32; ++w) den += s_red[w];
+  if (t == 0 && a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int x0 = 0; x0 < ns; x0 += 8) {
+    if (x0 > 0) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (x0 + u < ns) v[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(x0 + u) * kH * kD));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float fx = x0 + u < ns ? s_f[x0 + u] : 0.f;
+      if (fx != 0.f) {  // splits without rows wrote no partial
+        acc.x = fmaf(v[u].x, fx, acc.x);
+        acc.y = fmaf(v[u].y, fx, acc.y);
+        acc.z = fmaf(v[u].z, fx, acc.z);
+        acc.w = fmaf(v[u].w, fx, acc.w);
+      }
+    }
+  }
+  const float inv = 1.f / den;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (r * kH + h) * kD + 4 * t) = pk;
+}
+
 bool attn_uses_tensor_cores(int act, int H, int d, int k) {
   return act == CSA_BF16 && H == kH && d == kD && k <= kMaxK;
 }
@@ -1254,15 +1621,39 @@ TcAttnSplit plan_dense(int64_t rows, int64_t max_rows, int num_sms) {
 
 bool dense_uses_tensor_cores(int act, int H, int d) { return act == CSA_BF16 && H == kH && d == kD; }
 
+// attn_hca_dec_kernel's plan for few queries: about num_sms / rows CTAs a query (one of them
+// for the window), entry splits of a multiple of 128 rows, at most kHdTiles tiles and
+// kMaxSplitDec splits; n_split = 0 when the entries do not fit that.
+HdPlan plan_hca_dec(int64_t rows, int64_t E_cap, int W, int num_sms) {
+  HdPlan p{};
+  if (rows >= num_sms) return p;
+  const int win = W > 0 ? 1 : 0;
+  const int64_t want = std::max<int64_t>(1, num_sms / rows - win);
+  int64_t rps = (E_cap + want - 1) / want;
+  rps = std::max<int64_t>(rps, (E_cap + (kMaxSplitDec - win) - 1) / (kMaxSplitDec - win));
+  rps = std::max<int64_t>((rps + kRows - 1) / kRows * kRows, kRows);
+  if (rps > kHdTiles * kRows) return p;
+  p.rps = static_cast<int>(rps);
+  p.n_es = static_cast<int>((E_cap + rps - 1) / rps);
+  p.n_split = p.n_es + win;
+  return p;
+}
+
+size_t dense_partials_bytes(int64_t rows, int n_split) {
+  return align_up(static_cast<size_t>(rows * n_split * kH * kD) * 4, 256) +
+         align_up(static_cast<size_t>(rows * n_split * 2 * kH) * 4, 256);
+}
+
 }  // namespace
 
 size_t attn_dense_workspace_bytes(int B, int T, int H, int d, int64_t E_cap, int W, int act, int num_sms) {
   if (!dense_uses_tensor_cores(act, H, d)) return 0;
   const int64_t rows = static_cast<int64_t>(B) * T;
+  const HdPlan hp = plan_hca_dec(rows, E_cap, W, num_sms);
+  if (hp.n_split > 0) return dense_partials_bytes(rows, hp.n_split);
   const TcAttnSplit s = plan_dense(rows, E_cap + W, num_sms);
   if (s.n_split == 1) return 0;
-  return align_up(static_cast<size_t>(rows * s.n_split * kH * kD) * 4, 256) +
-         align_up(static_cast<size_t>(rows * s.n_split * 2 * kH) * 4, 256);
+  return dense_partials_bytes(rows, s.n_split);
 }
 
 size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
@@ -1278,6 +1669,40 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T;
   if (rows == 0) return cudaSuccess;
   if (a.dense_m > 0 && dense_uses_tensor_cores(a.act, a.H, a.d)) {
+    HdPlan hp = plan_hca_dec(rows, a.E_cap, a.W, a.num_sms);
+    if (hp.n_split > 0) {
+      uint8_t* ws = static_cast<uint8_t*>(a.ws);
+      hp.part_o = reinterpret_cast<float*>(ws);
+      hp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * hp.n_split * kH * kD) * 4, 256));
+      CUtensorMap kvmap, lmap, qmap;
+      const uint64_t kv_rows = std::max<int64_t>(1, static_cast<int64_t>(a.B) * a.E_cap);
+      const uint64_t l_rows = std::max<int64_t>(1, static_cast<int64_t>(a.B) * a.L);
+      if (!encode_tmap_2d(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a.kv_comp), kD, kv_rows,
+                          kD * 2, 64, kRows) ||
+          !encode_tmap_2d(&lmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a.kv_local), kD, l_rows, kD * 2,
+                          64, kRows) ||
+          !encode_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a.q), kD,
+                          static_cast<uint64_t>(rows) * kH, kD * 2, 64, kH))
+        return cudaErrorInvalidValue;
+      static bool hattr = false;
+      if (!hattr) {
+        cudaFuncSetAttribute(attn_hca_dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(HdLayout::kSmem));
+        hattr = true;
+      }
+      cudaError_t e = launch_pdl(attn_hca_dec_kernel, dim3(hp.n_split, static_cast<unsigned>(rows)),
+                                 dim3(kHdThreads), HdLayout::kSmem, s, kvmap, lmap, qmap, a, hp);
+      count_launches(1);
+      if (e != cudaSuccess) return e;
+      TcAttnSplit sp{};
+      sp.n_split = hp.n_split;
+      sp.rows_per_split = hp.rps;
+      sp.part_o = hp.part_o;
+      sp.part_ml = hp.part_ml;
+      e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
+      count_launches(1);
+      return e;
+    }
     TcAttnSplit sp = plan_dense(rows, a.E_cap + a.W, a.num_sms);
     if (sp.n_split > 1) {
       uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -1294,7 +1719,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
                                PfLayout::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess || sp.n_split == 1) return e;
-    e = launch_pdl(attn_merge_dec_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads), dim3(kD), 0, s, a, sp);
+    e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
     count_launches(1);
     return e;
   }

@@ -145,10 +145,13 @@ cudaError_t launch_impl(const CompressArgs& a, const QprepPart& qp, int qp_ctas,
 // Attention" (the same compressor at m' = 128 with one KV stream, so no overlap), and the
 // V4.1 diagram's "Encoder groups compress pairs" (ratio 2, channel-wise softmax per pair,
 // no positional embedding).  CTA = (entry, sequence, 64 channels); thread (slice s, lane l)
-// takes channels 2l, 2l+1 of the chunk over the tokens j = s, s+8, ... of the block with a
-// running max / sum / weighted sum, four tokens' loads in flight at a time; the eight slices
-// are combined through shared memory.
-constexpr int kC1Slices = 8, kC1Chan = 64;
+// takes channels 2l, 2l+1 of the chunk over the tokens j = s, s+16, ... of the block: the loads
+// of a batch of up to 8 tokens are issued before the first use (a whole m' = 128 block in
+// one round trip), the batch maximum is taken first and the weights 2^((z - max) log2 e) then
+// computed independently (the running sums are rescaled once a batch); the sixteen slices are
+// combined through shared memory.  Decode mode issues its loads before it reads the position.
+constexpr int kC1Slices = 16, kC1Chan = 64, kC1Batch = 8;  // 8 x 16 = 128 tokens' loads in one batch
+constexpr float kC1Log2e = 1.4426950408889634f;
 
 template <typename T>
 __device__ __forceinline__ float2 load_f2(const T* p);
@@ -169,27 +172,25 @@ __global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compres
   const int c = blockIdx.z * kC1Chan + 2 * lane;
   const bool live = c < a.dim;
   const int m = a.m;
-  int64_t entry, r0, n_tok;
+  // Stream rows of the block: decode mode holds tokens t-m+1 .. t in rows 0 .. m-1, so its
+  // loads are issued before q_pos is read; otherwise entry ent_begin + blockIdx.x.
+  int64_t entry = a.ent_begin + blockIdx.x, r0, n_tok;
   if (a.q_pos) {
-    const int64_t t = a.q_pos[b];
-    if ((t + 1) % m != 0) return;
-    entry = (t + 1) / m - 1;
     r0 = 0;
     n_tok = m;
   } else {
-    entry = a.ent_begin + blockIdx.x;
     r0 = static_cast<int64_t>(m) * entry - a.tok0;
     n_tok = a.n_tok;
   }
-  if (entry < 0 || entry >= a.E_cap) return;
   const T* kv = static_cast<const T*>(a.kv) + (static_cast<int64_t>(b) * n_tok + r0) * a.dim + c;
   const T* z = static_cast<const T*>(a.z) + (static_cast<int64_t>(b) * n_tok + r0) * a.dim + c;
   float mx0 = -INFINITY, mx1 = -INFINITY, sm0 = 0.f, sm1 = 0.f, ac0 = 0.f, ac1 = 0.f;
+  bool first = true;
   if (live) {
-    for (int j0 = sl; j0 < m; j0 += 4 * kC1Slices) {
-      float2 lg[4], v[4];
+    for (int j0 = sl; j0 < m; j0 += kC1Batch * kC1Slices) {
+      float2 lg[kC1Batch], v[kC1Batch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kC1Batch; ++u) {
         const int j = j0 + u * kC1Slices;
         if (j < m) {
           lg[u] = load_f2<T>(z + static_cast<int64_t>(j) * a.dim);
@@ -199,32 +200,48 @@ __global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compres
             lg[u].x += bb.x;
             lg[u].y += bb.y;
           }
+        } else {
+          lg[u] = make_float2(-INFINITY, -INFINITY);
+          v[u] = make_float2(0.f, 0.f);
         }
       }
+      if (first && a.q_pos) {  // decode: produce the entry only if the token completes it
+        const int64_t t = a.q_pos[b];
+        if ((t + 1) % m != 0) return;
+        entry = (t + 1) / m - 1;
+      }
+      first = false;
+      // the batch's maximum first, then its weights (independent of one another)
+      float b0 = mx0, b1 = mx1;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (j0 + u * kC1Slices < m) {
-          if (lg[u].x > mx0) {
-            const float f = expf(mx0 - lg[u].x);
-            sm0 *= f;
-            ac0 *= f;
-            mx0 = lg[u].x;
-          }
-          if (lg[u].y > mx1) {
-            const float f = expf(mx1 - lg[u].y);
-            sm1 *= f;
-            ac1 *= f;
-            mx1 = lg[u].y;
-          }
-          const float e0 = expf(lg[u].x - mx0), e1 = expf(lg[u].y - mx1);
-          sm0 += e0;
-          sm1 += e1;
-          ac0 = fmaf(e0, v[u].x, ac0);
-          ac1 = fmaf(e1, v[u].y, ac1);
-        }
+      for (int u = 0; u < kC1Batch; ++u) {
+        b0 = fmaxf(b0, lg[u].x);
+        b1 = fmaxf(b1, lg[u].y);
+      }
+      const float q0 = mx0 == -INFINITY ? 0.f : exp2f((mx0 - b0) * kC1Log2e);
+      const float q1 = mx1 == -INFINITY ? 0.f : exp2f((mx1 - b1) * kC1Log2e);
+      sm0 *= q0;
+      ac0 *= q0;
+      sm1 *= q1;
+      ac1 *= q1;
+      mx0 = b0;
+      mx1 = b1;
+#pragma unroll
+      for (int u = 0; u < kC1Batch; ++u) {
+        const float e0 = exp2f((lg[u].x - b0) * kC1Log2e), e1 = exp2f((lg[u].y - b1) * kC1Log2e);
+        sm0 += e0;
+        sm1 += e1;
+        ac0 = fmaf(e0, v[u].x, ac0);
+        ac1 = fmaf(e1, v[u].y, ac1);
       }
     }
   }
+  if (a.q_pos && (!live || sl >= m)) {  // threads that loaded nothing still take the decision
+    const int64_t t = a.q_pos[b];
+    if ((t + 1) % m != 0) return;
+    entry = (t + 1) / m - 1;
+  }
+  if (entry < 0 || entry >= a.E_cap) return;
   s_red[sl][0][2 * lane] = mx0;
   s_red[sl][0][2 * lane + 1] = mx1;
   s_red[sl][1][2 * lane] = sm0;
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compres
     for (int s = 0; s < kC1Slices; ++s) {
       const float ms = s_red[s][0][cc];
       if (ms != -INFINITY) {  // slices with no token of this block hold nothing
-        const float f = expf(ms - M);
+        const float f = exp2f((ms - M) * kC1Log2e);
         sum = fmaf(s_red[s][1][cc], f, sum);
         acc = fmaf(s_red[s][2][cc], f, acc);
       }

@@ -96,10 +96,12 @@ def _dense_ref(q, kv, kl, local_base, q_pos, sink, m, W, scale):
 @pytest.mark.parametrize("B,T,E,m", [
     (1, 300, 600, 128),    # many queries: one CTA per query, long dense row lists
     (2, 90, 1100, 128),    # 180 queries
-    (3, 1, 2000, 128),     # decode: rows split over CTAs, merged with the sink
+    (3, 1, 2000, 128),     # decode: TMA-streamed splits of the rows, merged with the sink
     (4, 1, 8192 + 37, 128),
     (2, 1, 100, 128),      # few rows: two splits
     (5, 1, 3000, 4),       # dense over a CSA-rate cache
+    (2, 20, 700, 128),     # few queries per sequence, each split over CTAs
+    (1, 1, 40000, 128),    # more entries than the streaming kernel's splits hold: pipelined splits
 ])
 def test_dense_attn_tensor_cores(B, T, E, m):
     H, d, W, L = 64, 512, 128, 300
