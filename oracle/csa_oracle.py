@@ -35,7 +35,14 @@ the pages):
     tokens of its own block only; HCA's positional bias is added to the gate logits by
     position inside the block, and the CSA2 compressor has none;
   * an HCA query at t attends to every entry s < floor((t + 1) / m') plus the same window
-    and sink as the CSA core attention.
+    and sink as the CSA core attention;
+  * RMSNorm: y = x / sqrt(mean(x^2) + eps) * weight over the head's d dims, eps = 1e-6 by
+    default, one weight vector [d] shared by the heads; it is applied before RoPE;
+  * RoPE on the last rope_dims (64) dims of a head: interleaved pairs (2j, 2j+1) of that
+    slice rotate by angle pos * theta^(-2j / rope_dims), theta = 10000 by default; a
+    compressed entry i sits at position m * i (the first token of its block); a window row
+    and a query at their token positions; inverse RoPE on an output uses position -t;
+  * FP8 output of the attention: one fp32 scale per (row, head), the key recipe.
 
 Parity status: every function here is pinned by tests (closed forms, hand-computed
 examples, brute force against library routines, invariants); see tests/test_oracle_pins.py.
@@ -403,3 +410,63 @@ def hca_decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: n
     r = hca_token(cfg, inp, b, 0, kv_comp)
     r["entry"] = entry
     return r
+
+
+# ----------------------------------------------------------------------------------
+# attention prologue / epilogue
+#   [V4] "Key and value are the same vector": RoPE on exactly the last 64 dims, and the fix
+#   for a shared key/value, RoPE at position minus the query's position on the last 64 dims
+#   of each head's output; vLLM fuses that inverse RoPE with the FP8 quantisation ahead of
+#   the output projection.  [V4] "Grouped output projection": RMSNorm per head on the queries
+#   and on the single head of the compressed KV entry, just before core attention.
+# ----------------------------------------------------------------------------------
+
+
+def rms_norm(x: np.ndarray, weight: Optional[np.ndarray], eps: float = 1e-6) -> np.ndarray:
+    """x / sqrt(mean(x^2 over the last axis) + eps), times weight (None: no weight)."""
+    x = np.asarray(x, np.float64)
+    y = x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    return y * np.asarray(weight, np.float64) if weight is not None else y
+
+
+def rope_angles(pos, rope_dims: int, theta: float = 10000.0) -> np.ndarray:
+    """Angle of pair j at each position: pos * theta^(-2j / rope_dims); shape [..., rope_dims/2]."""
+    j = np.arange(rope_dims // 2, dtype=np.float64)
+    freq = theta ** (-2.0 * j / rope_dims)
+    return np.asarray(pos, np.float64)[..., None] * freq
+
+
+def rope(x: np.ndarray, pos, rope_dims: int = 64, theta: float = 10000.0) -> np.ndarray:
+    """Rotate the last rope_dims dims of x (last axis) at position pos (broadcast over the
+    leading axes; a scalar or an array of x.shape[:-1] or a prefix of it): pair (2j, 2j+1)
+    of that slice rotates by its angle; the other dims are unchanged."""
+    x = np.asarray(x, np.float64).copy()
+    if rope_dims == 0:
+        return x
+    d = x.shape[-1]
+    p = np.asarray(pos, np.float64)
+    p = p.reshape(p.shape + (1,) * (x.ndim - 1 - p.ndim))
+    a = rope_angles(p, rope_dims, theta)
+    c, s_ = np.cos(a), np.sin(a)
+    x0 = x[..., d - rope_dims::2].copy()
+    x1 = x[..., d - rope_dims + 1::2].copy()
+    x[..., d - rope_dims::2] = x0 * c - x1 * s_
+    x[..., d - rope_dims + 1::2] = x0 * s_ + x1 * c
+    return x
+
+
+def norm_rope(x: np.ndarray, pos, weight, eps: float = 1e-6, rope_dims: int = 64, theta: float = 10000.0):
+    """RMSNorm over each head's dims (last axis; skipped when weight is None), then RoPE on
+    its last rope_dims dims."""
+    y = rms_norm(x, weight, eps) if weight is not None else np.asarray(x, np.float64)
+    return rope(y, pos, rope_dims, theta)
+
+
+def compressed_entry_position(m: int, i: int) -> int:
+    """RoPE position of compressed entry i: the first token of its block."""
+    return m * i
+
+
+def inverse_rope(o: np.ndarray, t, rope_dims: int = 64, theta: float = 10000.0) -> np.ndarray:
+    """The output fix of a shared key/value: RoPE at position -t on the last rope_dims dims."""
+    return rope(o, -np.asarray(t, np.float64), rope_dims, theta)

@@ -495,3 +495,71 @@ def test_hca_decode_step_writes_the_block_entry_first():
     r2 = O.hca_decode_step_sequence(C, inp, 0, kv2)
     assert r2["entry"] is None and r2["nv"] == 7
     np.testing.assert_array_equal(kv2, kv)
+
+
+# ------------------------------------------------------------------ RMSNorm, partial RoPE, inverse RoPE
+
+def test_rms_norm_matches_torch():
+    x = rng.standard_normal((5, 3, 64)) * 3.0
+    w = rng.standard_normal(64)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,), torch.from_numpy(w), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(x, w, 1e-6), ref, rtol=1e-13, atol=1e-13)
+    # unit weight: every row has mean square 1 / (1 + eps / ms)
+    y = O.rms_norm(x, None, 0.0)
+    np.testing.assert_allclose((y * y).mean(-1), 1.0, rtol=1e-13)
+
+
+def test_rope_is_complex_rotation_of_the_last_dims():
+    d, rd, theta = 48, 16, 500.0
+    x = rng.standard_normal((7, d))
+    pos = rng.integers(0, 10 ** 6, 7)
+    y = O.rope(x, pos, rd, theta)
+    np.testing.assert_array_equal(y[:, :d - rd], x[:, :d - rd])          # the other dims untouched
+    z = x[:, d - rd::2] + 1j * x[:, d - rd + 1::2]
+    freq = np.array([theta ** (-2.0 * j / rd) for j in range(rd // 2)])
+    zr = z * np.exp(1j * pos[:, None] * freq[None, :])
+    np.testing.assert_allclose(y[:, d - rd::2], zr.real, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(y[:, d - rd + 1::2], zr.imag, rtol=1e-9, atol=1e-12)
+    # a rotation: norms kept, and RoPE(-p) undoes RoPE(p); rope_dims = 0 is the identity
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    np.testing.assert_allclose(O.rope(y, -pos, rd, theta), x, rtol=1e-9, atol=1e-9)
+    np.testing.assert_array_equal(O.rope(x, pos, 0), x)
+    # pair 0 turns by exactly pos radians
+    p1 = O.rope(np.concatenate([np.zeros(d - rd), [1.0, 0.0], np.zeros(rd - 2)]), 2, rd, theta)
+    np.testing.assert_allclose(p1[d - rd:d - rd + 2], [math.cos(2.0), math.sin(2.0)], rtol=1e-15)
+
+
+def test_rope_scores_depend_on_relative_position():
+    d, rd = 32, 16
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    s1 = O.rope(q, 1000, rd) @ O.rope(k, 937, rd)
+    s2 = O.rope(q, 1000 + 4321, rd) @ O.rope(k, 937 + 4321, rd)
+    assert abs(s1 - s2) < 1e-9 * (1 + abs(s1))
+    assert abs(s1 - O.rope(q, 1000, rd) @ O.rope(k, 938, rd)) > 1e-6
+
+
+def test_inverse_rope_restores_translation_invariance_of_shared_kv():
+    # Key = value = RoPE'd row: the raw attention output depends on absolute positions; RoPE at
+    # minus the query position on the output makes it depend on distances only.
+    H, d, rd, n = 4, 32, 16, 9
+    q = rng.standard_normal((H, d))
+    rows = rng.standard_normal((n, d))
+    sink = rng.standard_normal(H)
+    t, pos = 5000, 5000 - rng.integers(0, 3000, n)
+
+    def attend(shift):
+        r = O.rope(rows, pos + shift, rd)
+        out, _ = O.sparse_attention(O.rope(q, t + shift, rd), r, sink, 0.2)
+        return out, O.inverse_rope(out, t + shift, rd)
+    raw0, fix0 = attend(0)
+    raw1, fix1 = attend(12345)
+    np.testing.assert_allclose(fix1, fix0, rtol=1e-9, atol=1e-12)
+    assert np.max(np.abs(raw1 - raw0)) > 1e-3
+
+
+def test_norm_rope_composition_and_entry_position():
+    x = rng.standard_normal((3, 2, 64))
+    w = rng.standard_normal(64)
+    pos = np.array([0, 17, 99])
+    np.testing.assert_allclose(O.norm_rope(x, pos, w, 1e-6, 16), O.rope(O.rms_norm(x, w, 1e-6), pos, 16), rtol=0)
+    assert O.compressed_entry_position(4, 10) == 40 and O.compressed_entry_position(128, 3) == 384
