@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -87,7 +87,9 @@ STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
                   3: ("indexer_tc_bf16_prefill_4K.md",) + _INDEXER_STAGE,
                   5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE,
                   6: ("hca_dense_attn_1M_decode.md",) + _DENSE_STAGE,
-                  7: ("hca_dense_attn_prefill_4K.md", ("attn_pf_kernel",), _DENSE_STAGE[1])}
+                  7: ("hca_dense_attn_prefill_4K.md", ("attn_pf_kernel",), _DENSE_STAGE[1]),
+                  9: ("epilogue_norm_rope_prefill_4K.md", ("norm_rope_kernel",),
+                      ("k_epilogue.cu", "csa_ptx.cuh", "csa_epi.h"))}
 
 
 def stage_traffic(config):
@@ -591,7 +593,87 @@ class HcaPrefill:
         return n, elapsed, desc
 
 
-WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill}
+class Epilogue:
+    """Attention prologue / epilogue of the prefill chunk: query RMSNorm + RoPE, the chunk's
+    compression fused with RMSNorm + RoPE + cache insert, inverse RoPE + FP8 of the output."""
+
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        B, T = cfg.B, cfg.T
+        self.units = B * T
+        self.metric = "CSA attention prologue/epilogue tok/s (4,096-token chunk)"
+        self.workload = (f"V4-Flash attention prologue/epilogue on a prefill chunk of {T:,} tokens after {cfg.N - T:,}: "
+                         f"query RMSNorm + RoPE ({cfg.H}x{cfg.d}, last 64 dims), compression of {T // cfg.m:,} entries "
+                         f"fused with RMSNorm + RoPE + cache insert, inverse RoPE + e4m3 of the attention output")
+        self.config_extra = {"batch": B, "chunk": T, "heads": cfg.H, "head_dim": cfg.d, "rope_dims": 64,
+                             "rope_theta": 10000.0, "m": cfg.m}
+        self.tok0 = cfg.N - T - cfg.m
+        self.e0, self.e1 = (cfg.N - T) // cfg.m, cfg.N // cfg.m
+        if host_only:
+            return
+        self.csa = csa
+        inp = gen.make_inputs(cfg, dev, row0=row0)
+        self.inp = inp
+        self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
+        self.nr_q = csa.NormRope(weight=inp["q_norm"], eps=1e-6, rope_dims=64, theta=10000.0)
+        self.nr_kv = csa.NormRope(weight=inp["kv_norm"], eps=1e-6, rope_dims=64, theta=10000.0)
+        self.q_out = torch.empty_like(inp["q"])
+        self.codes = torch.empty(inp["o"].shape, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(B * T, cfg.H, device=dev)
+        from compressed_sparse_attention_csa_gb300.accounting import epilogue_work
+        work = epilogue_work(cfg)
+        self.stage_label = "query RMSNorm + RoPE: norm_rope_kernel<bf16> (one warp per (token, head))"
+        self.stage_bound = "hbm"
+        self.stage_amount = work["q_bytes"]
+        self.step_bytes = work["bytes"]
+        self.touched_bytes = work["bytes"]
+        self.e2e_in = {k: inp[k] for k in ["q", "o", "q_pos", "kv_str", "z_str"]}
+        self.e2e_out = self.codes
+
+    def step(self):
+        csa, c, inp = self.csa, self.c, self.inp
+        self.stage_fn()
+        csa.compress_kv_norm_rope(c, 2, inp["kv_str"], inp["z_str"], inp["bias"], self.tok0, self.e0, self.e1,
+                                  inp["kv_comp"], self.nr_kv)
+        csa.inverse_rope_quant(c, inp["o"], inp["q_pos"], self.codes, out_scale=self.scales)
+
+    def stage_fn(self):
+        inp = self.inp
+        self.csa.norm_rope(self.c, inp["q"], inp["q_pos"], self.nr_q, out=self.q_out)
+
+    def oracle(self, n, inp_cpu=None):
+        """n tokens of the chunk (query RMSNorm + RoPE, inverse RoPE + e4m3 of the output) plus
+        n/T of the chunk's compression."""
+        import numpy as np
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        h = {k: _host64(src[k] if k in ("bias", "q_norm", "kv_norm", "q_pos") else src[k][0:1])
+             for k in ["q", "o", "q_pos", "kv_str", "z_str", "bias", "q_norm", "kv_norm"]}
+        t0 = time.perf_counter()
+        for i in range(self.e0, self.e1):
+            e = O.compress_entry(h["kv_str"][0], h["z_str"][0], h["bias"], cfg.m, i, tok0=self.tok0)
+            O.norm_rope(e, O.compressed_entry_position(cfg.m, i), h["kv_norm"], 1e-6, 64, 10000.0)
+        t_comp = time.perf_counter() - t0
+        t_rows = 0.0
+        for i in range(n):
+            tq = (i * (cfg.T - 1)) // max(n - 1, 1)
+            t = int(h["q_pos"][tq])
+            t0 = time.perf_counter()
+            O.norm_rope(h["q"][0, tq], t, h["q_norm"], 1e-6, 64, 10000.0)
+            r = O.inverse_rope(h["o"][0, tq], t, 64, 10000.0)
+            O.quantize_rows_e4m3(r.astype(np.float32))
+            t_rows += time.perf_counter() - t0
+        elapsed = t_rows + t_comp * n / cfg.T
+        desc = (f"{n} token(s) of the chunk (query RMSNorm + RoPE over {cfg.H} heads, inverse RoPE + e4m3 of the "
+                f"output) plus {n}/{cfg.T} of the chunk's fused compression ({t_comp:.1f} s whole), float64 numpy")
+        return n, elapsed, desc
+
+
+WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue}
 
 
 def config_of(wl):
@@ -599,7 +681,7 @@ def config_of(wl):
     return dict(workload=wl.workload, **wl.config_extra,
                 l2="inputs larger than L2: independent copies of the workload stepped in rotation",
                 timing="K steps replayed back to back as CUDA graphs between one pair of CUDA events")
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048}
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096}
 
 
 # ------------------------------------------------------------------ main
@@ -626,7 +708,7 @@ def main():
         # float64 numpy step takes seconds, so the run stops after REFERENCE_BUDGET_S of oracle
         # time even if fewer than --steps steps ran; `steps` reports the steps actually timed.
         wl = Wl(cfg, None, torch, "cpu", 0, host_only=True)
-        n1 = 4 if args.config in (3, 7) else 1
+        n1 = 4 if args.config in (3, 7) else (256 if args.config == 9 else 1)
         inp = gen.make_inputs(cfg.replace(B=1), "cpu")
         n_total, t_total, desc, done = 0, 0.0, "", 0
         while done < max(args.steps, 1) and (done == 0 or t_total < REFERENCE_BUDGET_S):

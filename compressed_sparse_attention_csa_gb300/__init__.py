@@ -3,6 +3,7 @@
 The computation lives in libcsa (hand-written CUDA, C ABI in include/csa.h); this package is
 its thin Python binding.  See :mod:`compressed_sparse_attention_csa_gb300.ops`.
 """
-from .ops import (Config, CsaError, block_pool, compress_kv, compress_kv_single, decode_step,  # noqa: F401
-                  dense_attn, get_last_error, hca_decode_step, indexer_scores, indexer_topk, launch_count,
-                  sparse_attn, topk, version, workspace_size)
+from .ops import (Config, CsaError, NormRope, block_pool, compress_kv, compress_kv_norm_rope,  # noqa: F401
+                  compress_kv_single, decode_step, dense_attn, get_last_error, hca_decode_step, indexer_scores,
+                  indexer_topk, inverse_rope_quant, launch_count, norm_rope, sparse_attn, topk, version,
+                  workspace_size)

@@ -37,6 +37,10 @@ class csa_hca_decode_args(ctypes.Structure):
                 ("local_base", c_vp), ("out", c_vp), ("lse", c_vp)]
 
 
+class csa_norm_rope(ctypes.Structure):
+    _fields_ = [("norm_weight", c_vp), ("eps", c_f32), ("rope_dims", c_i32), ("rope_theta", c_f32)]
+
+
 # name -> (restype, argtypes); the exported symbols of include/csa.h
 SIGNATURES = {
     "csa_version": (c_i32, []),
@@ -65,6 +69,12 @@ SIGNATURES = {
                                       c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "csa_hca_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_hca_decode_args), c_vp,
                                            c_sz, c_vp]),
+    "csa_norm_rope_apply": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i64, c_i32, c_i32, c_vp,
+                                           ctypes.POINTER(csa_norm_rope), c_vp]),
+    "csa_compress_kv_norm_rope": (ctypes.c_int, [ctypes.POINTER(csa_config), c_i32, c_i32, c_vp, c_vp, c_vp, c_i64,
+                                                 c_i64, c_i64, c_i64, c_vp, c_i64, ctypes.POINTER(csa_norm_rope), c_vp]),
+    "csa_inverse_rope_quant": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_vp, c_i32, c_f32, c_vp,
+                                              ctypes.c_int, c_vp, c_vp]),
     "csa_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
                                        c_vp]),
 }

@@ -142,3 +142,16 @@ def hca_prefill_work(cfg) -> Dict[str, float]:
     attn = B * (cfg.E * cfg.d * ab + T * 2 * cfg.H * cfg.d * ab)     # every entry once, q/out once
     return {"attention_rows": rows, "attention_flops": flops, "flops": flops, "attention_bytes": attn,
             "compress_bytes": comp, "bytes": attn + comp}
+
+
+def epilogue_work(cfg) -> Dict[str, float]:
+    """Algorithmic bytes of the attention prologue / epilogue of a prefill chunk: the queries
+    read and written once (RMSNorm + RoPE), the chunk's compression streams read and its
+    entries written once (fused RMSNorm + RoPE), the attention output read once and written
+    as e4m3 codes with one fp32 scale per (token, head)."""
+    ab = _act_bytes(cfg.act)
+    B, T, H, d, m = cfg.B, cfg.T, cfg.H, cfg.d, cfg.m
+    q = 2 * B * T * H * d * ab + B * T * 8
+    comp = B * ((T + m) * 2 * 2 * d * ab + (T // m) * d * ab) + 2 * m * d * 4 + d * 4
+    o = B * T * H * d * (ab + 1) + B * T * H * 4
+    return {"q_bytes": q, "compress_bytes": comp, "out_bytes": o, "bytes": q + comp + o}

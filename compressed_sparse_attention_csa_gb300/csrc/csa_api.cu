@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "csa_internal.h"
+#include "csa_epi.h"
 
 namespace csa {
 
@@ -311,6 +312,114 @@ csa_status csa_compress_kv_single(const csa_config* cfg, int32_t dim, const void
   a.n_ent = ent_end - ent_begin;
   a.E_cap = E_cap;
   return launch_status(launch_compress1(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+csa_status check_norm_rope(const csa_norm_rope* nr, int32_t dim) {
+  if (!nr) return CSA_ERR_NULL;
+  if (nr->norm_weight && !aligned16(nr->norm_weight)) return CSA_ERR_ALIGN;
+  if (nr->rope_dims < 0 || nr->rope_dims > dim || nr->rope_dims > kMaxRopeDims || (nr->rope_dims & 1) ||
+      !std::isfinite(nr->eps) || nr->eps < 0.f ||
+      (nr->rope_dims > 0 && !(nr->rope_theta > 1.f && std::isfinite(nr->rope_theta))))
+    return CSA_ERR_SHAPE;
+  return CSA_OK;
+}
+NormRope to_norm_rope(const csa_norm_rope* nr) {
+  NormRope r{};
+  r.weight = nr->norm_weight;
+  r.eps = nr->eps;
+  r.rope_dims = nr->rope_dims;
+  r.theta = nr->rope_theta;
+  make_rope_table(nr->rope_theta, nr->rope_dims, &r.tab);
+  return r;
+}
+}  // namespace
+
+csa_status csa_norm_rope_apply(const csa_config* cfg, const void* x, void* y, int64_t rows, int32_t heads, int32_t dim,
+                               const int64_t* pos, const csa_norm_rope* nr, csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!x || !y || !pos) return CSA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(pos)) return CSA_ERR_ALIGN;
+  if (rows < 0 || heads < 1 || dim < 8 || dim > 1024 || (dim & 7) || rows * heads >= (int64_t(1) << 40))
+    return CSA_ERR_SHAPE;
+  st = check_norm_rope(nr, dim);
+  if (st != CSA_OK) return st;
+  NormRopeArgs a{};
+  a.x = x;
+  a.y = y;
+  a.rows = rows;
+  a.heads = heads;
+  a.dim = dim;
+  a.pos = pos;
+  a.bf16 = cfg->act == CSA_BF16;
+  a.nr = to_norm_rope(nr);
+  return launch_status(launch_norm_rope(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_compress_kv_norm_rope(const csa_config* cfg, int32_t streams, int32_t dim, const void* kv, const void* z,
+                                     const float* bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
+                                     int64_t ent_end, void* out, int64_t E_cap, const csa_norm_rope* nr,
+                                     csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!kv || !z || !out || (streams == 2 && !bias)) return CSA_ERR_NULL;
+  if (!aligned16(kv) || !aligned16(z) || !aligned16(out) || (bias && !aligned16(bias))) return CSA_ERR_ALIGN;
+  const int64_t m = cfg->m;
+  if ((streams != 1 && streams != 2) || dim < 64 || dim > 1024 || (dim % 64) || n_tok < 0 || ent_begin < 0 ||
+      ent_end < ent_begin || ent_end > E_cap || E_cap * cfg->B >= (int64_t(1) << 31))
+    return CSA_ERR_SHAPE;
+  if (ent_end > ent_begin) {
+    const int64_t need_lo = streams == 2 ? (ent_begin > 0 ? m * (ent_begin - 1) : 0) : m * ent_begin;
+    if (tok0 > need_lo || m * ent_end > tok0 + n_tok) return CSA_ERR_SHAPE;
+  }
+  st = check_norm_rope(nr, dim);
+  if (st != CSA_OK) return st;
+  CompressEpiArgs a{};
+  a.two_stream = streams == 2;
+  a.kv = kv;
+  a.z = z;
+  a.bias = bias;
+  a.B = cfg->B;
+  a.m = cfg->m;
+  a.dim = dim;
+  a.n_tok = n_tok;
+  a.tok0 = tok0;
+  a.ent_begin = ent_begin;
+  a.n_ent = ent_end - ent_begin;
+  a.E_cap = E_cap;
+  a.out = out;
+  a.bf16 = cfg->act == CSA_BF16;
+  a.nr = to_norm_rope(nr);
+  return launch_status(launch_compress_norm_rope(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_inverse_rope_quant(const csa_config* cfg, const void* o, int64_t rows, const int64_t* pos,
+                                  int32_t rope_dims, float rope_theta, void* out, csa_dtype out_dtype, float* out_scale,
+                                  csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!o || !pos || !out || (out_dtype == CSA_E4M3 && !out_scale)) return CSA_ERR_NULL;
+  if (out_dtype != cfg->act && out_dtype != CSA_E4M3) return CSA_ERR_DTYPE;
+  if (!aligned16(o) || !aligned16(pos) || !aligned16(out) || (out_scale && !aligned16(out_scale))) return CSA_ERR_ALIGN;
+  if (rows < 0 || cfg->d < 8 || cfg->d > 1024 || (cfg->d & 7) || rope_dims < 0 || rope_dims > cfg->d ||
+      rope_dims > kMaxRopeDims || (rope_dims & 1) ||
+      (rope_dims > 0 && !(rope_theta > 1.f && std::isfinite(rope_theta))) || rows * cfg->H >= (int64_t(1) << 40))
+    return CSA_ERR_SHAPE;
+  InvRopeArgs a{};
+  a.o = o;
+  a.rows = rows;
+  a.heads = cfg->H;
+  a.dim = cfg->d;
+  a.pos = pos;
+  a.rope_dims = rope_dims;
+  a.theta = rope_theta;
+  if (rope_dims > 0) make_rope_table(rope_theta, rope_dims, &a.tab);
+  a.bf16 = cfg->act == CSA_BF16;
+  a.out = out;
+  a.e4m3 = out_dtype == CSA_E4M3;
+  a.out_scale = out_scale;
+  return launch_status(launch_inv_rope_quant(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float* w, int32_t T,

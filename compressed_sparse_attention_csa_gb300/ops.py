@@ -270,3 +270,54 @@ def hca_decode_step(cfg: Config, *, q_pos, q, sink, kv_comp, kv_tail, z_tail, bi
     ws = _workspace(lib.csa_workspace_size(L.CSA_OP_HCA_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1]), q.device)
     wp, wb = _ws_args(ws)
     _check("csa_hca_decode_step", lib.csa_hca_decode_step(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))
+
+
+@dataclass
+class NormRope:
+    """RMSNorm weight [dim] fp32 (None: no RMSNorm), epsilon, rotated dims at the end of each
+    head (0: no RoPE) and rotary base."""
+    weight: Optional[torch.Tensor] = None
+    eps: float = 1e-6
+    rope_dims: int = 64
+    theta: float = 10000.0
+
+    def c(self) -> L.csa_norm_rope:
+        return L.csa_norm_rope(_p(self.weight), self.eps, self.rope_dims, self.theta)
+
+
+def norm_rope(cfg: Config, x: torch.Tensor, pos: torch.Tensor, nr: NormRope, out: Optional[torch.Tensor] = None) -> None:
+    """csa_norm_rope_apply: x [rows, heads, dim] (or [B, T, heads, dim]), pos [rows] int64;
+    writes out (default: in place)."""
+    lib = L.load()
+    c = cfg.c()
+    y = x if out is None else out
+    heads, dim = x.shape[-2], x.shape[-1]
+    rows = x.numel() // (heads * dim)
+    n = nr.c()
+    _check("csa_norm_rope_apply",
+           lib.csa_norm_rope_apply(ctypes.byref(c), _p(x), _p(y), rows, heads, dim, _p(pos), ctypes.byref(n), _stream()))
+
+
+def compress_kv_norm_rope(cfg: Config, streams: int, kv: torch.Tensor, z: torch.Tensor, bias: Optional[torch.Tensor],
+                          tok0: int, ent_begin: int, ent_end: int, out: torch.Tensor, nr: NormRope) -> None:
+    """csa_compress_kv_norm_rope: streams 2 (kv, z [B, n_tok, 2, dim]) or 1 ([B, n_tok, dim]);
+    out [B, E_cap, dim] in cfg.act."""
+    lib = L.load()
+    c = cfg.c()
+    n = nr.c()
+    _check("csa_compress_kv_norm_rope",
+           lib.csa_compress_kv_norm_rope(ctypes.byref(c), streams, kv.shape[-1], _p(kv), _p(z), _p(bias), kv.shape[1],
+                                         tok0, ent_begin, ent_end, _p(out), out.shape[1], ctypes.byref(n), _stream()))
+
+
+def inverse_rope_quant(cfg: Config, o: torch.Tensor, pos: torch.Tensor, out: torch.Tensor,
+                       out_scale: Optional[torch.Tensor] = None, rope_dims: int = 64, theta: float = 10000.0) -> None:
+    """csa_inverse_rope_quant: o [rows, H, d] (or [B, T, H, d]) in cfg.act; out the same shape in
+    cfg.act, or uint8 e4m3 codes with out_scale [rows, H] fp32."""
+    lib = L.load()
+    c = cfg.c()
+    rows = o.numel() // (cfg.H * cfg.d)
+    od = L.CSA_E4M3 if out.dtype == torch.uint8 else (L.CSA_BF16 if out.dtype == torch.bfloat16 else L.CSA_F32)
+    _check("csa_inverse_rope_quant",
+           lib.csa_inverse_rope_quant(ctypes.byref(c), _p(o), rows, _p(pos), rope_dims, theta, _p(out), od,
+                                      _p(out_scale), _stream()))

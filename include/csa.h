@@ -276,6 +276,63 @@ typedef struct {
 csa_status csa_hca_decode_step(const csa_config *cfg, const csa_hca_decode_args *args, void *ws,
                                size_t ws_bytes, csa_stream_t stream);
 
+/*
+ * Attention prologue / epilogue ("Key and value are the same vector": RoPE on exactly the
+ * last 64 dims of each head, and RoPE at minus the query position on each head's output;
+ * "Grouped output projection": RMSNorm per head on the queries and on the compressed KV
+ * entry before core attention).  Conventions of these calls:
+ *   RMSNorm   y = x / sqrt(mean over the head's dim of x^2 + eps) * norm_weight[c]
+ *   RoPE      on dims [dim - rope_dims, dim): pair (2j, 2j+1) of that slice rotates by angle
+ *             pos * rope_theta^(-2j / rope_dims) (x0 cos - x1 sin, x0 sin + x1 cos); the phase
+ *             is exact to about 1e-9 rad for any int64 position (64-bit fixed-point turns)
+ *   a compressed entry i sits at position m * i (the first token of its block).
+ */
+typedef struct {
+  const float *norm_weight; /* [dim] fp32 RMSNorm weight (16-byte aligned), or NULL: no RMSNorm */
+  float eps;                /* RMSNorm epsilon, e.g. 1e-6                                        */
+  int32_t rope_dims;        /* rotated dims at the end of each head: even, 0 .. min(dim, 128)     */
+  float rope_theta;         /* rotary base (> 1), e.g. 10000                                     */
+} csa_norm_rope;
+
+/*
+ * csa_norm_rope_apply — RMSNorm then RoPE on every (row, head) vector: queries at their
+ * positions (q [B*T, H, d], pos = q_pos), window rows (pos = their token positions), or
+ * cache entries (pos = m * i).
+ *   x, y : [rows, heads, dim] in cfg->act (y may be x); dim % 8 == 0, 8 .. 1024
+ *   pos  : [rows] int64
+ * Only cfg->act is read (besides B, H, d, m, W checked as in the HCA calls).
+ */
+csa_status csa_norm_rope_apply(const csa_config *cfg, const void *x, void *y, int64_t rows, int32_t heads,
+                               int32_t dim, const int64_t *pos, const csa_norm_rope *nr,
+                               csa_stream_t stream);
+
+/*
+ * csa_compress_kv_norm_rope — the compressor fused with RMSNorm, RoPE at the entry's
+ * position m * i, and the store into the cache (the fusion vLLM applies to the compressor):
+ *   streams = 2: the gated two-stream compressor of csa_compress_kv (kv, z [B, n_tok, 2, dim],
+ *                bias [2, m, dim] required; entry i needs tokens m(i-1) .. m(i+1)-1);
+ *   streams = 1: the one-stream compressor of csa_compress_kv_single (kv, z [B, n_tok, dim],
+ *                bias [m, dim] or NULL).
+ *   dim % 64 == 0, 64 .. 1024; out [B, E_cap, dim] in cfg->act; rows outside
+ *   [ent_begin, ent_end) untouched.  m = cfg->m.
+ */
+csa_status csa_compress_kv_norm_rope(const csa_config *cfg, int32_t streams, int32_t dim, const void *kv,
+                                     const void *z, const float *bias, int64_t n_tok, int64_t tok0,
+                                     int64_t ent_begin, int64_t ent_end, void *out, int64_t E_cap,
+                                     const csa_norm_rope *nr, csa_stream_t stream);
+
+/*
+ * csa_inverse_rope_quant — RoPE at position -pos[r] on the last rope_dims dims of every head
+ * of the attention output o [rows, cfg->H, cfg->d] (cfg->act), written to out as cfg->act
+ * (out may be o), or, with out_dtype CSA_E4M3, as e4m3 codes [rows, H, d] with one fp32 scale
+ * per (row, head) in out_scale [rows, H]: scale = amax/448 of the rotated vector (1 for an
+ * all-zero vector), code = e4m3_rn_satfinite(x / scale).  cfg->d % 8 == 0, <= 1024;
+ * rope_dims even, <= min(cfg->d, 128).
+ */
+csa_status csa_inverse_rope_quant(const csa_config *cfg, const void *o, int64_t rows, const int64_t *pos,
+                                  int32_t rope_dims, float rope_theta, void *out, csa_dtype out_dtype,
+                                  float *out_scale, csa_stream_t stream);
+
 /* All inputs of one decode token per sequence (T = 1). */
 typedef struct {
   int64_t E_cap;             /* rows of kv_comp / kI / kscale per sequence                    */

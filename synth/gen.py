@@ -164,6 +164,11 @@ CONFIGS: Dict[int, CsaConfig] = {
     8: CsaConfig(8, "tiny HCA layer fp32 (N 4096, m' 128, 8x64 heads, W 128, 16 queries)",
                  B=1, N=4096, m=128, d=64, H=8, HI=4, dI=32, k=64, W=128, T=16,
                  act="f32", kidx="act", mode="hca_full"),
+    # attention prologue / epilogue on the prefill chunk: query RMSNorm + RoPE, the chunk's
+    # compression fused with RMSNorm + RoPE, inverse RoPE + FP8 of the attention output
+    9: CsaConfig(9, "V4-Flash attention prologue/epilogue, prefill chunk (4,096 tokens after 131,072)",
+                 B=1, N=131072 + 4096, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=4096,
+                 act="bf16", kidx="act", mode="epilogue"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)
@@ -237,6 +242,8 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
         out["sink"] = _gen(cfg, "sink", (H,), 1.0, f32, device)
     if cfg.mode.startswith("hca"):
         return _hca_inputs(cfg, out, device, row0, skip)
+    if cfg.mode == "epilogue":
+        return _epilogue_inputs(cfg, out, device, row0)
     out["qI"] = _gen(cfg, "qI", (B, T, HI, dI), 1 / math.sqrt(dI), act, device, row0=row0)
     out["w"] = _gen(cfg, "w", (B, T, HI), 1.0, f32, device, row0=row0)
 
@@ -296,6 +303,28 @@ def _hca_inputs(cfg: CsaConfig, out: Dict[str, torch.Tensor], device, row0: int,
     out["kv_str"] = _gen(cfg, "kv_str", (B, n_str, d), 1 / math.sqrt(d), act, device, row0=row0)
     out["z_str"] = _gen(cfg, "z_str", (B, n_str, d), 1 / math.sqrt(d), act, device, row0=row0)
     out["bias"] = _gen(cfg, "bias", (m, d), 0.1, torch.float32, device)
+    return out
+
+
+_IDS.update({"o": 16, "q_norm": 17, "kv_norm": 18})
+
+
+def _epilogue_inputs(cfg: CsaConfig, out: Dict[str, torch.Tensor], device, row0: int) -> Dict[str, torch.Tensor]:
+    """Attention prologue / epilogue inputs: the attention output o [B,T,H,d] ~ N(0,1)/sqrt(d),
+    RMSNorm weights q_norm / kv_norm [d] ~ 1 + N(0, 0.1^2), the chunk's two-stream compression
+    streams and bias, and the cache it writes into."""
+    act = cfg.torch_act
+    B, T, H, d, m, E = cfg.B, cfg.T, cfg.H, cfg.d, cfg.m, cfg.E
+    t0 = cfg.N - T
+    out["o"] = _gen(cfg, "o", (B, T, H, d), 1 / math.sqrt(d), act, device, row0=row0)
+    out["q_norm"] = 1.0 + _gen(cfg, "q_norm", (d,), 0.1, torch.float32, device)
+    out["kv_norm"] = 1.0 + _gen(cfg, "kv_norm", (d,), 0.1, torch.float32, device)
+    out["kv_comp"] = _gen(cfg, "kv_comp", (B, E, d), 1 / math.sqrt(d), act, device, row0=row0)
+    base, n_str = t0 - m, T + m
+    out["str_base"] = torch.full((B,), base, dtype=torch.int64, device=device)
+    out["kv_str"] = _gen(cfg, "kv_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device, row0=row0)
+    out["z_str"] = _gen(cfg, "z_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device, row0=row0)
+    out["bias"] = _gen(cfg, "bias", (2, m, d), 0.1, torch.float32, device)
     return out
 
 
