@@ -5,7 +5,10 @@ their step, exactly as the benchmark times them, then checked against the oracle
   decode @64K (batch 16, bf16 keys) and @1M (batch 4, FP8 keys): every sequence;
   prefill chunk (4,096 queries after 131,072 tokens): all 1,024 new entries of both caches,
   and indexer scores / top-k / attention on sampled query rows (first and last included);
-  CSA2 decoder group at 262,144 tokens (batch 8): every sequence through all four layers.
+  CSA2 decoder group at 262,144 tokens (batch 8): every sequence through all four layers;
+  HCA decode @1M (batch 4, 8,192 entries a sequence): every sequence; HCA prefill chunk: the 32
+  new entries and sampled query rows; the attention prologue / epilogue of the prefill chunk:
+  every new cache entry and sampled tokens of the query and output passes.
 Agreement criteria are those of the small-size parity tests.
 """
 import numpy as np
@@ -14,8 +17,11 @@ import torch
 
 import compressed_sparse_attention_csa_gb300 as csa
 from _helpers import (assert_decode_matches, assert_entries_close, assert_out_close_with_swaps, assert_pool_valid,
-                      assert_scores_close, assert_selection_ok, np64, oracle_decode, swap_bound)
-from bench import Csa2Group, Decode, Prefill
+                      assert_rows_close, assert_scores_close, assert_selection_ok, np64, np_inputs, oracle_decode,
+                      swap_bound)
+from test_gpu_epilogue import assert_vectors_close, e4m3_half_step
+from test_gpu_hca import assert_single_entries_close
+from bench import Csa2Group, Decode, Epilogue, HcaDecode, HcaPrefill, Prefill
 from oracle import csa_oracle as O
 from synth import gen
 
@@ -123,3 +129,60 @@ def test_csa2_group_full_size():
             bound = swap_bound(h["q"][layer][0], rl, cfg.softmax_scale, [h["kv_comp"][x] for x in g_set - r_set],
                                [h["kv_comp"][y] for y in r_set - g_set])
             assert_out_close_with_swaps(np64(wl.outs[layer, b, 0]), ro, 2e-2, bound, what=f"layer {layer} b={b}")
+
+
+def test_hca_decode_full_size():
+    cfg = gen.CONFIGS[6]
+    wl = HcaDecode(cfg, csa, torch, DEV, 0)
+    h = np_inputs(wl.inp)
+    kv_before = [h["kv_comp"][b].copy() for b in range(cfg.B)]
+    replay_once(wl.step)
+    for b in range(cfg.B):
+        kvc = kv_before[b]
+        r = O.hca_decode_step_sequence(cfg, h, b, kvc)
+        e, ent = r["entry"]
+        assert_single_entries_close(np64(wl.inp["kv_comp"][b, e]), ent, h["kv_str"][b], cfg.m, torch.bfloat16)
+        assert_rows_close(np64(wl.out[b]), r["out"], 2e-2, what=f"out b={b}")
+        np.testing.assert_allclose(np64(wl.lse[b]), r["lse"], atol=5e-3)
+
+
+def test_hca_prefill_full_size_sampled_rows():
+    cfg = gen.CONFIGS[7]
+    wl = HcaPrefill(cfg, csa, torch, DEV, 0)
+    inp = wl.inp
+    h = {k: host(v if k in ("bias", "sink", "q_pos") else v[0:1]) for k, v in inp.items()}
+    kv_o = h["kv_comp"][0].copy()
+    replay_once(wl.step)
+    new = O.compress_single_range(h["kv_str"][0], h["z_str"][0], h["bias"], cfg.m, wl.e0, wl.e1, tok0=wl.tok0)
+    assert_single_entries_close(np64(inp["kv_comp"][0, wl.e0:wl.e1]), new, h["kv_str"], cfg.m, torch.bfloat16)
+    kv_o[wl.e0:wl.e1] = new
+    sub = cfg.replace(B=1)
+    for tq in [0, 1, 127, 128, 2047, 4094, 4095]:
+        r = O.hca_token(sub, h, 0, tq, kv_o)
+        assert_rows_close(np64(wl.out[0, tq]), r["out"], 2e-2, what=f"out row {tq}")
+        np.testing.assert_allclose(np64(wl.lse[0, tq]), r["lse"], atol=5e-3)
+
+
+def test_epilogue_full_size_sampled_tokens():
+    cfg = gen.CONFIGS[9]
+    wl = Epilogue(cfg, csa, torch, DEV, 0)
+    inp = wl.inp
+    h = {k: host(inp[k] if k in ("bias", "q_norm", "kv_norm", "q_pos") else inp[k][0:1])
+         for k in ["q", "o", "q_pos", "kv_str", "z_str", "bias", "q_norm", "kv_norm"]}
+    replay_once(wl.step)
+    ents = np.stack([O.norm_rope(O.compress_entry(h["kv_str"][0], h["z_str"][0], h["bias"], cfg.m, i, tok0=wl.tok0),
+                                 O.compressed_entry_position(cfg.m, i), h["kv_norm"], 1e-6, 64, 10000.0)
+                     for i in range(wl.e0, wl.e1)])
+    assert_vectors_close(np64(inp["kv_comp"][0, wl.e0:wl.e1]), ents, torch.bfloat16, "new cache entries")
+    codes = wl.codes.cpu().numpy()
+    sc = wl.scales.cpu().numpy().astype(np.float64)
+    for tq in [0, 1, 1000, 4095]:
+        t = int(h["q_pos"][tq])
+        ref_q = O.norm_rope(h["q"][0, tq], t, h["q_norm"], 1e-6, 64, 10000.0)
+        assert_vectors_close(np64(wl.q_out[0, tq]), ref_q, torch.bfloat16, f"query {tq}")
+        ref_o = O.inverse_rope(h["o"][0, tq], t, 64, 10000.0)
+        amax = np.abs(ref_o).max(axis=-1)
+        np.testing.assert_allclose(sc[tq], amax / 448.0, rtol=2.0 ** -20)
+        deq = O.e4m3_decode(codes[0, tq]) * sc[tq][:, None]
+        tol = 1.01 * e4m3_half_step(ref_o / sc[tq][:, None]) * sc[tq][:, None] + 1e-6 * amax[:, None]
+        assert float((np.abs(deq - ref_o) / tol).max()) <= 1.0, f"fp8 output of token {tq}"
