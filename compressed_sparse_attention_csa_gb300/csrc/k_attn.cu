@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
     tc_fence_after();
     if (sp.n_split > 1) {
       // split partial: running (max, sum) per head and the unnormalised O (fp32,
-      // [query][split][head][dim]); attn_merge_dec_kernel adds the sink and normalises
+      // [query][split][head][dim]); attn_merge_wide_kernel adds the sink and normalises
       const int64_t ps = r * sp.n_split + split;
       if (own && ch == 0) {
         const bool any = ok && nt > 0;
@@ -929,7 +929,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
 // window first: the window rows, like the query, are inputs that no earlier kernel of the
 // step writes, so they are gathered before the wait on the top-k; the selected rows follow.
 // Partials are stored [query][split][head][dim] (each warp store is 128 contiguous bytes)
-// and merged, with the sink, by attn_merge_dec_kernel.
+// and merged, with the sink, by attn_merge_wide_kernel.
 template <int NH>
 struct DecLayout {
   static constexpr uint32_t kQ = 0;                          // 8 regions x (NH rows x 128 B)
@@ -1435,78 +1435,12 @@ __global__ void __launch_bounds__(kHdThreads, 1)
   }
 }
 
-// Fixed-order merge of the decode partials ([query][split][head][dim]) with the sink: one
-// CTA per (query, 4 heads), one thread per output dim.
-constexpr int kMaxSplitDec = 64;  // 2 * kMergeHeads * kMaxSplitDec <= kD threads load (m, l)
-__global__ void __launch_bounds__(kD) attn_merge_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
-  __shared__ float s_ml[kMaxSplitDec][2][kMergeHeads];  // (m, l) of every split
-  __shared__ float s_f[kMaxSplitDec][kMergeHeads];      // per split, per head: 2^(m_s - M) / den
-  pdl_wait();
-  pdl_trigger();
-  const int64_t r = blockIdx.x;
-  const int h0 = blockIdx.y * kMergeHeads;
-  const int dd = threadIdx.x;
-  const int ns = sp.n_split;
-  // every load of the CTA is issued before the first use: the partials of this thread's dim
-  // (all splits, 4 heads) and, by the first 2 * 4 * ns threads, one (m, l) value each
-  // (splits past the first kPre are loaded after the factors; the decode plans use 5)
-  constexpr int kPre = 8;
-  const float* po = sp.part_o + (r * ns * kH + h0) * kD + dd;
-  float v[kPre][kMergeHeads];
-#pragma unroll
-  for (int x = 0; x < kPre; ++x)
-#pragma unroll
-    for (int j = 0; j < kMergeHeads; ++j)
-      v[x][j] = x < ns ? __ldcg(po + (static_cast<int64_t>(x) * kH + j) * kD) : 0.f;
-  if (threadIdx.x < 2 * kMergeHeads * ns) {
-    const int x = threadIdx.x / (2 * kMergeHeads), w = (threadIdx.x / kMergeHeads) & 1, j = threadIdx.x % kMergeHeads;
-    s_ml[x][w][j] = __ldcg(sp.part_ml + (r * ns + x) * 2 * kH + w * kH + h0 + j);
-  }
-  __syncthreads();
-  if (threadIdx.x < kMergeHeads) {
-    const int j = threadIdx.x, h = h0 + j;
-    const float sk = a.sink[h] * kLog2e;
-    float M = sk;
-    for (int x = 0; x < ns; ++x) M = fmaxf(M, s_ml[x][0][j]);
-    float den = exp2f(sk - M);
-    for (int x = 0; x < ns; ++x) {
-      const float ms = s_ml[x][0][j];
-      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-      s_f[x][j] = f;
-      den = fmaf(s_ml[x][1][j], f, den);
-    }
-    const float inv = 1.f / den;
-    for (int x = 0; x < ns; ++x) s_f[x][j] *= inv;
-    if (a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
-  }
-  __syncthreads();
-  float acc[kMergeHeads] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int x = 0; x < kPre; ++x) {
-    if (x >= ns) break;
-#pragma unroll
-    for (int j = 0; j < kMergeHeads; ++j) {
-      const float f = s_f[x][j];
-      if (f != 0.f) acc[j] = fmaf(v[x][j], f, acc[j]);
-    }
-  }
-  for (int x = kPre; x < ns; ++x) {
-#pragma unroll
-    for (int j = 0; j < kMergeHeads; ++j) {
-      const float f = s_f[x][j];
-      if (f != 0.f) acc[j] = fmaf(__ldcg(po + (static_cast<int64_t>(x) * kH + j) * kD), f, acc[j]);
-    }
-  }
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (r * kH + h0) * kD + dd;
-#pragma unroll
-  for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j]);
-}
-
 // Merge of many split partials ([query][split][head][dim]) with the sink: one CTA per
 // (query, head), thread t owns dims 4t .. 4t+3.  Thread x < n_split reads split x's (m, l);
 // block reductions give M = max(m_x, sink) and den = sum_x l_x 2^(m_x - M) + 2^(sink - M);
 // the partials are then read 8 splits at a time (one float4 each, every load of a batch
 // issued before the first use) and summed in split order.
+constexpr int kMaxSplitDec = 64;  // split partials a query may have
 constexpr int kMwThreads = 128;
 __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnArgs a, const TcAttnSplit sp) {
   __shared__ float s_f[kMaxSplitDec];
@@ -1777,7 +1711,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
                             : launch_pdl(attn_dec_kernel<64>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_merge_dec_kernel, dim3(static_cast<unsigned>(rows), kH / kMergeHeads), dim3(kD), 0, s, a, sp);
+    e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
     count_launches(1);
     return e;
   }
