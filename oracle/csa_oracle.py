@@ -42,7 +42,10 @@ the pages):
     slice rotate by angle pos * theta^(-2j / rope_dims), theta = 10000 by default; a
     compressed entry i sits at position m * i (the first token of its block); a window row
     and a query at their token positions; inverse RoPE on an output uses position -t;
-  * FP8 output of the attention: one fp32 scale per (row, head), the key recipe.
+  * FP8 output of the attention: one fp32 scale per (row, head), the key recipe;
+  * FP8 main-KV entries (576 B): e4m3 codes of dims 0 .. d-65 (round to nearest even,
+    saturating, no scale: RMSNorm bounds the entries well inside e4m3's range), then the last
+    64 (RoPE) dims in bf16.
 
 Parity status: every function here is pinned by tests (closed forms, hand-computed
 examples, brute force against library routines, invariants); see tests/test_oracle_pins.py.
@@ -470,3 +473,34 @@ def compressed_entry_position(m: int, i: int) -> int:
 def inverse_rope(o: np.ndarray, t, rope_dims: int = 64, theta: float = 10000.0) -> np.ndarray:
     """The output fix of a shared key/value: RoPE at position -t on the last rope_dims dims."""
     return rope(o, -np.asarray(t, np.float64), rope_dims, theta)
+
+
+# ----------------------------------------------------------------------------------
+# production storage of the main KV  [V4] "What the cache costs, checked four ways": the
+# 64 RoPE dims in bf16 and the other 448 in FP8, 64 * 2 + 448 = 576 bytes an entry.
+# ----------------------------------------------------------------------------------
+
+KV_ROPE_DIMS = 64
+
+
+def kv_fp8_encode(x: np.ndarray) -> np.ndarray:
+    """Entries [..., d] -> bytes [..., d - 64 + 128]: e4m3 codes of dims 0 .. d-65, then the
+    bf16 bits (little endian) of the last 64 dims."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    nf = d - KV_ROPE_DIMS
+    codes = e4m3_encode(x[..., :nf])
+    rope = f32_to_bf16_bits(x[..., nf:].astype(np.float32))
+    out = np.empty(x.shape[:-1] + (nf + 2 * KV_ROPE_DIMS,), np.uint8)
+    out[..., :nf] = codes
+    out[..., nf:] = rope.astype("<u2").view(np.uint8).reshape(x.shape[:-1] + (2 * KV_ROPE_DIMS,))
+    return out
+
+
+def kv_fp8_decode(b: np.ndarray) -> np.ndarray:
+    """Bytes [..., d - 64 + 128] -> entries [..., d] in float64."""
+    b = np.asarray(b, np.uint8)
+    nf = b.shape[-1] - 2 * KV_ROPE_DIMS
+    head = e4m3_decode(b[..., :nf])
+    tail = bf16_bits_to_f64(np.ascontiguousarray(b[..., nf:]).view("<u2"))
+    return np.concatenate([head, tail], axis=-1)

@@ -563,3 +563,28 @@ def test_norm_rope_composition_and_entry_position():
     pos = np.array([0, 17, 99])
     np.testing.assert_allclose(O.norm_rope(x, pos, w, 1e-6, 16), O.rope(O.rms_norm(x, w, 1e-6), pos, 16), rtol=0)
     assert O.compressed_entry_position(4, 10) == 40 and O.compressed_entry_position(128, 3) == 384
+
+
+# ------------------------------------------------------------------ FP8 main-KV entries
+
+def test_kv_fp8_entry_layout_and_roundtrip():
+    # the pages' byte model: 64 RoPE dims in bf16 + 448 in FP8 = 576 bytes an entry
+    x = rng.standard_normal((5, 512)) * 3.0
+    b = O.kv_fp8_encode(x)
+    assert b.shape == (5, 576) and b.dtype == np.uint8 and 64 * 2 + 448 == 576
+    y = O.kv_fp8_decode(b)
+    # FP8 part: the nearest e4m3 value (torch's conversion); RoPE part: the nearest bf16
+    ref_head = torch.from_numpy(x[:, :448].astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ref_tail = torch.from_numpy(x[:, 448:].astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(y[:, :448], ref_head)
+    np.testing.assert_array_equal(y[:, 448:], ref_tail)
+    # values already on the grids survive exactly; beyond 448 the FP8 part saturates
+    np.testing.assert_array_equal(O.kv_fp8_decode(O.kv_fp8_encode(y)), y)
+    big = np.zeros(512)
+    big[0], big[1], big[500] = 1000.0, -1000.0, 1000.0
+    yb = O.kv_fp8_decode(O.kv_fp8_encode(big))
+    assert yb[0] == 448.0 and yb[1] == -448.0 and yb[500] == 1000.0
+    # little-endian bf16 bits of the RoPE dims, right after the 448 codes
+    one = np.zeros(512)
+    one[448] = 1.0
+    assert list(O.kv_fp8_encode(one)[448:450]) == [0x80, 0x3F]
