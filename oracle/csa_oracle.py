@@ -103,7 +103,8 @@ _E4M3_POS = _E4M3_ALL[:0x7F]  # codes 0x00..0x7E, ascending
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
-    """Nearest E4M3 code, ties to the even code, saturating to +-448 (finite inputs)."""
+    """Nearest E4M3 code, ties to the even code, saturating to +-448 (finite inputs); the sign
+    bit is kept, so -0 and negative values that round to zero encode as -0 (0x80)."""
     x = np.asarray(x, dtype=np.float64)
     a = np.minimum(np.abs(x), 448.0)
     hi = np.searchsorted(_E4M3_POS, a, side="left")          # first value >= a
@@ -113,7 +114,7 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     d_hi = _E4M3_POS[hi] - a
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
     code = np.where(pick_hi, hi, lo).astype(np.uint8)
-    return np.where((x < 0) & (code != 0), code | 0x80, code).astype(np.uint8)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
 
 
 def quantize_rows_e4m3(x_f32: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:

@@ -588,3 +588,10 @@ def test_kv_fp8_entry_layout_and_roundtrip():
     one = np.zeros(512)
     one[448] = 1.0
     assert list(O.kv_fp8_encode(one)[448:450]) == [0x80, 0x3F]
+
+
+def test_e4m3_encode_signed_zero_matches_torch():
+    # OCP E4M3 has a signed zero: -0 and negatives that round to zero keep the sign bit
+    v = np.array([0.0, -0.0, -1e-4, 1e-4, -2.0 ** -11, 2.0 ** -11, -3.0 * 2.0 ** -11, 448.0, -448.0])
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(O.e4m3_encode(v), ref)
