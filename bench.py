@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -673,15 +673,107 @@ class Epilogue:
         return n, elapsed, desc
 
 
-WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue}
+class Fp8KvAttn:
+    """The decode attention at 1M over FP8 main-KV entries (576 B: 448 e4m3 + 64 bf16 dims) for a
+    fixed selection; the same selection over the bf16 cache is timed beside it."""
+    _shared = {}
+
+    def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
+        from synth import gen
+        self.cfg = cfg
+        B = cfg.B
+        self.units = B
+        self.metric = "CSA decode attention tok/s @1M, FP8 main-KV entries"
+        self.workload = (f"V4-Flash CSA sparse attention, batch {B} @ {cfg.N:,} tokens ({cfg.E:,} entries/seq) over FP8 "
+                         f"main-KV entries (448 e4m3 + 64 bf16 dims, 576 B), k {cfg.k} selected + W {cfg.W} window rows, "
+                         f"{cfg.H}x{cfg.d} heads, sink")
+        self.config_extra = {"batch": B, "context": cfg.N, "entries_per_seq": cfg.E, "top_k": cfg.k, "window": cfg.W,
+                             "kv_entry_bytes": cfg.d - 64 + 128,
+                             "l2": ("the copies stepped in rotation share the cache and differ in their selections: "
+                                    "more than twice the L2 of distinct rows between two reads of a row")}
+        if host_only:
+            return
+        self.csa = csa
+        # The copies the benchmark rotates through share one cache (1.6 GB at 1M) and differ in
+        # their selections, so a step reads rows no recent step read.
+        key = (str(dev), row0)
+        shared = Fp8KvAttn._shared.get(key)
+        self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
+                            act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
+        if shared is None:
+            inp = gen.make_inputs(cfg, dev, row0=row0)
+            kv8 = torch.empty(B, cfg.E, cfg.d + 64, dtype=torch.uint8, device=dev)
+            csa.kv_pack_fp8(self.c, inp["kv_comp"], kv8)
+            shared = Fp8KvAttn._shared[key] = {"inp": inp, "kv8": kv8, "draws": 0}
+        self.kv8 = shared["kv8"]
+        inp = dict(shared["inp"])
+        if shared["draws"] > 0:
+            inp["idx"] = gen.fp8kv_selection(cfg, dev, row0, shared["draws"])
+        shared["draws"] += 1
+        self.inp = inp
+        self.out = torch.empty(B, 1, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
+        self.lse = torch.empty(B, 1, cfg.H, device=dev)
+        ab = 2
+        self.stage_label = "attn_dec_kernel<16, FP8 entries> + attn_merge_wide_kernel"
+        self.stage_bound = "hbm"
+        self.stage_amount = B * (cfg.k * (cfg.d + 64) + cfg.W * cfg.d * ab + 2 * cfg.H * cfg.d * ab + cfg.k * 4)
+        self.step_bytes = self.stage_amount
+        self.touched_bytes = self.stage_amount
+        self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_local", "idx"]}
+        self.e2e_out = self.out
+
+    def step(self):
+        inp = self.inp
+        self.csa.sparse_attn_fp8kv(self.c, inp["q"], self.kv8, inp["idx"], inp["kv_local"], inp["local_base"],
+                                   inp["q_pos"], inp["sink"], self.out, self.lse)
+
+    def stage_fn(self):
+        self.step()
+
+    def bf16_step(self):
+        inp = self.inp
+        self.csa.sparse_attn(self.c, inp["q"], inp["kv_comp"], inp["idx"], inp["kv_local"], inp["local_base"],
+                             inp["q_pos"], inp["sink"], self.out, self.lse)
+
+    def oracle(self, n, inp_cpu=None):
+        """n sequences: the oracle's FP8 encoding of the selected entries, then attention."""
+        import numpy as np
+        from oracle import csa_oracle as O
+        cfg = self.cfg
+        n = max(1, n)
+        src = inp_cpu if inp_cpu is not None else self.inp
+        nb = src["q_pos"].shape[0]
+        elapsed = 0.0
+        for i in range(n):
+            b = (i * nb) // n
+            h = {k: _host64(src[k] if k == "sink" else src[k][b:b + 1]) for k in
+                 ["q", "kv_local", "local_base", "q_pos", "sink", "idx"]}
+            sel = h["idx"][0]
+            ent = _host64(src["kv_comp"][b][src["idx"][b].long()])
+            t0 = time.perf_counter()
+            dec = O.kv_fp8_decode(O.kv_fp8_encode(ent))
+            cache = {int(x): dec[j] for j, x in enumerate(sel)}
+            rows = np.stack([cache[int(x)] for x in sel] + [h["kv_local"][0][p - int(h["local_base"][0])]
+                            for p in O.window_positions(int(h["q_pos"][0]), cfg.W, int(h["local_base"][0]),
+                                                        h["kv_local"].shape[1])])
+            O.sparse_attention(h["q"][0, 0], rows, h["sink"], cfg.softmax_scale)
+            elapsed += time.perf_counter() - t0
+        desc = (f"{n} sequence(s), one decode token each (FP8 encode/decode of the {cfg.k} selected entries, attention "
+                f"over {cfg.k}+{cfg.W} rows), float64 numpy, {elapsed:.2f} s")
+        return n, elapsed, desc
+
+
+WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn}
 
 
 def config_of(wl):
     """The JSON line's `config` (identical for both arms)."""
-    return dict(workload=wl.workload, **wl.config_extra,
-                l2="inputs larger than L2: independent copies of the workload stepped in rotation",
-                timing="K steps replayed back to back as CUDA graphs between one pair of CUDA events")
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096}
+    c = dict(workload=wl.workload, l2="inputs larger than L2: independent copies of the workload stepped in rotation",
+             timing=("K steps back to back between one pair of CUDA events: every full rotation of the copies "
+                     "replayed as one CUDA graph (a step of each copy), the remaining steps one graph each"))
+    c.update(wl.config_extra)
+    return c
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400}
 
 
 # ------------------------------------------------------------------ main
@@ -779,19 +871,35 @@ def main():
         torch.cuda.synchronize(dev)
         return g
 
-    def time_rotation(gs, n):
+    def time_rotation(gs, n, whole=None):
+        """Exactly n steps in rotation over the copies; with `whole` (one graph holding a step of
+        every copy, in order) the full rotations replay as one graph each, so the host's graph
+        launches keep ahead of a short step the way a serving loop's multi-layer graph does."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        full, rem = divmod(n, len(gs)) if whole is not None else (0, n)
         e0.record(stream)
-        for i in range(n):
+        for _ in range(full):
+            whole.replay()
+        for i in range(rem):
             gs[i % len(gs)].replay()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1)
 
+    def capture_all(fns):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for f in fns:
+                f()
+        torch.cuda.synchronize(dev)
+        return g
+
     n_cap = csa.launch_count()
     g_steps = [capture(w.step) for w in wls]
-    launches_per_step = (csa.launch_count() - n_cap) // R
+    g_all = capture_all([w.step for w in wls])
+    launches_per_step = (csa.launch_count() - n_cap) // (2 * R)
     time_rotation(g_steps, max(3, args.warmup))
+    g_all.replay()
     assert csa.get_last_error() == 0
 
     gpu_id = "0"
@@ -806,7 +914,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    total_ms = time_rotation(g_steps, K)
+    total_ms = time_rotation(g_steps, K, g_all)
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
@@ -834,9 +942,10 @@ def main():
 
     # ---- dominant kernel stage alone, same inputs and launch configuration, same rotation
     g_stages = [capture(w.stage_fn) for w in wls]
-    time_rotation(g_stages, 3 * R)
-    Ki = max(3, min(K, 500))
-    stage_ms = max_over_ranks(time_rotation(g_stages, Ki) / Ki)
+    g_stages_all = capture_all([w.stage_fn for w in wls])
+    time_rotation(g_stages, 3 * R, g_stages_all)
+    Ki = max(3 * R, min(K, 500))
+    stage_ms = max_over_ranks(time_rotation(g_stages, Ki, g_stages_all) / Ki)
     hbm, bf16, bf16_sus, peak_kind = peaks()
     if wl.stage_bound == "hbm":
         achieved = wl.stage_amount / (stage_ms / 1e3) / 1e9
@@ -854,10 +963,17 @@ def main():
 
     extra = {"flushed_step": {"ms_per_step": round(flushed_ms, 5),
                               "value": round(wl.units * world / (flushed_ms / 1e3), 1)}}
+    if isinstance(wl, Fp8KvAttn):
+        g_b = [capture(w.bf16_step) for w in wls]
+        g_b_all = capture_all([w.bf16_step for w in wls])
+        time_rotation(g_b, 3 * R, g_b_all)
+        b_ms = max_over_ranks(time_rotation(g_b, K, g_b_all) / K)
+        extra["bf16_entries"] = {"value": round(wl.units * world / (b_ms / 1e3), 1), "ms_per_step": round(b_ms, 5)}
     if isinstance(wl, Csa2Group):
         g_ns = [capture(w.step_without_scan) for w in wls]
-        time_rotation(g_ns, 3 * R)
-        ns_ms = max_over_ranks(time_rotation(g_ns, K) / K)
+        g_ns_all = capture_all([w.step_without_scan for w in wls])
+        time_rotation(g_ns, 3 * R, g_ns_all)
+        ns_ms = max_over_ranks(time_rotation(g_ns, K, g_ns_all) / K)
         extra["without_scan"] = {"value": round(wl.units * world / (ns_ms / 1e3), 1), "ms_per_step": round(ns_ms, 5),
                                  "frac_of_hbm": round(wl.work["bytes_without_scan"] / (ns_ms / 1e3) / 1e9 / hbm, 4)}
 

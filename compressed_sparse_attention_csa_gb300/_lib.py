@@ -75,6 +75,12 @@ SIGNATURES = {
                                                  c_i64, c_i64, c_i64, c_vp, c_i64, ctypes.POINTER(csa_norm_rope), c_vp]),
     "csa_inverse_rope_quant": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_vp, c_i32, c_f32, c_vp,
                                               ctypes.c_int, c_vp, c_vp]),
+    "csa_kv_pack_fp8": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i32, c_vp, c_vp]),
+    "csa_compress_kv_norm_rope_fp8kv": (ctypes.c_int, [ctypes.POINTER(csa_config), c_i32, c_i32, c_vp, c_vp, c_vp,
+                                                       c_i64, c_i64, c_i64, c_i64, c_vp, c_i64,
+                                                       ctypes.POINTER(csa_norm_rope), c_vp]),
+    "csa_sparse_attn_fp8kv": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i32, c_vp, c_i64, c_vp, c_vp, c_i64,
+                                             c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "csa_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
                                        c_vp]),
 }

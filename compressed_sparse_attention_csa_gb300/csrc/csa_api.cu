@@ -357,10 +357,10 @@ csa_status csa_norm_rope_apply(const csa_config* cfg, const void* x, void* y, in
   return launch_status(launch_norm_rope(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-csa_status csa_compress_kv_norm_rope(const csa_config* cfg, int32_t streams, int32_t dim, const void* kv, const void* z,
-                                     const float* bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
-                                     int64_t ent_end, void* out, int64_t E_cap, const csa_norm_rope* nr,
-                                     csa_stream_t stream) {
+namespace {
+csa_status compress_norm_rope_impl(const csa_config* cfg, int32_t streams, int32_t dim, const void* kv, const void* z,
+                                   const float* bias, int64_t n_tok, int64_t tok0, int64_t ent_begin, int64_t ent_end,
+                                   void* out, int64_t E_cap, const csa_norm_rope* nr, bool fp8kv, csa_stream_t stream) {
   csa_status st = check_cfg_hca(cfg);
   if (st != CSA_OK) return st;
   if (!kv || !z || !out || (streams == 2 && !bias)) return CSA_ERR_NULL;
@@ -390,8 +390,42 @@ csa_status csa_compress_kv_norm_rope(const csa_config* cfg, int32_t streams, int
   a.E_cap = E_cap;
   a.out = out;
   a.bf16 = cfg->act == CSA_BF16;
+  a.fp8kv = fp8kv;
   a.nr = to_norm_rope(nr);
   return launch_status(launch_compress_norm_rope(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+csa_status csa_compress_kv_norm_rope(const csa_config* cfg, int32_t streams, int32_t dim, const void* kv, const void* z,
+                                     const float* bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
+                                     int64_t ent_end, void* out, int64_t E_cap, const csa_norm_rope* nr,
+                                     csa_stream_t stream) {
+  return compress_norm_rope_impl(cfg, streams, dim, kv, z, bias, n_tok, tok0, ent_begin, ent_end, out, E_cap, nr,
+                                 false, stream);
+}
+
+csa_status csa_compress_kv_norm_rope_fp8kv(const csa_config* cfg, int32_t streams, int32_t dim, const void* kv,
+                                           const void* z, const float* bias, int64_t n_tok, int64_t tok0,
+                                           int64_t ent_begin, int64_t ent_end, void* out, int64_t E_cap,
+                                           const csa_norm_rope* nr, csa_stream_t stream) {
+  return compress_norm_rope_impl(cfg, streams, dim, kv, z, bias, n_tok, tok0, ent_begin, ent_end, out, E_cap, nr,
+                                 true, stream);
+}
+
+csa_status csa_kv_pack_fp8(const csa_config* cfg, const void* x, int64_t rows, int32_t dim, void* out,
+                           csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!x || !out) return CSA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(out)) return CSA_ERR_ALIGN;
+  if (rows < 0 || dim <= 64 || dim > 1024 || (dim % 16)) return CSA_ERR_SHAPE;
+  KvPackArgs a{};
+  a.x = x;
+  a.out = out;
+  a.rows = rows;
+  a.dim = dim;
+  a.bf16 = cfg->act == CSA_BF16;
+  return launch_status(launch_kv_pack_fp8(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_inverse_rope_quant(const csa_config* cfg, const void* o, int64_t rows, const int64_t* pos,
@@ -618,6 +652,49 @@ csa_status csa_sparse_attn(const csa_config* cfg, const void* q, int32_t T, cons
   a.err = err_word_ptr();
   a.num_sms = sms;
   return launch_status(launch_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_sparse_attn_fp8kv(const csa_config* cfg, const void* q, int32_t T, const void* kv_comp, int64_t E_cap,
+                           const int32_t* idx, const void* kv_local, int64_t L, const int64_t* local_base,
+                           const int64_t* q_pos, const float* sink, void* out, float* lse, void* ws,
+                           size_t ws_bytes, csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!q || !kv_comp || !idx || !kv_local || !local_base || !q_pos || !sink || !out) return CSA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv_comp) || !aligned16(idx) || !aligned16(kv_local) || !aligned16(local_base) ||
+      !aligned16(q_pos) || !aligned16(sink) || !aligned16(out) || (lse && !aligned16(lse)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  const int sms = device_sm_count();
+  if (T < 0 || E_cap < 0 || L < 0 || !attn_shape_ok(cfg) || E_cap * cfg->B >= (int64_t(1) << 31) ||
+      !attn_fp8kv_supported(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms))
+    return CSA_ERR_SHAPE;
+  const size_t need = attn_workspace_bytes(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms);
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  AttnArgs a{};
+  a.q = q;
+  a.kv_comp = kv_comp;
+  a.idx = idx;
+  a.kv_local = kv_local;
+  a.local_base = local_base;
+  a.q_pos = q_pos;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.B = cfg->B;
+  a.T = T;
+  a.H = cfg->H;
+  a.d = cfg->d;
+  a.k = cfg->k;
+  a.W = cfg->W;
+  a.E_cap = E_cap;
+  a.L = L;
+  a.softmax_scale = cfg->softmax_scale;
+  a.act = cfg->act;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.err = err_word_ptr();
+  a.num_sms = sms;
+  return launch_status(launch_attn_fp8kv(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 namespace {

@@ -44,8 +44,9 @@ struct CompressEpiArgs {
   const float* bias;    // [2, m, dim] / [m, dim] or null (one stream)
   int B, m, dim;        // dim even, <= 1024
   int64_t n_tok, tok0, ent_begin, n_ent, E_cap;
-  void* out;            // [B, E_cap, dim]
+  void* out;            // [B, E_cap, dim], or [B, E_cap, dim + 64] bytes with fp8kv
   bool bf16;
+  bool fp8kv;           // store the entry as an FP8 main-KV entry
   NormRope nr;
 };
 cudaError_t launch_compress_norm_rope(const CompressEpiArgs& a, cudaStream_t s);
@@ -66,5 +67,21 @@ struct InvRopeArgs {
   float* out_scale;     // [rows, heads] when e4m3
 };
 cudaError_t launch_inv_rope_quant(const InvRopeArgs& a, cudaStream_t s);
+
+// FP8 main-KV entries (d - 64 e4m3 codes, then the last 64 dims in bf16: 576 B for d = 512).
+// Pack rows [rows, d] (bf16 / fp32) into that format.
+struct KvPackArgs {
+  const void* x;
+  void* out;            // [rows, d + 64] bytes
+  int64_t rows;
+  int dim;              // % 16 == 0, 64 < dim <= 1024
+  bool bf16;
+};
+cudaError_t launch_kv_pack_fp8(const KvPackArgs& a, cudaStream_t s);
+
+// Sparse attention over FP8 main-KV entries (kv_comp [B, E_cap, 576] bytes), decode shapes:
+// the split plan of csa_sparse_attn's decode path (few queries, k + W > 128 rows).
+bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms);
+cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s);
 
 }  // namespace csa

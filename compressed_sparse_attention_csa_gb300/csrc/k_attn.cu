@@ -21,6 +21,7 @@
 // order with the sink; prefill runs one CTA per query.
 #include <algorithm>
 
+#include "csa_epi.h"
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
 
@@ -930,6 +931,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
 // step writes, so they are gathered before the wait on the top-k; the selected rows follow.
 // Partials are stored [query][split][head][dim] (each warp store is 128 contiguous bytes)
 // and merged, with the sink, by attn_merge_wide_kernel.
+// FP8 main-KV entries: 448 e4m3 codes (28 chunks of 16) then 64 bf16 (8 chunks of 16).
+constexpr int kFp8Chunks = (kD - 64) / 16;
+constexpr int kFp8RowBytes = (kD - 64) + 64 * 2;
+
 template <int NH>
 struct DecLayout {
   static constexpr uint32_t kQ = 0;                          // 8 regions x (NH rows x 128 B)
@@ -940,7 +945,7 @@ struct DecLayout {
   static constexpr size_t kSmem = 1024 + kMisc + kMiscBytes + kMaxK * 4;
 };
 
-template <int NH>
+template <int NH, bool FP8KV>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
   using LY = DecLayout<NH>;
   extern __shared__ uint8_t smem_raw[];
@@ -1008,14 +1013,74 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
   const int n_rows = n_win + n_sel;
   const int row_hi = min(n_rows, row_cap);
   const int nr = row_hi - row_lo;  // rows of this split (<= 0: none)
-  for (int i = tid; i < kRows * 64; i += kTcThreads) {
-    const int j = i >> 6, c = i & 63;
-    const int lp = row_lo + j;
-    uint8_t* dst = sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7);
-    if (lp >= row_hi) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    } else if (lp >= n_win) {
-      cp_async16(dst, kvc + static_cast<int64_t>(sel[lp - n_win]) * kD + c * 8);
+  if constexpr (!FP8KV) {
+    for (int i = tid; i < kRows * 64; i += kTcThreads) {
+      const int j = i >> 6, c = i & 63;
+      const int lp = row_lo + j;
+      uint8_t* dst = sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7);
+      if (lp >= row_hi) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      } else if (lp >= n_win) {
+        cp_async16(dst, kvc + static_cast<int64_t>(sel[lp - n_win]) * kD + c * 8);
+      }
+    }
+  } else {
+    // FP8 entries (576 B: e4m3 dims 0..447, bf16 dims 448..511): a row is 36 chunks of 16 B;
+    // chunk q < 28 holds dims 16q .. 16q+15 as e4m3 (two bf16 chunks of the tile once
+    // converted), chunk q >= 28 bf16 dims 448 + 8 (q - 28) .. (copied as they are).  Every
+    // load of a thread is issued before the first conversion.
+    constexpr int kQ = kFp8RowBytes / 16, kItems = (kRows * kQ + kTcThreads - 1) / kTcThreads;
+    const uint8_t* kvb = static_cast<const uint8_t*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kFp8RowBytes;
+    uint4 raw[kItems];
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kTcThreads;
+      if (i >= kRows * kQ) break;
+      const int j = i / kQ, q = i - j * kQ;
+      const int lp = row_lo + j;
+      if (lp >= row_hi) {
+        if (q < kFp8Chunks) {
+          *reinterpret_cast<uint4*>(sR + ((2 * q) >> 3) * (kRows * 128) + sw128(j, (2 * q) & 7)) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(sR + ((2 * q + 1) >> 3) * (kRows * 128) + sw128(j, (2 * q + 1) & 7)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          const int c = 2 * kFp8Chunks + (q - kFp8Chunks);
+          *reinterpret_cast<uint4*>(sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else if (lp >= n_win) {
+        const uint8_t* src = kvb + static_cast<int64_t>(sel[lp - n_win]) * kFp8RowBytes + q * 16;
+        if (q < kFp8Chunks) {
+          raw[u] = __ldg(reinterpret_cast<const uint4*>(src));
+        } else {
+          const int c = 2 * kFp8Chunks + (q - kFp8Chunks);
+          cp_async16(sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7), src);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kTcThreads;
+      if (i >= kRows * kQ) break;
+      const int j = i / kQ, q = i - j * kQ;
+      const int lp = row_lo + j;
+      if (lp < row_hi && lp >= n_win && q < kFp8Chunks) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[u]);
+        uint4 lo, hi;
+        uint32_t* l = reinterpret_cast<uint32_t*>(&lo);
+        uint32_t* h = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {  // 4 e4m3 codes -> 4 bf16
+          const __half2_raw p0 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[e] & 0xFFFFu), __NV_E4M3);
+          const __half2_raw p1 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[e] >> 16), __NV_E4M3);
+          const __nv_bfloat162 b0 = __float22bfloat162_rn(__half22float2(__half2(p0)));
+          const __nv_bfloat162 b1 = __float22bfloat162_rn(__half22float2(__half2(p1)));
+          uint32_t* dstw = e < 2 ? l : h;
+          dstw[(e & 1) * 2] = *reinterpret_cast<const uint32_t*>(&b0);
+          dstw[(e & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+        }
+        *reinterpret_cast<uint4*>(sR + ((2 * q) >> 3) * (kRows * 128) + sw128(j, (2 * q) & 7)) = lo;
+        *reinterpret_cast<uint4*>(sR + ((2 * q + 1) >> 3) * (kRows * 128) + sw128(j, (2 * q + 1) & 7)) = hi;
+      }
     }
   }
   cp_async_wait_all();
@@ -1697,18 +1762,19 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
     static bool dattr = false;
     if (!dattr) {
-      cudaFuncSetAttribute(attn_dec_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_dec_kernel<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<16>::kSmem));
-      cudaFuncSetAttribute(attn_dec_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_dec_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<32>::kSmem));
-      cudaFuncSetAttribute(attn_dec_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_dec_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<64>::kSmem));
       dattr = true;
     }
     dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
-    cudaError_t e = hg == 4 ? launch_pdl(attn_dec_kernel<16>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
-                  : hg == 2 ? launch_pdl(attn_dec_kernel<32>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
-                            : launch_pdl(attn_dec_kernel<64>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
+    cudaError_t e =
+        hg == 4 ? launch_pdl(attn_dec_kernel<16, false>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
+        : hg == 2 ? launch_pdl(attn_dec_kernel<32, false>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
+                  : launch_pdl(attn_dec_kernel<64, false>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess) return e;
     e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
@@ -1726,6 +1792,44 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
                          static_cast<int>(smem));
     e = launch_pdl(attn_simt_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(rows)), dim3(kSimtThreads), smem, s, a);
   }
+  count_launches(1);
+  return e;
+}
+
+bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
+  if (!attn_uses_tensor_cores(act, H, d, k)) return false;
+  const TcAttnSplit sp = plan_split(B, T, k, W, num_sms);
+  return sp.n_split > 1 && sp.rows_per_split == kRows;
+}
+
+cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.B) * a.T;
+  if (rows == 0) return cudaSuccess;
+  if (!attn_fp8kv_supported(a.B, a.T, a.H, a.d, a.k, a.W, a.act, a.num_sms)) return cudaErrorInvalidValue;
+  TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  sp.part_o = reinterpret_cast<float*>(ws);
+  sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));
+  const int64_t per = static_cast<int64_t>(sp.n_split) * rows;
+  const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
+  static bool fattr = false;
+  if (!fattr) {
+    cudaFuncSetAttribute(attn_dec_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(DecLayout<16>::kSmem));
+    cudaFuncSetAttribute(attn_dec_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(DecLayout<32>::kSmem));
+    cudaFuncSetAttribute(attn_dec_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(DecLayout<64>::kSmem));
+    fattr = true;
+  }
+  dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
+  cudaError_t e =
+      hg == 4 ? launch_pdl(attn_dec_kernel<16, true>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
+      : hg == 2 ? launch_pdl(attn_dec_kernel<32, true>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
+                : launch_pdl(attn_dec_kernel<64, true>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
   count_launches(1);
   return e;
 }

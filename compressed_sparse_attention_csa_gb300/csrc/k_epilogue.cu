@@ -341,6 +341,17 @@ __global__ void __launch_bounds__(512) compress_norm_rope_kernel(const CompressE
     v1 = x0 * sn + x1 * cs;
   }
   const int64_t row = static_cast<int64_t>(b) * a.E_cap + entry;
+  if (a.fp8kv) {  // FP8 main-KV entry: e4m3 codes of dims < dim - 64, then bf16
+    uint8_t* o = static_cast<uint8_t*>(a.out) + row * (a.dim + 64);
+    const int nf = a.dim - 64;
+    if (c < nf) {
+      *reinterpret_cast<uint16_t*>(o + c) =
+          static_cast<uint16_t>(f_to_e4m3(v0) | (static_cast<uint16_t>(f_to_e4m3(v1)) << 8));
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(o + nf + 2 * (c - nf)) = __floats2bfloat162_rn(v0, v1);
+    }
+    return;
+  }
   if constexpr (sizeof(T) == 2)
     *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.out) + row * a.dim + c) =
         __floats2bfloat162_rn(v0, v1);
@@ -348,7 +359,54 @@ __global__ void __launch_bounds__(512) compress_norm_rope_kernel(const CompressE
     *reinterpret_cast<float2*>(static_cast<float*>(a.out) + row * a.dim + c) = make_float2(v0, v1);
 }
 
+// ---- pack rows into FP8 main-KV entries, one warp per row
+template <typename T, int CPL>
+__global__ void __launch_bounds__(32 * kVecWarps) kv_pack_fp8_kernel(const KvPackArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * kVecWarps + (threadIdx.x >> 5);
+  if (r >= a.rows) return;
+  const int nch = a.dim >> 3, nf = a.dim - 64;
+  float x[CPL][8];
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) {
+    const int ch = lane + 32 * q;
+    if (ch < nch) load8<T>(static_cast<const T*>(a.x) + r * a.dim + 8 * ch, x[q]);
+  }
+  uint8_t* o = static_cast<uint8_t*>(a.out) + r * (a.dim + 64);
+#pragma unroll
+  for (int q = 0; q < CPL; ++q) {
+    const int ch = lane + 32 * q;
+    if (ch >= nch) continue;
+    if (8 * ch < nf) {
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i >> 2] |= static_cast<uint32_t>(f_to_e4m3(x[q][i])) << (8 * (i & 3));
+      *reinterpret_cast<uint2*>(o + 8 * ch) = make_uint2(w[0], w[1]);
+    } else {
+      store8<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16*>(o + nf + 2 * (8 * ch - nf)), x[q]);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_pack_fp8(const KvPackArgs& a, cudaStream_t s) {
+  if (a.rows == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((a.rows + kVecWarps - 1) / kVecWarps));
+  const dim3 blk(32 * kVecWarps);
+  const bool two = a.dim <= 512;
+  cudaError_t e;
+  if (a.bf16)
+    e = two ? launch_pdl(kv_pack_fp8_kernel<__nv_bfloat16, 2>, grid, blk, 0, s, a)
+            : launch_pdl(kv_pack_fp8_kernel<__nv_bfloat16, 4>, grid, blk, 0, s, a);
+  else
+    e = two ? launch_pdl(kv_pack_fp8_kernel<float, 2>, grid, blk, 0, s, a)
+            : launch_pdl(kv_pack_fp8_kernel<float, 4>, grid, blk, 0, s, a);
+  count_launches(1);
+  return e;
+}
 
 void make_rope_table(float theta, int rope_dims, RopeTable* t) {
   *t = RopeTable{};

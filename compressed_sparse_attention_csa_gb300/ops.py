@@ -321,3 +321,39 @@ def inverse_rope_quant(cfg: Config, o: torch.Tensor, pos: torch.Tensor, out: tor
     _check("csa_inverse_rope_quant",
            lib.csa_inverse_rope_quant(ctypes.byref(c), _p(o), rows, _p(pos), rope_dims, theta, _p(out), od,
                                       _p(out_scale), _stream()))
+
+
+def kv_pack_fp8(cfg: Config, x: torch.Tensor, out: torch.Tensor) -> None:
+    """csa_kv_pack_fp8: rows x [..., dim] in cfg.act -> FP8 main-KV entries out [..., dim + 64] uint8."""
+    lib = L.load()
+    c = cfg.c()
+    dim = x.shape[-1]
+    _check("csa_kv_pack_fp8", lib.csa_kv_pack_fp8(ctypes.byref(c), _p(x), x.numel() // dim, dim, _p(out), _stream()))
+
+
+def compress_kv_norm_rope_fp8kv(cfg: Config, streams: int, kv: torch.Tensor, z: torch.Tensor,
+                                bias: Optional[torch.Tensor], tok0: int, ent_begin: int, ent_end: int, out: torch.Tensor,
+                                nr: NormRope) -> None:
+    """csa_compress_kv_norm_rope_fp8kv: as compress_kv_norm_rope, out [B, E_cap, dim + 64] uint8."""
+    lib = L.load()
+    c = cfg.c()
+    n = nr.c()
+    _check("csa_compress_kv_norm_rope_fp8kv",
+           lib.csa_compress_kv_norm_rope_fp8kv(ctypes.byref(c), streams, kv.shape[-1], _p(kv), _p(z), _p(bias),
+                                               kv.shape[1], tok0, ent_begin, ent_end, _p(out), out.shape[1],
+                                               ctypes.byref(n), _stream()))
+
+
+def sparse_attn_fp8kv(cfg: Config, q: torch.Tensor, kv_fp8: torch.Tensor, idx: torch.Tensor, kv_local: torch.Tensor,
+                      local_base: torch.Tensor, q_pos: torch.Tensor, sink: torch.Tensor, out: torch.Tensor,
+                      lse: Optional[torch.Tensor] = None) -> None:
+    """csa_sparse_attn_fp8kv: kv_fp8 [B, E_cap, 576] uint8 FP8 entries; the rest as sparse_attn."""
+    lib = L.load()
+    c = cfg.c()
+    B, T = q.shape[0], q.shape[1]
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_ATTN, ctypes.byref(c), B * T, T), q.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_sparse_attn_fp8kv",
+           lib.csa_sparse_attn_fp8kv(ctypes.byref(c), _p(q), T, _p(kv_fp8), kv_fp8.shape[1], _p(idx), _p(kv_local),
+                                     kv_local.shape[1], _p(local_base), _p(q_pos), _p(sink), _p(out), _p(lse), wp, wb,
+                                     _stream()))

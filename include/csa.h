@@ -333,6 +333,33 @@ csa_status csa_inverse_rope_quant(const csa_config *cfg, const void *o, int64_t 
                                   int32_t rope_dims, float rope_theta, void *out, csa_dtype out_dtype,
                                   float *out_scale, csa_stream_t stream);
 
+/*
+ * FP8 main-KV entries ("What the cache costs, checked four ways": the 64 RoPE dims in bf16 and
+ * the other 448 in FP8, 576 bytes an entry): bytes [0, d-64) are e4m3 codes of dims 0 .. d-65
+ * (round to nearest even, saturating at +-448, no scale: RMSNorm keeps the entries well inside
+ * that range), bytes [d-64, d+64) the last 64 dims in bf16 (little endian).
+ *
+ * csa_kv_pack_fp8 — rows x [rows, dim] (cfg->act) -> out [rows, dim + 64] bytes; dim % 16 == 0,
+ *                   64 < dim <= 1024.
+ * csa_compress_kv_norm_rope_fp8kv — csa_compress_kv_norm_rope writing FP8 entries:
+ *                   out [B, E_cap, dim + 64] bytes.
+ * csa_sparse_attn_fp8kv — csa_sparse_attn with kv_comp [B, E_cap, 576] FP8 entries (the rows
+ *                   are widened to bf16 in shared memory before the tensor-core products);
+ *                   window rows stay cfg->act.  Decode shapes only (bf16, H = 64, d = 512 and
+ *                   the split plan of few queries: B*T below the SM count and k + W > 128);
+ *                   CSA_ERR_SHAPE otherwise.  Workspace: csa_workspace_size(CSA_OP_ATTN, ...).
+ */
+csa_status csa_kv_pack_fp8(const csa_config *cfg, const void *x, int64_t rows, int32_t dim, void *out,
+                           csa_stream_t stream);
+csa_status csa_compress_kv_norm_rope_fp8kv(const csa_config *cfg, int32_t streams, int32_t dim,
+                                           const void *kv, const void *z, const float *bias, int64_t n_tok,
+                                           int64_t tok0, int64_t ent_begin, int64_t ent_end, void *out,
+                                           int64_t E_cap, const csa_norm_rope *nr, csa_stream_t stream);
+csa_status csa_sparse_attn_fp8kv(const csa_config *cfg, const void *q, int32_t T, const void *kv_comp,
+                                 int64_t E_cap, const int32_t *idx, const void *kv_local, int64_t L,
+                                 const int64_t *local_base, const int64_t *q_pos, const float *sink,
+                                 void *out, float *lse, void *ws, size_t ws_bytes, csa_stream_t stream);
+
 /* All inputs of one decode token per sequence (T = 1). */
 typedef struct {
   int64_t E_cap;             /* rows of kv_comp / kI / kscale per sequence                    */

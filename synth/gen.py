@@ -169,6 +169,10 @@ CONFIGS: Dict[int, CsaConfig] = {
     9: CsaConfig(9, "V4-Flash attention prologue/epilogue, prefill chunk (4,096 tokens after 131,072)",
                  B=1, N=131072 + 4096, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=4096,
                  act="bf16", kidx="act", mode="epilogue"),
+    # the decode attention at 1M over FP8 main-KV entries (448 e4m3 + 64 bf16 dims, 576 B)
+    10: CsaConfig(10, "V4-Flash CSA decode attention @1M over FP8 main-KV entries (B 4, k 512, W 128)",
+                  B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
+                  act="bf16", kidx="act", mode="fp8kv_attn"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)
@@ -244,6 +248,8 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
         return _hca_inputs(cfg, out, device, row0, skip)
     if cfg.mode == "epilogue":
         return _epilogue_inputs(cfg, out, device, row0)
+    if cfg.mode == "fp8kv_attn":
+        return _fp8kv_inputs(cfg, out, device, row0)
     out["qI"] = _gen(cfg, "qI", (B, T, HI, dI), 1 / math.sqrt(dI), act, device, row0=row0)
     out["w"] = _gen(cfg, "w", (B, T, HI), 1.0, f32, device, row0=row0)
 
@@ -325,6 +331,29 @@ def _epilogue_inputs(cfg: CsaConfig, out: Dict[str, torch.Tensor], device, row0:
     out["kv_str"] = _gen(cfg, "kv_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device, row0=row0)
     out["z_str"] = _gen(cfg, "z_str", (B, n_str, 2, d), 1 / math.sqrt(d), act, device, row0=row0)
     out["bias"] = _gen(cfg, "bias", (2, m, d), 0.1, torch.float32, device)
+    return out
+
+
+_IDS.update({"sel": 19})
+
+
+def fp8kv_selection(cfg: CsaConfig, device, row0: int = 0, draw: int = 0) -> torch.Tensor:
+    """Selection `draw` of k distinct visible entries a query: the k smallest of uniform draws
+    over the entries, ascending ([B, k] int32)."""
+    B, E, k = cfg.B, cfg.E, cfg.k
+    seed = _tensor_seed(cfg.seed, _IDS["sel"] + 64 * draw)
+    rows = []
+    for b in range(B):
+        u = uniform01(seed, torch.arange((row0 + b) * E, (row0 + b + 1) * E, dtype=torch.int64, device=device))
+        rows.append(torch.sort(torch.topk(u, k, largest=False).indices).values.to(torch.int32))
+    return torch.stack(rows)
+
+
+def _fp8kv_inputs(cfg: CsaConfig, out: Dict[str, torch.Tensor], device, row0: int) -> Dict[str, torch.Tensor]:
+    """Cache entries at the scale RMSNorm leaves them (N(0, 1)) and selection 0."""
+    B, E, d = cfg.B, cfg.E, cfg.d
+    out["kv_comp"] = _gen(cfg, "kv_comp", (B, E, d), 1.0, cfg.torch_act, device, row0=row0)
+    out["idx"] = fp8kv_selection(cfg, device, row0, 0)
     return out
 
 

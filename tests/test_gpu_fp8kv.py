@@ -1,0 +1,103 @@
+"""Parity of the FP8 main-KV entries (448 e4m3 dims + 64 bf16 RoPE dims, 576 B) with the CPU
+oracle: the packer bit-exact, the fused compressor within the e4m3 / bf16 rounding of its
+output, and the decode attention over FP8 entries against the oracle's attention over the
+decoded entries (and bit-identical to the bf16 path over the same decoded values)."""
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_csa_gb300 as csa
+from _helpers import assert_rows_close, np64
+from oracle import csa_oracle as O
+from synth import gen
+from test_gpu_epilogue import assert_vectors_close, e4m3_half_step
+from test_gpu_parity import _attn_inputs, _attn_ref
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+def rnd(seed, shape, std=1.0, dtype=torch.float32):
+    n = int(np.prod(shape))
+    return gen.normal(seed, n, device=DEV, std=std).reshape(shape).to(dtype)
+
+
+def cfg_obj(**kw):
+    base = dict(B=2, H=64, d=512, HI=64, dI=128, m=4, k=512, W=128, act=BF16, fp8_keys=False, softmax_scale=None)
+    base.update(kw)
+    return csa.Config(**base)
+
+
+@pytest.mark.parametrize("act,dim", [(BF16, 512), (torch.float32, 512), (BF16, 128)])
+def test_kv_pack_fp8_bit_exact(act, dim):
+    rows = 333
+    x = rnd(800 + dim, (rows, dim), 30.0, act)          # wide range: saturation and subnormals
+    x[0, :8] = torch.tensor([0.0, -0.0, 448.0, -449.0, 1e-4, 2.0 ** -9, 3.0 * 2.0 ** -10, 1000.0])
+    out = torch.empty(rows, dim + 64, dtype=torch.uint8, device=DEV)
+    csa.kv_pack_fp8(cfg_obj(act=act), x, out)
+    assert csa.get_last_error() == 0
+    ref = O.kv_fp8_encode(np64(x))
+    got = out.cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_compress_norm_rope_fp8kv_matches_oracle():
+    B, m, dim, ent_begin, n_ent = 2, 4, 512, 5, 30
+    tok0 = m * (ent_begin - 1)
+    n_tok = m * (ent_begin + n_ent) - tok0
+    kv = rnd(810, (B, n_tok, 2, dim), dim ** -0.5, BF16)
+    z = rnd(811, (B, n_tok, 2, dim), 1.0, BF16)
+    bias = rnd(812, (2, m, dim), 0.1)
+    w = 1.0 + rnd(813, (dim,), 0.1)
+    E_cap = ent_begin + n_ent
+    out = torch.zeros(B, E_cap, dim + 64, dtype=torch.uint8, device=DEV)
+    nr = csa.NormRope(weight=w, eps=1e-6, rope_dims=64, theta=10000.0)
+    csa.compress_kv_norm_rope_fp8kv(cfg_obj(m=m, B=B), 2, kv, z, bias, tok0, ent_begin, E_cap, out, nr)
+    assert csa.get_last_error() == 0
+    for b in range(B):
+        ref = np.stack([O.norm_rope(O.compress_entry(np64(kv[b]), np64(z[b]), np64(bias), m, i, tok0=tok0),
+                                    O.compressed_entry_position(m, i), np64(w), 1e-6, 64, 10000.0)
+                        for i in range(ent_begin, E_cap)])
+        dec = O.kv_fp8_decode(out[b, ent_begin:].cpu().numpy())
+        tol = 1.01 * e4m3_half_step(ref[:, :448]) + 4e-6 * np.abs(ref).max(axis=-1, keepdims=True)
+        assert float((np.abs(dec[:, :448] - ref[:, :448]) / tol).max()) <= 1.0, f"FP8 dims b={b}"
+        assert_vectors_close(dec[:, 448:], ref[:, 448:], BF16, f"RoPE dims b={b}")
+        assert np.all(out[b, :ent_begin].cpu().numpy() == 0)
+
+
+@pytest.mark.parametrize("B,nsel", [(3, [512, 40, 0]), (4, [512]), (1, [300])])
+def test_sparse_attn_fp8kv_decode(B, nsel):
+    H, d, E, k, W, L, T = 64, 512, 1500, 512, 128, 200, 1
+    q, kv, kl, sink, idx = _attn_inputs(820 + B, B, T, H, d, E, k, L, BF16, nsel)
+    kv = kv * 8.0                                      # RMSNorm-scale entries (|x| ~ 0.35)
+    local_base = torch.tensor([[1000, 1040, 0][b % 3] for b in range(B)], dtype=torch.int64, device=DEV)
+    q_pos = torch.tensor([[1150, 1100, 50][b % 3] for b in range(B)], dtype=torch.int64, device=DEV)
+    c = cfg_obj(B=B)
+    packed = torch.empty(B, E, d + 64, dtype=torch.uint8, device=DEV)
+    csa.kv_pack_fp8(c, kv, packed)
+    assert np.array_equal(packed.cpu().numpy(), O.kv_fp8_encode(np64(kv)))   # the oracle's own encoding
+    out = torch.empty(B, T, H, d, device=DEV, dtype=BF16)
+    lse = torch.empty(B, T, H, device=DEV)
+    csa.sparse_attn_fp8kv(c, q, packed, idx, kl, local_base, q_pos, sink, out, lse)
+    assert csa.get_last_error() == 0
+    dec = torch.from_numpy(O.kv_fp8_decode(packed.cpu().numpy())).to(DEV).to(BF16)   # exact in bf16
+    ro, rl = _attn_ref(q, dec, idx, kl, local_base, q_pos, sink, W, d ** -0.5)
+    assert_rows_close(np64(out), ro, 2e-2)
+    np.testing.assert_allclose(np64(lse), rl, atol=5e-3, rtol=0)
+    # the same products as the bf16 path over the decoded entries
+    out_b = torch.empty_like(out)
+    lse_b = torch.empty_like(lse)
+    csa.sparse_attn(c, q, dec, idx, kl, local_base, q_pos, sink, out_b, lse_b)
+    assert torch.equal(out, out_b) and torch.equal(lse, lse_b)
+
+
+def test_sparse_attn_fp8kv_rejects_non_decode_shapes():
+    B, T, H, d, E, k, L = 1, 300, 64, 512, 1500, 512, 400
+    q, kv, kl, sink, idx = _attn_inputs(830, B, T, H, d, E, k, L, BF16)
+    packed = torch.zeros(B, E, d + 64, dtype=torch.uint8, device=DEV)
+    out = torch.empty(B, T, H, d, device=DEV, dtype=BF16)
+    with pytest.raises(csa.CsaError) as e:
+        csa.sparse_attn_fp8kv(cfg_obj(B=B), q, packed, idx, kl, torch.zeros(B, dtype=torch.int64, device=DEV),
+                              torch.arange(T, dtype=torch.int64, device=DEV), sink, out)
+    assert e.value.status == 2
