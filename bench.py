@@ -89,7 +89,9 @@ STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
                   6: ("hca_dense_attn_1M_decode.md",) + _DENSE_STAGE,
                   7: ("hca_dense_attn_prefill_4K.md", ("attn_pf_kernel",), _DENSE_STAGE[1]),
                   9: ("epilogue_norm_rope_prefill_4K.md", ("norm_rope_kernel",),
-                      ("k_epilogue.cu", "csa_ptx.cuh", "csa_epi.h"))}
+                      ("k_epilogue.cu", "csa_ptx.cuh", "csa_epi.h")),
+                  10: ("fp8kv_attn_1M_decode.md", ("attn_dec_kernel", "attn_merge_wide_kernel"),
+                       ("k_attn.cu", "csa_ptx.cuh", "csa_epi.h", "csa_internal.h"))}
 
 
 def stage_traffic(config):
