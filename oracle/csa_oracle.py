@@ -45,7 +45,11 @@ the pages):
   * FP8 output of the attention: one fp32 scale per (row, head), the key recipe;
   * FP8 main-KV entries (576 B): e4m3 codes of dims 0 .. d-65 (round to nearest even,
     saturating, no scale: RMSNorm bounds the entries well inside e4m3's range), then the last
-    64 (RoPE) dims in bf16.
+    64 (RoPE) dims in bf16;
+  * MXFP4 main-KV entries (288 B for 512 channels): per block of 16 channels one e4m3 scale
+    = e4m3(amax / 6) (amax / 6 in binary32), codes = nearest E2M1 value of x / scale in binary32
+    (ties to the even code, saturating at +-6, sign kept); element 2i in the low nibble of byte
+    i; the d/2 payload bytes, then the d/16 scale bytes.
 
 Parity status: every function here is pinned by tests (closed forms, hand-computed
 examples, brute force against library routines, invariants); see tests/test_oracle_pins.py.
@@ -505,3 +509,59 @@ def kv_fp8_decode(b: np.ndarray) -> np.ndarray:
     head = e4m3_decode(b[..., :nf])
     tail = bf16_bits_to_f64(np.ascontiguousarray(b[..., nf:]).view("<u2"))
     return np.concatenate([head, tail], axis=-1)
+
+
+# ----------------------------------------------------------------------------------
+# V4.1 main-KV storage  [V41] section 4 "FP4: the norm argument, and hunting the 890-byte
+# ledger": MXFP4 with E2M1 payloads and one E4M3 scale per 16 channels, no second-level global
+# scale, quantised after RoPE: 512 * 0.5 + 512 / 16 = 288 bytes a token side.
+# ----------------------------------------------------------------------------------
+
+# OCP Microscaling Formats: E2M1 (bias 1), magnitudes of codes 0..7; bit 3 is the sign
+_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+MX_BLOCK = 16
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, np.uint8)
+    v = _E2M1_POS[c & 7]
+    return np.where(c & 8, -v, v)
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 code, ties to the even code, saturating to +-6; the sign bit is kept."""
+    x = np.asarray(x, np.float64)
+    a = np.minimum(np.abs(x), 6.0)
+    hi = np.minimum(np.searchsorted(_E2M1_POS, a, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - _E2M1_POS[lo], _E2M1_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(x), code | 8, code).astype(np.uint8)
+
+
+def mxfp4_encode(x: np.ndarray) -> np.ndarray:
+    """Entries [..., d] (d % 16 == 0) -> bytes [..., d/2 + d/16]."""
+    x32 = np.asarray(x, np.float64).astype(np.float32)
+    d = x32.shape[-1]
+    blk = x32.reshape(x32.shape[:-1] + (d // MX_BLOCK, MX_BLOCK))
+    amax = np.abs(blk).max(axis=-1)
+    sc_code = e4m3_encode((amax / np.float32(6.0)).astype(np.float32))
+    sc = e4m3_decode(sc_code).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(sc[..., None] > 0, blk / np.where(sc[..., None] > 0, sc[..., None], np.float32(1)), np.float32(0))
+    codes = e2m1_encode(q.astype(np.float32)).reshape(x32.shape[:-1] + (d,))
+    payload = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return np.concatenate([payload, sc_code], axis=-1)
+
+
+def mxfp4_decode(b: np.ndarray) -> np.ndarray:
+    """Bytes [..., d/2 + d/16] -> entries [..., d] in float64."""
+    b = np.asarray(b, np.uint8)
+    d = b.shape[-1] * 16 // 9
+    payload, sc_code = b[..., :d // 2], b[..., d // 2:]
+    codes = np.empty(b.shape[:-1] + (d,), np.uint8)
+    codes[..., 0::2] = payload & 15
+    codes[..., 1::2] = payload >> 4
+    vals = e2m1_decode(codes).reshape(b.shape[:-1] + (d // MX_BLOCK, MX_BLOCK))
+    return (vals * e4m3_decode(sc_code)[..., None]).reshape(b.shape[:-1] + (d,))

@@ -595,3 +595,44 @@ def test_e4m3_encode_signed_zero_matches_torch():
     v = np.array([0.0, -0.0, -1e-4, 1e-4, -2.0 ** -11, 2.0 ** -11, -3.0 * 2.0 ** -11, 448.0, -448.0])
     ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     np.testing.assert_array_equal(O.e4m3_encode(v), ref)
+
+
+# ------------------------------------------------------------------ MXFP4 main-KV entries
+
+def test_e2m1_grid_and_rounding():
+    # OCP MX E2M1: codes 0..7 = 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 the sign
+    np.testing.assert_array_equal(O.e2m1_decode(np.arange(8)), [0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    np.testing.assert_array_equal(O.e2m1_decode(np.arange(8, 16)), -np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6]))
+    np.testing.assert_array_equal(O.e2m1_encode(O.e2m1_decode(np.arange(16))), [0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11,
+                                                                                   12, 13, 14, 15])
+    # midpoints tie to the even code; beyond 6 saturates; small negatives keep the sign
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 100.0, -0.1, -5.0])
+    np.testing.assert_array_equal(O.e2m1_decode(O.e2m1_encode(mids)), [0, 1, 1, 2, 2, 4, 4, 6, 6, -0.0, -4])
+    assert O.e2m1_encode(np.array([-0.1]))[0] == 8
+
+
+def test_mxfp4_entry_layout_range_and_roundtrip():
+    # the pages' ledger: 512 channels at 0.5 B + one scale byte per 16 = 288 B
+    x = rng.standard_normal((3, 512))
+    b = O.mxfp4_encode(x)
+    assert b.shape == (3, 288) and 512 // 2 + 512 // 16 == 288
+    # values on the grid of their block's scale survive exactly (amax = 6 * scale)
+    sc = np.array([0.5, 2.0 ** -6, 448.0, 0.0078125])
+    grid = np.tile(np.array([6, -4, 3, 0.5, 0, 1, -1.5, 2, 6, -6, 4, 3, 2, 1, 0.5, 0]), 4) * np.repeat(sc, 16)
+    y = np.concatenate([grid, rng.standard_normal(448)])
+    np.testing.assert_array_equal(O.mxfp4_decode(O.mxfp4_encode(y))[:64], grid)
+    # the largest magnitude: E2M1's 6 times E4M3's 448 = 2688
+    big = np.zeros(16)
+    big[3] = 2688.0
+    assert O.mxfp4_decode(O.mxfp4_encode(big))[3] == 2688.0
+    # element 2i in the low nibble, the scales after the payload
+    one = np.zeros(16)
+    one[0], one[1] = 6.0, -3.0          # scale 1, codes 7 and 8 | 5
+    e = O.mxfp4_encode(one)
+    assert e[0] == (7 | (13 << 4)) and O.e4m3_decode(e[8:9])[0] == 1.0
+    # per element, the error is at most half a step of the block's grid (plus the scale's rounding)
+    dec = O.mxfp4_decode(b).reshape(3, 32, 16)
+    xb = x.reshape(3, 32, 16)
+    s_ = O.e4m3_decode(b[:, 256:]).reshape(3, 32, 1)
+    step = np.where(np.abs(xb) / s_ < 2, 0.5, np.where(np.abs(xb) / s_ < 4, 1.0, 2.0)) * s_
+    assert np.all(np.abs(dec - xb) <= 0.5 * step + 1e-12 + np.maximum(np.abs(xb) - 6 * s_, 0))
