@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -91,6 +91,8 @@ STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
                   9: ("epilogue_norm_rope_prefill_4K.md", ("norm_rope_kernel",),
                       ("k_epilogue.cu", "csa_ptx.cuh", "csa_epi.h")),
                   10: ("fp8kv_attn_1M_decode.md", ("attn_dec_kernel", "attn_merge_wide_kernel"),
+                       ("k_attn.cu", "csa_ptx.cuh", "csa_epi.h", "csa_internal.h")),
+                  11: ("mxfp4kv_attn_1M_decode.md", ("attn_dec_kernel", "attn_merge_wide_kernel"),
                        ("k_attn.cu", "csa_ptx.cuh", "csa_epi.h", "csa_internal.h"))}
 
 
@@ -679,18 +681,22 @@ class Fp8KvAttn:
     """The decode attention at 1M over FP8 main-KV entries (576 B: 448 e4m3 + 64 bf16 dims) for a
     fixed selection; the same selection over the bf16 cache is timed beside it."""
     _shared = {}
+    FMT = "fp8"
 
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
         B = cfg.B
         self.units = B
-        self.metric = "CSA decode attention tok/s @1M, FP8 main-KV entries"
-        self.workload = (f"V4-Flash CSA sparse attention, batch {B} @ {cfg.N:,} tokens ({cfg.E:,} entries/seq) over FP8 "
-                         f"main-KV entries (448 e4m3 + 64 bf16 dims, 576 B), k {cfg.k} selected + W {cfg.W} window rows, "
-                         f"{cfg.H}x{cfg.d} heads, sink")
+        fp8 = self.FMT == "fp8"
+        self.entry_bytes = cfg.d - 64 + 128 if fp8 else cfg.d // 2 + cfg.d // 16
+        self.metric = "CSA decode attention tok/s @1M, " + ("FP8" if fp8 else "MXFP4") + " main-KV entries"
+        self.workload = (f"CSA sparse attention, batch {B} @ {cfg.N:,} tokens ({cfg.E:,} entries/seq) over "
+                         + ("FP8 main-KV entries (448 e4m3 + 64 bf16 dims, 576 B)" if fp8 else
+                            "MXFP4 main-KV entries (E2M1 + one e4m3 scale per 16 channels, 288 B)")
+                         + f", k {cfg.k} selected + W {cfg.W} window rows, {cfg.H}x{cfg.d} heads, sink")
         self.config_extra = {"batch": B, "context": cfg.N, "entries_per_seq": cfg.E, "top_k": cfg.k, "window": cfg.W,
-                             "kv_entry_bytes": cfg.d - 64 + 128,
+                             "kv_entry_bytes": self.entry_bytes,
                              "l2": ("the copies stepped in rotation share the cache and differ in their selections: "
                                     "more than twice the L2 of distinct rows between two reads of a row")}
         if host_only:
@@ -698,14 +704,14 @@ class Fp8KvAttn:
         self.csa = csa
         # The copies the benchmark rotates through share one cache (1.6 GB at 1M) and differ in
         # their selections, so a step reads rows no recent step read.
-        key = (str(dev), row0)
+        key = (str(dev), row0, self.FMT)
         shared = Fp8KvAttn._shared.get(key)
         self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
         if shared is None:
             inp = gen.make_inputs(cfg, dev, row0=row0)
-            kv8 = torch.empty(B, cfg.E, cfg.d + 64, dtype=torch.uint8, device=dev)
-            csa.kv_pack_fp8(self.c, inp["kv_comp"], kv8)
+            kv8 = torch.empty(B, cfg.E, self.entry_bytes, dtype=torch.uint8, device=dev)
+            (csa.kv_pack_fp8 if fp8 else csa.kv_pack_mxfp4)(self.c, inp["kv_comp"], kv8)
             shared = Fp8KvAttn._shared[key] = {"inp": inp, "kv8": kv8, "draws": 0}
         self.kv8 = shared["kv8"]
         inp = dict(shared["inp"])
@@ -716,9 +722,10 @@ class Fp8KvAttn:
         self.out = torch.empty(B, 1, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
         self.lse = torch.empty(B, 1, cfg.H, device=dev)
         ab = 2
-        self.stage_label = "attn_dec_kernel<16, FP8 entries> + attn_merge_wide_kernel"
+        self.stage_label = ("attn_dec_kernel<16, " + ("FP8" if fp8 else "MXFP4") + " entries> + "
+                            "attn_merge_wide_kernel")
         self.stage_bound = "hbm"
-        self.stage_amount = B * (cfg.k * (cfg.d + 64) + cfg.W * cfg.d * ab + 2 * cfg.H * cfg.d * ab + cfg.k * 4)
+        self.stage_amount = B * (cfg.k * self.entry_bytes + cfg.W * cfg.d * ab + 2 * cfg.H * cfg.d * ab + cfg.k * 4)
         self.step_bytes = self.stage_amount
         self.touched_bytes = self.stage_amount
         self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_local", "idx"]}
@@ -726,8 +733,9 @@ class Fp8KvAttn:
 
     def step(self):
         inp = self.inp
-        self.csa.sparse_attn_fp8kv(self.c, inp["q"], self.kv8, inp["idx"], inp["kv_local"], inp["local_base"],
-                                   inp["q_pos"], inp["sink"], self.out, self.lse)
+        fn = self.csa.sparse_attn_fp8kv if self.FMT == "fp8" else self.csa.sparse_attn_mxfp4kv
+        fn(self.c, inp["q"], self.kv8, inp["idx"], inp["kv_local"], inp["local_base"], inp["q_pos"], inp["sink"],
+           self.out, self.lse)
 
     def stage_fn(self):
         self.step()
@@ -753,19 +761,27 @@ class Fp8KvAttn:
             sel = h["idx"][0]
             ent = _host64(src["kv_comp"][b][src["idx"][b].long()])
             t0 = time.perf_counter()
-            dec = O.kv_fp8_decode(O.kv_fp8_encode(ent))
+            dec = (O.kv_fp8_decode(O.kv_fp8_encode(ent)) if self.FMT == "fp8"
+                   else O.mxfp4_decode(O.mxfp4_encode(ent)))
             cache = {int(x): dec[j] for j, x in enumerate(sel)}
             rows = np.stack([cache[int(x)] for x in sel] + [h["kv_local"][0][p - int(h["local_base"][0])]
                             for p in O.window_positions(int(h["q_pos"][0]), cfg.W, int(h["local_base"][0]),
                                                         h["kv_local"].shape[1])])
             O.sparse_attention(h["q"][0, 0], rows, h["sink"], cfg.softmax_scale)
             elapsed += time.perf_counter() - t0
-        desc = (f"{n} sequence(s), one decode token each (FP8 encode/decode of the {cfg.k} selected entries, attention "
+        desc = (f"{n} sequence(s), one decode token each ({self.FMT} encode/decode of the {cfg.k} selected entries, attention "
                 f"over {cfg.k}+{cfg.W} rows), float64 numpy, {elapsed:.2f} s")
         return n, elapsed, desc
 
 
-WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn}
+class Mxfp4KvAttn(Fp8KvAttn):
+    """The decode attention at 1M over MXFP4 main-KV entries (288 B)."""
+    _shared = {}
+    FMT = "mxfp4"
+
+
+WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
+             11: Mxfp4KvAttn}
 
 
 def config_of(wl):
@@ -775,7 +791,7 @@ def config_of(wl):
                      "replayed as one CUDA graph (a step of each copy), the remaining steps one graph each"))
     c.update(wl.config_extra)
     return c
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400}
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400}
 
 
 # ------------------------------------------------------------------ main

@@ -81,6 +81,9 @@ SIGNATURES = {
                                                        ctypes.POINTER(csa_norm_rope), c_vp]),
     "csa_sparse_attn_fp8kv": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i32, c_vp, c_i64, c_vp, c_vp, c_i64,
                                              c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "csa_kv_pack_mxfp4": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i32, c_vp, c_vp]),
+    "csa_sparse_attn_mxfp4kv": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i32, c_vp, c_i64, c_vp, c_vp,
+                                               c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "csa_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
                                        c_vp]),
 }

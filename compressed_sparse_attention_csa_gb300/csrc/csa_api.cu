@@ -412,6 +412,22 @@ csa_status csa_compress_kv_norm_rope_fp8kv(const csa_config* cfg, int32_t stream
                                  true, stream);
 }
 
+csa_status csa_kv_pack_mxfp4(const csa_config* cfg, const void* x, int64_t rows, int32_t dim, void* out,
+                             csa_stream_t stream) {
+  csa_status st = check_cfg_hca(cfg);
+  if (st != CSA_OK) return st;
+  if (!x || !out) return CSA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(out)) return CSA_ERR_ALIGN;
+  if (rows < 0 || dim < 16 || dim > 1024 || (dim % 16) || ((dim / 2 + dim / 16) % 8)) return CSA_ERR_SHAPE;
+  KvPackArgs a{};
+  a.x = x;
+  a.out = out;
+  a.rows = rows;
+  a.dim = dim;
+  a.bf16 = cfg->act == CSA_BF16;
+  return launch_status(launch_kv_pack_mxfp4(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 csa_status csa_kv_pack_fp8(const csa_config* cfg, const void* x, int64_t rows, int32_t dim, void* out,
                            csa_stream_t stream) {
   csa_status st = check_cfg_hca(cfg);
@@ -695,6 +711,49 @@ csa_status csa_sparse_attn_fp8kv(const csa_config* cfg, const void* q, int32_t T
   a.err = err_word_ptr();
   a.num_sms = sms;
   return launch_status(launch_attn_fp8kv(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_sparse_attn_mxfp4kv(const csa_config* cfg, const void* q, int32_t T, const void* kv_comp, int64_t E_cap,
+                           const int32_t* idx, const void* kv_local, int64_t L, const int64_t* local_base,
+                           const int64_t* q_pos, const float* sink, void* out, float* lse, void* ws,
+                           size_t ws_bytes, csa_stream_t stream) {
+  csa_status st = check_cfg(cfg);
+  if (st != CSA_OK) return st;
+  if (!q || !kv_comp || !idx || !kv_local || !local_base || !q_pos || !sink || !out) return CSA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv_comp) || !aligned16(idx) || !aligned16(kv_local) || !aligned16(local_base) ||
+      !aligned16(q_pos) || !aligned16(sink) || !aligned16(out) || (lse && !aligned16(lse)) || (ws && !aligned16(ws)))
+    return CSA_ERR_ALIGN;
+  const int sms = device_sm_count();
+  if (T < 0 || E_cap < 0 || L < 0 || !attn_shape_ok(cfg) || E_cap * cfg->B >= (int64_t(1) << 31) ||
+      !attn_fp8kv_supported(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms))
+    return CSA_ERR_SHAPE;
+  const size_t need = attn_workspace_bytes(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms);
+  if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
+  AttnArgs a{};
+  a.q = q;
+  a.kv_comp = kv_comp;
+  a.idx = idx;
+  a.kv_local = kv_local;
+  a.local_base = local_base;
+  a.q_pos = q_pos;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.B = cfg->B;
+  a.T = T;
+  a.H = cfg->H;
+  a.d = cfg->d;
+  a.k = cfg->k;
+  a.W = cfg->W;
+  a.E_cap = E_cap;
+  a.L = L;
+  a.softmax_scale = cfg->softmax_scale;
+  a.act = cfg->act;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.err = err_word_ptr();
+  a.num_sms = sms;
+  return launch_status(launch_attn_mxfp4kv(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 namespace {

@@ -83,5 +83,12 @@ cudaError_t launch_kv_pack_fp8(const KvPackArgs& a, cudaStream_t s);
 // the split plan of csa_sparse_attn's decode path (few queries, k + W > 128 rows).
 bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms);
 cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s);
+// The same over MXFP4 main-KV entries (kv_comp [B, E_cap, 288] bytes).
+cudaError_t launch_attn_mxfp4kv(const AttnArgs& a, cudaStream_t s);
+
+// MXFP4 entries: per 16 channels one e4m3 scale = e4m3(amax / 6); codes = the nearest E2M1
+// value of x / scale (ties to the even code, saturating, sign kept); element 2i in the low
+// nibble; the dim/2 payload bytes, then the dim/16 scales.
+cudaError_t launch_kv_pack_mxfp4(const KvPackArgs& a, cudaStream_t s);
 
 }  // namespace csa

@@ -21,6 +21,8 @@
 // order with the sink; prefill runs one CTA per query.
 #include <algorithm>
 
+#include <cuda_fp4.h>
+
 #include "csa_epi.h"
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
@@ -934,6 +936,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
 // FP8 main-KV entries: 448 e4m3 codes (28 chunks of 16) then 64 bf16 (8 chunks of 16).
 constexpr int kFp8Chunks = (kD - 64) / 16;
 constexpr int kFp8RowBytes = (kD - 64) + 64 * 2;
+// MXFP4 main-KV entries: 256 payload bytes (E2M1 nibbles) then 32 e4m3 scales (16 dims each).
+constexpr int kMxRowBytes = kD / 2 + kD / 16;
+
 
 template <int NH>
 struct DecLayout {
@@ -945,7 +950,7 @@ struct DecLayout {
   static constexpr size_t kSmem = 1024 + kMisc + kMiscBytes + kMaxK * 4;
 };
 
-template <int NH, bool FP8KV>
+template <int NH, int KVF>  // KVF: 0 bf16 entries, 1 FP8 entries, 2 MXFP4 entries
 __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs a, const TcAttnSplit sp) {
   using LY = DecLayout<NH>;
   extern __shared__ uint8_t smem_raw[];
@@ -1013,7 +1018,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
   const int n_rows = n_win + n_sel;
   const int row_hi = min(n_rows, row_cap);
   const int nr = row_hi - row_lo;  // rows of this split (<= 0: none)
-  if constexpr (!FP8KV) {
+  if constexpr (KVF == 0) {
     for (int i = tid; i < kRows * 64; i += kTcThreads) {
       const int j = i >> 6, c = i & 63;
       const int lp = row_lo + j;
@@ -1024,7 +1029,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
         cp_async16(dst, kvc + static_cast<int64_t>(sel[lp - n_win]) * kD + c * 8);
       }
     }
-  } else {
+  } else if constexpr (KVF == 1) {
     // FP8 entries (576 B: e4m3 dims 0..447, bf16 dims 448..511): a row is 36 chunks of 16 B;
     // chunk q < 28 holds dims 16q .. 16q+15 as e4m3 (two bf16 chunks of the tile once
     // converted), chunk q >= 28 bf16 dims 448 + 8 (q - 28) .. (copied as they are).  Every
@@ -1080,6 +1085,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
         }
         *reinterpret_cast<uint4*>(sR + ((2 * q) >> 3) * (kRows * 128) + sw128(j, (2 * q) & 7)) = lo;
         *reinterpret_cast<uint4*>(sR + ((2 * q + 1) >> 3) * (kRows * 128) + sw128(j, (2 * q + 1) & 7)) = hi;
+      }
+    }
+  } else {
+    // MXFP4 entries (288 B): payload chunk q (16 B) holds dims 32q .. 32q+31 as E2M1 nibbles
+    // (element 2i in the low nibble), scale bytes 256 + 2q, 2q+1 (e4m3) cover dims 32q .. +15
+    // and 32q+16 .. +31; widened to bf16 (exact: <= 2 + 4 significant bits) into tile chunks
+    // 4q .. 4q+3.  Every load of a thread is issued before the first conversion.
+    constexpr int kQ = kD / 32, kItems = kRows * kQ / kTcThreads;
+    const uint8_t* kvb = static_cast<const uint8_t*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kMxRowBytes;
+    uint4 raw[kItems];
+    uint32_t scb[kItems];
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kTcThreads;
+      const int j = i / kQ, q = i - j * kQ;
+      const int lp = row_lo + j;
+      if (lp >= row_hi) {
+#pragma unroll
+        for (int t4 = 0; t4 < 4; ++t4) {
+          const int c = 4 * q + t4;
+          *reinterpret_cast<uint4*>(sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else if (lp >= n_win) {
+        const uint8_t* src = kvb + static_cast<int64_t>(sel[lp - n_win]) * kMxRowBytes;
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(src + 16 * q));
+        scb[u] = __ldg(reinterpret_cast<const uint16_t*>(src + kD / 2 + 2 * q));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kTcThreads;
+      const int j = i / kQ, q = i - j * kQ;
+      const int lp = row_lo + j;
+      if (lp < row_hi && lp >= n_win) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[u]);
+#pragma unroll
+        for (int t4 = 0; t4 < 4; ++t4) {  // 8 dims = one 32-bit word of nibbles
+          // E2M1 pairs -> half2 (hardware conversion), times the block's e4m3 scale in half2
+          // (exact: at most 2 + 4 significant bits, 2^-10 .. 2688), then bf16 (exact)
+          const __half sc = __half(__nv_cvt_fp8_to_halfraw(
+              static_cast<__nv_fp8_storage_t>(scb[u] >> (8 * (t4 >> 1))), __NV_E4M3));
+          const __half2 sc2 = __half2half2(sc);
+          uint4 o;
+          uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h = __hmul2(
+                __half2(__nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(w[t4] >> (8 * e)), __NV_E2M1)),
+                sc2);
+            const __nv_bfloat162 two = __float22bfloat162_rn(__half22float2(h));
+            ow[e] = *reinterpret_cast<const uint32_t*>(&two);
+          }
+          const int c = 4 * q + t4;
+          *reinterpret_cast<uint4*>(sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7)) = o;
+        }
       }
     }
   }
@@ -1762,19 +1822,19 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
     static bool dattr = false;
     if (!dattr) {
-      cudaFuncSetAttribute(attn_dec_kernel<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_dec_kernel<16, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<16>::kSmem));
-      cudaFuncSetAttribute(attn_dec_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_dec_kernel<32, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<32>::kSmem));
-      cudaFuncSetAttribute(attn_dec_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_dec_kernel<64, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<64>::kSmem));
       dattr = true;
     }
     dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
     cudaError_t e =
-        hg == 4 ? launch_pdl(attn_dec_kernel<16, false>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
-        : hg == 2 ? launch_pdl(attn_dec_kernel<32, false>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
-                  : launch_pdl(attn_dec_kernel<64, false>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
+        hg == 4 ? launch_pdl(attn_dec_kernel<16, 0>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
+        : hg == 2 ? launch_pdl(attn_dec_kernel<32, 0>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
+                  : launch_pdl(attn_dec_kernel<64, 0>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess) return e;
     e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
@@ -1802,7 +1862,8 @@ bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int
   return sp.n_split > 1 && sp.rows_per_split == kRows;
 }
 
-cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s) {
+template <int KVF>
+cudaError_t launch_attn_quantkv(const AttnArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T;
   if (rows == 0) return cudaSuccess;
   if (!attn_fp8kv_supported(a.B, a.T, a.H, a.d, a.k, a.W, a.act, a.num_sms)) return cudaErrorInvalidValue;
@@ -1814,24 +1875,27 @@ cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s) {
   const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
   static bool fattr = false;
   if (!fattr) {
-    cudaFuncSetAttribute(attn_dec_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(attn_dec_kernel<16, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(DecLayout<16>::kSmem));
-    cudaFuncSetAttribute(attn_dec_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(attn_dec_kernel<32, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(DecLayout<32>::kSmem));
-    cudaFuncSetAttribute(attn_dec_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(attn_dec_kernel<64, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(DecLayout<64>::kSmem));
     fattr = true;
   }
   dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
   cudaError_t e =
-      hg == 4 ? launch_pdl(attn_dec_kernel<16, true>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
-      : hg == 2 ? launch_pdl(attn_dec_kernel<32, true>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
-                : launch_pdl(attn_dec_kernel<64, true>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
+      hg == 4 ? launch_pdl(attn_dec_kernel<16, KVF>, grid, dim3(kTcThreads), DecLayout<16>::kSmem, s, a, sp)
+      : hg == 2 ? launch_pdl(attn_dec_kernel<32, KVF>, grid, dim3(kTcThreads), DecLayout<32>::kSmem, s, a, sp)
+                : launch_pdl(attn_dec_kernel<64, KVF>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
   count_launches(1);
   if (e != cudaSuccess) return e;
   e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
   count_launches(1);
   return e;
 }
+
+cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s) { return launch_attn_quantkv<1>(a, s); }
+cudaError_t launch_attn_mxfp4kv(const AttnArgs& a, cudaStream_t s) { return launch_attn_quantkv<2>(a, s); }
 
 }  // namespace csa

@@ -390,7 +390,63 @@ __global__ void __launch_bounds__(32 * kVecWarps) kv_pack_fp8_kernel(const KvPac
   }
 }
 
+// Nearest E2M1 code of v (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; ties to the even code;
+// saturating at 6; bit 3 the sign).
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fminf(fabsf(v), 6.f);
+  uint32_t c;
+  if (a <= 0.25f) c = 0;
+  else if (a < 0.75f) c = 1;
+  else if (a <= 1.25f) c = 2;
+  else if (a < 1.75f) c = 3;
+  else if (a <= 2.5f) c = 4;
+  else if (a < 3.5f) c = 5;
+  else if (a <= 5.f) c = 6;
+  else c = 7;
+  return signbit(v) ? (c | 8u) : c;
+}
+
+// ---- pack rows into MXFP4 entries: one warp a row, lane = a block of 16 channels
+template <typename T>
+__global__ void __launch_bounds__(32 * kVecWarps) kv_pack_mxfp4_kernel(const KvPackArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * kVecWarps + (threadIdx.x >> 5);
+  if (r >= a.rows) return;
+  const int nb = a.dim >> 4;
+  uint8_t* o = static_cast<uint8_t*>(a.out) + r * (a.dim / 2 + nb);
+  for (int blk = lane; blk < nb; blk += 32) {
+    float x[16];
+    load8<T>(static_cast<const T*>(a.x) + r * a.dim + 16 * blk, *reinterpret_cast<float(*)[8]>(x));
+    load8<T>(static_cast<const T*>(a.x) + r * a.dim + 16 * blk + 8, *reinterpret_cast<float(*)[8]>(x + 8));
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(x[i]));
+    const uint8_t sc_code = f_to_e4m3(__fdiv_rn(am, 6.f));
+    const float sc = e4m3_to_f(sc_code);
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t c = sc > 0.f ? e2m1_code(__fdiv_rn(x[i], sc)) : 0u;
+      w[i >> 3] |= c << (4 * (i & 7));
+    }
+    *reinterpret_cast<uint2*>(o + 8 * blk) = make_uint2(w[0], w[1]);
+    o[a.dim / 2 + blk] = sc_code;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_pack_mxfp4(const KvPackArgs& a, cudaStream_t s) {
+  if (a.rows == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((a.rows + kVecWarps - 1) / kVecWarps));
+  const dim3 blk(32 * kVecWarps);
+  const cudaError_t e = a.bf16 ? launch_pdl(kv_pack_mxfp4_kernel<__nv_bfloat16>, grid, blk, 0, s, a)
+                               : launch_pdl(kv_pack_mxfp4_kernel<float>, grid, blk, 0, s, a);
+  count_launches(1);
+  return e;
+}
 
 cudaError_t launch_kv_pack_fp8(const KvPackArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;

@@ -357,3 +357,27 @@ def sparse_attn_fp8kv(cfg: Config, q: torch.Tensor, kv_fp8: torch.Tensor, idx: t
            lib.csa_sparse_attn_fp8kv(ctypes.byref(c), _p(q), T, _p(kv_fp8), kv_fp8.shape[1], _p(idx), _p(kv_local),
                                      kv_local.shape[1], _p(local_base), _p(q_pos), _p(sink), _p(out), _p(lse), wp, wb,
                                      _stream()))
+
+
+def kv_pack_mxfp4(cfg: Config, x: torch.Tensor, out: torch.Tensor) -> None:
+    """csa_kv_pack_mxfp4: rows x [..., dim] in cfg.act -> MXFP4 entries out [..., dim/2 + dim/16] uint8."""
+    lib = L.load()
+    c = cfg.c()
+    dim = x.shape[-1]
+    _check("csa_kv_pack_mxfp4", lib.csa_kv_pack_mxfp4(ctypes.byref(c), _p(x), x.numel() // dim, dim, _p(out),
+                                                      _stream()))
+
+
+def sparse_attn_mxfp4kv(cfg: Config, q: torch.Tensor, kv_mx: torch.Tensor, idx: torch.Tensor, kv_local: torch.Tensor,
+                        local_base: torch.Tensor, q_pos: torch.Tensor, sink: torch.Tensor, out: torch.Tensor,
+                        lse: Optional[torch.Tensor] = None) -> None:
+    """csa_sparse_attn_mxfp4kv: kv_mx [B, E_cap, 288] uint8 MXFP4 entries; the rest as sparse_attn."""
+    lib = L.load()
+    c = cfg.c()
+    B, T = q.shape[0], q.shape[1]
+    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_ATTN, ctypes.byref(c), B * T, T), q.device)
+    wp, wb = _ws_args(ws)
+    _check("csa_sparse_attn_mxfp4kv",
+           lib.csa_sparse_attn_mxfp4kv(ctypes.byref(c), _p(q), T, _p(kv_mx), kv_mx.shape[1], _p(idx), _p(kv_local),
+                                       kv_local.shape[1], _p(local_base), _p(q_pos), _p(sink), _p(out), _p(lse), wp,
+                                       wb, _stream()))

@@ -360,6 +360,26 @@ csa_status csa_sparse_attn_fp8kv(const csa_config *cfg, const void *q, int32_t T
                                  const int64_t *local_base, const int64_t *q_pos, const float *sink,
                                  void *out, float *lse, void *ws, size_t ws_bytes, csa_stream_t stream);
 
+/*
+ * MXFP4 main-KV entries (V4.1 page, section 4: E2M1 payloads with one E4M3 scale per 16
+ * channels, no global scale; 288 bytes for 512 channels): per block of 16 channels the scale
+ * is e4m3_rn_satfinite(amax / 6) and each code the nearest E2M1 value (0, 0.5, 1, 1.5, 2, 3, 4,
+ * 6; ties to the even code, saturating, sign kept) of x / scale, both quotients in binary32
+ * (a zero scale gives zero codes); element 2i sits in the low nibble of payload byte i; bytes
+ * [0, d/2) are the payload, [d/2, d/2 + d/16) the scales.
+ *
+ * csa_kv_pack_mxfp4 — rows x [rows, dim] (cfg->act) -> out [rows, dim/2 + dim/16] bytes;
+ *                     dim % 128 == 0, <= 1024.
+ * csa_sparse_attn_mxfp4kv — csa_sparse_attn_fp8kv over MXFP4 entries (kv_comp [B, E_cap, 288]):
+ *                     the same decode shapes, widened to bf16 in shared memory.
+ */
+csa_status csa_kv_pack_mxfp4(const csa_config *cfg, const void *x, int64_t rows, int32_t dim, void *out,
+                             csa_stream_t stream);
+csa_status csa_sparse_attn_mxfp4kv(const csa_config *cfg, const void *q, int32_t T, const void *kv_comp,
+                                   int64_t E_cap, const int32_t *idx, const void *kv_local, int64_t L,
+                                   const int64_t *local_base, const int64_t *q_pos, const float *sink,
+                                   void *out, float *lse, void *ws, size_t ws_bytes, csa_stream_t stream);
+
 /* All inputs of one decode token per sequence (T = 1). */
 typedef struct {
   int64_t E_cap;             /* rows of kv_comp / kI / kscale per sequence                    */

@@ -173,6 +173,10 @@ CONFIGS: Dict[int, CsaConfig] = {
     10: CsaConfig(10, "V4-Flash CSA decode attention @1M over FP8 main-KV entries (B 4, k 512, W 128)",
                   B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
                   act="bf16", kidx="act", mode="fp8kv_attn"),
+    # the same over V4.1's MXFP4 main-KV entries (E2M1 + one e4m3 scale per 16 channels, 288 B)
+    11: CsaConfig(11, "CSA decode attention @1M over MXFP4 main-KV entries (B 4, k 512, W 128)",
+                  B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
+                  act="bf16", kidx="act", mode="fp8kv_attn"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)

@@ -1,7 +1,8 @@
-"""Parity of the FP8 main-KV entries (448 e4m3 dims + 64 bf16 RoPE dims, 576 B) with the CPU
-oracle: the packer bit-exact, the fused compressor within the e4m3 / bf16 rounding of its
-output, and the decode attention over FP8 entries against the oracle's attention over the
-decoded entries (and bit-identical to the bf16 path over the same decoded values)."""
+"""Parity of the quantised main-KV entries with the CPU oracle: FP8 (448 e4m3 dims + 64 bf16
+RoPE dims, 576 B) and MXFP4 (E2M1 + one e4m3 scale per 16 channels, 288 B).  The packers are
+bit-exact, the fused compressor within the e4m3 / bf16 rounding of its output, and the decode
+attention over quantised entries agrees with the oracle's attention over the decoded entries
+(and is bit-identical to the bf16 path over the same decoded values)."""
 import numpy as np
 import pytest
 import torch
@@ -101,3 +102,41 @@ def test_sparse_attn_fp8kv_rejects_non_decode_shapes():
         csa.sparse_attn_fp8kv(cfg_obj(B=B), q, packed, idx, kl, torch.zeros(B, dtype=torch.int64, device=DEV),
                               torch.arange(T, dtype=torch.int64, device=DEV), sink, out)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("act,dim", [(BF16, 512), (torch.float32, 512), (BF16, 128)])
+def test_kv_pack_mxfp4_bit_exact(act, dim):
+    rows = 257
+    x = rnd(840 + dim, (rows, dim), 1.0, act) * rnd(841 + dim, (rows, 1), 3.0).abs().to(act)
+    x[0, :16] = torch.tensor([6.0, -0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.0, -0.0, 4.0, 3.0, 2.0, 1.0, 0.5, -6.0])
+    x[1, :16] = 0                                       # an all-zero block: scale code 0, zero codes
+    x[2, :16] = 1e-12                                   # a scale that underflows e4m3
+    out = torch.empty(rows, dim // 2 + dim // 16, dtype=torch.uint8, device=DEV)
+    csa.kv_pack_mxfp4(cfg_obj(act=act), x, out)
+    assert csa.get_last_error() == 0
+    assert np.array_equal(out.cpu().numpy(), O.mxfp4_encode(np64(x)))
+
+
+@pytest.mark.parametrize("B,nsel", [(3, [512, 40, 0]), (4, [512])])
+def test_sparse_attn_mxfp4kv_decode(B, nsel):
+    H, d, E, k, W, L, T = 64, 512, 1500, 512, 128, 200, 1
+    q, kv, kl, sink, idx = _attn_inputs(850 + B, B, T, H, d, E, k, L, BF16, nsel)
+    kv = kv * 8.0
+    local_base = torch.tensor([[1000, 1040, 0][b % 3] for b in range(B)], dtype=torch.int64, device=DEV)
+    q_pos = torch.tensor([[1150, 1100, 50][b % 3] for b in range(B)], dtype=torch.int64, device=DEV)
+    c = cfg_obj(B=B)
+    packed = torch.empty(B, E, d // 2 + d // 16, dtype=torch.uint8, device=DEV)
+    csa.kv_pack_mxfp4(c, kv, packed)
+    assert np.array_equal(packed.cpu().numpy(), O.mxfp4_encode(np64(kv)))   # the oracle's own encoding
+    out = torch.empty(B, T, H, d, device=DEV, dtype=BF16)
+    lse = torch.empty(B, T, H, device=DEV)
+    csa.sparse_attn_mxfp4kv(c, q, packed, idx, kl, local_base, q_pos, sink, out, lse)
+    assert csa.get_last_error() == 0
+    dec = torch.from_numpy(O.mxfp4_decode(packed.cpu().numpy())).to(DEV).to(BF16)   # exact in bf16
+    ro, rl = _attn_ref(q, dec, idx, kl, local_base, q_pos, sink, W, d ** -0.5)
+    assert_rows_close(np64(out), ro, 2e-2)
+    np.testing.assert_allclose(np64(lse), rl, atol=5e-3, rtol=0)
+    out_b = torch.empty_like(out)
+    lse_b = torch.empty_like(lse)
+    csa.sparse_attn(c, q, dec, idx, kl, local_base, q_pos, sink, out_b, lse_b)
+    assert torch.equal(out, out_b) and torch.equal(lse, lse_b)

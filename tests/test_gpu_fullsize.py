@@ -9,7 +9,8 @@ their step, exactly as the benchmark times them, then checked against the oracle
   HCA decode @1M (batch 4, 8,192 entries a sequence): every sequence; HCA prefill chunk: the 32
   new entries and sampled query rows; the attention prologue / epilogue of the prefill chunk:
   every new cache entry and sampled tokens of the query and output passes; the decode
-  attention @1M over FP8 main-KV entries: the packed cache bit-exact, every sequence's output.
+  attention @1M over FP8 and over MXFP4 main-KV entries: the packed rows bit-exact, every
+  sequence's output.
 Agreement criteria are those of the small-size parity tests.
 """
 import numpy as np
@@ -22,7 +23,7 @@ from _helpers import (assert_decode_matches, assert_entries_close, assert_out_cl
                       swap_bound)
 from test_gpu_epilogue import assert_vectors_close, e4m3_half_step
 from test_gpu_hca import assert_single_entries_close
-from bench import Csa2Group, Decode, Epilogue, Fp8KvAttn, HcaDecode, HcaPrefill, Prefill
+from bench import Csa2Group, Decode, Epilogue, Fp8KvAttn, HcaDecode, HcaPrefill, Mxfp4KvAttn, Prefill
 from oracle import csa_oracle as O
 from synth import gen
 
@@ -189,17 +190,19 @@ def test_epilogue_full_size_sampled_tokens():
         assert float((np.abs(deq - ref_o) / tol).max()) <= 1.0, f"fp8 output of token {tq}"
 
 
-def test_fp8kv_attention_full_size():
-    cfg = gen.CONFIGS[10]
-    wl = Fp8KvAttn(cfg, csa, torch, DEV, 0)
+@pytest.mark.parametrize("cid,Wl,enc,dec_fn", [(10, Fp8KvAttn, O.kv_fp8_encode, O.kv_fp8_decode),
+                                               (11, Mxfp4KvAttn, O.mxfp4_encode, O.mxfp4_decode)])
+def test_quantised_kv_attention_full_size(cid, Wl, enc, dec_fn):
+    cfg = gen.CONFIGS[cid]
+    wl = Wl(cfg, csa, torch, DEV, 0)
     inp = wl.inp
     replay_once(wl.step)
     for b in range(cfg.B):
         sel = inp["idx"][b].long()
         ent = np64(inp["kv_comp"][b][sel])
-        enc = O.kv_fp8_encode(ent)
-        assert np.array_equal(wl.kv8[b][sel].cpu().numpy(), enc)
-        dec = O.kv_fp8_decode(enc)
+        code = enc(ent)
+        assert np.array_equal(wl.kv8[b][sel].cpu().numpy(), code)
+        dec = dec_fn(code)
         lb, t = int(inp["local_base"][b]), int(inp["q_pos"][b])
         kl = np64(inp["kv_local"][b])
         rows = np.concatenate([dec, np.stack([kl[p - lb] for p in O.window_positions(t, cfg.W, lb, kl.shape[0])])])
