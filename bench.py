@@ -232,6 +232,7 @@ class Decode:
                          z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
                          biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"],
                          out=self.out, lse=self.lse, idx_out=self.idx)
+        self.call = None   # the step's arguments, marshalled at the first call
         from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
         work = decode_step_work(cfg)
         self.stage_label = "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<%s>" % (
@@ -245,7 +246,9 @@ class Decode:
         self.e2e_out = self.out
 
     def step(self):
-        self.csa.decode_step(self.c, **self.args)
+        if self.call is None:
+            self.call = self.csa.DecodeStepCall(self.c, **self.args)
+        self.call()
 
     def stage_fn(self):
         inp = self.inp
@@ -483,6 +486,7 @@ class HcaDecode:
         self.args = dict(q_pos=inp["q_pos"], q=inp["q"], sink=inp["sink"], kv_comp=inp["kv_comp"],
                          kv_tail=inp["kv_str"], z_tail=inp["z_str"], bias=inp["bias"], kv_local=inp["kv_local"],
                          local_base=inp["local_base"], out=self.out, lse=self.lse)
+        self.call = None
         from compressed_sparse_attention_csa_gb300.accounting import hca_decode_work
         work = hca_decode_work(cfg)
         self.stage_label = ("dense attention: attn_hca_dec_kernel (rows split over CTAs, two TMA passes) + "
@@ -495,7 +499,9 @@ class HcaDecode:
         self.e2e_out = self.out
 
     def step(self):
-        self.csa.hca_decode_step(self.c, **self.args)
+        if self.call is None:
+            self.call = self.csa.HcaDecodeStepCall(self.c, **self.args)
+        self.call()
 
     def stage_fn(self):
         inp = self.inp

@@ -381,3 +381,50 @@ def sparse_attn_mxfp4kv(cfg: Config, q: torch.Tensor, kv_mx: torch.Tensor, idx: 
            lib.csa_sparse_attn_mxfp4kv(ctypes.byref(c), _p(q), T, _p(kv_mx), kv_mx.shape[1], _p(idx), _p(kv_local),
                                        kv_local.shape[1], _p(local_base), _p(q_pos), _p(sink), _p(out), _p(lse), wp,
                                        wb, _stream()))
+
+
+class DecodeStepCall:
+    """csa_decode_step with its arguments marshalled once: for a decode loop that keeps its
+    buffers (caches, tails, window rows, outputs) fixed and rewrites their contents each step.
+    Calling the object enqueues one step on the current stream."""
+
+    def __init__(self, cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
+                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None):
+        self._lib = L.load()
+        self._c = cfg.c()
+        self._a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
+                                    _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias),
+                                    _p(biasI), _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse),
+                                    _p(idx_out))
+        nbytes = self._lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(self._c), cfg.B, kv_comp.shape[1])
+        if nbytes == ctypes.c_size_t(-1).value:
+            raise CsaError("csa_workspace_size", 2)
+        self._ws = _decode_workspace(nbytes, q.device, cfg.B)
+        self._wp, self._wb = _ws_args(self._ws)
+        self._refs = (q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias, biasI, kv_local,
+                      local_base, out, kscale, lse, idx_out)   # keep the buffers alive
+        self._cref, self._aref = ctypes.byref(self._c), ctypes.byref(self._a)
+
+    def __call__(self) -> None:
+        _check("csa_decode_step", self._lib.csa_decode_step(self._cref, self._aref, self._wp, self._wb, _stream()))
+
+
+class HcaDecodeStepCall:
+    """csa_hca_decode_step with its arguments marshalled once (see DecodeStepCall)."""
+
+    def __init__(self, cfg: Config, *, q_pos, q, sink, kv_comp, kv_tail, z_tail, bias, kv_local, local_base, out,
+                 lse=None):
+        self._lib = L.load()
+        self._c = cfg.c()
+        self._a = L.csa_hca_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(sink), _p(kv_comp), _p(kv_tail),
+                                        _p(z_tail), _p(bias), _p(kv_local), kv_local.shape[1], _p(local_base), _p(out),
+                                        _p(lse))
+        self._ws = _workspace(self._lib.csa_workspace_size(L.CSA_OP_HCA_DECODE, ctypes.byref(self._c), cfg.B,
+                                                           kv_comp.shape[1]), q.device)
+        self._wp, self._wb = _ws_args(self._ws)
+        self._refs = (q_pos, q, sink, kv_comp, kv_tail, z_tail, bias, kv_local, local_base, out, lse)
+        self._cref, self._aref = ctypes.byref(self._c), ctypes.byref(self._a)
+
+    def __call__(self) -> None:
+        _check("csa_hca_decode_step",
+               self._lib.csa_hca_decode_step(self._cref, self._aref, self._wp, self._wb, _stream()))

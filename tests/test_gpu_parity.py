@@ -495,3 +495,28 @@ def test_csa2_group_matches_oracle():
             bound = swap_bound(nb["q"][layer][b, 0], rl, cfg.softmax_scale,
                                [nb["kv_comp"][b][x] for x in g_set - r_set], [nb["kv_comp"][b][y] for y in r_set - g_set])
             assert_out_close_with_swaps(np64(outs[layer][b, 0]), ro, 2e-2, bound, what=f"layer {layer} b={b}")
+
+
+def test_decode_step_call_matches_decode_step():
+    """The prepared decode-step call enqueues exactly what decode_step does."""
+    cfg = gen.CONFIGS[2].replace(B=2, N=4 * 900)
+    inp = gen.make_inputs(cfg, DEV)
+    c = lib_config(cfg)
+    kwargs = dict(q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"], kv_comp=inp["kv_comp"],
+                  kI=inp["kI"], kv_tail=inp["kv_str"], z_tail=inp["z_str"], kvI_tail=inp["kvI_str"],
+                  zI_tail=inp["zI_str"], bias=inp["bias"], biasI=inp["biasI"], kv_local=inp["kv_local"],
+                  local_base=inp["local_base"])
+    outs = []
+    for prepared in (False, True):
+        out = torch.empty(cfg.B, cfg.H, cfg.d, device=DEV, dtype=BF16)
+        lse = torch.empty(cfg.B, cfg.H, device=DEV)
+        idx = torch.empty(cfg.B, cfg.k, dtype=torch.int32, device=DEV)
+        if prepared:
+            call = csa.DecodeStepCall(c, out=out, lse=lse, idx_out=idx, **kwargs)
+            call()
+            call()
+        else:
+            csa.decode_step(c, out=out, lse=lse, idx_out=idx, **kwargs)
+        check_dev_error()
+        outs.append((out, lse, idx))
+    assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
