@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11, 12])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,6 +83,7 @@ _INDEXER_STAGE = (("indexer_qprep_kernel", "indexer_tc_kernel"), ("k_indexer.cu"
 _DENSE_STAGE = (("attn_hca_dec_kernel", "attn_merge_wide_kernel"), ("k_attn.cu", "csa_ptx.cuh", "csa_internal.h"))
 # config -> (summary file, kernels of the stage, sources the summary's counters were taken with)
 STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
+                  12: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
                   2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE,
                   3: ("indexer_tc_bf16_prefill_4K.md",) + _INDEXER_STAGE,
                   5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE,
@@ -203,19 +204,25 @@ def _host64(x):
 
 
 class Decode:
+    FP8KV = False   # main-KV entries stored as FP8 entries (576 B)
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
         self.units = cfg.B
-        self.metric = "CSA decode tok/s @1M ctx" if cfg.cid == 4 else "CSA decode tok/s @64K ctx"
+        self.metric = "CSA decode tok/s @1M ctx" if cfg.N == 1 << 20 else "CSA decode tok/s @64K ctx"
+        if self.FP8KV:
+            self.metric += ", FP8 main-KV entries"
         self.workload = (f"V4-Flash CSA decode step, batch {cfg.B} @ {cfg.N:,}-token context "
                          f"({cfg.E:,} entries/seq), " +
                          ("FP8 e4m3 indexer keys + fp32 scale" if cfg.kidx == "fp8" else "bf16 indexer keys") +
-                         f", bf16 KV, {cfg.H}x{cfg.d} heads, indexer {cfg.HI}x{cfg.dI}, k {cfg.k}, W {cfg.W}")
+                         (", FP8 main-KV entries (448 e4m3 + 64 bf16 dims, 576 B)" if self.FP8KV else ", bf16 KV") +
+                         f", {cfg.H}x{cfg.d} heads, indexer {cfg.HI}x{cfg.dI}, k {cfg.k}, W {cfg.W}")
         self.config_extra = {"batch": cfg.B, "context": cfg.N, "m": cfg.m, "entries_per_seq": cfg.E,
                              "heads": cfg.H, "head_dim": cfg.d, "indexer": f"{cfg.HI}x{cfg.dI}", "top_k": cfg.k,
                              "window": cfg.W,
-                             "indexer_keys": "e4m3+fp32 scale" if cfg.kidx == "fp8" else "bf16"}
+                             "indexer_keys": "e4m3+fp32 scale" if cfg.kidx == "fp8" else "bf16",
+                             "kv_entries": "FP8 (576 B)" if self.FP8KV else "bf16 (1 KiB)"}
         if host_only:
             return
         self.csa = csa
@@ -227,14 +234,18 @@ class Decode:
         self.lse = torch.empty(cfg.B, cfg.H, device=dev)
         self.idx = torch.empty(cfg.B, cfg.k, device=dev, dtype=torch.int32)
         self.scores = torch.empty(cfg.B, cfg.E, device=dev)
+        if self.FP8KV:
+            self.kv8 = torch.empty(cfg.B, cfg.E, cfg.d + 64, dtype=torch.uint8, device=dev)
+            csa.kv_pack_fp8(self.c, inp["kv_comp"], self.kv8)
         self.args = dict(q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"],
-                         kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
+                         kv_comp=self.kv8 if self.FP8KV else inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"),
+                         kv_tail=inp["kv_str"],
                          z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
                          biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"],
                          out=self.out, lse=self.lse, idx_out=self.idx)
         self.call = None   # the step's arguments, marshalled at the first call
         from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
-        work = decode_step_work(cfg)
+        work = decode_step_work(cfg, kv_entry_bytes=cfg.d - 64 + 128 if self.FP8KV else None)
         self.stage_label = "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<%s>" % (
             "e4m3" if cfg.kidx == "fp8" else "bf16")
         self.stage_bound = "hbm"
@@ -247,7 +258,7 @@ class Decode:
 
     def step(self):
         if self.call is None:
-            self.call = self.csa.DecodeStepCall(self.c, **self.args)
+            self.call = self.csa.DecodeStepCall(self.c, fp8kv=self.FP8KV, **self.args)
         self.call()
 
     def stage_fn(self):
@@ -786,7 +797,12 @@ class Mxfp4KvAttn(Fp8KvAttn):
     FMT = "mxfp4"
 
 
-WORKLOADS = {2: Decode, 4: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
+class Fp8KvDecode(Decode):
+    """The decode step over FP8 main-KV entries (V4's production precision with FP8 keys)."""
+    FP8KV = True
+
+
+WORKLOADS = {2: Decode, 4: Decode, 12: Fp8KvDecode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
              11: Mxfp4KvAttn}
 
 
@@ -797,7 +813,7 @@ def config_of(wl):
                      "replayed as one CUDA graph (a step of each copy), the remaining steps one graph each"))
     c.update(wl.config_extra)
     return c
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400}
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400, 12: 12}
 
 
 # ------------------------------------------------------------------ main

@@ -86,6 +86,8 @@ SIGNATURES = {
                                                c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "csa_decode_step": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
                                        c_vp]),
+    "csa_decode_step_fp8kv": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
+                                             c_vp]),
 }
 
 _lib = None

@@ -26,11 +26,12 @@ def indexer_key_bytes(cfg) -> int:
     return cfg.dI * _act_bytes(cfg.act)
 
 
-def decode_step_work(cfg) -> Dict[str, float]:
+def decode_step_work(cfg, kv_entry_bytes=None) -> Dict[str, float]:
     """Per-step algorithmic bytes/flops of a decode workload (T queries per sequence).
 
     indexer: every visible key once, qI and w once per query.
-    attention: q and out once; each of the k selected entries and W window rows once.
+    attention: q and out once; each of the k selected entries (kv_entry_bytes each: a stored
+    format's size, default d activations) and W window rows once.
     compression: for a decode step, the 2m stream tokens (kv and gate, both streams, main
     and indexer dims) of the completed block and the two entries written.
     """
@@ -40,11 +41,13 @@ def decode_step_work(cfg) -> Dict[str, float]:
     key_b = indexer_key_bytes(cfg)
     idx_bytes = B * nv * key_b + B * T * cfg.HI * (cfg.dI * ab + 4)
     rows = min(cfg.k, nv) + cfg.W
-    attn_bytes = B * T * (rows * cfg.d * ab + 2 * cfg.H * cfg.d * ab + cfg.k * 4)
+    entry_b = kv_entry_bytes if kv_entry_bytes is not None else cfg.d * ab
+    sel = min(cfg.k, nv)
+    attn_bytes = B * T * (sel * entry_b + cfg.W * cfg.d * ab + 2 * cfg.H * cfg.d * ab + cfg.k * 4)
     comp_bytes = 0
     if cfg.mode == "decode":
         comp_bytes = B * (2 * cfg.m * 2 * 2 * (cfg.d + cfg.dI) * ab
-                          + cfg.d * ab + key_b)
+                          + entry_b + key_b)
     idx_flops = 2 * indexer_macs(cfg.HI, cfg.dI, nv) * B * T
     attn_flops = 4 * cfg.H * cfg.d * rows * B * T
     return {

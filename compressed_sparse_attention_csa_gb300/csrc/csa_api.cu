@@ -847,8 +847,9 @@ csa_status csa_hca_decode_step(const csa_config* cfg, const csa_hca_decode_args*
   return launch_status(launch_attn(a, s));
 }
 
-csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
-                           csa_stream_t stream) {
+namespace {
+csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
+                            csa_stream_t stream, bool fp8kv) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!d) return CSA_ERR_NULL;
@@ -867,6 +868,9 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
       cfg->HI > 128 || d->E_cap * cfg->B >= (int64_t(1) << 31))
     return CSA_ERR_SHAPE;
   const int sms = device_sm_count();
+  if (fp8kv && !(cfg->act == CSA_BF16 && cfg->d == 512 && cfg->m <= 8 &&
+                 attn_fp8kv_supported(cfg->B, 1, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms)))
+    return CSA_ERR_SHAPE;
   if (!ws || ws_bytes < decode_ws(cfg, d->E_cap, sms)) return CSA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* err = err_word_ptr();
@@ -925,6 +929,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
     f.zI_tail = d->zI_tail;
     f.biasI = d->biasI;
     f.act_bf16 = cfg->act == CSA_BF16;
+    f.kv_fp8 = fp8kv;
     f.hist = hist_cnt;
     ia.images_ready = true;
     e = launch_indexer(ia, s);
@@ -932,6 +937,7 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
     e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   } else {
+    if (fp8kv) return CSA_ERR_SHAPE;  // FP8 entries: the fused path only
     // 1. compress the block the new token completes (main KV, then indexer keys)
     CompressArgs c{};
     c.B = cfg->B;
@@ -988,7 +994,18 @@ csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void
   aa.ws = ws_attn;
   aa.err = err;
   aa.num_sms = sms;
-  return launch_status(launch_attn(aa, s));
+  return launch_status(fp8kv ? launch_attn_fp8kv(aa, s) : launch_attn(aa, s));
+}
+}  // namespace
+
+csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
+                           csa_stream_t stream) {
+  return decode_step_impl(cfg, d, ws, ws_bytes, stream, false);
+}
+
+csa_status csa_decode_step_fp8kv(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
+                                 csa_stream_t stream) {
+  return decode_step_impl(cfg, d, ws, ws_bytes, stream, true);
 }
 
 }  // extern "C"

@@ -72,6 +72,7 @@ struct DecodeFuse {
   const void* zI_tail;
   const float* biasI;    // [2, m, dI]
   bool act_bf16;         // stream and kv_comp dtype
+  bool kv_fp8;           // kv_comp holds FP8 main-KV entries: d - 64 e4m3 codes, then 64 bf16 dims
   uint32_t* hist;        // histograms + tickets
 };
 inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + B; }

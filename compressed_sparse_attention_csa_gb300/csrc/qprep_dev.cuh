@@ -180,6 +180,19 @@ __device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64
                          f.bias, f.act_bf16, m, d, c, e > 0, o);
     v[n] = o[0];
   }
+  if (f.kv_fp8) {  // FP8 main-KV entry: e4m3 codes of dims < d - 64, then the last 64 in bf16
+    uint8_t* row8 = static_cast<uint8_t*>(f.kv_comp) + (static_cast<int64_t>(b) * a.E_cap + e) * (d + 64);
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      const int ch = t256 + 256 * n;
+      if (ch >= d) continue;
+      if (ch < d - 64)
+        row8[ch] = f_to_e4m3(v[n]);
+      else
+        reinterpret_cast<__nv_bfloat16*>(row8 + d - 64)[ch - (d - 64)] = __float2bfloat16_rn(v[n]);
+    }
+    return;
+  }
   const int64_t row = (static_cast<int64_t>(b) * a.E_cap + e) * d;
 #pragma unroll
   for (int n = 0; n < 2; ++n) {

@@ -230,8 +230,9 @@ def sparse_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, idx: torch.
 
 
 def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
-                biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None) -> None:
-    """csa_decode_step: one token per sequence (T = 1); caches are updated in place."""
+                biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, fp8kv: bool = False) -> None:
+    """csa_decode_step (csa_decode_step_fp8kv with fp8kv: kv_comp [B, E_cap, 576] uint8 FP8
+    entries): one token per sequence (T = 1); caches are updated in place."""
     lib = L.load()
     c = cfg.c()
     a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
@@ -241,7 +242,8 @@ def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_t
     if nbytes == ctypes.c_size_t(-1).value:
         raise CsaError("csa_workspace_size", 2)
     wp, wb = _ws_args(_decode_workspace(nbytes, q.device, cfg.B))
-    _check("csa_decode_step", lib.csa_decode_step(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))
+    fn = lib.csa_decode_step_fp8kv if fp8kv else lib.csa_decode_step
+    _check("csa_decode_step", fn(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))
 
 
 def dense_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, kv_local: torch.Tensor, local_base: torch.Tensor,
@@ -389,8 +391,9 @@ class DecodeStepCall:
     Calling the object enqueues one step on the current stream."""
 
     def __init__(self, cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
-                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None):
+                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, fp8kv: bool = False):
         self._lib = L.load()
+        self._fn = self._lib.csa_decode_step_fp8kv if fp8kv else self._lib.csa_decode_step
         self._c = cfg.c()
         self._a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                                     _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias),
@@ -406,7 +409,7 @@ class DecodeStepCall:
         self._cref, self._aref = ctypes.byref(self._c), ctypes.byref(self._a)
 
     def __call__(self) -> None:
-        _check("csa_decode_step", self._lib.csa_decode_step(self._cref, self._aref, self._wp, self._wb, _stream()))
+        _check("csa_decode_step", self._fn(self._cref, self._aref, self._wp, self._wb, _stream()))
 
 
 class HcaDecodeStepCall:

@@ -420,6 +420,16 @@ typedef struct {
 csa_status csa_decode_step(const csa_config *cfg, const csa_decode_args *args, void *ws,
                            size_t ws_bytes, csa_stream_t stream);
 
+/*
+ * csa_decode_step_fp8kv — csa_decode_step over a main-KV cache of FP8 entries (kv_comp
+ * [B, E_cap, 576] bytes, the format of csa_kv_pack_fp8): the entry the token completes is
+ * written as an FP8 entry and the attention reads FP8 entries.  bf16, d == 512, m <= 8, the
+ * tensor-core indexer and the decode split plan (see csa_sparse_attn_fp8kv); CSA_ERR_SHAPE
+ * otherwise.  Same workspace as csa_decode_step.
+ */
+csa_status csa_decode_step_fp8kv(const csa_config *cfg, const csa_decode_args *args, void *ws,
+                                 size_t ws_bytes, csa_stream_t stream);
+
 /* Synchronise `stream`, then return and clear the first device-side error recorded since the
  * last call (CSA_OK if none; CSA_ERR_CUDA if the stream itself reports an error). */
 csa_status csa_get_last_error(csa_stream_t stream);

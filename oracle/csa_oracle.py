@@ -364,13 +364,14 @@ def decode_token(cfg, inp: Dict[str, np.ndarray], b: int, tq: int,
 
 
 def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.ndarray,
-                         kI_deq: np.ndarray, fp8_keys: bool = False) -> Dict[str, np.ndarray]:
+                         kI_deq: np.ndarray, fp8_keys: bool = False, fp8_kv: bool = False) -> Dict[str, np.ndarray]:
     """One decode token of sequence b (T = 1).
 
     When the token at t completes a block ((t + 1) % m == 0), entry (t + 1)/m - 1 is
     compressed from the tail streams (rows = tokens t-2m+1 .. t) into the caches kv_comp
     [E, d] and kI_deq [E, dI] (updated in place; FP8 keys are stored as e4m3 codes with one
-    fp32 scale and read back dequantised); then indexer -> top-k -> attention.
+    fp32 scale and read back dequantised; with fp8_kv the main-KV entry is stored as an FP8
+    entry and read back decoded); then indexer -> top-k -> attention.
     """
     t = int(inp["q_pos"][b])
     entry = None
@@ -378,6 +379,8 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
         e = (t + 1) // cfg.m - 1
         tok0 = t - 2 * cfg.m + 1
         kv_comp[e] = compress_entry(inp["kv_str"][b], inp["z_str"][b], inp["bias"], cfg.m, e, tok0)
+        if fp8_kv:   # kv_comp holds the cache as stored: FP8 entries, read back decoded
+            kv_comp[e] = kv_fp8_decode(kv_fp8_encode(kv_comp[e]))
         ki = compress_entry(inp["kvI_str"][b], inp["zI_str"][b], inp["biasI"], cfg.m, e, tok0)
         if fp8_keys:
             codes, sc = quantize_rows_e4m3(ki.astype(np.float32)[None, :])

@@ -177,6 +177,10 @@ CONFIGS: Dict[int, CsaConfig] = {
     11: CsaConfig(11, "CSA decode attention @1M over MXFP4 main-KV entries (B 4, k 512, W 128)",
                   B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
                   act="bf16", kidx="act", mode="fp8kv_attn"),
+    # the 1M decode step at V4's production precision: FP8 indexer keys and FP8 main-KV entries
+    12: CsaConfig(12, "V4-Flash CSA decode @1M ctx, FP8 indexer keys + FP8 main-KV entries (576 B)",
+                  B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
+                  act="bf16", kidx="fp8", mode="decode"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)

@@ -140,3 +140,59 @@ def test_sparse_attn_mxfp4kv_decode(B, nsel):
     lse_b = torch.empty_like(lse)
     csa.sparse_attn(c, q, dec, idx, kl, local_base, q_pos, sink, out_b, lse_b)
     assert torch.equal(out, out_b) and torch.equal(lse, lse_b)
+
+
+@pytest.mark.parametrize("cid,N", [(4, 4 * 2500), (2, 4 * 1500)])
+def test_decode_step_fp8kv_matches_oracle(cid, N):
+    """The full decode step over an FP8-entry main-KV cache: the entry the token completes is
+    stored as an FP8 entry, the attention reads FP8 entries (oracle: the same on the decoded
+    cache)."""
+    from _helpers import (assert_out_close_with_swaps, assert_selection_ok, keys_f64, lib_config, np_inputs,
+                          swap_bound)
+    cfg = gen.CONFIGS[cid].replace(B=3, N=N)
+    inp = gen.make_inputs(cfg, DEV)
+    inp["q_pos"][1] = N - 3                          # this token completes no block
+    c = lib_config(cfg)
+    kv8 = torch.empty(cfg.B, cfg.E, cfg.d + 64, dtype=torch.uint8, device=DEV)
+    csa.kv_pack_fp8(c, inp["kv_comp"], kv8)
+    assert np.array_equal(kv8.cpu().numpy(), O.kv_fp8_encode(np64(inp["kv_comp"])))
+    dec_cache = O.kv_fp8_decode(kv8.cpu().numpy())
+    nb = np_inputs(inp)
+    fp8k = cfg.kidx == "fp8"
+    refs = []
+    for b in range(cfg.B):
+        kdeq = keys_f64(inp["kI"][b], inp["kscale"][b] if fp8k else None)
+        kvc = dec_cache[b].copy()
+        r = O.decode_step_sequence(cfg, nb, b, kvc, kdeq, fp8_keys=fp8k, fp8_kv=True)
+        r["kv_comp"] = kvc
+        refs.append(r)
+    before = kv8.clone()
+    out = torch.empty(cfg.B, cfg.H, cfg.d, device=DEV, dtype=BF16)
+    lse = torch.empty(cfg.B, cfg.H, device=DEV)
+    idx = torch.empty(cfg.B, cfg.k, dtype=torch.int32, device=DEV)
+    csa.decode_step(c, q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"], kv_comp=kv8,
+                    kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"], z_tail=inp["z_str"],
+                    kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"], biasI=inp["biasI"],
+                    kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse, idx_out=idx, fp8kv=True)
+    assert csa.get_last_error() == 0
+    rtol_s = 5e-2 if fp8k else 1e-2
+    for b in range(cfg.B):
+        r = refs[b]
+        if r["entry"] is None:
+            assert torch.equal(kv8[b], before[b])
+        else:
+            e, ent, _ = r["entry"]
+            got = O.kv_fp8_decode(kv8[b, e].cpu().numpy())
+            exact = O.compress_entry(nb["kv_str"][b], nb["z_str"][b], nb["bias"], cfg.m, e, int(nb["q_pos"][b]) - 2 * cfg.m + 1)
+            tol = 1.01 * e4m3_half_step(exact[:448]) + 1e-6 * np.abs(exact).max()
+            assert np.all(np.abs(got[:448] - exact[:448]) <= tol), f"FP8 part of the new entry b={b}"
+            assert_vectors_close(got[448:][None], exact[448:][None], BF16, f"bf16 part of the new entry b={b}")
+        fin = r["scores"][np.isfinite(r["scores"])]
+        tol_s = rtol_s * max(np.sqrt((fin ** 2).mean()), 1e-30)
+        gi = idx[b].cpu().numpy()
+        swaps = assert_selection_ok(gi, r["idx"], r["scores"], cfg.k, tol_s)
+        g_set, r_set = set(gi[gi >= 0].tolist()), set(r["idx"][r["idx"] >= 0].tolist())
+        bound = swap_bound(r["q"] if "q" in r else nb["q"][b, 0], r["lse"], cfg.softmax_scale,
+                           [r["kv_comp"][x] for x in g_set - r_set], [r["kv_comp"][y] for y in r_set - g_set])
+        assert_out_close_with_swaps(np64(out[b]), r["out"], 2e-2, bound, what=f"out b={b} swaps={swaps}")
+        np.testing.assert_allclose(np64(lse[b]), r["lse"], atol=5e-3)
