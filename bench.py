@@ -80,13 +80,15 @@ def peaks():
 
 
 _INDEXER_STAGE = (("indexer_qprep_kernel", "indexer_tc_kernel"), ("k_indexer.cu", "csa_ptx.cuh", "csa_internal.h"))
+# one query per sequence: the indexer CTAs build the query image themselves (no query-prep launch)
+_INDEXER_STAGE_1Q = (("indexer_tc_kernel",), _INDEXER_STAGE[1])
 _DENSE_STAGE = (("attn_hca_dec_kernel", "attn_merge_wide_kernel"), ("k_attn.cu", "csa_ptx.cuh", "csa_internal.h"))
 # config -> (summary file, kernels of the stage, sources the summary's counters were taken with)
-STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
-                  12: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE,
-                  2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE,
+STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE_1Q,
+                  12: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE_1Q,
+                  2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE_1Q,
                   3: ("indexer_tc_bf16_prefill_4K.md",) + _INDEXER_STAGE,
-                  5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE,
+                  5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE_1Q,
                   6: ("hca_dense_attn_1M_decode.md",) + _DENSE_STAGE,
                   7: ("hca_dense_attn_prefill_4K.md", ("attn_pf_kernel",), _DENSE_STAGE[1]),
                   9: ("epilogue_norm_rope_prefill_4K.md", ("norm_rope_kernel",),
@@ -246,7 +248,7 @@ class Decode:
         self.call = None   # the step's arguments, marshalled at the first call
         from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
         work = decode_step_work(cfg, kv_entry_bytes=cfg.d - 64 + 128 if self.FP8KV else None)
-        self.stage_label = "indexer stage: indexer_qprep_kernel + indexer_tc_kernel<%s>" % (
+        self.stage_label = "indexer stage: indexer_tc_kernel<%s> (query image built in each CTA)" % (
             "e4m3" if cfg.kidx == "fp8" else "bf16")
         self.stage_bound = "hbm"
         self.stage_amount = work["indexer_bytes"] + cfg.B * cfg.E * 4   # + the fp32 scores written
@@ -410,7 +412,7 @@ class Csa2Group:
         from compressed_sparse_attention_csa_gb300.accounting import csa2_group_work
         work = csa2_group_work(cfg, self.N_BLOCKS, 8, self.layers)
         self.work = work
-        self.stage_label = "Full-layer scan, indexer stage: indexer_qprep_kernel + indexer_tc_kernel<bf16>"
+        self.stage_label = "Full-layer scan, indexer stage: indexer_tc_kernel<bf16> (query image built in each CTA)"
         self.stage_bound = "hbm"
         self.stage_amount = work["scan_bytes"] + B * E * 4
         self.step_bytes = work["bytes"]

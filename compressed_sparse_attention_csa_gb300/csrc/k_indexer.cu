@@ -13,7 +13,8 @@
 // epilogue.  Key tiles stream through a TMA ring (evict-first); one thread issues the MMAs
 // into a ring of TMEM accumulators; two groups of four epilogue warps take alternate tiles.
 // The query operand of each query group is prepared once (indexer_qprep_kernel) as the
-// exact shared-memory image, and every CTA of the group pulls it with one bulk copy.
+// exact shared-memory image, and every CTA of the group pulls it with one bulk copy; with one
+// query per sequence and the key range split over CTAs, each CTA builds the image itself.
 //
 // E4M3 keys use kind::f8f6f4.  The query is split into two E4M3 terms, q/s = hi + lo with
 // s = per-head amax/448, and both terms run through the same accumulator (the K loop is
@@ -85,6 +86,12 @@ constexpr int kMaxG = 8;
 constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
 
 using TcLayout = IndexerLayout;
+
+// One query per sequence over dense keys (two CTAs per SM, the key range split): every CTA
+// converts the query itself (16 KiB read from L2) instead of waiting for a query-prep launch.
+__host__ __device__ __forceinline__ bool image_in_cta(const IndexerArgs& a, const TcLayout& L) {
+  return !L.wide && a.T == 1 && a.cand == nullptr;
+}
 
 __device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
   float* sRed4 = reinterpret_cast<float*>(sTmem + 8);        // [4] decode step: key amax
   uint32_t* sHist = sTmem + 12;                               // [4096] when a histogram is kept (G == 1)
   constexpr bool fuse = FUSE;  // decode step: see DecodeFuse
+  const bool img_cta = FUSE || image_in_cta(a, L);  // the epilogue warps write the query image
   const bool hist = (a.hist_out != nullptr || fuse) && G == 1;
   const int NA = L.n_acc;
 
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 32 * 4 * gpt);
     }
-    mbar_init(qbar, fuse ? 32 * EPI : 1);
+    mbar_init(qbar, img_cta ? 32 * EPI : 1);
     mbar_init(kbar, 1);
     fence_mbar_init();
   }
@@ -316,9 +324,9 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // the group's query image (B operand + gates): one bulk copy, or (decode step) written
-      // by the epilogue warps
-      if (!fuse) {
+      // the group's query image (B operand + gates): one bulk copy, or (one query per
+      // sequence) written by the epilogue warps
+      if (!img_cta) {
         const uint8_t* img = images + (static_cast<size_t>(b) * L.n_qgroups + qg) * (L.b_bytes + L.w_bytes);
         mbar_arrive_expect_tx(qbar, L.b_bytes + L.w_bytes);
         bulk_g2s(sB, img, L.b_bytes, qbar);
@@ -358,7 +366,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
         }
         if (committed > 0) wait_time_only(&tfull[(committed - 1) % NA], ((committed - 1) / NA) & 1);
       }
-      if (!q_ok && !fuse) wait_time_only(qbar, 0);  // the image copy must land before the CTA exits
+      if (!q_ok && !img_cta) wait_time_only(qbar, 0);  // the image copy must land before the CTA exits
     }
   } else {
     // ---- epilogue: group gp (0/1) takes tiles gp, gp + 2, ...; warp (warp & 3) owns TMEM
@@ -370,10 +378,12 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
     const int g_lo = gpt == 2 ? ch * gh : 0, g_hi = gpt == 2 ? min(G, g_lo + gh) : G;
     const int rin = q * 32 + lane;
     uint32_t* hist_row = hist ? a.hist_out + qrow0 * kTopkHistRowWords : nullptr;
-    if constexpr (FUSE) {
+    if (img_cta) {
       build_image_cta<FP8>(a, L, sB, b, tid - 64);
       fence_proxy_async_smem();
       mbar_arrive(qbar);
+    }
+    if constexpr (FUSE) {
       hist_row = a.fuse.hist + static_cast<size_t>(b) * kTopkHistRowWords;
       // the new key entry, if this CTA scores it (first epilogue group, one channel a thread)
       const bool own_new =
@@ -538,7 +548,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
       return cudaErrorInvalidValue;
     uint8_t* images = static_cast<uint8_t*>(a.ws);
     cudaError_t e = cudaSuccess;
-    if (!a.images_ready) {
+    if (!a.images_ready && !image_in_cta(a, L)) {
       dim3 gq(L.n_qgroups, a.B, (L.N + 7) / 8);
       e = fp8 ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
               : launch_pdl(indexer_qprep_kernel<false>, gq, dim3(256), 0, s, a, L, images);
