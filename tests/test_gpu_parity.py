@@ -101,6 +101,8 @@ def _indexer_ref(qI, w, q_pos, kdeq, m, T):
 
 @pytest.mark.parametrize("HI,T,fp8", [(64, 1, False), (64, 37, False), (32, 21, False), (64, 1, True),
                                       (64, 9, True),
+                                      # one query per sequence: the CTAs build the query image
+                                      (32, 1, True), (128, 1, False), (128, 1, True),
                                       # enough query groups for one CTA per SM over the whole key range
                                       (64, 700, False), (32, 700, False), (64, 700, True)])
 def test_indexer_tensor_cores(HI, T, fp8):
