@@ -455,7 +455,11 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
     if (hist) {
       named_sync(6, 32 * EPI);
       uint32_t* rh = hist_row;
-      for (int i = tid - 64; i < kTopkHistBins; i += 32 * EPI) {
+      // the CTAs of a row start their flush at different bins, so that their atomics meet
+      // different addresses at the same time
+      const int rot = (split * 256) & (kTopkHistBins - 1);
+      for (int j = tid - 64; j < kTopkHistBins; j += 32 * EPI) {
+        const int i = (j + rot) & (kTopkHistBins - 1);
         const uint32_t c = sHist[i];
         if (c) atomicAdd(&rh[i], c);
       }
