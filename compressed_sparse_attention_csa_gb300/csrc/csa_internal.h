@@ -57,7 +57,7 @@ cudaError_t launch_compress1(const Compress1Args& a, cudaStream_t s);
 
 // ---- indexer ----------------------------------------------------------------------
 // Decode step (T = 1, tensor-core path): the indexer launch also compresses the entry the
-// new token completes (main KV by the first CTA of each sequence, indexer key by the CTA
+// new token completes (main KV spread over the CTAs of each sequence, indexer key by the CTA
 // that scores it, before that tile is loaded), builds its query image in shared memory, and
 // histograms its scores into `hist` ([B][4160] rows then B top-k tickets), which the top-k
 // kernel reads and leaves zero again: zero before the first step.

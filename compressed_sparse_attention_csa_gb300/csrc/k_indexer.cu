@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
         }
       }
       // the sequence's new main-KV entry
-      if (split == 0 && e_new >= 0) decode_new_kv(a, b, e_new, tid - 64);
+      if (e_new >= 0) decode_new_kv(a, b, e_new, tid - 64, split, L.n_splits);
     }
     const bool w_ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, a.err, sAbort));  // gates landed with the image
     const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;

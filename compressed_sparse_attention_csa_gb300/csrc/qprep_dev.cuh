@@ -164,17 +164,22 @@ __device__ __forceinline__ float decode_new_key(const IndexerArgs& a, int b, int
   return scale;
 }
 
-// The new main-KV entry e of sequence b by 256 threads (t256 = 0..255), two channels each
-// (d <= 512).
-__device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64_t e, int t256) {
+// The new main-KV entry e of sequence b (d <= 512), its channels spread over the n_parts
+// CTAs that score the sequence's keys: part p takes channels p + n_parts * i, i = t256 and
+// t256 + 256 (t256 = 0..255), so no CTA holds its key stream back for the whole entry.
+__device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64_t e, int t256, int part,
+                                              int n_parts) {
   const DecodeFuse& f = a.fuse;
   const int d = f.d, m = a.m;
   const size_t elem = f.act_bf16 ? 2 : 4;
   const size_t tail = static_cast<size_t>(b) * 2 * m * 2 * d * elem;
+  int chs[2];
   float v[2];
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
-    const int c[1] = {t256 + 256 * n < d ? t256 + 256 * n : 0};
+    chs[n] = part + n_parts * (t256 + 256 * n);
+    if (chs[n] >= d) continue;
+    const int c[1] = {chs[n]};
     float o[1];
     compress_tail_any<1>(static_cast<const uint8_t*>(f.kv_tail) + tail, static_cast<const uint8_t*>(f.z_tail) + tail,
                          f.bias, f.act_bf16, m, d, c, e > 0, o);
@@ -184,7 +189,7 @@ __device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64
     uint8_t* row8 = static_cast<uint8_t*>(f.kv_comp) + (static_cast<int64_t>(b) * a.E_cap + e) * (d + 64);
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
-      const int ch = t256 + 256 * n;
+      const int ch = chs[n];
       if (ch >= d) continue;
       if (ch < d - 64)
         row8[ch] = f_to_e4m3(v[n]);
@@ -196,7 +201,7 @@ __device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64
   const int64_t row = (static_cast<int64_t>(b) * a.E_cap + e) * d;
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
-    const int ch = t256 + 256 * n;
+    const int ch = chs[n];
     if (ch >= d) continue;
     if (f.act_bf16)
       static_cast<__nv_bfloat16*>(f.kv_comp)[row + ch] = __float2bfloat16_rn(v[n]);
