@@ -72,6 +72,23 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return u32.view(np.float32).astype(np.float64)
 
 
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bfloat16 value (8 significant bits, ties to even) of float64 values in bf16's
+    normal range, taken in one rounding from float64; returned as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                       # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def round_to_store(x: np.ndarray, store: str) -> np.ndarray:
+    """A value as a cache of the given dtype holds it: "bf16", "f32" (IEEE binary32) or "f64"."""
+    if store == "bf16":
+        return round_to_bf16(x)
+    if store == "f32":
+        return np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+    return np.asarray(x, np.float64)
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round binary32 to bfloat16 bits, round-to-nearest, ties to even (finite inputs)."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
@@ -367,27 +384,34 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
                          kI_deq: np.ndarray, fp8_keys: bool = False, fp8_kv: bool = False) -> Dict[str, np.ndarray]:
     """One decode token of sequence b (T = 1).
 
-    When the token at t completes a block ((t + 1) % m == 0), entry (t + 1)/m - 1 is
-    compressed from the tail streams (rows = tokens t-2m+1 .. t) into the caches kv_comp
-    [E, d] and kI_deq [E, dI] (updated in place; FP8 keys are stored as e4m3 codes with one
-    fp32 scale and read back dequantised; with fp8_kv the main-KV entry is stored as an FP8
-    entry and read back decoded); then indexer -> top-k -> attention.
+    When the token at t completes a block ((t + 1) % m == 0), entry e = (t + 1)/m - 1 is
+    compressed from the tail streams (rows = tokens t-2m+1 .. t, so the previous block's
+    b-stream tokens m(e-1) .. me-1 sit in rows 0 .. m-1) and stored into the caches kv_comp
+    [E, d] and kI_deq [E, dI] (updated in place) before anything is scored: each value is
+    computed in float64 and stored in the cache's dtype (cfg.act: "bf16" or "f32"; FP8 keys as
+    e4m3 codes with one binary32 scale amax/448, read back dequantised; with fp8_kv the main-KV
+    entry as an FP8 entry, read back decoded); then indexer -> top-k -> attention over the
+    caches as stored.  r["entry"] = (e, stored main-KV entry, stored key, exact main-KV entry,
+    exact key) or None.
     """
     t = int(inp["q_pos"][b])
+    store = getattr(cfg, "act", "f64")
     entry = None
     if (t + 1) % cfg.m == 0:
         e = (t + 1) // cfg.m - 1
         tok0 = t - 2 * cfg.m + 1
-        kv_comp[e] = compress_entry(inp["kv_str"][b], inp["z_str"][b], inp["bias"], cfg.m, e, tok0)
+        kv_exact = compress_entry(inp["kv_str"][b], inp["z_str"][b], inp["bias"], cfg.m, e, tok0)
         if fp8_kv:   # kv_comp holds the cache as stored: FP8 entries, read back decoded
-            kv_comp[e] = kv_fp8_decode(kv_fp8_encode(kv_comp[e]))
+            kv_comp[e] = kv_fp8_decode(kv_fp8_encode(kv_exact))
+        else:
+            kv_comp[e] = round_to_store(kv_exact, store)
         ki = compress_entry(inp["kvI_str"][b], inp["zI_str"][b], inp["biasI"], cfg.m, e, tok0)
         if fp8_keys:
             codes, sc = quantize_rows_e4m3(ki.astype(np.float32)[None, :])
             kI_deq[e] = e4m3_decode(codes[0]) * float(sc[0])
         else:
-            kI_deq[e] = ki
-        entry = (e, kv_comp[e].copy(), ki)
+            kI_deq[e] = round_to_store(ki, store)
+        entry = (e, kv_comp[e].copy(), kI_deq[e].copy(), kv_exact, ki)
     r = decode_token(cfg, inp, b, 0, kv_comp, kI_deq)
     r["entry"] = entry
     return r

@@ -64,6 +64,30 @@ def test_quantize_rows_e4m3_roundtrip_bound():
     assert np.all(np.max(np.abs(back), axis=1) == pytest.approx(np.max(np.abs(x), axis=1), rel=1e-6))
 
 
+
+def test_quantize_rows_e4m3_divisor_is_448():
+    # a row whose amax is 56 = 448 / 8: the scale is exactly 1/8 and the amax lands on e4m3's
+    # largest normal code 0x7E (= 448); -1.5 -> -12 and 0.7 -> 5.6 -> nearest 5.5 (step 0.5)
+    x = np.array([[56.0, -1.5, 3.0, 0.7]], np.float32)
+    codes, scale = O.quantize_rows_e4m3(x)
+    assert scale[0] == np.float32(0.125)
+    assert codes[0, 0] == 0x7E
+    np.testing.assert_array_equal(O.e4m3_decode(codes[0]) * float(scale[0]), [56.0, -1.5, 3.0, 0.6875])
+
+
+def test_round_to_bf16_single_rounding():
+    # binary32 inputs: the same as the (torch-pinned) binary32 -> bf16 conversion
+    x = (rng.standard_normal(5000) * 10.0 ** rng.integers(-3, 3, 5000)).astype(np.float32)
+    np.testing.assert_array_equal(O.round_to_bf16(x.astype(np.float64)), O.bf16_bits_to_f64(O.f32_to_bf16_bits(x)))
+    # exact halfway points go to the even neighbour; a float64 value just above a halfway point
+    # rounds up (rounding through binary32 first would land on the halfway point and go down)
+    assert O.round_to_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert O.round_to_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+    assert O.round_to_bf16(np.array([1.0 + 2.0 ** -8 + 2.0 ** -30]))[0] == 1.0 + 2.0 ** -7
+    assert O.round_to_bf16(np.array([-3.0]))[0] == -3.0 and O.round_to_bf16(np.array([0.0]))[0] == 0.0
+    assert O.round_to_store(np.array([0.1]), "f32")[0] == float(np.float32(0.1))
+
+
 # ------------------------------------------------------------------ compressor
 
 def _load_compress_golden():
@@ -226,6 +250,19 @@ def test_indexer_mac_count_matches_pages():
     from compressed_sparse_attention_csa_gb300.accounting import indexer_macs
     assert indexer_macs(vals["heads"], vals["dim"], vals["positions_full"]) == vals["macs_full"]
     assert indexer_macs(vals["heads"], vals["dim"], vals["pool_blocks"] * vals["pool_block"]) == vals["macs_pool"]
+
+
+
+def test_indexer_scores_subset_brute_force():
+    HI, dI, E = 3, 5, 40
+    qI = rng.standard_normal((HI, dI))
+    kI = rng.standard_normal((E, dI))
+    w = rng.standard_normal(HI)
+    pos = np.array([0, 7, 8, 31, 39, 7])             # any order, repeats allowed
+    got = O.indexer_scores_subset(qI, w, kI, pos)
+    brute = [sum(w[h] * max(0.0, math.fsum(qI[h, c] * kI[p, c] for c in range(dI))) for h in range(HI)) for p in pos]
+    np.testing.assert_allclose(got, brute, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(got, O.indexer_scores(qI, w, kI, E)[pos], rtol=1e-14, atol=1e-15)
 
 
 # ------------------------------------------------------------------ top-k
@@ -495,6 +532,105 @@ def test_hca_decode_step_writes_the_block_entry_first():
     r2 = O.hca_decode_step_sequence(C, inp, 0, kv2)
     assert r2["entry"] is None and r2["nv"] == 7
     np.testing.assert_array_equal(kv2, kv)
+
+
+
+def test_decode_token_composition_against_torch():
+    """Indexer -> top-k -> attention for one query, recomputed with torch routines: scores by a
+    torch matmul + ReLU, selection by torch.topk (continuous scores, no ties), attention by SDPA
+    over the selected entries then the window rows, the sink as a zero-value key."""
+    class C:
+        m, k, W, T, softmax_scale = 4, 5, 3, 2, 0.3
+    H, d, HI, dI, E = 3, 8, 2, 6, 30
+    t = 4 * 20 + 1                                   # nv = 20
+    inp = {"q_pos": np.array([t - 5, t]), "q": rng.standard_normal((1, 2, H, d)),
+           "qI": rng.standard_normal((1, 2, HI, dI)), "w": rng.standard_normal((1, 2, HI)),
+           "sink": rng.standard_normal(H), "kv_local": rng.standard_normal((1, 10, d)),
+           "local_base": np.array([t - 8])}
+    kv = rng.standard_normal((E, d))
+    kI = rng.standard_normal((E, dI))
+    r = O.decode_token(C, inp, 0, 1, kv, kI)
+    nv = 20
+    assert r["nv"] == nv
+    qI_t, w_t = torch.from_numpy(inp["qI"][0, 1]), torch.from_numpy(inp["w"][0, 1])
+    ref_s = torch.relu(torch.from_numpy(kI[:nv]) @ qI_t.T) @ w_t
+    np.testing.assert_allclose(r["scores"][:nv], ref_s.numpy(), rtol=1e-12)
+    assert np.all(np.isneginf(r["scores"][nv:]))
+    sel = np.sort(torch.topk(torch.from_numpy(r["scores_f32"][:nv].copy()), C.k).indices.numpy())
+    np.testing.assert_array_equal(r["idx"], sel)
+    rows = np.concatenate([kv[sel], inp["kv_local"][0][t - 2 - (t - 8):t + 1 - (t - 8)]])
+    ref_out = _sdpa_with_sink(inp["q"][0, 1], rows, inp["sink"], C.softmax_scale)
+    np.testing.assert_allclose(r["out"], ref_out, rtol=1e-12, atol=1e-14)
+
+
+def _decode_case(store, d=6):
+    class C:
+        m, W, T, k, softmax_scale = 4, 3, 1, 4, 0.25
+    C.act = store
+    m, H, HI, dI, E = 4, 2, 2, 4, 12
+    t = 4 * 9 - 1                                   # completes block 8
+    tok0 = t - 2 * m + 1                            # rows 0..3: block 7, rows 4..7: block 8
+    kv_str = rng.standard_normal((1, 2 * m, 2, d))
+    z_str = rng.standard_normal((1, 2 * m, 2, d))
+    kvI_str = rng.standard_normal((1, 2 * m, 2, dI))
+    zI_str = rng.standard_normal((1, 2 * m, 2, dI))
+    # main KV: token 33 of stream a (the current block) dominates every channel's softmax
+    u = np.resize(np.array([0.1, -0.3, 1.0 / 3.0, 2.0, -7.77, 1e-3]), d)
+    z_str[0, 33 - tok0, 0, :] = 800.0
+    kv_str[0, 33 - tok0, 0] = u
+    # indexer key: token 30 of stream b (the previous block) dominates
+    v = np.array([56.0, -1.5, 3.0, 0.7])
+    zI_str[0, 30 - tok0, 1, :] = 800.0
+    kvI_str[0, 30 - tok0, 1] = v
+    inp = {"q_pos": np.array([t]), "q": rng.standard_normal((1, 1, H, d)), "sink": rng.standard_normal(H),
+           "qI": np.array([[[[1.0, 0.0, 0.0, 0.0], [0.0, 0.0, 1.0, 0.0]]]]), "w": np.array([[[1.0, 2.0]]]),
+           "kv_local": rng.standard_normal((1, 8, d)), "local_base": np.array([t - 7]),
+           "kv_str": kv_str, "z_str": z_str, "kvI_str": kvI_str, "zI_str": zI_str,
+           "bias": rng.standard_normal((2, m, d)) * 0.1, "biasI": rng.standard_normal((2, m, dI)) * 0.1}
+    kv = rng.standard_normal((E, d))
+    kI = rng.standard_normal((E, dI)) * 0.1
+    kI[8] = 0.0                                     # stale row: indexing before the write scores 0
+    return C, inp, kv, kI, t, u, v
+
+
+@pytest.mark.parametrize("store", ["bf16", "f32"])
+def test_decode_step_stores_the_entry_before_indexing(store):
+    C, inp, kv, kI, t, u, v = _decode_case(store)
+    kv0, kI0 = kv.copy(), kI.copy()
+    r = O.decode_step_sequence(C, inp, 0, kv, kI)
+    e = r["entry"][0]
+    assert e == 8 and r["nv"] == 9
+    want_u = O.round_to_bf16(u) if store == "bf16" else u.astype(np.float32).astype(np.float64)
+    want_v = O.round_to_bf16(v) if store == "bf16" else v.astype(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(kv[8], want_u)            # the stream-a token, as the cache stores it
+    np.testing.assert_array_equal(kI[8], want_v)            # the stream-b token of the previous block
+    assert not np.array_equal(kv[8], u)
+    np.testing.assert_array_equal(r["entry"][3], u)         # exact entry before storage
+    np.testing.assert_array_equal(np.delete(kv, 8, 0), np.delete(kv0, 8, 0))
+    np.testing.assert_array_equal(np.delete(kI, 8, 0), np.delete(kI0, 8, 0))
+    # the new key is scored in this step: 1 * relu(56) + 2 * relu(3) = 62 is the best score
+    assert r["scores"][8] == 62.0
+    assert 8 in r["idx"] and (r["idx"] >= 0).sum() == 4
+    rows = np.concatenate([kv[r["idx"]], inp["kv_local"][0][5:8]])
+    out, lse = O.sparse_attention(inp["q"][0, 0], rows, inp["sink"], 0.25)
+    np.testing.assert_allclose(r["out"], out, rtol=1e-15)
+    # a token inside a block stores nothing and sees the same 9 entries
+    inp["q_pos"] = np.array([t + 2])
+    inp["local_base"] = np.array([t - 5])
+    kv2, kI2 = kv.copy(), kI.copy()
+    r2 = O.decode_step_sequence(C, inp, 0, kv2, kI2)
+    assert r2["entry"] is None and r2["nv"] == 9
+    np.testing.assert_array_equal(kv2, kv)
+    np.testing.assert_array_equal(kI2, kI)
+
+
+def test_decode_step_fp8_key_and_entry_storage():
+    C, inp, kv, kI, t, u, v = _decode_case("bf16", d=72)   # an FP8 entry: 8 e4m3 dims + 64 bf16 dims
+    r = O.decode_step_sequence(C, inp, 0, kv, kI, fp8_keys=True, fp8_kv=True)
+    # the key re-quantised with scale amax / 448 = 56 / 448 = 1/8: 0.7 / (1/8) = 5.6 -> 5.5
+    np.testing.assert_array_equal(kI[8], [56.0, -1.5, 3.0, 0.6875])
+    assert r["scores"][8] == 62.0
+    np.testing.assert_array_equal(kv[8], O.kv_fp8_decode(O.kv_fp8_encode(u)))
 
 
 # ------------------------------------------------------------------ RMSNorm, partial RoPE, inverse RoPE
