@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill-chunk leg that the default (1M decode) run adds to its line")
     ap.add_argument("--only", choices=["step", "stage", "indexer"], default=None,
                     help="run only the step or the workload's dominant stage (\"indexer\": the stage of the CSA "
                          "workloads), eagerly (for profiler captures)")
@@ -818,6 +820,73 @@ def config_of(wl):
 DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400, 12: 12}
 
 
+def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):
+    """The other half of the headline metric, measured in the same run: the V4-Flash prefill
+    chunk (4,096 new tokens after 131,072) stepped in rotation over independent copies, every
+    full rotation one CUDA graph, between one event pair; then its indexer stage (the
+    tensor-core GEMM that dominates it) timed alone the same way, against the measured dense
+    bf16 peaks."""
+    from synth import gen
+    cfg = gen.CONFIGS[3]
+    w0 = Prefill(cfg, csa, torch, dev, row0)
+    R = copies_for(w0.touched_bytes)
+    wls = [w0] + [Prefill(cfg, csa, torch, dev, row0) for _ in range(R - 1)]
+    for w in wls:
+        w.step()
+    torch.cuda.synchronize(dev)
+    assert csa.get_last_error() == 0
+    stream = torch.cuda.current_stream(dev)
+
+    def graphs(fn_name):
+        gs = []
+        for w in wls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                getattr(w, fn_name)()
+            gs.append(g)
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all):
+            for w in wls:
+                getattr(w, fn_name)()
+        torch.cuda.synchronize(dev)
+        return gs, g_all
+
+    def timed(gs, g_all, n):
+        full, rem = divmod(n, len(gs))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(full):
+            g_all.replay()
+        for i in range(rem):
+            gs[i].replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    Kp = max(3 * R, min(K, 200))
+    gs, g_all = graphs("step")
+    timed(gs, g_all, 3 * R)
+    step_ms = max_over_ranks(timed(gs, g_all, Kp) / Kp)
+    gs_s, g_all_s = graphs("stage_fn")
+    timed(gs_s, g_all_s, 3 * R)
+    stage_ms = max_over_ranks(timed(gs_s, g_all_s, Kp) / Kp)
+    assert csa.get_last_error() == 0
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    tflops = w0.stage_amount / (stage_ms / 1e3) / 1e12
+    out = {"metric": w0.metric, "value": round(w0.units * world / (step_ms / 1e3), 1), "unit": "tok/s",
+           "ms_per_step": round(step_ms, 5), "steps": Kp, "step_tflops": round(w0.step_flops / (step_ms / 1e3) / 1e12, 1),
+           "config": config_of(w0),
+           "roofline": {"bound": "tensor", "kernel": w0.stage_label, "achieved": round(tflops, 1), "peak": bf16,
+                        "unit": "TFLOP/s", "frac": round(tflops / bf16, 4), "peak_sustained": bf16_sus,
+                        "frac_of_sustained": round(tflops / bf16_sus, 4),
+                        "peak_kind": f"{peak_kind} dense bf16 GEMM throughput (burst; sustained beside it)",
+                        "amount_per_launch": w0.stage_amount, "launch_us": round(stage_ms * 1e3, 2),
+                        "traffic": stage_traffic(3)}}
+    del gs, g_all, gs_s, g_all_s, wls, w0
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -1040,6 +1109,11 @@ def main():
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in eve) / Ke)
     e2e_val = wl.units * world / (e2e_ms / 1e3)
 
+    # ---- the prefill half of the headline metric (the default decode run only)
+    prefill = None
+    if args.config == 4 and not args.no_prefill:
+        prefill = prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, t, desc = wl.oracle(sample_n)
@@ -1055,6 +1129,8 @@ def main():
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "clocks": clocks}
         line.update(extra)
+        if prefill is not None:
+            line["prefill"] = prefill
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

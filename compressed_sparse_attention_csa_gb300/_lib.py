@@ -28,7 +28,8 @@ class csa_decode_args(ctypes.Structure):
     _fields_ = [("E_cap", c_i64), ("q_pos", c_vp), ("q", c_vp), ("qI", c_vp), ("w", c_vp), ("sink", c_vp),
                 ("kv_comp", c_vp), ("kI", c_vp), ("kscale", c_vp), ("kv_tail", c_vp), ("z_tail", c_vp),
                 ("kvI_tail", c_vp), ("zI_tail", c_vp), ("bias", c_vp), ("biasI", c_vp), ("kv_local", c_vp),
-                ("L", c_i64), ("local_base", c_vp), ("out", c_vp), ("lse", c_vp), ("idx_out", c_vp)]
+                ("L", c_i64), ("local_base", c_vp), ("out", c_vp), ("lse", c_vp), ("idx_out", c_vp),
+                ("scores_out", c_vp)]
 
 
 class csa_hca_decode_args(ctypes.Structure):
@@ -45,6 +46,7 @@ class csa_norm_rope(ctypes.Structure):
 SIGNATURES = {
     "csa_version": (c_i32, []),
     "csa_launch_count": (c_i64, []),
+    "csa_debug_set": (ctypes.c_int, [ctypes.c_int, c_i64]),
     "csa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "csa_get_last_error": (ctypes.c_int, [c_vp]),
     "csa_workspace_size": (c_sz, [ctypes.c_int, ctypes.POINTER(csa_config), c_i64, c_i64]),

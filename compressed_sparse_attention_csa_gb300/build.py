@@ -2,12 +2,17 @@
 
 Each translation unit under csrc/ compiles to _build/<name>.o in parallel; the objects link
 into compressed_sparse_attention_csa_gb300/libcsa.so against the shared CUDA runtime.
-Rebuilds only what is stale.  Usable as `python -m compressed_sparse_attention_csa_gb300.build`.
+Rebuilds what is stale by modification time, and everything when the objects were built for
+another host machine or another set of sources and flags (a stamp file records the machine
+and a hash of the sources, headers and flags), so objects copied in from another machine are
+never linked.  Usable as `python -m compressed_sparse_attention_csa_gb300.build`.
 """
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -56,13 +61,29 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
+def _stamp(srcs) -> str:
+    h = hashlib.sha256()
+    h.update(platform.machine().encode())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    for f in sorted(srcs) + sorted(_headers()):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     """Compile every csrc/*.cu and link libcsa.so; returns the library path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    if force:
+    stamp_path = os.path.join(BUILD_DIR, "stamp.txt")
+    stamp = _stamp(srcs)
+    old = open(stamp_path).read().strip() if os.path.exists(stamp_path) else ""
+    if force or old != stamp:
         for o in glob.glob(os.path.join(BUILD_DIR, "*.o")):
             os.remove(o)
+        if os.path.exists(LIB_PATH):
+            os.remove(LIB_PATH)
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
     if _stale(LIB_PATH, objs):
@@ -70,6 +91,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    with open(stamp_path, "w") as fh:
+        fh.write(stamp + "\n")
     return LIB_PATH
 
 

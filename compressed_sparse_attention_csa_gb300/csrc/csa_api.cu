@@ -17,19 +17,61 @@ static __device__ int g_err_word;  // first device-side error since the last rea
 
 static constexpr int kMaxDevices = 64;
 
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+bool first_use_in_context(std::atomic<unsigned long long>& slot) {
+  const unsigned long long id = current_context_id();
+  if (id == 0) return true;
+  return slot.exchange(id) != id;
+}
+
+// Device address of g_err_word in the current context (looked up again when the context
+// changes).
 static int* err_word_ptr() {
-  static int* ptrs[kMaxDevices] = {};
+  struct Slot {
+    unsigned long long ctx;
+    int* ptr;
+  };
+  static Slot slots[kMaxDevices] = {};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!ptrs[dev]) {
+  const unsigned long long id = current_context_id();
+  std::lock_guard<std::mutex> lock(mu);
+  if (!slots[dev].ptr || id == 0 || slots[dev].ctx != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
+    slots[dev] = Slot{current_context_id(), static_cast<int*>(p)};
   }
-  return ptrs[dev];
+  return slots[dev].ptr;
 }
 
 static std::atomic<int64_t> g_launches{0};
+// fault-injection knobs (csa_debug_set): the decode step's wait budget and skipped key loads
+static std::atomic<uint64_t> g_debug_wait_ns{kDefaultWaitNs};
+static std::atomic<int> g_debug_skip_loads{0};
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int device_sm_count() {
@@ -178,6 +220,19 @@ extern "C" {
 int32_t csa_version(void) { return 100; }
 
 int64_t csa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+csa_status csa_debug_set(csa_debug_knob knob, int64_t value) {
+  switch (knob) {
+    case CSA_DEBUG_WAIT_BUDGET_NS:
+      if (value < 1000 || value > static_cast<int64_t>(kDefaultWaitNs)) return CSA_ERR_SHAPE;
+      g_debug_wait_ns.store(static_cast<uint64_t>(value), std::memory_order_relaxed);
+      return CSA_OK;
+    case CSA_DEBUG_SKIP_KEY_LOADS:
+      g_debug_skip_loads.store(value != 0 ? 1 : 0, std::memory_order_relaxed);
+      return CSA_OK;
+  }
+  return CSA_ERR_SHAPE;
+}
 
 const char* csa_status_string(csa_status s) {
   switch (s) {
@@ -862,7 +917,8 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   for (const void* p : ptrs)
     if (!aligned16(p)) return CSA_ERR_ALIGN;
   if ((d->kscale && !aligned16(d->kscale)) || (d->lse && !aligned16(d->lse)) ||
-      (d->idx_out && !aligned16(d->idx_out)) || (ws && !aligned16(ws)))
+      (d->idx_out && !aligned16(d->idx_out)) || (d->scores_out && !aligned16(d->scores_out)) ||
+      (ws && !aligned16(ws)))
     return CSA_ERR_ALIGN;
   if (d->E_cap < 1 || d->E_cap > (int64_t(1) << 24) || d->L < 0 || !attn_shape_ok(cfg) || cfg->d > 512 || cfg->m > 16 ||
       cfg->HI > 128 || d->E_cap * cfg->B >= (int64_t(1) << 31))
@@ -886,12 +942,14 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   p += align_up(static_cast<size_t>(cfg->B) * 4, 256);
   int32_t* idx = reinterpret_cast<int32_t*>(p);
   p += align_up(static_cast<size_t>(cfg->B) * cfg->k * 4, 256);
+  // the top-k scratch: the fused selection's candidate lists, or the top-k kernels' workspace
   const size_t topk_ws =
       std::max(topk_workspace_bytes(cfg->B, d->E_cap, cfg->k, sms), topk_hist_workspace_bytes(cfg->B, d->E_cap));
   void* ws_topk = p;
   p += align_up(topk_ws, 256);
   void* ws_attn = p;
   if (d->idx_out) idx = d->idx_out;
+  if (d->scores_out) scores = d->scores_out;
 
   // indexer over the visible entries (the tensor-core path also histograms the scores)
   IndexerArgs ia{};
@@ -914,6 +972,8 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   ia.num_sms = sms;
   ia.nv_out = nv;
   ia.ws = q_images;
+  ia.wait_ns = g_debug_wait_ns.load(std::memory_order_relaxed);
+  ia.skip_key_loads = g_debug_skip_loads.load(std::memory_order_relaxed) != 0;
   cudaError_t e;
   if (indexer_uses_tensor_cores(ia) && cfg->m <= 8) {
     // 1-2. one launch: compression of the completed block (both caches), the query images,

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (csa_api.cu) and the kernel translation units.
 #pragma once
 #include <cstddef>
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -8,6 +9,19 @@
 #include "csa.h"
 
 namespace csa {
+
+// Budget of a device-side bounded wait, after which it records CSA_ERR_TIMEOUT and gives up.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// Unique id of the CUDA context current on this thread (0 when none is current or the driver
+// cannot tell).  Device addresses of the library's __device__ objects and kernel attributes
+// belong to a context, so caches of them are keyed by this id (a device reset or a new
+// primary context gets a new id).
+unsigned long long current_context_id();
+// True the first time the call site owning `slot` runs in the current context (and whenever
+// the context cannot be identified): the site then sets its kernels' attributes, which are
+// per context.  Thread-safe; setting an attribute twice is harmless.
+bool first_use_in_context(std::atomic<unsigned long long>& slot);
 
 // ---- compression ------------------------------------------------------------------
 struct CompressJob {    // one cache produced by the compressor
@@ -59,8 +73,8 @@ cudaError_t launch_compress1(const Compress1Args& a, cudaStream_t s);
 // Decode step (T = 1, tensor-core path): the indexer launch also compresses the entry the
 // new token completes (main KV spread over the CTAs of each sequence, indexer key by the CTA
 // that scores it, before that tile is loaded), builds its query image in shared memory, and
-// histograms its scores into `hist` ([B][4160] rows then B top-k tickets), which the top-k
-// kernel reads and leaves zero again: zero before the first step.
+// histograms its scores into `hist` ([B][4160] rows), which the top-k kernel reads and
+// leaves zero again: zero before the first step.
 struct DecodeFuse {
   bool on;
   const void* kv_tail;   // [B, 2m, 2, d] tokens t-2m+1..t (stream a, stream b)
@@ -73,8 +87,10 @@ struct DecodeFuse {
   const float* biasI;    // [2, m, dI]
   bool act_bf16;         // stream and kv_comp dtype
   bool kv_fp8;           // kv_comp holds FP8 main-KV entries: d - 64 e4m3 codes, then 64 bf16 dims
-  uint32_t* hist;        // histograms + tickets
+  uint32_t* hist;        // histograms
 };
+// decode-step state kept across steps: the histograms [B][4160] and the top-k tickets [B]; zero
+// before the first step, left zero by every step
 inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + B; }
 struct IndexerArgs {
   const void* qI;        // [B*T, HI, dI]
@@ -98,6 +114,8 @@ struct IndexerArgs {
   void* ws;              // tensor-core path: query images (indexer_workspace_bytes)
   bool images_ready;     // the query images in ws were already written (fused decode prep)
   DecodeFuse fuse;       // decode step only
+  uint64_t wait_ns = kDefaultWaitNs;  // budget of every bounded wait of the launch
+  bool skip_key_loads = false;        // fault injection (tests): the producer issues no key load
 };
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
 bool indexer_uses_tensor_cores(const IndexerArgs& a);

@@ -8,10 +8,13 @@
 // until the process exits) and allocates nothing.
 //
 // The array's name in host code is only a host-side stand-in for the device object, so its
-// device address is looked up once per device with cudaGetSymbolAddress (on the first call
-// made while that device is current) and passed to the kernels.  Every call shares the one
-// array and finds it as the previous call left it: whatever must start at zero is cleared
-// on the stream before use, and two calls whose work overlaps on the GPU race on it.
+// device address is looked up with cudaGetSymbolAddress and passed to the kernels.  The
+// lookup runs on the first call in each CUDA context (with that context's device current) and
+// again whenever the current context changes (a device reset or a new primary context loads
+// the module again, at a new address); the address is cached per device with the id of the
+// context it belongs to.  Every call shares the one array and finds it as the previous call
+// left it: whatever must start at zero is cleared on the stream before use, and two calls
+// whose work overlaps on the GPU race on it.
 #include <mutex>
 
 #include "csa_internal.h"
@@ -23,20 +26,25 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDev = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDev] = {};
+struct ScratchSlot {
+  unsigned long long ctx;  // id of the context the address belongs to
+  void* ptr;
+};
+ScratchSlot g_scratch[kMaxDev] = {};
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array in the current context.
 csa_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return CSA_ERR_CUDA;
+  const unsigned long long id = csa::current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch[dev].ptr || id == 0 || g_scratch[dev].ctx != id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return CSA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    g_scratch[dev] = ScratchSlot{csa::current_context_id(), p};
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return CSA_OK;
 }
 

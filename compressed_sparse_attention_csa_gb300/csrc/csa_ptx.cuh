@@ -31,6 +31,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// p (a shared-memory pointer) rounded up to a multiple of `align` bytes, by pointer arithmetic
+// on p itself: the compiler keeps the result in the shared state space, so the loads, stores
+// and atomics through it stay shared-memory instructions (an integer round trip would make
+// every access through it a generic one).
+template <typename T>
+__device__ __forceinline__ T* smem_align(T* p, uint32_t align) {
+  const uint32_t a = smem_u32(p);
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(p) + (((a + align - 1u) & ~(align - 1u)) - a));
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 // Kernels of a dependent chain are launched with programmatic stream serialization: a kernel
 // may start while its predecessor drains, runs only its independent prologue, and waits here
@@ -66,20 +76,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  Returns false (and records a timeout)
-// when the budget runs out or when *abort is raised by another role of the CTA.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
-                                          volatile int* abort) {
+// when the budget (nanoseconds) runs out or when *abort is raised by another role of the CTA.
+__device__ __forceinline__ bool mbar_wait_b(uint64_t* bar, uint32_t parity, int* err, volatile int* abort,
+                                            uint64_t budget_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
-    if (global_ns() - t0 > kWaitBudgetNs) {
+    if (global_ns() - t0 > budget_ns) {
       set_error(err, kErrTimeout);
       if (abort) *abort = 1;
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
+  return mbar_wait_b(bar, parity, err, abort, kWaitBudgetNs);
 }
 
 // Barrier over the first nthreads threads that reach named barrier `id` (whole warps).
@@ -146,17 +159,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-
-// Four rows (row0..row3) of a 2D tensor map whose box is {box_inner, 1}, starting at column
-// c0 (a multiple of 16 bytes), into four consecutive box-sized rows of shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int r0,
-                                            int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
 }
 
 // ------------------------------------------------------------------ cp.async (16 B)

@@ -1743,11 +1743,10 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
           !encode_tmap_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a.q), kD,
                           static_cast<uint64_t>(rows) * kH, kD * 2, 64, kH))
         return cudaErrorInvalidValue;
-      static bool hattr = false;
-      if (!hattr) {
+      static std::atomic<unsigned long long> hattr{0};
+      if (first_use_in_context(hattr)) {
         cudaFuncSetAttribute(attn_hca_dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(HdLayout::kSmem));
-        hattr = true;
       }
       cudaError_t e = launch_pdl(attn_hca_dec_kernel, dim3(hp.n_split, static_cast<unsigned>(rows)),
                                  dim3(kHdThreads), HdLayout::kSmem, s, kvmap, lmap, qmap, a, hp);
@@ -1768,11 +1767,10 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       sp.part_o = reinterpret_cast<float*>(ws);
       sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));
     }
-    static bool dattr = false;
-    if (!dattr) {
+    static std::atomic<unsigned long long> dattr{0};
+    if (first_use_in_context(dattr)) {
       cudaFuncSetAttribute(attn_pf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(PfLayout::kSmem));
-      dattr = true;
     }
     cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows), sp.n_split), dim3(kPfThreads),
                                PfLayout::kSmem, s, a, sp);
@@ -1790,17 +1788,15 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));
     }
     const size_t smem = 1024 + kMiscOff + (kH * 7 + 32) * 4 + 64 + static_cast<size_t>(kMaxK) * 4;
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    if (first_use_in_context(attr)) {
       cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      attr = true;
     }
     if (sp.n_split == 1 && a.k <= kPfMaxK) {
-      static bool pattr = false;
-      if (!pattr) {
+      static std::atomic<unsigned long long> pattr{0};
+      if (first_use_in_context(pattr)) {
         cudaFuncSetAttribute(attn_pf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PfLayout::kSmem));
-        pattr = true;
       }
       const cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows)), dim3(kPfThreads),
                                        PfLayout::kSmem, s, a, sp);
@@ -1820,15 +1816,14 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     // decode: head groups so that split x group x query fills the SMs once
     const int64_t per = static_cast<int64_t>(sp.n_split) * rows;
     const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
-    static bool dattr = false;
-    if (!dattr) {
+    static std::atomic<unsigned long long> dattr{0};
+    if (first_use_in_context(dattr)) {
       cudaFuncSetAttribute(attn_dec_kernel<16, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<16>::kSmem));
       cudaFuncSetAttribute(attn_dec_kernel<32, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<32>::kSmem));
       cudaFuncSetAttribute(attn_dec_kernel<64, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(DecLayout<64>::kSmem));
-      dattr = true;
     }
     dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
     cudaError_t e =
@@ -1873,15 +1868,14 @@ cudaError_t launch_attn_quantkv(const AttnArgs& a, cudaStream_t s) {
   sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));
   const int64_t per = static_cast<int64_t>(sp.n_split) * rows;
   const int hg = per * 4 <= a.num_sms ? 4 : (per * 2 <= a.num_sms ? 2 : 1);
-  static bool fattr = false;
-  if (!fattr) {
+  static std::atomic<unsigned long long> fattr{0};
+  if (first_use_in_context(fattr)) {
     cudaFuncSetAttribute(attn_dec_kernel<16, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(DecLayout<16>::kSmem));
     cudaFuncSetAttribute(attn_dec_kernel<32, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(DecLayout<32>::kSmem));
     cudaFuncSetAttribute(attn_dec_kernel<64, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(DecLayout<64>::kSmem));
-    fattr = true;
   }
   dim3 grid(sp.n_split, hg, static_cast<unsigned>(rows));
   cudaError_t e =

@@ -145,13 +145,13 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
                                                                    const IndexerArgs a, const TcLayout L,
                                                                    const uint8_t* images, const int64_t n_cols) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   const int HI = a.HI, G = L.G, N = L.N, S = L.stages;
   uint8_t* sB = smem;
   float* sW = reinterpret_cast<float*>(smem + L.b_bytes);  // [G][HI], right after the B image
   uint8_t* sA = smem + L.b_bytes + align_up_dev(L.w_bytes, 1024);
   int* sNv = reinterpret_cast<int*>(sA + static_cast<size_t>(S) * L.stage_bytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sNv + kMaxG) + 7) & ~uintptr_t(7));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_align(reinterpret_cast<uint8_t*>(sNv + kMaxG), 8));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;       // [4] accumulator ready for the epilogue
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       }
       auto issue = [&](int it) {
         const int st = it % S;
-        if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort)) return false;
+        if (!mbar_wait_b(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort, a.wait_ns)) return false;
         mbar_arrive_expect_tx(&full[st], L.stage_bytes);
         const int64_t row64 =
             static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it * tile_step) * kTile;
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
         };
         for (int it = 0; ok && it < n_it; ++it) {
           const int st = it % S;
-          if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort);
+          if (lane == 0) ok = mbar_wait_b(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort, a.wait_ns);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
@@ -306,9 +306,9 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         for (int j = max(0, issued - lag); j < issued; ++j) land(j);
-      } else if (lane == 0) {
+      } else if (lane == 0 && !a.skip_key_loads) {
         for (int it = 0; ok && it < key_it; ++it) ok = issue(it), issued += ok;
-        if (FUSE && own_new && ok) ok = mbar_wait(kbar, 0, a.err, sAbort);
+        if (FUSE && own_new && ok) ok = mbar_wait_b(kbar, 0, a.err, sAbort, a.wait_ns);
         for (int it = key_it; ok && it < n_it; ++it) ok = issue(it), issued += ok;
         // every load issued must have landed before the CTA may exit
         for (int it = max(0, issued - S); it < issued; ++it) wait_time_only(&full[it % S], (it / S) & 1);
@@ -332,15 +332,15 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
         bulk_g2s(sB, img, L.b_bytes, qbar);
         bulk_g2s(sW, img + L.b_bytes, L.w_bytes, qbar);
       }
-      const bool q_ok = mbar_wait(qbar, 0, a.err, sAbort);
+      const bool q_ok = mbar_wait_b(qbar, 0, a.err, sAbort, a.wait_ns);
       if (q_ok && n_it > 0) {
         const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
         const uint32_t bBase = smem_u32(sB);
         int committed = 0;
         for (int it = 0; it < n_it; ++it) {
           const int st = it % S, acc = it % NA;
-          if (!mbar_wait(&full[st], (it / S) & 1, a.err, sAbort)) break;
-          if (!mbar_wait(&tempty[acc], ((it / NA) & 1) ^ 1, a.err, sAbort)) break;
+          if (!mbar_wait_b(&full[st], (it / S) & 1, a.err, sAbort, a.wait_ns)) break;
+          if (!mbar_wait_b(&tempty[acc], ((it / NA) & 1) ^ 1, a.err, sAbort, a.wait_ns)) break;
           tc_fence_after();
           const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
           const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       // the sequence's new main-KV entry
       if (e_new >= 0) decode_new_kv(a, b, e_new, tid - 64, split, L.n_splits);
     }
-    const bool w_ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, a.err, sAbort));  // gates landed with the image
+    const bool w_ok = __all_sync(0xffffffffu, mbar_wait_b(qbar, 0, a.err, sAbort, a.wait_ns));  // gates landed with the image
     const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
     const int32_t* cand_b = !FUSE && a.cand ? a.cand + static_cast<int64_t>(qrow0) * a.n_cand : nullptr;
     // the key row of slot sx: the slot itself, or (candidate mode) its position (-1: none)
@@ -416,12 +416,12 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       const float ksc = ks_next;
       ks_next = scale_of(it + 2);
       // (waits are made warp-uniform: the TMEM loads and the histogram below are warp-wide)
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], (it / NA) & 1, a.err, sAbort))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_b(&tfull[acc], (it / NA) & 1, a.err, sAbort, a.wait_ns))) break;
       tc_fence_after();
       const int64_t s = static_cast<int64_t>(tile_lo + it * tile_step) * kTile + rin;
       float ksc_use = ksc;
       if (FUSE && FP8 && __any_sync(0xffffffffu, s == e_new)) {  // the key compressed in this launch
-        if (!__all_sync(0xffffffffu, mbar_wait(kbar, 0, a.err, sAbort))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_b(kbar, 0, a.err, sAbort, a.wait_ns))) break;
         if (s == e_new) ksc_use = *sNewScale;
       }
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * N);
@@ -560,8 +560,8 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
       if (e != cudaSuccess) return e;
     }
     dim3 grid(L.n_splits, L.n_qgroups, a.B);
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    if (first_use_in_context(attr)) {
       const int mx = 227 * 1024;
       cudaFuncSetAttribute(indexer_tc_kernel<true, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
       cudaFuncSetAttribute(indexer_tc_kernel<false, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
@@ -569,7 +569,6 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
       cudaFuncSetAttribute(indexer_tc_kernel<false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
       cudaFuncSetAttribute(indexer_tc_kernel<true, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
       cudaFuncSetAttribute(indexer_tc_kernel<false, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      attr = true;
     }
     const uint8_t* cimages = images;
     const dim3 blk(L.wide && !a.fuse.on ? tc_threads(1) : tc_threads(2));

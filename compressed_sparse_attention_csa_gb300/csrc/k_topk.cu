@@ -407,13 +407,12 @@ cudaError_t run_levels(const Plan& pl, const float* scores, int64_t ld, int64_t 
     }
     dim3 grid(static_cast<unsigned>(pl.n_chunks[l]), static_cast<unsigned>(rows));
     const size_t smem = level_smem(p.chunk, l == 0);
-    static bool attr_set = false;  // one opt-in per process (both instantiations, largest chunk)
-    if (!attr_set) {
+    static std::atomic<unsigned long long> attr_set{0};  // both instantiations, largest chunk
+    if (first_use_in_context(attr_set)) {
       cudaFuncSetAttribute(topk_level_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(level_smem(kRawChunkMax, true)));
       cudaFuncSetAttribute(topk_level_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(level_smem(kCandChunk, false)));
-      attr_set = true;
     }
     cudaError_t e = (l == 0) ? launch_pdl(topk_level_kernel<true>, grid, dim3(NT), smem, s, p)
                              : launch_pdl(topk_level_kernel<false>, grid, dim3(NT), smem, s, p);
@@ -432,8 +431,11 @@ size_t levels_ws(const Plan& pl, int64_t rows, int k) {
 }  // namespace
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms) {
-  const size_t lv = levels_ws(make_plan(rows, n_cols, k, num_sms), rows, k);
-  return topk_uses_hist(rows, n_cols, false) ? std::max(lv, topk_hist_standalone_bytes(rows, n_cols)) : lv;
+  // the scratch of the path launch_topk takes: the histogram path's counts and slots, none for
+  // the row kernel (shared memory only), else the level path's ping-pong candidate buffers
+  if (topk_uses_hist(rows, n_cols, false)) return topk_hist_standalone_bytes(rows, n_cols);
+  if (topk_uses_rows(rows, n_cols, false, k)) return 0;
+  return levels_ws(make_plan(rows, n_cols, k, num_sms), rows, k);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {

@@ -1,20 +1,23 @@
-// Histogram-guided top-k for a few long rows (the decode step).
+// Histogram-guided top-k for long rows (csa_topk, csa_indexer_topk, csa_block_pool).
 //
 // Same contract as the chunked top-k ("DeepSeek V4-Flash: The Cost of Deciding What to
 // Read", section "The Lightning Indexer": keep the k best entries; ties go to the lowest
 // position; output ascending, -1 padded).
 //
-// Every visible score of row r is counted in a two-level histogram of its order-preserving
-// key: 4096 fine bins (key >> 20) and 64 coarse bins (key >> 26).  The decode step fills it
-// in the indexer epilogue; the standalone call fills it with topk_hist_build_kernel.  From it,
-// the threshold digit b1 is the largest fine bin whose suffix count reaches k, so every one
-// of the k best scores has digit >= b1.
-//  1. topk_filter_kernel (wide grid) appends every score with digit >= b1 to the row's
-//     candidate list (about k plus one bin's worth; order irrelevant).
-//  2. topk_final_kernel (one CTA per row) finds the exact k-th key by radix select over the
-//     candidates, resolves ties at that key by lowest position, and writes the winners in
-//     ascending position with a bucket-counting sort.  If the list overflowed its capacity
-//     (a bin full of ties) it selects over the whole row instead, in position order.
+// Every visible score of a row is counted in a histogram of its order-preserving key: 4096
+// fine bins (key >> 20) and 64 coarse bins (key >> 26).  The threshold digit b1 is the
+// largest fine bin whose suffix count reaches k, so every one of the k best scores has digit
+// >= b1.
+//  * Few long rows: topk_hist_build_kernel fills the histogram, then topk_select_kernel runs
+//    one CTA per 4,096-position chunk:
+//    each keeps its scores with digit >= b1, in position order, in its slot of the workspace
+//    and takes a ticket; the row's last CTA gathers the slots, finds the exact k-th key by
+//    radix passes over the low 20 bits of the b1 bin, takes the lowest positions among equal
+//    keys, writes the winners ascending and clears the histogram row.  If the slots overflow
+//    (a bin full of ties) it selects over the whole row instead, in position order.
+//  * Many long rows (the prefill chunk, the block pool): topk_row_kernel, one CTA per row with
+//    the histogram in shared memory and the same exact selection.
+// The decode step runs topk_select_kernel on the histogram its indexer launch fills.
 #include <algorithm>
 
 #include <cooperative_groups.h>
@@ -525,11 +528,10 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
 cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s,
                              const int32_t* cmap) {
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<unsigned long long> attr{0};
+  if (first_use_in_context(attr)) {
     cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(sel_smem_bytes(4096)));
-    attr = true;
   }
   const int n_chunks = std::max(1, sel_chunks(n_cols));
   const cudaError_t e =
@@ -549,13 +551,12 @@ bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k) {
 
 cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              int k, int32_t* idx, cudaStream_t s, const int32_t* cmap) {
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<unsigned long long> attr{0};
+  if (first_use_in_context(attr)) {
     cudaFuncSetAttribute(topk_row_kernel<2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(row_smem_bytes<2048>(512)));
     cudaFuncSetAttribute(topk_row_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(row_smem_bytes<8192>(4096)));
-    attr = true;
   }
   const dim3 grid(static_cast<unsigned>(rows));
   const cudaError_t e =

@@ -67,9 +67,15 @@ __device__ void team_select_largest(F val, int n, int want, int lo_bits, uint32_
     const int nb = 1 << wbits;
     for (int i = t; i < nb; i += NT) hist[i] = 0u;
     team_sync<NT>(bar);
-    for (int e = t; e < n; e += NT) {
-      const uint32_t v = val(e);
-      if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+    // values of a warp that share a bin are counted with one atomic (the top values of a row
+    // often share their leading digits)
+    for (int e0 = 0; e0 < n; e0 += NT) {
+      const int e = e0 + t;
+      const uint32_t v = e < n ? val(e) : 0u;
+      const bool in = e < n && (v & mask) == prefix;
+      const uint32_t bin = in ? (v >> shift) & static_cast<uint32_t>(nb - 1) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (in && (t & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
     }
     team_sync<NT>(bar);
     // thread t owns `per` consecutive bins counted from the top
@@ -137,18 +143,25 @@ __device__ uint32_t team_threshold_digit(const uint32_t* fine, int k, uint32_t* 
   return b1;
 }
 
-// The same threshold digit from a histogram in shared memory.
+// The same threshold digit from a histogram in shared memory (16-byte aligned; read as vectors).
 template <int NT>
 __device__ uint32_t team_threshold_digit_smem(const uint32_t* fine, int k, uint32_t* tmp, uint32_t* res, int t,
                                               int bar) {
   constexpr int per = kTopkHistBins / NT;
+  static_assert(per % 4 == 0, "16-byte reads");
   uint32_t c[per];
   uint32_t mine = 0;
+  const uint4* src = reinterpret_cast<const uint4*>(fine + kTopkHistBins - per * (t + 1));
 #pragma unroll
-  for (int q = 0; q < per; ++q) {
-    c[q] = fine[kTopkHistBins - 1 - (t * per + q)];
-    mine += c[q];
+  for (int w = 0; w < per / 4; ++w) {
+    const uint4 x = src[w];
+    c[per - 1 - 4 * w] = x.x;
+    c[per - 2 - 4 * w] = x.y;
+    c[per - 3 - 4 * w] = x.z;
+    c[per - 4 - 4 * w] = x.w;
   }
+#pragma unroll
+  for (int q = 0; q < per; ++q) mine += c[q];
   if (t == 0) res[4] = 0u;
   uint32_t run = team_scan<NT>(mine, t, tmp, nullptr, bar);
 #pragma unroll

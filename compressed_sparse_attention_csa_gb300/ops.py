@@ -230,14 +230,17 @@ def sparse_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, idx: torch.
 
 
 def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
-                biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, fp8kv: bool = False) -> None:
+                biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, scores_out=None,
+                fp8kv: bool = False) -> None:
     """csa_decode_step (csa_decode_step_fp8kv with fp8kv: kv_comp [B, E_cap, 576] uint8 FP8
-    entries): one token per sequence (T = 1); caches are updated in place."""
+    entries): one token per sequence (T = 1); caches are updated in place.  scores_out
+    [B, E_cap] fp32 (optional) receives the indexer scores the step selected from."""
     lib = L.load()
     c = cfg.c()
     a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                           _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias), _p(biasI),
-                          _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse), _p(idx_out))
+                          _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse), _p(idx_out),
+                          _p(scores_out))
     nbytes = lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1])
     if nbytes == ctypes.c_size_t(-1).value:
         raise CsaError("csa_workspace_size", 2)
@@ -391,21 +394,22 @@ class DecodeStepCall:
     Calling the object enqueues one step on the current stream."""
 
     def __init__(self, cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
-                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, fp8kv: bool = False):
+                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, scores_out=None,
+                 fp8kv: bool = False):
         self._lib = L.load()
         self._fn = self._lib.csa_decode_step_fp8kv if fp8kv else self._lib.csa_decode_step
         self._c = cfg.c()
         self._a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                                     _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias),
                                     _p(biasI), _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse),
-                                    _p(idx_out))
+                                    _p(idx_out), _p(scores_out))
         nbytes = self._lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(self._c), cfg.B, kv_comp.shape[1])
         if nbytes == ctypes.c_size_t(-1).value:
             raise CsaError("csa_workspace_size", 2)
         self._ws = _decode_workspace(nbytes, q.device, cfg.B)
         self._wp, self._wb = _ws_args(self._ws)
         self._refs = (q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias, biasI, kv_local,
-                      local_base, out, kscale, lse, idx_out)   # keep the buffers alive
+                      local_base, out, kscale, lse, idx_out, scores_out)   # keep the buffers alive
         self._cref, self._aref = ctypes.byref(self._c), ctypes.byref(self._a)
 
     def __call__(self) -> None:

@@ -183,8 +183,10 @@ csa_status csa_topk(const csa_config *cfg, const float *scores, int64_t ld, int6
  * loads the library holds until the process exits); this call allocates nothing.  Sizes whose
  * scratch need (csa_workspace_size(CSA_OP_TOPK, ...)) exceeds that limit are rejected with
  * CSA_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device (with that device current) looks up the array's device address
- *    with cudaGetSymbolAddress; make that first call before any stream capture.
+ *  - The first call in a CUDA context (with that context's device current) looks up the
+ *    array's device address with cudaGetSymbolAddress, and a call looks it up again when the
+ *    current context has changed since (after a device reset, for example); make the first
+ *    call in a context before any stream capture.
  *  - All calls share the one array and find it as the previous call left it; what must start
  *    at zero is cleared on the stream.  Calls whose work overlaps on the GPU (different streams,
  *    or different host threads without ordering) race on it: order them on one stream.
@@ -403,6 +405,8 @@ typedef struct {
   void *out;                 /* [B, H, d]                                                     */
   float *lse;                /* [B, H] or NULL                                                */
   int32_t *idx_out;          /* [B, k] or NULL: the entries the step selected                 */
+  float *scores_out;         /* [B, E_cap] fp32 or NULL: the indexer scores the step selected
+                                from (-inf past the visible entries); NULL keeps them in ws    */
 } csa_decode_args;
 
 /*
@@ -439,6 +443,22 @@ const char *csa_status_string(csa_status s);
 
 /* Number of kernels this process has enqueued through libcsa so far (all devices). */
 int64_t csa_launch_count(void);
+
+/*
+ * csa_debug_set — fault-injection hooks for tests of the failure path; the pages have no
+ * counterpart.  Process-wide; they apply to the csa_decode_step / csa_decode_step_fp8kv calls
+ * made after them (the indexer launch of the step):
+ *   CSA_DEBUG_WAIT_BUDGET_NS : budget of the launch's bounded device waits, 1e3 .. 2e9 ns
+ *                              (default 2e9); CSA_ERR_SHAPE outside that range.
+ *   CSA_DEBUG_SKIP_KEY_LOADS : nonzero makes the indexer's producer issue no key-tile load, so
+ *                              its consumers' waits run out: the step records CSA_ERR_TIMEOUT
+ *                              (read with csa_get_last_error), every kernel role still reaches
+ *                              its exit, the step's selection is empty and the workspace state
+ *                              is left clean for the next step.  0 (default) turns it off.
+ * Leave both at their defaults outside such tests.
+ */
+typedef enum { CSA_DEBUG_WAIT_BUDGET_NS = 0, CSA_DEBUG_SKIP_KEY_LOADS = 1 } csa_debug_knob;
+csa_status csa_debug_set(csa_debug_knob knob, int64_t value);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t csa_version(void);

@@ -121,7 +121,7 @@ def oracle_decode(cfg, inp):
     return res
 
 
-def run_gpu_decode(cfg, inp):
+def run_gpu_decode(cfg, inp, scores_out=None):
     c = lib_config(cfg)
     out = torch.empty(cfg.B, cfg.H, cfg.d, device=inp["q"].device, dtype=cfg.torch_act)
     lse = torch.empty(cfg.B, cfg.H, device=inp["q"].device)
@@ -130,9 +130,23 @@ def run_gpu_decode(cfg, inp):
                     kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
                     z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
                     biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse,
-                    idx_out=idx)
+                    idx_out=idx, scores_out=scores_out)
     assert csa.get_last_error() == 0
     return out, lse, idx
+
+
+def assert_step_selection_exact(cfg, ref, idx, scores_out):
+    """The decode step's selection is exactly the top-k (score desc, position asc; ascending,
+    -1 padded) of the fp32 scores it wrote, and those scores match the oracle's within the
+    indexer tolerance, -inf past the visible entries."""
+    rtol_s = 5e-2 if cfg.kidx == "fp8" else 1e-2
+    for b in range(cfg.B):
+        nv = ref[b]["nv"]
+        s32 = scores_out[b].cpu().numpy()
+        assert np.all(np.isneginf(s32[nv:])), f"b={b}: invisible entries must be -inf"
+        assert_scores_close(s32[:nv], ref[b]["scores"][:nv], rtol_s, what=f"step scores b={b}")
+        gi = idx[b].cpu().numpy().astype(np.int64)
+        np.testing.assert_array_equal(gi, O.topk(s32, nv, cfg.k), err_msg=f"b={b}: selection differs from the top-k")
 
 
 def assert_decode_matches(cfg, inp, ref, out, lse, idx):
@@ -152,8 +166,8 @@ def assert_decode_matches(cfg, inp, ref, out, lse, idx):
         assert_out_close_with_swaps(np64(out[b]), r["out"], 2e-2, bound, what=f"out b={b} swaps={swaps}")
         np.testing.assert_allclose(np64(lse[b]), r["lse"], atol=5e-3)
         if r["entry"] is not None:
-            e, ent, _ = r["entry"]
-            assert_entries_close(np64(inp["kv_comp"][b, e]), ent, np64(inp["kv_str"][b]))
+            e, _, _, ent_exact, _ = r["entry"]
+            assert_entries_close(np64(inp["kv_comp"][b, e]), ent_exact, np64(inp["kv_str"][b]))
 
 
 def assert_pool_valid(gpool, ref_scores_f32, nv: int, block: int, n_blocks: int, score_tol: float):

@@ -99,7 +99,7 @@ def test_decode_step_argument_errors(lib):
     args = L.csa_decode_args()
     assert lib.csa_decode_step(ctypes.byref(c), ctypes.byref(args), A, 1 << 30, None) == 1
     for name, _ in L.csa_decode_args._fields_:
-        if name not in ("E_cap", "L", "kscale", "lse", "idx_out"):
+        if name not in ("E_cap", "L", "kscale", "lse", "idx_out", "scores_out"):
             setattr(args, name, 0x10000)
     args.E_cap, args.L = 1 << 16, 128
     assert lib.csa_decode_step(ctypes.byref(c), ctypes.byref(args), A, 16, None) == 5        # workspace

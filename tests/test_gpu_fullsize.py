@@ -18,7 +18,7 @@ import pytest
 import torch
 
 import compressed_sparse_attention_csa_gb300 as csa
-from _helpers import (assert_decode_matches, assert_entries_close, assert_out_close_with_swaps, assert_pool_valid,
+from _helpers import (assert_decode_matches, assert_step_selection_exact, assert_entries_close, assert_out_close_with_swaps, assert_pool_valid,
                       assert_rows_close, assert_scores_close, assert_selection_ok, np64, np_inputs, oracle_decode,
                       swap_bound)
 from test_gpu_epilogue import assert_vectors_close, e4m3_half_step
@@ -50,9 +50,11 @@ def host(x):
 def test_decode_full_size(cid):
     cfg = gen.CONFIGS[cid]
     wl = Decode(cfg, csa, torch, DEV, 0)
+    wl.args["scores_out"] = wl.scores          # the step's scores, for the exact selection check
     ref = oracle_decode(cfg, wl.inp)          # reads the caches before the step writes entry E-1
     replay_once(wl.step)
     assert_decode_matches(cfg, wl.inp, ref, wl.out, wl.lse, wl.idx)
+    assert_step_selection_exact(cfg, ref, wl.idx, wl.scores)
 
 
 def test_prefill_full_size_sampled_rows():

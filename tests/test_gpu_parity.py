@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import compressed_sparse_attention_csa_gb300 as csa
-from _helpers import (assert_out_close_with_swaps, assert_rows_close, assert_scores_close, assert_selection_ok,
+from _helpers import (assert_out_close_with_swaps, assert_step_selection_exact, assert_rows_close, assert_scores_close, assert_selection_ok,
                       keys_f64, lib_config, np64, np_inputs, oracle_decode, run_gpu_decode, swap_bound,
                       assert_decode_matches, assert_entries_close, assert_pool_valid)
 from oracle import csa_oracle as O
@@ -411,11 +411,46 @@ def test_decode_step_matches_oracle(cid, N, HI):
     inp["q_pos"][1] = N - 3          # this token completes no block: no compression
     kv_before = inp["kv_comp"].clone()
     ref = oracle_decode(cfg, inp)   # oracle reads the inputs before the step mutates the caches
-    out, lse, idx = run_gpu_decode(cfg, inp)
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    out, lse, idx = run_gpu_decode(cfg, inp, scores_out=scores)
     assert_decode_matches(cfg, inp, ref, out, lse, idx)
+    assert_step_selection_exact(cfg, ref, idx, scores)
     for b in range(cfg.B):
         if ref[b]["entry"] is None:
             assert torch.equal(inp["kv_comp"][b], kv_before[b])
+
+
+@pytest.mark.parametrize("cid", [2, 4])
+@pytest.mark.parametrize("kind", ["duplicate_keys", "zero_gates", "skewed"])
+def test_decode_step_selection_exact_on_ties(cid, kind):
+    """The in-step selection on rows full of exact ties or skewed toward the end: 3,000 copies
+    of one key row (equal scores straddling the threshold), all gates zero (every score 0:
+    positions 0 .. k-1), and key magnitudes growing with the position (the best scores crowd
+    the end of the row)."""
+    cfg = gen.CONFIGS[cid].replace(B=2, N=4 * 5000)
+    inp = gen.make_inputs(cfg, DEV)
+    if kind == "duplicate_keys":
+        inp["kI"][:, 1000:4000] = inp["kI"][:, 7:8]
+        if "kscale" in inp:
+            inp["kscale"][:, 1000:4000] = inp["kscale"][:, 7:8]
+    elif kind == "zero_gates":
+        inp["w"].zero_()
+    else:
+        inp["qI"].abs_()
+        inp["w"].abs_()
+        if "kscale" in inp:
+            inp["kI"].copy_(inp["kI"] & 0x7F)      # positive e4m3 codes
+            inp["kscale"].copy_(torch.arange(1, cfg.E + 1, device=DEV, dtype=torch.float32)[None] * 1e-3)
+        else:
+            inp["kI"].copy_((inp["kI"].float().abs() * torch.arange(1, cfg.E + 1, device=DEV)[None, :, None] * 1e-3)
+                            .to(inp["kI"].dtype))
+    ref = oracle_decode(cfg, inp)
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    out, lse, idx = run_gpu_decode(cfg, inp, scores_out=scores)
+    assert_step_selection_exact(cfg, ref, idx, scores)
+    if kind == "zero_gates":
+        np.testing.assert_array_equal(idx.cpu().numpy(), np.tile(np.arange(cfg.k), (cfg.B, 1)))
+    assert_decode_matches(cfg, inp, ref, out, lse, idx)
 
 
 def test_tiny_end_to_end_fp32():

@@ -3,15 +3,17 @@
 Such callers (a plugin inside another runtime that owns every device allocation, or a
 latency-critical path where an allocation could block or fail) have no workspace to give
 csa_topk.  The no-allocation entry point uses a fixed scratch array inside the library; its
-results must equal csa_topk's exactly (the selection is exact), on consecutive calls that
-reuse the same scratch.
+results must equal csa_topk's exactly (the selection is exact), and the oracle's top-k of the
+same fp32 scores, on consecutive calls that reuse the same scratch.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 from compressed_sparse_attention_csa_gb300 import _lib as L
+from oracle import csa_oracle as O
 from synth import gen
 
 pytestmark = pytest.mark.gpu
@@ -62,13 +64,20 @@ def test_noalloc_equals_topk_on_two_calls(rows, n, k):
         got = _topk_noalloc(lib, x, k, nv)
         assert lib.csa_get_last_error(_stream()) == 0
         assert torch.equal(got, ref), f"call {call}"
+        xs, nvs, gs = x.cpu().numpy(), nv.cpu().numpy(), got.cpu().numpy()
+        for r in range(rows):
+            np.testing.assert_array_equal(gs[r], O.topk(xs[r], int(nvs[r]), k), err_msg=f"call {call} row {r}")
 
 
 def test_noalloc_rejects_sizes_beyond_the_scratch():
     lib = L.load()
     cfg = _cfg(512)
-    dummy = torch.empty(16, dtype=torch.float32, device="cuda")
-    out = torch.empty(16, dtype=torch.int32, device="cuda")
-    # 4096 rows of 33,792 scores need far more than the fixed scratch
-    st = lib.csa_topk_noalloc(ctypes.byref(cfg), _ptr(dummy), 33792, 4096, 33792, None, None, _ptr(out), _stream())
+    rows, n = 16, 262144     # the histogram path's candidate slots for these need about 8.4 MB
+    need = lib.csa_workspace_size(L.CSA_OP_TOPK, ctypes.byref(cfg), rows, n)
+    assert need > (4 << 20)
+    scores = torch.zeros(rows, n, dtype=torch.float32, device="cuda")
+    out = torch.full((rows, 512), -7, dtype=torch.int32, device="cuda")
+    st = lib.csa_topk_noalloc(ctypes.byref(cfg), _ptr(scores), n, rows, n, None, None, _ptr(out), _stream())
     assert st == 5  # CSA_ERR_WORKSPACE, nothing launched
+    torch.cuda.synchronize()
+    assert bool((out == -7).all())
