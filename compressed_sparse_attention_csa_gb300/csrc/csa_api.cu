@@ -1058,6 +1058,15 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
 }
 }  // namespace
 
+csa_status csa_decode_step_reset(const csa_config* cfg, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  if (!cfg || !ws) return CSA_ERR_NULL;
+  if (cfg->B < 1) return CSA_ERR_SHAPE;
+  if (!aligned16(ws)) return CSA_ERR_ALIGN;
+  const size_t bytes = decode_state_words(cfg->B) * 4;
+  if (ws_bytes < bytes) return CSA_ERR_WORKSPACE;
+  return launch_status(cudaMemsetAsync(ws, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
                            csa_stream_t stream) {
   return decode_step_impl(cfg, d, ws, ws_bytes, stream, false);

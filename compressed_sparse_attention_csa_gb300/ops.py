@@ -249,6 +249,20 @@ def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_t
     _check("csa_decode_step", fn(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))
 
 
+def decode_step_reset(cfg: Config, device=None) -> None:
+    """csa_decode_step_reset on the decode workspace this binding keeps for (device, cfg.B):
+    clears the state one step hands to the next, e.g. after a step that reported an error.
+    Enqueued on the current stream; a no-op when no step has run on that workspace yet."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    buf = _decode_ws.get((str(device), cfg.B))
+    if buf is None:
+        return
+    lib = L.load()
+    c = cfg.c()
+    wp, wb = _ws_args(buf)
+    _check("csa_decode_step_reset", lib.csa_decode_step_reset(ctypes.byref(c), wp, wb, _stream()))
+
+
 def dense_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, kv_local: torch.Tensor, local_base: torch.Tensor,
                q_pos: torch.Tensor, sink: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None) -> None:
     """csa_dense_attn (HCA): every entry s < floor((q_pos+1)/cfg.m) of kv_comp [B, E_cap, d] plus

@@ -119,3 +119,16 @@ def test_workspace_queries(lib):
     assert lib.csa_block_pool_workspace_size(8, 262144, 8, 5000) == ctypes.c_size_t(-1).value
     bad = _cfg(dI=7)
     assert lib.csa_workspace_size(L.CSA_OP_TOPK, ctypes.byref(bad), 1, 10) == ctypes.c_size_t(-1).value
+
+
+def test_decode_step_reset_argument_errors(lib):
+    c = _cfg(B=3)
+    need = 4 * 4161 * 3
+    f = lib.csa_decode_step_reset
+    assert f(None, A, need, None) == 1
+    assert f(ctypes.byref(c), None, need, None) == 1
+    assert f(ctypes.byref(_cfg(B=0)), A, need, None) == 2
+    assert f(ctypes.byref(c), MIS, need, None) == 4
+    assert f(ctypes.byref(c), A, need - 1, None) == 5
+    # the state region is at the front of the step's own workspace
+    assert lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), 3, 262144) >= need

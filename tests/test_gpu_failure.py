@@ -61,3 +61,23 @@ def test_decode_step_timeout_is_reported_and_the_next_step_is_clean(cid):
     out, lse, idx = run_gpu_decode(cfg, inp, scores_out=scores)
     assert_decode_matches(cfg, inp, ref, out, lse, idx)
     assert_step_selection_exact(cfg, ref, idx, scores)
+
+
+def test_decode_step_reset_clears_a_dirty_workspace():
+    """A workspace whose carried state is dirty (as after a step whose launches never ran) is
+    made usable again by csa_decode_step_reset: the next step matches the oracle exactly."""
+    from compressed_sparse_attention_csa_gb300 import ops
+    cfg = gen.CONFIGS[2].replace(B=3, N=4 * 2500)
+    inp = gen.make_inputs(cfg, DEV)
+    ref = oracle_decode(cfg, inp)
+    run_gpu_decode(cfg, gen.make_inputs(cfg, DEV))          # the workspace exists and is clean
+    ws = ops._decode_ws[(str(DEV), cfg.B)]
+    state = 4 * 4161 * cfg.B
+    ws[:state].fill_(0x5A)                                   # dirty every carried histogram and ticket
+    csa.decode_step_reset(lib_config(cfg))
+    torch.cuda.synchronize()
+    assert int(ws[:state].count_nonzero()) == 0
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    out, lse, idx = run_gpu_decode(cfg, inp, scores_out=scores)
+    assert_decode_matches(cfg, inp, ref, out, lse, idx)
+    assert_step_selection_exact(cfg, ref, idx, scores)
