@@ -49,7 +49,13 @@ the pages):
   * MXFP4 main-KV entries (288 B for 512 channels): per block of 16 channels one e4m3 scale
     = e4m3(amax / 6) (amax / 6 in binary32), codes = nearest E2M1 value of x / scale in binary32
     (ties to the even code, saturating at +-6, sign kept); element 2i in the low nibble of byte
-    i; the d/2 payload bytes, then the d/16 scale bytes.
+    i; the d/2 payload bytes, then the d/16 scale bytes;
+  * MXFP4 indexer keys (68 B for 128 channels): per block of 32 channels one UE8M0 scale
+    X = 2^(floor(log2(amax)) - 2), the OCP MX rule with E2M1's largest exponent 2, its
+    exponent clamped to [-127, 127] (an all-zero or subnormal block gets 2^-127); codes = the
+    nearest E2M1 value of x / X (ties to the even code, saturating at +-6, sign kept), decided
+    on the binary32 key; element 2i in the low nibble of byte i; the 64 payload bytes, and the
+    4 scale bytes (byte j for channels 32j .. 32j+31) kept beside them as one 32-bit word.
 
 Parity status: every function here is pinned by tests (closed forms, hand-computed
 examples, brute force against library routines, invariants); see tests/test_oracle_pins.py.
@@ -381,7 +387,8 @@ def decode_token(cfg, inp: Dict[str, np.ndarray], b: int, tq: int,
 
 
 def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.ndarray,
-                         kI_deq: np.ndarray, fp8_keys: bool = False, fp8_kv: bool = False) -> Dict[str, np.ndarray]:
+                         kI_deq: np.ndarray, fp8_keys: bool = False, fp8_kv: bool = False,
+                         mx_keys: bool = False) -> Dict[str, np.ndarray]:
     """One decode token of sequence b (T = 1).
 
     When the token at t completes a block ((t + 1) % m == 0), entry e = (t + 1)/m - 1 is
@@ -389,7 +396,8 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
     b-stream tokens m(e-1) .. me-1 sit in rows 0 .. m-1) and stored into the caches kv_comp
     [E, d] and kI_deq [E, dI] (updated in place) before anything is scored: each value is
     computed in float64 and stored in the cache's dtype (cfg.act: "bf16" or "f32"; FP8 keys as
-    e4m3 codes with one binary32 scale amax/448, read back dequantised; with fp8_kv the main-KV
+    e4m3 codes with one binary32 scale amax/448, read back dequantised; MXFP4 keys (mx_keys) as
+    E2M1 codes with a UE8M0 scale per 32 channels, read back decoded; with fp8_kv the main-KV
     entry as an FP8 entry, read back decoded); then indexer -> top-k -> attention over the
     caches as stored.  r["entry"] = (e, stored main-KV entry, stored key, exact main-KV entry,
     exact key) or None.
@@ -409,6 +417,8 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
         if fp8_keys:
             codes, sc = quantize_rows_e4m3(ki.astype(np.float32)[None, :])
             kI_deq[e] = e4m3_decode(codes[0]) * float(sc[0])
+        elif mx_keys:
+            kI_deq[e] = mxfp4_key_decode(*mxfp4_key_encode(ki))
         else:
             kI_deq[e] = round_to_store(ki, store)
         entry = (e, kv_comp[e].copy(), kI_deq[e].copy(), kv_exact, ki)
@@ -592,3 +602,62 @@ def mxfp4_decode(b: np.ndarray) -> np.ndarray:
     codes[..., 1::2] = payload >> 4
     vals = e2m1_decode(codes).reshape(b.shape[:-1] + (d // MX_BLOCK, MX_BLOCK))
     return (vals * e4m3_decode(sc_code)[..., None]).reshape(b.shape[:-1] + (d,))
+
+
+# ----------------------------------------------------------------------------------
+# V4.1 indexer keys  [V41d] byte ledger "Single request / logical serving KV storage" (Indexer
+# K: 128 channels in MXFP4, 64 packed bytes + 4 UE8M0 scales); [V4] "FP4, down to the index
+# scores" (the indexer's keys cached and multiplied in FP4).  The block format is the OCP
+# Microscaling (MX) one: 32 E2M1 elements sharing one power-of-two scale.
+# ----------------------------------------------------------------------------------
+
+MXK_BLOCK = 32
+E2M1_EMAX = 2          # exponent of E2M1's largest normal value, 6 = 1.5 * 2^2
+
+
+def ue8m0_decode(codes: np.ndarray) -> np.ndarray:
+    """UE8M0 (8 exponent bits, bias 127, no sign, no mantissa): 2^(c - 127); 0xFF is NaN."""
+    c = np.asarray(codes, np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - 127))
+
+
+def mxfp4_key_encode(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Keys [..., dI] (dI % 32 == 0) -> (payload [..., dI/2] uint8, scales [..., dI/32] uint8).
+
+    Per block of 32 channels: X = 2^(floor(log2(amax)) - 2) (exponent clamped to [-127, 127];
+    amax 0 or subnormal gives 2^-127), codes = e2m1_encode(x / X), all on the binary32 key.
+    """
+    x32 = np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+    dI = x32.shape[-1]
+    blk = x32.reshape(x32.shape[:-1] + (dI // MXK_BLOCK, MXK_BLOCK))
+    amax = np.abs(blk).max(axis=-1)
+    _, ex = np.frexp(amax)                       # amax = f * 2^ex, 0.5 <= f < 1: floor(log2) = ex - 1
+    e_x = np.where(amax >= np.ldexp(1.0, -126), ex - 1 - E2M1_EMAX, -127)
+    e_x = np.clip(e_x, -127, 127)
+    codes = e2m1_encode(blk / np.ldexp(1.0, e_x)[..., None]).reshape(x32.shape)
+    payload = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return payload, (e_x + 127).astype(np.uint8)
+
+
+def mxfp4_key_decode(payload: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """(payload [..., dI/2], scales [..., dI/32]) -> keys [..., dI] in float64."""
+    p = np.asarray(payload, np.uint8)
+    dI = p.shape[-1] * 2
+    codes = np.empty(p.shape[:-1] + (dI,), np.uint8)
+    codes[..., 0::2] = p & 15
+    codes[..., 1::2] = p >> 4
+    vals = e2m1_decode(codes).reshape(p.shape[:-1] + (dI // MXK_BLOCK, MXK_BLOCK))
+    return (vals * ue8m0_decode(scales)[..., None]).reshape(p.shape[:-1] + (dI,))
+
+
+def mxfp4_key_words(scales: np.ndarray) -> np.ndarray:
+    """The 4 scale bytes of a 128-channel key as one little-endian 32-bit word (byte j = block j)."""
+    s = np.asarray(scales, np.uint32)
+    return (s[..., 0] | (s[..., 1] << 8) | (s[..., 2] << 16) | (s[..., 3] << 24)).astype(np.uint32)
+
+
+def mxfp4_key_unwords(words: np.ndarray) -> np.ndarray:
+    """Inverse of mxfp4_key_words: [...] uint32 -> [..., 4] uint8."""
+    w = np.asarray(words, np.uint32)
+    return np.stack([(w >> np.uint32(8 * j)) & np.uint32(0xFF) for j in range(4)], axis=-1).astype(np.uint8)
+

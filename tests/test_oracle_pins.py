@@ -563,11 +563,11 @@ def test_decode_token_composition_against_torch():
     np.testing.assert_allclose(r["out"], ref_out, rtol=1e-12, atol=1e-14)
 
 
-def _decode_case(store, d=6):
+def _decode_case(store, d=6, dI=4):
     class C:
         m, W, T, k, softmax_scale = 4, 3, 1, 4, 0.25
     C.act = store
-    m, H, HI, dI, E = 4, 2, 2, 4, 12
+    m, H, HI, E = 4, 2, 2, 12
     t = 4 * 9 - 1                                   # completes block 8
     tok0 = t - 2 * m + 1                            # rows 0..3: block 7, rows 4..7: block 8
     kv_str = rng.standard_normal((1, 2 * m, 2, d))
@@ -579,11 +579,12 @@ def _decode_case(store, d=6):
     z_str[0, 33 - tok0, 0, :] = 800.0
     kv_str[0, 33 - tok0, 0] = u
     # indexer key: token 30 of stream b (the previous block) dominates
-    v = np.array([56.0, -1.5, 3.0, 0.7])
+    v = np.zeros(dI)
+    v[:4] = [56.0, -1.5, 3.0, 0.7]
     zI_str[0, 30 - tok0, 1, :] = 800.0
     kvI_str[0, 30 - tok0, 1] = v
     inp = {"q_pos": np.array([t]), "q": rng.standard_normal((1, 1, H, d)), "sink": rng.standard_normal(H),
-           "qI": np.array([[[[1.0, 0.0, 0.0, 0.0], [0.0, 0.0, 1.0, 0.0]]]]), "w": np.array([[[1.0, 2.0]]]),
+           "qI": np.eye(dI)[[0, 2]][None, None], "w": np.array([[[1.0, 2.0]]]),
            "kv_local": rng.standard_normal((1, 8, d)), "local_base": np.array([t - 7]),
            "kv_str": kv_str, "z_str": z_str, "kvI_str": kvI_str, "zI_str": zI_str,
            "bias": rng.standard_normal((2, m, d)) * 0.1, "biasI": rng.standard_normal((2, m, dI)) * 0.1}
@@ -631,6 +632,78 @@ def test_decode_step_fp8_key_and_entry_storage():
     np.testing.assert_array_equal(kI[8], [56.0, -1.5, 3.0, 0.6875])
     assert r["scores"][8] == 62.0
     np.testing.assert_array_equal(kv[8], O.kv_fp8_decode(O.kv_fp8_encode(u)))
+
+
+def test_decode_step_mxfp4_key_storage():
+    C, inp, kv, kI, t, u, v = _decode_case("bf16", dI=32)
+    r = O.decode_step_sequence(C, inp, 0, kv, kI, mx_keys=True)
+    # one block of 32 channels, amax 56: X = 2^(floor(log2 56) - 2) = 2^3; 56/8 = 7 saturates to
+    # 6 (48), -1.5/8 = -0.1875 -> -0, 3/8 = 0.375 -> 0.5 (4), 0.7/8 = 0.0875 -> 0
+    want = np.zeros(32)
+    want[:4] = [48.0, -0.0, 4.0, 0.0]
+    np.testing.assert_array_equal(kI[8], want)
+    assert np.signbit(kI[8][1])
+    assert r["scores"][8] == 1.0 * 48.0 + 2.0 * 4.0
+
+
+# ------------------------------------------------------------------ MXFP4 indexer keys (OCP MX)
+
+def test_mxfp4_key_ledger_and_scale_rule():
+    # [V41d]: 128 channels = 64 packed bytes + 4 UE8M0 scales = 68 B a key
+    p, sc = O.mxfp4_key_encode(np.ones((3, 128)))
+    assert p.shape == (3, 64) and sc.shape == (3, 4) and p.itemsize * 64 + sc.itemsize * 4 == 68
+    # UE8M0: 2^(c - 127), 0xFF is NaN
+    np.testing.assert_array_equal(O.ue8m0_decode([127, 0, 254, 128]), [1.0, 2.0 ** -127, 2.0 ** 127, 2.0])
+    assert np.isnan(O.ue8m0_decode([255])[0])
+    # the shared exponent is floor(log2 amax) - 2 (E2M1's emax), as a biased byte: hand values
+    cases = {6.0: 127, 4.0: 127, 3.99: 126, 8.0: 128, 7.99: 127, 0.088: 121, 1.0: 125, 2.0 ** 100: 225,
+             0.0: 0, 1e-40: 0, 2.0 ** -125: 0, 2.0 ** -120: 5}
+    for amax, byte in cases.items():
+        blk = np.zeros(32)
+        blk[5] = -amax
+        assert O.mxfp4_key_encode(blk)[1][0] == byte, amax
+
+
+def test_mxfp4_key_worked_example_and_nibble_order():
+    x = np.zeros(128)
+    x[:4] = [6.0, -0.5, 0.25, 3.3]        # block 0: X = 1; codes 7, 0x9, 0 (tie to even), 5 (3.3 -> 3)
+    x[32] = 7.9                            # block 1: X = 1, 7.9 saturates to 6
+    x[64] = 8.0                            # block 2: X = 2, 8/2 = 4 -> code 6
+    p, sc = O.mxfp4_key_encode(x)
+    assert p[0] == 0x97 and p[1] == 0x50 and p[16] == 0x07 and p[32] == 0x06
+    np.testing.assert_array_equal(sc, [127, 127, 128, 0])
+    d = O.mxfp4_key_decode(p, sc)
+    np.testing.assert_array_equal(d[[0, 1, 2, 3, 32, 64]], [6.0, -0.5, 0.0, 3.0, 6.0, 8.0])
+    # element 2i in the low nibble of byte i
+    y = np.zeros(32)
+    y[:2] = [1.0, 0.5]                     # X = 2^(0 - 2): codes of 4 and 2 -> 6 and 4
+    assert O.mxfp4_key_encode(y)[0][0] == 0x46
+    # the scale word keeps block j in byte j
+    assert O.mxfp4_key_words(np.array([1, 2, 3, 4], np.uint8)) == 0x04030201
+    np.testing.assert_array_equal(O.mxfp4_key_unwords(np.uint32(0x04030201)), [1, 2, 3, 4])
+
+
+def test_mxfp4_key_round_trip_and_error_bound():
+    # blocks whose largest magnitude is 4X or 6X re-encode to the same bytes
+    codes = rng.integers(0, 16, (40, 128)).astype(np.uint8)
+    codes[codes == 8] = 0                              # -0 decodes to 0 and re-encodes as +0
+    for j in range(4):
+        codes[:, 32 * j + rng.integers(0, 32)] = rng.choice([6, 7, 14, 15], 40)
+    sc = rng.integers(100, 150, (40, 4)).astype(np.uint8)
+    payload = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    p2, s2 = O.mxfp4_key_encode(O.mxfp4_key_decode(payload, sc))
+    np.testing.assert_array_equal(p2, payload)
+    np.testing.assert_array_equal(s2, sc)
+    # error: at most half a grid step of the E2M1 value, times X (within the unsaturated range)
+    x = rng.standard_normal((64, 128)) * np.exp(rng.uniform(-8, 8, (64, 1)))
+    p, sc = O.mxfp4_key_encode(x)
+    x32 = x.astype(np.float32).astype(np.float64)
+    err = np.abs(O.mxfp4_key_decode(p, sc) - x32).reshape(64, 4, 32)
+    X = O.ue8m0_decode(sc)[..., None]
+    a = np.abs(x32).reshape(64, 4, 32) / X
+    half = np.where(a < 2, 0.25, np.where(a < 4, 0.5, np.where(a <= 6, 1.0, 2.0)))
+    assert np.all(err <= half * X * (1 + 1e-12))
+    assert np.all(a < 8)                   # floor(log2 amax) - 2 keeps every x / X below 8
 
 
 # ------------------------------------------------------------------ RMSNorm, partial RoPE, inverse RoPE
