@@ -11,7 +11,7 @@ LIB_PATH = os.path.join(HERE, "libcsa.so")
 
 c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
-CSA_F32, CSA_BF16, CSA_E4M3 = 0, 1, 2
+CSA_F32, CSA_BF16, CSA_E4M3, CSA_MXFP4 = 0, 1, 2, 3
 (CSA_OP_COMPRESS, CSA_OP_INDEXER, CSA_OP_TOPK, CSA_OP_ATTN, CSA_OP_DECODE, CSA_OP_POOL, CSA_OP_INDEXER_TOPK,
  CSA_OP_DENSE_ATTN, CSA_OP_HCA_DECODE) = range(9)
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_DTYPE", 4: "CSA_ERR_ALIGN",

@@ -144,13 +144,27 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The indexer keys of cfg->kidx: scales present for the quantised formats; MXFP4 payloads
+// 32-byte aligned (the unpacking TMA's rule) and E_cap a multiple of 4 (a tile's TMA boxes
+// take every fourth key of a sequence).
+csa_status check_keys(const csa_config* c, const void* kI, const void* kscale, int64_t E_cap) {
+  if ((c->kidx == CSA_E4M3 || c->kidx == CSA_MXFP4) && !kscale) return CSA_ERR_NULL;
+  if (c->kidx == CSA_MXFP4) {
+    if ((reinterpret_cast<uintptr_t>(kI) & 31u) != 0) return CSA_ERR_ALIGN;
+    if (E_cap % 4 != 0) return CSA_ERR_SHAPE;
+  }
+  return CSA_OK;
+}
+
 csa_status check_cfg(const csa_config* c) {
   if (!c) return CSA_ERR_NULL;
   if (c->B < 1 || c->H < 1 || c->d < 1 || c->HI < 1 || c->m < 1 || c->k < 1 || c->k > 4096 || c->W < 0)
     return CSA_ERR_SHAPE;
   if (c->dI != 32 && c->dI != 64 && c->dI != 128) return CSA_ERR_SHAPE;
   if (c->act != CSA_F32 && c->act != CSA_BF16) return CSA_ERR_DTYPE;
-  if (c->kidx != c->act && c->kidx != CSA_E4M3) return CSA_ERR_DTYPE;
+  if (c->kidx != c->act && c->kidx != CSA_E4M3 && c->kidx != CSA_MXFP4) return CSA_ERR_DTYPE;
+  if (c->kidx == CSA_MXFP4 && c->act != CSA_BF16) return CSA_ERR_DTYPE;
+  if (c->kidx == CSA_MXFP4 && c->dI != 128) return CSA_ERR_SHAPE;
   if (!std::isfinite(c->softmax_scale)) return CSA_ERR_SHAPE;
   return CSA_OK;
 }
@@ -310,12 +324,14 @@ size_t csa_block_pool_workspace_size(int64_t rows, int64_t n_cols, int32_t block
 
 csa_status csa_compress_kv(const csa_config* cfg, int32_t dim, const void* kv, const void* z, const float* bias,
                            int64_t n_tok, int64_t tok0, int64_t ent_begin, int64_t ent_end, void* out,
-                           csa_dtype out_dtype, float* out_scale, int64_t E_cap, csa_stream_t stream) {
+                           csa_dtype out_dtype, void* out_scale, int64_t E_cap, csa_stream_t stream) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!kv || !z || !bias || !out) return CSA_ERR_NULL;
-  if (out_dtype == CSA_E4M3 && !out_scale) return CSA_ERR_NULL;
-  if (out_dtype != CSA_F32 && out_dtype != CSA_BF16 && out_dtype != CSA_E4M3) return CSA_ERR_DTYPE;
+  if ((out_dtype == CSA_E4M3 || out_dtype == CSA_MXFP4) && !out_scale) return CSA_ERR_NULL;
+  if (out_dtype != CSA_F32 && out_dtype != CSA_BF16 && out_dtype != CSA_E4M3 && out_dtype != CSA_MXFP4)
+    return CSA_ERR_DTYPE;
+  if (out_dtype == CSA_MXFP4 && dim != 128) return CSA_ERR_SHAPE;
   if (!aligned16(kv) || !aligned16(z) || !aligned16(bias) || !aligned16(out) || (out_scale && !aligned16(out_scale)))
     return CSA_ERR_ALIGN;
   if (dim < 1 || dim > 512 || cfg->m > 16 || n_tok < 0 || ent_begin < 0 || ent_end < ent_begin || ent_end > E_cap)
@@ -528,13 +544,13 @@ csa_status csa_inverse_rope_quant(const csa_config* cfg, const void* o, int64_t 
 }
 
 csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float* w, int32_t T,
-                              const int64_t* q_pos, const void* kI, const float* kscale, int64_t E_cap,
+                              const int64_t* q_pos, const void* kI, const void* kscale, int64_t E_cap,
                               const int32_t* cand, int32_t n_cand, float* scores, int64_t ld_scores, void* ws,
                               size_t ws_bytes, csa_stream_t stream) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!qI || !w || !q_pos || !kI || !scores) return CSA_ERR_NULL;
-  if (cfg->kidx == CSA_E4M3 && !kscale) return CSA_ERR_NULL;
+  if ((st = check_keys(cfg, kI, kscale, E_cap)) != CSA_OK) return st;
   if (!aligned16(qI) || !aligned16(w) || !aligned16(q_pos) || !aligned16(kI) || !aligned16(scores) ||
       (kscale && !aligned16(kscale)) || (cand && !aligned16(cand)) || (ws && !aligned16(ws)))
     return CSA_ERR_ALIGN;
@@ -569,12 +585,12 @@ csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float
 }
 
 csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* w, int32_t T, const int64_t* q_pos,
-                            const void* kI, const float* kscale, int64_t E_cap, int32_t* idx, void* ws,
+                            const void* kI, const void* kscale, int64_t E_cap, int32_t* idx, void* ws,
                             size_t ws_bytes, csa_stream_t stream) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!qI || !w || !q_pos || !kI || !idx) return CSA_ERR_NULL;
-  if (cfg->kidx == CSA_E4M3 && !kscale) return CSA_ERR_NULL;
+  if ((st = check_keys(cfg, kI, kscale, E_cap)) != CSA_OK) return st;
   if (!aligned16(qI) || !aligned16(w) || !aligned16(q_pos) || !aligned16(kI) || !aligned16(idx) ||
       (kscale && !aligned16(kscale)) || (ws && !aligned16(ws)))
     return CSA_ERR_ALIGN;
@@ -911,7 +927,7 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   if (!d->q_pos || !d->q || !d->qI || !d->w || !d->sink || !d->kv_comp || !d->kI || !d->kv_tail || !d->z_tail ||
       !d->kvI_tail || !d->zI_tail || !d->bias || !d->biasI || !d->kv_local || !d->local_base || !d->out)
     return CSA_ERR_NULL;
-  if (cfg->kidx == CSA_E4M3 && !d->kscale) return CSA_ERR_NULL;
+  if ((st = check_keys(cfg, d->kI, d->kscale, d->E_cap)) != CSA_OK) return st;
   const void* ptrs[] = {d->q_pos, d->q, d->qI, d->w, d->sink, d->kv_comp, d->kI, d->kv_tail, d->z_tail,
                         d->kvI_tail, d->zI_tail, d->bias, d->biasI, d->kv_local, d->local_base, d->out};
   for (const void* p : ptrs)

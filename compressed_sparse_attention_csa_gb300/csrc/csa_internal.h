@@ -29,9 +29,9 @@ struct CompressJob {    // one cache produced by the compressor
   const void* z;        // [B, n_tok, 2, dim]
   const float* bias;    // [2, m, dim]
   int dim;              // <= 512
-  void* out;            // [B, E_cap, dim]
-  int out_dtype;        // CSA_F32 / CSA_BF16 / CSA_E4M3
-  float* out_scale;     // [B, E_cap] for e4m3
+  void* out;            // [B, E_cap, dim] (MXFP4: [B, E_cap, dim/2] payload bytes)
+  int out_dtype;        // CSA_F32 / CSA_BF16 / CSA_E4M3 / CSA_MXFP4 (dim 128)
+  void* out_scale;      // [B, E_cap]: fp32 scales (e4m3) or UE8M0 scale words (MXFP4)
 };
 struct CompressArgs {
   CompressJob job[2];
@@ -96,8 +96,8 @@ struct IndexerArgs {
   const void* qI;        // [B*T, HI, dI]
   const float* w;        // [B*T, HI]
   const int64_t* q_pos;  // [B*T]
-  const void* kI;        // [B, E_cap, dI]
-  const float* kscale;   // [B, E_cap] (e4m3)
+  const void* kI;        // [B, E_cap, dI] (MXFP4: [B, E_cap, 64] payload bytes)
+  const void* kscale;    // [B, E_cap]: fp32 scales (e4m3) or UE8M0 scale words (MXFP4)
   const int32_t* cand;   // [B*T, n_cand] or null
   int n_cand;
   float* scores;         // [B*T, ld]
@@ -105,7 +105,7 @@ struct IndexerArgs {
   int B, T, HI, dI, m;
   int64_t E_cap;
   int act;               // CSA_F32 / CSA_BF16
-  int kidx;              // CSA_F32 / CSA_BF16 / CSA_E4M3
+  int kidx;              // CSA_F32 / CSA_BF16 / CSA_E4M3 / CSA_MXFP4
   int* err;
   int num_sms;
   int32_t* nv_out;       // [B*T] visible-entry count per query row, or null

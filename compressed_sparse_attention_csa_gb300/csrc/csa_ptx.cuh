@@ -155,6 +155,14 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                                 int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -205,6 +213,25 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled MMA, kind::mxf8f6f4 with one UE8M0 scale per 32 K elements (scale_vec::1X):
+// D(tmem) (+)= (A * scale_A) (B * scale_B), the scales read from TMEM at sfa / sfb (column
+// groups aligned to 4).  For M = 128, row r of A takes its scale from lane r, column
+// sfa + r / 32, byte = the instruction descriptor's A scale id; B's scales likewise.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Copy 32 rows x 16 bytes from shared memory (descriptor sdesc) into TMEM columns taddr ..
+// taddr + 3 of lanes 0..31, replicated into the other three lane quadrants.  Executed by
+// the tensor core in issue order with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_32x128b_w4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -251,6 +278,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// 32 lanes x 4 consecutive 32-bit columns; the warp writes its own lane quadrant.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -267,6 +300,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= static_cast<uint64_t>(kSwizzle128B) << 61;
   return d;
 }
+// Shared-memory descriptor without swizzling (rows of 16 bytes, 8-row groups 128 bytes apart),
+// for tcgen05.cp sources.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
 // Instruction descriptor, kind::f16 with bf16 inputs and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
@@ -276,6 +319,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 // Instruction descriptor, kind::f8f6f4 with e4m3 x e4m3 inputs, fp32 accumulation, K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: A E2M1 (code 5), B E4M3 (code 0),
+// UE8M0 scales (bit 23), K-major; a_sf / b_sf pick the scale byte (bits 29-30 / 4-5).
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | (5u << 7) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (a_sf << 29);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled
@@ -292,6 +342,39 @@ __device__ __forceinline__ float e4m3_to_f(uint8_t c) {
 }
 __device__ __forceinline__ uint8_t f_to_e4m3(float x) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Nearest E2M1 code of v (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; ties to the even code;
+// saturating at 6; bit 3 the sign).
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fminf(fabsf(v), 6.f);
+  uint32_t c;
+  if (a <= 0.25f) c = 0;
+  else if (a < 0.75f) c = 1;
+  else if (a <= 1.25f) c = 2;
+  else if (a < 1.75f) c = 3;
+  else if (a <= 2.5f) c = 4;
+  else if (a < 3.5f) c = 5;
+  else if (a <= 5.f) c = 6;
+  else c = 7;
+  return signbit(v) ? (c | 8u) : c;
+}
+// Value of an E2M1 code: exponent field e = bits 2..1 (bias 1), mantissa bit 0, sign bit 3.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float mag = e == 0 ? 0.5f * static_cast<float>(m) : (1.f + 0.5f * static_cast<float>(m)) * static_cast<float>(1u << (e - 1));
+  return (c & 8u) ? -mag : mag;
+}
+// UE8M0 scale byte of an MX block (OCP MX, E2M1 elements): X = 2^(floor(log2 amax) - 2) as
+// the biased exponent floor(log2 amax) - 2 + 127, clamped to [0, 254]; a zero or subnormal
+// amax gives 0 (2^-127).
+__device__ __forceinline__ uint32_t mx_e2m1_scale_byte(float amax) {
+  const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // amax >= 0, finite
+  return static_cast<uint32_t>(ef >= 2 ? ef - 2 : 0);
+}
+// 2^(byte - 127) as a float (byte 0: the subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_value(uint32_t byte) {
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
 }
 
 // Order-preserving map of fp32 to uint32 (larger key = larger float); -0 maps like +0.

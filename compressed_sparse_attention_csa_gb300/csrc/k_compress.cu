@@ -10,7 +10,9 @@
 // Bandwidth/latency-bound: one CTA per (entry, sequence, job) where a job is one cache (main
 // KV or indexer keys, both in one launch); one thread per channel; the 2m gate and value
 // loads of a channel are issued before any arithmetic.  fp32 math; an E4M3 output gets one
-// fp32 scale per entry (amax/448, codes rounded to nearest, saturating).  In the decode step
+// fp32 scale per entry (amax/448, codes rounded to nearest, saturating); an MXFP4 output (the
+// indexer keys, dim 128) one UE8M0 scale per 32 channels (a warp: the OCP MX rule
+// 2^(floor(log2 amax) - 2)) and E2M1 codes, two to a byte.  In the decode step
 // the same launch carries extra CTAs that write the indexer's query images (qprep_dev.cuh).
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
@@ -118,7 +120,19 @@ __global__ void __launch_bounds__(512) compress_kernel(CompressArgs a, QprepPart
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) am = fmaxf(am, s_red[w]);
     const float scale = am > 0.f ? __fdiv_rn(am, 448.f) : 1.f;
     if (c < dim) static_cast<uint8_t*>(job.out)[row * dim + c] = f_to_e4m3(__fdiv_rn(v, scale));
-    if (threadIdx.x == 0) job.out_scale[row] = scale;
+    if (threadIdx.x == 0) static_cast<float*>(job.out_scale)[row] = scale;
+  } else if (job.out_dtype == CSA_MXFP4) {
+    // one warp = one block of 32 channels (dim is a multiple of 32; warps past dim hold none)
+    float am = c < dim ? fabsf(v) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const uint32_t sb = mx_e2m1_scale_byte(am);
+    const uint32_t code = e2m1_code(__fdiv_rn(v, ue8m0_value(sb)));
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);  // channel c + 1
+    if (c < dim) {
+      if ((c & 1) == 0) static_cast<uint8_t*>(job.out)[row * (dim / 2) + c / 2] = static_cast<uint8_t>(code | (hi << 4));
+      if ((c & 31) == 0) static_cast<uint8_t*>(job.out_scale)[row * (dim / 32) + c / 32] = static_cast<uint8_t>(sb);
+    }
   } else if (c < dim) {
     if (job.out_dtype == CSA_BF16)
       static_cast<__nv_bfloat16*>(job.out)[row * dim + c] = __float2bfloat16_rn(v);

@@ -390,22 +390,6 @@ __global__ void __launch_bounds__(32 * kVecWarps) kv_pack_fp8_kernel(const KvPac
   }
 }
 
-// Nearest E2M1 code of v (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; ties to the even code;
-// saturating at 6; bit 3 the sign).
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  const float a = fminf(fabsf(v), 6.f);
-  uint32_t c;
-  if (a <= 0.25f) c = 0;
-  else if (a < 0.75f) c = 1;
-  else if (a <= 1.25f) c = 2;
-  else if (a < 1.75f) c = 3;
-  else if (a <= 2.5f) c = 4;
-  else if (a < 3.5f) c = 5;
-  else if (a <= 5.f) c = 6;
-  else c = 7;
-  return signbit(v) ? (c | 8u) : c;
-}
-
 // ---- pack rows into MXFP4 entries: one warp a row, lane = a block of 16 channels
 template <typename T>
 __global__ void __launch_bounds__(32 * kVecWarps) kv_pack_mxfp4_kernel(const KvPackArgs a) {

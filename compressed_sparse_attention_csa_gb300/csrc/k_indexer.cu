@@ -20,7 +20,18 @@
 // s = per-head amax/448, and both terms run through the same accumulator (the K loop is
 // issued twice, with the same key tile), so D = k . (hi + lo) to about bf16 accuracy.  The
 // per-key fp32 scale and the per-head s are positive and factor out of the ReLU.
+//
+// MXFP4 keys ("FP4, down to the index scores"; 64 payload bytes + 4 UE8M0 scales a key) use
+// the block-scaled kind::mxf8f6f4: A = E2M1 keys, B = the same two E4M3 query terms, and the
+// keys' scales applied by the MMA from TMEM.  TMA unpacks the packed payload into the 8-bit
+// slots the MMA reads (16 codes in each 16-byte chunk), so a key tile has the FP8 tile's
+// shared-memory footprint at half its HBM bytes.  The MMA takes row r's scale from TMEM lane
+// r, column (r / 32) of a 4-column group; a tile therefore holds key 4l + c (l = 0..31,
+// c = 0..3) in row 32c + l, so that the tile's 128 scale words, contiguous in memory, are
+// exactly the 32 lines of 16 bytes one tcgen05.cp (32x128b, copied to all four lane
+// quadrants) puts in place.
 #include <algorithm>
+#include <type_traits>
 
 #include "csa_internal.h"
 #include "csa_ptx.cuh"
@@ -30,6 +41,8 @@ namespace csa {
 namespace {
 
 // ------------------------------------------------------------------ CUDA-core path
+struct MxKey {};  // key type tag: MXFP4 keys (DI/2 payload bytes and one scale word per key)
+
 template <typename TQ, typename TK, int DI>
 __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_t n_cols) {
   extern __shared__ float sm[];
@@ -54,7 +67,13 @@ __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_
   if (s >= 0 && s < nv) {
     float kv[DI];
     const int64_t krow = static_cast<int64_t>(b) * a.E_cap + s;
-    if constexpr (sizeof(TK) == 1) {
+    if constexpr (std::is_same<TK, MxKey>::value) {
+      const uint8_t* kp = static_cast<const uint8_t*>(a.kI) + krow * (DI / 2);
+      const uint32_t sw = static_cast<const uint32_t*>(a.kscale)[krow];
+#pragma unroll
+      for (int c = 0; c < DI; ++c)
+        kv[c] = e2m1_value((kp[c >> 1] >> (4 * (c & 1))) & 15u) * ue8m0_value((sw >> (8 * (c >> 5))) & 0xFFu);
+    } else if constexpr (std::is_same<TK, uint8_t>::value) {
       const uint8_t* kp = static_cast<const uint8_t*>(a.kI) + krow * DI;
 #pragma unroll
       for (int c = 0; c < DI; ++c) kv[c] = e4m3_to_f(kp[c]);
@@ -70,7 +89,7 @@ __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_
       for (int c = 0; c < DI; ++c) dot = fmaf(sq[h * DI + c], kv[c], dot);
       acc = fmaf(sw[h], fmaxf(dot, 0.f), acc);
     }
-    if constexpr (sizeof(TK) == 1) acc *= a.kscale[krow];
+    if constexpr (std::is_same<TK, uint8_t>::value) acc *= static_cast<const float*>(a.kscale)[krow];
     score = acc;
   }
   a.scores[row * a.ld + col] = score;
@@ -83,7 +102,11 @@ constexpr int tc_threads(int minb) { return 64 + 32 * epi_warps(minb); }
 constexpr int kTcThreads = tc_threads(2);
 constexpr int kTile = 128;                       // keys per tile (MMA M)
 constexpr int kMaxG = 8;
-constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes
+constexpr uint32_t kKeyTileBytesF8 = kTile * 128;  // 128 keys x 128 e4m3 codes (or unpacked E2M1)
+// key formats of the tensor-core path
+constexpr int kKeyBf16 = 0, kKeyE4m3 = 1, kKeyMx = 2;
+constexpr uint32_t kMxScaleSlot = kTile * 4;       // a tile's 128 scale words
+constexpr uint32_t kMxBoxBytes = 32 * 64;          // one TMA box: 32 keys x 64 packed bytes
 
 using TcLayout = IndexerLayout;
 
@@ -140,17 +163,22 @@ __global__ void __launch_bounds__(256) indexer_qprep_kernel(const IndexerArgs a,
 // alternate tiles; with 16 epilogue warps (one CTA per SM) the two groups of a tile parity
 // split its queries between them, which doubles the warps that hide the TMEM and shared
 // memory latencies of the reduction.
-template <bool FP8, bool FUSE, int MINB>
+template <int KF, bool FUSE, int MINB>
 __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const IndexerArgs a, const TcLayout L,
                                                                    const uint8_t* images, const int64_t n_cols) {
+  constexpr bool FP8 = KF == kKeyE4m3;   // e4m3 keys with one fp32 scale each
+  constexpr bool MX = KF == kKeyMx;      // MXFP4 keys, block-scaled MMA
+  constexpr bool F8Q = KF != kKeyBf16;   // the query as two e4m3 terms (both 8-bit key formats)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align(smem_raw, 1024);
   const int HI = a.HI, G = L.G, N = L.N, S = L.stages;
   uint8_t* sB = smem;
   float* sW = reinterpret_cast<float*>(smem + L.b_bytes);  // [G][HI], right after the B image
   uint8_t* sA = smem + L.b_bytes + align_up_dev(L.w_bytes, 1024);
-  int* sNv = reinterpret_cast<int*>(sA + static_cast<size_t>(S) * L.stage_bytes);
+  // MXFP4: each stage's 128 key scale words
+  uint8_t* sSc = sA + static_cast<size_t>(S) * L.stage_bytes;
+  int* sNv = reinterpret_cast<int*>(sSc + (MX ? static_cast<size_t>(S) * kMxScaleSlot : 0));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_align(reinterpret_cast<uint8_t*>(sNv + kMaxG), 8));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -158,7 +186,8 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
   uint64_t* tempty = bars + 2 * S + 4;  // [4] accumulator drained
   uint64_t* qbar = bars + 2 * S + 8;    // query image landed
   uint64_t* kbar = bars + 2 * S + 9;    // decode step: the new key entry is written
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 10);
+  uint64_t* sbar = bars + 2 * S + 10;   // MXFP4: the query side's scales are in TMEM
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 11);
   volatile int* sAbort = reinterpret_cast<volatile int*>(sTmem + 1);
   int64_t* sNew = reinterpret_cast<int64_t*>(sTmem + 2);     // decode step: new entry (-1: none)
   float* sNewScale = reinterpret_cast<float*>(sTmem + 5);
@@ -168,6 +197,11 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
   const bool img_cta = FUSE || image_in_cta(a, L);  // the epilogue warps write the query image
   const bool hist = (a.hist_out != nullptr || fuse) && G == 1;
   const int NA = L.n_acc;
+  // MXFP4: TMEM columns after the accumulators: a 4-column scale group per accumulator (the
+  // tile's key scales), then the query side's scales (8 columns, 2^0 in every byte), each
+  // group 8-aligned
+  const uint32_t sf0 = (static_cast<uint32_t>(NA * N) + 7u) & ~7u;
+  const uint32_t sfb_col = sf0 + 8u * static_cast<uint32_t>(NA);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, qg = blockIdx.y, g0 = qg * G, split = blockIdx.x;
@@ -206,6 +240,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
     }
     mbar_init(qbar, img_cta ? 32 * EPI : 1);
     mbar_init(kbar, 1);
+    mbar_init(sbar, 128);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -239,7 +274,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       uint64_t pol = 0;
       bool ok = true;
       int issued = 0;
-      const bool gather = !FUSE && a.cand != nullptr;  // the decode step has no candidate lists
+      const bool gather = !FUSE && !MX && a.cand != nullptr;  // the decode step has no candidate lists
       if (lane == 0 && !gather) {
         tma_prefetch_desc(&kmap);
         pol = policy_evict_first();
@@ -247,11 +282,25 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       auto issue = [&](int it) {
         const int st = it % S;
         if (!mbar_wait_b(&empty[st], ((it / S) & 1) ^ 1, a.err, sAbort, a.wait_ns)) return false;
-        mbar_arrive_expect_tx(&full[st], L.stage_bytes);
         const int64_t row64 =
             static_cast<int64_t>(b) * a.E_cap + static_cast<int64_t>(tile_lo + it * tile_step) * kTile;
-        const int row = static_cast<int>(row64);
         uint8_t* dst = sA + static_cast<size_t>(st) * L.stage_bytes;
+        if constexpr (MX) {
+          // four boxes of 32 keys each: box c takes keys 4l + c (l = 0..31) of the tile into
+          // rows 32c + l; the tile's scale words follow in one bulk copy (the last tile of the
+          // cache copies only the words that exist)
+          const int64_t left = static_cast<int64_t>(a.B) * a.E_cap - row64;
+          const uint32_t sc_bytes = left >= kTile ? kMxScaleSlot : static_cast<uint32_t>(left) * 4u;
+          mbar_arrive_expect_tx(&full[st], 4 * kMxBoxBytes + sc_bytes);
+          const int r4 = static_cast<int>(row64 / 4);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_load_3d_hint(dst + c * 4096, &kmap, &full[st], 0, c, r4, pol);
+          bulk_g2s(sSc + static_cast<size_t>(st) * kMxScaleSlot, static_cast<const uint32_t*>(a.kscale) + row64,
+                   sc_bytes, &full[st]);
+          return true;
+        }
+        mbar_arrive_expect_tx(&full[st], L.stage_bytes);
+        const int row = static_cast<int>(row64);
         // innermost coordinate 0 or 64 elements: always 16-byte aligned
         tma_load_2d_hint(dst, &kmap, &full[st], 0, row, pol);
         if constexpr (!FP8) tma_load_2d_hint(dst + 16384, &kmap, &full[st], 64, row, pol);
@@ -334,17 +383,34 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       }
       const bool q_ok = mbar_wait_b(qbar, 0, a.err, sAbort, a.wait_ns);
       if (q_ok && n_it > 0) {
-        const uint32_t idesc = FP8 ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
+        const uint32_t idesc = F8Q ? idesc_e4m3(kTile, N) : idesc_bf16(kTile, N, false, false);
         const uint32_t bBase = smem_u32(sB);
+        bool s_ok = true;
+        if constexpr (MX) {  // the query side's scales, stored by the first epilogue group
+          s_ok = mbar_wait_b(sbar, 0, a.err, sAbort, a.wait_ns);
+          tc_fence_after();
+        }
         int committed = 0;
-        for (int it = 0; it < n_it; ++it) {
+        for (int it = 0; s_ok && it < n_it; ++it) {
           const int st = it % S, acc = it % NA;
           if (!mbar_wait_b(&full[st], (it / S) & 1, a.err, sAbort, a.wait_ns)) break;
           if (!mbar_wait_b(&tempty[acc], ((it / NA) & 1) ^ 1, a.err, sAbort, a.wait_ns)) break;
           tc_fence_after();
           const uint32_t aBase = smem_u32(sA + static_cast<size_t>(st) * L.stage_bytes);
           const uint32_t d = tmem + static_cast<uint32_t>(acc * N);
-          if constexpr (FP8) {
+          if constexpr (MX) {
+            // the tile's key scales into this accumulator's group, then D = k . hi (+)= k . lo
+            // with the key scale byte of K block ks & 3
+            const uint32_t sfa = tmem + sf0 + 8u * static_cast<uint32_t>(acc);
+            tmem_cp_32x128b_w4(sfa, smem_desc_plain(smem_u32(sSc + static_cast<size_t>(st) * kMxScaleSlot)));
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t koff = (ks & 3) * 32u;
+              const uint32_t boff = (ks >> 2) * static_cast<uint32_t>(N * 128) + koff;
+              mma_mx(d, smem_desc(aBase + koff, 16, 1024), smem_desc(bBase + boff, 16, 1024),
+                     idesc_mx_e2m1_e4m3(kTile, N, static_cast<uint32_t>(ks & 3), 0u), sfa, tmem + sfb_col, ks > 0);
+            }
+          } else if constexpr (FP8) {
             // D = k . hi (+)= k . lo: the same key descriptors against both query terms
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -378,8 +444,17 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
     const int g_lo = gpt == 2 ? ch * gh : 0, g_hi = gpt == 2 ? min(G, g_lo + gh) : G;
     const int rin = q * 32 + lane;
     uint32_t* hist_row = hist ? a.hist_out + qrow0 * kTopkHistRowWords : nullptr;
+    if (MX && gq == 0) {
+      // the B scales: 2^0 (byte 127) in 8 columns of this warp's 32 lanes
+      const uint32_t sb = tmem + (static_cast<uint32_t>(q * 32) << 16) + sfb_col;
+      tmem_st4(sb, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st4(sb + 4u, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sbar);
+    }
     if (img_cta) {
-      build_image_cta<FP8>(a, L, sB, b, tid - 64);
+      build_image_cta<F8Q>(a, L, sB, b, tid - 64);
       fence_proxy_async_smem();
       mbar_arrive(qbar);
     }
@@ -389,7 +464,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       const bool own_new =
           e_new >= 0 && n_it > 0 && static_cast<int64_t>(tile_lo + (n_it - 1) * tile_step) == e_new / kTile;
       if (own_new && gp == 0) {
-        const float sc = decode_new_key<FP8>(a, b, e_new, tid - 64, sRed4, 7);
+        const float sc = decode_new_key<KF>(a, b, e_new, tid - 64, sRed4, 7);
         if (tid == 64) {
           *sNewScale = sc;
           mbar_arrive(kbar);
@@ -399,7 +474,7 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       if (e_new >= 0) decode_new_kv(a, b, e_new, tid - 64, split, L.n_splits);
     }
     const bool w_ok = __all_sync(0xffffffffu, mbar_wait_b(qbar, 0, a.err, sAbort, a.wait_ns));  // gates landed with the image
-    const float* kscale_b = FP8 ? a.kscale + static_cast<int64_t>(b) * a.E_cap : nullptr;
+    const float* kscale_b = FP8 ? static_cast<const float*>(a.kscale) + static_cast<int64_t>(b) * a.E_cap : nullptr;
     const int32_t* cand_b = !FUSE && a.cand ? a.cand + static_cast<int64_t>(qrow0) * a.n_cand : nullptr;
     // the key row of slot sx: the slot itself, or (candidate mode) its position (-1: none)
     auto pos_of = [&](int64_t sx) -> int64_t {
@@ -418,7 +493,8 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
       // (waits are made warp-uniform: the TMEM loads and the histogram below are warp-wide)
       if (!__all_sync(0xffffffffu, mbar_wait_b(&tfull[acc], (it / NA) & 1, a.err, sAbort, a.wait_ns))) break;
       tc_fence_after();
-      const int64_t s = static_cast<int64_t>(tile_lo + it * tile_step) * kTile + rin;
+      // the key in this lane's row: the tile's row rin (MXFP4 tiles hold key 4 * lane + q there)
+      const int64_t s = static_cast<int64_t>(tile_lo + it * tile_step) * kTile + (MX ? 4 * lane + q : rin);
       float ksc_use = ksc;
       if (FUSE && FP8 && __any_sync(0xffffffffu, s == e_new)) {  // the key compressed in this launch
         if (!__all_sync(0xffffffffu, mbar_wait_b(kbar, 0, a.err, sAbort, a.wait_ns))) break;
@@ -487,30 +563,45 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
 TcLayout plan_tc(const IndexerArgs& a) {
   TcLayout L{};
   const bool fp8 = a.kidx == CSA_E4M3;
+  const bool mx = a.kidx == CSA_MXFP4;
   L.G = std::max(1, std::min({256 / a.HI, a.T, kMaxG}));
+  // MXFP4 keys also keep scale groups in TMEM (8 columns per accumulator + 8): two
+  // accumulators and those must fit the CTA's share
+  if (mx) L.G = std::max(1, std::min(L.G, (512 - 24) / (2 * a.HI)));
+  const int64_t n_cols = a.cand ? a.n_cand : a.E_cap;  // candidate slots or cache positions
+  const int tiles = static_cast<int>((n_cols + kTile - 1) / kTile);
+  auto groups_of = [&](int G) { return static_cast<int64_t>(a.B) * ((a.T + G - 1) / G); };
+  // few long rows (decode): two CTAs per SM, key range split over them
+  bool decode_like = groups_of(L.G) < a.num_sms;
+  if (mx && decode_like) {
+    L.G = std::max(1, std::min(L.G, (256 - 24) / (2 * a.HI)));
+    decode_like = groups_of(L.G) < a.num_sms;
+  }
   L.N = L.G * a.HI;
   L.b_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * 256, 1024));  // bf16 rows or hi+lo
   L.w_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(L.N) * 4, 16));
-  L.stage_bytes = fp8 ? kKeyTileBytesF8 : 32768u;
+  L.stage_bytes = (fp8 || mx) ? kKeyTileBytesF8 : 32768u;
   L.n_qgroups = (a.T + L.G - 1) / L.G;
-  const int64_t n_cols = a.cand ? a.n_cand : a.E_cap;  // candidate slots or cache positions
-  const int tiles = static_cast<int>((n_cols + kTile - 1) / kTile);
-  const int64_t groups = static_cast<int64_t>(a.B) * L.n_qgroups;
-  // few long rows (decode): two CTAs per SM, key range split over them
-  const bool decode_like = groups < a.num_sms;
+  const int64_t groups = groups_of(L.G);
   const size_t misc = 1024 + align_up(L.w_bytes, 1024) + 64 + 32 * 8 + 64 +
                       ((a.hist_out || a.fuse.on) && L.G == 1 ? kTopkHistBins * 4 : 0);
   const size_t budget = decode_like ? (113 * 1024) : (227 * 1024);
-  int S = static_cast<int>((budget - misc - L.b_bytes) / L.stage_bytes);
+  const size_t per_stage = L.stage_bytes + (mx ? kMxScaleSlot : 0);
+  int S = static_cast<int>((budget - misc - L.b_bytes) / per_stage);
   S = std::max(2, std::min(S, 8));
   L.stages = S;
   L.wide = !decode_like;  // one CTA per SM
-  L.smem_bytes = static_cast<uint32_t>(misc + L.b_bytes + static_cast<size_t>(S) * L.stage_bytes);
+  L.smem_bytes = static_cast<uint32_t>(misc + L.b_bytes + static_cast<size_t>(S) * per_stage);
   // as many accumulators (2..4) as the TMEM share of this CTA (512 columns per SM) holds
   const int share = decode_like ? 256 : 512;
-  L.n_acc = std::max(2, std::min(4, share / L.N));
+  auto cols_needed = [&](int na) {
+    const int acc = na * L.N;
+    return mx ? ((acc + 7) & ~7) + 8 * na + 8 : acc;
+  };
+  L.n_acc = 2;
+  while (L.n_acc < 4 && cols_needed(L.n_acc + 1) <= share) ++L.n_acc;
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(L.n_acc * L.N)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(cols_needed(L.n_acc))) cols <<= 1;
   L.tmem_cols = cols;
   if (decode_like) {
     const int64_t target = 2 * static_cast<int64_t>(a.num_sms);
@@ -527,9 +618,12 @@ IndexerLayout indexer_layout(const IndexerArgs& a) { return plan_tc(a); }
 
 
 bool indexer_uses_tensor_cores(const IndexerArgs& a) {
+  if (a.act != CSA_BF16 || a.dI != 128) return false;
+  // MXFP4 keys: dense key ranges, 32 or 64 heads (the TMEM scale groups need the room)
+  if (a.kidx == CSA_MXFP4) return a.cand == nullptr && (a.HI == 32 || a.HI == 64);
   // candidate lists on the tensor cores for one query per sequence (the CSA2 Reindex step)
-  return (a.cand == nullptr || (a.T == 1 && !a.fuse.on && a.hist_out == nullptr)) && a.act == CSA_BF16 &&
-         a.dI == 128 && (a.HI == 32 || a.HI == 64 || a.HI == 128) && (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
+  return (a.cand == nullptr || (a.T == 1 && !a.fuse.on && a.hist_out == nullptr)) &&
+         (a.HI == 32 || a.HI == 64 || a.HI == 128) && (a.kidx == CSA_BF16 || a.kidx == CSA_E4M3);
 }
 
 size_t indexer_workspace_bytes(const IndexerArgs& a) {
@@ -543,18 +637,30 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
   const int64_t n_cols = a.cand ? a.n_cand : a.E_cap;
   if (rows == 0 || n_cols == 0) return cudaSuccess;
   if (indexer_uses_tensor_cores(a)) {
-    const bool fp8 = a.kidx == CSA_E4M3;
+    const int kf = a.kidx == CSA_MXFP4 ? kKeyMx : a.kidx == CSA_E4M3 ? kKeyE4m3 : kKeyBf16;
+    const bool f8q = kf != kKeyBf16;
     const TcLayout L = plan_tc(a);
     CUtensorMap map;
-    if (!encode_tmap_2d(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        const_cast<void*>(a.kI), 128, static_cast<uint64_t>(a.B) * a.E_cap, fp8 ? 128 : 256,
-                        fp8 ? 128 : 64, kTile))
-      return cudaErrorInvalidValue;
+    bool enc;
+    if (kf == kKeyMx) {
+      // packed E2M1 payload (64 B a key) unpacked by TMA into 8-bit slots; a 3D view whose box
+      // (128 codes, 1, 32) at (0, c, r) takes keys 4(r + l) + c, l = 0..31
+      const uint64_t dims[3] = {128, 4, static_cast<uint64_t>(a.B) * a.E_cap / 4};
+      const uint64_t strides[2] = {64, 256};
+      const uint32_t box[3] = {128, 1, 32};
+      enc = encode_tmap_generic(&map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(a.kI), dims, strides,
+                                box, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      enc = encode_tmap_2d(&map, kf == kKeyE4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           const_cast<void*>(a.kI), 128, static_cast<uint64_t>(a.B) * a.E_cap, kf == kKeyE4m3 ? 128 : 256,
+                           kf == kKeyE4m3 ? 128 : 64, kTile);
+    }
+    if (!enc) return cudaErrorInvalidValue;
     uint8_t* images = static_cast<uint8_t*>(a.ws);
     cudaError_t e = cudaSuccess;
     if (!a.images_ready && !image_in_cta(a, L)) {
       dim3 gq(L.n_qgroups, a.B, (L.N + 7) / 8);
-      e = fp8 ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
+      e = f8q ? launch_pdl(indexer_qprep_kernel<true>, gq, dim3(256), 0, s, a, L, images)
               : launch_pdl(indexer_qprep_kernel<false>, gq, dim3(256), 0, s, a, L, images);
       count_launches(1);
       if (e != cudaSuccess) return e;
@@ -563,26 +669,27 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
     static std::atomic<unsigned long long> attr{0};
     if (first_use_in_context(attr)) {
       const int mx = 227 * 1024;
-      cudaFuncSetAttribute(indexer_tc_kernel<true, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      cudaFuncSetAttribute(indexer_tc_kernel<false, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      cudaFuncSetAttribute(indexer_tc_kernel<true, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      cudaFuncSetAttribute(indexer_tc_kernel<false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      cudaFuncSetAttribute(indexer_tc_kernel<true, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      cudaFuncSetAttribute(indexer_tc_kernel<false, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+#define CSA_IDX_ATTR(KF, FU, MB) \
+  cudaFuncSetAttribute(indexer_tc_kernel<KF, FU, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)
+      CSA_IDX_ATTR(kKeyBf16, false, 2); CSA_IDX_ATTR(kKeyE4m3, false, 2); CSA_IDX_ATTR(kKeyMx, false, 2);
+      CSA_IDX_ATTR(kKeyBf16, true, 2);  CSA_IDX_ATTR(kKeyE4m3, true, 2);  CSA_IDX_ATTR(kKeyMx, true, 2);
+      CSA_IDX_ATTR(kKeyBf16, false, 1); CSA_IDX_ATTR(kKeyE4m3, false, 1); CSA_IDX_ATTR(kKeyMx, false, 1);
+#undef CSA_IDX_ATTR
     }
     const uint8_t* cimages = images;
     const dim3 blk(L.wide && !a.fuse.on ? tc_threads(1) : tc_threads(2));
     const size_t sm = L.smem_bytes;
-    if (a.fuse.on) {
-      e = fp8 ? launch_pdl(indexer_tc_kernel<true, true, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols)
-              : launch_pdl(indexer_tc_kernel<false, true, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols);
-    } else if (L.wide) {
-      e = fp8 ? launch_pdl(indexer_tc_kernel<true, false, 1>, grid, blk, sm, s, map, a, L, cimages, n_cols)
-              : launch_pdl(indexer_tc_kernel<false, false, 1>, grid, blk, sm, s, map, a, L, cimages, n_cols);
-    } else {
-      e = fp8 ? launch_pdl(indexer_tc_kernel<true, false, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols)
-              : launch_pdl(indexer_tc_kernel<false, false, 2>, grid, blk, sm, s, map, a, L, cimages, n_cols);
-    }
+#define CSA_IDX_LAUNCH(FU, MB)                                                                               \
+  (kf == kKeyMx     ? launch_pdl(indexer_tc_kernel<kKeyMx, FU, MB>, grid, blk, sm, s, map, a, L, cimages, n_cols)   \
+   : kf == kKeyE4m3 ? launch_pdl(indexer_tc_kernel<kKeyE4m3, FU, MB>, grid, blk, sm, s, map, a, L, cimages, n_cols) \
+                    : launch_pdl(indexer_tc_kernel<kKeyBf16, FU, MB>, grid, blk, sm, s, map, a, L, cimages, n_cols))
+    if (a.fuse.on)
+      e = CSA_IDX_LAUNCH(true, 2);
+    else if (L.wide)
+      e = CSA_IDX_LAUNCH(false, 1);
+    else
+      e = CSA_IDX_LAUNCH(false, 2);
+#undef CSA_IDX_LAUNCH
     count_launches(1);
     return e;
   }
@@ -603,7 +710,9 @@ cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
     else                            \
       CSA_SIMT(TQ, TK, 128);        \
   } while (0)
-  if (a.act == CSA_F32) {
+  if (a.kidx == CSA_MXFP4) {  // bf16 queries, dI = 128 (checked by the caller)
+    CSA_SIMT(__nv_bfloat16, MxKey, 128);
+  } else if (a.act == CSA_F32) {
     if (a.kidx == CSA_E4M3)
       CSA_SIMT_DI(float, uint8_t);
     else

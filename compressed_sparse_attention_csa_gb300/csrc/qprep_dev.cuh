@@ -130,10 +130,12 @@ __device__ __forceinline__ void compress_tail_any(const void* kv, const void* z,
 }
 
 // The new indexer-key entry e of sequence b (dI = 128), by 128 threads (one channel each,
-// t128 = 0..127, named barrier `bar`): stored as e4m3 codes with one fp32 scale (amax/448,
-// as the compressor does) or as bf16.  Returns the scale (1 for bf16 keys).  Every thread
-// fences its global writes for the TMA load of the same row that follows in this CTA.
-template <bool FP8>
+// t128 = 0..127, named barrier `bar`), stored as the compressor stores it: KF = 1, e4m3 codes
+// with one fp32 scale (amax/448); KF = 2, MXFP4 (per warp = block of 32 channels one UE8M0
+// scale byte, E2M1 codes two to a byte); KF = 0, bf16.  Returns the fp32 scale (1 unless
+// e4m3).  Every thread fences its global writes for the TMA loads of the same row that follow
+// in this CTA.
+template <int KF>
 __device__ __forceinline__ float decode_new_key(const IndexerArgs& a, int b, int64_t e, int t128, float* red4,
                                                 int bar) {
   const DecodeFuse& f = a.fuse;
@@ -146,7 +148,18 @@ __device__ __forceinline__ float decode_new_key(const IndexerArgs& a, int b, int
                        f.biasI, f.act_bf16, m, dI, c, e > 0, v);
   const int64_t row = static_cast<int64_t>(b) * a.E_cap + e;
   float scale = 1.f;
-  if constexpr (FP8) {
+  if constexpr (KF == 2) {
+    float am = fabsf(v[0]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const uint32_t sb = mx_e2m1_scale_byte(am);
+    const uint32_t code = e2m1_code(__fdiv_rn(v[0], ue8m0_value(sb)));
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+    if ((t128 & 1) == 0)
+      static_cast<uint8_t*>(const_cast<void*>(a.kI))[row * (dI / 2) + t128 / 2] = static_cast<uint8_t>(code | (hi << 4));
+    if ((t128 & 31) == 0)
+      static_cast<uint8_t*>(const_cast<void*>(a.kscale))[row * (dI / 32) + t128 / 32] = static_cast<uint8_t>(sb);
+  } else if constexpr (KF == 1) {
     float am = fabsf(v[0]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -155,7 +168,7 @@ __device__ __forceinline__ float decode_new_key(const IndexerArgs& a, int b, int
     am = fmaxf(fmaxf(red4[0], red4[1]), fmaxf(red4[2], red4[3]));
     scale = am > 0.f ? __fdiv_rn(am, 448.f) : 1.f;
     static_cast<uint8_t*>(const_cast<void*>(a.kI))[row * dI + t128] = f_to_e4m3(__fdiv_rn(v[0], scale));
-    if (t128 == 0) const_cast<float*>(a.kscale)[row] = scale;
+    if (t128 == 0) static_cast<float*>(const_cast<void*>(a.kscale))[row] = scale;
   } else {
     static_cast<__nv_bfloat16*>(const_cast<void*>(a.kI))[row * dI + t128] = __float2bfloat16_rn(v[0]);
   }

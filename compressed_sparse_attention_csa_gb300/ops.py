@@ -35,12 +35,13 @@ class Config:
     act: torch.dtype = torch.bfloat16          # torch.float32 or torch.bfloat16
     fp8_keys: bool = False                     # indexer keys stored as e4m3 + fp32 scale
     softmax_scale: Optional[float] = None      # default 1/sqrt(d)
+    mx_keys: bool = False                      # indexer keys stored as MXFP4 (payload + scale words)
 
     def c(self) -> L.csa_config:
         act = L.CSA_F32 if self.act == torch.float32 else L.CSA_BF16
         scale = self.softmax_scale if self.softmax_scale is not None else self.d ** -0.5
-        return L.csa_config(self.B, self.H, self.d, self.HI, self.dI, self.m, self.k, self.W, act,
-                            L.CSA_E4M3 if self.fp8_keys else act, scale)
+        kidx = L.CSA_MXFP4 if self.mx_keys else L.CSA_E4M3 if self.fp8_keys else act
+        return L.csa_config(self.B, self.H, self.d, self.HI, self.dI, self.m, self.k, self.W, act, kidx, scale)
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -118,7 +119,9 @@ def workspace_size(op: int, cfg: Config, rows: int, n_cols: int) -> int:
 
 def compress_kv(cfg: Config, kv: torch.Tensor, z: torch.Tensor, bias: torch.Tensor, tok0: int, ent_begin: int,
                 ent_end: int, out: torch.Tensor, out_scale: Optional[torch.Tensor] = None) -> None:
-    """csa_compress_kv: kv, z [B, n_tok, 2, dim]; bias [2, m, dim] fp32; out [B, E_cap, dim]."""
+    """csa_compress_kv: kv, z [B, n_tok, 2, dim]; bias [2, m, dim] fp32; out [B, E_cap, dim] (fp32,
+    bf16, or e4m3 codes with out_scale [B, E_cap] fp32), or MXFP4 keys: out [B, E_cap, dim/2]
+    uint8 payload with out_scale [B, E_cap] int32 scale words."""
     lib = L.load()
     c = cfg.c()
     dim = kv.shape[-1]
@@ -127,7 +130,7 @@ def compress_kv(cfg: Config, kv: torch.Tensor, z: torch.Tensor, bias: torch.Tens
     elif out.dtype == torch.bfloat16:
         od = L.CSA_BF16
     elif out.dtype == torch.uint8:
-        od = L.CSA_E4M3
+        od = L.CSA_MXFP4 if out.shape[-1] * 2 == dim else L.CSA_E4M3
     else:
         raise ValueError("out dtype")
     _check("csa_compress_kv", lib.csa_compress_kv(ctypes.byref(c), dim, _p(kv), _p(z), _p(bias), kv.shape[1], tok0,

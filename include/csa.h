@@ -47,7 +47,13 @@ typedef enum {
   CSA_ERR_INDEX = 8        /* a selected index was >= E_cap (the row was skipped)          */
 } csa_status;
 
-typedef enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2 } csa_dtype;
+/* CSA_MXFP4 is a storage format of indexer keys only (csa_config.kidx, csa_compress_kv's
+ * out_dtype): per key of 128 channels, 64 payload bytes of E2M1 codes (channel 2i in the low
+ * nibble of byte i) and, in a separate array, 4 UE8M0 scale bytes (byte j for channels
+ * 32j .. 32j+31, value 2^(byte - 127)) kept as one little-endian 32-bit word: 68 bytes a key
+ * (V4.1 diagram, byte ledger "Single request / logical serving KV storage": "Indexer K:
+ * 128 channels, MXFP4, 64 packed bytes + 4 UE8M0 scales"). */
+typedef enum { CSA_F32 = 0, CSA_BF16 = 1, CSA_E4M3 = 2, CSA_MXFP4 = 3 } csa_dtype;
 
 typedef struct {
   int32_t B, H, d;      /* sequences, query heads, head dim (= compressed entry dim)        */
@@ -56,7 +62,8 @@ typedef struct {
   int32_t k;            /* entries kept by the top-k                                        */
   int32_t W;            /* sliding-window length                                            */
   csa_dtype act;        /* CSA_F32 or CSA_BF16: q, qI, KV streams, caches, window, output   */
-  csa_dtype kidx;       /* storage of indexer keys: == act, or CSA_E4M3 (+ fp32 row scale)  */
+  csa_dtype kidx;       /* indexer keys: == act, CSA_E4M3 (+ fp32 row scale), or CSA_MXFP4
+                           (act == CSA_BF16, dI == 128, HI 32 or 64; E_cap % 4 == 0)       */
   float softmax_scale;  /* attention logit scale, e.g. 1/sqrt(d)                            */
 } csa_config;
 
@@ -90,14 +97,19 @@ size_t csa_workspace_size(csa_op op, const csa_config *cfg, int64_t rows, int64_
  *   bias       : [2, m, dim] fp32 — B^a, B^b by position inside the block
  *   ent_begin, ent_end : entries to produce; needs tok0 <= m*max(ent_begin-1, 0) and
  *                m*ent_end <= tok0 + n_tok (else CSA_ERR_SHAPE)
- *   out        : [B, E_cap, dim] in out_dtype (CSA_F32, CSA_BF16 or CSA_E4M3); entry i is
+ *   out        : [B, E_cap, dim] in out_dtype (CSA_F32, CSA_BF16 or CSA_E4M3), or
+ *                [B, E_cap, dim/2] E2M1 payload bytes for CSA_MXFP4 (dim == 128); entry i is
  *                written at row i, rows outside [ent_begin, ent_end) are untouched
- *   out_scale  : [B, E_cap] fp32, required iff out_dtype == CSA_E4M3 (scale = amax/448,
- *                code = e4m3_rn_satfinite(x / scale); an all-zero row gets scale 1)
+ *   out_scale  : CSA_E4M3: [B, E_cap] fp32 (scale = amax/448, code = e4m3_rn_satfinite(x /
+ *                scale); an all-zero row gets scale 1).  CSA_MXFP4: [B, E_cap] 32-bit words of
+ *                4 UE8M0 bytes, per 32 channels X = 2^(floor(log2(amax)) - 2) (the OCP MX
+ *                rule; exponent clamped to [-127, 127], an all-zero block gets 2^-127) and
+ *                code = nearest E2M1 value of x / X (ties to even, saturating at 6, sign kept).
+ *                Required iff out_dtype is one of the two; 16-byte aligned.
  */
 csa_status csa_compress_kv(const csa_config *cfg, int32_t dim, const void *kv, const void *z,
                            const float *bias, int64_t n_tok, int64_t tok0, int64_t ent_begin,
-                           int64_t ent_end, void *out, csa_dtype out_dtype, float *out_scale,
+                           int64_t ent_end, void *out, csa_dtype out_dtype, void *out_scale,
                            int64_t E_cap, csa_stream_t stream);
 
 /*
@@ -127,16 +139,20 @@ csa_status csa_compress_kv_single(const csa_config *cfg, int32_t dim, const void
  * column of the row is set to -inf.
  *
  *   qI     : [B, T, HI, dI] (cfg->act);  w : [B, T, HI] fp32;  q_pos : [B*T] int64
- *   kI     : [B, E_cap, dI] in cfg->kidx; kscale : [B, E_cap] fp32 iff kidx == CSA_E4M3
+ *   kI     : [B, E_cap, dI] in cfg->kidx ([B, E_cap, 64] payload bytes for CSA_MXFP4, 32-byte
+ *            aligned); kscale : [B, E_cap] fp32 iff kidx == CSA_E4M3, [B, E_cap] 32-bit
+ *            UE8M0 scale words iff kidx == CSA_MXFP4 (see csa_dtype), else NULL
  *   cand   : NULL — score every column s in [0, n_cols) with n_cols = E_cap;
  *            else [B*T, n_cand] int32 positions (CSA2 Reindex: a candidate pool); column j
  *            scores position cand[r, j]; cand < 0 or >= nv gives -inf.
  *   scores : [B*T, ld_scores] fp32, ld_scores >= n_cols (E_cap or n_cand)
  * bf16 keys with dI == 128 run on the tcgen05 tensor cores (fp32 accumulate); E4M3 keys run
- * the FP8 tensor-core path with qI split into two E4M3 terms; otherwise a CUDA-core path.
+ * the FP8 tensor-core path with qI split into two E4M3 terms; MXFP4 keys run the block-scaled
+ * tensor-core path (E2M1 keys x the two E4M3 query terms, the keys' UE8M0 scales applied by
+ * the MMA; "FP4, down to the index scores"); otherwise a CUDA-core path.
  */
 csa_status csa_indexer_scores(const csa_config *cfg, const void *qI, const float *w, int32_t T,
-                              const int64_t *q_pos, const void *kI, const float *kscale,
+                              const int64_t *q_pos, const void *kI, const void *kscale,
                               int64_t E_cap, const int32_t *cand, int32_t n_cand, float *scores,
                               int64_t ld_scores, void *ws, size_t ws_bytes, csa_stream_t stream);
 
@@ -153,7 +169,7 @@ csa_status csa_indexer_scores(const csa_config *cfg, const void *qI, const float
  * separate calls run on them.
  */
 csa_status csa_indexer_topk(const csa_config *cfg, const void *qI, const float *w, int32_t T,
-                            const int64_t *q_pos, const void *kI, const float *kscale, int64_t E_cap,
+                            const int64_t *q_pos, const void *kI, const void *kscale, int64_t E_cap,
                             int32_t *idx, void *ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
@@ -391,8 +407,8 @@ typedef struct {
   const float *w;            /* [B, HI]                                                       */
   const float *sink;         /* [H]                                                           */
   void *kv_comp;             /* [B, E_cap, d]    row (t+1)/m - 1 rewritten when (t+1) % m == 0 */
-  void *kI;                  /* [B, E_cap, dI]   (cfg->kidx), same row                         */
-  float *kscale;             /* [B, E_cap] iff kidx == CSA_E4M3                               */
+  void *kI;                  /* [B, E_cap, dI]   (cfg->kidx; MXFP4: [B, E_cap, 64]), same row  */
+  void *kscale;              /* [B, E_cap] fp32 (CSA_E4M3) or scale words (CSA_MXFP4)         */
   const void *kv_tail;       /* [B, 2m, 2, d]  C^a/C^b of tokens t-2m+1 .. t                  */
   const void *z_tail;        /* [B, 2m, 2, d]  Z^a/Z^b of the same tokens                     */
   const void *kvI_tail;      /* [B, 2m, 2, dI] indexer-key streams of the same tokens          */

@@ -13,7 +13,9 @@ CUDA device, with identical bits:
 Values are drawn in float64 and then rounded once to the storage dtype by torch's own
 round-to-nearest-even conversion.  Indexer keys stored as FP8 e4m3 get one fp32 scale
 per entry, scale = amax / 448, codes = e4m3(x / scale); that is the input recipe, not a
-step of the method.
+step of the method.  Indexer keys stored as MXFP4 are drawn as codes: uniform random
+payload bytes (every E2M1 code equally likely) and per 32 channels a scale byte uniform in
+121 .. 124 (2^-6 .. 2^-3, the range the N(0, 1/128) keys' blocks take).
 
 The tensors and their distributions follow the workload descriptions of the CSA
 pages: q, qI, the a/b KV and gate streams, compressed caches and window rows are
@@ -58,6 +60,16 @@ def uniform01(seed: int, counter: torch.Tensor) -> torch.Tensor:
     """Uniform float64 in the open interval (0, 1)."""
     top53 = _lsr(splitmix64(seed, counter), 11).to(torch.float64)
     return (top53 + 0.5) * (2.0 ** -53)
+
+
+def random_bytes(seed: int, numel: int, *, device="cpu", offset: int = 0, chunk: int = 1 << 23) -> torch.Tensor:
+    """Flat uint8 tensor: the low byte of splitmix64 for elements offset .. offset+numel-1."""
+    out = torch.empty(numel, dtype=torch.uint8, device=device)
+    for lo in range(0, numel, chunk):
+        hi = min(numel, lo + chunk)
+        e = torch.arange(offset + lo, offset + hi, dtype=torch.int64, device=device)
+        out[lo:hi] = torch.bitwise_and(splitmix64(seed, e), 0xFF).to(torch.uint8)
+    return out
 
 
 def _tensor_seed(base: int, tensor_id: int) -> int:
@@ -111,7 +123,7 @@ class CsaConfig:
     W: int            # sliding window
     T: int            # query tokens per sequence, at t = N-T .. N-1
     act: str          # "f32" | "bf16": dtype of q, qI, KV streams, caches, window rows
-    kidx: str         # "act" | "fp8": storage of the indexer keys
+    kidx: str         # "act" | "fp8" | "mxfp4": storage of the indexer keys
     mode: str         # "full" | "decode" | "prefill" | "csa2" | "hca_full" | "hca_decode" | "hca_prefill"
     pool_block: int = 8
     pool_blocks: int = 2048
@@ -181,13 +193,17 @@ CONFIGS: Dict[int, CsaConfig] = {
     12: CsaConfig(12, "V4-Flash CSA decode @1M ctx, FP8 indexer keys + FP8 main-KV entries (576 B)",
                   B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
                   act="bf16", kidx="fp8", mode="decode"),
+    # the 1M decode step with FP4 indexer keys: MXFP4, 64 payload bytes + 4 UE8M0 scales a key
+    13: CsaConfig(13, "CSA decode @1M ctx (B 4, MXFP4 indexer keys: 64 B + 4 UE8M0 scales)",
+                  B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
+                  act="bf16", kidx="mxfp4", mode="decode"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)
 _IDS = {
     "q": 1, "qI": 2, "w": 3, "sink": 4, "kv_local": 5, "kv_comp": 6, "kI": 7,
     "kv_str": 8, "z_str": 9, "kvI_str": 10, "zI_str": 11, "bias": 12, "biasI": 13,
-    "qI_full": 14, "w_full": 15,
+    "qI_full": 14, "w_full": 15, "kI_mx": 16, "kscale_mx": 17,
 }
 
 
@@ -211,6 +227,18 @@ def quantize_keys_e4m3(x: torch.Tensor):
     return codes, scale
 
 
+def mxfp4_keys(cfg: CsaConfig, B: int, E: int, dI: int, device, row0: int = 0):
+    """Drawn MXFP4 keys: payload [B, E, dI/2] uint8 and the scale bytes of every key as one
+    little-endian word (byte j for channels 32j .. 32j+31), [B, E] int32 (dI = 128)."""
+    payload = random_bytes(_tensor_seed(cfg.seed, _IDS["kI_mx"]), B * E * dI // 2, device=device,
+                           offset=row0 * E * dI // 2).reshape(B, E, dI // 2)
+    sb = random_bytes(_tensor_seed(cfg.seed, _IDS["kscale_mx"]), B * E * 4, device=device,
+                      offset=row0 * E * 4).reshape(B, E, 4)
+    sb = (121 + torch.bitwise_and(sb, 3)).to(torch.int32)
+    words = sb[..., 0] | (sb[..., 1] << 8) | (sb[..., 2] << 16) | (sb[..., 3] << 24)
+    return payload, words
+
+
 def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict[str, torch.Tensor]:
     """All input tensors of one preset, generated on `device`.
 
@@ -221,7 +249,8 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
     Keys (shapes use B, T, H, d, HI, dI, E = N // m, L = window rows held):
       q [B,T,H,d], qI [B,T,HI,dI], w [B,T,HI] f32, sink [H] f32, q_pos [B*T] i64,
       kv_local [B,L,d], local_base [B] i64,
-      kv_comp [B,E,d], kI [B,E,dI] (or kI codes u8 + kscale [B,E] f32 for FP8),
+      kv_comp [B,E,d], kI [B,E,dI] (or kI codes u8 + kscale [B,E] f32 for FP8, or
+      kI payload u8 [B,E,dI/2] + kscale [B,E] i32 scale words for MXFP4),
       compression streams kv_str/z_str [B,n_str,2,d], kvI_str/zI_str [B,n_str,2,dI],
       bias [2,m,d] f32, biasI [2,m,dI] f32, str_base [B] i64 (token of stream row 0).
     CSA2 presets add per-layer q/kv_local/sink stacks and the Full-layer indexer query.
@@ -267,7 +296,13 @@ def make_inputs(cfg: CsaConfig, device="cpu", *, skip=(), row0: int = 0) -> Dict
             out["kv_comp"] = torch.zeros((B, E, d), dtype=act, device=device)
         else:
             out["kv_comp"] = _gen(cfg, "kv_comp", (B, E, d), 1 / math.sqrt(d), act, device, row0=row0)
-    if "kI" not in skip:
+    if "kI" not in skip and cfg.kidx == "mxfp4":
+        if cfg.mode == "full":
+            out["kI"] = torch.zeros((B, E, dI // 2), dtype=torch.uint8, device=device)
+            out["kscale"] = torch.zeros((B, E), dtype=torch.int32, device=device)
+        else:
+            out["kI"], out["kscale"] = mxfp4_keys(cfg, B, E, dI, device, row0)
+    elif "kI" not in skip:
         if cfg.mode == "full":
             kI = torch.zeros((B, E, dI), dtype=f32, device=device)
         else:

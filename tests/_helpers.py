@@ -10,7 +10,8 @@ from oracle import csa_oracle as O
 
 def lib_config(cfg, **kw) -> Config:
     c = Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
-               act=cfg.torch_act, fp8_keys=(cfg.kidx == "fp8"), softmax_scale=cfg.softmax_scale)
+               act=cfg.torch_act, fp8_keys=(cfg.kidx == "fp8"), softmax_scale=cfg.softmax_scale,
+               mx_keys=(cfg.kidx == "mxfp4"))
     for k, v in kw.items():
         setattr(c, k, v)
     return c
@@ -22,7 +23,11 @@ def np64(t: torch.Tensor) -> np.ndarray:
 
 
 def keys_f64(kI: torch.Tensor, kscale=None) -> np.ndarray:
-    """Dequantised indexer keys as the oracle reads them."""
+    """Dequantised indexer keys as the oracle reads them (MXFP4: uint8 payload [.., dI/2] with
+    int32 scale words)."""
+    if kI.dtype == torch.uint8 and kscale is not None and kscale.dtype == torch.int32:
+        words = kscale.cpu().numpy().view(np.uint32)
+        return O.mxfp4_key_decode(kI.cpu().numpy(), O.mxfp4_key_unwords(words))
     if kI.dtype == torch.uint8:
         return O.e4m3_decode(kI.cpu().numpy()) * kscale.cpu().numpy().astype(np.float64)[..., None]
     return np64(kI)
@@ -110,11 +115,12 @@ def oracle_decode(cfg, inp):
     """The oracle's decode step for every sequence of the batch."""
     nb = np_inputs(inp)
     fp8 = cfg.kidx == "fp8"
+    mx = cfg.kidx == "mxfp4"
     res = []
     for b in range(cfg.B):
-        kdeq = keys_f64(inp["kI"][b], inp["kscale"][b] if fp8 else None)
+        kdeq = keys_f64(inp["kI"][b], inp["kscale"][b] if (fp8 or mx) else None)
         kvc = nb["kv_comp"][b].copy()
-        r = O.decode_step_sequence(cfg, nb, b, kvc, kdeq, fp8_keys=fp8)
+        r = O.decode_step_sequence(cfg, nb, b, kvc, kdeq, fp8_keys=fp8, mx_keys=mx)
         r["kv_comp"] = kvc
         r["q"] = nb["q"][b, 0]
         res.append(r)
@@ -139,7 +145,7 @@ def assert_step_selection_exact(cfg, ref, idx, scores_out):
     """The decode step's selection is exactly the top-k (score desc, position asc; ascending,
     -1 padded) of the fp32 scores it wrote, and those scores match the oracle's within the
     indexer tolerance, -inf past the visible entries."""
-    rtol_s = 5e-2 if cfg.kidx == "fp8" else 1e-2
+    rtol_s = 5e-2 if cfg.kidx in ("fp8", "mxfp4") else 1e-2
     for b in range(cfg.B):
         nv = ref[b]["nv"]
         s32 = scores_out[b].cpu().numpy()
@@ -153,7 +159,7 @@ def assert_decode_matches(cfg, inp, ref, out, lse, idx):
     """Decode-step agreement per sequence: selection valid up to score-tolerance swaps, output
     within 2e-2 of the row maximum plus the swaps' first-order effect, LSE within 5e-3, and
     the compressed entry (when the token completed a block) within bf16 rounding."""
-    rtol_s = 5e-2 if cfg.kidx == "fp8" else 1e-2
+    rtol_s = 5e-2 if cfg.kidx in ("fp8", "mxfp4") else 1e-2
     for b in range(cfg.B):
         r = ref[b]
         fin = r["scores"][np.isfinite(r["scores"])]

@@ -132,3 +132,29 @@ def test_decode_step_reset_argument_errors(lib):
     assert f(ctypes.byref(c), A, need - 1, None) == 5
     # the state region is at the front of the step's own workspace
     assert lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), 3, 262144) >= need
+
+
+def test_mxfp4_key_argument_errors(lib):
+    f = lib.csa_indexer_scores
+    mx = _cfg(kidx=L.CSA_MXFP4)
+    A32 = ctypes.c_void_p(0x10020)                 # 32-byte aligned
+    A16 = ctypes.c_void_p(0x10010)                 # 16-byte but not 32-byte aligned
+    assert f(ctypes.byref(mx), A, A, 1, A, A32, None, 100, None, 0, A, 100, None, 0, None) == 1   # scale words
+    assert f(ctypes.byref(mx), A, A, 1, A, A16, A, 100, None, 0, A, 100, None, 0, None) == 4      # payload alignment
+    assert f(ctypes.byref(mx), A, A, 1, A, A32, A, 102, None, 0, A, 102, None, 0, None) == 2      # E_cap % 4
+    assert f(ctypes.byref(_cfg(kidx=L.CSA_MXFP4, act=L.CSA_F32)), A, A, 1, A, A32, A, 100, None, 0, A, 100,
+             None, 0, None) == 3                                                                  # bf16 queries only
+    assert f(ctypes.byref(_cfg(kidx=L.CSA_MXFP4, dI=64)), A, A, 1, A, A32, A, 100, None, 0, A, 100,
+             None, 0, None) == 2                                                                  # 128 channels
+    g = lib.csa_compress_kv
+    assert g(ctypes.byref(mx), 128, A, A, A, 12, 4, 2, 4, A, L.CSA_MXFP4, None, 8, None) == 1    # scale words
+    assert g(ctypes.byref(mx), 64, A, A, A, 12, 4, 2, 4, A, L.CSA_MXFP4, A, 8, None) == 2        # dim 128 only
+    args = L.csa_decode_args()
+    for name, _ in L.csa_decode_args._fields_:
+        if name not in ("E_cap", "L", "kscale", "lse", "idx_out", "scores_out"):
+            setattr(args, name, 0x10020)
+    args.E_cap, args.L = 1 << 16, 128
+    assert lib.csa_decode_step(ctypes.byref(mx), ctypes.byref(args), A, 1 << 30, None) == 1        # scale words
+    args.kscale = 0x10020
+    args.E_cap = (1 << 16) + 2
+    assert lib.csa_decode_step(ctypes.byref(mx), ctypes.byref(args), A, 1 << 30, None) == 2        # E_cap % 4
