@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11, 12])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -88,6 +88,7 @@ _DENSE_STAGE = (("attn_hca_dec_kernel", "attn_merge_wide_kernel"), ("k_attn.cu",
 # config -> (summary file, kernels of the stage, sources the summary's counters were taken with)
 STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE_1Q,
                   12: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE_1Q,
+                  13: ("indexer_tc_mxfp4_1M_decode.md",) + _INDEXER_STAGE_1Q,
                   2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE_1Q,
                   3: ("indexer_tc_bf16_prefill_4K.md",) + _INDEXER_STAGE,
                   5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE_1Q,
@@ -217,15 +218,19 @@ class Decode:
         self.metric = "CSA decode tok/s @1M ctx" if cfg.N == 1 << 20 else "CSA decode tok/s @64K ctx"
         if self.FP8KV:
             self.metric += ", FP8 main-KV entries"
+        if cfg.kidx == "mxfp4":
+            self.metric += ", MXFP4 indexer keys"
+        keys = {"fp8": "FP8 e4m3 indexer keys + fp32 scale",
+                "mxfp4": "MXFP4 indexer keys (64 B E2M1 + 4 UE8M0 scales)"}.get(cfg.kidx, "bf16 indexer keys")
         self.workload = (f"V4-Flash CSA decode step, batch {cfg.B} @ {cfg.N:,}-token context "
                          f"({cfg.E:,} entries/seq), " +
-                         ("FP8 e4m3 indexer keys + fp32 scale" if cfg.kidx == "fp8" else "bf16 indexer keys") +
+                         keys +
                          (", FP8 main-KV entries (448 e4m3 + 64 bf16 dims, 576 B)" if self.FP8KV else ", bf16 KV") +
                          f", {cfg.H}x{cfg.d} heads, indexer {cfg.HI}x{cfg.dI}, k {cfg.k}, W {cfg.W}")
         self.config_extra = {"batch": cfg.B, "context": cfg.N, "m": cfg.m, "entries_per_seq": cfg.E,
                              "heads": cfg.H, "head_dim": cfg.d, "indexer": f"{cfg.HI}x{cfg.dI}", "top_k": cfg.k,
                              "window": cfg.W,
-                             "indexer_keys": "e4m3+fp32 scale" if cfg.kidx == "fp8" else "bf16",
+                             "indexer_keys": {"fp8": "e4m3+fp32 scale", "mxfp4": "MXFP4 E2M1+UE8M0/32"}.get(cfg.kidx, "bf16"),
                              "kv_entries": "FP8 (576 B)" if self.FP8KV else "bf16 (1 KiB)"}
         if host_only:
             return
@@ -233,7 +238,8 @@ class Decode:
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
         self.c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
-                            act=torch.bfloat16, fp8_keys=cfg.kidx == "fp8", softmax_scale=cfg.softmax_scale)
+                            act=torch.bfloat16, fp8_keys=cfg.kidx == "fp8", softmax_scale=cfg.softmax_scale,
+                            mx_keys=cfg.kidx == "mxfp4")
         self.out = torch.empty(cfg.B, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
         self.lse = torch.empty(cfg.B, cfg.H, device=dev)
         self.idx = torch.empty(cfg.B, cfg.k, device=dev, dtype=torch.int32)
@@ -251,7 +257,7 @@ class Decode:
         from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
         work = decode_step_work(cfg, kv_entry_bytes=cfg.d - 64 + 128 if self.FP8KV else None)
         self.stage_label = "indexer stage: indexer_tc_kernel<%s> (query image built in each CTA)" % (
-            "e4m3" if cfg.kidx == "fp8" else "bf16")
+            {"fp8": "e4m3", "mxfp4": "mxfp4"}.get(cfg.kidx, "bf16"))
         self.stage_bound = "hbm"
         self.stage_amount = work["indexer_bytes"] + cfg.B * cfg.E * 4   # + the fp32 scores written
         self.step_bytes = work["bytes"]
@@ -292,9 +298,14 @@ class Decode:
             kscale = host.pop("kscale", None)
             kv_comp = host["kv_comp"][0].copy()
             t0 = time.perf_counter()
-            kdeq = (O.e4m3_decode(codes[0]) * kscale[0][:, None] if kscale is not None
-                    else codes[0].astype(np.float64))
-            O.decode_step_sequence(sub, host, 0, kv_comp, kdeq, fp8_keys=kscale is not None)
+            mx = cfg.kidx == "mxfp4"
+            if mx:
+                kdeq = O.mxfp4_key_decode(codes[0], O.mxfp4_key_unwords(kscale[0].astype(np.uint32)))
+            elif kscale is not None:
+                kdeq = O.e4m3_decode(codes[0]) * kscale[0][:, None]
+            else:
+                kdeq = codes[0].astype(np.float64)
+            O.decode_step_sequence(sub, host, 0, kv_comp, kdeq, fp8_keys=kscale is not None and not mx, mx_keys=mx)
             elapsed += time.perf_counter() - t0
         desc = (f"{n} sequence(s) of this workload, one decode token each (compress, {cfg.E:,}-key indexer, "
                 f"top-{cfg.k}, attention over {cfg.k}+{cfg.W} rows), float64 numpy, {elapsed:.1f} s")
@@ -806,7 +817,7 @@ class Fp8KvDecode(Decode):
     FP8KV = True
 
 
-WORKLOADS = {2: Decode, 4: Decode, 12: Fp8KvDecode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
+WORKLOADS = {2: Decode, 4: Decode, 12: Fp8KvDecode, 13: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
              11: Mxfp4KvAttn}
 
 
@@ -817,7 +828,7 @@ def config_of(wl):
                      "replayed as one CUDA graph (a step of each copy), the remaining steps one graph each"))
     c.update(wl.config_extra)
     return c
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400, 12: 12}
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400, 12: 12, 13: 12}
 
 
 def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):

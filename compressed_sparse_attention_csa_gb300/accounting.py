@@ -20,9 +20,12 @@ def _act_bytes(act: str) -> int:
 
 
 def indexer_key_bytes(cfg) -> int:
-    """Bytes of one stored indexer key (FP8 keys carry one fp32 scale)."""
+    """Bytes of one stored indexer key (FP8 keys carry one fp32 scale; MXFP4 keys are dI/2 payload
+    bytes and one UE8M0 byte per 32 channels: 64 + 4 for dI = 128)."""
     if cfg.kidx == "fp8":
         return cfg.dI + 4
+    if cfg.kidx == "mxfp4":
+        return cfg.dI // 2 + cfg.dI // 32
     return cfg.dI * _act_bytes(cfg.act)
 
 

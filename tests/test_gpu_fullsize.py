@@ -2,7 +2,7 @@
 
 The workloads are built by bench.py's workload classes and run as a CUDA-graph replay of
 their step, exactly as the benchmark times them, then checked against the oracle:
-  decode @64K (batch 16, bf16 keys) and @1M (batch 4, FP8 keys): every sequence;
+  decode @64K (batch 16, bf16 keys) and @1M (batch 4, FP8 keys; and MXFP4 keys): every sequence;
   prefill chunk (4,096 queries after 131,072 tokens): all 1,024 new entries of both caches,
   and indexer scores / top-k / attention on sampled query rows (first and last included);
   CSA2 decoder group at 262,144 tokens (batch 8): every sequence through all four layers;
@@ -46,7 +46,7 @@ def host(x):
     return np64(x) if x.is_floating_point() else x.cpu().numpy()
 
 
-@pytest.mark.parametrize("cid", [2, 4])
+@pytest.mark.parametrize("cid", [2, 4, 13])
 def test_decode_full_size(cid):
     cfg = gen.CONFIGS[cid]
     wl = Decode(cfg, csa, torch, DEV, 0)
