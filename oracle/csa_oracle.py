@@ -288,6 +288,18 @@ def topk(scores_f32: np.ndarray, nv: int, k: int) -> np.ndarray:
     return out
 
 
+def topk_bf16(scores_f32: np.ndarray, nv: int, k: int) -> np.ndarray:
+    """The selector on BF16 index scores ([V4] "FP4, down to the index scores": the scores are
+    quantised from FP32 to BF16 before the top-k): each binary32 score rounded to the nearest
+    BF16 value (ties to even), then the same (score desc, index asc) top-k.  Scores that BF16
+    makes equal are ties, won by the lowest index."""
+    s = np.asarray(scores_f32, np.float32).astype(np.float64)
+    fin = np.isfinite(s)
+    r = s.copy()
+    r[fin] = round_to_bf16(s[fin])
+    return topk(r, nv, k)
+
+
 # ----------------------------------------------------------------------------------
 # a3': CSA2 hierarchical candidate pool  [V41] section 3, [V41d] "Hierarchical indexing"
 # ----------------------------------------------------------------------------------

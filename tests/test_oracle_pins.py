@@ -294,6 +294,30 @@ def test_topk_adversarial_ties():
     assert list(O.topk(inc, 5, k)) == list(range(5)) + [-1] * (k - 5)
 
 
+def test_topk_bf16_ties_and_brute_force():
+    # 1 + 2^-10 is above 1 in binary32 but rounds to 1 in BF16: the two tie, the lower index wins
+    s = np.array([1.0, 1.0 + 2.0 ** -10, 0.5, -0.0], np.float32)
+    assert list(O.topk(s, 4, 1)) == [1]
+    assert list(O.topk_bf16(s, 4, 1)) == [0]
+    # 1 + 2^-8 + 2^-9 and 1 + 3 * 2^-9 both round to 1 + 2^-7; 1 + 2^-8 (half an ulp) ties to even, 1
+    t = np.array([1.0 + 2.0 ** -8 + 2.0 ** -9, 1.0 + 3 * 2.0 ** -9, 1.0 + 2.0 ** -8], np.float32)
+    assert list(O.topk_bf16(t, 3, 1)) == [0]          # both round to 1 + 2^-7: index 0 first
+    assert list(O.topk_bf16(np.array([0.0, -0.0, 0.0], np.float32), 3, 2)) == [0, 1]
+    inf = np.array([-np.inf, 1.0, -np.inf], np.float32)
+    assert list(O.topk_bf16(inf, 3, 3)) == [0, 1, 2]
+    # brute force: sort (bf16 value via torch, index) pairs
+    for trial in range(30):
+        n = int(rng.integers(1, 400))
+        k = int(rng.integers(1, 90))
+        nv = int(rng.integers(0, n + 1))
+        x = (rng.standard_normal(n) * 3).astype(np.float32)
+        b = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+        pairs = sorted(((-float(b[i]), i) for i in range(nv)))
+        expect = sorted(i for _, i in pairs[:min(k, nv)])
+        got = O.topk_bf16(x, nv, k)
+        assert list(got[:len(expect)]) == expect and np.all(got[len(expect):] == -1)
+
+
 # ------------------------------------------------------------------ hierarchical pool
 
 def test_hier_pool_superset_of_topk_and_size():
