@@ -13,7 +13,7 @@ c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
 
 CSA_F32, CSA_BF16, CSA_E4M3, CSA_MXFP4 = 0, 1, 2, 3
 (CSA_OP_COMPRESS, CSA_OP_INDEXER, CSA_OP_TOPK, CSA_OP_ATTN, CSA_OP_DECODE, CSA_OP_POOL, CSA_OP_INDEXER_TOPK,
- CSA_OP_DENSE_ATTN, CSA_OP_HCA_DECODE) = range(9)
+ CSA_OP_DENSE_ATTN, CSA_OP_HCA_DECODE, CSA_OP_TOPK_BF16, CSA_OP_INDEXER_TOPK_BF16) = range(11)
 STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_DTYPE", 4: "CSA_ERR_ALIGN",
           5: "CSA_ERR_WORKSPACE", 6: "CSA_ERR_CUDA", 7: "CSA_ERR_TIMEOUT", 8: "CSA_ERR_INDEX"}
 
@@ -29,7 +29,7 @@ class csa_decode_args(ctypes.Structure):
                 ("kv_comp", c_vp), ("kI", c_vp), ("kscale", c_vp), ("kv_tail", c_vp), ("z_tail", c_vp),
                 ("kvI_tail", c_vp), ("zI_tail", c_vp), ("bias", c_vp), ("biasI", c_vp), ("kv_local", c_vp),
                 ("L", c_i64), ("local_base", c_vp), ("out", c_vp), ("lse", c_vp), ("idx_out", c_vp),
-                ("scores_out", c_vp)]
+                ("scores_out", c_vp), ("bf16_scores", ctypes.c_int32)]
 
 
 class csa_hca_decode_args(ctypes.Structure):
@@ -57,10 +57,16 @@ SIGNATURES = {
                                               c_i64, c_i64, c_vp, c_i64, c_vp]),
     "csa_indexer_scores": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64,
                                           c_vp, c_i32, c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "csa_indexer_scores_bf16": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                               c_i64, c_vp, c_i32, c_vp, c_i64, c_vp, c_sz, c_vp]),
     "csa_indexer_topk": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64,
                                         c_vp, c_vp, c_sz, c_vp]),
+    "csa_indexer_topk_bf16": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                             c_i64, c_vp, c_vp, c_sz, c_vp]),
     "csa_topk": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp, c_vp,
                                 c_sz, c_vp]),
+    "csa_topk_bf16": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp,
+                                     c_vp, c_sz, c_vp]),
     "csa_topk_noalloc": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp,
                                         c_vp]),
     "csa_block_pool": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_i32,

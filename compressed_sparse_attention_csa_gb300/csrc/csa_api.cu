@@ -207,11 +207,11 @@ IndexerArgs indexer_shape(const csa_config* c, int T, int64_t E_cap, int sms) {
 }
 
 // csa_indexer_topk: [query images][scores rows*E_cap*4][visible counts][top-k workspace].
-size_t indexer_topk_ws(const csa_config* c, int T, int64_t E_cap, int sms) {
+size_t indexer_topk_ws(const csa_config* c, int T, int64_t E_cap, int sms, bool bf16 = false) {
   const int64_t rows = static_cast<int64_t>(c->B) * T;
   return align_up(indexer_workspace_bytes(indexer_shape(c, T, E_cap, sms)), 256) +
-         align_up(static_cast<size_t>(rows * E_cap) * 4, 256) + align_up(static_cast<size_t>(rows) * 4, 256) +
-         align_up(topk_workspace_bytes(rows, E_cap, c->k, sms), 256);
+         align_up(static_cast<size_t>(rows * E_cap) * (bf16 ? 2 : 4), 256) + align_up(static_cast<size_t>(rows) * 4, 256) +
+         align_up(topk_workspace_bytes(rows, E_cap, c->k, sms, bf16), 256);
 }
 
 size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
@@ -295,8 +295,9 @@ size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_
       return indexer_workspace_bytes(indexer_shape(cfg, static_cast<int>(n_cols), 1, sms));
     }
     case CSA_OP_TOPK:
+    case CSA_OP_TOPK_BF16:
       if (n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
-      return topk_workspace_bytes(rows, n_cols, cfg->k, sms);
+      return topk_workspace_bytes(rows, n_cols, cfg->k, sms, op == CSA_OP_TOPK_BF16);
     case CSA_OP_ATTN: {
       if (n_cols < 1 || rows % n_cols) return static_cast<size_t>(-1);
       return attn_workspace_bytes(static_cast<int>(rows / n_cols), static_cast<int>(n_cols), cfg->H, cfg->d,
@@ -308,8 +309,9 @@ size_t csa_workspace_size(csa_op op, const csa_config* cfg, int64_t rows, int64_
     case CSA_OP_POOL:
       return static_cast<size_t>(-1);
     case CSA_OP_INDEXER_TOPK:  // rows = B*T, n_cols = E_cap
+    case CSA_OP_INDEXER_TOPK_BF16:
       if (rows % cfg->B || n_cols < 1 || n_cols > (int64_t(1) << 24)) return static_cast<size_t>(-1);
-      return indexer_topk_ws(cfg, static_cast<int>(rows / cfg->B), n_cols, sms);
+      return indexer_topk_ws(cfg, static_cast<int>(rows / cfg->B), n_cols, sms, op == CSA_OP_INDEXER_TOPK_BF16);
     default:
       break;
   }
@@ -543,10 +545,10 @@ csa_status csa_inverse_rope_quant(const csa_config* cfg, const void* o, int64_t 
   return launch_status(launch_inv_rope_quant(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float* w, int32_t T,
-                              const int64_t* q_pos, const void* kI, const void* kscale, int64_t E_cap,
-                              const int32_t* cand, int32_t n_cand, float* scores, int64_t ld_scores, void* ws,
-                              size_t ws_bytes, csa_stream_t stream) {
+static csa_status indexer_scores_impl(const csa_config* cfg, const void* qI, const float* w, int32_t T, const int64_t* q_pos,
+                               const void* kI, const void* kscale, int64_t E_cap, const int32_t* cand, int32_t n_cand,
+                               void* scores, int64_t ld_scores, void* ws, size_t ws_bytes, csa_stream_t stream,
+                               bool bf16) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!qI || !w || !q_pos || !kI || !scores) return CSA_ERR_NULL;
@@ -567,7 +569,8 @@ csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float
   a.kscale = kscale;
   a.cand = cand;
   a.n_cand = n_cand;
-  a.scores = scores;
+  a.scores = static_cast<float*>(scores);
+  a.scores_bf16 = bf16;
   a.ld = ld_scores;
   a.B = cfg->B;
   a.T = T;
@@ -584,9 +587,25 @@ csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float
   return launch_status(launch_indexer(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* w, int32_t T, const int64_t* q_pos,
-                            const void* kI, const void* kscale, int64_t E_cap, int32_t* idx, void* ws,
-                            size_t ws_bytes, csa_stream_t stream) {
+csa_status csa_indexer_scores(const csa_config* cfg, const void* qI, const float* w, int32_t T,
+                              const int64_t* q_pos, const void* kI, const void* kscale, int64_t E_cap,
+                              const int32_t* cand, int32_t n_cand, float* scores, int64_t ld_scores, void* ws,
+                              size_t ws_bytes, csa_stream_t stream) {
+  return indexer_scores_impl(cfg, qI, w, T, q_pos, kI, kscale, E_cap, cand, n_cand, scores, ld_scores, ws, ws_bytes,
+                             stream, false);
+}
+
+csa_status csa_indexer_scores_bf16(const csa_config* cfg, const void* qI, const float* w, int32_t T,
+                                   const int64_t* q_pos, const void* kI, const void* kscale, int64_t E_cap,
+                                   const int32_t* cand, int32_t n_cand, void* scores, int64_t ld_scores, void* ws,
+                                   size_t ws_bytes, csa_stream_t stream) {
+  return indexer_scores_impl(cfg, qI, w, T, q_pos, kI, kscale, E_cap, cand, n_cand, scores, ld_scores, ws, ws_bytes,
+                             stream, true);
+}
+
+static csa_status indexer_topk_impl(const csa_config* cfg, const void* qI, const float* w, int32_t T, const int64_t* q_pos,
+                             const void* kI, const void* kscale, int64_t E_cap, int32_t* idx, void* ws,
+                             size_t ws_bytes, csa_stream_t stream, bool bf16) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!qI || !w || !q_pos || !kI || !idx) return CSA_ERR_NULL;
@@ -600,7 +619,7 @@ csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* 
   const int64_t rows = static_cast<int64_t>(cfg->B) * T;
   if (rows == 0) return CSA_OK;
   const int sms = device_sm_count();
-  const size_t need = indexer_topk_ws(cfg, T, E_cap, sms);
+  const size_t need = indexer_topk_ws(cfg, T, E_cap, sms, bf16);
   if (!ws || ws_bytes < need) return CSA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   IndexerArgs a = indexer_shape(cfg, T, E_cap, sms);
@@ -614,11 +633,12 @@ csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* 
   a.ws = p;
   p += align_up(indexer_workspace_bytes(a), 256);
   const size_t per_row = align_up(static_cast<size_t>(rows) * 4, 256);
-  float* scores = reinterpret_cast<float*>(p);
-  p += align_up(static_cast<size_t>(rows * E_cap) * 4, 256);
+  float* scores = reinterpret_cast<float*>(p);  // fp32, or BF16 (2 bytes a score)
+  p += align_up(static_cast<size_t>(rows * E_cap) * (bf16 ? 2 : 4), 256);
   int32_t* nv = reinterpret_cast<int32_t*>(p);
   p += per_row;
   a.scores = scores;
+  a.scores_bf16 = bf16;
   a.ld = E_cap;
   a.nv_out = nv;
   cudaError_t e = launch_indexer(a, s);
@@ -636,12 +656,25 @@ csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* 
   t.ws_bytes = ws_bytes - static_cast<size_t>(p - static_cast<uint8_t*>(ws));
   t.err = a.err;
   t.num_sms = sms;
+  t.bf16 = bf16;
   return launch_status(launch_topk(t, s));
 }
 
-csa_status csa_topk(const csa_config* cfg, const float* scores, int64_t ld, int64_t rows, int64_t n_cols,
-                    const int32_t* n_valid, const int32_t* cand, int32_t* idx, void* ws, size_t ws_bytes,
-                    csa_stream_t stream) {
+csa_status csa_indexer_topk(const csa_config* cfg, const void* qI, const float* w, int32_t T, const int64_t* q_pos,
+                            const void* kI, const void* kscale, int64_t E_cap, int32_t* idx, void* ws,
+                            size_t ws_bytes, csa_stream_t stream) {
+  return indexer_topk_impl(cfg, qI, w, T, q_pos, kI, kscale, E_cap, idx, ws, ws_bytes, stream, false);
+}
+
+csa_status csa_indexer_topk_bf16(const csa_config* cfg, const void* qI, const float* w, int32_t T,
+                                 const int64_t* q_pos, const void* kI, const void* kscale, int64_t E_cap, int32_t* idx,
+                                 void* ws, size_t ws_bytes, csa_stream_t stream) {
+  return indexer_topk_impl(cfg, qI, w, T, q_pos, kI, kscale, E_cap, idx, ws, ws_bytes, stream, true);
+}
+
+static csa_status topk_impl(const csa_config* cfg, const void* scores, int64_t ld, int64_t rows, int64_t n_cols,
+                     const int32_t* n_valid, const int32_t* cand, int32_t* idx, void* ws, size_t ws_bytes,
+                     csa_stream_t stream, bool bf16) {
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!scores || !idx) return CSA_ERR_NULL;
@@ -650,7 +683,7 @@ csa_status csa_topk(const csa_config* cfg, const float* scores, int64_t ld, int6
     return CSA_ERR_ALIGN;
   if (rows < 0 || n_cols < 0 || ld < n_cols || n_cols > (int64_t(1) << 24) || rows > 65535) return CSA_ERR_SHAPE;
   const int sms = device_sm_count();
-  const size_t need = topk_workspace_bytes(rows, n_cols, cfg->k, sms);
+  const size_t need = topk_workspace_bytes(rows, n_cols, cfg->k, sms, bf16);
   if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
   TopkArgs a{};
   a.scores = scores;
@@ -665,7 +698,20 @@ csa_status csa_topk(const csa_config* cfg, const float* scores, int64_t ld, int6
   a.ws_bytes = ws_bytes;
   a.err = err_word_ptr();
   a.num_sms = sms;
+  a.bf16 = bf16;
   return launch_status(launch_topk(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_topk(const csa_config* cfg, const float* scores, int64_t ld, int64_t rows, int64_t n_cols,
+                    const int32_t* n_valid, const int32_t* cand, int32_t* idx, void* ws, size_t ws_bytes,
+                    csa_stream_t stream) {
+  return topk_impl(cfg, scores, ld, rows, n_cols, n_valid, cand, idx, ws, ws_bytes, stream, false);
+}
+
+csa_status csa_topk_bf16(const csa_config* cfg, const void* scores, int64_t ld, int64_t rows, int64_t n_cols,
+                         const int32_t* n_valid, const int32_t* cand, int32_t* idx, void* ws, size_t ws_bytes,
+                         csa_stream_t stream) {
+  return topk_impl(cfg, scores, ld, rows, n_cols, n_valid, cand, idx, ws, ws_bytes, stream, true);
 }
 
 csa_status csa_block_pool(const csa_config* cfg, const float* scores, int64_t ld, int64_t rows, int64_t n_cols,
@@ -975,6 +1021,7 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   ia.kI = d->kI;
   ia.kscale = d->kscale;
   ia.scores = scores;
+  ia.scores_bf16 = d->bf16_scores != 0;
   ia.ld = d->E_cap;
   ia.B = cfg->B;
   ia.T = 1;
@@ -1010,7 +1057,8 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
     ia.images_ready = true;
     e = launch_indexer(ia, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
-    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s);
+    e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s, nullptr,
+                         ia.scores_bf16);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   } else {
     if (fp8kv) return CSA_ERR_SHAPE;  // FP8 entries: the fused path only
@@ -1042,6 +1090,7 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
     ta.ws_bytes = topk_ws;
     ta.err = err;
     ta.num_sms = sms;
+    ta.bf16 = ia.scores_bf16;
     e = launch_topk(ta, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   }

@@ -100,7 +100,7 @@ struct IndexerArgs {
   const void* kscale;    // [B, E_cap]: fp32 scales (e4m3) or UE8M0 scale words (MXFP4)
   const int32_t* cand;   // [B*T, n_cand] or null
   int n_cand;
-  float* scores;         // [B*T, ld]
+  float* scores;         // [B*T, ld] fp32, or BF16 when scores_bf16
   int64_t ld;
   int B, T, HI, dI, m;
   int64_t E_cap;
@@ -114,6 +114,7 @@ struct IndexerArgs {
   void* ws;              // tensor-core path: query images (indexer_workspace_bytes)
   bool images_ready;     // the query images in ws were already written (fused decode prep)
   DecodeFuse fuse;       // decode step only
+  bool scores_bf16 = false;           // write the scores rounded to BF16 (RNE), 2 bytes each
   uint64_t wait_ns = kDefaultWaitNs;  // budget of every bounded wait of the launch
   bool skip_key_loads = false;        // fault injection (tests): the producer issues no key load
 };
@@ -150,7 +151,7 @@ cudaError_t launch_compress_with_qprep(const CompressArgs& a, const QprepPart& q
 
 // ---- top-k ------------------------------------------------------------------------
 struct TopkArgs {
-  const float* scores;   // [rows, ld]
+  const void* scores;    // [rows, ld] fp32, or BF16 (bf16 = true)
   int64_t ld, rows, n_cols;
   const int32_t* n_valid;
   const int32_t* cand;   // [rows, n_cols] or null
@@ -160,8 +161,9 @@ struct TopkArgs {
   size_t ws_bytes;
   int* err;
   int num_sms;
+  bool bf16 = false;     // BF16 scores: the histogram and row paths only
 };
-size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms);
+size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms, bool bf16 = false);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 
 // Histogram-guided top-k for a few long rows.  hist_cnt holds, per row, 4096 fine digit
@@ -175,14 +177,14 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols);  // the candidat
 bool topk_uses_hist(int64_t rows, int64_t n_cols, bool has_cand);
 // Many long rows: one CTA per row with a shared-memory histogram (no workspace).
 bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k);
-cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             int k, int32_t* idx, cudaStream_t s, const int32_t* cmap = nullptr);
+cudaError_t launch_topk_rows(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+                             int k, int32_t* idx, cudaStream_t s, const int32_t* cmap = nullptr, bool bf16 = false);
 size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols);
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
 // hist_cnt: [rows][4160] then rows tickets; left zero for the next use.
-cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+cudaError_t launch_topk_hist(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s,
-                             const int32_t* cmap = nullptr);
+                             const int32_t* cmap = nullptr, bool bf16 = false);
 
 struct PoolArgs {
   const float* scores;

@@ -40,6 +40,18 @@
 namespace csa {
 namespace {
 
+// A score as the scores array holds it: fp32, or rounded to BF16 (nearest even) when the
+// caller asked for BF16 scores; the histogram digit is taken from the stored value.
+__device__ __forceinline__ float stored_score(const IndexerArgs& a, float v) {
+  return a.scores_bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+__device__ __forceinline__ void store_score(const IndexerArgs& a, int64_t i, float v) {
+  if (a.scores_bf16)
+    reinterpret_cast<__nv_bfloat16*>(a.scores)[i] = __float2bfloat16_rn(v);
+  else
+    a.scores[i] = v;
+}
+
 // ------------------------------------------------------------------ CUDA-core path
 struct MxKey {};  // key type tag: MXFP4 keys (DI/2 payload bytes and one scale word per key)
 
@@ -92,7 +104,7 @@ __global__ void __launch_bounds__(128) indexer_simt_kernel(IndexerArgs a, int64_
     if constexpr (std::is_same<TK, uint8_t>::value) acc *= static_cast<const float*>(a.kscale)[krow];
     score = acc;
   }
-  a.scores[row * a.ld + col] = score;
+  store_score(a, row * a.ld + col, score);
 }
 
 // ------------------------------------------------------------------ tensor-core path
@@ -367,8 +379,9 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
     if (split == L.n_splits - 1) {
       for (int g = 0; g < G; ++g) {
         if (g0 + g >= T) break;
-        float* dst = a.scores + (qrow0 + g) * a.ld;
-        for (int64_t c = static_cast<int64_t>(tiles_needed) * kTile + lane; c < n_cols; c += 32) dst[c] = -INFINITY;
+        const int64_t r0 = (qrow0 + g) * a.ld;
+        for (int64_t c = static_cast<int64_t>(tiles_needed) * kTile + lane; c < n_cols; c += 32)
+          store_score(a, r0 + c, -INFINITY);
       }
     }
   } else if (warp == 1) {
@@ -523,10 +536,10 @@ __global__ void __launch_bounds__(tc_threads(MINB), MINB) indexer_tc_kernel(cons
         for (int g = 0; g < kMaxG; ++g) {
           if (g < g_lo || g >= g_hi || g0 + g >= T) continue;
           const float sc = res[g] * ksc_use;
-          a.scores[(qrow0 + g) * a.ld + s] = (FUSE || ps >= 0) && ps < sNv[g] ? sc : -INFINITY;
+          store_score(a, (qrow0 + g) * a.ld + s, (FUSE || ps >= 0) && ps < sNv[g] ? sc : -INFINITY);
         }
       }
-      if (hist && s < n_cols && s < sNv[0]) atomicAdd(&sHist[f2key(res[0] * ksc_use) >> 20], 1u);
+      if (hist && s < n_cols && s < sNv[0]) atomicAdd(&sHist[f2key(stored_score(a, res[0] * ksc_use)) >> 20], 1u);
     }
     if (hist) {
       named_sync(6, 32 * EPI);

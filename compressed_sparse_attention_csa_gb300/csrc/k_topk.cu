@@ -430,21 +430,23 @@ size_t levels_ws(const Plan& pl, int64_t rows, int k) {
 
 }  // namespace
 
-size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms) {
+size_t topk_workspace_bytes(int64_t rows, int64_t n_cols, int k, int num_sms, bool bf16) {
   // the scratch of the path launch_topk takes: the histogram path's counts and slots, none for
-  // the row kernel (shared memory only), else the level path's ping-pong candidate buffers
+  // the row kernel (shared memory only; BF16 rows of any length), else the level path's
+  // ping-pong candidate buffers
   if (topk_uses_hist(rows, n_cols, false)) return topk_hist_standalone_bytes(rows, n_cols);
-  if (topk_uses_rows(rows, n_cols, false, k)) return 0;
+  if (bf16 || topk_uses_rows(rows, n_cols, false, k)) return 0;
   return levels_ws(make_plan(rows, n_cols, k, num_sms), rows, k);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
   if (topk_uses_hist(a.rows, a.n_cols, a.cand != nullptr)) return launch_topk_hist_standalone(a, s);
-  if (topk_uses_rows(a.rows, a.n_cols, a.cand != nullptr, a.k))
-    return launch_topk_rows(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, a.k, a.idx, s, a.cand);
+  if (a.bf16 || topk_uses_rows(a.rows, a.n_cols, a.cand != nullptr, a.k))
+    return launch_topk_rows(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, a.k, a.idx, s, a.cand, a.bf16);
   const Plan pl = make_plan(a.rows, std::max<int64_t>(a.n_cols, 1), a.k, a.num_sms);
-  return run_levels(pl, a.scores, a.ld, a.rows, a.n_valid, a.cand, a.k, a.idx, static_cast<uint8_t*>(a.ws), s);
+  return run_levels(pl, static_cast<const float*>(a.scores), a.ld, a.rows, a.n_valid, a.cand, a.k, a.idx,
+                    static_cast<uint8_t*>(a.ws), s);
 }
 
 size_t pool_workspace_bytes(int64_t rows, int64_t n_cols, int block, int n_blocks, int num_sms) {

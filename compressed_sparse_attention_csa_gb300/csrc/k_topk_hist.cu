@@ -18,7 +18,14 @@
 //  * Many long rows (the prefill chunk, the block pool): topk_row_kernel, one CTA per row with
 //    the histogram in shared memory and the same exact selection.
 // The decode step runs topk_select_kernel on the histogram its indexer launch fills.
+//
+// BF16 scores ("FP4, down to the index scores": the index scores rounded to BF16 before the
+// selector) run the same kernels (B16 = true) on the 16-bit order-preserving key, widened to
+// 32 bits by 16 zero bits: the fine digit is the same 12 bits (sign, exponent, 3 mantissa
+// bits), and the exact refinement inside the threshold bin has 4 bits left instead of 20, one
+// radix pass instead of two.
 #include <algorithm>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -42,6 +49,69 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
+}
+
+// Scores of a row as order-preserving 32-bit keys (0 is reserved for "not a candidate": the
+// smallest key maps to 1).  fp32: f2key.  BF16: the 16-bit key (-0 as +0) in the upper half.
+template <bool B16>
+struct ScoreKey {
+  using T = typename std::conditional<B16, uint16_t, float>::type;
+  static constexpr int kLowBits = B16 ? 4 : 20;  // refinement bits below the 12-bit digit
+  __device__ static __forceinline__ uint32_t of(T x) {
+    uint32_t y;
+    if constexpr (B16) {
+      uint32_t u = x;
+      if (u == 0x8000u) u = 0u;
+      y = ((u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u)) << 16;
+    } else {
+      y = f2key(x);
+    }
+    return y == 0u ? 1u : y;
+  }
+  __device__ static __forceinline__ T load(const T* p) { return __ldcg(p); }
+};
+
+// Eight consecutive keys of a row starting at t0 (< n checked per element; 16-byte vector
+// loads when aligned).
+template <bool B16>
+__device__ __forceinline__ void load_keys8(const typename ScoreKey<B16>::T* srow, int64_t t0, int64_t n,
+                                           uint32_t (&key)[8]) {
+  using K = ScoreKey<B16>;
+  if constexpr (B16) {
+    if (t0 + 8 <= n && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+      const uint4 x = __ldcg(reinterpret_cast<const uint4*>(srow + t0));
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int u = 0; u < 8; ++u) key[u] = K::of(static_cast<uint16_t>(w[u >> 1] >> (16 * (u & 1))));
+      return;
+    }
+  } else {
+    if (t0 + 8 <= n && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + t0));
+      const float4 y = __ldcg(reinterpret_cast<const float4*>(srow + t0 + 4));
+      const float v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int u = 0; u < 8; ++u) key[u] = K::of(v[u]);
+      return;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) key[u] = t0 + u < n ? K::of(K::load(srow + t0 + u)) : 1u;
+}
+
+// The exact threshold inside digit b1: the `want` largest keys with that digit are every key
+// above *T plus *quota keys equal to *T (radix passes on the refinement bits).
+template <bool B16, int NTT, typename F>
+__device__ __forceinline__ void select_in_bin(F key_at, int n, int want, uint32_t b1, uint32_t* hist, uint32_t* tmp,
+                                              uint32_t* res, uint32_t* T, int* quota, int t) {
+  if constexpr (B16) {
+    uint32_t t16 = 0;
+    team_select_largest<NTT>([key_at](int x) { return key_at(x) >> 16; }, n, want, 4, b1 << 4, 0xFFF0u, hist, tmp,
+                             res, &t16, quota, t, 0);
+    *T = t16 << 16;
+  } else {
+    team_select_largest<NTT>(key_at, n, want, 20, b1 << 20, 0xFFF00000u, hist, tmp, res, T, quota, t, 0);
+  }
 }
 
 __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int64_t row, int64_t n_cols) {
@@ -76,9 +146,12 @@ __device__ int64_t warp_cand_prefix(const int32_t* cm, int64_t nv) {
   return lo;
 }
 
-__global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
+template <bool B16>
+__global__ void __launch_bounds__(NT) topk_hist_build_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
                                                              int64_t n_cols, uint32_t* hist, int chunk,
                                                              const int32_t* cmap) {
+  using K = ScoreKey<B16>;
+  const typename K::T* scores = static_cast<const typename K::T*>(scores_v);
   __shared__ uint32_t h[kFine];
   pdl_wait();
   pdl_trigger();
@@ -89,7 +162,7 @@ __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const float* scores
   if (cmap) nv = warp_cand_prefix(cmap + row * n_cols, nv);
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * chunk;
   const int64_t c1 = c0 + chunk < nv ? c0 + chunk : nv;
-  for (int64_t s = c0 + threadIdx.x; s < c1; s += NT) atomicAdd(&h[f2key(scores[row * ld + s]) >> 20], 1u);
+  for (int64_t s = c0 + threadIdx.x; s < c1; s += NT) atomicAdd(&h[K::of(scores[row * ld + s]) >> 20], 1u);
   __syncthreads();
   uint32_t* rh = hist + row * kRowWords;
   for (int i = threadIdx.x; i < kFine; i += NT)
@@ -132,9 +205,12 @@ struct SelSmem {
 
 size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
 
-__global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
+template <bool B16>
+__global__ void __launch_bounds__(NT) topk_select_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
                                                          int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
                                                          uint32_t* cand, int n_chunks, const int32_t* cmap) {
+  using K = ScoreKey<B16>;
+  const typename K::T* scores = static_cast<const typename K::T*>(scores_v);
   extern __shared__ __align__(16) uint8_t sel_raw[];
   SelSmem& S = *reinterpret_cast<SelSmem*>(sel_raw);
   int32_t* sel = reinterpret_cast<int32_t*>(sel_raw + sizeof(SelSmem));  // [k] (whole-row path)
@@ -144,26 +220,15 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   const int chunk_id = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  const float* srow = scores + row * ld;
+  const typename K::T* srow = scores + row * ld;
   // this CTA's positions: thread t holds c0 + t*kSelPer .. +kSelPer-1 (contiguous, so the
   // compaction below keeps position order); the loads (bounded by the row length, the
   // visible count is applied after) are in flight with those of n_valid and the histogram
+  static_assert(kSelPer == 8, "eight keys a thread");
   const int64_t c0 = static_cast<int64_t>(chunk_id) * kSelChunk;
-  float v[kSelPer];
+  uint32_t v[kSelPer];
   const int64_t t0 = c0 + tid * kSelPer;
-  if (t0 + kSelPer <= n_cols && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
-#pragma unroll
-    for (int u = 0; u < kSelPer; u += 4) {
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + t0 + u));
-      v[u] = x.x;
-      v[u + 1] = x.y;
-      v[u + 2] = x.z;
-      v[u + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int u = 0; u < kSelPer; ++u) v[u] = t0 + u < n_cols ? __ldcg(srow + t0 + u) : 0.f;
-  }
+  load_keys8<B16>(srow, t0, n_cols, v);
   int64_t nvr = row_valid(n_valid, row, n_cols);
   if (cmap) nvr = warp_cand_prefix(cmap + row * n_cols, nvr);
   // histogram rows, then the tickets
@@ -176,8 +241,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
 #pragma unroll
   for (int u = 0; u < kSelPer; ++u) {
     const int64_t s = c0 + tid * kSelPer + u;
-    uint32_t x = f2key(v[u]);
-    if (x == 0u) x = 1u;
+    const uint32_t x = v[u];
     key[u] = (s < nvr && (x >> 20) >= b1) ? x : 0u;
     cnt += key[u] != 0u;
   }
@@ -261,8 +325,7 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
     int quota = 0x7fffffff;
     if (n_all - static_cast<int>(n_gt) > need) {
       const uint32_t* ak = S.ak;
-      team_select_largest<NT>([ak](int x) { return ak[x]; }, n_all, need, 20, b1 << 20, 0xFFF00000u, S.hist, S.tmp,
-                           S.res, &T, &quota, tid, 0);
+      select_in_bin<B16, NT>([ak](int x) { return ak[x]; }, n_all, need, b1, S.hist, S.tmp, S.res, &T, &quota, tid);
     }
     // stable compaction over contiguous segments: keys above T, then the first quota keys
     // equal to T in position order
@@ -299,11 +362,8 @@ __global__ void __launch_bounds__(NT) topk_select_kernel(const float* scores, in
   } else {
     // too many candidates (a bin full of ties, or crowded into one chunk): select over the whole
     // row in position order
-    const float* rowp = srow;
-    auto key_at = [rowp](int x) {
-      const uint32_t y = f2key(__ldcg(rowp + x));
-      return y == 0u ? 1u : y;
-    };
+    const typename K::T* rowp = srow;
+    auto key_at = [rowp](int x) { return K::of(K::load(rowp + x)); };
     const int n = static_cast<int>(nvr);
     uint32_t T = 1u;
     int quota = 0x7fffffff;
@@ -357,21 +417,13 @@ struct RowSmem {
 template <int CAP>
 size_t row_smem_bytes(int k) { return sizeof(RowSmem<CAP>) + 2 * static_cast<size_t>(k) * 4 + 16; }
 
-__device__ __forceinline__ void load_row8(const float* srow, int64_t t0, int64_t n, float (&v)[kRowPer]) {
-  if (t0 + kRowPer <= n && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + t0));
-    const float4 y = __ldcg(reinterpret_cast<const float4*>(srow + t0 + 4));
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-  } else {
-#pragma unroll
-    for (int u = 0; u < kRowPer; ++u) v[u] = t0 + u < n ? __ldcg(srow + t0 + u) : 0.f;
-  }
-}
+static_assert(kRowPer == 8, "eight keys a thread");
 
-template <int CAP>
-__global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64_t ld, const int32_t* n_valid,
+template <int CAP, bool B16>
+__global__ void __launch_bounds__(NT) topk_row_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
                                                       int64_t n_cols, int k, int32_t* idx, const int32_t* cmap) {
+  using K = ScoreKey<B16>;
+  const typename K::T* scores = static_cast<const typename K::T*>(scores_v);
   extern __shared__ __align__(16) uint8_t row_raw[];
   RowSmem<CAP>& S = *reinterpret_cast<RowSmem<CAP>*>(row_raw);
   int32_t* sel = reinterpret_cast<int32_t*>(row_raw + sizeof(RowSmem<CAP>));  // [k] (whole-row path)
@@ -383,22 +435,18 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
   pdl_trigger();
   int64_t nvr = row_valid(n_valid, row, n_cols);
   if (cmap) nvr = warp_cand_prefix(cmap + row * n_cols, nvr);
-  const float* srow = scores + row * ld;
-  auto key_of = [](float x) {
-    const uint32_t y = f2key(x);
-    return y == 0u ? 1u : y;
-  };
+  const typename K::T* srow = scores + row * ld;
   __syncthreads();
   // pass 1: the histogram of the visible scores (two batches of loads in flight)
   for (int64_t base = 0; base < nvr; base += 2 * kRowBatch) {
-    float v[kRowPer], w[kRowPer];
+    uint32_t v[kRowPer], w[kRowPer];
     const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer, t1 = t0 + kRowBatch;
-    load_row8(srow, t0, nvr, v);
-    load_row8(srow, t1, nvr, w);
+    load_keys8<B16>(srow, t0, nvr, v);
+    load_keys8<B16>(srow, t1, nvr, w);
 #pragma unroll
     for (int u = 0; u < kRowPer; ++u) {
-      if (t0 + u < nvr) atomicAdd(&S.hist[key_of(v[u]) >> 20], 1u);
-      if (t1 + u < nvr) atomicAdd(&S.hist[key_of(w[u]) >> 20], 1u);
+      if (t0 + u < nvr) atomicAdd(&S.hist[v[u] >> 20], 1u);
+      if (t1 + u < nvr) atomicAdd(&S.hist[w[u] >> 20], 1u);
     }
   }
   __syncthreads();
@@ -406,14 +454,14 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
   // pass 2: the candidates (digit >= b1) in position order
   uint32_t n_all = 0, n_gt = 0;
   for (int64_t base = 0; base < nvr; base += kRowBatch) {
-    float v[kRowPer];
+    uint32_t v[kRowPer];
     const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
-    load_row8(srow, t0, nvr, v);
+    load_keys8<B16>(srow, t0, nvr, v);
     uint32_t key[kRowPer];
     uint32_t c = 0, g = 0;
 #pragma unroll
     for (int u = 0; u < kRowPer; ++u) {
-      const uint32_t x = key_of(v[u]);
+      const uint32_t x = v[u];
       key[u] = (t0 + u < nvr && (x >> 20) >= b1) ? x : 0u;
       c += key[u] != 0u;
       g += key[u] != 0u && (x >> 20) > b1;
@@ -445,8 +493,7 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
     int quota = 0x7fffffff;
     if (na - static_cast<int>(n_gt) > need) {
       const uint32_t* ak = S.ak;
-      team_select_largest<NT>([ak](int x) { return ak[x]; }, na, need, 20, b1 << 20, 0xFFF00000u, S.sort, S.tmp,
-                              S.res, &T, &quota, tid, 0);
+      select_in_bin<B16, NT>([ak](int x) { return ak[x]; }, na, need, b1, S.sort, S.tmp, S.res, &T, &quota, tid);
     }
     // stable compaction over contiguous segments: keys above T, then the first quota keys
     // equal to T in position order
@@ -482,8 +529,8 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const float* scores, int64
     for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
   } else {
     // too many candidates (a bin full of ties): select over the whole row in position order
-    const float* rowp = srow;
-    auto key_at = [rowp, key_of](int x) { return key_of(__ldcg(rowp + x)); };
+    const typename K::T* rowp = srow;
+    auto key_at = [rowp](int x) { return K::of(K::load(rowp + x)); };
     const int n = static_cast<int>(nvr);
     uint32_t T = 1u;
     int quota = 0x7fffffff;
@@ -525,19 +572,23 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
   return align_up(static_cast<size_t>(rows) * sel_chunks(n_cols) * kSlotWords * 4, 256);
 }
 
-cudaError_t launch_topk_hist(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+cudaError_t launch_topk_hist(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s,
-                             const int32_t* cmap) {
+                             const int32_t* cmap, bool bf16) {
   static std::atomic<unsigned long long> attr{0};
   if (first_use_in_context(attr)) {
-    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(topk_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(sel_smem_bytes(4096)));
+    cudaFuncSetAttribute(topk_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(sel_smem_bytes(4096)));
   }
   const int n_chunks = std::max(1, sel_chunks(n_cols));
+  const dim3 grid(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows));
   const cudaError_t e =
-      launch_pdl(topk_select_kernel, dim3(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows)), dim3(NT),
-                 sel_smem_bytes(k), s, scores, ld, n_valid, n_cols, hist_cnt, k, idx,
-                 static_cast<uint32_t*>(ws_cand), n_chunks, cmap);
+      bf16 ? launch_pdl(topk_select_kernel<true>, grid, dim3(NT), sel_smem_bytes(k), s, scores, ld, n_valid, n_cols,
+                        hist_cnt, k, idx, static_cast<uint32_t*>(ws_cand), n_chunks, cmap)
+           : launch_pdl(topk_select_kernel<false>, grid, dim3(NT), sel_smem_bytes(k), s, scores, ld, n_valid, n_cols,
+                        hist_cnt, k, idx, static_cast<uint32_t*>(ws_cand), n_chunks, cmap);
   count_launches(1);
   return e;
 }
@@ -549,21 +600,31 @@ bool topk_uses_rows(int64_t rows, int64_t n_cols, bool has_cand, int k) {
   return n_cols >= 2048 && k <= 4096 && !topk_uses_hist(rows, n_cols, has_cand);
 }
 
-cudaError_t launch_topk_rows(const float* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
-                             int k, int32_t* idx, cudaStream_t s, const int32_t* cmap) {
+cudaError_t launch_topk_rows(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
+                             int k, int32_t* idx, cudaStream_t s, const int32_t* cmap, bool bf16) {
   static std::atomic<unsigned long long> attr{0};
   if (first_use_in_context(attr)) {
-    cudaFuncSetAttribute(topk_row_kernel<2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(topk_row_kernel<2048, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(row_smem_bytes<2048>(512)));
-    cudaFuncSetAttribute(topk_row_kernel<8192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(topk_row_kernel<8192, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(row_smem_bytes<8192>(4096)));
+    cudaFuncSetAttribute(topk_row_kernel<2048, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(row_smem_bytes<2048>(512)));
+    cudaFuncSetAttribute(topk_row_kernel<8192, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(row_smem_bytes<8192>(4096)));
   }
   const dim3 grid(static_cast<unsigned>(rows));
-  const cudaError_t e =
-      k <= 512 ? launch_pdl(topk_row_kernel<2048>, grid, dim3(NT), row_smem_bytes<2048>(k), s, scores, ld, n_valid,
-                            n_cols, k, idx, cmap)
-               : launch_pdl(topk_row_kernel<8192>, grid, dim3(NT), row_smem_bytes<8192>(k), s, scores, ld, n_valid,
-                            n_cols, k, idx, cmap);
+  cudaError_t e;
+  if (k <= 512)
+    e = bf16 ? launch_pdl(topk_row_kernel<2048, true>, grid, dim3(NT), row_smem_bytes<2048>(k), s, scores, ld, n_valid,
+                          n_cols, k, idx, cmap)
+             : launch_pdl(topk_row_kernel<2048, false>, grid, dim3(NT), row_smem_bytes<2048>(k), s, scores, ld,
+                          n_valid, n_cols, k, idx, cmap);
+  else
+    e = bf16 ? launch_pdl(topk_row_kernel<8192, true>, grid, dim3(NT), row_smem_bytes<8192>(k), s, scores, ld, n_valid,
+                          n_cols, k, idx, cmap)
+             : launch_pdl(topk_row_kernel<8192, false>, grid, dim3(NT), row_smem_bytes<8192>(k), s, scores, ld,
+                          n_valid, n_cols, k, idx, cmap);
   count_launches(1);
   return e;
 }
@@ -580,12 +641,14 @@ cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int chunk = 8192;
   dim3 g(static_cast<unsigned>((a.n_cols + chunk - 1) / chunk), static_cast<unsigned>(a.rows));
-  e = launch_pdl(topk_hist_build_kernel, g, dim3(NT), 0, s, a.scores, a.ld, a.n_valid, a.n_cols, hist_cnt, chunk,
-                 a.cand);
+  e = a.bf16 ? launch_pdl(topk_hist_build_kernel<true>, g, dim3(NT), 0, s, a.scores, a.ld, a.n_valid, a.n_cols,
+                          hist_cnt, chunk, a.cand)
+             : launch_pdl(topk_hist_build_kernel<false>, g, dim3(NT), 0, s, a.scores, a.ld, a.n_valid, a.n_cols,
+                          hist_cnt, chunk, a.cand);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return launch_topk_hist(a.scores, a.ld, a.rows, a.n_cols, a.n_valid, hist_cnt, a.k, a.idx,
-                          w + align_up(hbytes, 256), a.num_sms, s, a.cand);
+                          w + align_up(hbytes, 256), a.num_sms, s, a.cand, a.bf16);
 }
 
 }  // namespace csa

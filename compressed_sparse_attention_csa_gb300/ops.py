@@ -152,44 +152,53 @@ def compress_kv_single(cfg: Config, kv: torch.Tensor, z: torch.Tensor, bias: Opt
 def indexer_scores(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.Tensor, kI: torch.Tensor,
                    scores: torch.Tensor, kscale: Optional[torch.Tensor] = None,
                    cand: Optional[torch.Tensor] = None) -> None:
-    """csa_indexer_scores: qI [B, T, HI, dI], w [B, T, HI], kI [B, E_cap, dI] (+ kscale)."""
+    """csa_indexer_scores: qI [B, T, HI, dI], w [B, T, HI], kI [B, E_cap, dI] (+ kscale); scores
+    fp32, or bfloat16 (csa_indexer_scores_bf16: each score rounded to BF16)."""
     lib = L.load()
     c = cfg.c()
     T = qI.shape[1]
     n_cand = cand.shape[-1] if cand is not None else 0
     ws = _workspace(lib.csa_workspace_size(L.CSA_OP_INDEXER, ctypes.byref(c), cfg.B * T, T), qI.device)
     wp, wb = _ws_args(ws)
-    _check("csa_indexer_scores",
-           lib.csa_indexer_scores(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), kI.shape[1],
-                                  _p(cand), n_cand, _p(scores), scores.shape[-1], wp, wb, _stream()))
+    bf16 = scores.dtype == torch.bfloat16
+    fn = lib.csa_indexer_scores_bf16 if bf16 else lib.csa_indexer_scores
+    _check("csa_indexer_scores_bf16" if bf16 else "csa_indexer_scores",
+           fn(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), kI.shape[1],
+              _p(cand), n_cand, _p(scores), scores.shape[-1], wp, wb, _stream()))
 
 
 def indexer_topk(cfg: Config, qI: torch.Tensor, w: torch.Tensor, q_pos: torch.Tensor, kI: torch.Tensor,
-                 idx: torch.Tensor, kscale: Optional[torch.Tensor] = None) -> None:
-    """csa_indexer_topk: the k best visible entries of every query row (ascending, -1 padded),
-    the scores kept in the call's workspace.  qI [B, T, HI, dI], w [B, T, HI], kI [B, E_cap, dI]."""
+                 idx: torch.Tensor, kscale: Optional[torch.Tensor] = None, bf16_scores: bool = False) -> None:
+    """csa_indexer_topk (csa_indexer_topk_bf16 with bf16_scores): the k best visible entries of
+    every query row (ascending, -1 padded), the scores kept in the call's workspace.
+    qI [B, T, HI, dI], w [B, T, HI], kI [B, E_cap, dI]."""
     lib = L.load()
     c = cfg.c()
     T = qI.shape[1]
     E_cap = kI.shape[1]
-    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_INDEXER_TOPK, ctypes.byref(c), cfg.B * T, E_cap), qI.device)
+    op = L.CSA_OP_INDEXER_TOPK_BF16 if bf16_scores else L.CSA_OP_INDEXER_TOPK
+    ws = _workspace(lib.csa_workspace_size(op, ctypes.byref(c), cfg.B * T, E_cap), qI.device)
     wp, wb = _ws_args(ws)
-    _check("csa_indexer_topk",
-           lib.csa_indexer_topk(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), E_cap, _p(idx),
-                                wp, wb, _stream()))
+    fn = lib.csa_indexer_topk_bf16 if bf16_scores else lib.csa_indexer_topk
+    _check("csa_indexer_topk_bf16" if bf16_scores else "csa_indexer_topk",
+           fn(ctypes.byref(c), _p(qI), _p(w), T, _p(q_pos), _p(kI), _p(kscale), E_cap, _p(idx), wp, wb, _stream()))
 
 
 def topk(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional[torch.Tensor] = None,
          cand: Optional[torch.Tensor] = None, n_cols: Optional[int] = None) -> None:
-    """csa_topk: scores [rows, ld] fp32 -> idx [rows, k] int32 (ascending, -1 padded)."""
+    """csa_topk: scores [rows, ld] fp32 (csa_topk_bf16: bfloat16) -> idx [rows, k] int32
+    (ascending, -1 padded)."""
     lib = L.load()
     c = cfg.c()
     rows, ld = scores.shape
     n_cols = ld if n_cols is None else n_cols
-    ws = _workspace(lib.csa_workspace_size(L.CSA_OP_TOPK, ctypes.byref(c), rows, n_cols), scores.device)
+    bf16 = scores.dtype == torch.bfloat16
+    op = L.CSA_OP_TOPK_BF16 if bf16 else L.CSA_OP_TOPK
+    ws = _workspace(lib.csa_workspace_size(op, ctypes.byref(c), rows, n_cols), scores.device)
     wp, wb = _ws_args(ws)
-    _check("csa_topk", lib.csa_topk(ctypes.byref(c), _p(scores), ld, rows, n_cols, _p(n_valid), _p(cand), _p(idx),
-                                    wp, wb, _stream()))
+    fn = lib.csa_topk_bf16 if bf16 else lib.csa_topk
+    _check("csa_topk_bf16" if bf16 else "csa_topk",
+           fn(ctypes.byref(c), _p(scores), ld, rows, n_cols, _p(n_valid), _p(cand), _p(idx), wp, wb, _stream()))
 
 
 def topk_noalloc(cfg: Config, scores: torch.Tensor, idx: torch.Tensor, n_valid: Optional[torch.Tensor] = None,
@@ -234,16 +243,17 @@ def sparse_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, idx: torch.
 
 def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, scores_out=None,
-                fp8kv: bool = False) -> None:
+                fp8kv: bool = False, bf16_scores: bool = False) -> None:
     """csa_decode_step (csa_decode_step_fp8kv with fp8kv: kv_comp [B, E_cap, 576] uint8 FP8
     entries): one token per sequence (T = 1); caches are updated in place.  scores_out
-    [B, E_cap] fp32 (optional) receives the indexer scores the step selected from."""
+    [B, E_cap] fp32 (optional; bfloat16 with bf16_scores) receives the indexer scores the step
+    selected from.  bf16_scores: the scores are rounded to BF16 before the selection."""
     lib = L.load()
     c = cfg.c()
     a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                           _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias), _p(biasI),
                           _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse), _p(idx_out),
-                          _p(scores_out))
+                          _p(scores_out), int(bf16_scores))
     nbytes = lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(c), cfg.B, kv_comp.shape[1])
     if nbytes == ctypes.c_size_t(-1).value:
         raise CsaError("csa_workspace_size", 2)
@@ -412,14 +422,14 @@ class DecodeStepCall:
 
     def __init__(self, cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
                  biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, scores_out=None,
-                 fp8kv: bool = False):
+                 fp8kv: bool = False, bf16_scores: bool = False):
         self._lib = L.load()
         self._fn = self._lib.csa_decode_step_fp8kv if fp8kv else self._lib.csa_decode_step
         self._c = cfg.c()
         self._a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                                     _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias),
                                     _p(biasI), _p(kv_local), kv_local.shape[1], _p(local_base), _p(out), _p(lse),
-                                    _p(idx_out), _p(scores_out))
+                                    _p(idx_out), _p(scores_out), int(bf16_scores))
         nbytes = self._lib.csa_workspace_size(L.CSA_OP_DECODE, ctypes.byref(self._c), cfg.B, kv_comp.shape[1])
         if nbytes == ctypes.c_size_t(-1).value:
             raise CsaError("csa_workspace_size", 2)

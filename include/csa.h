@@ -71,7 +71,7 @@ typedef struct {
 typedef enum {
   CSA_OP_COMPRESS = 0, CSA_OP_INDEXER = 1, CSA_OP_TOPK = 2, CSA_OP_ATTN = 3,
   CSA_OP_DECODE = 4, CSA_OP_POOL = 5, CSA_OP_INDEXER_TOPK = 6, CSA_OP_DENSE_ATTN = 7,
-  CSA_OP_HCA_DECODE = 8
+  CSA_OP_HCA_DECODE = 8, CSA_OP_TOPK_BF16 = 9, CSA_OP_INDEXER_TOPK_BF16 = 10
 } csa_op;
 
 /*
@@ -157,6 +157,17 @@ csa_status csa_indexer_scores(const csa_config *cfg, const void *qI, const float
                               int64_t ld_scores, void *ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
+ * csa_indexer_scores_bf16 — csa_indexer_scores writing each score rounded to BF16 (round to
+ * nearest even of the fp32 score csa_indexer_scores writes; -inf as BF16 -inf): scores is
+ * [B*T, ld_scores] 16-bit ("FP4, down to the index scores": the index scores in BF16 before
+ * the top-k selector).  Same arguments, workspace and errors.
+ */
+csa_status csa_indexer_scores_bf16(const csa_config *cfg, const void *qI, const float *w, int32_t T,
+                                   const int64_t *q_pos, const void *kI, const void *kscale,
+                                   int64_t E_cap, const int32_t *cand, int32_t n_cand, void *scores,
+                                   int64_t ld_scores, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
  * csa_indexer_topk — csa_indexer_scores followed by csa_topk over each row's visible entries
  * ("The Lightning Indexer": keep the k best; ties to the lowest position) in one call:
  * idx[r, 0:k] holds the k best visible positions of query row r in ascending order, -1
@@ -173,6 +184,15 @@ csa_status csa_indexer_topk(const csa_config *cfg, const void *qI, const float *
                             int32_t *idx, void *ws, size_t ws_bytes, csa_stream_t stream);
 
 /*
+ * csa_indexer_topk_bf16 — csa_indexer_topk over BF16 scores: idx is exactly what
+ * csa_topk_bf16 returns on the scores csa_indexer_scores_bf16 writes (the scores, 2 bytes
+ * each, live in ws).  ws : csa_workspace_size(CSA_OP_INDEXER_TOPK_BF16, cfg, B*T, E_cap).
+ */
+csa_status csa_indexer_topk_bf16(const csa_config *cfg, const void *qI, const float *w, int32_t T,
+                                 const int64_t *q_pos, const void *kI, const void *kscale, int64_t E_cap,
+                                 int32_t *idx, void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
  * csa_topk — per row, the cfg->k best of scores[r, 0:n_valid[r]] under the total order
  * (score descending, position ascending; -0 == +0), written to idx[r, 0:k] in ascending
  * position order, padded with -1 when fewer than k are valid.  Deterministic.
@@ -186,6 +206,18 @@ csa_status csa_indexer_topk(const csa_config *cfg, const void *qI, const float *
 csa_status csa_topk(const csa_config *cfg, const float *scores, int64_t ld, int64_t rows,
                     int64_t n_cols, const int32_t *n_valid, const int32_t *cand, int32_t *idx,
                     void *ws, size_t ws_bytes, csa_stream_t stream);
+
+/*
+ * csa_topk_bf16 — csa_topk over BF16 scores ([rows, ld] 16-bit): the same total order on the
+ * BF16 values (score descending, position ascending; -0 == +0), output ascending, -1 padded.
+ * BF16 rounding makes many scores equal; ties go to the lowest position.  Rows of any length
+ * run the one-CTA-per-row or the histogram path (a 12-bit digit of the 16-bit key, then one
+ * 4-bit radix pass inside the threshold bin).  ws : csa_workspace_size(CSA_OP_TOPK_BF16, cfg,
+ * rows, n_cols) bytes (0 except for few long rows).
+ */
+csa_status csa_topk_bf16(const csa_config *cfg, const void *scores, int64_t ld, int64_t rows, int64_t n_cols,
+                         const int32_t *n_valid, const int32_t *cand, int32_t *idx, void *ws, size_t ws_bytes,
+                         csa_stream_t stream);
 
 /*
  * csa_topk_noalloc — csa_topk for callers that cannot allocate device memory.  There is no
@@ -421,8 +453,12 @@ typedef struct {
   void *out;                 /* [B, H, d]                                                     */
   float *lse;                /* [B, H] or NULL                                                */
   int32_t *idx_out;          /* [B, k] or NULL: the entries the step selected                 */
-  float *scores_out;         /* [B, E_cap] fp32 or NULL: the indexer scores the step selected
-                                from (-inf past the visible entries); NULL keeps them in ws    */
+  float *scores_out;         /* [B, E_cap] fp32 (BF16 with bf16_scores) or NULL: the indexer
+                                scores the step selected from (-inf past the visible entries);
+                                NULL keeps them in ws                                          */
+  int32_t bf16_scores;       /* non-zero: the scores are rounded to BF16 (nearest even) before
+                                the selection, which then runs on them ("FP4, down to the index
+                                scores": BF16 index scores for the selector)                   */
 } csa_decode_args;
 
 /*

@@ -127,7 +127,7 @@ def oracle_decode(cfg, inp):
     return res
 
 
-def run_gpu_decode(cfg, inp, scores_out=None):
+def run_gpu_decode(cfg, inp, scores_out=None, bf16_scores=False):
     c = lib_config(cfg)
     out = torch.empty(cfg.B, cfg.H, cfg.d, device=inp["q"].device, dtype=cfg.torch_act)
     lse = torch.empty(cfg.B, cfg.H, device=inp["q"].device)
@@ -136,7 +136,7 @@ def run_gpu_decode(cfg, inp, scores_out=None):
                     kv_comp=inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"],
                     z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
                     biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse,
-                    idx_out=idx, scores_out=scores_out)
+                    idx_out=idx, scores_out=scores_out, bf16_scores=bf16_scores)
     assert csa.get_last_error() == 0
     return out, lse, idx
 
@@ -148,7 +148,7 @@ def assert_step_selection_exact(cfg, ref, idx, scores_out):
     rtol_s = 5e-2 if cfg.kidx in ("fp8", "mxfp4") else 1e-2
     for b in range(cfg.B):
         nv = ref[b]["nv"]
-        s32 = scores_out[b].cpu().numpy()
+        s32 = scores_out[b].float().cpu().numpy()
         assert np.all(np.isneginf(s32[nv:])), f"b={b}: invisible entries must be -inf"
         assert_scores_close(s32[:nv], ref[b]["scores"][:nv], rtol_s, what=f"step scores b={b}")
         gi = idx[b].cpu().numpy().astype(np.int64)
