@@ -58,7 +58,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13, 14])
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="oracle sample size (sequences for decode / CSA2, query rows for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -89,6 +89,7 @@ _DENSE_STAGE = (("attn_hca_dec_kernel", "attn_merge_wide_kernel"), ("k_attn.cu",
 STAGE_PROFILES = {4: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE_1Q,
                   12: ("indexer_tc_e4m3_1M_decode.md",) + _INDEXER_STAGE_1Q,
                   13: ("indexer_tc_mxfp4_1M_decode.md",) + _INDEXER_STAGE_1Q,
+                  14: ("indexer_tc_mxfp4_1M_decode.md",) + _INDEXER_STAGE_1Q,
                   2: ("indexer_tc_bf16_64K_decode.md",) + _INDEXER_STAGE_1Q,
                   3: ("indexer_tc_bf16_prefill_4K.md",) + _INDEXER_STAGE,
                   5: ("indexer_tc_bf16_csa2_scan_256K.md",) + _INDEXER_STAGE_1Q,
@@ -210,6 +211,7 @@ def _host64(x):
 
 class Decode:
     FP8KV = False   # main-KV entries stored as FP8 entries (576 B)
+    MXKV = False    # main-KV entries stored as MXFP4 entries (288 B)
 
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
@@ -218,6 +220,8 @@ class Decode:
         self.metric = "CSA decode tok/s @1M ctx" if cfg.N == 1 << 20 else "CSA decode tok/s @64K ctx"
         if self.FP8KV:
             self.metric += ", FP8 main-KV entries"
+        if self.MXKV:
+            self.metric += ", MXFP4 main-KV entries"
         if cfg.kidx == "mxfp4":
             self.metric += ", MXFP4 indexer keys"
         keys = {"fp8": "FP8 e4m3 indexer keys + fp32 scale",
@@ -225,13 +229,14 @@ class Decode:
         self.workload = (f"V4-Flash CSA decode step, batch {cfg.B} @ {cfg.N:,}-token context "
                          f"({cfg.E:,} entries/seq), " +
                          keys +
-                         (", FP8 main-KV entries (448 e4m3 + 64 bf16 dims, 576 B)" if self.FP8KV else ", bf16 KV") +
+                         (", FP8 main-KV entries (448 e4m3 + 64 bf16 dims, 576 B)" if self.FP8KV else
+                          ", MXFP4 main-KV entries (E2M1 + e4m3 scale per 16 dims, 288 B)" if self.MXKV else ", bf16 KV") +
                          f", {cfg.H}x{cfg.d} heads, indexer {cfg.HI}x{cfg.dI}, k {cfg.k}, W {cfg.W}")
         self.config_extra = {"batch": cfg.B, "context": cfg.N, "m": cfg.m, "entries_per_seq": cfg.E,
                              "heads": cfg.H, "head_dim": cfg.d, "indexer": f"{cfg.HI}x{cfg.dI}", "top_k": cfg.k,
                              "window": cfg.W,
                              "indexer_keys": {"fp8": "e4m3+fp32 scale", "mxfp4": "MXFP4 E2M1+UE8M0/32"}.get(cfg.kidx, "bf16"),
-                             "kv_entries": "FP8 (576 B)" if self.FP8KV else "bf16 (1 KiB)"}
+                             "kv_entries": "FP8 (576 B)" if self.FP8KV else "MXFP4 (288 B)" if self.MXKV else "bf16 (1 KiB)"}
         if host_only:
             return
         self.csa = csa
@@ -247,15 +252,20 @@ class Decode:
         if self.FP8KV:
             self.kv8 = torch.empty(cfg.B, cfg.E, cfg.d + 64, dtype=torch.uint8, device=dev)
             csa.kv_pack_fp8(self.c, inp["kv_comp"], self.kv8)
+        if self.MXKV:
+            self.kv8 = torch.empty(cfg.B, cfg.E, cfg.d // 2 + cfg.d // 16, dtype=torch.uint8, device=dev)
+            csa.kv_pack_mxfp4(self.c, inp["kv_comp"], self.kv8)
         self.args = dict(q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"],
-                         kv_comp=self.kv8 if self.FP8KV else inp["kv_comp"], kI=inp["kI"], kscale=inp.get("kscale"),
+                         kv_comp=self.kv8 if (self.FP8KV or self.MXKV) else inp["kv_comp"], kI=inp["kI"],
+                         kscale=inp.get("kscale"),
                          kv_tail=inp["kv_str"],
                          z_tail=inp["z_str"], kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"],
                          biasI=inp["biasI"], kv_local=inp["kv_local"], local_base=inp["local_base"],
                          out=self.out, lse=self.lse, idx_out=self.idx)
         self.call = None   # the step's arguments, marshalled at the first call
         from compressed_sparse_attention_csa_gb300.accounting import decode_step_work
-        work = decode_step_work(cfg, kv_entry_bytes=cfg.d - 64 + 128 if self.FP8KV else None)
+        work = decode_step_work(cfg, kv_entry_bytes=cfg.d - 64 + 128 if self.FP8KV else
+                                cfg.d // 2 + cfg.d // 16 if self.MXKV else None)
         self.stage_label = "indexer stage: indexer_tc_kernel<%s> (query image built in each CTA)" % (
             {"fp8": "e4m3", "mxfp4": "mxfp4"}.get(cfg.kidx, "bf16"))
         self.stage_bound = "hbm"
@@ -268,8 +278,15 @@ class Decode:
 
     def step(self):
         if self.call is None:
-            self.call = self.csa.DecodeStepCall(self.c, fp8kv=self.FP8KV, **self.args)
+            self.call = self.csa.DecodeStepCall(self.c, fp8kv=self.FP8KV, mxfp4kv=self.MXKV, **self.args)
         self.call()
+
+    def step_bf16(self):
+        """The same step with the index scores rounded to BF16 before the selection."""
+        if getattr(self, "call16", None) is None:
+            self.call16 = self.csa.DecodeStepCall(self.c, fp8kv=self.FP8KV, mxfp4kv=self.MXKV, bf16_scores=True,
+                                                  **self.args)
+        self.call16()
 
     def stage_fn(self):
         inp = self.inp
@@ -305,7 +322,8 @@ class Decode:
                 kdeq = O.e4m3_decode(codes[0]) * kscale[0][:, None]
             else:
                 kdeq = codes[0].astype(np.float64)
-            O.decode_step_sequence(sub, host, 0, kv_comp, kdeq, fp8_keys=kscale is not None and not mx, mx_keys=mx)
+            O.decode_step_sequence(sub, host, 0, kv_comp, kdeq, fp8_keys=kscale is not None and not mx, mx_keys=mx,
+                                   fp8_kv=self.FP8KV, mxfp4_kv=self.MXKV)
             elapsed += time.perf_counter() - t0
         desc = (f"{n} sequence(s) of this workload, one decode token each (compress, {cfg.E:,}-key indexer, "
                 f"top-{cfg.k}, attention over {cfg.k}+{cfg.W} rows), float64 numpy, {elapsed:.1f} s")
@@ -358,6 +376,32 @@ class Prefill:
         csa.topk(c, self.scores, self.idx)
         csa.sparse_attn(c, inp["q"], inp["kv_comp"], self.idx, inp["kv_local"], inp["local_base"], inp["q_pos"],
                         inp["sink"], self.out, self.lse)
+
+    def _bf16_buffers(self):
+        if getattr(self, "scores16", None) is None:
+            import torch
+            cfg = self.cfg
+            self.scores16 = torch.empty(cfg.B * cfg.T, cfg.E, device=self.scores.device, dtype=torch.bfloat16)
+            self.idx16 = torch.empty_like(self.idx)
+
+    def step_bf16(self):
+        """The step with the index scores written in BF16 and the selector run on them."""
+        csa, c, inp = self.csa, self.c, self.inp
+        self._bf16_buffers()
+        csa.compress_kv(c, inp["kv_str"], inp["z_str"], inp["bias"], self.tok0, self.e0, self.e1, inp["kv_comp"])
+        csa.compress_kv(c, inp["kvI_str"], inp["zI_str"], inp["biasI"], self.tok0, self.e0, self.e1, inp["kI"])
+        csa.indexer_scores(c, inp["qI"], inp["w"], inp["q_pos"], inp["kI"],
+                           self.scores16.view(self.cfg.B, self.cfg.T, self.cfg.E))
+        csa.topk(c, self.scores16, self.idx16)
+        csa.sparse_attn(c, inp["q"], inp["kv_comp"], self.idx16, inp["kv_local"], inp["local_base"], inp["q_pos"],
+                        inp["sink"], self.out, self.lse)
+
+    def topk_fp32(self):
+        self.csa.topk(self.c, self.scores, self.idx)
+
+    def topk_bf16(self):
+        self._bf16_buffers()
+        self.csa.topk(self.c, self.scores16, self.idx16)
 
     def stage_fn(self):
         inp = self.inp
@@ -817,7 +861,12 @@ class Fp8KvDecode(Decode):
     FP8KV = True
 
 
-WORKLOADS = {2: Decode, 4: Decode, 12: Fp8KvDecode, 13: Decode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
+class Mxfp4KvDecode(Decode):
+    """The decode step over MXFP4 main-KV entries with MXFP4 indexer keys (V4.1's storage)."""
+    MXKV = True
+
+
+WORKLOADS = {2: Decode, 4: Decode, 12: Fp8KvDecode, 13: Decode, 14: Mxfp4KvDecode, 3: Prefill, 5: Csa2Group, 6: HcaDecode, 7: HcaPrefill, 9: Epilogue, 10: Fp8KvAttn,
              11: Mxfp4KvAttn}
 
 
@@ -828,7 +877,7 @@ def config_of(wl):
                      "replayed as one CUDA graph (a step of each copy), the remaining steps one graph each"))
     c.update(wl.config_extra)
     return c
-DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400, 12: 12, 13: 12}
+DEFAULT_SAMPLE = {2: 12, 4: 12, 3: 16, 5: 6, 6: 64, 7: 2048, 9: 4096, 10: 400, 11: 400, 12: 12, 13: 12, 14: 12}
 
 
 def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):
@@ -882,6 +931,29 @@ def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):
     timed(gs_s, g_all_s, 3 * R)
     stage_ms = max_over_ranks(timed(gs_s, g_all_s, Kp) / Kp)
     assert csa.get_last_error() == 0
+    # BF16 index scores ("FP4, down to the index scores"): the whole step with the indexer writing
+    # BF16 and the selector run on them, the selector alone on fp32 vs BF16 scores of the same
+    # rows, and the recall of the BF16 selection against the fp32 one
+    for w in wls:
+        w.step_bf16()
+    gs16, g_all16 = graphs("step_bf16")
+    timed(gs16, g_all16, 3 * R)
+    step16_ms = max_over_ranks(timed(gs16, g_all16, Kp) / Kp)
+    sel = {}
+    for name in ("topk_fp32", "topk_bf16"):
+        gx, gx_all = graphs(name)
+        timed(gx, gx_all, 3 * R)
+        sel[name] = max_over_ranks(timed(gx, gx_all, Kp) / Kp)
+        del gx, gx_all
+    w0.step()
+    w0.step_bf16()
+    torch.cuda.synchronize(dev)
+    a32, a16 = w0.idx, w0.idx16
+    m32 = torch.zeros(a32.shape[0], cfg.E, dtype=torch.bool, device=dev)
+    m32.scatter_(1, a32.clamp(min=0).long(), a32 >= 0)
+    hits = int(torch.gather(m32, 1, a16.clamp(min=0).long()).logical_and(a16 >= 0).sum())
+    recall = hits / max(int((a32 >= 0).sum()), 1)
+    assert csa.get_last_error() == 0
     hbm, bf16, bf16_sus, peak_kind = peaks()
     tflops = w0.stage_amount / (stage_ms / 1e3) / 1e12
     out = {"metric": w0.metric, "value": round(w0.units * world / (step_ms / 1e3), 1), "unit": "tok/s",
@@ -892,8 +964,13 @@ def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):
                         "frac_of_sustained": round(tflops / bf16_sus, 4),
                         "peak_kind": f"{peak_kind} dense bf16 GEMM throughput (burst; sustained beside it)",
                         "amount_per_launch": w0.stage_amount, "launch_us": round(stage_ms * 1e3, 2),
-                        "traffic": stage_traffic(3)}}
-    del gs, g_all, gs_s, g_all_s, wls, w0
+                        "traffic": stage_traffic(3)},
+           "bf16_scores": {"value": round(w0.units * world / (step16_ms / 1e3), 1), "ms_per_step": round(step16_ms, 5),
+                           "selector_us_fp32": round(sel["topk_fp32"] * 1e3, 2),
+                           "selector_us_bf16": round(sel["topk_bf16"] * 1e3, 2),
+                           "selector_speedup": round(sel["topk_fp32"] / sel["topk_bf16"], 3),
+                           "recall_vs_fp32": round(recall, 5)}}
+    del gs, g_all, gs_s, g_all_s, gs16, g_all16, wls, w0
     torch.cuda.empty_cache()
     return out
 
@@ -1091,6 +1168,16 @@ def main():
         time_rotation(g_b, 3 * R, g_b_all)
         b_ms = max_over_ranks(time_rotation(g_b, K, g_b_all) / K)
         extra["bf16_entries"] = {"value": round(wl.units * world / (b_ms / 1e3), 1), "ms_per_step": round(b_ms, 5)}
+    if isinstance(wl, Decode):
+        # the same step with the index scores rounded to BF16 before the selection
+        for w in wls:
+            w.step_bf16()
+        g_16 = [capture(w.step_bf16) for w in wls]
+        g_16_all = capture_all([w.step_bf16 for w in wls])
+        time_rotation(g_16, 3 * R, g_16_all)
+        s16_ms = max_over_ranks(time_rotation(g_16, K, g_16_all) / K)
+        extra["bf16_scores"] = {"value": round(wl.units * world / (s16_ms / 1e3), 1), "ms_per_step": round(s16_ms, 5)}
+        assert csa.get_last_error() == 0
     if isinstance(wl, Csa2Group):
         g_ns = [capture(w.step_without_scan) for w in wls]
         g_ns_all = capture_all([w.step_without_scan for w in wls])

@@ -96,6 +96,8 @@ SIGNATURES = {
                                        c_vp]),
     "csa_decode_step_fp8kv": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
                                              c_vp]),
+    "csa_decode_step_mxfp4kv": (ctypes.c_int, [ctypes.POINTER(csa_config), ctypes.POINTER(csa_decode_args), c_vp, c_sz,
+                                             c_vp]),
     "csa_decode_step_reset": (ctypes.c_int, [ctypes.POINTER(csa_config), c_vp, c_sz, c_vp]),
 }
 

@@ -966,7 +966,8 @@ csa_status csa_hca_decode_step(const csa_config* cfg, const csa_hca_decode_args*
 
 namespace {
 csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
-                            csa_stream_t stream, bool fp8kv) {
+                            csa_stream_t stream, int kv_fmt) {
+  const bool qkv = kv_fmt != 0;  // quantised main-KV entries (FP8 or MXFP4): the fused path only
   csa_status st = check_cfg(cfg);
   if (st != CSA_OK) return st;
   if (!d) return CSA_ERR_NULL;
@@ -986,8 +987,8 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
       cfg->HI > 128 || d->E_cap * cfg->B >= (int64_t(1) << 31))
     return CSA_ERR_SHAPE;
   const int sms = device_sm_count();
-  if (fp8kv && !(cfg->act == CSA_BF16 && cfg->d == 512 && cfg->m <= 8 &&
-                 attn_fp8kv_supported(cfg->B, 1, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms)))
+  if (qkv && !(cfg->act == CSA_BF16 && cfg->d == 512 && cfg->m <= 8 &&
+                attn_fp8kv_supported(cfg->B, 1, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms)))
     return CSA_ERR_SHAPE;
   if (!ws || ws_bytes < decode_ws(cfg, d->E_cap, sms)) return CSA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1052,7 +1053,7 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
     f.zI_tail = d->zI_tail;
     f.biasI = d->biasI;
     f.act_bf16 = cfg->act == CSA_BF16;
-    f.kv_fp8 = fp8kv;
+    f.kv_fmt = kv_fmt;
     f.hist = hist_cnt;
     ia.images_ready = true;
     e = launch_indexer(ia, s);
@@ -1061,7 +1062,7 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
                          ia.scores_bf16);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   } else {
-    if (fp8kv) return CSA_ERR_SHAPE;  // FP8 entries: the fused path only
+    if (qkv) return CSA_ERR_SHAPE;  // quantised entries: the fused path only
     // 1. compress the block the new token completes (main KV, then indexer keys)
     CompressArgs c{};
     c.B = cfg->B;
@@ -1119,7 +1120,7 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   aa.ws = ws_attn;
   aa.err = err;
   aa.num_sms = sms;
-  return launch_status(fp8kv ? launch_attn_fp8kv(aa, s) : launch_attn(aa, s));
+  return launch_status(kv_fmt == 2 ? launch_attn_mxfp4kv(aa, s) : kv_fmt == 1 ? launch_attn_fp8kv(aa, s) : launch_attn(aa, s));
 }
 }  // namespace
 
@@ -1134,12 +1135,17 @@ csa_status csa_decode_step_reset(const csa_config* cfg, void* ws, size_t ws_byte
 
 csa_status csa_decode_step(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
                            csa_stream_t stream) {
-  return decode_step_impl(cfg, d, ws, ws_bytes, stream, false);
+  return decode_step_impl(cfg, d, ws, ws_bytes, stream, 0);
 }
 
 csa_status csa_decode_step_fp8kv(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
                                  csa_stream_t stream) {
-  return decode_step_impl(cfg, d, ws, ws_bytes, stream, true);
+  return decode_step_impl(cfg, d, ws, ws_bytes, stream, 1);
+}
+
+csa_status csa_decode_step_mxfp4kv(const csa_config* cfg, const csa_decode_args* d, void* ws, size_t ws_bytes,
+                                   csa_stream_t stream) {
+  return decode_step_impl(cfg, d, ws, ws_bytes, stream, 2);
 }
 
 }  // extern "C"

@@ -86,7 +86,8 @@ struct DecodeFuse {
   const void* zI_tail;
   const float* biasI;    // [2, m, dI]
   bool act_bf16;         // stream and kv_comp dtype
-  bool kv_fp8;           // kv_comp holds FP8 main-KV entries: d - 64 e4m3 codes, then 64 bf16 dims
+  int kv_fmt;            // kv_comp rows: 0 the activation dtype; 1 FP8 main-KV entries (d - 64 e4m3
+                         // codes, then 64 bf16 dims); 2 MXFP4 entries (d/2 E2M1 bytes, d/16 e4m3 scales)
   uint32_t* hist;        // histograms
 };
 // decode-step state kept across steps: the histograms [B][4160] and the top-k tickets [B]; zero

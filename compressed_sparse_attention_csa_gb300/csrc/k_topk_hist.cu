@@ -60,9 +60,9 @@ struct ScoreKey {
   __device__ static __forceinline__ uint32_t of(T x) {
     uint32_t y;
     if constexpr (B16) {
-      uint32_t u = x;
-      if (u == 0x8000u) u = 0u;
-      y = ((u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u)) << 16;
+      // negative: all 16 bits flipped; positive (and -0, made +0): the sign bit set
+      const uint32_t u = x == 0x8000u ? 0u : static_cast<uint32_t>(x);
+      y = (u ^ (((u >> 15) * 0x7FFFu) | 0x8000u)) << 16;
     } else {
       y = f2key(x);
     }
@@ -206,7 +206,7 @@ struct SelSmem {
 size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
 
 template <bool B16>
-__global__ void __launch_bounds__(NT) topk_select_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
+__global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
                                                          int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
                                                          uint32_t* cand, int n_chunks, const int32_t* cmap) {
   using K = ScoreKey<B16>;

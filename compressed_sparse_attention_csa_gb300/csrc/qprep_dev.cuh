@@ -177,49 +177,59 @@ __device__ __forceinline__ float decode_new_key(const IndexerArgs& a, int b, int
   return scale;
 }
 
-// The new main-KV entry e of sequence b (d <= 512), its channels spread over the n_parts
-// CTAs that score the sequence's keys: part p takes channels p + n_parts * i, i = t256 and
-// t256 + 256 (t256 = 0..255), so no CTA holds its key stream back for the whole entry.
+// The new main-KV entry e of sequence b (d <= 512, d % 16 == 0), its channels split over the
+// n_parts CTAs that score the sequence's keys in contiguous ranges of `chunk` channels (a
+// multiple of 16: whole sectors of the tails, and an MXFP4 block of 16 channels stays inside
+// one CTA and one half-warp), one channel a thread (t256 = 0..255), so no CTA holds its key
+// stream back for the whole entry.  Stored in the cache's format: the activation dtype; FP8
+// entries (e4m3 codes of dims < d - 64, then the last 64 in bf16); or MXFP4 entries (per 16
+// channels scale = e4m3(amax / 6), codes = nearest E2M1 of x / scale, two to a byte; the d/2
+// payload bytes, then the d/16 scale bytes).
 __device__ __forceinline__ void decode_new_kv(const IndexerArgs& a, int b, int64_t e, int t256, int part,
                                               int n_parts) {
   const DecodeFuse& f = a.fuse;
   const int d = f.d, m = a.m;
+  const int chunk = ((d + n_parts - 1) / n_parts + 15) & ~15;
+  const int c_lo = part * chunk, c_hi = min(d, c_lo + chunk);
+  if (c_lo >= d) return;  // uniform across the CTA
   const size_t elem = f.act_bf16 ? 2 : 4;
   const size_t tail = static_cast<size_t>(b) * 2 * m * 2 * d * elem;
-  int chs[2];
-  float v[2];
-#pragma unroll
-  for (int n = 0; n < 2; ++n) {
-    chs[n] = part + n_parts * (t256 + 256 * n);
-    if (chs[n] >= d) continue;
-    const int c[1] = {chs[n]};
-    float o[1];
-    compress_tail_any<1>(static_cast<const uint8_t*>(f.kv_tail) + tail, static_cast<const uint8_t*>(f.z_tail) + tail,
-                         f.bias, f.act_bf16, m, d, c, e > 0, o);
-    v[n] = o[0];
-  }
-  if (f.kv_fp8) {  // FP8 main-KV entry: e4m3 codes of dims < d - 64, then the last 64 in bf16
-    uint8_t* row8 = static_cast<uint8_t*>(f.kv_comp) + (static_cast<int64_t>(b) * a.E_cap + e) * (d + 64);
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-      const int ch = chs[n];
-      if (ch >= d) continue;
-      if (ch < d - 64)
-        row8[ch] = f_to_e4m3(v[n]);
-      else
-        reinterpret_cast<__nv_bfloat16*>(row8 + d - 64)[ch - (d - 64)] = __float2bfloat16_rn(v[n]);
+  const int64_t row = static_cast<int64_t>(b) * a.E_cap + e;
+  for (int c0 = c_lo; c0 < c_hi; c0 += 256) {  // uniform loop: every lane reaches the shuffles
+    const int ch = c0 + t256;
+    const bool live = ch < c_hi;
+    float v = 0.f;
+    if (live) {
+      const int c[1] = {ch};
+      float o[1];
+      compress_tail_any<1>(static_cast<const uint8_t*>(f.kv_tail) + tail,
+                           static_cast<const uint8_t*>(f.z_tail) + tail, f.bias, f.act_bf16, m, d, c, e > 0, o);
+      v = o[0];
     }
-    return;
-  }
-  const int64_t row = (static_cast<int64_t>(b) * a.E_cap + e) * d;
+    if (f.kv_fmt == 2) {
+      // one MXFP4 block = 16 consecutive channels = the 16 lanes of a half-warp
+      float am = fabsf(v);
 #pragma unroll
-  for (int n = 0; n < 2; ++n) {
-    const int ch = chs[n];
-    if (ch >= d) continue;
-    if (f.act_bf16)
-      static_cast<__nv_bfloat16*>(f.kv_comp)[row + ch] = __float2bfloat16_rn(v[n]);
-    else
-      static_cast<float*>(f.kv_comp)[row + ch] = v[n];
+      for (int off = 8; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+      const uint8_t sc_code = f_to_e4m3(__fdiv_rn(am, 6.f));
+      const float sc = e4m3_to_f(sc_code);
+      const uint32_t code = sc > 0.f ? e2m1_code(__fdiv_rn(v, sc)) : 0u;
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+      uint8_t* row4 = static_cast<uint8_t*>(f.kv_comp) + row * (d / 2 + d / 16);
+      if (live && (ch & 1) == 0) row4[ch / 2] = static_cast<uint8_t>(code | (hi << 4));
+      if (live && (ch & 15) == 0) row4[d / 2 + ch / 16] = sc_code;
+    } else if (live && f.kv_fmt == 1) {
+      uint8_t* row8 = static_cast<uint8_t*>(f.kv_comp) + row * (d + 64);
+      if (ch < d - 64)
+        row8[ch] = f_to_e4m3(v);
+      else
+        reinterpret_cast<__nv_bfloat16*>(row8 + d - 64)[ch - (d - 64)] = __float2bfloat16_rn(v);
+    } else if (live) {
+      if (f.act_bf16)
+        static_cast<__nv_bfloat16*>(f.kv_comp)[row * d + ch] = __float2bfloat16_rn(v);
+      else
+        static_cast<float*>(f.kv_comp)[row * d + ch] = v;
+    }
   }
 }
 

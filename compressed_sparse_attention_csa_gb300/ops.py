@@ -243,9 +243,10 @@ def sparse_attn(cfg: Config, q: torch.Tensor, kv_comp: torch.Tensor, idx: torch.
 
 def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
                 biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, scores_out=None,
-                fp8kv: bool = False, bf16_scores: bool = False) -> None:
+                fp8kv: bool = False, bf16_scores: bool = False, mxfp4kv: bool = False) -> None:
     """csa_decode_step (csa_decode_step_fp8kv with fp8kv: kv_comp [B, E_cap, 576] uint8 FP8
-    entries): one token per sequence (T = 1); caches are updated in place.  scores_out
+    entries; csa_decode_step_mxfp4kv with mxfp4kv: [B, E_cap, 288] uint8 MXFP4 entries): one
+    token per sequence (T = 1); caches are updated in place.  scores_out
     [B, E_cap] fp32 (optional; bfloat16 with bf16_scores) receives the indexer scores the step
     selected from.  bf16_scores: the scores are rounded to BF16 before the selection."""
     lib = L.load()
@@ -258,7 +259,7 @@ def decode_step(cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_t
     if nbytes == ctypes.c_size_t(-1).value:
         raise CsaError("csa_workspace_size", 2)
     wp, wb = _ws_args(_decode_workspace(nbytes, q.device, cfg.B))
-    fn = lib.csa_decode_step_fp8kv if fp8kv else lib.csa_decode_step
+    fn = lib.csa_decode_step_mxfp4kv if mxfp4kv else lib.csa_decode_step_fp8kv if fp8kv else lib.csa_decode_step
     _check("csa_decode_step", fn(ctypes.byref(c), ctypes.byref(a), wp, wb, _stream()))
 
 
@@ -422,9 +423,10 @@ class DecodeStepCall:
 
     def __init__(self, cfg: Config, *, q_pos, q, qI, w, sink, kv_comp, kI, kv_tail, z_tail, kvI_tail, zI_tail, bias,
                  biasI, kv_local, local_base, out, kscale=None, lse=None, idx_out=None, scores_out=None,
-                 fp8kv: bool = False, bf16_scores: bool = False):
+                 fp8kv: bool = False, bf16_scores: bool = False, mxfp4kv: bool = False):
         self._lib = L.load()
-        self._fn = self._lib.csa_decode_step_fp8kv if fp8kv else self._lib.csa_decode_step
+        self._fn = (self._lib.csa_decode_step_mxfp4kv if mxfp4kv else
+                    self._lib.csa_decode_step_fp8kv if fp8kv else self._lib.csa_decode_step)
         self._c = cfg.c()
         self._a = L.csa_decode_args(kv_comp.shape[1], _p(q_pos), _p(q), _p(qI), _p(w), _p(sink), _p(kv_comp), _p(kI),
                                     _p(kscale), _p(kv_tail), _p(z_tail), _p(kvI_tail), _p(zI_tail), _p(bias),

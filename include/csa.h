@@ -500,6 +500,16 @@ csa_status csa_decode_step_reset(const csa_config *cfg, void *ws, size_t ws_byte
 csa_status csa_decode_step_fp8kv(const csa_config *cfg, const csa_decode_args *args, void *ws,
                                  size_t ws_bytes, csa_stream_t stream);
 
+/*
+ * csa_decode_step_mxfp4kv — csa_decode_step over a main-KV cache of MXFP4 entries (kv_comp
+ * [B, E_cap, 288] bytes, the format of csa_kv_pack_mxfp4: V4.1 section 4 "FP4: the norm
+ * argument…"): the entry the token completes is written as an MXFP4 entry (per 16 channels
+ * scale = e4m3(amax / 6), codes = nearest E2M1 value of x / scale) and the attention reads
+ * MXFP4 entries.  Same shapes, limits and workspace as csa_decode_step_fp8kv.
+ */
+csa_status csa_decode_step_mxfp4kv(const csa_config *cfg, const csa_decode_args *args, void *ws,
+                                   size_t ws_bytes, csa_stream_t stream);
+
 /* Synchronise `stream`, then return and clear the first device-side error recorded since the
  * last call (CSA_OK if none; CSA_ERR_CUDA if the stream itself reports an error). */
 csa_status csa_get_last_error(csa_stream_t stream);

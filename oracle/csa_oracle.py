@@ -400,7 +400,7 @@ def decode_token(cfg, inp: Dict[str, np.ndarray], b: int, tq: int,
 
 def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.ndarray,
                          kI_deq: np.ndarray, fp8_keys: bool = False, fp8_kv: bool = False,
-                         mx_keys: bool = False) -> Dict[str, np.ndarray]:
+                         mx_keys: bool = False, mxfp4_kv: bool = False) -> Dict[str, np.ndarray]:
     """One decode token of sequence b (T = 1).
 
     When the token at t completes a block ((t + 1) % m == 0), entry e = (t + 1)/m - 1 is
@@ -410,7 +410,8 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
     computed in float64 and stored in the cache's dtype (cfg.act: "bf16" or "f32"; FP8 keys as
     e4m3 codes with one binary32 scale amax/448, read back dequantised; MXFP4 keys (mx_keys) as
     E2M1 codes with a UE8M0 scale per 32 channels, read back decoded; with fp8_kv the main-KV
-    entry as an FP8 entry, read back decoded); then indexer -> top-k -> attention over the
+    entry as an FP8 entry, with mxfp4_kv as an MXFP4 entry, read back decoded); then indexer ->
+    top-k -> attention over the
     caches as stored.  r["entry"] = (e, stored main-KV entry, stored key, exact main-KV entry,
     exact key) or None.
     """
@@ -423,6 +424,8 @@ def decode_step_sequence(cfg, inp: Dict[str, np.ndarray], b: int, kv_comp: np.nd
         kv_exact = compress_entry(inp["kv_str"][b], inp["z_str"][b], inp["bias"], cfg.m, e, tok0)
         if fp8_kv:   # kv_comp holds the cache as stored: FP8 entries, read back decoded
             kv_comp[e] = kv_fp8_decode(kv_fp8_encode(kv_exact))
+        elif mxfp4_kv:
+            kv_comp[e] = mxfp4_decode(mxfp4_encode(kv_exact))
         else:
             kv_comp[e] = round_to_store(kv_exact, store)
         ki = compress_entry(inp["kvI_str"][b], inp["zI_str"][b], inp["biasI"], cfg.m, e, tok0)

@@ -197,6 +197,10 @@ CONFIGS: Dict[int, CsaConfig] = {
     13: CsaConfig(13, "CSA decode @1M ctx (B 4, MXFP4 indexer keys: 64 B + 4 UE8M0 scales)",
                   B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
                   act="bf16", kidx="mxfp4", mode="decode"),
+    # V4.1's storage throughout: MXFP4 indexer keys and MXFP4 main-KV entries (288 B)
+    14: CsaConfig(14, "CSA decode @1M ctx (B 4, MXFP4 indexer keys + MXFP4 main-KV entries)",
+                  B=4, N=1 << 20, m=4, d=512, H=64, HI=64, dI=128, k=512, W=128, T=1,
+                  act="bf16", kidx="mxfp4", mode="decode"),
 }
 
 # tensor ids of the per-tensor streams (stable: changing one changes the inputs)

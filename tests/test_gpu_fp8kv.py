@@ -196,3 +196,65 @@ def test_decode_step_fp8kv_matches_oracle(cid, N):
                            [r["kv_comp"][x] for x in g_set - r_set], [r["kv_comp"][y] for y in r_set - g_set])
         assert_out_close_with_swaps(np64(out[b]), r["out"], 2e-2, bound, what=f"out b={b} swaps={swaps}")
         np.testing.assert_allclose(np64(lse[b]), r["lse"], atol=5e-3)
+
+
+@pytest.mark.parametrize("cid,N", [(13, 4 * 2500), (4, 4 * 2500), (2, 4 * 1500)])
+def test_decode_step_mxfp4kv_matches_oracle(cid, N):
+    """The fused decode step over an MXFP4-entry main-KV cache (V4.1's 288-byte entries): the
+    entry the token completes is written as an MXFP4 entry by the indexer CTAs (16-channel
+    blocks inside one CTA), the attention reads MXFP4 entries (oracle: the same on the decoded
+    cache); with MXFP4, FP8 and bf16 indexer keys."""
+    from _helpers import (assert_out_close_with_swaps, assert_selection_ok, keys_f64, lib_config, np_inputs,
+                          swap_bound)
+    cfg = gen.CONFIGS[cid].replace(B=3, N=N)
+    inp = gen.make_inputs(cfg, DEV)
+    inp["q_pos"][1] = N - 3                          # this token completes no block
+    c = lib_config(cfg)
+    kv4 = torch.empty(cfg.B, cfg.E, cfg.d // 2 + cfg.d // 16, dtype=torch.uint8, device=DEV)
+    csa.kv_pack_mxfp4(c, inp["kv_comp"], kv4)
+    dec_cache = O.mxfp4_decode(kv4.cpu().numpy())
+    nb = np_inputs(inp)
+    qk = cfg.kidx in ("fp8", "mxfp4")
+    refs = []
+    for b in range(cfg.B):
+        kdeq = keys_f64(inp["kI"][b], inp["kscale"][b] if qk else None)
+        kvc = dec_cache[b].copy()
+        r = O.decode_step_sequence(cfg, nb, b, kvc, kdeq, fp8_keys=cfg.kidx == "fp8", mx_keys=cfg.kidx == "mxfp4",
+                                   mxfp4_kv=True)
+        r["kv_comp"] = kvc
+        refs.append(r)
+    before = kv4.clone()
+    out = torch.empty(cfg.B, cfg.H, cfg.d, device=DEV, dtype=BF16)
+    lse = torch.empty(cfg.B, cfg.H, device=DEV)
+    idx = torch.empty(cfg.B, cfg.k, dtype=torch.int32, device=DEV)
+    csa.decode_step(c, q_pos=inp["q_pos"], q=inp["q"], qI=inp["qI"], w=inp["w"], sink=inp["sink"], kv_comp=kv4,
+                    kI=inp["kI"], kscale=inp.get("kscale"), kv_tail=inp["kv_str"], z_tail=inp["z_str"],
+                    kvI_tail=inp["kvI_str"], zI_tail=inp["zI_str"], bias=inp["bias"], biasI=inp["biasI"],
+                    kv_local=inp["kv_local"], local_base=inp["local_base"], out=out, lse=lse, idx_out=idx,
+                    mxfp4kv=True)
+    assert csa.get_last_error() == 0
+    rtol_s = 5e-2 if qk else 1e-2
+    for b in range(cfg.B):
+        r = refs[b]
+        if r["entry"] is None:
+            assert torch.equal(kv4[b], before[b])
+        else:
+            e = r["entry"][0]
+            raw = kv4[b, e].cpu().numpy()
+            exact = r["entry"][3]
+            ref_raw = O.mxfp4_encode(exact)
+            assert int((raw != ref_raw).sum()) <= 4, f"new MXFP4 entry b={b}: {int((raw != ref_raw).sum())} bytes differ"
+            got = O.mxfp4_decode(raw)
+            sc = O.e4m3_decode(raw[cfg.d // 2:]).repeat(16)
+            amax = np.abs(exact).reshape(-1, 16).max(-1).repeat(16)
+            bound = 1.01 * sc + np.maximum(0.0, amax - 6 * sc) + 1e-6 * np.abs(exact).max()
+            assert np.all(np.abs(got - exact) <= bound), f"new MXFP4 entry b={b}"
+        fin = r["scores"][np.isfinite(r["scores"])]
+        tol_s = rtol_s * max(np.sqrt((fin ** 2).mean()), 1e-30)
+        gi = idx[b].cpu().numpy()
+        swaps = assert_selection_ok(gi, r["idx"], r["scores"], cfg.k, tol_s)
+        g_set, r_set = set(gi[gi >= 0].tolist()), set(r["idx"][r["idx"] >= 0].tolist())
+        bound = swap_bound(nb["q"][b, 0], r["lse"], cfg.softmax_scale,
+                           [r["kv_comp"][x] for x in g_set - r_set], [r["kv_comp"][y] for y in r_set - g_set])
+        assert_out_close_with_swaps(np64(out[b]), r["out"], 2e-2, bound, what=f"out b={b} swaps={swaps}")
+        np.testing.assert_allclose(np64(lse[b]), r["lse"], atol=5e-3)

@@ -658,6 +658,16 @@ def test_decode_step_fp8_key_and_entry_storage():
     np.testing.assert_array_equal(kv[8], O.kv_fp8_decode(O.kv_fp8_encode(u)))
 
 
+def test_decode_step_mxfp4_entry_storage():
+    C, inp, kv, kI, t, u, v = _decode_case("bf16", d=32)   # two MXFP4 blocks of 16 channels
+    r = O.decode_step_sequence(C, inp, 0, kv, kI, mxfp4_kv=True)
+    np.testing.assert_array_equal(kv[8], O.mxfp4_decode(O.mxfp4_encode(r["entry"][3])))
+    assert not np.array_equal(kv[8], r["entry"][3])
+    # block 0 of u = [0.1, -0.3, 1/3, 2, -7.77, 1e-3, ...]: amax 7.77, scale e4m3(7.77/6 = 1.295) = 1.25;
+    # -7.77 / 1.25 = -6.216 saturates to -6 (-7.5); 2 / 1.25 = 1.6 -> 1.5 (1.875)
+    assert kv[8][4] == -7.5 and kv[8][3] == 1.875
+
+
 def test_decode_step_mxfp4_key_storage():
     C, inp, kv, kI, t, u, v = _decode_case("bf16", dI=32)
     r = O.decode_step_sequence(C, inp, 0, kv, kI, mx_keys=True)
