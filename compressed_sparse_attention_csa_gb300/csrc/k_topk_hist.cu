@@ -195,12 +195,13 @@ constexpr int kMaxChunkPer = kMaxChunks / NT;
 
 struct SelSmem {
   uint32_t cpre[kMaxChunks];  // last CTA: first candidate index of every chunk
+  uint32_t ccnt[kMaxChunks];  // last CTA: candidates of every chunk
   uint32_t ak[kAllCap];      // last CTA: the row's candidates in position order
   int32_t ap[kAllCap];
   uint32_t hist[2 * kSortBuckets];
   uint32_t tmp[32];
   uint32_t res[8];
-  uint32_t b1, last, n_gt;
+  uint32_t b1, last, n_gt, n_eq;
 };
 
 size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
@@ -276,9 +277,10 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
   for (int i = tid; i < kRowWords; i += NT) rh[i] = 0u;
   if (tid == 0) *ticket = 0u;
 
-  // ---- the row's last CTA: gather the candidates in chunk (= position) order
+  // ---- the row's last CTA: the chunks' candidate counts and their prefix (one block scan)
   const uint32_t* base = cand + static_cast<size_t>(row) * n_chunks * kSlotWords;
-  uint32_t my_n = 0, my_over = 0;
+  uint32_t my_n = 0;
+  bool my_over = false;
   const int cpt = (n_chunks + NT - 1) / NT;  // chunks per thread (contiguous)
   uint32_t cc[kMaxChunkPer];
 #pragma unroll
@@ -286,15 +288,22 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
     const int ch = tid * cpt + q;
     cc[q] = (q < cpt && ch < n_chunks) ? __ldcg(base + static_cast<size_t>(ch) * kSlotWords) : 0u;
     my_n += cc[q];
-    my_over += cc[q] > static_cast<uint32_t>(kSlotCap);
+    my_over |= cc[q] > static_cast<uint32_t>(kSlotCap);
   }
-  uint32_t n_all_u, n_over;
+  if (tid == 0) {
+    S.n_gt = 0u;
+    S.n_eq = 0u;
+  }
+  uint32_t n_all_u;
   uint32_t run = block_exclusive_scan<NT>(my_n, S.tmp, &n_all_u);
-  block_exclusive_scan<NT>(my_over, S.tmp, &n_over);
+  const bool any_over = __syncthreads_or(my_over) != 0;
 #pragma unroll
   for (int q = 0; q < kMaxChunkPer; ++q) {
     const int ch = tid * cpt + q;
-    if (q < cpt && ch < n_chunks) S.cpre[ch] = run;
+    if (q < cpt && ch < n_chunks) {
+      S.cpre[ch] = run;
+      S.ccnt[ch] = cc[q];
+    }
     run += cc[q];
   }
   __syncthreads();
@@ -302,24 +311,26 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
   int32_t* orow = idx + row * k;
   // with a candidate map (ascending positions) the winners' slots are written as positions
   const int32_t* cm = cmap ? cmap + row * n_cols : nullptr;
-  if (n_all <= kAllCap && n_over == 0) {
+  if (n_all <= kAllCap && !any_over) {
+    // the candidates, chunk by chunk in position order: tpc threads a chunk, so every load is in
+    // flight at once; the keys above the threshold digit are counted on the way
+    int tpc = 1;
+    while (tpc * 2 * n_chunks <= NT) tpc *= 2;
     uint32_t gt = 0;
-    for (int e = tid; e < n_all; e += NT) {
-      // the chunk holding candidate e: the last chunk whose prefix is <= e
-      int lo = 0, hi = n_chunks - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (S.cpre[mid] <= static_cast<uint32_t>(e)) lo = mid; else hi = mid - 1;
+    for (int ch = tid / tpc; ch < n_chunks; ch += NT / tpc) {
+      const uint32_t* sl = base + static_cast<size_t>(ch) * kSlotWords;
+      const uint32_t c0 = S.cpre[ch], cn = S.ccnt[ch];
+      for (uint32_t j = static_cast<uint32_t>(tid % tpc); j < cn; j += static_cast<uint32_t>(tpc)) {
+        const uint32_t key = __ldcg(sl + 4 + j);
+        S.ak[c0 + j] = key;
+        S.ap[c0 + j] = static_cast<int32_t>(__ldcg(sl + 4 + kSlotCap + j));
+        gt += (key >> 20) > b1 ? 1u : 0u;
       }
-      const uint32_t* sl = base + static_cast<size_t>(lo) * kSlotWords;
-      const uint32_t j = static_cast<uint32_t>(e) - S.cpre[lo];
-      const uint32_t key = __ldcg(sl + 4 + j);
-      S.ak[e] = key;
-      S.ap[e] = static_cast<int32_t>(__ldcg(sl + 4 + kSlotCap + j));
-      gt += (key >> 20) > b1 ? 1u : 0u;
     }
-    uint32_t n_gt;
-    block_exclusive_scan<NT>(gt, S.tmp, &n_gt);  // (its barriers also publish ak / ap)
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    if ((tid & 31) == 0 && gt) atomicAdd(&S.n_gt, gt);
+    __syncthreads();
+    const uint32_t n_gt = S.n_gt;
     const int need = k - static_cast<int>(n_gt);
     uint32_t T = 1u;
     int quota = 0x7fffffff;
@@ -327,38 +338,56 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
       const uint32_t* ak = S.ak;
       select_in_bin<B16, NT>([ak](int x) { return ak[x]; }, n_all, need, b1, S.hist, S.tmp, S.res, &T, &quota, tid);
     }
-    // stable compaction over contiguous segments: keys above T, then the first quota keys
-    // equal to T in position order
+    // the winners in position order: every key above T, then the first quota keys equal to T
     const int seg = (n_all + NT - 1) / NT;
     const int lo = tid * seg, hi = min(n_all, lo + seg);
-    uint32_t c_tie = 0;
-    for (int e = lo; e < hi; ++e) c_tie += S.ak[e] == T;
-    uint32_t tie_r = block_exclusive_scan<NT>(c_tie, S.tmp, nullptr);
-    uint32_t c_win = 0;
-    {
-      uint32_t tr = tie_r;
-      for (int e = lo; e < hi; ++e) {
-        const uint32_t key = S.ak[e];
-        if (key > T) {
-          ++c_win;
-        } else if (key == T) {
-          if (tr < static_cast<uint32_t>(quota)) ++c_win;
-          ++tr;
-        }
-      }
-    }
-    uint32_t n_win;
-    uint32_t out = block_exclusive_scan<NT>(c_win, S.tmp, &n_win);
+    uint32_t c_tie = 0, c_ge = 0;
     for (int e = lo; e < hi; ++e) {
       const uint32_t key = S.ak[e];
-      bool w = key > T;
-      if (key == T) {
-        w = tie_r < static_cast<uint32_t>(quota);
-        ++tie_r;
-      }
-      if (w && out < static_cast<uint32_t>(k)) orow[out++] = cm ? cm[S.ap[e]] : S.ap[e];
+      c_tie += key == T;
+      c_ge += key >= T;
     }
-    for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
+    const uint32_t wt = __reduce_add_sync(0xffffffffu, c_tie);
+    if ((tid & 31) == 0 && wt) atomicAdd(&S.n_eq, wt);
+    __syncthreads();
+    if (S.n_eq <= static_cast<uint32_t>(quota)) {
+      // every key equal to T wins (the usual case: no tie at the threshold is cut)
+      uint32_t n_win;
+      uint32_t out = block_exclusive_scan<NT>(c_ge, S.tmp, &n_win);
+      for (int e = lo; e < hi; ++e)
+        if (S.ak[e] >= T && out < static_cast<uint32_t>(k)) {
+          orow[out++] = cm ? cm[S.ap[e]] : S.ap[e];
+        }
+      for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
+    } else {
+      // stable compaction over contiguous segments: ties ranked in position order
+      uint32_t tie_r = block_exclusive_scan<NT>(c_tie, S.tmp, nullptr);
+      uint32_t c_win = 0;
+      {
+        uint32_t tr = tie_r;
+        for (int e = lo; e < hi; ++e) {
+          const uint32_t key = S.ak[e];
+          if (key > T) {
+            ++c_win;
+          } else if (key == T) {
+            if (tr < static_cast<uint32_t>(quota)) ++c_win;
+            ++tr;
+          }
+        }
+      }
+      uint32_t n_win;
+      uint32_t out = block_exclusive_scan<NT>(c_win, S.tmp, &n_win);
+      for (int e = lo; e < hi; ++e) {
+        const uint32_t key = S.ak[e];
+        bool w = key > T;
+        if (key == T) {
+          w = tie_r < static_cast<uint32_t>(quota);
+          ++tie_r;
+        }
+        if (w && out < static_cast<uint32_t>(k)) orow[out++] = cm ? cm[S.ap[e]] : S.ap[e];
+      }
+      for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
+    }
   } else {
     // too many candidates (a bin full of ties, or crowded into one chunk): select over the whole
     // row in position order
