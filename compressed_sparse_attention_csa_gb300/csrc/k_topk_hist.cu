@@ -425,9 +425,11 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
 
 // ---- one CTA per row (many long rows: the prefill chunk, the block pool)
 // The row is histogrammed in shared memory (4096 fine bins of the order-preserving key), the
-// threshold bin b1 found, and the row read again (now from L2) keeping the (key, position) of
-// every score with digit >= b1 in position order (per-thread contiguous slices, one block
-// scan per batch); the exact selection then runs as in topk_select_kernel.
+// threshold bin b1 found, and the row read again (now from L2) appending the (key, position)
+// of every score with digit >= b1 in any order (one shared-memory atomic per warp and batch);
+// the exact threshold key T then comes from radix passes inside the b1 bin, ties at T are cut
+// to the lowest positions by a radix pass on their positions, and the winners are written
+// ascending by a counting sort on their positions.
 // The candidate list holds CAP entries: 2048 for k <= 512 (four CTAs fit on an SM), else 8192.
 constexpr int kRowPer = 8;                 // scores per thread per batch
 constexpr int kRowBatch = kRowPer * NT;    // 4096
@@ -440,7 +442,7 @@ struct RowSmem {
   uint32_t sort[2 * kSortBuckets];
   uint32_t tmp[32];
   uint32_t res[8];
-  uint32_t n_gt;
+  uint32_t n_gt, n_app, n_eq, n_win, n_tie;
 };
 
 template <int CAP>
@@ -449,7 +451,7 @@ size_t row_smem_bytes(int k) { return sizeof(RowSmem<CAP>) + 2 * static_cast<siz
 static_assert(kRowPer == 8, "eight keys a thread");
 
 template <int CAP, bool B16>
-__global__ void __launch_bounds__(NT) topk_row_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
+__global__ void __launch_bounds__(NT, CAP <= 2048 ? 4 : 1) topk_row_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
                                                       int64_t n_cols, int k, int32_t* idx, const int32_t* cmap) {
   using K = ScoreKey<B16>;
   const typename K::T* scores = static_cast<const typename K::T*>(scores_v);
@@ -480,38 +482,55 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const void* scores_v, int6
   }
   __syncthreads();
   const uint32_t b1 = team_threshold_digit_smem<NT>(S.hist, k, S.tmp, S.res, tid, 0);
-  // pass 2: the candidates (digit >= b1) in position order
-  uint32_t n_all = 0, n_gt = 0;
+  // pass 2: the candidates (digit >= b1), appended in any order (each warp reserves its batch's
+  // slots with one shared-memory atomic: no block barrier inside the loop)
+  if (tid == 0) {
+    S.n_gt = 0u;
+    S.n_app = 0u;
+    S.n_eq = 0u;
+    S.n_win = 0u;
+    S.n_tie = 0u;
+  }
+  __syncthreads();
+  const int lane = tid & 31;
+  uint32_t my_gt = 0;
   for (int64_t base = 0; base < nvr; base += kRowBatch) {
     uint32_t v[kRowPer];
     const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
     load_keys8<B16>(srow, t0, nvr, v);
-    uint32_t key[kRowPer];
-    uint32_t c = 0, g = 0;
+    uint32_t c = 0;
 #pragma unroll
     for (int u = 0; u < kRowPer; ++u) {
-      const uint32_t x = v[u];
-      key[u] = (t0 + u < nvr && (x >> 20) >= b1) ? x : 0u;
-      c += key[u] != 0u;
-      g += key[u] != 0u && (x >> 20) > b1;
+      const bool in = t0 + u < nvr && (v[u] >> 20) >= b1;
+      c += in;
+      my_gt += in && (v[u] >> 20) > b1;
     }
-    uint32_t tot, gtot;
-    uint32_t off = n_all + block_exclusive_scan<NT>(c, S.tmp, &tot);
-    block_exclusive_scan<NT>(g, S.tmp, &gtot);
+    uint32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const uint32_t wtot = __shfl_sync(0xffffffffu, x, 31);
+    uint32_t wbase = 0;
+    if (lane == 31 && wtot) wbase = atomicAdd(&S.n_app, wtot);
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    uint32_t off = wbase + x - c;
 #pragma unroll
     for (int u = 0; u < kRowPer; ++u) {
-      if (key[u] != 0u) {
+      if (t0 + u < nvr && (v[u] >> 20) >= b1) {
         if (off < static_cast<uint32_t>(CAP)) {
-          S.ak[off] = key[u];
+          S.ak[off] = v[u];
           S.ap[off] = static_cast<int32_t>(t0 + u);
         }
         ++off;
       }
     }
-    n_all += tot;
-    n_gt += gtot;
   }
+  my_gt = __reduce_add_sync(0xffffffffu, my_gt);
+  if (lane == 0 && my_gt) atomicAdd(&S.n_gt, my_gt);
   __syncthreads();
+  const uint32_t n_all = S.n_app, n_gt = S.n_gt;
   int32_t* orow = idx + row * k;
   // with a candidate map (ascending positions) the winners' slots are written as positions
   const int32_t* cm = cmap ? cmap + row * n_cols : nullptr;
@@ -524,38 +543,55 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const void* scores_v, int6
       const uint32_t* ak = S.ak;
       select_in_bin<B16, NT>([ak](int x) { return ak[x]; }, na, need, b1, S.sort, S.tmp, S.res, &T, &quota, tid);
     }
-    // stable compaction over contiguous segments: keys above T, then the first quota keys
-    // equal to T in position order
-    const int seg = (na + NT - 1) / NT;
-    const int lo = tid * seg, hi = min(na, lo + seg);
-    uint32_t c_tie = 0;
-    for (int e = lo; e < hi; ++e) c_tie += S.ak[e] == T;
-    uint32_t tie_r = block_exclusive_scan<NT>(c_tie, S.tmp, nullptr);
-    uint32_t c_win = 0;
-    {
-      uint32_t tr = tie_r;
-      for (int e = lo; e < hi; ++e) {
-        const uint32_t key = S.ak[e];
-        if (key > T) {
-          ++c_win;
-        } else if (key == T) {
-          if (tr < static_cast<uint32_t>(quota)) ++c_win;
-          ++tr;
-        }
+    // the keys equal to T: all of them win unless the quota cuts them; then the quota lowest
+    // positions among them win
+    uint32_t c_eq = 0;
+    for (int e = tid; e < na; e += NT) c_eq += S.ak[e] == T;
+    c_eq = __reduce_add_sync(0xffffffffu, c_eq);
+    if (lane == 0 && c_eq) atomicAdd(&S.n_eq, c_eq);
+    __syncthreads();
+    const uint32_t n_eq = S.n_eq;
+    int32_t pos_cut = 0x7fffffff;  // ties with a position <= pos_cut win
+    if (n_eq > static_cast<uint32_t>(quota) && n_eq <= 256u) {
+      // few ties (BF16 scores make them common): list their positions, rank each against the
+      // list; the tie of rank quota - 1 is the last winner
+      uint32_t* tl = S.sort;
+      for (int e = tid; e < na; e += NT)
+        if (S.ak[e] == T) tl[atomicAdd(&S.n_tie, 1u)] = static_cast<uint32_t>(S.ap[e]);
+      __syncthreads();
+      for (int i = tid; i < static_cast<int>(n_eq); i += NT) {
+        const uint32_t pi = tl[i];
+        int r = 0;
+        for (int j = 0; j < static_cast<int>(n_eq); ++j) r += tl[j] < pi;
+        if (r == quota - 1) S.res[0] = pi;
       }
+      __syncthreads();
+      pos_cut = static_cast<int32_t>(S.res[0]);
+      __syncthreads();  // S.sort and S.res are reused below
+    } else if (n_eq > static_cast<uint32_t>(quota)) {
+      // many ties: the quota largest values ~pos among them (positions < 2^24 and distinct, so
+      // exactly quota of them), by radix passes on the 24 position bits
+      const uint32_t* ak = S.ak;
+      const int32_t* ap = S.ap;
+      const uint32_t Tk = T;
+      uint32_t Tp = 0u;
+      int qp = 0;
+      team_select_largest<NT>(
+          [ak, ap, Tk](int x) { return ak[x] == Tk ? (0x80000000u | (~static_cast<uint32_t>(ap[x]) & 0xFFFFFFu)) : 0u; },
+          na, quota, 24, 0x80000000u, 0xFF000000u, S.sort, S.tmp, S.res, &Tp, &qp, tid, 0);
+      pos_cut = static_cast<int32_t>(~Tp & 0xFFFFFFu);
     }
-    uint32_t n_win;
-    uint32_t out = block_exclusive_scan<NT>(c_win, S.tmp, &n_win);
-    for (int e = lo; e < hi; ++e) {
+    // the winners' positions, appended in any order, then written ascending
+    for (int e = tid; e < na; e += NT) {
       const uint32_t key = S.ak[e];
-      bool w = key > T;
-      if (key == T) {
-        w = tie_r < static_cast<uint32_t>(quota);
-        ++tie_r;
+      if (key > T || (key == T && S.ap[e] <= pos_cut)) {
+        const uint32_t w = atomicAdd(&S.n_win, 1u);
+        if (w < static_cast<uint32_t>(k)) sel[w] = S.ap[e];
       }
-      if (w && out < static_cast<uint32_t>(k)) orow[out++] = cm ? cm[S.ap[e]] : S.ap[e];
     }
-    for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
+    __syncthreads();
+    const int n_win = min(static_cast<int>(S.n_win), k);
+    team_write_sorted<NT>(sel, n_win, k, nvr, S.sort, S.tmp, srt, orow, cm, tid, 0);
   } else {
     // too many candidates (a bin full of ties): select over the whole row in position order
     const typename K::T* rowp = srow;
