@@ -399,6 +399,33 @@ class Prefill:
     def topk_fp32(self):
         self.csa.topk(self.c, self.scores, self.idx)
 
+    def _packed(self):
+        if getattr(self, "kv8", None) is None:
+            import torch
+            cfg, inp = self.cfg, self.inp
+            dev = inp["kv_comp"].device
+            self.kv8 = torch.empty(cfg.B, cfg.E, cfg.d + 64, dtype=torch.uint8, device=dev)
+            self.kv4 = torch.empty(cfg.B, cfg.E, cfg.d // 2 + cfg.d // 16, dtype=torch.uint8, device=dev)
+            self.csa.kv_pack_fp8(self.c, inp["kv_comp"], self.kv8)
+            self.csa.kv_pack_mxfp4(self.c, inp["kv_comp"], self.kv4)
+
+    def attn_bf16(self):
+        inp = self.inp
+        self.csa.sparse_attn(self.c, inp["q"], inp["kv_comp"], self.idx, inp["kv_local"], inp["local_base"],
+                             inp["q_pos"], inp["sink"], self.out, self.lse)
+
+    def attn_fp8(self):
+        inp = self.inp
+        self._packed()
+        self.csa.sparse_attn_fp8kv(self.c, inp["q"], self.kv8, self.idx, inp["kv_local"], inp["local_base"],
+                                   inp["q_pos"], inp["sink"], self.out, self.lse)
+
+    def attn_mxfp4(self):
+        inp = self.inp
+        self._packed()
+        self.csa.sparse_attn_mxfp4kv(self.c, inp["q"], self.kv4, self.idx, inp["kv_local"], inp["local_base"],
+                                     inp["q_pos"], inp["sink"], self.out, self.lse)
+
     def topk_bf16(self):
         self._bf16_buffers()
         self.csa.topk(self.c, self.scores16, self.idx16)
@@ -945,6 +972,17 @@ def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):
         timed(gx, gx_all, 3 * R)
         sel[name] = max_over_ranks(timed(gx, gx_all, Kp) / Kp)
         del gx, gx_all
+    # the chunk's attention over the selected entries stored as bf16 rows, FP8 entries (576 B) and
+    # MXFP4 entries (288 B): the same selections, the quantised rows widened in the gather
+    for w in wls:
+        w.step()
+        w.attn_fp8()
+        w.attn_mxfp4()
+    for name in ("attn_bf16", "attn_fp8", "attn_mxfp4"):
+        gx, gx_all = graphs(name)
+        timed(gx, gx_all, 3 * R)
+        sel[name] = max_over_ranks(timed(gx, gx_all, Kp) / Kp)
+        del gx, gx_all
     w0.step()
     w0.step_bf16()
     torch.cuda.synchronize(dev)
@@ -969,7 +1007,10 @@ def prefill_leg(csa, torch, dev, row0, K, max_over_ranks, world):
                            "selector_us_fp32": round(sel["topk_fp32"] * 1e3, 2),
                            "selector_us_bf16": round(sel["topk_bf16"] * 1e3, 2),
                            "selector_speedup": round(sel["topk_fp32"] / sel["topk_bf16"], 3),
-                           "recall_vs_fp32": round(recall, 5)}}
+                           "recall_vs_fp32": round(recall, 5)},
+           "entry_formats": {"attention_us_bf16_entries": round(sel["attn_bf16"] * 1e3, 2),
+                             "attention_us_fp8_entries": round(sel["attn_fp8"] * 1e3, 2),
+                             "attention_us_mxfp4_entries": round(sel["attn_mxfp4"] * 1e3, 2)}}
     del gs, g_all, gs_s, g_all_s, gs16, g_all16, wls, w0
     torch.cuda.empty_cache()
     return out

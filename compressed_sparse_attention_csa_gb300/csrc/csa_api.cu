@@ -799,7 +799,7 @@ csa_status csa_sparse_attn_fp8kv(const csa_config* cfg, const void* q, int32_t T
     return CSA_ERR_ALIGN;
   const int sms = device_sm_count();
   if (T < 0 || E_cap < 0 || L < 0 || !attn_shape_ok(cfg) || E_cap * cfg->B >= (int64_t(1) << 31) ||
-      !attn_fp8kv_supported(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms))
+      !attn_quantkv_supported(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms))
     return CSA_ERR_SHAPE;
   const size_t need = attn_workspace_bytes(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms);
   if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;
@@ -842,7 +842,7 @@ csa_status csa_sparse_attn_mxfp4kv(const csa_config* cfg, const void* q, int32_t
     return CSA_ERR_ALIGN;
   const int sms = device_sm_count();
   if (T < 0 || E_cap < 0 || L < 0 || !attn_shape_ok(cfg) || E_cap * cfg->B >= (int64_t(1) << 31) ||
-      !attn_fp8kv_supported(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms))
+      !attn_quantkv_supported(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms))
     return CSA_ERR_SHAPE;
   const size_t need = attn_workspace_bytes(cfg->B, T, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms);
   if (need > 0 && (!ws || ws_bytes < need)) return CSA_ERR_WORKSPACE;

@@ -81,7 +81,8 @@ cudaError_t launch_kv_pack_fp8(const KvPackArgs& a, cudaStream_t s);
 
 // Sparse attention over FP8 main-KV entries (kv_comp [B, E_cap, 576] bytes), decode shapes:
 // the split plan of csa_sparse_attn's decode path (few queries, k + W > 128 rows).
-bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms);
+bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms);  // decode split plan
+bool attn_quantkv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms);  // + many queries
 cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s);
 // The same over MXFP4 main-KV entries (kv_comp [B, E_cap, 288] bytes).
 cudaError_t launch_attn_mxfp4kv(const AttnArgs& a, cudaStream_t s);

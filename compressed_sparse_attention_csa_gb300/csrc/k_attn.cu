@@ -558,6 +558,45 @@ __global__ void __launch_bounds__(kD) attn_merge_kernel(const AttnArgs a, const 
   for (int j = 0; j < kMergeHeads; ++j) out[j * kD] = __float2bfloat16_rn(acc[j] * s_inv[j]);
 }
 
+// FP8 main-KV entries: 448 e4m3 codes (28 chunks of 16) then 64 bf16 (8 chunks of 16).
+constexpr int kFp8Chunks = (kD - 64) / 16;
+constexpr int kFp8RowBytes = (kD - 64) + 64 * 2;
+// MXFP4 main-KV entries: 256 payload bytes (E2M1 nibbles) then 32 e4m3 scales (16 dims each).
+constexpr int kMxRowBytes = kD / 2 + kD / 16;
+
+// 16 e4m3 codes (one 16-byte load) -> 16 bf16 (exact) as two 16-byte tile chunks
+__device__ __forceinline__ void widen_e4m3x16(const uint4& raw, uint4& lo, uint4& hi) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw);
+  uint32_t* l = reinterpret_cast<uint32_t*>(&lo);
+  uint32_t* h = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2_raw p0 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[e] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw p1 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[e] >> 16), __NV_E4M3);
+    const __nv_bfloat162 b0 = __float22bfloat162_rn(__half22float2(__half2(p0)));
+    const __nv_bfloat162 b1 = __float22bfloat162_rn(__half22float2(__half2(p1)));
+    uint32_t* dstw = e < 2 ? l : h;
+    dstw[(e & 1) * 2] = *reinterpret_cast<const uint32_t*>(&b0);
+    dstw[(e & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+  }
+}
+// 8 E2M1 codes (one 32-bit word, element 2i in the low nibble) times their block's e4m3 scale
+// -> 8 bf16 (exact: at most 2 + 4 significant bits) as one 16-byte tile chunk
+__device__ __forceinline__ uint4 widen_e2m1x8(uint32_t w, uint8_t sc_code) {
+  const __half sc = __half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sc_code), __NV_E4M3));
+  const __half2 sc2 = __half2half2(sc);
+  uint4 o;
+  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2 hh =
+        __hmul2(__half2(__nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(w >> (8 * e)), __NV_E2M1)), sc2);
+    const __nv_bfloat162 two = __float22bfloat162_rn(__half22float2(hh));
+    ow[e] = *reinterpret_cast<const uint32_t*>(&two);
+  }
+  return o;
+}
+
 // ------------------------------------------------------------------ pipelined path (many queries)
 // One CTA per query over its whole row list, in tiles of 64 rows that 11 gather warps stage
 // (16-byte cp.async, many requests in flight per SM) into two shared-memory buffers while the
@@ -602,6 +641,10 @@ __device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint
                : "memory");
 }
 
+// KVF: the selected entries' storage: 0 bf16 rows, 1 FP8 entries, 2 MXFP4 entries (widened to
+// bf16 in the gather, exactly, so the products are those of the bf16 path over the decoded
+// cache); the window rows are bf16 in every case.
+template <int KVF>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a, const TcAttnSplit sp) {
   using LY = PfLayout;
   extern __shared__ uint8_t smem_raw[];
@@ -675,6 +718,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
     //      i / 64, 16-byte piece i % 64); the query likewise
     const int g = tid - 32 * 9;
     const __nv_bfloat16* kvc = static_cast<const __nv_bfloat16*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kD;
+    const uint8_t* kvq = static_cast<const uint8_t*>(a.kv_comp) +
+                         static_cast<int64_t>(b) * a.E_cap * (KVF == 1 ? kFp8RowBytes : kMxRowBytes);
     const __nv_bfloat16* kvl = static_cast<const __nv_bfloat16*>(a.kv_local) + static_cast<int64_t>(b) * a.L * kD;
     const int64_t lbase = a.local_base[b];
     // many queries re-read the caches (keep them in L2); a split query reads its rows once
@@ -702,11 +747,65 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
         uint8_t* d = dst + (c >> 3) * (kPR * 128) + sw128(j, c & 7);
         const int lp = row_lo + it * kPR + j;
         if (lp < row_hi) {
+          if (KVF != 0 && lp < n_sel) {
+            // quantised entry: the FP8 entry's bf16 tail (dims >= d - 64) is copied as is; the
+            // rest is widened below
+            if (KVF == 1 && c >= kFp8Chunks * 2)
+              cp_async16_hint(d, kvq + entry_at(a, sel, lp) * kFp8RowBytes + kFp8Chunks * 16 + (c - kFp8Chunks * 2) * 16,
+                              pol);
+            continue;
+          }
           const __nv_bfloat16* src = lp < n_sel ? kvc + entry_at(a, sel, lp) * kD
                                                 : kvl + (p_lo + (lp - n_sel) - lbase) * kD;
           cp_async16_hint(d, src + c * 8, pol);
         } else {
           *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if constexpr (KVF != 0) {
+        // the quantised parts of the tile's selected entries: every load of a thread first,
+        // then the widening into the swizzled tile (FP8: item = 16 codes -> two chunks;
+        // MXFP4: item = 16 payload bytes (32 dims) + their two scale bytes -> four chunks)
+        constexpr int kQI = KVF == 1 ? kFp8Chunks : kD / 32;   // items a row
+        constexpr int kIt = (kPR * kQI + kGath - 1) / kGath;
+        uint4 raw[kIt];
+        uint32_t scb[kIt];
+#pragma unroll
+        for (int u = 0; u < kIt; ++u) {
+          const int i = g + u * kGath;
+          const int j = i / kQI, q = i - j * kQI;
+          const int lp = row_lo + it * kPR + j;
+          if (i < kPR * kQI && lp < row_hi && lp < n_sel) {
+            const int64_t e = entry_at(a, sel, lp);
+            if constexpr (KVF == 1) {
+              raw[u] = __ldg(reinterpret_cast<const uint4*>(kvq + e * kFp8RowBytes + q * 16));
+            } else {
+              raw[u] = __ldg(reinterpret_cast<const uint4*>(kvq + e * kMxRowBytes + q * 16));
+              scb[u] = __ldg(reinterpret_cast<const uint16_t*>(kvq + e * kMxRowBytes + kD / 2 + 2 * q));
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kIt; ++u) {
+          const int i = g + u * kGath;
+          const int j = i / kQI, q = i - j * kQI;
+          const int lp = row_lo + it * kPR + j;
+          if (i < kPR * kQI && lp < row_hi && lp < n_sel) {
+            if constexpr (KVF == 1) {
+              uint4 lo, hi;
+              widen_e4m3x16(raw[u], lo, hi);
+              *reinterpret_cast<uint4*>(dst + ((2 * q) >> 3) * (kPR * 128) + sw128(j, (2 * q) & 7)) = lo;
+              *reinterpret_cast<uint4*>(dst + ((2 * q + 1) >> 3) * (kPR * 128) + sw128(j, (2 * q + 1) & 7)) = hi;
+            } else {
+              const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[u]);
+#pragma unroll
+              for (int t4 = 0; t4 < 4; ++t4) {
+                const int c = 4 * q + t4;
+                *reinterpret_cast<uint4*>(dst + (c >> 3) * (kPR * 128) + sw128(j, c & 7)) =
+                    widen_e2m1x8(w[t4], static_cast<uint8_t>(scb[u] >> (8 * (t4 >> 1))));
+              }
+            }
+          }
         }
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
@@ -933,11 +1032,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
 // step writes, so they are gathered before the wait on the top-k; the selected rows follow.
 // Partials are stored [query][split][head][dim] (each warp store is 128 contiguous bytes)
 // and merged, with the sink, by attn_merge_wide_kernel.
-// FP8 main-KV entries: 448 e4m3 codes (28 chunks of 16) then 64 bf16 (8 chunks of 16).
-constexpr int kFp8Chunks = (kD - 64) / 16;
-constexpr int kFp8RowBytes = (kD - 64) + 64 * 2;
-// MXFP4 main-KV entries: 256 payload bytes (E2M1 nibbles) then 32 e4m3 scales (16 dims each).
-constexpr int kMxRowBytes = kD / 2 + kD / 16;
 
 
 template <int NH>
@@ -1769,10 +1863,10 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     }
     static std::atomic<unsigned long long> dattr{0};
     if (first_use_in_context(dattr)) {
-      cudaFuncSetAttribute(attn_pf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_pf_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(PfLayout::kSmem));
     }
-    cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows), sp.n_split), dim3(kPfThreads),
+    cudaError_t e = launch_pdl(attn_pf_kernel<0>, dim3(static_cast<unsigned>(rows), sp.n_split), dim3(kPfThreads),
                                PfLayout::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess || sp.n_split == 1) return e;
@@ -1795,10 +1889,10 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     if (sp.n_split == 1 && a.k <= kPfMaxK) {
       static std::atomic<unsigned long long> pattr{0};
       if (first_use_in_context(pattr)) {
-        cudaFuncSetAttribute(attn_pf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(attn_pf_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PfLayout::kSmem));
       }
-      const cudaError_t e = launch_pdl(attn_pf_kernel, dim3(static_cast<unsigned>(rows)), dim3(kPfThreads),
+      const cudaError_t e = launch_pdl(attn_pf_kernel<0>, dim3(static_cast<unsigned>(rows)), dim3(kPfThreads),
                                        PfLayout::kSmem, s, a, sp);
       count_launches(1);
       return e;
@@ -1857,11 +1951,33 @@ bool attn_fp8kv_supported(int B, int T, int H, int d, int k, int W, int act, int
   return sp.n_split > 1 && sp.rows_per_split == kRows;
 }
 
+// Quantised entries: the decode split plan (few queries), or one CTA a query over its whole
+// row list (many queries: the prefill chunk) on attn_pf_kernel.
+static bool attn_quantkv_pf(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
+  if (!attn_uses_tensor_cores(act, H, d, k)) return false;
+  return plan_split(B, T, k, W, num_sms).n_split == 1 && k <= kPfMaxK;
+}
+
+bool attn_quantkv_supported(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
+  return attn_fp8kv_supported(B, T, H, d, k, W, act, num_sms) || attn_quantkv_pf(B, T, H, d, k, W, act, num_sms);
+}
+
 template <int KVF>
 cudaError_t launch_attn_quantkv(const AttnArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T;
   if (rows == 0) return cudaSuccess;
-  if (!attn_fp8kv_supported(a.B, a.T, a.H, a.d, a.k, a.W, a.act, a.num_sms)) return cudaErrorInvalidValue;
+  if (!attn_fp8kv_supported(a.B, a.T, a.H, a.d, a.k, a.W, a.act, a.num_sms)) {
+    if (!attn_quantkv_pf(a.B, a.T, a.H, a.d, a.k, a.W, a.act, a.num_sms)) return cudaErrorInvalidValue;
+    static std::atomic<unsigned long long> pattr{0};
+    if (first_use_in_context(pattr))
+      cudaFuncSetAttribute(attn_pf_kernel<KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(PfLayout::kSmem));
+    const TcAttnSplit sp1 = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
+    const cudaError_t e = launch_pdl(attn_pf_kernel<KVF>, dim3(static_cast<unsigned>(rows)), dim3(kPfThreads),
+                                     PfLayout::kSmem, s, a, sp1);
+    count_launches(1);
+    return e;
+  }
   TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   sp.part_o = reinterpret_cast<float*>(ws);

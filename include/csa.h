@@ -394,10 +394,12 @@ csa_status csa_inverse_rope_quant(const csa_config *cfg, const void *o, int64_t 
  * csa_compress_kv_norm_rope_fp8kv — csa_compress_kv_norm_rope writing FP8 entries:
  *                   out [B, E_cap, dim + 64] bytes.
  * csa_sparse_attn_fp8kv — csa_sparse_attn with kv_comp [B, E_cap, 576] FP8 entries (the rows
- *                   are widened to bf16 in shared memory before the tensor-core products);
- *                   window rows stay cfg->act.  Decode shapes only (bf16, H = 64, d = 512 and
- *                   the split plan of few queries: B*T below the SM count and k + W > 128);
- *                   CSA_ERR_SHAPE otherwise.  Workspace: csa_workspace_size(CSA_OP_ATTN, ...).
+ *                   are widened to bf16 in shared memory before the tensor-core products, exactly,
+ *                   so the result equals csa_sparse_attn over the decoded cache); window rows
+ *                   stay cfg->act.  bf16, H = 64, d = 512, and either few queries (B*T below the
+ *                   SM count, k + W > 128: the decode split plan) or one CTA a query (many
+ *                   queries, such as a prefill chunk; k <= 2048); CSA_ERR_SHAPE otherwise.
+ *                   Workspace: csa_workspace_size(CSA_OP_ATTN, ...).
  */
 csa_status csa_kv_pack_fp8(const csa_config *cfg, const void *x, int64_t rows, int32_t dim, void *out,
                            csa_stream_t stream);
@@ -421,7 +423,7 @@ csa_status csa_sparse_attn_fp8kv(const csa_config *cfg, const void *q, int32_t T
  * csa_kv_pack_mxfp4 — rows x [rows, dim] (cfg->act) -> out [rows, dim/2 + dim/16] bytes;
  *                     dim % 128 == 0, <= 1024.
  * csa_sparse_attn_mxfp4kv — csa_sparse_attn_fp8kv over MXFP4 entries (kv_comp [B, E_cap, 288]):
- *                     the same decode shapes, widened to bf16 in shared memory.
+ *                     the same shapes, widened to bf16 in shared memory (exactly).
  */
 csa_status csa_kv_pack_mxfp4(const csa_config *cfg, const void *x, int64_t rows, int32_t dim, void *out,
                              csa_stream_t stream);

@@ -93,15 +93,42 @@ def test_sparse_attn_fp8kv_decode(B, nsel):
     assert torch.equal(out, out_b) and torch.equal(lse, lse_b)
 
 
-def test_sparse_attn_fp8kv_rejects_non_decode_shapes():
-    B, T, H, d, E, k, L = 1, 300, 64, 512, 1500, 512, 400
-    q, kv, kl, sink, idx = _attn_inputs(830, B, T, H, d, E, k, L, BF16)
-    packed = torch.zeros(B, E, d + 64, dtype=torch.uint8, device=DEV)
+@pytest.mark.parametrize("fmt", ["fp8", "mxfp4"])
+@pytest.mark.parametrize("B,T", [(1, 300), (2, 170)])
+def test_sparse_attn_quantkv_many_queries(fmt, B, T):
+    """Many queries (a prefill chunk: one CTA a query on the pipelined kernel) over FP8 / MXFP4
+    entries: the rows widened to bf16 in the gather, exactly, so the result is bit-identical to
+    csa_sparse_attn over the decoded cache, and it matches the oracle; ragged selections (fewer
+    than k rows, an empty one) and windows clipped at the cache start."""
+    H, d, E, k, W, L = 64, 512, 1500, 512, 128, 400
+    nsel = [512, 300, 0, 511] if T > 1 else None
+    q, kv, kl, sink, idx = _attn_inputs(830 + T, B, T, H, d, E, k, L, BF16, nsel)
+    kv = kv * 8.0
+    c = cfg_obj(B=B)
+    if fmt == "fp8":
+        packed = torch.empty(B, E, d + 64, dtype=torch.uint8, device=DEV)
+        csa.kv_pack_fp8(c, kv, packed)
+        dec = torch.from_numpy(O.kv_fp8_decode(packed.cpu().numpy())).to(DEV).to(BF16)
+        fn = csa.sparse_attn_fp8kv
+    else:
+        packed = torch.empty(B, E, d // 2 + d // 16, dtype=torch.uint8, device=DEV)
+        csa.kv_pack_mxfp4(c, kv, packed)
+        dec = torch.from_numpy(O.mxfp4_decode(packed.cpu().numpy())).to(DEV).to(BF16)
+        fn = csa.sparse_attn_mxfp4kv
+    local_base = torch.tensor([0, 60][:B], dtype=torch.int64, device=DEV)
+    q_pos = (torch.arange(T, dtype=torch.int64, device=DEV)[None, :] + torch.tensor([20, 200][:B], device=DEV)[:, None])
+    q_pos = q_pos.reshape(-1).contiguous()
     out = torch.empty(B, T, H, d, device=DEV, dtype=BF16)
-    with pytest.raises(csa.CsaError) as e:
-        csa.sparse_attn_fp8kv(cfg_obj(B=B), q, packed, idx, kl, torch.zeros(B, dtype=torch.int64, device=DEV),
-                              torch.arange(T, dtype=torch.int64, device=DEV), sink, out)
-    assert e.value.status == 2
+    lse = torch.empty(B, T, H, device=DEV)
+    fn(c, q, packed, idx, kl, local_base, q_pos, sink, out, lse)
+    assert csa.get_last_error() == 0
+    out_b = torch.empty_like(out)
+    lse_b = torch.empty_like(lse)
+    csa.sparse_attn(c, q, dec, idx, kl, local_base, q_pos, sink, out_b, lse_b)
+    assert torch.equal(out, out_b) and torch.equal(lse, lse_b)
+    ro, rl = _attn_ref(q, dec, idx, kl, local_base, q_pos, sink, W, d ** -0.5)
+    assert_rows_close(np64(out), ro, 2e-2)
+    np.testing.assert_allclose(np64(lse), rl, atol=5e-3, rtol=0)
 
 
 @pytest.mark.parametrize("act,dim", [(BF16, 512), (torch.float32, 512), (BF16, 128)])
