@@ -959,8 +959,9 @@ csa_status csa_hca_decode_step(const csa_config* cfg, const csa_hca_decode_args*
   c.E_cap = d->E_cap;
   cudaError_t e = launch_compress1(c, s);
   if (e != cudaSuccess) return launch_status(e);
-  const AttnArgs a = dense_args(cfg, d->q, 1, d->kv_comp, d->E_cap, d->kv_local, d->L, d->local_base, d->q_pos,
-                                d->sink, d->out, d->lse, ws, ws_bytes);
+  AttnArgs a = dense_args(cfg, d->q, 1, d->kv_comp, d->E_cap, d->kv_local, d->L, d->local_base, d->q_pos,
+                          d->sink, d->out, d->lse, ws, ws_bytes);
+  a.dense_step = 1;
   return launch_status(launch_attn(a, s));
 }
 

@@ -218,6 +218,8 @@ struct AttnArgs {
   float softmax_scale;
   int act;
   int dense_m;            // > 0: no idx; the entries are every s < min(floor((t+1)/dense_m), E_cap)
+  int dense_step;         // dense decode step: the kernel before is the step's compressor (it
+                          // writes only entry floor((t+1)/dense_m) - 1, after its own wait)
   void* ws;
   size_t ws_bytes;
   int* err;

@@ -1384,8 +1384,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
 //  softmax: the exact per-head maximum over the split, then P^T = 2^(S - max) in bf16, one
 //          128-row tile at a time in two buffers, and the per-head sums;
 //  pass 2: the same tiles again (L2-resident by then): O^T += R^T P^T (M = 128 dims a chunk,
-//          N = 64 heads, K = 128 rows); rows past the split's end are zeroed in the slot first
-//          (they may hold anything, and 0 x NaN is NaN).
+//          N = 64 heads, K = 128 rows); rows past the split's end (only in its last tile, the
+//          one still resident from pass 1 and read first) are zeroed by the softmax warps
+//          beside their P^T rows (they may hold anything, and 0 x NaN is NaN).
 // Warps 0-7: softmax and epilogue (warp w: TMEM lanes 32 (w & 3) .. +31, heads 32 (w >> 2) ..
 // +31; a lane is a row, then a dim); warp 8: TMA producer and TMEM owner; warp 9: MMA issuer.
 // The partials (max, sum, unnormalised O) are merged with the sink by attn_merge_wide_kernel.
@@ -1459,12 +1460,16 @@ __global__ void __launch_bounds__(kHdThreads, 1)
     tmem_alloc(sTmem, 512);
     tmem_relinquish();
   }
-  pdl_wait();  // the entry the step compresses comes from the kernel before this one
+  // Decode step (a.dense_step): the kernel before this one is the step's compressor, which
+  // triggers only after its own wait, so every row but the entry it writes this step is
+  // already visible; only the split holding that entry waits, before its last tile.
+  if (!a.dense_step) pdl_wait();
   pdl_trigger();
   const int64_t t = a.q_pos[r];
   int n;          // rows of this split
   int64_t row0;   // their first row in the tensor map
   const CUtensorMap* map;
+  bool wait_last = false;  // the last tile holds the entry written this step
   if (split < hp.n_es) {
     int64_t nv = t >= 0 ? (t + 1) / a.dense_m : 0;
     nv = nv < a.E_cap ? nv : a.E_cap;
@@ -1473,6 +1478,7 @@ __global__ void __launch_bounds__(kHdThreads, 1)
     n = cnt <= 0 ? 0 : (cnt < hp.rps ? static_cast<int>(cnt) : hp.rps);
     row0 = static_cast<int64_t>(b) * a.E_cap + lo;
     map = &kvmap;
+    wait_last = a.dense_step && n > 0 && (t + 1) % a.dense_m == 0 && (t + 1) / a.dense_m - 1 == lo + n - 1;
   } else {
     const int64_t lbase = a.local_base[b];
     int64_t p_lo;
@@ -1500,6 +1506,7 @@ __global__ void __launch_bounds__(kHdThreads, 1)
         const int slot = j & 7, use = j >> 3, tile = use < nt ? use : 2 * nt - 2 - use;
         if (use > 0) ok = mbar_wait(&empty[slot], (use - 1) & 1, a.err, sAbort);
         if (!ok) break;
+        if (wait_last && j == 8 * (nt - 1)) pdl_wait();
         mbar_arrive_expect_tx(&full[slot], LY::kSlot);
         const int y = static_cast<int>(row0 + static_cast<int64_t>(tile) * kRows);
         if (use < nt)
@@ -1509,7 +1516,7 @@ __global__ void __launch_bounds__(kHdThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ---- MMA issuer (lane 0 issues; the whole warp zeroes the tail rows of pass 2)
+    // ---- MMA issuer (lane 0 issues)
     if (nt > 0) {
       bool ok = __all_sync(0xffffffffu, mbar_wait(qfull, 0, a.err, sAbort));
       const uint32_t ring = smem_u32(sRing), qb = smem_u32(sQ), pb = smem_u32(sP);
@@ -1533,24 +1540,13 @@ __global__ void __launch_bounds__(kHdThreads, 1)
       if (ok && lane == 0) mma_commit(sdone);
       // pass 2, tiles nt-1 .. 0: the k-th is in P^T buffer k & 1 and (k > 0) in use nt-1+k
       for (int k = 0; ok && k < nt; ++k) {
-        const int i = nt - 1 - k, use = nt - 1 + k;
+        const int use = nt - 1 + k;
         ok = __all_sync(0xffffffffu, mbar_wait(&pfull[k & 1], (k >> 1) & 1, a.err, sAbort));
-        const int vr = n - i * kRows;  // valid rows of this tile (> 0)
         for (int cc = 0; ok && cc < 4; ++cc) {
           if (k > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&full[2 * cc], use & 1, a.err, sAbort) &&
                                              mbar_wait(&full[2 * cc + 1], use & 1, a.err, sAbort));
           if (!ok) break;
-          if (vr < kRows) {  // zero rows vr..127 of both regions (whole 128-byte rows); the S
-                             // products that read them completed before the softmax began
-            for (int q = lane; q < 2 * (kRows - vr) * 8; q += 32) {
-              const int reg = q / ((kRows - vr) * 8), rem = q % ((kRows - vr) * 8);
-              *reinterpret_cast<uint4*>(sRing + (2 * cc + reg) * LY::kSlot + (vr + rem / 8) * 128 + (rem % 8) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
           tc_fence_after();
           if (lane == 0) {
 #pragma unroll
@@ -1606,6 +1602,16 @@ __global__ void __launch_bounds__(kHdThreads, 1)
         const bool valid = i * kRows + row < n;
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = valid ? ex2_approx(fmaf(x[e], scale_log2, -mh[e])) : 0.f;
+        if (!valid) {  // only in the resident last tile (k = 0): zero the row in the ring, as
+                       // pass 2 multiplies it by P = 0 and 0 x NaN is NaN; the S products that
+                       // read it completed before the softmax began
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(sRing + ((hb >> 5) * 4 + g) * LY::kSlot + row * 128 + c * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+        }
         uint8_t* prow = sP + buf * (kRows * 128);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -1646,6 +1652,7 @@ __global__ void __launch_bounds__(kHdThreads, 1)
       ml[kH + tid] = 0.f;
     }
   }
+  if (a.dense_step) pdl_wait();  // complete only after the compressor: keeps the stream order
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
@@ -1655,26 +1662,32 @@ __global__ void __launch_bounds__(kHdThreads, 1)
 }
 
 // Merge of many split partials ([query][split][head][dim]) with the sink: one CTA per
-// (query, head), thread t owns dims 4t .. 4t+3.  Thread x < n_split reads split x's (m, l);
-// block reductions give M = max(m_x, sink) and den = sum_x l_x 2^(m_x - M) + 2^(sink - M);
-// the partials are then read 8 splits at a time (one float4 each, every load of a batch
-// issued before the first use) and summed in split order.
+// (query, head), thread t owns dims 4t .. 4t+3.  Thread 0 stages the n_split partial rows of
+// the head (2 KiB each, contiguous) into shared memory with bulk copies on one mbarrier, all
+// in flight at once; meanwhile thread x < n_split reads split x's (m, l) and block reductions
+// give M = max(m_x, sink) and den = sum_x l_x 2^(m_x - M) + 2^(sink - M); the staged rows are
+// then summed in split order.
 constexpr int kMaxSplitDec = 64;  // split partials a query may have
 constexpr int kMwThreads = 128;
 __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnArgs a, const TcAttnSplit sp) {
+  extern __shared__ __align__(16) float s_po[];  // [n_split][kD]
   __shared__ float s_f[kMaxSplitDec];
   __shared__ float s_red[kMwThreads / 32];
-  pdl_wait();
-  pdl_trigger();
+  __shared__ uint64_t s_bar;
   const int64_t r = blockIdx.x;
   const int h = blockIdx.y;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int ns = sp.n_split;
-  const float* po = sp.part_o + (r * ns * kH + h) * kD + 4 * t;
-  float4 v[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    if (u < ns) v[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(u) * kH * kD));
+  if (t == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (t == 0) {
+    mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(ns) * kD * 4);
+    for (int x = 0; x < ns; ++x) bulk_g2s(s_po + x * kD, sp.part_o + ((r * ns + x) * kH + h) * kD, kD * 4, &s_bar);
+  }
   float m = -INFINITY, l = 0.f;
   if (t < ns) {
     m = __ldcg(sp.part_ml + (r * ns + t) * 2 * kH + h);
@@ -1685,7 +1698,7 @@ __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnA
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (lane == 0) s_red[warp] = M;
-  __syncthreads();
+  __syncthreads();  // (also publishes the barrier's initialisation)
   M = sk;
 #pragma unroll
   for (int w = 0; w < kMwThreads / 32; ++w) M = fmaxf(M, s_red[w]);
@@ -1701,22 +1714,16 @@ __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnA
 #pragma unroll
   for (int w = 0; w < kMwThreads / 32; ++w) den += s_red[w];
   if (t == 0 && a.lse) a.lse[r * kH + h] = (M + log2f(den)) * kLn2;
+  mbar_wait(&s_bar, 0, a.err, nullptr);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int x0 = 0; x0 < ns; x0 += 8) {
-    if (x0 > 0) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (x0 + u < ns) v[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(x0 + u) * kH * kD));
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float fx = x0 + u < ns ? s_f[x0 + u] : 0.f;
-      if (fx != 0.f) {  // splits without rows wrote no partial
-        acc.x = fmaf(v[u].x, fx, acc.x);
-        acc.y = fmaf(v[u].y, fx, acc.y);
-        acc.z = fmaf(v[u].z, fx, acc.z);
-        acc.w = fmaf(v[u].w, fx, acc.w);
-      }
+  for (int x = 0; x < ns; ++x) {
+    const float fx = s_f[x];
+    if (fx != 0.f) {  // splits without rows wrote no partial
+      const float4 v = *reinterpret_cast<const float4*>(s_po + x * kD + 4 * t);
+      acc.x = fmaf(v.x, fx, acc.x);
+      acc.y = fmaf(v.y, fx, acc.y);
+      acc.z = fmaf(v.z, fx, acc.z);
+      acc.w = fmaf(v.w, fx, acc.w);
     }
   }
   const float inv = 1.f / den;
@@ -1726,6 +1733,17 @@ __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnA
   pk.x = *reinterpret_cast<uint32_t*>(&lo);
   pk.y = *reinterpret_cast<uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (r * kH + h) * kD + 4 * t) = pk;
+}
+
+// The merge of sp.n_split (<= kMaxSplitDec) partials a query.
+cudaError_t launch_merge_wide(const AttnArgs& a, const TcAttnSplit& sp, int64_t rows, cudaStream_t s) {
+  static std::atomic<unsigned long long> mattr{0};
+  if (first_use_in_context(mattr))
+    cudaFuncSetAttribute(attn_merge_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSplitDec * kD * 4);
+  const cudaError_t e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads),
+                                   static_cast<size_t>(sp.n_split) * kD * 4, s, a, sp);
+  count_launches(1);
+  return e;
 }
 
 bool attn_uses_tensor_cores(int act, int H, int d, int k) {
@@ -1776,7 +1794,9 @@ bool dense_uses_tensor_cores(int act, int H, int d) { return act == CSA_BF16 && 
 
 // attn_hca_dec_kernel's plan for few queries: about num_sms / rows CTAs a query (one of them
 // for the window), entry splits of a multiple of 128 rows, at most kHdTiles tiles and
-// kMaxSplitDec splits; n_split = 0 when the entries do not fit that.
+// kMaxSplitDec splits; n_split = 0 when the entries do not fit that.  (Splits of any multiple
+// of 16 rows that fill every SM measured slower: their partial last tiles cost more in pass 2
+// than the extra CTAs gain.)
 HdPlan plan_hca_dec(int64_t rows, int64_t E_cap, int W, int num_sms) {
   HdPlan p{};
   if (rows >= num_sms) return p;
@@ -1851,9 +1871,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
       sp.rows_per_split = hp.rps;
       sp.part_o = hp.part_o;
       sp.part_ml = hp.part_ml;
-      e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
-      count_launches(1);
-      return e;
+      return launch_merge_wide(a, sp, rows, s);
     }
     TcAttnSplit sp = plan_dense(rows, a.E_cap + a.W, a.num_sms);
     if (sp.n_split > 1) {
@@ -1870,9 +1888,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
                                PfLayout::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess || sp.n_split == 1) return e;
-    e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
-    count_launches(1);
-    return e;
+    return launch_merge_wide(a, sp, rows, s);
   }
   if (attn_uses_tensor_cores(a.act, a.H, a.d, a.k)) {
     TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
@@ -1926,9 +1942,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
                   : launch_pdl(attn_dec_kernel<64, 0>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
     count_launches(1);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
-    count_launches(1);
-    return e;
+    return launch_merge_wide(a, sp, rows, s);
   }
   const size_t smem = (static_cast<size_t>(a.H) * a.d * 2 + kSimtTile * (a.d + 1) + a.H * kSimtTile + 3 * a.H + 32) * 4 +
                       static_cast<size_t>(a.k) * 4;
@@ -2000,9 +2014,7 @@ cudaError_t launch_attn_quantkv(const AttnArgs& a, cudaStream_t s) {
                 : launch_pdl(attn_dec_kernel<64, KVF>, grid, dim3(kTcThreads), DecLayout<64>::kSmem, s, a, sp);
   count_launches(1);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(attn_merge_wide_kernel, dim3(static_cast<unsigned>(rows), kH), dim3(kMwThreads), 0, s, a, sp);
-  count_launches(1);
-  return e;
+  return launch_merge_wide(a, sp, rows, s);
 }
 
 cudaError_t launch_attn_fp8kv(const AttnArgs& a, cudaStream_t s) { return launch_attn_quantkv<1>(a, s); }

@@ -136,13 +136,6 @@ __device__ __forceinline__ bool wait_time_only(uint64_t* bar, uint32_t parity) {
 }
 
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
 // sum_j w[j] * relu(v[j]) over 32 values (w in shared memory, read as float4), four chains
 __device__ __forceinline__ float relu_dot32(const float (&v)[32], const float* w) {
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
