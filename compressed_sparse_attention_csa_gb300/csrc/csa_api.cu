@@ -1040,9 +1040,14 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   ia.wait_ns = g_debug_wait_ns.load(std::memory_order_relaxed);
   ia.skip_key_loads = g_debug_skip_loads.load(std::memory_order_relaxed) != 0;
   cudaError_t e;
+  // the attention on the decode split plan waits for each query's list through the step
+  // counters after the histograms and tickets, not for the whole selection kernel
+  uint32_t* sel_done = hist_cnt + static_cast<size_t>(cfg->B) * 4160 + cfg->B;
+  bool handoff = false;
   if (indexer_uses_tensor_cores(ia) && cfg->m <= 8) {
     // 1-2. one launch: compression of the completed block (both caches), the query images,
     //      the scores and their histogram; 3. the top-k from that histogram
+    handoff = attn_fp8kv_supported(cfg->B, 1, cfg->H, cfg->d, cfg->k, cfg->W, cfg->act, sms);
     DecodeFuse& f = ia.fuse;
     f.on = true;
     f.kv_tail = d->kv_tail;
@@ -1059,8 +1064,15 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
     ia.images_ready = true;
     e = launch_indexer(ia, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
+    SelHandoff ho{};
+    if (handoff) {
+      ho.done = sel_done;
+      ho.pf_rows = static_cast<const uint8_t*>(d->kv_comp);
+      ho.pf_row_bytes = kv_fmt == 1 ? 576 : kv_fmt == 2 ? 288 : static_cast<int64_t>(cfg->d) * 2;
+      ho.pf_seq_rows = d->E_cap;
+    }
     e = launch_topk_hist(scores, d->E_cap, cfg->B, d->E_cap, nv, hist_cnt, cfg->k, idx, ws_topk, sms, s, nullptr,
-                         ia.scores_bf16);
+                         ia.scores_bf16, ho);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   } else {
     if (qkv) return CSA_ERR_SHAPE;  // quantised entries: the fused path only
@@ -1121,6 +1133,10 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   aa.ws = ws_attn;
   aa.err = err;
   aa.num_sms = sms;
+  if (handoff) {
+    aa.sel_done = sel_done;
+    aa.sel_seen = sel_done + cfg->B;
+  }
   return launch_status(kv_fmt == 2 ? launch_attn_mxfp4kv(aa, s) : kv_fmt == 1 ? launch_attn_fp8kv(aa, s) : launch_attn(aa, s));
 }
 }  // namespace

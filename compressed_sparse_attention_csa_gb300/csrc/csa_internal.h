@@ -90,9 +90,11 @@ struct DecodeFuse {
                          // codes, then 64 bf16 dims); 2 MXFP4 entries (d/2 E2M1 bytes, d/16 e4m3 scales)
   uint32_t* hist;        // histograms
 };
-// decode-step state kept across steps: the histograms [B][4160] and the top-k tickets [B]; zero
-// before the first step, left zero by every step
-inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + B; }
+// decode-step state kept across steps: the histograms [B][4160], the top-k tickets [B] (zero
+// before the first step, left zero by every step), then two step counters [B] each: selections
+// completed (the selection's last CTA of a row adds one) and selections consumed (the split
+// merge copies the first after the step's attention); zero before the first step, left equal
+inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + 3 * static_cast<size_t>(B); }
 struct IndexerArgs {
   const void* qI;        // [B*T, HI, dI]
   const float* w;        // [B*T, HI]
@@ -183,9 +185,16 @@ cudaError_t launch_topk_rows(const void* scores, int64_t ld, int64_t rows, int64
 size_t topk_hist_standalone_bytes(int64_t rows, int64_t n_cols);
 cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
 // hist_cnt: [rows][4160] then rows tickets; left zero for the next use.
+// Decode-step extras of the histogram selection (all null / zero: none).
+struct SelHandoff {
+  uint32_t* done;            // [rows] counters the row's last CTA increments once its list is written
+  const uint8_t* pf_rows;    // cache rows the list indexes: every candidate's row (row r's entry s at
+  int64_t pf_row_bytes;      // pf_rows + (r * pf_seq_rows + s) * pf_row_bytes, a multiple of 16
+  int64_t pf_seq_rows;       // bytes) is prefetched into L2 as soon as its chunk keeps it
+};
 cudaError_t launch_topk_hist(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s,
-                             const int32_t* cmap = nullptr, bool bf16 = false);
+                             const int32_t* cmap = nullptr, bool bf16 = false, const SelHandoff& ho = SelHandoff{});
 
 struct PoolArgs {
   const float* scores;
@@ -220,6 +229,10 @@ struct AttnArgs {
   int dense_m;            // > 0: no idx; the entries are every s < min(floor((t+1)/dense_m), E_cap)
   int dense_step;         // dense decode step: the kernel before is the step's compressor (it
                           // writes only entry floor((t+1)/dense_m) - 1, after its own wait)
+  uint32_t* sel_done;     // sparse decode step (or null): [B] selections completed, counted by the
+  uint32_t* sel_seen;     // selection kernel before this one; [B] selections consumed (the merge
+                          // sets it to sel_done): query r's list is ready once sel_done[r] passes
+                          // sel_seen[r], and holds its entries first (ascending), then -1
   void* ws;
   size_t ws_bytes;
   int* err;

@@ -94,6 +94,25 @@ __device__ __forceinline__ bool mbar_wait_b(uint64_t* bar, uint32_t parity, int*
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
   return mbar_wait_b(bar, parity, err, abort, kWaitBudgetNs);
 }
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until the counter *ctr (incremented by other CTAs, possibly of an earlier
+// kernel still running) reaches want (modulo 2^32).  Returns false (and records a timeout)
+// when the budget runs out.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t want, int* err) {
+  if (static_cast<int32_t>(ld_acquire_u32(ctr) - want) >= 0) return true;
+  const uint64_t t0 = global_ns();
+  while (static_cast<int32_t>(ld_acquire_u32(ctr) - want) < 0) {
+    if (global_ns() - t0 > kWaitBudgetNs) {
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
 
 // Barrier over the first nthreads threads that reach named barrier `id` (whole warps).
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -162,6 +181,10 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       "[%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
+}
+// bulk prefetch of global memory into L2 (address 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 // untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16)
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

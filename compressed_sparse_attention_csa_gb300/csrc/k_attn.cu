@@ -1106,21 +1106,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
       if (lp < w_hi) cp_async16(sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7), kvl + (p_lo + lp - lbase) * kD + c * 8);
     }
   }
-  pdl_wait();  // the selection (and the entry compressed this step) come from earlier kernels
-  pdl_trigger();
-  const int n_sel = compact_idx<kTcThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
-  const int n_rows = n_win + n_sel;
-  const int row_hi = min(n_rows, row_cap);
+  int row_hi;
+  if (a.sel_done) {
+    // decode step: wait for this query's list only (counted done by the selection's last CTA
+    // of the row once written), not for the whole selection kernel; the list holds its entries
+    // first, so this split reads just its own slice, and its valid rows are a prefix
+    if (tid == 0) wait_count(a.sel_done + r, __ldcg(a.sel_seen + r) + 1u, a.err);
+    __syncthreads();
+    pdl_trigger();
+    bool valid = false;
+    if (tid < kRows) {
+      const int lp = row_lo + tid, e = lp - n_win;
+      valid = lp < n_win;
+      if (e >= 0 && e < a.k) {
+        int32_t v = __ldcg(a.idx + r * a.k + e);
+        if (v >= a.E_cap) {
+          set_error(a.err, kErrIndex);
+          v = -1;
+        }
+        sel[e] = v;
+        valid = v >= 0;
+      }
+    }
+    row_hi = row_lo + __syncthreads_count(valid);
+  } else {
+    pdl_wait();  // the selection (and the entry compressed this step) come from earlier kernels
+    pdl_trigger();
+    const int n_sel = compact_idx<kTcThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
+    row_hi = min(n_win + n_sel, row_cap);
+  }
   const int nr = row_hi - row_lo;  // rows of this split (<= 0: none)
   if constexpr (KVF == 0) {
-    for (int i = tid; i < kRows * 64; i += kTcThreads) {
-      const int j = i >> 6, c = i & 63;
+    // thread = one 16-byte column c of rows j0, j0 + 4, ...: a warp moves 512 contiguous bytes
+    // of a row, and the copy's addresses cost an add and a multiply-add
+    static_assert(kTcThreads == 256, "four rows a pass");
+    const int c = tid & 63, j0 = tid >> 6;
+    uint8_t* dcol = sR + (c >> 3) * (kRows * 128);
+    const __nv_bfloat16* scol = kvc + c * 8;
+#pragma unroll 8
+    for (int j = j0; j < kRows; j += 4) {
       const int lp = row_lo + j;
-      uint8_t* dst = sR + (c >> 3) * (kRows * 128) + sw128(j, c & 7);
+      uint8_t* dst = dcol + sw128(j, c & 7);
       if (lp >= row_hi) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       } else if (lp >= n_win) {
-        cp_async16(dst, kvc + static_cast<int64_t>(sel[lp - n_win]) * kD + c * 8);
+        cp_async16(dst, scol + static_cast<int64_t>(sel[lp - n_win]) * kD);
       }
     }
   } else if constexpr (KVF == 1) {
@@ -1260,42 +1290,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
       }
       mma_commit(&bars[0]);
     }
-    float x[NH];
-    if (warp < 4) {
+    // softmax on all 8 warps: warp w takes TMEM lanes 32 (w & 3) .. +31 (a lane is a row) and
+    // heads HH (w >> 2) .. +HH-1 of the CTA's NH
+    constexpr int HH = NH / 2;
+    const int hh0 = (warp >> 2) * HH;
+    float x[HH];
+    {
       mbar_wait(&bars[0], 0, a.err, nullptr);
       tc_fence_after();
-      const bool valid = (warp * 32 + lane) < nr;
+      const bool valid = ((warp & 3) * 32 + lane) < nr;
+      float v[32];
+      tmem_ld32(tS + qbase + hh0, v);  // (columns past NH are read and ignored)
+      tmem_wait_ld(v);
 #pragma unroll
-      for (int hc = 0; hc < NH; hc += 32) {
-        float v[32];
-        tmem_ld32(tS + qbase + hc, v);
-        tmem_wait_ld(v);
+      for (int e = 0; e < HH; ++e) x[e] = valid ? v[e] * scale_log2 : -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (hc + e < NH) x[hc + e] = valid ? v[e] * scale_log2 : -INFINITY;
-      }
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
+      for (int h = 0; h < HH; ++h) {
         float mx = x[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) s_red[warp * NH + h] = mx;
+        if (lane == 0) s_red[warp * HH + h] = mx;  // [head half][quadrant][HH]
       }
     }
     __syncthreads();
-    if (tid < NH)
-      s_m[tid] = fmaxf(fmaxf(s_red[tid], s_red[NH + tid]), fmaxf(s_red[2 * NH + tid], s_red[3 * NH + tid]));
-    __syncthreads();
-    if (warp < 4) {
-      const int j = warp * 32 + lane;
-      float p[NH];
+    {
+      const int j = (warp & 3) * 32 + lane;
+      const float* rm = s_red + (warp >> 2) * 4 * HH;
+      float p[HH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float mu = s_m[h];
+      for (int h = 0; h < HH; ++h) {
+        const float mu = fmaxf(fmaxf(rm[h], rm[HH + h]), fmaxf(rm[2 * HH + h], rm[3 * HH + h]));
         p[h] = (mu == -INFINITY) ? 0.f : exp2f(x[h] - mu);
       }
 #pragma unroll
-      for (int c = 0; c < NH / 8; ++c) {
+      for (int c = 0; c < HH / 8; ++c) {
         uint4 pk;
         uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
 #pragma unroll
@@ -1303,20 +1331,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
           __nv_bfloat162 two = __floats2bfloat162_rn(p[c * 8 + 2 * e], p[c * 8 + 2 * e + 1]);
           w[e] = *reinterpret_cast<uint32_t*>(&two);
         }
-        *reinterpret_cast<uint4*>(sP + sw128(j, c)) = pk;
+        *reinterpret_cast<uint4*>(sP + sw128(j, hh0 / 8 + c)) = pk;
       }
+      float sm[HH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        float sm = p[h];
+      for (int h = 0; h < HH; ++h) {
+        sm[h] = p[h];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-        if (lane == 0) s_red[warp * NH + h] = sm;
+        for (int o = 16; o > 0; o >>= 1) sm[h] += __shfl_xor_sync(0xffffffffu, sm[h], o);
+      }
+      // (every thread has read s_red's maxima before the sums overwrite the other half)
+      if (tid < NH) {
+        const float* qm = s_red + (tid / HH) * 4 * HH + tid % HH;
+        s_m[tid] = fmaxf(fmaxf(qm[0], qm[HH]), fmaxf(qm[2 * HH], qm[3 * HH]));
+      }
+      __syncthreads();
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < HH; ++h) s_red[warp * HH + h] = sm[h];
       }
       tc_fence_before();
       fence_proxy_async_smem();
     }
     __syncthreads();
-    if (tid < NH) s_l[tid] = (s_red[tid] + s_red[NH + tid]) + (s_red[2 * NH + tid] + s_red[3 * NH + tid]);
+    if (tid < NH) {
+      const float* ql = s_red + (tid / HH) * 4 * HH + tid % HH;
+      s_l[tid] = (ql[0] + ql[HH]) + (ql[2 * HH] + ql[3 * HH]);
+    }
     // ---- O^T = R^T P^T  (M = 128 dims per chunk, N = 64 head columns, K = 128 rows)
     if (warp == 4 && lane == 0) {
       tc_fence_after();
@@ -1365,6 +1406,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
         if (hc + e < NH) o[(hc + e) * kD] = v[e];
     }
   }
+  if (a.sel_done) pdl_wait();  // complete only after the selection: keeps the stream order
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {
@@ -1684,6 +1726,7 @@ __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnA
   }
   pdl_wait();
   pdl_trigger();
+  if (a.sel_seen && h == 0 && t == 0) a.sel_seen[r] = __ldcg(a.sel_done + r);  // this step's list consumed
   if (t == 0) {
     mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(ns) * kD * 4);
     for (int x = 0; x < ns; ++x) bulk_g2s(s_po + x * kD, sp.part_o + ((r * ns + x) * kH + h) * kD, kD * 4, &s_bar);

@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(NT) topk_hist_build_kernel(const void* scores_
 // scores has digit >= b1), keeps the (key, position) of every score of its chunk with digit
 // >= b1, compacted in position order, in its own slot of the workspace, and takes a ticket.
 // The CTA that takes a row's last ticket reads the slots back in chunk order (so the row's
-// candidates are in position order), finds the exact k-th key among the b1 bin by radix
+// candidates are in position order; with at most 64 chunks the counts and each chunk's first
+// 4 NT / n_chunks candidates come in one round trip), finds the exact k-th key among the b1 bin by radix
 // passes on its low 20 bits, and writes the winners (every key above it, then the lowest
 // positions among keys equal to it) with one stable compaction: the output is already
 // ascending.  If the candidates exceed kAllCap (a bin full of ties) it selects over the whole
@@ -209,7 +210,8 @@ size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(
 template <bool B16>
 __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v, int64_t ld, const int32_t* n_valid,
                                                          int64_t n_cols, uint32_t* hist, int k, int32_t* idx,
-                                                         uint32_t* cand, int n_chunks, const int32_t* cmap) {
+                                                         uint32_t* cand, int n_chunks, const int32_t* cmap,
+                                                         const SelHandoff ho) {
   using K = ScoreKey<B16>;
   const typename K::T* scores = static_cast<const typename K::T*>(scores_v);
   extern __shared__ __align__(16) uint8_t sel_raw[];
@@ -260,6 +262,11 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
         spos[off] = static_cast<uint32_t>(c0 + tid * kSelPer + u);
       }
       ++off;
+      // decode step: the candidate's cache row starts towards L2 while the row's last CTA
+      // selects (the attention gathers the winners right after)
+      if (ho.pf_rows)
+        bulk_prefetch_l2(ho.pf_rows + (row * ho.pf_seq_rows + c0 + tid * kSelPer + u) * ho.pf_row_bytes,
+                         static_cast<uint32_t>(ho.pf_row_bytes));
     }
   }
   if (tid == 0) slot[0] = n_mine;
@@ -279,34 +286,59 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
 
   // ---- the row's last CTA: the chunks' candidate counts and their prefix (one block scan)
   const uint32_t* base = cand + static_cast<size_t>(row) * n_chunks * kSlotWords;
-  uint32_t my_n = 0;
-  bool my_over = false;
-  const int cpt = (n_chunks + NT - 1) / NT;  // chunks per thread (contiguous)
-  uint32_t cc[kMaxChunkPer];
-#pragma unroll
-  for (int q = 0; q < kMaxChunkPer; ++q) {
-    const int ch = tid * cpt + q;
-    cc[q] = (q < cpt && ch < n_chunks) ? __ldcg(base + static_cast<size_t>(ch) * kSlotWords) : 0u;
-    my_n += cc[q];
-    my_over |= cc[q] > static_cast<uint32_t>(kSlotCap);
-  }
   if (tid == 0) {
     S.n_gt = 0u;
     S.n_eq = 0u;
   }
   uint32_t n_all_u;
-  uint32_t run = block_exclusive_scan<NT>(my_n, S.tmp, &n_all_u);
-  const bool any_over = __syncthreads_or(my_over) != 0;
+  bool any_over;
+  // at most NT / 4 chunks (tpc >= 4 threads a chunk): each chunk's count and its first
+  // 4 tpc candidates come in one round trip (loads past a chunk's count read unused entries of
+  // its slot and are dropped)
+  int tpc = 1;
+  while (tpc * 2 * n_chunks <= NT) tpc *= 2;
+  const bool fused = tpc >= 4;
+  const int fch = tid / tpc, fq = tid % tpc;
+  uint32_t fk[4], fp[4], fcn = 0, fpre = 0;
+  if (fused) {
+    if (fch < n_chunks) {
+      const uint32_t* sl = base + static_cast<size_t>(fch) * kSlotWords;
+      fcn = __ldcg(sl);
 #pragma unroll
-  for (int q = 0; q < kMaxChunkPer; ++q) {
-    const int ch = tid * cpt + q;
-    if (q < cpt && ch < n_chunks) {
-      S.cpre[ch] = run;
-      S.ccnt[ch] = cc[q];
+      for (int u = 0; u < 4; ++u) {
+        fk[u] = __ldcg(sl + 4 + fq + tpc * u);
+        fp[u] = __ldcg(sl + 4 + kSlotCap + fq + tpc * u);
+      }
     }
-    run += cc[q];
+    const uint32_t run = block_exclusive_scan<NT>(fq == 0 ? fcn : 0u, S.tmp, &n_all_u);
+    if (fq == 0 && fch < n_chunks) S.cpre[fch] = run;
+    any_over = __syncthreads_or(fcn > static_cast<uint32_t>(kSlotCap)) != 0;
+    if (fch < n_chunks) fpre = S.cpre[fch];
+  } else {
+    uint32_t my_n = 0;
+    bool my_over = false;
+    const int cpt = (n_chunks + NT - 1) / NT;  // chunks per thread (contiguous)
+    uint32_t cc[kMaxChunkPer];
+#pragma unroll
+    for (int q = 0; q < kMaxChunkPer; ++q) {
+      const int ch = tid * cpt + q;
+      cc[q] = (q < cpt && ch < n_chunks) ? __ldcg(base + static_cast<size_t>(ch) * kSlotWords) : 0u;
+      my_n += cc[q];
+      my_over |= cc[q] > static_cast<uint32_t>(kSlotCap);
+    }
+    uint32_t run = block_exclusive_scan<NT>(my_n, S.tmp, &n_all_u);
+    any_over = __syncthreads_or(my_over) != 0;
+#pragma unroll
+    for (int q = 0; q < kMaxChunkPer; ++q) {
+      const int ch = tid * cpt + q;
+      if (q < cpt && ch < n_chunks) {
+        S.cpre[ch] = run;
+        S.ccnt[ch] = cc[q];
+      }
+      run += cc[q];
+    }
+    __syncthreads();
   }
-  __syncthreads();
   const int n_all = static_cast<int>(n_all_u);
   int32_t* orow = idx + row * k;
   // with a candidate map (ascending positions) the winners' slots are written as positions
@@ -314,17 +346,36 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
   if (n_all <= kAllCap && !any_over) {
     // the candidates, chunk by chunk in position order: tpc threads a chunk, so every load is in
     // flight at once; the keys above the threshold digit are counted on the way
-    int tpc = 1;
-    while (tpc * 2 * n_chunks <= NT) tpc *= 2;
     uint32_t gt = 0;
-    for (int ch = tid / tpc; ch < n_chunks; ch += NT / tpc) {
-      const uint32_t* sl = base + static_cast<size_t>(ch) * kSlotWords;
-      const uint32_t c0 = S.cpre[ch], cn = S.ccnt[ch];
-      for (uint32_t j = static_cast<uint32_t>(tid % tpc); j < cn; j += static_cast<uint32_t>(tpc)) {
-        const uint32_t key = __ldcg(sl + 4 + j);
-        S.ak[c0 + j] = key;
-        S.ap[c0 + j] = static_cast<int32_t>(__ldcg(sl + 4 + kSlotCap + j));
-        gt += (key >> 20) > b1 ? 1u : 0u;
+    if (fused) {
+      if (fch < n_chunks) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t j = static_cast<uint32_t>(fq + tpc * u);
+          if (j < fcn) {
+            S.ak[fpre + j] = fk[u];
+            S.ap[fpre + j] = static_cast<int32_t>(fp[u]);
+            gt += (fk[u] >> 20) > b1 ? 1u : 0u;
+          }
+        }
+        const uint32_t* sl = base + static_cast<size_t>(fch) * kSlotWords;
+        for (uint32_t j = static_cast<uint32_t>(4 * tpc + fq); j < fcn; j += static_cast<uint32_t>(tpc)) {
+          const uint32_t key = __ldcg(sl + 4 + j);
+          S.ak[fpre + j] = key;
+          S.ap[fpre + j] = static_cast<int32_t>(__ldcg(sl + 4 + kSlotCap + j));
+          gt += (key >> 20) > b1 ? 1u : 0u;
+        }
+      }
+    } else {
+      for (int ch = tid / tpc; ch < n_chunks; ch += NT / tpc) {
+        const uint32_t* sl = base + static_cast<size_t>(ch) * kSlotWords;
+        const uint32_t c0 = S.cpre[ch], cn = S.ccnt[ch];
+        for (uint32_t j = static_cast<uint32_t>(tid % tpc); j < cn; j += static_cast<uint32_t>(tpc)) {
+          const uint32_t key = __ldcg(sl + 4 + j);
+          S.ak[c0 + j] = key;
+          S.ap[c0 + j] = static_cast<int32_t>(__ldcg(sl + 4 + kSlotCap + j));
+          gt += (key >> 20) > b1 ? 1u : 0u;
+        }
       }
     }
     gt = __reduce_add_sync(0xffffffffu, gt);
@@ -420,6 +471,15 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
       }
     __syncthreads();
     team_write_sorted<NT>(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow, cm, tid, 0);
+  }
+  // decode step: the row's list is complete; count it done for the attention waiting on it
+  // (the barrier orders every thread's writes before the fence)
+  if (ho.done) {
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(ho.done + row, 1u);
+    }
   }
 }
 
@@ -639,7 +699,7 @@ size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {
 
 cudaError_t launch_topk_hist(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int, cudaStream_t s,
-                             const int32_t* cmap, bool bf16) {
+                             const int32_t* cmap, bool bf16, const SelHandoff& ho) {
   static std::atomic<unsigned long long> attr{0};
   if (first_use_in_context(attr)) {
     cudaFuncSetAttribute(topk_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -651,9 +711,9 @@ cudaError_t launch_topk_hist(const void* scores, int64_t ld, int64_t rows, int64
   const dim3 grid(static_cast<unsigned>(n_chunks), static_cast<unsigned>(rows));
   const cudaError_t e =
       bf16 ? launch_pdl(topk_select_kernel<true>, grid, dim3(NT), sel_smem_bytes(k), s, scores, ld, n_valid, n_cols,
-                        hist_cnt, k, idx, static_cast<uint32_t*>(ws_cand), n_chunks, cmap)
+                        hist_cnt, k, idx, static_cast<uint32_t*>(ws_cand), n_chunks, cmap, ho)
            : launch_pdl(topk_select_kernel<false>, grid, dim3(NT), sel_smem_bytes(k), s, scores, ld, n_valid, n_cols,
-                        hist_cnt, k, idx, static_cast<uint32_t*>(ws_cand), n_chunks, cmap);
+                        hist_cnt, k, idx, static_cast<uint32_t*>(ws_cand), n_chunks, cmap, ho);
   count_launches(1);
   return e;
 }
