@@ -214,6 +214,19 @@ size_t indexer_topk_ws(const csa_config* c, int T, int64_t E_cap, int sms, bool 
          align_up(topk_workspace_bytes(rows, E_cap, c->k, sms, bf16), 256);
 }
 
+// Candidate mode of the decode step's attention (decode split plan, a window of at most 128
+// rows, at most 64 selection chunks, and a grid of 1 + kCandCap / 128 splits a query in at
+// least two head groups that still fits the SMs): a row with at most kCandCap candidates is
+// attended over its candidates, gathered before the selection's threshold is known and masked
+// by it.  (With one head group, B 16 at 64K, the wider grid cost more than the overlap gained.)
+constexpr int kCandCap = 1024;
+int decode_cand_cap(const csa_config* c, int64_t E_cap, int sms) {
+  if (!attn_fp8kv_supported(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms)) return 0;
+  if (c->W > 128 || sel_chunks(E_cap) > 64 || kCandCap > sel_slot_cap()) return 0;
+  if (static_cast<int64_t>(1 + kCandCap / 128) * c->B * 2 > sms) return 0;
+  return kCandCap;
+}
+
 size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   const int64_t B = c->B;
   // first, at a fixed offset: the top-k histograms and tickets kept across steps
@@ -223,7 +236,8 @@ size_t decode_ws(const csa_config* c, int64_t E_cap, int sms) {
   bytes += align_up(static_cast<size_t>(B) * 4, 256);                 // visible counts
   bytes += align_up(static_cast<size_t>(B) * c->k * 4, 256);          // idx
   bytes += align_up(std::max(topk_workspace_bytes(B, E_cap, c->k, sms), topk_hist_workspace_bytes(B, E_cap)), 256);
-  bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms), 256);
+  const int cap = decode_cand_cap(c, E_cap, sms);
+  bytes += align_up(attn_workspace_bytes(c->B, 1, c->H, c->d, c->k, c->W, c->act, sms, cap > 0 ? 1 + cap / 128 : 0), 256);
   return bytes;
 }
 
@@ -1043,7 +1057,11 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   // the attention on the decode split plan waits for each query's list through the step
   // counters after the histograms and tickets, not for the whole selection kernel
   uint32_t* sel_done = hist_cnt + static_cast<size_t>(cfg->B) * 4160 + cfg->B;
+  uint32_t* sel_seen = sel_done + cfg->B;
+  uint32_t* sel_chunk_ctr = sel_seen + cfg->B;
+  uint32_t* sel_thr = sel_chunk_ctr + cfg->B;  // [B][2]
   bool handoff = false;
+  int cand_cap = 0;
   if (indexer_uses_tensor_cores(ia) && cfg->m <= 8) {
     // 1-2. one launch: compression of the completed block (both caches), the query images,
     //      the scores and their histogram; 3. the top-k from that histogram
@@ -1066,7 +1084,13 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     SelHandoff ho{};
     if (handoff) {
+      cand_cap = decode_cand_cap(cfg, d->E_cap, sms);
       ho.done = sel_done;
+      if (cand_cap > 0) {
+        ho.chunks = sel_chunk_ctr;
+        ho.thr = sel_thr;
+        ho.cand_cap = cand_cap;
+      }
       ho.pf_rows = static_cast<const uint8_t*>(d->kv_comp);
       ho.pf_row_bytes = kv_fmt == 1 ? 576 : kv_fmt == 2 ? 288 : static_cast<int64_t>(cfg->d) * 2;
       ho.pf_seq_rows = d->E_cap;
@@ -1135,7 +1159,17 @@ csa_status decode_step_impl(const csa_config* cfg, const csa_decode_args* d, voi
   aa.num_sms = sms;
   if (handoff) {
     aa.sel_done = sel_done;
-    aa.sel_seen = sel_done + cfg->B;
+    aa.sel_seen = sel_seen;
+    if (cand_cap > 0) {
+      aa.cand_cap = cand_cap;
+      aa.sel_chunks = sel_chunk_ctr;
+      aa.sel_thr = sel_thr;
+      aa.sel_slots = static_cast<const uint32_t*>(ws_topk);
+      aa.sel_n_chunks = sel_chunks(d->E_cap);
+      aa.sel_slot_words = sel_slot_words();
+      aa.sel_slot_cap = sel_slot_cap();
+      aa.min_split = 1 + cand_cap / 128;
+    }
   }
   return launch_status(kv_fmt == 2 ? launch_attn_mxfp4kv(aa, s) : kv_fmt == 1 ? launch_attn_fp8kv(aa, s) : launch_attn(aa, s));
 }

@@ -93,8 +93,9 @@ struct DecodeFuse {
 // decode-step state kept across steps: the histograms [B][4160], the top-k tickets [B] (zero
 // before the first step, left zero by every step), then two step counters [B] each: selections
 // completed (the selection's last CTA of a row adds one) and selections consumed (the split
-// merge copies the first after the step's attention); zero before the first step, left equal
-inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + 3 * static_cast<size_t>(B); }
+// merge copies the first after the step's attention), zero before the first step and left
+// equal; the chunks' counters [B] (left zero by the merge) and the published thresholds [B][2]
+inline size_t decode_state_words(int B) { return static_cast<size_t>(B) * 4160 + 6 * static_cast<size_t>(B); }
 struct IndexerArgs {
   const void* qI;        // [B*T, HI, dI]
   const float* w;        // [B*T, HI]
@@ -188,10 +189,22 @@ cudaError_t launch_topk_hist_standalone(const TopkArgs& a, cudaStream_t s);
 // Decode-step extras of the histogram selection (all null / zero: none).
 struct SelHandoff {
   uint32_t* done;            // [rows] counters the row's last CTA increments once its list is written
+                             // (or, with cand_cap, once its threshold is published)
+  uint32_t* chunks;          // [rows] counters every chunk CTA increments once its slot is written
+  uint32_t* thr;             // [rows][2]: threshold key T and tie cut P of the published threshold
+  int cand_cap;              // > 0: rows with at most cand_cap candidates publish (T, P) and count
+                             // done before writing the list (a candidate wins iff key > T, or
+                             // key == T and position <= P); others count done after the list
   const uint8_t* pf_rows;    // cache rows the list indexes: every candidate's row (row r's entry s at
   int64_t pf_row_bytes;      // pf_rows + (r * pf_seq_rows + s) * pf_row_bytes, a multiple of 16
   int64_t pf_seq_rows;       // bytes) is prefetched into L2 as soon as its chunk keeps it
 };
+// The selection's per-chunk candidate slots in the top-k workspace (ws_cand of launch_topk_hist):
+// row r's chunk c at words ((r * n_chunks + c) * sel_slot_words(); [count, 3 pad][keys x
+// sel_slot_cap()][positions x sel_slot_cap()]; n_chunks = sel_chunks(n_cols).
+int sel_slot_words();
+int sel_slot_cap();
+int sel_chunks(int64_t n_cols);
 cudaError_t launch_topk_hist(const void* scores, int64_t ld, int64_t rows, int64_t n_cols, const int32_t* n_valid,
                              uint32_t* hist_cnt, int k, int32_t* idx, void* ws_cand, int num_sms, cudaStream_t s,
                              const int32_t* cmap = nullptr, bool bf16 = false, const SelHandoff& ho = SelHandoff{});
@@ -233,12 +246,20 @@ struct AttnArgs {
   uint32_t* sel_seen;     // selection kernel before this one; [B] selections consumed (the merge
                           // sets it to sel_done): query r's list is ready once sel_done[r] passes
                           // sel_seen[r], and holds its entries first (ascending), then -1
+  int cand_cap;           // > 0 (with sel_done): candidate mode for rows of at most cand_cap
+                          // candidates (see SelHandoff): split 0 the window, split s > 0 the
+                          // candidates 128 (s - 1) .. +127, masked by the published threshold
+  uint32_t* sel_chunks;   // [B] chunk counters (the merge zeroes them after the step)
+  const uint32_t* sel_thr;    // [B][2] published thresholds
+  const uint32_t* sel_slots;  // the selection's candidate slots
+  int sel_n_chunks, sel_slot_words, sel_slot_cap;
+  int min_split;          // decode split plan: at least this many splits
   void* ws;
   size_t ws_bytes;
   int* err;
   int num_sms;
 };
-size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms);
+size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms, int min_split = 0);
 // Dense (HCA) attention: workspace for the split plan over at most E_cap + W rows a query.
 size_t attn_dense_workspace_bytes(int B, int T, int H, int d, int64_t E_cap, int W, int act, int num_sms);
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);

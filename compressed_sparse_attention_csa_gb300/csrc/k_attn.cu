@@ -1089,7 +1089,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
   int64_t p_lo;
   int n_win;
   window_of(t, a.W, lbase, a.L, p_lo, n_win);
-  const int row_lo = split * sp.rows_per_split;
+  int row_lo = split * sp.rows_per_split;  // (candidate mode: reset to 0 below)
   const int row_cap = row_lo + kRows;
   const __nv_bfloat16* kvc = static_cast<const __nv_bfloat16*>(a.kv_comp) + static_cast<int64_t>(b) * a.E_cap * kD;
   const __nv_bfloat16* kvl = static_cast<const __nv_bfloat16*>(a.kv_local) + static_cast<int64_t>(b) * a.L * kD;
@@ -1107,7 +1107,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
     }
   }
   int row_hi;
-  if (a.sel_done) {
+  // candidate mode (decode step, few candidates): split 0 holds the window rows only, split
+  // s > 0 the selection's candidates 128 (s - 1) .. +127 (in slot order), gathered before the
+  // threshold is known and masked by it in the softmax; skey: their keys
+  bool cand = false;
+  uint32_t* skey = reinterpret_cast<uint32_t*>(sel + kRows);        // [kRows]
+  uint32_t* cpre = skey + kRows;                                     // [64] chunk prefix, then n_all
+  bool list_mode = true;
+  if (a.sel_done && a.cand_cap > 0) {
+    pdl_trigger();
+    if (tid == 0) wait_count(a.sel_chunks + r, static_cast<uint32_t>(a.sel_n_chunks), a.err);
+    __syncthreads();
+    const uint32_t* sb = a.sel_slots + static_cast<size_t>(r) * a.sel_n_chunks * a.sel_slot_words;
+    if (warp == 0) {
+      // the chunks' candidate counts (at most 64) and their exclusive prefix
+      const uint32_t c0 = lane < a.sel_n_chunks ? __ldcg(sb + static_cast<size_t>(lane) * a.sel_slot_words) : 0u;
+      const uint32_t c1 =
+          lane + 32 < a.sel_n_chunks ? __ldcg(sb + static_cast<size_t>(lane + 32) * a.sel_slot_words) : 0u;
+      uint32_t i0 = c0, i1 = c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v0 = __shfl_up_sync(0xffffffffu, i0, o), v1 = __shfl_up_sync(0xffffffffu, i1, o);
+        if (lane >= o) {
+          i0 += v0;
+          i1 += v1;
+        }
+      }
+      const uint32_t t0 = __shfl_sync(0xffffffffu, i0, 31), t1 = __shfl_sync(0xffffffffu, i1, 31);
+      cpre[lane] = i0 - c0;
+      cpre[lane + 32] = t0 + i1 - c1;
+      if (lane == 0) cpre[64] = t0 + t1;
+    }
+    __syncthreads();
+    const int n_all = static_cast<int>(cpre[64]);
+    if (n_all <= a.cand_cap) {
+      list_mode = false;
+      if (split == 0) {
+        row_hi = n_win;  // the window rows, loaded above
+      } else {
+        cand = true;
+        const int g0 = (split - 1) * kRows;
+        row_lo = 0;
+        n_win = 0;
+        row_hi = min(max(n_all - g0, 0), kRows);
+        if (tid < row_hi) {
+          const int gi = g0 + tid;
+          int lo = 0, hi = a.sel_n_chunks - 1;  // the last chunk whose prefix is <= gi
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<int>(cpre[mid]) <= gi) lo = mid;
+            else hi = mid - 1;
+          }
+          const uint32_t* sl = sb + static_cast<size_t>(lo) * a.sel_slot_words;
+          const int e = gi - static_cast<int>(cpre[lo]);
+          skey[tid] = __ldcg(sl + 4 + e);
+          sel[tid] = static_cast<int32_t>(__ldcg(sl + 4 + a.sel_slot_cap + e));
+        }
+        __syncthreads();
+      }
+    }
+  }
+  if (a.sel_done && list_mode) {
     // decode step: wait for this query's list only (counted done by the selection's last CTA
     // of the row once written), not for the whole selection kernel; the list holds its entries
     // first, so this split reads just its own slice, and its valid rows are a prefix
@@ -1129,7 +1189,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
       }
     }
     row_hi = row_lo + __syncthreads_count(valid);
-  } else {
+  } else if (!a.sel_done) {
     pdl_wait();  // the selection (and the entry compressed this step) come from earlier kernels
     pdl_trigger();
     const int n_sel = compact_idx<kTcThreads>(a.idx + r * a.k, a.k, a.E_cap, sel, tmp, a.err);
@@ -1295,10 +1355,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_dec_kernel(const AttnArgs 
     constexpr int HH = NH / 2;
     const int hh0 = (warp >> 2) * HH;
     float x[HH];
+    uint32_t thr_t = 0u;  // candidate mode: the published threshold (key, tie cut)
+    int32_t thr_p = 0;
+    if (cand) {
+      if (tid == 0) wait_count(a.sel_done + r, __ldcg(a.sel_seen + r) + 1u, a.err);
+      __syncthreads();
+      thr_t = __ldcg(a.sel_thr + 2 * r);
+      thr_p = static_cast<int32_t>(__ldcg(a.sel_thr + 2 * r + 1));
+    }
     {
       mbar_wait(&bars[0], 0, a.err, nullptr);
       tc_fence_after();
-      const bool valid = ((warp & 3) * 32 + lane) < nr;
+      const int jr = (warp & 3) * 32 + lane;
+      bool valid = jr < nr;
+      if (cand && valid) {
+        const uint32_t kj = skey[jr];
+        valid = kj > thr_t || (kj == thr_t && sel[jr] <= thr_p);
+        if (!valid) {  // a candidate left out: zero this half of its row (P = 0, and 0 x NaN is NaN)
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(sR + ((warp >> 2) * 4 + g) * (kRows * 128) + sw128(jr, c)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       float v[32];
       tmem_ld32(tS + qbase + hh0, v);  // (columns past NH are read and ignored)
       tmem_wait_ld(v);
@@ -1726,7 +1807,10 @@ __global__ void __launch_bounds__(kMwThreads) attn_merge_wide_kernel(const AttnA
   }
   pdl_wait();
   pdl_trigger();
-  if (a.sel_seen && h == 0 && t == 0) a.sel_seen[r] = __ldcg(a.sel_done + r);  // this step's list consumed
+  if (a.sel_seen && h == 0 && t == 0) {  // this step's list consumed
+    a.sel_seen[r] = __ldcg(a.sel_done + r);
+    if (a.sel_chunks) a.sel_chunks[r] = 0u;
+  }
   if (t == 0) {
     mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(ns) * kD * 4);
     for (int x = 0; x < ns; ++x) bulk_g2s(s_po + x * kD, sp.part_o + ((r * ns + x) * kH + h) * kD, kD * 4, &s_bar);
@@ -1872,9 +1956,16 @@ size_t attn_dense_workspace_bytes(int B, int T, int H, int d, int64_t E_cap, int
   return dense_partials_bytes(rows, s.n_split);
 }
 
-size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms) {
+// The decode split plan with at least min_split splits (candidate mode of the decode step).
+TcAttnSplit plan_split_min(int B, int T, int k, int W, int num_sms, int min_split) {
+  TcAttnSplit s = plan_split(B, T, k, W, num_sms);
+  if (s.n_split > 1 && s.rows_per_split == kRows && min_split > s.n_split) s.n_split = min_split;
+  return s;
+}
+
+size_t attn_workspace_bytes(int B, int T, int H, int d, int k, int W, int act, int num_sms, int min_split) {
   if (!attn_uses_tensor_cores(act, H, d, k)) return 0;
-  const TcAttnSplit s = plan_split(B, T, k, W, num_sms);
+  const TcAttnSplit s = plan_split_min(B, T, k, W, num_sms, min_split);
   if (s.n_split == 1) return 0;
   const int64_t rows = static_cast<int64_t>(B) * T;
   return align_up(static_cast<size_t>(rows * s.n_split * kH * kD) * 4, 256) +
@@ -1934,7 +2025,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     return launch_merge_wide(a, sp, rows, s);
   }
   if (attn_uses_tensor_cores(a.act, a.H, a.d, a.k)) {
-    TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
+    TcAttnSplit sp = plan_split_min(a.B, a.T, a.k, a.W, a.num_sms, a.min_split);
     if (sp.n_split > 1) {
       uint8_t* ws = static_cast<uint8_t*>(a.ws);
       sp.part_o = reinterpret_cast<float*>(ws);
@@ -2035,7 +2126,7 @@ cudaError_t launch_attn_quantkv(const AttnArgs& a, cudaStream_t s) {
     count_launches(1);
     return e;
   }
-  TcAttnSplit sp = plan_split(a.B, a.T, a.k, a.W, a.num_sms);
+  TcAttnSplit sp = plan_split_min(a.B, a.T, a.k, a.W, a.num_sms, a.min_split);
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   sp.part_o = reinterpret_cast<float*>(ws);
   sp.part_ml = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(rows * sp.n_split * kH * kD) * 4, 256));

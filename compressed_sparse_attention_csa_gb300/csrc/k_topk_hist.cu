@@ -205,6 +205,15 @@ struct SelSmem {
   uint32_t b1, last, n_gt, n_eq;
 };
 
+// Decode step: the row's threshold (key T, tie cut P) for the attention, then the row counted
+// done (one thread; the fence orders the two words before the count).
+__device__ __forceinline__ void publish_threshold(const SelHandoff& ho, int64_t row, uint32_t T, uint32_t P) {
+  ho.thr[2 * row] = T;
+  ho.thr[2 * row + 1] = P;
+  __threadfence();
+  atomicAdd(ho.done + row, 1u);
+}
+
 size_t sel_smem_bytes(int k) { return sizeof(SelSmem) + 2 * static_cast<size_t>(k) * 4 + 16; }
 
 template <bool B16>
@@ -275,10 +284,12 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
   __syncthreads();
   if (tid == 0) {
     __threadfence();
+    if (ho.chunks) atomicAdd(ho.chunks + row, 1u);  // decode step: this chunk's slot is readable
     S.last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(n_chunks - 1) ? 1u : 0u;
   }
   __syncthreads();
   if (!S.last) return;
+  bool publish = false;  // decode step: the row's threshold was published before its list
   __threadfence();
   // every CTA of the row has read the histogram: clear it and the ticket for the next use
   for (int i = tid; i < kRowWords; i += NT) rh[i] = 0u;
@@ -401,6 +412,10 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
     const uint32_t wt = __reduce_add_sync(0xffffffffu, c_tie);
     if ((tid & 31) == 0 && wt) atomicAdd(&S.n_eq, wt);
     __syncthreads();
+    // decode step: a row with few candidates publishes its threshold before the list (the
+    // attention masks the candidates it gathered with it)
+    publish = ho.cand_cap > 0 && n_all <= ho.cand_cap;
+    if (publish && tid == 0 && S.n_eq <= static_cast<uint32_t>(quota)) publish_threshold(ho, row, T, 0x7FFFFFFF);
     if (S.n_eq <= static_cast<uint32_t>(quota)) {
       // every key equal to T wins (the usual case: no tie at the threshold is cut)
       uint32_t n_win;
@@ -412,7 +427,18 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
       for (int j = static_cast<int>(n_win) + tid; j < k; j += NT) orow[j] = -1;
     } else {
       // stable compaction over contiguous segments: ties ranked in position order
+      if (publish && tid == 0) S.res[5] = 0xFFFFFFFFu;  // (no key equal to T wins: P = -1)
       uint32_t tie_r = block_exclusive_scan<NT>(c_tie, S.tmp, nullptr);
+      if (publish) {
+        // the tie cut: the position of the last winning key equal to T (ties are in position order)
+        if (tie_r < static_cast<uint32_t>(quota) && tie_r + c_tie >= static_cast<uint32_t>(quota)) {
+          uint32_t tr = tie_r;
+          for (int e = lo; e < hi; ++e)
+            if (S.ak[e] == T && ++tr == static_cast<uint32_t>(quota)) S.res[5] = static_cast<uint32_t>(S.ap[e]);
+        }
+        __syncthreads();
+        if (tid == 0) publish_threshold(ho, row, T, S.res[5]);
+      }
       uint32_t c_win = 0;
       {
         uint32_t tr = tie_r;
@@ -473,8 +499,9 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
     team_write_sorted<NT>(sel, n_above + take, k, nvr, S.hist, S.tmp, srt, orow, cm, tid, 0);
   }
   // decode step: the row's list is complete; count it done for the attention waiting on it
-  // (the barrier orders every thread's writes before the fence)
-  if (ho.done) {
+  // (the barrier orders every thread's writes before the fence), unless its threshold was
+  // published (and counted) already
+  if (ho.done && !publish) {
     __syncthreads();
     if (tid == 0) {
       __threadfence();
@@ -690,7 +717,9 @@ __global__ void __launch_bounds__(NT, CAP <= 2048 ? 4 : 1) topk_row_kernel(const
 
 int topk_hist_cap(int k) { return std::max(kAllCap, k); }
 
-static int sel_chunks(int64_t n_cols) { return static_cast<int>((n_cols + kSelChunk - 1) / kSelChunk); }
+int sel_chunks(int64_t n_cols) { return static_cast<int>((n_cols + kSelChunk - 1) / kSelChunk); }
+int sel_slot_words() { return kSlotWords; }
+int sel_slot_cap() { return kSlotCap; }
 
 // Per-chunk candidate slots ([count, keys, positions] per chunk of every row).
 size_t topk_hist_workspace_bytes(int64_t rows, int64_t n_cols) {

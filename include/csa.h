@@ -471,8 +471,9 @@ typedef struct {
  * csa_sparse_attn in that order with T = 1.
  *
  * Workspace state: the first bytes of ws (a fixed size that depends on cfg->B only) carry
- * the top-k histograms and two step counters a sequence from one step to the next (the
- * attention starts on a sequence as soon as its selection is counted done).  ws must be
+ * the top-k histograms and step counters a sequence from one step to the next (the attention
+ * starts on a sequence as soon as its selection's candidates, then its threshold, are
+ * counted ready).  ws must be
  * zeroed before the first call (csa_decode_step_reset, or a zero-filled allocation), every
  * call leaves that region ready for the next (also when a bounded wait gives up), and it must
  * not be handed to other calls in between.  Steps on one ws must run in stream order.
@@ -482,10 +483,11 @@ csa_status csa_decode_step(const csa_config *cfg, const csa_decode_args *args, v
 
 /*
  * csa_decode_step_reset — zero the part of a decode-step workspace that carries state from
- * one step to the next: its first 4 * 4163 * cfg->B bytes (per sequence a 4096-bin top-k
- * histogram with its ticket, and two step counters), asynchronously on `stream`.  Only cfg->B
- * is read.  A step leaves that state ready for the next (histograms and tickets zero, the
- * counters equal) even when its bounded waits give up (CSA_ERR_TIMEOUT); call this
+ * one step to the next: its first 4 * 4166 * cfg->B bytes (per sequence a 4096-bin top-k
+ * histogram with its ticket, three step counters and the selection's published threshold),
+ * asynchronously on `stream`.  Only cfg->B is read.  A step leaves that state ready for the
+ * next (histograms and tickets zero, the counters consistent) even when its bounded waits give
+ * up (CSA_ERR_TIMEOUT); call this
  * before the first step on a workspace that was not zero-filled, and after a step whose
  * launches failed (CSA_ERR_CUDA) or were never run.
  * Errors: CSA_ERR_NULL (cfg or ws NULL), CSA_ERR_SHAPE (cfg->B < 1), CSA_ERR_ALIGN (ws not

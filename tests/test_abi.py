@@ -123,7 +123,7 @@ def test_workspace_queries(lib):
 
 def test_decode_step_reset_argument_errors(lib):
     c = _cfg(B=3)
-    need = 4 * 4163 * 3
+    need = 4 * 4166 * 3
     f = lib.csa_decode_step_reset
     assert f(None, A, need, None) == 1
     assert f(ctypes.byref(c), None, need, None) == 1

@@ -72,7 +72,7 @@ def test_decode_step_reset_clears_a_dirty_workspace():
     ref = oracle_decode(cfg, inp)
     run_gpu_decode(cfg, gen.make_inputs(cfg, DEV))          # the workspace exists and is clean
     ws = ops._decode_ws[(str(DEV), cfg.B)]
-    state = 4 * 4163 * cfg.B
+    state = 4 * 4166 * cfg.B
     ws[:state].fill_(0x5A)                                   # dirty every carried histogram, ticket, counter
     csa.decode_step_reset(lib_config(cfg))
     torch.cuda.synchronize()

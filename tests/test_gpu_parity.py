@@ -453,6 +453,47 @@ def test_decode_step_selection_exact_on_ties(cid, kind):
     assert_decode_matches(cfg, inp, ref, out, lse, idx)
 
 
+def _candidates(s32, nv, k):
+    """Candidates of the histogram selection over s32[:nv]: scores whose 12-bit digit (of the
+    order-preserving key) is at least the digit of the k-th largest."""
+    bits = s32[:nv].astype(np.float32).view(np.uint32)
+    key = np.where(bits >> 31, ~bits, bits | np.uint32(0x80000000)).astype(np.uint32)
+    dig = key >> 20
+    b1 = np.sort(dig)[::-1][min(k, nv) - 1]
+    return int((dig >= b1).sum())
+
+
+@pytest.mark.parametrize("cid", [2, 4])
+def test_decode_step_cut_tie_among_few_candidates(cid):
+    """Sixty keys given one score ranked just above the k-th largest, in a row of few
+    candidates: the step's attention starts on the candidates before the list is written and
+    masks them with the published threshold and tie cut; the selection (lowest positions among
+    the tied keys) and the outputs stay exact."""
+    cfg = gen.CONFIGS[cid].replace(B=2, N=4 * 20000)
+    inp = gen.make_inputs(cfg, DEV)
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    run_gpu_decode(cfg, {kk: v.clone() for kk, v in inp.items()}, scores_out=scores)
+    nv = [min(int(inp["q_pos"][b]) + 1, cfg.m * cfg.E) // cfg.m for b in range(cfg.B)]
+    for b in range(cfg.B):
+        order = torch.argsort(scores[b, :nv[b] - 1], descending=True).cpu()
+        src = int(order[cfg.k - 25])
+        dst = order[cfg.k + 100:cfg.k + 160].to(DEV)      # sixty keys ranked below it
+        inp["kI"][b, dst] = inp["kI"][b, src].clone()
+        if "kscale" in inp:
+            inp["kscale"][b, dst] = inp["kscale"][b, src].clone()
+    ref = oracle_decode(cfg, inp)
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    out, lse, idx = run_gpu_decode(cfg, inp, scores_out=scores)
+    for b in range(cfg.B):
+        s32 = scores[b].cpu().numpy()
+        assert _candidates(s32, nv[b], cfg.k) <= 1024, "the row must stay in the candidate mode"
+        top = O.topk(s32, nv[b], cfg.k)
+        t = np.sort(s32[:nv[b]])[::-1][cfg.k - 1]
+        assert int((s32[:nv[b]] == t).sum()) > int((s32[top] == t).sum()), "a tie must be cut"
+    assert_step_selection_exact(cfg, ref, idx, scores)
+    assert_decode_matches(cfg, inp, ref, out, lse, idx)
+
+
 def test_tiny_end_to_end_fp32():
     """Preset 1: compress every entry from the streams, index, select, attend (16 queries)."""
     cfg = gen.CONFIGS[1]
