@@ -202,18 +202,22 @@ __global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compres
   bool first = true;
   if (live) {
     for (int j0 = sl; j0 < m; j0 += kC1Batch * kC1Slices) {
-      float2 lg[kC1Batch], v[kC1Batch];
+      // every load of the batch first (rows past the block read its row 0 and are masked
+      // after), so that they are in flight together
+      float2 lg[kC1Batch], v[kC1Batch], bb[kC1Batch];
 #pragma unroll
       for (int u = 0; u < kC1Batch; ++u) {
         const int j = j0 + u * kC1Slices;
-        if (j < m) {
-          lg[u] = load_f2<T>(z + static_cast<int64_t>(j) * a.dim);
-          v[u] = load_f2<T>(kv + static_cast<int64_t>(j) * a.dim);
-          if (a.bias) {
-            const float2 bb = *reinterpret_cast<const float2*>(a.bias + static_cast<int64_t>(j) * a.dim + c);
-            lg[u].x += bb.x;
-            lg[u].y += bb.y;
-          }
+        const int64_t jr = j < m ? j : 0;
+        lg[u] = load_f2<T>(z + jr * a.dim);
+        v[u] = load_f2<T>(kv + jr * a.dim);
+        bb[u] = a.bias ? *reinterpret_cast<const float2*>(a.bias + jr * a.dim + c) : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kC1Batch; ++u) {
+        if (j0 + u * kC1Slices < m) {
+          lg[u].x += bb[u].x;
+          lg[u].y += bb[u].y;
         } else {
           lg[u] = make_float2(-INFINITY, -INFINITY);
           v[u] = make_float2(0.f, 0.f);
@@ -263,10 +267,11 @@ __global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compres
   s_red[sl][2][2 * lane] = ac0;
   s_red[sl][2][2 * lane + 1] = ac1;
   __syncthreads();
-  if (sl != 0 || !live) return;
-  float res[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
+  // the slices combined by warps 0 and 1: warp q takes channel 2 lane + q
+  if (sl > 1 || !live) return;
+  const int q = sl;
+  float res;
+  {
     const int cc = 2 * lane + q;
     float M = -INFINITY;
 #pragma unroll
@@ -281,14 +286,13 @@ __global__ void __launch_bounds__(32 * kC1Slices) compress1_kernel(const Compres
         acc = fmaf(s_red[s][2][cc], f, acc);
       }
     }
-    res[q] = acc / sum;
+    res = acc / sum;
   }
   const int64_t row = static_cast<int64_t>(b) * a.E_cap + entry;
   if (a.act_bf16)
-    *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.out) + row * a.dim + c) =
-        __floats2bfloat162_rn(res[0], res[1]);
+    static_cast<__nv_bfloat16*>(a.out)[row * a.dim + c + q] = __float2bfloat16_rn(res);
   else
-    *reinterpret_cast<float2*>(static_cast<float*>(a.out) + row * a.dim + c) = make_float2(res[0], res[1]);
+    static_cast<float*>(a.out)[row * a.dim + c + q] = res;
 }
 
 }  // namespace
