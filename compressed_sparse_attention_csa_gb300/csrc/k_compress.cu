@@ -69,18 +69,22 @@ __global__ void __launch_bounds__(512) compress_kernel(CompressArgs a, QprepPart
   const T* kv = static_cast<const T*>(job.kv) + static_cast<int64_t>(b) * n_tok * 2 * dim;
   const T* z = static_cast<const T*>(job.z) + static_cast<int64_t>(b) * n_tok * 2 * dim;
 
-  float lg[kMaxTok], val[kMaxTok];
+  // every load first (tokens past the block read its first row and are dropped below), so
+  // that they are in flight together; the bias is added once they have landed
+  float lg[kMaxTok], val[kMaxTok], bs[kMaxTok];
   if (c < dim) {
 #pragma unroll
     for (int j = 0; j < kMaxTok; ++j) {
-      if (j < 2 * m && (j < m || b_ok)) {
-        const int st = j < m ? 0 : 1;
-        const int jj = j < m ? j : j - m;
-        const int64_t off = (((st == 0 ? ra0 : rb0) + jj) * 2 + st) * dim + c;
-        lg[j] = load_f<T>(z + off) + job.bias[(st * m + jj) * dim + c];
-        val[j] = load_f<T>(kv + off);
-      }
+      const bool in = j < 2 * m && (j < m || b_ok);
+      const int st = in && j >= m ? 1 : 0;
+      const int jj = !in ? 0 : (j < m ? j : j - m);
+      const int64_t off = (((st == 0 ? ra0 : rb0) + jj) * 2 + st) * dim + c;
+      lg[j] = load_f<T>(z + off);
+      bs[j] = job.bias[(st * m + jj) * dim + c];
+      val[j] = load_f<T>(kv + off);
     }
+#pragma unroll
+    for (int j = 0; j < kMaxTok; ++j) lg[j] += bs[j];
   }
   if (a.q_pos) {
     const int64_t t = a.q_pos[b];

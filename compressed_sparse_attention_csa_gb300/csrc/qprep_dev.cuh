@@ -81,20 +81,26 @@ __device__ __forceinline__ uint8_t* qprep_image(const IndexerLayout& L, uint8_t*
 template <typename T, int MT, int NC>
 __device__ __forceinline__ void compress_tail(const T* kv, const T* z, const float* bias, int m, int dim,
                                               const int (&c)[NC], bool has_b, float (&out)[NC]) {
-  float lg[NC][MT], val[NC][MT];
+  // every load first (tokens past the block read its first row and are dropped below), so
+  // that they are in flight together; the bias is added once they have landed
+  float lg[NC][MT], val[NC][MT], bs[NC][MT];
 #pragma unroll
   for (int j = 0; j < MT; ++j) {
-    if (j < 2 * m && (j < m || has_b)) {
-      const int st = j < m ? 0 : 1;
-      const int jj = j < m ? j : j - m;
-      const int64_t row = static_cast<int64_t>((st == 0 ? m : 0) + jj) * 2 + st;
+    const bool in = j < 2 * m && (j < m || has_b);
+    const int st = in && j >= m ? 1 : 0;
+    const int jj = !in ? 0 : (j < m ? j : j - m);
+    const int64_t row = static_cast<int64_t>((st == 0 ? m : 0) + jj) * 2 + st;
 #pragma unroll
-      for (int n = 0; n < NC; ++n) {
-        lg[n][j] = load_f<T>(z + row * dim + c[n]) + bias[(st * m + jj) * dim + c[n]];
-        val[n][j] = load_f<T>(kv + row * dim + c[n]);
-      }
+    for (int n = 0; n < NC; ++n) {
+      lg[n][j] = load_f<T>(z + row * dim + c[n]);
+      bs[n][j] = bias[(st * m + jj) * dim + c[n]];
+      val[n][j] = load_f<T>(kv + row * dim + c[n]);
     }
   }
+#pragma unroll
+  for (int j = 0; j < MT; ++j)
+#pragma unroll
+    for (int n = 0; n < NC; ++n) lg[n][j] += bs[n][j];
   const int nt = has_b ? 2 * m : m;
 #pragma unroll
   for (int n = 0; n < NC; ++n) {
