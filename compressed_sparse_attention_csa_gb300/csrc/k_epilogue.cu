@@ -226,39 +226,39 @@ __global__ void __launch_bounds__(512) compress_norm_rope_kernel(const CompressE
   // token u of this thread -> (element offset of its (C, Z) pair, bias offset)
   const int n_tk = TWO ? (entry > 0 ? 2 * m : m) : (m - sl + S - 1) / S;
   for (int u0 = 0; u0 < n_tk; u0 += 16) {
-    float2 lg[16], val[16];
+    // every load of the batch first (tokens past the list read its first token and are
+    // dropped below), so that they are in flight together; the bias is added after
+    float2 lg[16], val[16], bb[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-      const int u = u0 + q;
-      if (u < n_tk) {
-        int64_t off;
-        int64_t boff;
-        if (TWO) {
-          const int st = u < m ? 0 : 1, j = u < m ? u : u - m;
-          const int64_t row = (st == 0 ? m * entry : m * (entry - 1)) + j - a.tok0;
-          off = ((static_cast<int64_t>(b) * a.n_tok + row) * 2 + st) * a.dim + c;
-          boff = static_cast<int64_t>(st * m + j) * a.dim + c;
-        } else {
-          const int j = sl + S * u;
-          const int64_t row = m * entry + j - a.tok0;
-          off = (static_cast<int64_t>(b) * a.n_tok + row) * a.dim + c;
-          boff = static_cast<int64_t>(j) * a.dim + c;
-        }
-        float2 zz, vv;
-        if constexpr (sizeof(T) == 2) {
-          zz = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(z + off));
-          vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kv + off));
-        } else {
-          zz = *reinterpret_cast<const float2*>(z + off);
-          vv = *reinterpret_cast<const float2*>(kv + off);
-        }
-        if (a.bias) {
-          const float2 bb = *reinterpret_cast<const float2*>(a.bias + boff);
-          zz.x += bb.x;
-          zz.y += bb.y;
-        }
-        lg[q] = zz;
-        val[q] = vv;
+      const int u = u0 + q < n_tk ? u0 + q : 0;
+      int64_t off;
+      int64_t boff;
+      if (TWO) {
+        const int st = u < m ? 0 : 1, j = u < m ? u : u - m;
+        const int64_t row = (st == 0 ? m * entry : m * (entry - 1)) + j - a.tok0;
+        off = ((static_cast<int64_t>(b) * a.n_tok + row) * 2 + st) * a.dim + c;
+        boff = static_cast<int64_t>(st * m + j) * a.dim + c;
+      } else {
+        const int j = sl + S * u;
+        const int64_t row = m * entry + j - a.tok0;
+        off = (static_cast<int64_t>(b) * a.n_tok + row) * a.dim + c;
+        boff = static_cast<int64_t>(j) * a.dim + c;
+      }
+      if constexpr (sizeof(T) == 2) {
+        lg[q] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(z + off));
+        val[q] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kv + off));
+      } else {
+        lg[q] = *reinterpret_cast<const float2*>(z + off);
+        val[q] = *reinterpret_cast<const float2*>(kv + off);
+      }
+      bb[q] = a.bias ? *reinterpret_cast<const float2*>(a.bias + boff) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      if (u0 + q < n_tk) {
+        lg[q].x += bb[q].x;
+        lg[q].y += bb[q].y;
       } else {
         lg[q] = make_float2(-INFINITY, -INFINITY);
         val[q] = make_float2(0.f, 0.f);
