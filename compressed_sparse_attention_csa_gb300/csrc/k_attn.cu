@@ -1030,8 +1030,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_pf_kernel(const AttnArgs a
 // with N = NH; O^T += R^T P^T with the P tile zero beyond NH heads).  The list puts the
 // window first: the window rows, like the query, are inputs that no earlier kernel of the
 // step writes, so they are gathered before the wait on the top-k; the selected rows follow.
-// Partials are stored [query][split][head][dim] (each warp store is 128 contiguous bytes)
-// and merged, with the sink, by attn_merge_wide_kernel.
+// In the decode step a split waits on its own query's step counters (AttnArgs::sel_done)
+// rather than on the whole selection kernel, and with few candidates (AttnArgs::cand_cap)
+// works on the selection's candidates before the threshold that picks them is published:
+// split 0 the window, split s the candidates 128 (s - 1) .. +127; the softmax keeps a
+// candidate iff its key is above the threshold key, or equal to it at a position up to the
+// tie cut.  Partials are stored [query][split][head][dim] (each warp store is 128 contiguous
+// bytes) and merged, with the sink, by attn_merge_wide_kernel.
 
 
 template <int NH>
