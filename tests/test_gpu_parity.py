@@ -494,6 +494,35 @@ def test_decode_step_cut_tie_among_few_candidates(cid):
     assert_decode_matches(cfg, inp, ref, out, lse, idx)
 
 
+def test_decode_step_counters_across_modes():
+    """Consecutive steps on one workspace alternate between a row of few candidates (the
+    attention starts on them before the selection writes its list) and a row whose threshold
+    bin holds thousands of equal scores (the attention waits for the written list): the step
+    counters stay in step and every selection is exact."""
+    cfg = gen.CONFIGS[4].replace(B=2, N=4 * 20000)
+    plain = gen.make_inputs(cfg, DEV)
+    tied = {kk: v.clone() for kk, v in plain.items()}
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    run_gpu_decode(cfg, {kk: v.clone() for kk, v in plain.items()}, scores_out=scores)
+    nv = [min(int(plain["q_pos"][b]) + 1, cfg.m * cfg.E) // cfg.m for b in range(cfg.B)]
+    for b in range(cfg.B):
+        order = torch.argsort(scores[b, :nv[b] - 1], descending=True).cpu()
+        src = int(order[cfg.k - 25])
+        dst = order[cfg.k + 100:cfg.k + 3100].to(DEV)     # 3,000 keys ranked below it
+        tied["kI"][b, dst] = tied["kI"][b, src].clone()
+        tied["kscale"][b, dst] = tied["kscale"][b, src].clone()
+    for inp, list_mode in ((plain, False), (tied, True), (plain, False), (tied, True), (plain, False)):
+        run = {kk: v.clone() for kk, v in inp.items()}
+        ref = oracle_decode(cfg, run)
+        scores = torch.empty(cfg.B, cfg.E, device=DEV)
+        out, lse, idx = run_gpu_decode(cfg, run, scores_out=scores)
+        for b in range(cfg.B):
+            n_cand = _candidates(scores[b].cpu().numpy(), nv[b], cfg.k)
+            assert (n_cand > 1024) == list_mode, (b, n_cand, list_mode)
+        assert_step_selection_exact(cfg, ref, idx, scores)
+        assert_decode_matches(cfg, run, ref, out, lse, idx)
+
+
 def test_tiny_end_to_end_fp32():
     """Preset 1: compress every entry from the streams, index, select, attend (16 queries)."""
     cfg = gen.CONFIGS[1]
