@@ -19,7 +19,8 @@ then K timed steps: CUDA-graph replays of the step's library calls, back to back
 pair of CUDA events on the launching stream.  `value` uses inputs resident in HBM;
 `flushed_step` times one copy's step alone after a 512 MiB L2 flush, one event pair per step;
 `e2e` calls the public API eagerly and adds, every step, the pinned-host -> device copy of
-the step's inputs and the device -> host copy of its output.  The dominant kernel stage is
+the step's inputs (one copy: they sit in one StepInputs buffer) and the device -> host copy
+of its output.  The dominant kernel stage is
 timed in the same rotation on its own for the roofline entry.
 
 `--impl reference` times the CPU oracle (oracle/csa_oracle.py, float64 numpy) on a bounded
@@ -205,13 +206,24 @@ def _host64(x):
 #   step()             one pass of the whole hot path over the batch (inputs resident)
 #   units              tokens per step (the metric's unit)
 #   stage_fn()         the dominant kernel stage alone, with stage_bound / stage_amount
-#   e2e_in / e2e_out   the per-step inputs a user copies in and the output read back
+#   staging / e2e_out  the per-step inputs a user copies in (StepInputs) and the output read back
 #   oracle(n)          (units, seconds, description) of the CPU oracle on a bounded sample
+
+
+def staged(csa, inp, keys):
+    """Pack a workload's per-step inputs into one StepInputs buffer (one host-to-device copy a
+    step) and point the workload's input dict at its views."""
+    st = csa.StepInputs({k: inp[k] for k in keys})
+    inp.update(st.dev)
+    return st
 
 
 class Decode:
     FP8KV = False   # main-KV entries stored as FP8 entries (576 B)
     MXKV = False    # main-KV entries stored as MXFP4 entries (288 B)
+
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str", "kv_local"]
 
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
@@ -242,6 +254,7 @@ class Decode:
         self.csa = csa
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, fp8_keys=cfg.kidx == "fp8", softmax_scale=cfg.softmax_scale,
                             mx_keys=cfg.kidx == "mxfp4")
@@ -272,8 +285,6 @@ class Decode:
         self.stage_amount = work["indexer_bytes"] + cfg.B * cfg.E * 4   # + the fp32 scores written
         self.step_bytes = work["bytes"]
         self.touched_bytes = work["bytes"] + cfg.B * cfg.E * 4
-        self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str",
-                                            "kv_local"]}
         self.e2e_out = self.out
 
     def step(self):
@@ -331,6 +342,9 @@ class Decode:
 
 
 class Prefill:
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str", "kv_local"]
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
@@ -351,6 +365,7 @@ class Prefill:
         self.csa = csa
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, fp8_keys=False, softmax_scale=cfg.softmax_scale)
         self.scores = torch.empty(B * T, E, device=dev)
@@ -364,8 +379,6 @@ class Prefill:
         self.stage_amount = work["indexer_flops"]
         self.step_flops = work["flops"]
         self.touched_bytes = work["bytes"] + B * T * E * 4
-        self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str",
-                                            "kv_local"]}
         self.e2e_out = self.out
 
     def step(self):
@@ -466,6 +479,9 @@ class Prefill:
 class Csa2Group:
     N_BLOCKS = 2048
 
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "qI", "w", "qI_full", "w_full", "q_pos", "kv_local"]
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
@@ -484,6 +500,7 @@ class Csa2Group:
         self.csa = csa
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, fp8_keys=False, softmax_scale=cfg.softmax_scale)
         P = self.N_BLOCKS * 8
@@ -501,7 +518,6 @@ class Csa2Group:
         self.stage_amount = work["scan_bytes"] + B * E * 4
         self.step_bytes = work["bytes"]
         self.touched_bytes = work["bytes"] + B * E * 4
-        self.e2e_in = {k: inp[k] for k in ["q", "qI", "w", "qI_full", "w_full", "q_pos", "kv_local"]}
         self.e2e_out = self.outs
 
     def stage_fn(self):
@@ -561,6 +577,9 @@ class HcaDecode:
     """HCA ("Heavily Compressed Attention") decode: one-stream compression of the block the
     token completes, then dense attention over every visible entry plus the window."""
 
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "q_pos", "kv_str", "z_str", "kv_local"]
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
@@ -576,6 +595,7 @@ class HcaDecode:
         self.csa = csa
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.c = csa.Config(B=cfg.B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
         self.out = torch.empty(cfg.B, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
@@ -592,7 +612,6 @@ class HcaDecode:
         self.stage_amount = work["attention_bytes"]
         self.step_bytes = work["bytes"]
         self.touched_bytes = work["bytes"]
-        self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_str", "z_str", "kv_local"]}
         self.e2e_out = self.out
 
     def step(self):
@@ -632,6 +651,9 @@ class HcaPrefill:
     """HCA prefill chunk: one-stream compression of the chunk's new entries, then dense
     attention for every query of the chunk."""
 
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "q_pos", "kv_str", "z_str", "kv_local"]
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
@@ -650,6 +672,7 @@ class HcaPrefill:
         self.csa = csa
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
         self.out = torch.empty(B, T, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
@@ -661,7 +684,6 @@ class HcaPrefill:
         self.stage_amount = work["attention_flops"]
         self.step_flops = work["flops"]
         self.touched_bytes = work["bytes"]
-        self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_str", "z_str", "kv_local"]}
         self.e2e_out = self.out
 
     def step(self):
@@ -704,6 +726,9 @@ class Epilogue:
     """Attention prologue / epilogue of the prefill chunk: query RMSNorm + RoPE, the chunk's
     compression fused with RMSNorm + RoPE + cache insert, inverse RoPE + FP8 of the output."""
 
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "o", "q_pos", "kv_str", "z_str"]
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
@@ -722,6 +747,7 @@ class Epilogue:
         self.csa = csa
         inp = gen.make_inputs(cfg, dev, row0=row0)
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.c = csa.Config(B=B, H=cfg.H, d=cfg.d, HI=cfg.HI, dI=cfg.dI, m=cfg.m, k=cfg.k, W=cfg.W,
                             act=torch.bfloat16, softmax_scale=cfg.softmax_scale)
         self.nr_q = csa.NormRope(weight=inp["q_norm"], eps=1e-6, rope_dims=64, theta=10000.0)
@@ -736,7 +762,6 @@ class Epilogue:
         self.stage_amount = work["q_bytes"]
         self.step_bytes = work["bytes"]
         self.touched_bytes = work["bytes"]
-        self.e2e_in = {k: inp[k] for k in ["q", "o", "q_pos", "kv_str", "z_str"]}
         self.e2e_out = self.codes
 
     def step(self):
@@ -786,6 +811,9 @@ class Fp8KvAttn:
     _shared = {}
     FMT = "fp8"
 
+    # the per-step inputs: one StepInputs buffer, copied in every end-to-end step
+    E2E_KEYS = ["q", "q_pos", "kv_local", "idx"]
+
     def __init__(self, cfg, csa, torch, dev, row0, host_only=False):
         from synth import gen
         self.cfg = cfg
@@ -822,6 +850,7 @@ class Fp8KvAttn:
             inp["idx"] = gen.fp8kv_selection(cfg, dev, row0, shared["draws"])
         shared["draws"] += 1
         self.inp = inp
+        self.staging = staged(csa, inp, self.E2E_KEYS)
         self.out = torch.empty(B, 1, cfg.H, cfg.d, device=dev, dtype=torch.bfloat16)
         self.lse = torch.empty(B, 1, cfg.H, device=dev)
         ab = 2
@@ -831,7 +860,6 @@ class Fp8KvAttn:
         self.stage_amount = B * (cfg.k * self.entry_bytes + cfg.W * cfg.d * ab + 2 * cfg.H * cfg.d * ab + cfg.k * 4)
         self.step_bytes = self.stage_amount
         self.touched_bytes = self.stage_amount
-        self.e2e_in = {k: inp[k] for k in ["q", "q_pos", "kv_local", "idx"]}
         self.e2e_out = self.out
 
     def step(self):
@@ -1228,18 +1256,17 @@ def main():
                                  "frac_of_hbm": round(wl.work["bytes_without_scan"] / (ns_ms / 1e3) / 1e9 / hbm, 4)}
 
     # ---- end to end: the public API called eagerly with host buffers; every step copies its
-    #      inputs in from pinned host memory and its output back, inside its own event pair
-    host_in = {k: v.cpu().pin_memory() for k, v in wl.e2e_in.items()}
+    #      inputs in from pinned host memory (the workload's StepInputs mirror, which holds
+    #      them: one copy) and its output back, inside its own event pair
     host_out = torch.empty(wl.e2e_out.shape, dtype=wl.e2e_out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    h2d = wl.staging.nbytes
     d2h = host_out.numel() * host_out.element_size()
     Ke = max(3, min(K, 500))
     eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     for i in range(Ke):
         w = wls[i % R]
         eve[i][0].record(stream)
-        for k, v in host_in.items():
-            w.e2e_in[k].copy_(v, non_blocking=True)
+        w.staging.upload()
         w.step()
         host_out.copy_(w.e2e_out, non_blocking=True)
         eve[i][1].record(stream)

@@ -464,3 +464,42 @@ class HcaDecodeStepCall:
     def __call__(self) -> None:
         _check("csa_hca_decode_step",
                self._lib.csa_hca_decode_step(self._cref, self._aref, self._wp, self._wb, _stream()))
+
+
+class StepInputs:
+    """A step's per-step input tensors packed back to back in one device buffer, with a host
+    mirror of the same layout (pinned when the buffer is on a GPU).
+
+    The caller writes a step's inputs into ``host[name]`` and ``upload()`` moves all of them
+    with one host-to-device copy on the current stream; the step reads ``dev[name]``.  Each
+    tensor starts on a 256-byte boundary of the buffer, so the views keep the alignment the
+    library's kernels ask of their inputs.  The views are contiguous and have the shapes and
+    dtypes of the tensors given; their initial contents are those tensors' values."""
+
+    ALIGN = 256
+
+    def __init__(self, tensors: dict, device=None):
+        if not tensors:
+            raise ValueError("StepInputs needs at least one tensor")
+        device = torch.device(device) if device is not None else next(iter(tensors.values())).device
+        spans, off = {}, 0
+        for name, t in tensors.items():
+            nb = t.numel() * t.element_size()
+            spans[name] = (off, nb, t.shape, t.dtype)
+            off += (nb + self.ALIGN - 1) // self.ALIGN * self.ALIGN
+        self.nbytes = off
+        self._dbuf = torch.empty(off, dtype=torch.uint8, device=device)
+        self._hbuf = torch.empty(off, dtype=torch.uint8, pin_memory=device.type == "cuda")
+        self.dev, self.host = {}, {}
+        for name, (o, nb, shape, dt) in spans.items():
+            self.dev[name] = self._dbuf[o:o + nb].view(dt).view(shape)
+            self.host[name] = self._hbuf[o:o + nb].view(dt).view(shape)
+            self.host[name].copy_(tensors[name])
+            self.dev[name].copy_(tensors[name])
+
+    def upload(self) -> None:
+        """Enqueue the one host-to-device copy of every input on the current stream."""
+        if self._dbuf.is_cuda:
+            self._dbuf.copy_(self._hbuf, non_blocking=True)
+        else:
+            self._dbuf.copy_(self._hbuf)

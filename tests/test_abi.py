@@ -158,3 +158,26 @@ def test_mxfp4_key_argument_errors(lib):
     args.kscale = 0x10020
     args.E_cap = (1 << 16) + 2
     assert lib.csa_decode_step(ctypes.byref(mx), ctypes.byref(args), A, 1 << 30, None) == 2        # E_cap % 4
+
+
+def test_step_inputs_layout_on_cpu():
+    """StepInputs packs the tensors 256-byte aligned, keeps shapes, dtypes and values, and its
+    upload moves the host mirror's contents into the device views in one copy."""
+    import torch
+    from compressed_sparse_attention_csa_gb300.ops import StepInputs
+    g = torch.Generator().manual_seed(5)
+    ts = {"q": torch.randn(3, 5, 7, generator=g).to(torch.bfloat16),
+          "pos": torch.tensor([1, 2, 3], dtype=torch.int64),
+          "x": torch.randn(33, generator=g)}
+    st = StepInputs(ts, "cpu")
+    assert st.nbytes == 256 * (1 + 1 + 1)
+    for k, t in ts.items():
+        assert st.dev[k].shape == t.shape and st.dev[k].dtype == t.dtype and st.dev[k].is_contiguous()
+        assert st.dev[k].data_ptr() % 256 == st.dev["q"].data_ptr() % 256
+        assert torch.equal(st.dev[k], t) and torch.equal(st.host[k], t)
+    st.host["pos"].copy_(torch.tensor([7, 8, 9]))
+    st.host["x"].zero_()
+    assert torch.equal(st.dev["pos"], ts["pos"])
+    st.upload()
+    assert torch.equal(st.dev["pos"], torch.tensor([7, 8, 9])) and not st.dev["x"].any()
+    assert torch.equal(st.dev["q"], ts["q"])

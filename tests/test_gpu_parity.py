@@ -523,6 +523,30 @@ def test_decode_step_counters_across_modes():
         assert_decode_matches(cfg, run, ref, out, lse, idx)
 
 
+def test_decode_step_through_step_inputs():
+    """The decode step reading its per-step inputs (queries, gates, stream tails, window rows)
+    from one StepInputs buffer: another sequence pair's inputs written into the host mirror and
+    moved with one upload give the outputs the oracle computes for them."""
+    cfg = gen.CONFIGS[2].replace(B=2, N=4 * 5000)
+    keys = ["q", "qI", "w", "q_pos", "kv_str", "z_str", "kvI_str", "zI_str", "kv_local"]
+    inp = gen.make_inputs(cfg, DEV)
+    other = gen.make_inputs(cfg, DEV, row0=2)
+    st = csa.StepInputs({k: inp[k] for k in keys})
+    run = dict(inp)
+    run.update(st.dev)
+    for k in keys:
+        if k != "q_pos":            # the caches and window base stay those of the first pair
+            st.host[k].copy_(other[k])
+    st.upload()
+    want = {k: v.clone() for k, v in run.items()}
+    ref = oracle_decode(cfg, want)
+    scores = torch.empty(cfg.B, cfg.E, device=DEV)
+    out, lse, idx = run_gpu_decode(cfg, run, scores_out=scores)
+    assert torch.equal(run["q"], other["q"])
+    assert_step_selection_exact(cfg, ref, idx, scores)
+    assert_decode_matches(cfg, run, ref, out, lse, idx)
+
+
 def test_tiny_end_to_end_fp32():
     """Preset 1: compress every entry from the streams, index, select, attend (16 queries)."""
     cfg = gen.CONFIGS[1]
