@@ -20,7 +20,9 @@ pair of CUDA events on the launching stream.  `value` uses inputs resident in HB
 `flushed_step` times one copy's step alone after a 512 MiB L2 flush, one event pair per step;
 `e2e` calls the public API eagerly and adds, every step, the pinned-host -> device copy of
 the step's inputs (one copy: they sit in one StepInputs buffer) and the device -> host copy
-of its output.  The dominant kernel stage is
+of its output, pipelined on two copy streams beside the previous step's compute (one event
+pair around all the steps); `e2e_serial` does the same with the copies and the step in order
+on one stream, one event pair a step.  The dominant kernel stage is
 timed in the same rotation on its own for the roofline entry.
 
 `--impl reference` times the CPU oracle (oracle/csa_oracle.py, float64 numpy) on a bounded
