@@ -16,7 +16,10 @@
 //    keys, writes the winners ascending and clears the histogram row.  If the slots overflow
 //    (a bin full of ties) it selects over the whole row instead, in position order.
 //  * Many long rows (the prefill chunk, the block pool): topk_row_kernel, one CTA per row with
-//    the histogram in shared memory and the same exact selection.
+//    the histogram in shared memory and the same exact selection; a long row first estimates
+//    b1 from a one-in-eight sample and keeps the scores at or above the estimate when they
+//    hold the top k and fit the candidate list (exact b1 from their own histogram), else
+//    histograms the whole row.
 // The decode step runs topk_select_kernel on the histogram its indexer launch fills.
 //
 // BF16 scores ("FP4, down to the index scores": the index scores rounded to BF16 before the
@@ -520,6 +523,7 @@ __global__ void __launch_bounds__(NT, 2) topk_select_kernel(const void* scores_v
 // The candidate list holds CAP entries: 2048 for k <= 512 (four CTAs fit on an SM), else 8192.
 constexpr int kRowPer = 8;                 // scores per thread per batch
 constexpr int kRowBatch = kRowPer * NT;    // 4096
+constexpr int64_t kSampleMinRow = 16384;   // rows at least this long estimate the threshold first
 
 template <int CAP>
 struct RowSmem {
@@ -555,67 +559,133 @@ __global__ void __launch_bounds__(NT, CAP <= 2048 ? 4 : 1) topk_row_kernel(const
   if (cmap) nvr = warp_cand_prefix(cmap + row * n_cols, nvr);
   const typename K::T* srow = scores + row * ld;
   __syncthreads();
-  // pass 1: the histogram of the visible scores (two batches of loads in flight)
-  for (int64_t base = 0; base < nvr; base += 2 * kRowBatch) {
-    uint32_t v[kRowPer], w[kRowPer];
-    const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer, t1 = t0 + kRowBatch;
-    load_keys8<B16>(srow, t0, nvr, v);
-    load_keys8<B16>(srow, t1, nvr, w);
-#pragma unroll
-    for (int u = 0; u < kRowPer; ++u) {
-      if (t0 + u < nvr) atomicAdd(&S.hist[v[u] >> 20], 1u);
-      if (t1 + u < nvr) atomicAdd(&S.hist[w[u] >> 20], 1u);
-    }
-  }
-  __syncthreads();
-  const uint32_t b1 = team_threshold_digit_smem<NT>(S.hist, k, S.tmp, S.res, tid, 0);
-  // pass 2: the candidates (digit >= b1), appended in any order (each warp reserves its batch's
-  // slots with one shared-memory atomic: no block barrier inside the loop)
-  if (tid == 0) {
-    S.n_gt = 0u;
-    S.n_app = 0u;
-    S.n_eq = 0u;
-    S.n_win = 0u;
-    S.n_tie = 0u;
-  }
-  __syncthreads();
   const int lane = tid & 31;
-  uint32_t my_gt = 0;
-  for (int64_t base = 0; base < nvr; base += kRowBatch) {
-    uint32_t v[kRowPer];
-    const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
-    load_keys8<B16>(srow, t0, nvr, v);
-    uint32_t c = 0;
-#pragma unroll
-    for (int u = 0; u < kRowPer; ++u) {
-      const bool in = t0 + u < nvr && (v[u] >> 20) >= b1;
-      c += in;
-      my_gt += in && (v[u] >> 20) > b1;
+  // pass 2: the candidates (digit >= bmin), appended in any order (each warp reserves its
+  // batch's slots with one shared-memory atomic: no block barrier inside the loop); S.n_app
+  // counts them all, S.n_gt those above bmin
+  auto collect = [&](uint32_t bmin) {
+    if (tid == 0) {
+      S.n_gt = 0u;
+      S.n_app = 0u;
+      S.n_eq = 0u;
+      S.n_win = 0u;
+      S.n_tie = 0u;
     }
-    uint32_t x = c;
+    __syncthreads();
+    uint32_t my_gt = 0;
+    for (int64_t base = 0; base < nvr; base += kRowBatch) {
+      uint32_t v[kRowPer];
+      const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer;
+      load_keys8<B16>(srow, t0, nvr, v);
+      uint32_t c = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    const uint32_t wtot = __shfl_sync(0xffffffffu, x, 31);
-    uint32_t wbase = 0;
-    if (lane == 31 && wtot) wbase = atomicAdd(&S.n_app, wtot);
-    wbase = __shfl_sync(0xffffffffu, wbase, 31);
-    uint32_t off = wbase + x - c;
+      for (int u = 0; u < kRowPer; ++u) {
+        const bool in = t0 + u < nvr && (v[u] >> 20) >= bmin;
+        c += in;
+        my_gt += in && (v[u] >> 20) > bmin;
+      }
+      uint32_t x = c;
 #pragma unroll
-    for (int u = 0; u < kRowPer; ++u) {
-      if (t0 + u < nvr && (v[u] >> 20) >= b1) {
-        if (off < static_cast<uint32_t>(CAP)) {
-          S.ak[off] = v[u];
-          S.ap[off] = static_cast<int32_t>(t0 + u);
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const uint32_t wtot = __shfl_sync(0xffffffffu, x, 31);
+      uint32_t wbase = 0;
+      if (lane == 31 && wtot) wbase = atomicAdd(&S.n_app, wtot);
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      uint32_t off = wbase + x - c;
+#pragma unroll
+      for (int u = 0; u < kRowPer; ++u) {
+        if (t0 + u < nvr && (v[u] >> 20) >= bmin) {
+          if (off < static_cast<uint32_t>(CAP)) {
+            S.ak[off] = v[u];
+            S.ap[off] = static_cast<int32_t>(t0 + u);
+          }
+          ++off;
         }
-        ++off;
       }
     }
+    my_gt = __reduce_add_sync(0xffffffffu, my_gt);
+    if (lane == 0 && my_gt) atomicAdd(&S.n_gt, my_gt);
+    __syncthreads();
+  };
+  // Long rows first estimate the threshold digit from a sample, the first 8 scores of every
+  // 64: the largest digit whose sample suffix reaches 1.5 k (scaled to the sample) + 16.  If
+  // the row holds between k and CAP scores at or above that digit, they are the candidates
+  // (every score of the top k is among them) and the exact digit b1 of the k-th largest comes
+  // from their own histogram; otherwise the whole row's histogram decides, as below.
+  uint32_t b1 = 0u;
+  uint32_t n_in = 0u;  // candidates with digit >= b1 (the rest of the list lies below b1)
+  bool sampled = false;
+  const int64_t n_groups = nvr / 64;
+  const int64_t n_s = n_groups * 8;
+  if (nvr >= kSampleMinRow && 16 * static_cast<int64_t>(k) <= nvr) {
+    for (int64_t g0 = 0; g0 < n_groups; g0 += 2 * NT) {
+      uint32_t v[kRowPer], w[kRowPer];
+      const int64_t ga = g0 + tid, gb = ga + NT;
+      if (ga < n_groups) load_keys8<B16>(srow, ga * 64, nvr, v);
+      if (gb < n_groups) load_keys8<B16>(srow, gb * 64, nvr, w);
+#pragma unroll
+      for (int u = 0; u < kRowPer; ++u) {
+        if (ga < n_groups) atomicAdd(&S.hist[v[u] >> 20], 1u);
+        if (gb < n_groups) atomicAdd(&S.hist[w[u] >> 20], 1u);
+      }
+    }
+    __syncthreads();
+    const int k_s = static_cast<int>(min(n_s, (3 * static_cast<int64_t>(k) * n_s) / (2 * nvr) + 16));
+    const uint32_t bs = team_threshold_digit_smem<NT>(S.hist, k_s, S.tmp, S.res, tid, 0);
+    collect(bs);
+    const uint32_t n_app = S.n_app;
+    if (n_app >= static_cast<uint32_t>(k) && n_app <= static_cast<uint32_t>(CAP)) {
+      for (int i = tid; i < kFine; i += NT) S.hist[i] = 0u;
+      __syncthreads();
+      for (int e = tid; e < static_cast<int>(n_app); e += NT) atomicAdd(&S.hist[S.ak[e] >> 20], 1u);
+      __syncthreads();
+      b1 = team_threshold_digit_smem<NT>(S.hist, k, S.tmp, S.res, tid, 0);
+      uint32_t c_gt = 0, c_in = 0;
+      for (int e = tid; e < static_cast<int>(n_app); e += NT) {
+        const uint32_t dg = S.ak[e] >> 20;
+        c_gt += dg > b1;
+        c_in += dg >= b1;
+      }
+      c_gt = __reduce_add_sync(0xffffffffu, c_gt);
+      c_in = __reduce_add_sync(0xffffffffu, c_in);
+      if (tid == 0) {
+        S.n_gt = 0u;
+        S.n_tie = 0u;
+      }
+      __syncthreads();
+      if (lane == 0 && c_gt) atomicAdd(&S.n_gt, c_gt);
+      if (lane == 0 && c_in) atomicAdd(&S.n_tie, c_in);
+      __syncthreads();
+      n_in = S.n_tie;
+      __syncthreads();
+      if (tid == 0) S.n_tie = 0u;
+      sampled = true;
+    } else {
+      for (int i = tid; i < kFine; i += NT) S.hist[i] = 0u;
+      __syncthreads();
+    }
   }
-  my_gt = __reduce_add_sync(0xffffffffu, my_gt);
-  if (lane == 0 && my_gt) atomicAdd(&S.n_gt, my_gt);
+  if (!sampled) {
+    // pass 1: the histogram of the visible scores (two batches of loads in flight)
+    for (int64_t base = 0; base < nvr; base += 2 * kRowBatch) {
+      uint32_t v[kRowPer], w[kRowPer];
+      const int64_t t0 = base + static_cast<int64_t>(tid) * kRowPer, t1 = t0 + kRowBatch;
+      load_keys8<B16>(srow, t0, nvr, v);
+      load_keys8<B16>(srow, t1, nvr, w);
+#pragma unroll
+      for (int u = 0; u < kRowPer; ++u) {
+        if (t0 + u < nvr) atomicAdd(&S.hist[v[u] >> 20], 1u);
+        if (t1 + u < nvr) atomicAdd(&S.hist[w[u] >> 20], 1u);
+      }
+    }
+    __syncthreads();
+    b1 = team_threshold_digit_smem<NT>(S.hist, k, S.tmp, S.res, tid, 0);
+    collect(b1);
+    n_in = S.n_app;
+  }
   __syncthreads();
   const uint32_t n_all = S.n_app, n_gt = S.n_gt;
   int32_t* orow = idx + row * k;
@@ -624,9 +694,9 @@ __global__ void __launch_bounds__(NT, CAP <= 2048 ? 4 : 1) topk_row_kernel(const
   if (n_all <= static_cast<uint32_t>(CAP)) {
     const int na = static_cast<int>(n_all);
     const int need = k - static_cast<int>(n_gt);
-    uint32_t T = 1u;
+    uint32_t T = b1 << 20;  // the least key of digit b1: with no cut every candidate >= it wins
     int quota = 0x7fffffff;
-    if (na - static_cast<int>(n_gt) > need) {
+    if (static_cast<int>(n_in) - static_cast<int>(n_gt) > need) {
       const uint32_t* ak = S.ak;
       select_in_bin<B16, NT>([ak](int x) { return ak[x]; }, na, need, b1, S.sort, S.tmp, S.res, &T, &quota, tid);
     }

@@ -293,6 +293,24 @@ def test_topk_many_prefill_rows():
     _topk_check(s2.contiguous(), 512, n_valid=[50000, 40000, 7, 600, 36865] * 14)
 
 
+def test_topk_many_rows_structured_against_the_sample():
+    """Long rows of the one-CTA-per-row kernel whose large scores sit at positions the
+    threshold estimate samples (the first 8 of every 64) or never samples: the estimate then
+    finds all of them, none of them, or fewer than k at or above its digit (the whole-row
+    histogram decides), and the selection stays exact."""
+    rows, n = 80, 33792
+    s = rnd(38, (rows, n)).cpu()
+    pos = torch.arange(n)
+    spikes = 100.0 + rnd(39, (rows, n)).cpu()
+    s[20:40] = torch.where(pos % 64 == 3, spikes[20:40], s[20:40])      # all sampled
+    s[40:60] = torch.where(pos % 64 == 40, spikes[40:60], s[40:60])     # never sampled
+    s[60:80] = torch.where(pos % 64 < 8, spikes[60:80], s[60:80])       # the whole sample
+    s = s.to(DEV).contiguous()
+    for k in (512, 600, 64):
+        _topk_check(s, k)
+    _topk_check(s, 512, n_valid=[n, 16384, 16383, 8192] * 20)
+
+
 def test_topk_candidate_map():
     rows, n = 4, 16384
     s = rnd(33, (rows, n))
